@@ -1,0 +1,306 @@
+/*
+ * verify.h - C ABI of the exact width-k verification pass (one GB300, sm_103a).
+ *
+ * A speculative-decoding verify pass runs a block of k draft rows (k = 1..16;
+ * the pages measure 1..9) through the target model in one pass and must give,
+ * row for row, what k ordinary one-row steps give.  This library provides the
+ * data-parallel hot path of that pass for hybrid Gated-DeltaNet / MoE models:
+ *
+ *   q4_qmv_k            affine 4-bit (group 64) weight x k BF16 rows
+ *   q4_gather_experts_k routed top-k experts: fused gate/up + SwiGLU + down +
+ *                       fixed-order combine (optionally a sigmoid-gated shared
+ *                       expert)
+ *   gdn_verify_k        k-row Gated DeltaNet step with per-row state snapshots
+ *   gdn_commit          accepted-prefix rollback by slot (pointer) swap
+ *   verify_rmsnorm_k    the layer glue norm used by a full verify layer
+ *
+ * Sources (pages, cited by title and section):
+ *   [T]  "Flash-Next optimization transfer to Ornith and Qwen 27B":
+ *        table "Shared architecture and implemented paths" and section
+ *        "Exact verification kernels and benchmark admission".
+ *   [R]  "Red Lite dev45 - speculative decoding with the Qwen3-Next MTP block":
+ *        section "What it is" (2-row verify) and "Tried and kept or not".
+ *   [F]  "QWEN38FLASH.md - Plan for supporting Qwen/Qwen3.8-Flash-Next":
+ *        section 2.1 "Gated DeltaNet (GDN)", 2.3 "MoE", 2.4 (norm forms),
+ *        3.1 (KDA -> GDN adaptations), 5.1 (GDN kernel list).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Memory: every tensor argument is a DEVICE pointer owned by the caller
+ *    (cudaMalloc / PyTorch).  The library never frees or keeps caller memory
+ *    beyond the call.  verify_init allocates the library's own scratch on the
+ *    chosen device; verify_destroy frees it.  Host pointers are rejected with
+ *    VERIFY_EINVAL (checked with cudaPointerGetAttributes).
+ *  - Streams: every compute call is asynchronous on the caller's stream
+ *    (a cudaStream_t passed as `struct CUstream_st*`; NULL = legacy default
+ *    stream).  Nothing synchronises the host.  Calls that share one ctx
+ *    share its scratch, so they must be ordered on one stream (or otherwise
+ *    serialised); concurrent calls on one ctx from different streams race.
+ *  - Errors: each call returns a verify_status.  Argument errors are found on
+ *    the host before anything is launched (the call then has no effect).
+ *    VERIFY_ECUDA reports a launch error.  Kernels never trap: a device-side
+ *    problem (a pipeline wait that timed out, an out-of-range expert index)
+ *    sets the ctx's device error word, read by verify_device_status.
+ *    verify_last_error returns a static, human-readable string for the last
+ *    failing call on that ctx.
+ *  - BF16 tensors are passed as uint16_t bit patterns.  Outputs requested as
+ *    VERIFY_BF16 are the round-to-nearest-even of the fp32 result.
+ *  - Exactness (the property the pages require, [T] "Exact verification
+ *    kernels", [R] "What it is": "each row in exactly the 1-row kernel's
+ *    order"): for every call, row r of a width-k result is bit-identical to a
+ *    width-1 call on row r alone.  Accumulation is fp32 in an order that
+ *    depends only on the matrix shape and the GPU, never on k or on the other
+ *    rows.
+ */
+#ifndef VERIFY_H_
+#define VERIFY_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* == cudaStream_t without pulling in CUDA headers */
+
+typedef enum {
+  VERIFY_OK = 0,
+  VERIFY_EINVAL = 1,       /* null / host / misaligned pointer, bad size, bad state */
+  VERIFY_EUNSUPPORTED = 2, /* k out of range, K % 64 != 0, group != 64, bits != 4,
+                              shapes above the library's limits */
+  VERIFY_ECUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  VERIFY_EDEVICE = 4       /* a kernel reported an error in the device error word */
+} verify_status;
+
+typedef enum {
+  VERIFY_F32 = 0,     /* write fp32 */
+  VERIFY_BF16 = 1,    /* write bf16 (RNE of the fp32 result) */
+  VERIFY_F32_ADD = 2  /* y(fp32) += result: the residual add of a verify layer */
+} verify_dtype;
+
+#define VERIFY_MAX_K 16          /* widest verify block any call accepts */
+#define VERIFY_GDN_MAX_SLOTS 17  /* VERIFY_MAX_K + 1 state slots */
+
+typedef struct verify_ctx verify_ctx;
+
+/*
+ * One affine Q4 matrix with group size 64 ([T] table "Shared architecture":
+ * "affine Q4, group size 64, and compatible BF16 tensors").  Layout (the
+ * affine convention the MLX runtime of [T] uses):
+ *   packed : uint32 [n_out, k_in/8], row-major; input column c of row n is
+ *            bits 4*(c%8) .. 4*(c%8)+3 of packed[n*(k_in/8) + c/8]
+ *            (lowest nibble = lowest column).
+ *   scales : bf16 [n_out, k_in/64];  biases : bf16 [n_out, k_in/64]
+ *   weight : w[n][c] = scales[n][c/64] * q[n][c] + biases[n][c/64]
+ * Requirements: packed 16-byte aligned; scales, biases 4-byte aligned;
+ * k_in % 64 == 0; group_size == 64; bits == 4.
+ */
+typedef struct {
+  const uint32_t* packed;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  int32_t n_out;
+  int32_t k_in;
+  int32_t group_size; /* must be 64 */
+  int32_t bits;       /* must be 4 */
+} verify_q4_weight;
+
+/*
+ * A stack of n_experts matrices of identical shape, stored back to back:
+ * packed [E, n_out, k_in/8], scales/biases [E, n_out, k_in/64].  `w` holds
+ * the per-expert shape and the pointers to expert 0.
+ */
+typedef struct {
+  verify_q4_weight w;
+  int32_t n_experts;
+} verify_q4_experts;
+
+/* ---------------------------------------------------------------- context */
+
+/* Creates a context on `device` (makes it current) and allocates the
+ * library's scratch there.  *out receives the context.  The scratch is sized
+ * for the limits listed with each call. */
+verify_status verify_init(int device, verify_ctx** out);
+
+/* Frees the scratch and the context.  Synchronises the device first. */
+verify_status verify_destroy(verify_ctx* ctx);
+
+/* Static string describing the last failing call on ctx ("" if none). */
+const char* verify_last_error(const verify_ctx* ctx);
+
+/* Synchronises `stream`, reads and clears the device error word.  Returns
+ * VERIFY_OK if no kernel reported a problem since the last check, else
+ * VERIFY_EDEVICE with *code (if non-NULL) set to the first error code:
+ * 1 = pipeline wait timed out, 2 = expert index out of range. */
+verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, int32_t* code);
+
+/* Number of kernels the library launched on this ctx since verify_init. */
+int64_t verify_launch_count(const verify_ctx* ctx);
+
+/* ------------------------------------------------------------ q4_qmv_k */
+
+/*
+ * Dense width-k product ([T] "Exact verification kernels": the small-batch
+ * Q4 kernel at widths 4/8/9 agrees exactly with serial QMV; [R] "What it is":
+ * two-vector kernels decode each weight once and compute each row in the
+ * 1-row kernel's order):
+ *
+ *     y[r][n] = sum_c w[n][c] * x[r][c]      r < k, n < n_out
+ *
+ * x : bf16 [k, k_in] row-major, 16-byte aligned.
+ * y : [k, n_out] row-major, fp32 (VERIFY_F32 / VERIFY_F32_ADD) or bf16.
+ * k : 1..VERIFY_MAX_K.   Limits: n_out <= 1<<20, k_in <= 1<<17.
+ * Each packed weight is read from HBM once per call for all k rows.
+ */
+verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W,
+                       const uint16_t* x, int k, void* y, int dtype_out,
+                       struct CUstream_st* stream);
+
+/* ------------------------------------------------- q4_gather_experts_k */
+
+/*
+ * Routed mixture-of-experts for k rows ([T] "Exact verification kernels":
+ * gathered expert kernel, affine Q4/group-64, top-8 of 256, fused gate/up;
+ * [R] "What it is": all rows' (expert,row) pairs in one dispatch and one
+ * tail; [F] 2.3: gate+up concatenated [E, 2I, H], SwiGLU, a sigmoid-gated
+ * shared expert).  Per row r:
+ *
+ *   idx[r][0..T)  = the T largest router logits of row r, in descending
+ *                   order (equal logits: lower expert index first)
+ *   wts[r][j]     = exp(l_j - l_0) / sum_{j'<T} exp(l_j' - l_0)
+ *                   (softmax over all E, keep T, renormalise == softmax of
+ *                   the T selected logits)
+ *   for j < T, e = idx[r][j]:
+ *     g = W_gu[e][0..I)  . x[r],  u = W_gu[e][I..2I) . x[r]
+ *     h = bf16( silu(g) * u )                          (silu(t) = t/(1+e^-t))
+ *     p_j = W_d[e] . h
+ *   y[r] = sum_{j=0..T-1} wts[r][j] * p_j    (ascending j, fp32)
+ *   if a shared expert is given: y[r] += sigmoid(sg[r]) * (W_sd . bf16(silu(W_sgu[0..I).x) * W_sgu[I..2I).x))
+ *
+ * gate_up : experts [E, 2I, H];  down : experts [E, H, I].
+ * logits  : fp32, row r at logits + r*logits_ld, E entries.
+ * x       : bf16 [k, H].   idx_out : int32 [k, T];  w_out : fp32 [k, T].
+ * y       : fp32 [k, H] (VERIFY_F32 or VERIFY_F32_ADD) or bf16.
+ * shared_gate_up [2I, H], shared_down [H, I], shared_gate_logit (fp32, row r
+ * at shared_gate_logit + r*logits_ld) may all be NULL (no shared expert).
+ * Limits: E <= 1024, 1 <= T <= 16, H <= 8192, I <= 4096, H % 64 == I % 64 == 0.
+ * Expert weights are read once per call for every distinct selected expert
+ * (the union of the rows' routes).
+ */
+verify_status q4_gather_experts_k(verify_ctx* ctx,
+                                  const verify_q4_experts* gate_up,
+                                  const verify_q4_experts* down,
+                                  const float* logits, int64_t logits_ld,
+                                  int top_k, const uint16_t* x, int k,
+                                  int32_t* idx_out, float* w_out,
+                                  void* y, int dtype_out,
+                                  const verify_q4_weight* shared_gate_up,
+                                  const verify_q4_weight* shared_down,
+                                  const float* shared_gate_logit,
+                                  struct CUstream_st* stream);
+
+/* ------------------------------------------------------- gdn_verify_k */
+
+/*
+ * Gated DeltaNet layer geometry and parameters ([F] 2.1, 3.1):
+ *   C = 2*n_qk_heads*head_dim_k + n_v_heads*head_dim_v conv channels
+ *   (q | k | v, in that order).  V head h uses QK head h / (n_v_heads/n_qk_heads).
+ * conv_w  : fp32 [C, conv_kernel]; tap conv_kernel-1 multiplies the current row.
+ * A_log, dt_bias : fp32 [n_v_heads].   norm_w : fp32 [head_dim_v].
+ * Supported: head_dim_k == head_dim_v in {32, 64, 128}, conv_kernel == 4,
+ * n_v_heads % n_qk_heads == 0.
+ */
+typedef struct {
+  int32_t n_qk_heads, n_v_heads, head_dim_k, head_dim_v, conv_kernel;
+  float q_scale;  /* multiplies the L2-normalised q (1/sqrt(head_dim_k)) */
+  float l2_eps;   /* q,k L2 norm: x / sqrt(sum x^2 + l2_eps) (1e-6) */
+  float norm_eps; /* gated RMSNorm epsilon (1e-6) */
+  int32_t gate_act; /* 0 = sigmoid (default), 1 = silu */
+  const float* conv_w;
+  const float* A_log;
+  const float* dt_bias;
+  const float* norm_w;
+} verify_gdn_params;
+
+/*
+ * Recurrent state of one GDN layer as a ring of caller-allocated slots.
+ * Slot s holds S_slots[s]: fp32 [n_v_heads, head_dim_v, head_dim_k]
+ * (S[h][i][j], i = value row, j = key column) and conv_slots[s]: bf16
+ * [conv_kernel-1, C] (the last conv_kernel-1 input rows, oldest first).
+ * `cur` is the committed slot.  After gdn_verify_k(k), pending[r] is the slot
+ * that holds the state after the first r rows (pending[0] == cur) and
+ * pending_k == k; gdn_commit turns one of them into `cur`.
+ * The caller fills S_slots/conv_slots/n_slots/cur once (n_slots >= k+1 for
+ * every verify) and then only reads the struct.
+ */
+typedef struct {
+  float* S_slots[VERIFY_GDN_MAX_SLOTS];
+  uint16_t* conv_slots[VERIFY_GDN_MAX_SLOTS];
+  int32_t n_slots;
+  int32_t cur;
+  int32_t pending_k;
+  int32_t pending[VERIFY_GDN_MAX_SLOTS];
+} verify_gdn_state;
+
+/* Inputs of a width-k GDN call: bf16, row r of each at ptr + r*ld.  qkv has
+ * C entries per row, z n_v_heads*head_dim_v, a and b n_v_heads each. */
+typedef struct {
+  const uint16_t* qkv; int64_t ld_qkv;
+  const uint16_t* z;   int64_t ld_z;
+  const uint16_t* a;   int64_t ld_a;
+  const uint16_t* b;   int64_t ld_b;
+} verify_gdn_inputs;
+
+/*
+ * k-row Gated DeltaNet step ([F] 2.1 per-token pipeline and delta rule;
+ * [R] "What it is": row r runs from row r-1's state and the state after
+ * each row is written to snapshot buffers inside the kernels; [T] table
+ * "Fused GDN preparation" widths 1..9).  Starting from slot st->cur, for
+ * r = 0..k-1 and every V head h (QK head hq):
+ *   conv:   c = silu(sum_t conv_w[ch][t] * window_r[t]) per channel, window_r
+ *           = the conv_kernel most recent input rows ending at row r
+ *   q = c[q channels of hq] / sqrt(|.|^2 + l2_eps) * q_scale
+ *   kk = c[k channels of hq] / sqrt(|.|^2 + l2_eps);  v = c[v channels of h]
+ *   beta = sigmoid(b[r][h]);  g = exp(-exp(A_log[h]) * softplus(a[r][h] + dt_bias[h]))
+ *   S <- g*S;  m = S.kk;  delta = (v - m)*beta;  S[i][j] += delta[i]*kk[j];  y = S.q
+ *   o[r][h*dv + i] = y_i / sqrt(mean(y^2) + norm_eps) * norm_w[i] * act(z[r][h*dv+i])
+ * The state (S and conv window) after row r is written to slot pending[r+1]
+ * (the free slots in ascending index order); slot cur is only read.
+ * o : [k, n_v_heads*head_dim_v] fp32 or bf16 (VERIFY_F32 / VERIFY_BF16).
+ * Requires n_slots >= k+1, all slot pointers 16-byte aligned.
+ * A second verify without a commit in between starts again from `cur`.
+ */
+verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p,
+                           verify_gdn_state* st, const verify_gdn_inputs* in,
+                           int k, void* o, int dtype_out,
+                           struct CUstream_st* stream);
+
+/*
+ * Accepted-prefix rollback ([R] "What it is": a rejected draft is undone by
+ * swapping the DeltaNet state pointers with the snapshots; "Acceptance").
+ * Makes the state after the first `accepted` rows of the last verify current:
+ * cur = pending[accepted]; accepted = 0 keeps the pre-verify state.
+ * Host-only, O(1), touches no device memory and launches nothing.
+ * Errors: VERIFY_EINVAL if nothing is pending (a second commit) or accepted
+ * is outside 0..pending_k.
+ */
+verify_status gdn_commit(verify_gdn_state* st, int accepted);
+
+/* --------------------------------------------------------- layer glue */
+
+/*
+ * Row RMSNorm used around a verify layer ([F] 2.4: non-gated norms are
+ * zero-centred, y*(1+w)):
+ *   out[r][c] = x[r][c] / sqrt(mean_c x[r][c]^2 + eps) * (zero_centered ? 1 + w[c] : w[c])
+ * x fp32 [k, n]; w fp32 [n]; out [k, n] bf16 or fp32.  n <= 16384, n % 4 == 0.
+ */
+verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w,
+                               float eps, int zero_centered, int n, int k,
+                               void* out, int dtype_out,
+                               struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_H_ */

@@ -1,0 +1,354 @@
+/*
+ * oracle.c - plain, slow CPU reference of the exact width-k verify pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the smoke check and the bench's CPU
+ * baseline use it.  It shares no code, header, table or helper with the CUDA
+ * library; the two meet only in the seeded input generator.
+ *
+ * Arithmetic is float64 throughout (inputs are bf16 / fp32 and widen exactly),
+ * summed in ascending index order, with no blocking or fusion: each function
+ * is the plain definition the pages give.  Pages are cited by title:
+ *   [T] "Flash-Next optimization transfer to Ornith and Qwen 27B"
+ *   [R] "Red Lite dev45 - speculative decoding with the Qwen3-Next MTP block"
+ *   [F] "QWEN38FLASH.md - Plan for supporting Qwen/Qwen3.8-Flash-Next"
+ * Readings taken where the pages are silent are marked READING.
+ *
+ * Pins (checked by the CPU tests against closed forms, brute force and
+ * invariants, not against this file): q4 nibble order and group indexing,
+ * exact integer products, top-k order/ties and softmax identities, the
+ * single-expert special case, the delta-rule identities (zero state, unit
+ * gates, beta = 0, decay 1/2), conv taps, norms.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------ bf16 helpers */
+
+/* bf16 bit pattern -> value (exact). */
+static double bf16_value(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* value -> nearest bf16 (ties to even), rounded once from float64. */
+uint16_t oracle_round_bf16(double v) {
+  if (v == 0.0 || !isfinite(v)) {
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+  }
+  int e;
+  double m = frexp(v, &e);             /* v = m * 2^e, 0.5 <= |m| < 1 */
+  double scaled = ldexp(m, 8);         /* 8 significant bits: 128 <= |scaled| < 256 */
+  double r = nearbyint(scaled);        /* default rounding mode: ties to even */
+  float f = (float)ldexp(r, e - 8);    /* exact: 8-bit significand */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+static double sigmoid(double t) { return 1.0 / (1.0 + exp(-t)); }
+static double silu(double t) { return t / (1.0 + exp(-t)); }
+static double softplus(double t) { return (t > 0 ? t : 0.0) + log1p(exp(-fabs(t))); }
+
+/* ------------------------------------------------------------- q4 weights */
+
+/*
+ * Affine Q4, group size 64 ([T] table "Shared architecture and implemented
+ * paths": "affine Q4, group size 64, and compatible BF16 tensors").
+ * READING (layout; the pages give only the format name): packed uint32
+ * [n_out, k_in/8] row-major with column c in bits 4*(c%8).., scales and
+ * biases bf16 [n_out, k_in/64], w = scale * q + bias.
+ */
+static double q4_weight(const uint32_t* packed, const uint16_t* scales,
+                        const uint16_t* biases, int k_in, int64_t n, int c) {
+  uint32_t word = packed[n * (k_in / 8) + c / 8];
+  int q = (int)((word >> (4 * (c % 8))) & 15u);
+  double s = bf16_value(scales[n * (k_in / 64) + c / 64]);
+  double b = bf16_value(biases[n * (k_in / 64) + c / 64]);
+  return s * q + b;
+}
+
+/*
+ * y[r][n] = sum_c w[n][c] * x[r][c]  for r < k, n < n_out (ascending c).
+ * Width-k is k independent width-1 products by construction ([T] "Exact
+ * verification kernels": agreement with serial QMV; [R] "What it is").
+ * x: bf16 [k, k_in] (row r at x + r*ldx); y: float64 [k, n_out].
+ */
+int oracle_q4_qmv(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases,
+                  int n_out, int k_in, const uint16_t* x, int64_t ldx, int k, double* y) {
+  if (k_in % 64 != 0 || n_out < 0 || k < 0) return 1;
+  double* w = (double*)malloc(sizeof(double) * (size_t)k_in);
+  if (!w) return 2;
+  for (int64_t n = 0; n < n_out; ++n) {
+    for (int c = 0; c < k_in; ++c) w[c] = q4_weight(packed, scales, biases, k_in, n, c);
+    for (int r = 0; r < k; ++r) {
+      double acc = 0.0;
+      for (int c = 0; c < k_in; ++c) acc += w[c] * bf16_value(x[r * ldx + c]);
+      y[(int64_t)r * n_out + n] = acc;
+    }
+  }
+  free(w);
+  return 0;
+}
+
+/* ------------------------------------------------------------ router top-k */
+
+/*
+ * Top-T routing of one row ([T] "Exact verification kernels": top-eight of
+ * 256; [F] 2.3: router over 512 logits, top-k).  READING (scoring function
+ * left open by [F] 2.3): softmax over all E, keep the T largest, renormalise;
+ * this equals the softmax of the T selected logits, which is what is
+ * computed.  Order: descending logit; equal logits: lower expert index first
+ * (READING, the pages are silent).
+ */
+int oracle_route_topk(const float* logits, int64_t ld, int k, int E, int T,
+                      int32_t* idx, double* w) {
+  if (T < 1 || T > E) return 1;
+  char* taken = (char*)malloc((size_t)E);
+  if (!taken) return 2;
+  for (int r = 0; r < k; ++r) {
+    const float* l = logits + r * ld;
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < T; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e)
+        if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;
+      taken[best] = 1;
+      idx[r * T + j] = best;
+    }
+    double top = l[idx[r * T]];
+    double sum = 0.0;
+    for (int j = 0; j < T; ++j) sum += exp((double)l[idx[r * T + j]] - top);
+    for (int j = 0; j < T; ++j) w[r * T + j] = exp((double)l[idx[r * T + j]] - top) / sum;
+  }
+  free(taken);
+  return 0;
+}
+
+/* ---------------------------------------------------------- routed experts */
+
+/*
+ * One SwiGLU expert applied to one row: g = W_gu[0..I).x, u = W_gu[I..2I).x
+ * ([F] 2.3: gate+up concatenated [2I, H], SwiGLU), h = bf16(silu(g)*u),
+ * p = W_d.h.  READING: h is rounded to bf16 because the down projection, like
+ * every Q4 product of [T], takes BF16 activation rows.
+ */
+static int expert_row(const uint32_t* gp, const uint16_t* gs, const uint16_t* gb,
+                      const uint32_t* dp, const uint16_t* ds, const uint16_t* db,
+                      int H, int I, const uint16_t* xrow, double* p, uint16_t* h_out) {
+  double* gu = (double*)malloc(sizeof(double) * 2 * (size_t)I);
+  uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+  if (!gu || !h) { free(gu); free(h); return 2; }
+  oracle_q4_qmv(gp, gs, gb, 2 * I, H, xrow, H, 1, gu);
+  for (int i = 0; i < I; ++i) h[i] = oracle_round_bf16(silu(gu[i]) * gu[I + i]);
+  if (h_out) memcpy(h_out, h, sizeof(uint16_t) * (size_t)I);
+  oracle_q4_qmv(dp, ds, db, H, I, h, I, 1, p);
+  free(gu);
+  free(h);
+  return 0;
+}
+
+/*
+ * Routed MoE for k rows ([T] "Exact verification kernels": gathered
+ * affine-Q4 experts with fused gate/up; [R] "What it is": all (expert,row)
+ * pairs in one dispatch, one tail).  y[r] = sum_{j<T} w[r][j] * p_{r,j},
+ * ascending j ([F] 5.3 fused sum over the top-k), then, if a shared expert is
+ * given, + sigmoid(sg[r]) * shared(x[r]) ([F] 2.3: 10 routed + 1 shared;
+ * READING: the shared expert's sigmoid gate as in the Qwen3-Next lineage [F]
+ * section 3 names, added after the routed sum).
+ * Gate/up stack [E, 2I, H], down stack [E, H, I].  h_out (optional) receives
+ * the bf16 SwiGLU rows [k, T(+1), I].
+ */
+int oracle_gather_experts(const uint32_t* gup, const uint16_t* gus, const uint16_t* gub,
+                          const uint32_t* dnp, const uint16_t* dns, const uint16_t* dnb,
+                          int E, int H, int I, const float* logits, int64_t ld, int T,
+                          const uint16_t* x, int k, int32_t* idx, double* w, double* y,
+                          const uint32_t* sgup, const uint16_t* sgus, const uint16_t* sgub,
+                          const uint32_t* sdnp, const uint16_t* sdns, const uint16_t* sdnb,
+                          const float* sg_logit, uint16_t* h_out) {
+  if (H % 64 || I % 64) return 1;
+  int rc = oracle_route_topk(logits, ld, k, E, T, idx, w);
+  if (rc) return rc;
+  int slots = T + (sgup ? 1 : 0);
+  double* p = (double*)malloc(sizeof(double) * (size_t)H);
+  if (!p) return 2;
+  const int64_t gu_w = (int64_t)2 * I * (H / 8), gu_g = (int64_t)2 * I * (H / 64);
+  const int64_t dn_w = (int64_t)H * (I / 8), dn_g = (int64_t)H * (I / 64);
+  for (int r = 0; r < k; ++r) {
+    double* yr = y + (int64_t)r * H;
+    for (int n = 0; n < H; ++n) yr[n] = 0.0;
+    for (int j = 0; j < T; ++j) {
+      int64_t e = idx[r * T + j];
+      rc = expert_row(gup + e * gu_w, gus + e * gu_g, gub + e * gu_g,
+                      dnp + e * dn_w, dns + e * dn_g, dnb + e * dn_g, H, I,
+                      x + (int64_t)r * H, p, h_out ? h_out + ((int64_t)r * slots + j) * I : NULL);
+      if (rc) { free(p); return rc; }
+      for (int n = 0; n < H; ++n) yr[n] += w[r * T + j] * p[n];
+    }
+    if (sgup) {
+      rc = expert_row(sgup, sgus, sgub, sdnp, sdns, sdnb, H, I, x + (int64_t)r * H, p,
+                      h_out ? h_out + ((int64_t)r * slots + T) * I : NULL);
+      if (rc) { free(p); return rc; }
+      double gate = sigmoid((double)sg_logit[r * ld]);
+      for (int n = 0; n < H; ++n) yr[n] += gate * p[n];
+    }
+  }
+  free(p);
+  return 0;
+}
+
+/* ------------------------------------------------------- Gated DeltaNet */
+
+/*
+ * k-row Gated DeltaNet verify, one row after the other, every row starting
+ * from the previous row's state ([R] "What it is": row 1 runs from row 0's
+ * state; [F] 2.1 per-token pipeline):
+ *   1. causal depthwise conv over the q|k|v channels: window = the last W
+ *      input rows ending at the current one ([F] 3.1 table: 3-tap history +
+ *      current, 4 weights per channel; tap W-1 = current row), then SiLU
+ *      (READING: the conv activation is not named on the pages; SiLU as in
+ *      the Qwen3-Next lineage [F] section 3 cites).
+ *   2. q = conv[QK head hq], k = conv[Hk*dk + QK head hq], v = conv[2*Hk*dk +
+ *      V head h]; V head h uses QK head h / (Hv/Hk) ([F] 3.1: each k head
+ *      shared by 3 v heads; READING: contiguous grouping).
+ *   3. L2 norm per QK head: q <- q / sqrt(|q|^2 + l2_eps) * q_scale,
+ *      k <- k / sqrt(|k|^2 + l2_eps) ([F] 2.1; READING: eps inside the sqrt,
+ *      q_scale = 1/sqrt(dk)).
+ *   4. beta = sigmoid(b), g = exp(-exp(A_log) * softplus(a + dt_bias)) ([F]
+ *      3.1: per-head scalar decay in the A_log/dt_bias softplus form, scalar
+ *      sigmoid beta; READING: the plainest form using all three quantities,
+ *      the formula itself is elided in [F] 5.1 item 5).
+ *   5. delta rule, state S[h] in [Dv, Dk] ([F] 2.1 steps 1-5): S <- g S;
+ *      m_i = sum_j S_ij k_j; delta_i = (v_i - m_i) beta; S_ij += delta_i k_j
+ *      (the k (x) delta outer product laid out in S's [Dv, Dk] order);
+ *      y_i = sum_j S_ij q_j.
+ *   6. gated RMSNorm per V head ([F] 2.1 output; 2.4: the gated variant uses
+ *      y*weight): o_i = y_i / sqrt(mean(y^2) + norm_eps) * norm_w_i * act(z_i),
+ *      act = sigmoid ([F] 2.1: sigmoid gates) or silu (gate_act = 1).
+ *   7. the state after row r (S and the conv window) is snapshot r+1
+ *      ([R] "What it is": the state after row 0 is written to snapshot
+ *      buffers); S_snap[r], tail_snap[r] hold it.
+ * S0: float64 [Hv, Dv, Dk]; tail0: bf16 [W-1, C] oldest first.
+ * o: float64 [k, Hv*Dv].  dbg (optional): per row q[Hk*dk] k[Hk*dk]
+ * v[Hv*dv] g[Hv] beta[Hv] y[Hv*dv] (pre-norm).
+ */
+int oracle_gdn_verify(int Hk, int Hv, int dk, int dv, int W, double q_scale,
+                      double l2_eps, double norm_eps, int gate_act,
+                      const float* conv_w, const float* A_log, const float* dt_bias,
+                      const float* norm_w, const double* S0, const uint16_t* tail0,
+                      const uint16_t* qkv, int64_t ld_qkv, const uint16_t* z, int64_t ld_z,
+                      const uint16_t* a, int64_t ld_a, const uint16_t* b, int64_t ld_b,
+                      int k, double* o, double* S_snap, uint16_t* tail_snap, double* dbg) {
+  if (Hv % Hk || W < 1) return 1;
+  const int C = 2 * Hk * dk + Hv * dv;
+  const int64_t nS = (int64_t)Hv * dv * dk;
+  double* S = (double*)malloc(sizeof(double) * (size_t)nS);
+  uint16_t* tail = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)((W - 1) * C + 1));
+  double* c = (double*)malloc(sizeof(double) * (size_t)C);
+  double* y = (double*)malloc(sizeof(double) * (size_t)dv);
+  if (!S || !tail || !c || !y) { free(S); free(tail); free(c); free(y); return 2; }
+  memcpy(S, S0, sizeof(double) * (size_t)nS);
+  memcpy(tail, tail0, sizeof(uint16_t) * (size_t)((W - 1) * C));
+
+  for (int r = 0; r < k; ++r) {
+    const uint16_t* xr = qkv + r * ld_qkv;
+    /* 1. conv + SiLU, then slide the window */
+    for (int ch = 0; ch < C; ++ch) {
+      double acc = 0.0;
+      for (int t = 0; t < W; ++t) {
+        double v = (t < W - 1) ? bf16_value(tail[t * C + ch]) : bf16_value(xr[ch]);
+        acc += (double)conv_w[ch * W + t] * v;
+      }
+      c[ch] = silu(acc);
+    }
+    for (int t = 0; t + 1 < W - 1; ++t) memcpy(tail + t * C, tail + (t + 1) * C, sizeof(uint16_t) * C);
+    if (W > 1) memcpy(tail + (W - 2) * C, xr, sizeof(uint16_t) * C);
+
+    /* 3. L2 norms per QK head (in place on the conv output) */
+    for (int hq = 0; hq < Hk; ++hq) {
+      double* q = c + hq * dk;
+      double* kk = c + Hk * dk + hq * dk;
+      double sq = 0.0, sk = 0.0;
+      for (int j = 0; j < dk; ++j) { sq += q[j] * q[j]; sk += kk[j] * kk[j]; }
+      double nq = sqrt(sq + l2_eps), nk = sqrt(sk + l2_eps);
+      for (int j = 0; j < dk; ++j) { q[j] = q[j] / nq * q_scale; kk[j] = kk[j] / nk; }
+    }
+    double* dbg_r = dbg ? dbg + (int64_t)r * (2 * Hk * dk + 2 * Hv * dv + 2 * Hv) : NULL;
+    if (dbg_r) {
+      memcpy(dbg_r, c, sizeof(double) * (size_t)(2 * Hk * dk));
+      memcpy(dbg_r + 2 * Hk * dk, c + 2 * Hk * dk, sizeof(double) * (size_t)(Hv * dv));
+    }
+
+    for (int h = 0; h < Hv; ++h) {
+      const int hq = h / (Hv / Hk);
+      const double* q = c + hq * dk;
+      const double* kk = c + Hk * dk + hq * dk;
+      const double* v = c + 2 * Hk * dk + h * dv;
+      /* 4. gates */
+      double beta = sigmoid(bf16_value(b[r * ld_b + h]));
+      double g = exp(-exp((double)A_log[h]) * softplus(bf16_value(a[r * ld_a + h]) + (double)dt_bias[h]));
+      /* 5. delta rule on S[h] (row i = value index, column j = key index) */
+      double* Sh = S + (int64_t)h * dv * dk;
+      for (int64_t e = 0; e < (int64_t)dv * dk; ++e) Sh[e] *= g;
+      for (int i = 0; i < dv; ++i) {
+        double m = 0.0;
+        for (int j = 0; j < dk; ++j) m += Sh[i * dk + j] * kk[j];
+        double delta = (v[i] - m) * beta;
+        for (int j = 0; j < dk; ++j) Sh[i * dk + j] += delta * kk[j];
+      }
+      for (int i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += Sh[i * dk + j] * q[j];
+        y[i] = acc;
+      }
+      /* 6. gated RMSNorm over the head's dv outputs */
+      double ss = 0.0;
+      for (int i = 0; i < dv; ++i) ss += y[i] * y[i];
+      double inv = 1.0 / sqrt(ss / dv + norm_eps);
+      for (int i = 0; i < dv; ++i) {
+        double zz = bf16_value(z[r * ld_z + h * dv + i]);
+        double act = gate_act == 1 ? silu(zz) : sigmoid(zz);
+        o[(int64_t)r * Hv * dv + h * dv + i] = y[i] * inv * (double)norm_w[i] * act;
+      }
+      if (dbg_r) {
+        dbg_r[2 * Hk * dk + Hv * dv + h] = g;
+        dbg_r[2 * Hk * dk + Hv * dv + Hv + h] = beta;
+        memcpy(dbg_r + 2 * Hk * dk + Hv * dv + 2 * Hv + h * dv, y, sizeof(double) * (size_t)dv);
+      }
+    }
+    /* 7. snapshot r+1 */
+    memcpy(S_snap + (int64_t)r * nS, S, sizeof(double) * (size_t)nS);
+    memcpy(tail_snap + (int64_t)r * (W - 1) * C, tail, sizeof(uint16_t) * (size_t)((W - 1) * C));
+  }
+  free(S); free(tail); free(c); free(y);
+  return 0;
+}
+
+/* ------------------------------------------------------------- layer glue */
+
+/*
+ * Row RMSNorm ([F] 2.4: non-gated norms are zero-centred, y*(1+weight); the
+ * conventional form is y*weight): out = x / sqrt(mean(x^2) + eps) * wt,
+ * wt = 1 + w (zero_centered) or w.  x, out: float64 [k, n].
+ */
+int oracle_rmsnorm(const double* x, const float* w, double eps, int zero_centered,
+                   int n, int k, double* out) {
+  for (int r = 0; r < k; ++r) {
+    const double* xr = x + (int64_t)r * n;
+    double ss = 0.0;
+    for (int c = 0; c < n; ++c) ss += xr[c] * xr[c];
+    double inv = 1.0 / sqrt(ss / n + eps);
+    for (int c = 0; c < n; ++c) {
+      double wt = zero_centered ? 1.0 + (double)w[c] : (double)w[c];
+      out[(int64_t)r * n + c] = xr[c] * inv * wt;
+    }
+  }
+  return 0;
+}
