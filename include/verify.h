@@ -183,7 +183,8 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W,
  * y       : fp32 [k, H] (VERIFY_F32 or VERIFY_F32_ADD) or bf16.
  * shared_gate_up [2I, H], shared_down [H, I], shared_gate_logit (fp32, row r
  * at shared_gate_logit + r*logits_ld) may all be NULL (no shared expert).
- * Limits: E <= 1024, 1 <= T <= 16, H <= 8192, I <= 4096, H % 64 == I % 64 == 0.
+ * Limits: E <= 512, 1 <= T <= 16, 256 <= H <= 8192, 256 <= I <= 4096,
+ * H % 128 == I % 128 == 0.
  * Expert weights are read once per call for every distinct selected expert
  * (the union of the rows' routes).
  */

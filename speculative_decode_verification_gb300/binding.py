@@ -1,0 +1,207 @@
+"""Thin ctypes binding of libverify.so (include/verify.h).
+
+Argument marshalling only: every step of the verify pass runs in the CUDA
+library.  Tensors are passed as device pointers (``tensor.data_ptr()``) and
+the stream as ``torch.cuda.current_stream().cuda_stream``; PyTorch is used for
+device memory and streams, nothing else.  There is no CPU fallback: if the
+library is missing, loading fails with an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libverify.so")
+
+OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE = 0, 1, 2, 3, 4
+F32, BF16, F32_ADD = 0, 1, 2
+MAX_K = 16
+GDN_MAX_SLOTS = 17
+
+_lib = None
+
+
+class VerifyError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+class Q4Weight(C.Structure):
+    _fields_ = [("packed", C.c_void_p), ("scales", C.c_void_p), ("biases", C.c_void_p),
+                ("n_out", C.c_int32), ("k_in", C.c_int32), ("group_size", C.c_int32), ("bits", C.c_int32)]
+
+
+class Q4Experts(C.Structure):
+    _fields_ = [("w", Q4Weight), ("n_experts", C.c_int32)]
+
+
+class GdnParams(C.Structure):
+    _fields_ = [("n_qk_heads", C.c_int32), ("n_v_heads", C.c_int32), ("head_dim_k", C.c_int32),
+                ("head_dim_v", C.c_int32), ("conv_kernel", C.c_int32), ("q_scale", C.c_float),
+                ("l2_eps", C.c_float), ("norm_eps", C.c_float), ("gate_act", C.c_int32),
+                ("conv_w", C.c_void_p), ("A_log", C.c_void_p), ("dt_bias", C.c_void_p), ("norm_w", C.c_void_p)]
+
+
+class GdnState(C.Structure):
+    _fields_ = [("S_slots", C.c_void_p * GDN_MAX_SLOTS), ("conv_slots", C.c_void_p * GDN_MAX_SLOTS),
+                ("n_slots", C.c_int32), ("cur", C.c_int32), ("pending_k", C.c_int32),
+                ("pending", C.c_int32 * GDN_MAX_SLOTS)]
+
+
+class GdnInputs(C.Structure):
+    _fields_ = [("qkv", C.c_void_p), ("ld_qkv", C.c_int64), ("z", C.c_void_p), ("ld_z", C.c_int64),
+                ("a", C.c_void_p), ("ld_a", C.c_int64), ("b", C.c_void_p), ("ld_b", C.c_int64)]
+
+
+def load():
+    """Loads libverify.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    L = C.CDLL(LIB_PATH)
+    p, i, i64, f = C.c_void_p, C.c_int, C.c_int64, C.c_float
+    sig = {
+        "verify_init": [i, C.POINTER(p)],
+        "verify_destroy": [p],
+        "verify_last_error": [p],
+        "verify_device_status": [p, p, C.POINTER(C.c_int32)],
+        "verify_launch_count": [p],
+        "q4_qmv_k": [p, C.POINTER(Q4Weight), p, i, p, i, p],
+        "q4_gather_experts_k": [p, C.POINTER(Q4Experts), C.POINTER(Q4Experts), p, i64, i, p, i, p, p, p, i,
+                                C.POINTER(Q4Weight), C.POINTER(Q4Weight), p, p],
+        "gdn_verify_k": [p, C.POINTER(GdnParams), C.POINTER(GdnState), C.POINTER(GdnInputs), i, p, i, p],
+        "gdn_commit": [C.POINTER(GdnState), i],
+        "verify_rmsnorm_k": [p, p, p, f, i, i, i, p, i, p],
+        "verify_synth_q4": [p, p, p, p, i64, i64, C.c_uint64, C.c_uint64, C.c_uint64, f, f, f, f, p],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = C.c_int
+    L.verify_last_error.restype = C.c_char_p
+    L.verify_launch_count.restype = C.c_int64
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def q4_weight(packed, scales, biases) -> Q4Weight:
+    """Q4Weight over device tensors packed [N, K/8] (int32/uint32), scales/biases [N, K/64] (bf16 bits)."""
+    n_out, k_in = packed.shape[-2], packed.shape[-1] * 8
+    return Q4Weight(packed.data_ptr(), scales.data_ptr(), biases.data_ptr(), n_out, k_in, 64, 4)
+
+
+def q4_experts(packed, scales, biases) -> Q4Experts:
+    """Q4Experts over device tensors packed [E, N, K/8], scales/biases [E, N, K/64]."""
+    E, n_out, k_in = packed.shape[0], packed.shape[1], packed.shape[2] * 8
+    return Q4Experts(Q4Weight(packed.data_ptr(), scales.data_ptr(), biases.data_ptr(), n_out, k_in, 64, 4), E)
+
+
+class Verify:
+    """One library context (verify_ctx) on one device."""
+
+    def __init__(self, device: int = 0):
+        self.lib = load()
+        self.ctx = C.c_void_p()
+        st = self.lib.verify_init(device, C.byref(self.ctx))
+        if st != OK:
+            raise VerifyError(st, f"verify_init failed on device {device}")
+
+    def close(self):
+        if self.ctx:
+            self.lib.verify_destroy(self.ctx)
+            self.ctx = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, st):
+        if st != OK:
+            raise VerifyError(st, self.lib.verify_last_error(self.ctx).decode())
+
+    @staticmethod
+    def _stream(stream):
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream().cuda_stream
+        return C.c_void_p(int(stream))
+
+    def launch_count(self) -> int:
+        return int(self.lib.verify_launch_count(self.ctx))
+
+    def device_status(self, stream=None):
+        code = C.c_int32(0)
+        st = self.lib.verify_device_status(self.ctx, self._stream(stream), C.byref(code))
+        return st, code.value
+
+    # ------------------------------------------------------------ entry points
+
+    def q4_qmv_k(self, W: Q4Weight, x, k: int, y, dtype_out: int = F32, stream=None):
+        self._check(self.lib.q4_qmv_k(self.ctx, C.byref(W), _ptr(x), k, _ptr(y), dtype_out,
+                                      self._stream(stream)))
+
+    def q4_gather_experts_k(self, gate_up: Q4Experts, down: Q4Experts, logits, logits_ld: int, top_k: int,
+                            x, k: int, idx_out, w_out, y, dtype_out: int = F32, shared_gate_up=None,
+                            shared_down=None, shared_gate_logit=None, stream=None):
+        self._check(self.lib.q4_gather_experts_k(
+            self.ctx, C.byref(gate_up), C.byref(down), _ptr(logits), logits_ld, top_k, _ptr(x), k,
+            _ptr(idx_out), _ptr(w_out), _ptr(y), dtype_out,
+            C.byref(shared_gate_up) if shared_gate_up is not None else None,
+            C.byref(shared_down) if shared_down is not None else None,
+            _ptr(shared_gate_logit), self._stream(stream)))
+
+    def gdn_verify_k(self, params: GdnParams, state: GdnState, inputs: GdnInputs, k: int, o,
+                     dtype_out: int = F32, stream=None):
+        self._check(self.lib.gdn_verify_k(self.ctx, C.byref(params), C.byref(state), C.byref(inputs), k,
+                                          _ptr(o), dtype_out, self._stream(stream)))
+
+    def gdn_commit(self, state: GdnState, accepted: int):
+        st = self.lib.gdn_commit(C.byref(state), accepted)
+        if st != OK:
+            raise VerifyError(st, f"gdn_commit({accepted}) rejected")
+
+    def verify_rmsnorm_k(self, x, w, eps: float, zero_centered: bool, n: int, k: int, out,
+                         dtype_out: int = BF16, stream=None):
+        self._check(self.lib.verify_rmsnorm_k(self.ctx, _ptr(x), _ptr(w), eps, int(bool(zero_centered)), n, k,
+                                              _ptr(out), dtype_out, self._stream(stream)))
+
+    def synth_q4(self, packed, scales, biases, seeds, scale_range, bias_range, stream=None):
+        self._check(self.lib.verify_synth_q4(self.ctx, _ptr(packed), _ptr(scales), _ptr(biases),
+                                             packed.numel(), scales.numel(), *[C.c_uint64(s) for s in seeds],
+                                             scale_range[0], scale_range[1], bias_range[0], bias_range[1],
+                                             self._stream(stream)))
+
+
+def gdn_params(Hk, Hv, d, conv_w, A_log, dt_bias, norm_w, q_scale=None, l2_eps=1e-6, norm_eps=1e-6,
+               gate_act=0) -> GdnParams:
+    if q_scale is None:
+        q_scale = d ** -0.5
+    return GdnParams(Hk, Hv, d, d, 4, q_scale, l2_eps, norm_eps, gate_act, conv_w.data_ptr(), A_log.data_ptr(),
+                     dt_bias.data_ptr(), norm_w.data_ptr())
+
+
+def gdn_state(S_slots, conv_slots, cur=0) -> GdnState:
+    st = GdnState()
+    for s, (S, t) in enumerate(zip(S_slots, conv_slots)):
+        st.S_slots[s] = S.data_ptr()
+        st.conv_slots[s] = t.data_ptr()
+    st.n_slots = len(S_slots)
+    st.cur = cur
+    st.pending_k = 0
+    return st
+
+
+def gdn_inputs(qkv, z, a, b) -> GdnInputs:
+    return GdnInputs(qkv.data_ptr(), qkv.stride(0), z.data_ptr(), z.stride(0), a.data_ptr(), a.stride(0),
+                     b.data_ptr(), b.stride(0))

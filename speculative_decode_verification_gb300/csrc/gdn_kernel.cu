@@ -1,0 +1,260 @@
+// gdn_kernel.cu - k-row Gated DeltaNet verify step with in-kernel snapshots.
+//
+// What is computed (pages, by title): "QWEN38FLASH.md - Plan for supporting
+// Qwen/Qwen3.8-Flash-Next" section 2.1 (causal depthwise conv over q|k|v, L2
+// norm of q and k per head, softplus/exp decay from A_log/dt_bias, the
+// delta rule S <- gS; m = S k; delta = (v - m) beta; S += delta k^T;
+// y = S q, gated RMSNorm) and 3.1 (scalar per-head decay, sigmoid beta, each
+// k head shared by Hv/Hk v heads); "Red Lite dev45 - speculative decoding
+// with the Qwen3-Next MTP block", "What it is" (row r runs from row r-1's
+// state; the state after each row is written to snapshot buffers from inside
+// the kernel).
+//
+// Design (GB300): one thread-block cluster per V head, one CTA per 16 value
+// rows of that head (8 CTAs for head dim 128, 384 CTAs for 48 heads).  The
+// value rows of the delta rule are independent, so each CTA keeps its
+// 16 x 128 slice of the fp32 state in registers (16 floats per thread, 8
+// threads per value row) for all k rows: the state is read from HBM once and
+// each snapshot is written once with coalesced 16-byte stores.  The conv, the
+// L2 norms and the gates are cheap and recomputed by every CTA of the head.
+// The only cross-CTA step, the RMSNorm's sum of squares over the head's value
+// rows, goes through distributed shared memory in fixed rank order.  There is
+// no atomic and no order that depends on k: row r of a width-k call is
+// bit-identical to a width-1 call from the snapshot after r rows.
+#include "common.cuh"
+#include "internal.h"
+
+namespace vk {
+
+constexpr int kGdnRows = 16;      // value rows per CTA
+constexpr int kGdnThreads = 128;  // 8 threads per value row
+constexpr int kGdnMaxK = 16;
+
+__device__ __forceinline__ float sigmoidf_(float t) { return 1.f / (1.f + expf(-t)); }
+__device__ __forceinline__ float siluf_(float t) { return t / (1.f + expf(-t)); }
+__device__ __forceinline__ float softplusf_(float t) { return fmaxf(t, 0.f) + log1pf(expf(-fabsf(t))); }
+
+template <int D>
+__global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a) {
+  constexpr int P = D / kGdnRows;   // CTAs per head (cluster size)
+  constexpr int JPT = D / 8;        // state columns per thread
+  __shared__ __align__(16) float qn[kGdnMaxK][D];
+  __shared__ __align__(16) float kn[kGdnMaxK][D];
+  __shared__ float vs[kGdnMaxK][kGdnRows];
+  __shared__ float ys[kGdnMaxK][kGdnRows];
+  __shared__ float gs[kGdnMaxK], bs[kGdnMaxK], kq[kGdnMaxK];
+  __shared__ float ss_part[kGdnMaxK];
+
+  const int p = (int)cluster_rank();
+  const int h = blockIdx.x / P;
+  const int hq = h / (a.Hv / a.Hk);
+  const int tid = threadIdx.x;
+  const int k = a.k;
+  const int C = 2 * a.Hk * D + a.Hv * D;
+  const bool owns_qk_tail = (h % (a.Hv / a.Hk)) == 0;
+
+  // ---- 1. causal depthwise conv + SiLU for the q, k channels of QK head hq
+  //         and the v channels of this CTA's value rows; slide the window.
+  for (int cl = tid; cl < 2 * D + kGdnRows; cl += kGdnThreads) {
+    int ch;
+    bool write_tail;
+    if (cl < D) { ch = hq * D + cl; write_tail = owns_qk_tail && (cl / (D / P) == p); }
+    else if (cl < 2 * D) { ch = a.Hk * D + hq * D + (cl - D); write_tail = owns_qk_tail && ((cl - D) / (D / P) == p); }
+    else { ch = 2 * a.Hk * D + h * D + p * kGdnRows + (cl - 2 * D); write_tail = true; }
+    float w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) w[t] = a.conv_w[ch * 4 + t];
+    uint16_t w0 = a.tail_in[ch], w1 = a.tail_in[C + ch], w2 = a.tail_in[2 * C + ch];
+    for (int r = 0; r < k; ++r) {
+      const uint16_t xr = a.qkv[r * a.ld_qkv + ch];
+      float acc = w[0] * bf16f(w0);
+      acc = fmaf(w[1], bf16f(w1), acc);
+      acc = fmaf(w[2], bf16f(w2), acc);
+      acc = fmaf(w[3], bf16f(xr), acc);
+      const float cv = siluf_(acc);
+      if (cl < D) qn[r][cl] = cv;
+      else if (cl < 2 * D) kn[r][cl - D] = cv;
+      else vs[r][cl - 2 * D] = cv;
+      w0 = w1; w1 = w2; w2 = xr;
+      if (write_tail) {
+        a.tail_out[r][ch] = w0;
+        a.tail_out[r][C + ch] = w1;
+        a.tail_out[r][2 * C + ch] = w2;
+      }
+    }
+  }
+  // ---- gates
+  if (tid < k) {
+    const int r = tid;
+    const float av = bf16f(a.a[r * a.ld_a + h]), bv = bf16f(a.b[r * a.ld_b + h]);
+    bs[r] = sigmoidf_(bv);
+    gs[r] = expf(-expf(a.A_log[h]) * softplusf_(av + a.dt_bias[h]));
+  }
+  __syncthreads();
+
+  // ---- 2. L2 norms of q and k per row (warp w: rows w, w+4, ...), k.q
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int r = warp; r < k; r += kGdnThreads / 32) {
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int j = lane; j < D; j += 32) {
+        sq = fmaf(qn[r][j], qn[r][j], sq);
+        sk = fmaf(kn[r][j], kn[r][j], sk);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+      }
+      const float nq = sqrtf(sq + a.l2_eps), nk = sqrtf(sk + a.l2_eps);
+      float dot = 0.f;
+#pragma unroll
+      for (int j = lane; j < D; j += 32) {
+        const float qv = qn[r][j] / nq * a.q_scale;
+        const float kv = kn[r][j] / nk;
+        qn[r][j] = qv;
+        kn[r][j] = kv;
+        dot = fmaf(kv, qv, dot);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      if (lane == 0) kq[r] = dot;
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. delta rule over the k rows, state slice in registers
+  const int il = tid >> 3, l = tid & 7;
+  const int i = p * kGdnRows + il;  // value row within the head
+  float s[JPT];
+  {
+    const float* src = a.S_in + ((long long)h * D + i) * D;
+#pragma unroll
+    for (int m = 0; m < JPT / 4; ++m) {
+      const float4 v = *reinterpret_cast<const float4*>(src + 4 * l + 32 * m);
+      s[4 * m] = v.x; s[4 * m + 1] = v.y; s[4 * m + 2] = v.z; s[4 * m + 3] = v.w;
+    }
+  }
+  for (int r = 0; r < k; ++r) {
+    const float g = gs[r], beta = bs[r];
+    float mk = 0.f, mq = 0.f;
+#pragma unroll
+    for (int m = 0; m < JPT / 4; ++m) {
+      const float4 kv = *reinterpret_cast<const float4*>(&kn[r][4 * l + 32 * m]);
+      const float4 qv = *reinterpret_cast<const float4*>(&qn[r][4 * l + 32 * m]);
+      const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
+      const float qq[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float sv = g * s[4 * m + e];
+        s[4 * m + e] = sv;
+        mk = fmaf(sv, kk[e], mk);
+        mq = fmaf(sv, qq[e], mq);
+      }
+    }
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {
+      mk += __shfl_xor_sync(0xffffffffu, mk, off);
+      mq += __shfl_xor_sync(0xffffffffu, mq, off);
+    }
+    const float delta = (vs[r][il] - mk) * beta;
+    const float y = fmaf(delta, kq[r], mq);  // (S + delta k^T) q = S q + delta (k.q)
+    float* dst = a.S_out[r] + ((long long)h * D + i) * D;
+#pragma unroll
+    for (int m = 0; m < JPT / 4; ++m) {
+      const float4 kv = *reinterpret_cast<const float4*>(&kn[r][4 * l + 32 * m]);
+      s[4 * m] = fmaf(delta, kv.x, s[4 * m]);
+      s[4 * m + 1] = fmaf(delta, kv.y, s[4 * m + 1]);
+      s[4 * m + 2] = fmaf(delta, kv.z, s[4 * m + 2]);
+      s[4 * m + 3] = fmaf(delta, kv.w, s[4 * m + 3]);
+      *reinterpret_cast<float4*>(dst + 4 * l + 32 * m) = make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]);
+    }
+    if (l == 0) ys[r][il] = y;
+  }
+  __syncthreads();
+
+  // ---- 4. gated RMSNorm over the head's D value rows (cluster-wide sum)
+  if (tid < k) {
+    float ss = 0.f;
+    for (int t = 0; t < kGdnRows; ++t) ss = fmaf(ys[tid][t], ys[tid][t], ss);
+    ss_part[tid] = ss;
+  }
+  cluster_sync();
+  for (int e = tid; e < k * kGdnRows; e += kGdnThreads) {
+    const int r = e / kGdnRows, ii = e % kGdnRows;
+    float tot = 0.f;
+    for (int q = 0; q < P; ++q) tot += ld_dsmem_f32(&ss_part[r], (uint32_t)q);
+    const float inv = 1.f / sqrtf(tot / (float)D + a.norm_eps);
+    const int iv = p * kGdnRows + ii;
+    const float zz = bf16f(a.z[r * a.ld_z + h * D + iv]);
+    const float act = a.gate_act == 1 ? siluf_(zz) : sigmoidf_(zz);
+    const float ov = ys[r][ii] * inv * a.norm_w[iv] * act;
+    const long long oi = (long long)r * a.Hv * D + h * D + iv;
+    if (a.dtype == 1) reinterpret_cast<uint16_t*>(a.o)[oi] = f2bf16(ov);
+    else reinterpret_cast<float*>(a.o)[oi] = ov;
+  }
+  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+}
+
+template <int D>
+static cudaError_t launch_gdn_d(const GdnArgs& a, cudaStream_t s) {
+  constexpr int P = D / kGdnRows;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hv * P);
+  cfg.blockDim = dim3(kGdnThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = P;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gdn_verify_kernel<D>, a);
+}
+
+cudaError_t gdn_setup_kernels() { return cudaSuccess; }
+
+cudaError_t launch_gdn(const GdnArgs& a, cudaStream_t s) {
+  switch (a.d) {
+    case 32: return launch_gdn_d<32>(a, s);
+    case 64: return launch_gdn_d<64>(a, s);
+    case 128: return launch_gdn_d<128>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// ------------------------------------------------------------------ glue
+
+// out = x / sqrt(mean(x^2) + eps) * (zc ? 1 + w : w), one CTA per row.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const float* w, float eps, int zc, int n,
+                                                      void* out, int dtype) {
+  const int r = blockIdx.x;
+  const float* xr = x + (long long)r * n;
+  __shared__ float red[8];
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < n; c += blockDim.x) ss = fmaf(xr[c], xr[c], ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
+  const float inv = 1.f / sqrtf(tot / (float)n + eps);
+  for (int c = threadIdx.x; c < n; c += blockDim.x) {
+    const float wt = zc ? 1.f + w[c] : w[c];
+    const float v = xr[c] * inv * wt;
+    if (dtype == 1) reinterpret_cast<uint16_t*>(out)[(long long)r * n + c] = f2bf16(v);
+    else reinterpret_cast<float*>(out)[(long long)r * n + c] = v;
+  }
+}
+
+cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, int n, int k, void* out, int dtype,
+                           cudaStream_t s) {
+  rmsnorm_kernel<<<k, 256, 0, s>>>(x, w, eps, zc, n, out, dtype);
+  return cudaGetLastError();
+}
+
+}  // namespace vk

@@ -1,0 +1,689 @@
+// q4_kernels.cu - affine Q4/g64 weight x k BF16 rows on the GB300 tensor cores.
+//
+// What is computed (pages, by title): "Flash-Next optimization transfer to
+// Ornith and Qwen 27B", table "Shared architecture and implemented paths"
+// (affine Q4, group 64, BF16) and section "Exact verification kernels"
+// (width-k equals serial QMV; gathered top-8 experts with fused gate/up);
+// "Red Lite dev45 - speculative decoding with the Qwen3-Next MTP block",
+// "What it is" (decode each weight once for all rows, each row in the 1-row
+// order; all (expert,row) pairs in one dispatch, one tail).
+//
+// Design (GB300, sm_103a):
+//  * One CTA = 1 producer warp + 4 consumer warps; 2 CTAs per SM.  The
+//    producer streams 128-row x 256-column weight tiles with TMA (128-byte
+//    swizzle) into a 4-stage shared-memory ring, plus the tile's bf16 scales
+//    and biases and the activation rows with cp.async, all completing on one
+//    mbarrier per stage.  Each weight byte crosses HBM once per call.
+//  * Consumers decode each packed word once into bf16 code pairs (128 + q,
+//    exact) with one byte permute + one lop3 per pair and feed them to
+//    mma.sync m16n8k16 as the A operand; the k activation rows are the N
+//    columns (8 per MMA, two MMA columns blocks for k > 8).  Per 64-column
+//    group the fp32 result C = sum (128+q) x is folded as
+//        acc += s*C + (b - 128 s) * sum(x)
+//    where sum(x) comes from one extra MMA with A = 1.  Products of integer
+//    codes with bf16 x are exact, accumulation is fp32.
+//  * Every output column is an independent dot product, the group order is
+//    fixed and the split of the K range across CTAs depends only on (N, K,
+//    SM count): row r of a width-k call is bit-identical to a width-1 call.
+//  * Dense: persistent stream-K grid; a row tile split across CTAs is
+//    reduced by the last CTA to arrive (an atomic counter, no waiting), in
+//    ascending K order.  Routed MoE: items = (distinct expert, row tile) with
+//    the full K per item; the down kernel's last arriver per 128 outputs does
+//    the fixed-order combine.
+#include "common.cuh"
+#include "internal.h"
+
+namespace vk {
+
+template <int NT>
+struct Q4Layout {
+  static constexpr int NB = 8 * NT;                          // activation rows held per stage
+  static constexpr int W_BYTES = kBM * 128;                  // 128 rows x 32 packed words
+  static constexpr int X_BYTES = kGroupsPerUnit * NB * 128;  // [group][row][64 bf16]
+  static constexpr int SB_BYTES = 2 * kBM * 8;               // scales then biases, 4 groups per row
+  static constexpr int STAGE = W_BYTES + X_BYTES + SB_BYTES;
+  static constexpr int BAR_OFF = kStages * STAGE;
+  static constexpr int MISC_OFF = BAR_OFF + 2 * kStages * 8;
+  static constexpr int MISC_BYTES = 64;
+  static constexpr int BASE_BYTES = MISC_OFF + MISC_BYTES;
+  static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
+};
+
+// Routing tables kept in shared memory by the MoE kernels.
+struct RouteSmem {
+  uint32_t mask[kMaxExperts];      // bit r set: row r selected the expert
+  int16_t ulist[kMaxExperts];      // distinct selected experts, ascending
+  int32_t idx[16 * kMaxTopK];      // [r][j]
+  float w[16 * kMaxTopK];          // [r][j]
+  int U;
+};
+
+// One pipeline fill: what the producer needs to know about a tile.
+struct TileSrc {
+  const CUtensorMap* map;
+  int y0, y1;          // TMA row coordinate of the box(es)
+  int two_boxes;       // 1: two 64-row boxes (gate rows, up rows); 0: one 128-row box
+  int row_limit;       // tile rows i with (row index within its matrix) >= limit are empty
+  int mat_row0;        // matrix row of tile row 0 (for the limit test)
+  const uint16_t* scales;  // base of the scales/biases arrays addressed with global rows
+  const uint16_t* biases;
+  int KG;
+};
+
+__device__ __forceinline__ int tile_global_row(const TileSrc& t, int i) {
+  if (t.two_boxes) return i < 64 ? t.y0 + i : t.y1 + (i - 64);
+  return (t.mat_row0 + i < t.row_limit) ? t.y0 + i : -1;
+}
+
+// ---------------------------------------------------------------- producer
+
+template <int NT>
+__device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_bar, const TileSrc& t, int kc,
+                                              int gcount, const uint16_t* const* brow, int nb, int lane) {
+  using L = Q4Layout<NT>;
+  const uint32_t w_dst = smem_addr(stage_ptr);
+  const uint32_t x_dst = w_dst + L::W_BYTES;
+  const uint32_t sb_dst = x_dst + L::X_BYTES;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(full_bar, L::W_BYTES);
+    if (t.two_boxes) {
+      tma_load_2d(w_dst, t.map, full_bar, kc * 32, t.y0);
+      tma_load_2d(w_dst + 64 * 128, t.map, full_bar, kc * 32, t.y1);
+    } else {
+      tma_load_2d(w_dst, t.map, full_bar, kc * 32, t.y0);
+    }
+  }
+  // scales / biases: 128 rows x 2 words (4 groups) per array
+  const int e0 = 4 * kc;
+#pragma unroll
+  for (int idx = lane; idx < 2 * kBM * 2; idx += 32) {
+    const int arr = idx >> 8;
+    const int row = (idx >> 1) & (kBM - 1);
+    const int word = idx & 1;
+    const int gr = tile_global_row(t, row);
+    const bool valid = gr >= 0 && 2 * word < gcount;
+    const uint16_t* base = arr ? t.biases : t.scales;
+    const uint16_t* src = valid ? base + (long long)gr * t.KG + e0 + 2 * word : base;
+    cp_async4(sb_dst + arr * (kBM * 8) + row * 8 + word * 4, src, valid ? 4u : 0u);
+  }
+  // activation rows: [group][row][8 chunks of 16 B], chunk index xor (row & 7)
+#pragma unroll
+  for (int idx = lane; idx < L::NB * 32; idx += 32) {
+    const int b = idx >> 5;
+    const int G = (idx >> 3) & 3;
+    const int ch = idx & 7;
+    const bool valid = b < nb && G < gcount;
+    const uint16_t* src = valid ? brow[b] + kc * 256 + G * 64 + ch * 8 : brow[0];
+    cp_async16(x_dst + G * (L::NB * 128) + b * 128 + ((ch ^ (b & 7)) << 4), src, valid ? 16u : 0u);
+  }
+  cp_async_mbar_arrive_noinc(full_bar);
+}
+
+// ---------------------------------------------------------------- consumer
+
+__device__ __forceinline__ uint32_t decode_pair(uint32_t v, uint32_t vs, uint32_t sel) {
+  // bf16x2 (128 + nibble 2b, 128 + nibble 2b+1) of byte b of v; vs = v >> 4
+  return and_or(prmt(v, vs, sel), 0x000F000Fu, 0x43004300u);
+}
+
+// Accumulates one pipeline stage (gcount groups) into acc.  rbase[m] is the
+// tile row of M-tile m's first row for this warp.
+template <int NT>
+__device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, int gcount, const int (&rbase)[2], int lane,
+                                              float (&acc)[2][NT][4]) {
+  using L = Q4Layout<NT>;
+  const uint32_t w_src = smem_addr(stage_ptr);
+  const uint32_t x_src = w_src + L::W_BYTES;
+  const uint32_t sb_src = x_src + L::X_BYTES;
+  const int g = lane >> 2, c = lane & 3;
+  constexpr uint32_t ONE2 = 0x3F803F80u;  // bf16x2 (1, 1)
+
+  // scales / biases of this thread's four rows, four groups each
+  uint2 sw[2][2], bw[2][2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = rbase[m] + g + 8 * h;
+      sw[m][h] = lds64(sb_src + row * 8);
+      bw[m][h] = lds64(sb_src + kBM * 8 + row * 8);
+    }
+
+#pragma unroll
+  for (int G = 0; G < kGroupsPerUnit; ++G) {
+    if (G >= gcount) break;
+    // B fragments: activation row 8t+g, columns 16c .. 16c+15 of the group
+    uint32_t bf[NT][8];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int b = 8 * t + g;
+      const uint32_t rowa = x_src + G * (L::NB * 128) + b * 128;
+      const uint4 xa = lds128(rowa + (((2 * c) ^ (b & 7)) << 4));
+      const uint4 xb = lds128(rowa + (((2 * c + 1) ^ (b & 7)) << 4));
+      bf[t][0] = xa.x; bf[t][1] = xa.y; bf[t][2] = xa.z; bf[t][3] = xa.w;
+      bf[t][4] = xb.x; bf[t][5] = xb.y; bf[t][6] = xb.z; bf[t][7] = xb.w;
+    }
+    // sum of the group's activations per column (A = 1)
+    float sx[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      sx[t][0] = sx[t][1] = sx[t][2] = sx[t][3] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_bf16_16816(sx[t], ONE2, ONE2, ONE2, ONE2, bf[t][2 * j], bf[t][2 * j + 1]);
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int row = rbase[m] + g;
+      const uint32_t off = (uint32_t)((((2 * G + (c >> 1)) ^ (row & 7)) << 4) + ((c & 1) << 3));
+      const uint2 wa = lds64(w_src + row * 128 + off);        // words 2c, 2c+1 of row g
+      const uint2 wb = lds64(w_src + (row + 8) * 128 + off);  // same for row g+8
+      uint32_t A[4][4];
+      {
+        const uint32_t va0 = wa.x, va1 = wa.y, vb0 = wb.x, vb1 = wb.y;
+        const uint32_t sa0 = va0 >> 4, sa1 = va1 >> 4, sb0 = vb0 >> 4, sb1 = vb1 >> 4;
+        // MMA j = 2*word + half uses bytes 2*half (cols 2c,2c+1) and 2*half+1 (cols 2c+8,2c+9)
+        A[0][0] = decode_pair(va0, sa0, 0x0400); A[0][1] = decode_pair(vb0, sb0, 0x0400);
+        A[0][2] = decode_pair(va0, sa0, 0x0501); A[0][3] = decode_pair(vb0, sb0, 0x0501);
+        A[1][0] = decode_pair(va0, sa0, 0x0602); A[1][1] = decode_pair(vb0, sb0, 0x0602);
+        A[1][2] = decode_pair(va0, sa0, 0x0703); A[1][3] = decode_pair(vb0, sb0, 0x0703);
+        A[2][0] = decode_pair(va1, sa1, 0x0400); A[2][1] = decode_pair(vb1, sb1, 0x0400);
+        A[2][2] = decode_pair(va1, sa1, 0x0501); A[2][3] = decode_pair(vb1, sb1, 0x0501);
+        A[3][0] = decode_pair(va1, sa1, 0x0602); A[3][1] = decode_pair(vb1, sb1, 0x0602);
+        A[3][2] = decode_pair(va1, sa1, 0x0703); A[3][3] = decode_pair(vb1, sb1, 0x0703);
+      }
+      const uint32_t s_lo = (G & 2) ? sw[m][0].y : sw[m][0].x;
+      const uint32_t s_hi = (G & 2) ? sw[m][1].y : sw[m][1].x;
+      const uint32_t b_lo = (G & 2) ? bw[m][0].y : bw[m][0].x;
+      const uint32_t b_hi = (G & 2) ? bw[m][1].y : bw[m][1].x;
+      const float sA = (G & 1) ? bf16hi(s_lo) : bf16lo(s_lo);
+      const float sB = (G & 1) ? bf16hi(s_hi) : bf16lo(s_hi);
+      const float bA = fmaf(-128.f, sA, (G & 1) ? bf16hi(b_lo) : bf16lo(b_lo));
+      const float bB = fmaf(-128.f, sB, (G & 1) ? bf16hi(b_hi) : bf16lo(b_hi));
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float cg[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16_16816(cg, A[j][0], A[j][1], A[j][2], A[j][3], bf[t][2 * j], bf[t][2 * j + 1]);
+        acc[m][t][0] = fmaf(bA, sx[t][0], fmaf(sA, cg[0], acc[m][t][0]));
+        acc[m][t][1] = fmaf(bA, sx[t][1], fmaf(sA, cg[1], acc[m][t][1]));
+        acc[m][t][2] = fmaf(bB, sx[t][2], fmaf(sB, cg[2], acc[m][t][2]));
+        acc[m][t][3] = fmaf(bB, sx[t][3], fmaf(sB, cg[3], acc[m][t][3]));
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void store_out(void* y, int dtype, long long i, float v) {
+  if (dtype == 1) {
+    reinterpret_cast<uint16_t*>(y)[i] = f2bf16(v);
+  } else if (dtype == 2) {
+    reinterpret_cast<float*>(y)[i] += v;
+  } else {
+    reinterpret_cast<float*>(y)[i] = v;
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[2][NT][4]) {
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[m][t][q] = 0.f;
+}
+
+__device__ __forceinline__ void init_barriers(uint32_t bar_base) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_base + 8 * s, 33);                        // full: producer lane 0 tx + 32 cp.async arrivals
+      mbar_init(bar_base + 8 * (kStages + s), kConsumerWarps);  // empty: one arrival per consumer warp
+    }
+    fence_mbar_init();
+  }
+}
+
+// On abort the producer keeps the CTA alive until its TMA writes have landed.
+template <int NT>
+__device__ __forceinline__ void producer_drain(uint32_t bar_base, long long fills, volatile int* abort) {
+  for (long long f = (fills > kStages ? fills - kStages : 0); f < fills; ++f) {
+    const int s = (int)(f % kStages);
+    const uint32_t ph = (uint32_t)((f / kStages) & 1);
+    if (mbar_try_wait(bar_base + 8 * s, ph)) continue;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar_base + 8 * s, ph) && clock64() - t0 < kWaitTimeoutCycles) {
+    }
+  }
+  (void)abort;
+}
+
+// ================================================================== dense
+
+__device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
+  return (int)(((u + 1) * (long long)G - 1) / U);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
+    q4_dense_kernel(const __grid_constant__ CUtensorMap wmap, const DenseArgs a) {
+  using L = Q4Layout<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t bar_base = smem_addr(smem + L::BAR_OFF);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
+  volatile int* bcast = abort + 1;
+  if (threadIdx.x == 0) { *abort = 0; *bcast = 0; }
+  init_barriers(bar_base);
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long u0 = (long long)blockIdx.x * a.U / a.G;
+  const long long u1 = (long long)(blockIdx.x + 1) * a.U / a.G;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) tma_prefetch_desc(&wmap);
+    const uint16_t* brow[L::NB];
+#pragma unroll
+    for (int b = 0; b < L::NB; ++b) brow[b] = a.x + (long long)(b < a.k ? b : 0) * a.K;
+    long long fills = 0;
+    for (long long u = u0; u < u1; ++u, ++fills) {
+      const int s = (int)(fills % kStages);
+      const uint32_t ph = (uint32_t)((fills / kStages) & 1);
+      if (!mbar_wait(bar_base + 8 * (kStages + s), ph ^ 1, abort, a.err)) break;
+      const int tile = (int)(u / a.KC), kc = (int)(u % a.KC);
+      TileSrc ts;
+      ts.map = &wmap; ts.y0 = tile * kBM; ts.y1 = 0; ts.two_boxes = 0;
+      ts.row_limit = a.N; ts.mat_row0 = tile * kBM;
+      ts.scales = a.scales; ts.biases = a.biases; ts.KG = a.KG;
+      const int gcount = min(kGroupsPerUnit, a.KG - 4 * kc);
+      produce_stage<NT>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, gcount, brow, a.k, lane);
+    }
+    if (*abort) producer_drain<NT>(bar_base, fills, abort);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, c = lane & 3;
+  const int rbase[2] = {32 * warp, 32 * warp + 16};
+  float acc[2][NT][4];
+  zero_acc<NT>(acc);
+  long long fills = 0;
+  int cur_tile = (int)(u0 / a.KC);
+  long long seg_start = u0;
+
+  auto flush = [&](int tile, long long s_begin, long long s_end) {
+    const long long tfirst = (long long)tile * a.KC, tlast = tfirst + a.KC - 1;
+    const int row0 = tile * kBM + 32 * warp;
+    if (s_begin == tfirst && s_end == tlast + 1) {
+      if (*abort) return;
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int row = row0 + 16 * m + g + 8 * (q >> 1);
+            const int col = 8 * t + 2 * c + (q & 1);
+            if (row < a.N && col < a.k) store_out(a.y, a.dtype, (long long)col * a.N + row, acc[m][t][q]);
+          }
+      return;
+    }
+    // partial tile: publish, count arrivals, the last arriver reduces in K order
+    constexpr int SLOT = kConsumerWarps * 2 * NT * 32 * 4;
+    const int slot = (s_begin == u0) ? 2 * blockIdx.x : 2 * blockIdx.x + 1;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float4* dst = reinterpret_cast<float4*>(a.part + (long long)slot * SLOT + (((warp * 2 + m) * NT + t) * 32 + lane) * 4);
+        *dst = make_float4(acc[m][t][0], acc[m][t][1], acc[m][t][2], acc[m][t][3]);
+      }
+    __threadfence();
+    named_bar(1, kConsumerWarps * 32);
+    const int cfirst = cta_of_unit(tfirst, a.U, a.G), clast = cta_of_unit(tlast, a.U, a.G);
+    if (threadIdx.x == 0) {
+      int last = 0;
+      if (!*abort) {
+        const int old = atomicAdd(a.cnt + tile, 1);
+        last = (old == clast - cfirst);
+        if (last) atomicExch(a.cnt + tile, 0);
+      }
+      *bcast = last;
+    }
+    named_bar(1, kConsumerWarps * 32);
+    if (!*bcast) return;
+    __threadfence();
+    float tot[2][NT][4];
+    zero_acc<NT>(tot);
+    for (int cc = cfirst; cc <= clast; ++cc) {
+      const long long cu0 = (long long)cc * a.U / a.G;
+      const int cslot = (cu0 >= tfirst) ? 2 * cc : 2 * cc + 1;
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(
+              a.part + (long long)cslot * SLOT + (((warp * 2 + m) * NT + t) * 32 + lane) * 4));
+          tot[m][t][0] += v.x; tot[m][t][1] += v.y; tot[m][t][2] += v.z; tot[m][t][3] += v.w;
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int row = row0 + 16 * m + g + 8 * (q >> 1);
+          const int col = 8 * t + 2 * c + (q & 1);
+          if (row < a.N && col < a.k) store_out(a.y, a.dtype, (long long)col * a.N + row, tot[m][t][q]);
+        }
+  };
+
+  for (long long u = u0; u < u1; ++u, ++fills) {
+    const int tile = (int)(u / a.KC), kc = (int)(u % a.KC);
+    if (tile != cur_tile) {
+      flush(cur_tile, seg_start, u);
+      zero_acc<NT>(acc);
+      cur_tile = tile;
+      seg_start = u;
+    }
+    const int s = (int)(fills % kStages);
+    const uint32_t ph = (uint32_t)((fills / kStages) & 1);
+    if (mbar_wait(bar_base + 8 * s, ph, abort, a.err)) {
+      const int gcount = min(kGroupsPerUnit, a.KG - 4 * kc);
+      consume_stage<NT>(smem + s * L::STAGE, gcount, rbase, lane, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
+  }
+  flush(cur_tile, seg_start, u1);
+}
+
+// ================================================================== MoE
+
+__device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+  for (int e = tid; e < a.E; e += nthr) rs->mask[e] = 0u;
+  __syncthreads();
+  for (int r = warp; r < a.k; r += nwarps) {
+    const float* l = a.logits + (long long)r * a.logits_ld;
+    float v[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < a.E ? l[e] : 0.f;
+    }
+    uint32_t taken = 0;
+    float myv = 0.f;
+    int mye = -1;
+    for (int j = 0; j < a.T; ++j) {
+      float bv = 0.f;
+      int be = -1;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        if (e < a.E && !((taken >> i) & 1u) && (be < 0 || v[i] > bv)) { bv = v[i]; be = e; }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be))) { bv = ov; be = oe; }
+      }
+      if (lane == (be & 31)) taken |= 1u << (be >> 5);
+      if (lane == j) { myv = bv; mye = be; }
+    }
+    const float top = __shfl_sync(0xffffffffu, myv, 0);
+    const float ex = lane < a.T ? expf(myv - top) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    sum = __shfl_sync(0xffffffffu, sum, 0);
+    if (lane < a.T) {
+      rs->idx[r * kMaxTopK + lane] = mye;
+      rs->w[r * kMaxTopK + lane] = ex / sum;
+      atomicOr(&rs->mask[mye], 1u << r);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int running = 0;
+    for (int base = 0; base < a.E; base += 32) {
+      const int e = base + lane;
+      const bool f = e < a.E && rs->mask[e] != 0u;
+      const uint32_t bal = __ballot_sync(0xffffffffu, f);
+      if (f) rs->ulist[running + __popc(bal & ((1u << lane) - 1u))] = (int16_t)e;
+      running += __popc(bal);
+    }
+    if (lane == 0) rs->U = running;
+  }
+  __syncthreads();
+}
+
+// Row r and rank j of the b-th (ascending row) pair routed to expert slot u.
+__device__ __forceinline__ void pair_of(const RouteSmem* rs, const MoeArgs& a, int u, int b, int& r, int& j) {
+  const int U = rs->U;
+  if (u >= U) {  // shared expert: every row, slot T
+    r = b;
+    j = a.T;
+    return;
+  }
+  const int e = rs->ulist[u];
+  uint32_t m = rs->mask[e];
+  for (int i = 0; i < b; ++i) m &= m - 1u;
+  r = __ffs(m) - 1;
+  j = 0;
+  for (int jj = 0; jj < a.T; ++jj)
+    if (rs->idx[r * kMaxTopK + jj] == e) j = jj;
+}
+
+__device__ __forceinline__ int pairs_of(const RouteSmem* rs, const MoeArgs& a, int u) {
+  return u >= rs->U ? a.k : __popc(rs->mask[rs->ulist[u]]);
+}
+
+template <int NT, bool GATEUP>
+__global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
+    moe_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap smap, const MoeArgs a) {
+  using L = Q4Layout<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t bar_base = smem_addr(smem + L::BAR_OFF);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
+  volatile int* bcast = abort + 1;
+  RouteSmem* rs = reinterpret_cast<RouteSmem*>(smem + L::BASE_BYTES);
+  if (threadIdx.x == 0) { *abort = 0; *bcast = 0; }
+  init_barriers(bar_base);
+  route_rows(a, rs);  // contains __syncthreads
+
+  const int TS = a.T + a.has_shared;
+  if (GATEUP && blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < a.k * a.T; i += blockDim.x) {
+      a.idx_out[i] = rs->idx[(i / a.T) * kMaxTopK + i % a.T];
+      a.w_out[i] = rs->w[(i / a.T) * kMaxTopK + i % a.T];
+    }
+  }
+  const int n_experts = rs->U + a.has_shared;
+  const int ntiles = GATEUP ? a.I / 64 : (a.H + kBM - 1) / kBM;
+  const int n_items = n_experts * ntiles;
+  const int K = GATEUP ? a.H : a.I;
+  const int KG = K / 64, KC = (KG + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) { tma_prefetch_desc(&map); if (a.has_shared) tma_prefetch_desc(&smap); }
+    long long fills = 0;
+    for (int item = blockIdx.x; item < n_items && !*abort; item += a.G) {
+      const int u = item / ntiles, tile = item % ntiles;
+      const bool shared = u >= rs->U;
+      const int e = shared ? 0 : rs->ulist[u];
+      const int nb = pairs_of(rs, a, u);
+      const uint16_t* brow[L::NB];
+#pragma unroll
+      for (int b = 0; b < L::NB; ++b) {
+        int r = 0, j = 0;
+        if (b < nb) pair_of(rs, a, u, b, r, j);
+        brow[b] = GATEUP ? a.x + (long long)r * a.H : a.hbuf + ((long long)r * TS + j) * a.I;
+      }
+      TileSrc ts;
+      ts.map = shared ? &smap : &map;
+      ts.KG = KG;
+      if (GATEUP) {
+        ts.two_boxes = 1;
+        ts.y0 = (shared ? 0 : e * 2 * a.I) + 64 * tile;
+        ts.y1 = ts.y0 + a.I;
+        ts.row_limit = 0; ts.mat_row0 = 0;
+        ts.scales = shared ? a.sgu_scales : a.gu_scales;
+        ts.biases = shared ? a.sgu_biases : a.gu_biases;
+      } else {
+        ts.two_boxes = 0;
+        ts.y0 = (shared ? 0 : e * a.H) + kBM * tile;
+        ts.y1 = 0;
+        ts.row_limit = a.H; ts.mat_row0 = kBM * tile;
+        ts.scales = shared ? a.sdn_scales : a.dn_scales;
+        ts.biases = shared ? a.sdn_biases : a.dn_biases;
+      }
+      for (int kc = 0; kc < KC; ++kc, ++fills) {
+        const int s = (int)(fills % kStages);
+        const uint32_t ph = (uint32_t)((fills / kStages) & 1);
+        if (!mbar_wait(bar_base + 8 * (kStages + s), ph ^ 1, abort, a.err)) break;
+        const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
+        produce_stage<NT>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, gcount, brow, nb, lane);
+      }
+    }
+    if (*abort) producer_drain<NT>(bar_base, fills, abort);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, c = lane & 3;
+  int rbase[2];
+  if (GATEUP) { rbase[0] = 16 * warp; rbase[1] = 64 + 16 * warp; }
+  else { rbase[0] = 32 * warp; rbase[1] = 32 * warp + 16; }
+  long long fills = 0;
+  for (int item = blockIdx.x; item < n_items; item += a.G) {
+    const int u = item / ntiles, tile = item % ntiles;
+    const int nb = pairs_of(rs, a, u);
+    float acc[2][NT][4];
+    zero_acc<NT>(acc);
+    for (int kc = 0; kc < KC; ++kc, ++fills) {
+      const int s = (int)(fills % kStages);
+      const uint32_t ph = (uint32_t)((fills / kStages) & 1);
+      if (mbar_wait(bar_base + 8 * s, ph, abort, a.err)) {
+        const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
+        consume_stage<NT>(smem + s * L::STAGE, gcount, rbase, lane, acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
+    }
+    // pair ids of this thread's columns
+    long long pid[NT][2];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int b = 8 * t + 2 * c + q;
+        int r = 0, j = 0;
+        if (b < nb) pair_of(rs, a, u, b, r, j);
+        pid[t][q] = b < nb ? (long long)r * TS + j : -1;
+      }
+    if (GATEUP) {
+      if (*abort) continue;
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const long long p = pid[t][q & 1];
+          if (p < 0) continue;
+          const int i = 64 * tile + 16 * warp + g + 8 * (q >> 1);
+          const float gate = acc[0][t][q], up = acc[1][t][q];
+          const float h = gate / (1.f + expf(-gate)) * up;
+          a.hbuf[p * a.I + i] = f2bf16(h);
+        }
+    } else {
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const long long p = pid[t][q & 1];
+            const int n = kBM * tile + 32 * warp + 16 * m + g + 8 * (q >> 1);
+            if (p >= 0 && n < a.H) a.part[p * a.H + n] = acc[m][t][q];
+          }
+      __threadfence();
+      named_bar(1, kConsumerWarps * 32);
+      if (threadIdx.x == 0) {
+        int last = 0;
+        if (!*abort) {
+          const int old = atomicAdd(a.cnt + tile, 1);
+          last = (old == n_experts - 1);
+          if (last) atomicExch(a.cnt + tile, 0);
+        }
+        *bcast = last;
+      }
+      named_bar(1, kConsumerWarps * 32);
+      if (*bcast) {
+        __threadfence();
+        const int n = kBM * tile + threadIdx.x;
+        if (n < a.H) {
+          for (int r = 0; r < a.k; ++r) {
+            float y = 0.f;
+            for (int j = 0; j < a.T; ++j)
+              y = fmaf(rs->w[r * kMaxTopK + j], __ldcg(a.part + ((long long)r * TS + j) * a.H + n), y);
+            if (a.has_shared) {
+              const float sg = a.shared_logit[(long long)r * a.logits_ld];
+              const float gate = 1.f / (1.f + expf(-sg));
+              y = fmaf(gate, __ldcg(a.part + ((long long)r * TS + a.T) * a.H + n), y);
+            }
+            store_out(a.y, a.dtype, (long long)r * a.H + n, y);
+          }
+        }
+        named_bar(1, kConsumerWarps * 32);
+      }
+    }
+  }
+}
+
+// ================================================================ launchers
+
+template <int NT>
+static size_t dense_smem() { return Q4Layout<NT>::BASE_BYTES + 1024; }
+template <int NT>
+static size_t moe_smem() { return Q4Layout<NT>::BASE_BYTES + sizeof(RouteSmem) + 1024; }
+
+cudaError_t q4_setup_kernels() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(q4_dense_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dense_smem<1>()))) return e;
+  if ((e = cudaFuncSetAttribute(q4_dense_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dense_smem<2>()))) return e;
+  if ((e = cudaFuncSetAttribute(moe_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)moe_smem<1>()))) return e;
+  if ((e = cudaFuncSetAttribute(moe_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)moe_smem<2>()))) return e;
+  if ((e = cudaFuncSetAttribute(moe_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)moe_smem<1>()))) return e;
+  if ((e = cudaFuncSetAttribute(moe_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)moe_smem<2>()))) return e;
+  return cudaSuccess;
+}
+
+cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, cudaStream_t s) {
+  if (nt == 1) q4_dense_kernel<1><<<a.G, kQ4Threads, dense_smem<1>(), s>>>(wmap, a);
+  else q4_dense_kernel<2><<<a.G, kQ4Threads, dense_smem<2>(), s>>>(wmap, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, const CUtensorMap& sgu_map,
+                       const CUtensorMap& sdn_map, const MoeArgs& a, int nt, cudaStream_t s, int* launches) {
+  if (nt == 1) moe_kernel<1, true><<<a.G, kQ4Threads, moe_smem<1>(), s>>>(gu_map, sgu_map, a);
+  else moe_kernel<2, true><<<a.G, kQ4Threads, moe_smem<2>(), s>>>(gu_map, sgu_map, a);
+  cudaError_t e = cudaGetLastError();
+  if (e) return e;
+  ++*launches;
+  if (nt == 1) moe_kernel<1, false><<<a.G, kQ4Threads, moe_smem<1>(), s>>>(dn_map, sdn_map, a);
+  else moe_kernel<2, false><<<a.G, kQ4Threads, moe_smem<2>(), s>>>(dn_map, sdn_map, a);
+  e = cudaGetLastError();
+  if (!e) ++*launches;
+  return e;
+}
+
+}  // namespace vk

@@ -1,0 +1,372 @@
+// verify_abi.cu - the C ABI declared in include/verify.h: context and scratch,
+// argument validation (all done before anything is launched), TMA
+// descriptors, launches on the caller's stream, GDN slot bookkeeping.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "verify.h"
+
+struct verify_ctx {
+  int device = 0;
+  int num_sms = 0;
+  float* dense_part = nullptr;
+  int* dense_cnt = nullptr;
+  uint16_t* moe_hbuf = nullptr;
+  float* moe_part = nullptr;
+  int* moe_cnt = nullptr;
+  int* err = nullptr;
+  int64_t launches = 0;
+  char msg[512] = {0};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+
+namespace {
+
+constexpr int kMaxN = 1 << 20;
+constexpr int kMaxKin = 1 << 17;
+constexpr int kMaxH = 8192;
+constexpr int kMaxI = 4096;
+constexpr int kDenseSlotFloats = vk::kConsumerWarps * 2 * 2 * 32 * 4;  // NT = 2
+constexpr size_t kHbufElems = (size_t)VERIFY_MAX_K * (vk::kMaxTopK + 1) * kMaxI;
+constexpr size_t kMoePartElems = (size_t)VERIFY_MAX_K * (vk::kMaxTopK + 1) * kMaxH;
+
+verify_status fail(verify_ctx* ctx, verify_status st, const char* fmt, const char* what = "") {
+  if (ctx) snprintf(ctx->msg, sizeof ctx->msg, fmt, what);
+  return st;
+}
+
+verify_status cuda_fail(verify_ctx* ctx, cudaError_t e, const char* where) {
+  if (ctx) snprintf(ctx->msg, sizeof ctx->msg, "%s: %s", where, cudaGetErrorString(e));
+  return VERIFY_ECUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// true if p is device (or managed) memory that this GPU can use
+bool is_device_ptr(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+verify_status check_dev(verify_ctx* ctx, const void* p, size_t align, const char* name) {
+  if (!p) return fail(ctx, VERIFY_EINVAL, "%s is NULL", name);
+  if (!aligned(p, align)) return fail(ctx, VERIFY_EINVAL, "%s is misaligned", name);
+  if (!is_device_ptr(p)) return fail(ctx, VERIFY_EINVAL, "%s is not device memory", name);
+  return VERIFY_OK;
+}
+
+verify_status use_device(verify_ctx* ctx) {
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e) return cuda_fail(ctx, e, "cudaGetDevice");
+  if (cur != ctx->device && (e = cudaSetDevice(ctx->device))) return cuda_fail(ctx, e, "cudaSetDevice");
+  return VERIFY_OK;
+}
+
+// Packed-weight TMA map: uint32 [rows, words], box 32 words x box_rows, 128B swizzle.
+verify_status make_wmap(verify_ctx* ctx, CUtensorMap* m, const void* base, uint64_t rows, uint64_t words,
+                        uint32_t box_rows) {
+  cuuint64_t dims[2] = {words, rows};
+  cuuint64_t strides[1] = {words * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = ctx->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(ctx->msg, sizeof ctx->msg, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return VERIFY_ECUDA;
+  }
+  return VERIFY_OK;
+}
+
+verify_status check_q4(verify_ctx* ctx, const verify_q4_weight* W, const char* name) {
+  if (!W) return fail(ctx, VERIFY_EINVAL, "%s is NULL", name);
+  if (W->group_size != 64 || W->bits != 4) return fail(ctx, VERIFY_EUNSUPPORTED, "%s: only 4-bit, group 64", name);
+  if (W->k_in % 128 != 0 || W->k_in < 256 || W->k_in > kMaxKin)
+    return fail(ctx, VERIFY_EUNSUPPORTED, "%s: k_in must be a multiple of 128 in [256, 131072]", name);
+  if (W->n_out < 1 || W->n_out > kMaxN) return fail(ctx, VERIFY_EUNSUPPORTED, "%s: n_out out of range", name);
+  verify_status s;
+  if ((s = check_dev(ctx, W->packed, 16, "packed"))) return s;
+  if ((s = check_dev(ctx, W->scales, 4, "scales"))) return s;
+  if ((s = check_dev(ctx, W->biases, 4, "biases"))) return s;
+  return VERIFY_OK;
+}
+
+verify_status check_dtype(verify_ctx* ctx, int dtype, bool allow_add) {
+  if (dtype == VERIFY_F32 || dtype == VERIFY_BF16 || (allow_add && dtype == VERIFY_F32_ADD)) return VERIFY_OK;
+  return fail(ctx, VERIFY_EINVAL, "unsupported dtype_out%s", "");
+}
+
+}  // namespace
+
+extern "C" {
+
+verify_status verify_init(int device, verify_ctx** out) {
+  if (!out) return VERIFY_EINVAL;
+  *out = nullptr;
+  cudaError_t e = cudaSetDevice(device);
+  if (e) return VERIFY_ECUDA;
+  verify_ctx* ctx = new verify_ctx();
+  ctx->device = device;
+  auto bail = [&](cudaError_t err) {
+    verify_destroy(ctx);
+    (void)err;
+    return VERIFY_ECUDA;
+  };
+  if ((e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device))) return bail(e);
+  const size_t dense_part = (size_t)2 * vk::kQ4CtasPerSm * ctx->num_sms * kDenseSlotFloats * sizeof(float);
+  const size_t dense_cnt = (size_t)(kMaxN / vk::kBM) * sizeof(int);
+  if ((e = cudaMalloc(&ctx->dense_part, dense_part))) return bail(e);
+  if ((e = cudaMalloc(&ctx->dense_cnt, dense_cnt))) return bail(e);
+  if ((e = cudaMalloc(&ctx->moe_hbuf, kHbufElems * sizeof(uint16_t)))) return bail(e);
+  if ((e = cudaMalloc(&ctx->moe_part, kMoePartElems * sizeof(float)))) return bail(e);
+  if ((e = cudaMalloc(&ctx->moe_cnt, (kMaxH / vk::kBM) * sizeof(int)))) return bail(e);
+  if ((e = cudaMalloc(&ctx->err, sizeof(int)))) return bail(e);
+  if ((e = cudaMemset(ctx->dense_cnt, 0, dense_cnt))) return bail(e);
+  if ((e = cudaMemset(ctx->moe_cnt, 0, (kMaxH / vk::kBM) * sizeof(int)))) return bail(e);
+  if ((e = cudaMemset(ctx->err, 0, sizeof(int)))) return bail(e);
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if ((e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q)) ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return bail(e);
+  ctx->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  if ((e = vk::q4_setup_kernels())) return bail(e);
+  if ((e = vk::gdn_setup_kernels())) return bail(e);
+  if ((e = cudaDeviceSynchronize())) return bail(e);
+  *out = ctx;
+  return VERIFY_OK;
+}
+
+verify_status verify_destroy(verify_ctx* ctx) {
+  if (!ctx) return VERIFY_EINVAL;
+  cudaSetDevice(ctx->device);
+  cudaDeviceSynchronize();
+  cudaFree(ctx->dense_part);
+  cudaFree(ctx->dense_cnt);
+  cudaFree(ctx->moe_hbuf);
+  cudaFree(ctx->moe_part);
+  cudaFree(ctx->moe_cnt);
+  cudaFree(ctx->err);
+  delete ctx;
+  return VERIFY_OK;
+}
+
+const char* verify_last_error(const verify_ctx* ctx) { return ctx ? ctx->msg : "null context"; }
+
+int64_t verify_launch_count(const verify_ctx* ctx) { return ctx ? ctx->launches : -1; }
+
+verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, int32_t* code) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s = use_device(ctx);
+  if (s) return s;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+  int h = 0;
+  if ((e = cudaMemcpy(&h, ctx->err, sizeof(int), cudaMemcpyDeviceToHost))) return cuda_fail(ctx, e, "cudaMemcpy");
+  if (code) *code = h;
+  if (h == 0) return VERIFY_OK;
+  // an aborted kernel may have left arrival counters behind: reset the scratch state
+  cudaMemset(ctx->err, 0, sizeof(int));
+  cudaMemset(ctx->dense_cnt, 0, (size_t)(kMaxN / vk::kBM) * sizeof(int));
+  cudaMemset(ctx->moe_cnt, 0, (kMaxH / vk::kBM) * sizeof(int));
+  cudaDeviceSynchronize();
+  snprintf(ctx->msg, sizeof ctx->msg, "device error code %d", h);
+  return VERIFY_EDEVICE;
+}
+
+verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W, const uint16_t* x, int k, void* y,
+                       int dtype_out, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if ((s = check_q4(ctx, W, "W"))) return s;
+  if ((s = check_dtype(ctx, dtype_out, true))) return s;
+  if ((s = check_dev(ctx, x, 16, "x"))) return s;
+  if ((s = check_dev(ctx, y, dtype_out == VERIFY_BF16 ? 2 : 4, "y"))) return s;
+
+  vk::DenseArgs a{};
+  a.scales = W->scales; a.biases = W->biases; a.x = x; a.y = y;
+  a.part = ctx->dense_part; a.cnt = ctx->dense_cnt; a.err = ctx->err;
+  a.N = W->n_out; a.K = W->k_in; a.k = k; a.dtype = dtype_out;
+  a.KG = a.K / 64; a.KC = (a.KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
+  a.RB = (a.N + vk::kBM - 1) / vk::kBM;
+  a.U = (long long)a.RB * a.KC;
+  const long long gmax = (long long)vk::kQ4CtasPerSm * ctx->num_sms;
+  a.G = (int)(a.U < gmax ? a.U : gmax);
+  CUtensorMap map;
+  if ((s = make_wmap(ctx, &map, W->packed, (uint64_t)a.N, (uint64_t)a.K / 8, vk::kBM))) return s;
+  cudaError_t e = vk::launch_q4_dense(map, a, k <= 8 ? 1 : 2, stream);
+  if (e) return cuda_fail(ctx, e, "q4_qmv_k launch");
+  ctx->launches += 1;
+  return VERIFY_OK;
+}
+
+verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate_up, const verify_q4_experts* down,
+                                  const float* logits, int64_t logits_ld, int top_k, const uint16_t* x, int k,
+                                  int32_t* idx_out, float* w_out, void* y, int dtype_out,
+                                  const verify_q4_weight* shared_gate_up, const verify_q4_weight* shared_down,
+                                  const float* shared_gate_logit, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (!gate_up || !down) return fail(ctx, VERIFY_EINVAL, "expert stacks are NULL%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  const int E = gate_up->n_experts;
+  if (E < 1 || E > vk::kMaxExperts || down->n_experts != E)
+    return fail(ctx, VERIFY_EUNSUPPORTED, "n_experts must match and be in 1..512%s");
+  if (top_k < 1 || top_k > vk::kMaxTopK || top_k > E) return fail(ctx, VERIFY_EUNSUPPORTED, "top_k out of range%s");
+  if ((s = check_q4(ctx, &gate_up->w, "gate_up"))) return s;
+  if ((s = check_q4(ctx, &down->w, "down"))) return s;
+  const int H = gate_up->w.k_in, I = gate_up->w.n_out / 2;
+  if (gate_up->w.n_out != 2 * I || down->w.n_out != H || down->w.k_in != I)
+    return fail(ctx, VERIFY_EINVAL, "expert shapes must be gate_up [2I, H], down [H, I]%s");
+  if (H > kMaxH || I > kMaxI || I % 128 != 0)
+    return fail(ctx, VERIFY_EUNSUPPORTED, "H <= 8192, I <= 4096, multiples of 128%s");
+  if (logits_ld < E) return fail(ctx, VERIFY_EINVAL, "logits_ld < n_experts%s");
+  if ((s = check_dtype(ctx, dtype_out, true))) return s;
+  if ((s = check_dev(ctx, logits, 4, "logits"))) return s;
+  if ((s = check_dev(ctx, x, 16, "x"))) return s;
+  if ((s = check_dev(ctx, idx_out, 4, "idx_out"))) return s;
+  if ((s = check_dev(ctx, w_out, 4, "w_out"))) return s;
+  if ((s = check_dev(ctx, y, dtype_out == VERIFY_BF16 ? 2 : 4, "y"))) return s;
+  const int n_shared = (shared_gate_up != nullptr) + (shared_down != nullptr) + (shared_gate_logit != nullptr);
+  if (n_shared != 0 && n_shared != 3)
+    return fail(ctx, VERIFY_EINVAL, "shared expert: give all of gate_up, down and gate logit, or none%s");
+  if (n_shared == 3) {
+    if ((s = check_q4(ctx, shared_gate_up, "shared_gate_up"))) return s;
+    if ((s = check_q4(ctx, shared_down, "shared_down"))) return s;
+    if (shared_gate_up->n_out != 2 * I || shared_gate_up->k_in != H || shared_down->n_out != H ||
+        shared_down->k_in != I)
+      return fail(ctx, VERIFY_EINVAL, "shared expert shape differs from the routed experts%s");
+    if ((s = check_dev(ctx, shared_gate_logit, 4, "shared_gate_logit"))) return s;
+  }
+
+  CUtensorMap gu, dn, sgu, sdn;
+  if ((s = make_wmap(ctx, &gu, gate_up->w.packed, (uint64_t)E * 2 * I, (uint64_t)H / 8, 64))) return s;
+  if ((s = make_wmap(ctx, &dn, down->w.packed, (uint64_t)E * H, (uint64_t)I / 8, vk::kBM))) return s;
+  if (n_shared == 3) {
+    if ((s = make_wmap(ctx, &sgu, shared_gate_up->packed, (uint64_t)2 * I, (uint64_t)H / 8, 64))) return s;
+    if ((s = make_wmap(ctx, &sdn, shared_down->packed, (uint64_t)H, (uint64_t)I / 8, vk::kBM))) return s;
+  } else {
+    sgu = gu;
+    sdn = dn;
+  }
+  vk::MoeArgs a{};
+  a.logits = logits; a.logits_ld = logits_ld; a.shared_logit = n_shared ? shared_gate_logit : nullptr;
+  a.x = x;
+  a.gu_scales = gate_up->w.scales; a.gu_biases = gate_up->w.biases;
+  a.dn_scales = down->w.scales; a.dn_biases = down->w.biases;
+  if (n_shared) {
+    a.sgu_scales = shared_gate_up->scales; a.sgu_biases = shared_gate_up->biases;
+    a.sdn_scales = shared_down->scales; a.sdn_biases = shared_down->biases;
+  }
+  a.hbuf = ctx->moe_hbuf; a.part = ctx->moe_part; a.cnt = ctx->moe_cnt;
+  a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;
+  a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
+  a.has_shared = n_shared ? 1 : 0;
+  a.G = vk::kQ4CtasPerSm * ctx->num_sms;
+  int launched = 0;
+  cudaError_t e = vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, stream, &launched);
+  ctx->launches += launched;
+  if (e) return cuda_fail(ctx, e, "q4_gather_experts_k launch");
+  return VERIFY_OK;
+}
+
+verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p, verify_gdn_state* st,
+                           const verify_gdn_inputs* in, int k, void* o, int dtype_out, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (!p || !st || !in) return fail(ctx, VERIFY_EINVAL, "params, state or inputs is NULL%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if (p->n_qk_heads < 1 || p->n_v_heads < 1 || p->n_v_heads % p->n_qk_heads != 0)
+    return fail(ctx, VERIFY_EUNSUPPORTED, "n_v_heads must be a positive multiple of n_qk_heads%s");
+  if (p->head_dim_k != p->head_dim_v ||
+      (p->head_dim_k != 32 && p->head_dim_k != 64 && p->head_dim_k != 128))
+    return fail(ctx, VERIFY_EUNSUPPORTED, "head_dim_k == head_dim_v in {32, 64, 128}%s");
+  if (p->conv_kernel != 4) return fail(ctx, VERIFY_EUNSUPPORTED, "conv_kernel must be 4%s");
+  if (p->gate_act != 0 && p->gate_act != 1) return fail(ctx, VERIFY_EINVAL, "gate_act must be 0 or 1%s");
+  if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16) return fail(ctx, VERIFY_EINVAL, "dtype_out F32 or BF16%s");
+  if (st->n_slots < k + 1 || st->n_slots > VERIFY_GDN_MAX_SLOTS)
+    return fail(ctx, VERIFY_EINVAL, "n_slots must be in k+1..17%s");
+  if (st->cur < 0 || st->cur >= st->n_slots) return fail(ctx, VERIFY_EINVAL, "cur is not a slot%s");
+  const int d = p->head_dim_k, Hk = p->n_qk_heads, Hv = p->n_v_heads;
+  const int C = 2 * Hk * d + Hv * d;
+  if (in->ld_qkv < C || in->ld_z < (int64_t)Hv * d || in->ld_a < Hv || in->ld_b < Hv)
+    return fail(ctx, VERIFY_EINVAL, "an input row stride is smaller than its row%s");
+  if ((s = check_dev(ctx, p->conv_w, 4, "conv_w")) || (s = check_dev(ctx, p->A_log, 4, "A_log")) ||
+      (s = check_dev(ctx, p->dt_bias, 4, "dt_bias")) || (s = check_dev(ctx, p->norm_w, 4, "norm_w")) ||
+      (s = check_dev(ctx, in->qkv, 2, "qkv")) || (s = check_dev(ctx, in->z, 2, "z")) ||
+      (s = check_dev(ctx, in->a, 2, "a")) || (s = check_dev(ctx, in->b, 2, "b")) ||
+      (s = check_dev(ctx, o, dtype_out == VERIFY_BF16 ? 2 : 4, "o")))
+    return s;
+
+  int pending[VERIFY_GDN_MAX_SLOTS];
+  pending[0] = st->cur;
+  for (int sl = 0, r = 1; sl < st->n_slots && r <= k; ++sl)
+    if (sl != st->cur) pending[r++] = sl;
+  for (int r = 0; r <= k; ++r) {
+    if ((s = check_dev(ctx, st->S_slots[pending[r]], 16, "S slot"))) return s;
+    if ((s = check_dev(ctx, st->conv_slots[pending[r]], 2, "conv slot"))) return s;
+  }
+
+  vk::GdnArgs a{};
+  a.S_in = st->S_slots[st->cur];
+  a.tail_in = st->conv_slots[st->cur];
+  for (int r = 0; r < k; ++r) {
+    a.S_out[r] = st->S_slots[pending[r + 1]];
+    a.tail_out[r] = st->conv_slots[pending[r + 1]];
+  }
+  a.qkv = in->qkv; a.ld_qkv = in->ld_qkv; a.z = in->z; a.ld_z = in->ld_z;
+  a.a = in->a; a.ld_a = in->ld_a; a.b = in->b; a.ld_b = in->ld_b;
+  a.conv_w = p->conv_w; a.A_log = p->A_log; a.dt_bias = p->dt_bias; a.norm_w = p->norm_w;
+  a.o = o; a.err = ctx->err;
+  a.Hk = Hk; a.Hv = Hv; a.d = d; a.W = p->conv_kernel; a.k = k; a.dtype = dtype_out; a.gate_act = p->gate_act;
+  a.q_scale = p->q_scale; a.l2_eps = p->l2_eps; a.norm_eps = p->norm_eps;
+  cudaError_t e = vk::launch_gdn(a, stream);
+  if (e) return cuda_fail(ctx, e, "gdn_verify_k launch");
+  ctx->launches += 1;
+  for (int r = 0; r <= k; ++r) st->pending[r] = pending[r];
+  st->pending_k = k;
+  return VERIFY_OK;
+}
+
+verify_status gdn_commit(verify_gdn_state* st, int accepted) {
+  if (!st) return VERIFY_EINVAL;
+  if (st->pending_k <= 0) return VERIFY_EINVAL;
+  if (accepted < 0 || accepted > st->pending_k) return VERIFY_EINVAL;
+  st->cur = st->pending[accepted];
+  st->pending_k = 0;
+  return VERIFY_OK;
+}
+
+verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w, float eps, int zero_centered, int n,
+                               int k, void* out, int dtype_out, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (n < 4 || n > 16384 || n % 4 != 0) return fail(ctx, VERIFY_EUNSUPPORTED, "n must be a multiple of 4 in [4, 16384]%s");
+  if (k < 1 || k > 65535) return fail(ctx, VERIFY_EINVAL, "k out of range%s");
+  if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16) return fail(ctx, VERIFY_EINVAL, "dtype_out F32 or BF16%s");
+  if ((s = check_dev(ctx, x, 4, "x")) || (s = check_dev(ctx, w, 4, "w")) ||
+      (s = check_dev(ctx, out, dtype_out == VERIFY_BF16 ? 2 : 4, "out")))
+    return s;
+  cudaError_t e = vk::launch_rmsnorm(x, w, eps, zero_centered, n, k, out, dtype_out, stream);
+  if (e) return cuda_fail(ctx, e, "verify_rmsnorm_k launch");
+  ctx->launches += 1;
+  return VERIFY_OK;
+}
+
+}  // extern "C"

@@ -155,6 +155,18 @@ def q4_rows(seed: int, name: str, n_out: int, k_in: int, rows, expert: int = 0,
     return Q4Matrix(packed, scales, biases, len(rows), k_in)
 
 
+def q4_expert(seed: int, name: str, n_out: int, k_in: int, expert: int,
+              scale_range=SCALE_RANGE, bias_range=BIAS_RANGE) -> Q4Matrix:
+    """Re-draw one whole expert matrix of a q4_matrix(..., n_experts=E) stack."""
+    sp, ss, sb = q4_seeds(seed, name)
+    wpr, gpr = k_in // 8, k_in // 64
+    packed = packed_words(sp, n_out * wpr, start=expert * n_out * wpr)
+    scales = f32_to_bf16(uniform_f32(ss, n_out * gpr, *scale_range, start=expert * n_out * gpr))
+    biases = f32_to_bf16(uniform_f32(sb, n_out * gpr, *bias_range, start=expert * n_out * gpr))
+    return Q4Matrix(packed.reshape(n_out, wpr), scales.reshape(n_out, gpr), biases.reshape(n_out, gpr),
+                    n_out, k_in)
+
+
 def bf16_normal(seed: int, name: str, shape, mean=0.0, std=1.0) -> np.ndarray:
     n = int(np.prod(shape))
     return f32_to_bf16(normal_f32(tensor_seed(seed, name), n, mean, std)).reshape(shape)

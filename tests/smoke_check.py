@@ -1,0 +1,62 @@
+"""One small width-k verify through every entry point on cuda:0, checked
+against the CPU oracle (used by __graft_entry__.smoke)."""
+import numpy as np
+
+from oracle import oracle as O
+from speculative_decode_verification_gb300 import binding as B
+from speculative_decode_verification_gb300 import synth as S
+from tests.gpu_util import DevQ4, assert_close, dev, host
+
+
+def run():
+    import torch
+
+    assert torch.cuda.is_available(), "smoke needs cuda:0"
+    torch.cuda.set_device(0)
+    vf = B.Verify(0)
+    k = 4
+    # dense Q4 product (tiny workload)
+    m = S.q4_matrix(0, "tiny.q4", 512, 512)
+    x = S.bf16_normal(0, "smoke.x", (k, 512))
+    y = torch.zeros((k, 512), device="cuda")
+    vf.q4_qmv_k(DevQ4(m).struct, dev(x), k, y)
+    torch.cuda.synchronize()
+    assert_close(host(y), O.q4_qmv(m.packed, m.scales, m.biases, x), what="q4_qmv_k")
+    # routed experts
+    E, H, I, T = 16, 256, 256, 4
+    gu = S.q4_matrix(0, "smoke.gu", 2 * I, H, n_experts=E)
+    dn = S.q4_matrix(0, "smoke.dn", H, I, n_experts=E)
+    xm = S.bf16_normal(0, "smoke.xm", (k, H))
+    lg = S.f32_normal(0, "smoke.lg", (k, E))
+    idx = torch.zeros((k, T), dtype=torch.int32, device="cuda")
+    w = torch.zeros((k, T), device="cuda")
+    ym = torch.zeros((k, H), device="cuda")
+    vf.q4_gather_experts_k(DevQ4(gu).struct, DevQ4(dn).struct, dev(lg), E, T, dev(xm), k, idx, w, ym)
+    torch.cuda.synchronize()
+    oi, _, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases), lg, T, xm)
+    assert np.array_equal(host(idx), oi)
+    assert_close(host(ym), oy, what="q4_gather_experts_k")
+    # Gated DeltaNet verify + commit (tiny workload)
+    Hk = Hv = 2
+    d = 32
+    C = 2 * Hk * d + Hv * d
+    p = S.gdn_params(0, "gdn", Hk, Hv, d)
+    dp = {key: dev(v) for key, v in p.items()}
+    S0, t0 = S.gdn_initial_state(0, "gdn", Hk, Hv, d)
+    slots = [torch.zeros((Hv, d, d), device="cuda") for _ in range(k + 1)]
+    tails = [torch.zeros((3, C), dtype=torch.int16, device="cuda") for _ in range(k + 1)]
+    st = B.gdn_state(slots, tails)
+    inp = S.gdn_inputs(0, "smoke.gdn", k, Hk, Hv, d)
+    di = {key: dev(v) for key, v in inp.items()}
+    o = torch.zeros((k, Hv * d), device="cuda")
+    vf.gdn_verify_k(B.gdn_params(Hk, Hv, d, dp["conv_w"], dp["A_log"], dp["dt_bias"], dp["norm_w"]), st,
+                    B.gdn_inputs(di["qkv"], di["z"], di["a"], di["b"]), k, o)
+    vf.gdn_commit(st, 2)
+    torch.cuda.synchronize()
+    oo, oS, _ = O.gdn_verify(Hk, Hv, d, p, S0.astype(np.float64), t0, inp, k)
+    assert_close(host(o), oo, what="gdn_verify_k")
+    assert_close(host(slots[st.cur]), oS[1], what="gdn_commit state")
+    status, code = vf.device_status()
+    assert status == B.OK, f"device error word {code}"
+    vf.close()
+    print("smoke OK")

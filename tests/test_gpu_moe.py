@@ -1,0 +1,167 @@
+"""GPU parity of the routed experts (q4_gather_experts_k) against the CPU oracle.
+
+Pages: "Flash-Next optimization transfer to Ornith and Qwen 27B", section
+"Exact verification kernels" (gathered affine-Q4 experts, top-8 of 256,
+2048/512, fused gate/up, widths 2..9); "Red Lite dev45 - speculative decoding
+with the Qwen3-Next MTP block", "What it is" (all (expert,row) pairs in one
+dispatch, one tail); "QWEN38FLASH.md - Plan for supporting
+Qwen/Qwen3.8-Flash-Next", 2.3 (512 experts, 10 routed + 1 shared, 640).
+"""
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from speculative_decode_verification_gb300 import binding as B
+from speculative_decode_verification_gb300 import synth as S
+from tests.gpu_util import DevQ4, assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vf():
+    import torch
+
+    assert torch.cuda.is_available()
+    v = B.Verify(0)
+    yield v
+    st, code = v.device_status()
+    assert st == B.OK, f"device error word {code}"
+    v.close()
+
+
+def gather(vf, gu, dn, logits, T, x, k, H, shared=None, dtype=B.F32):
+    import torch
+
+    idx = torch.zeros((k, T), dtype=torch.int32, device="cuda")
+    w = torch.zeros((k, T), dtype=torch.float32, device="cuda")
+    y = torch.zeros((k, H), dtype=torch.float32 if dtype != B.BF16 else torch.int16, device="cuda")
+    E = logits.shape[1]
+    if shared is None:
+        vf.q4_gather_experts_k(gu.struct, dn.struct, logits, E, T, x, k, idx, w, y, dtype)
+    else:
+        sgu, sdn, sl = shared
+        vf.q4_gather_experts_k(gu.struct, dn.struct, logits, E, T, x, k, idx, w, y, dtype,
+                               sgu.struct, sdn.struct, sl)
+    torch.cuda.synchronize()
+    return host(idx), host(w), host(y)
+
+
+def moe_case(seed, E, H, I):
+    gu = S.q4_matrix(seed, "moe.gu", 2 * I, H, n_experts=E)
+    dn = S.q4_matrix(seed, "moe.dn", H, I, n_experts=E)
+    return gu, dn
+
+
+@pytest.mark.parametrize("k", [1, 2, 5, 9, 16])
+def test_small_moe_matches_oracle(vf, k):
+    E, H, I, T = 16, 256, 256, 4
+    gu, dn = moe_case(10, E, H, I)
+    x = S.bf16_normal(10, f"moe.x{k}", (k, H))
+    logits = S.f32_normal(10, f"moe.l{k}", (k, E))
+    oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
+                                     logits, T, x)
+    gi, gw, gy = gather(vf, DevQ4(gu), DevQ4(dn), dev(logits), T, dev(x), k, H)
+    assert np.array_equal(gi, oi)
+    np.testing.assert_allclose(gw, ow, rtol=1e-5, atol=1e-6)
+    assert_close(gy, oy, what=f"k={k}")
+
+
+def test_shared_expert_and_ragged_down(vf):
+    """640-wide intermediate (ragged last 256-column chunk), 10 routed + 1 shared."""
+    E, H, I, T, k = 24, 384, 640, 10, 9
+    gu, dn = moe_case(11, E, H, I)
+    sgu = S.q4_matrix(11, "moe.sgu", 2 * I, H)
+    sdn = S.q4_matrix(11, "moe.sdn", H, I)
+    x = S.bf16_normal(11, "moe.xs", (k, H))
+    logits = S.f32_normal(11, "moe.ls", (k, E))
+    sl = S.f32_normal(11, "moe.sl", (k,))
+    oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
+                                     logits, T, x, shared=((sgu.packed, sgu.scales, sgu.biases),
+                                                           (sdn.packed, sdn.scales, sdn.biases)),
+                                     shared_logit=sl)
+    # the shared gate logit is read at row stride logits_ld = E: store it in a [k, E] array
+    slm = np.zeros((k, E), np.float32)
+    slm[:, 0] = sl
+    gi, gw, gy = gather(vf, DevQ4(gu), DevQ4(dn), dev(logits), T, dev(x), k, H,
+                        shared=(DevQ4(sgu), DevQ4(sdn), dev(slm)))
+    assert np.array_equal(gi, oi)
+    assert_close(gy, oy, what="shared")
+
+
+def test_width_k_rows_bit_identical_to_width_1(vf):
+    E, H, I, T = 32, 512, 256, 8
+    gu, dn = moe_case(12, E, H, I)
+    G, D = DevQ4(gu), DevQ4(dn)
+    x = S.bf16_normal(12, "moe.xb", (9, H))
+    logits = S.f32_normal(12, "moe.lb", (9, E))
+    _, _, y9 = gather(vf, G, D, dev(logits), T, dev(x), 9, H)
+    for r in range(9):
+        _, _, y1 = gather(vf, G, D, dev(logits[r:r + 1]), T, dev(x[r:r + 1]), 1, H)
+        assert np.array_equal(y9[r].view(np.uint32), y1[0].view(np.uint32)), f"row {r}"
+
+
+def test_single_expert_reduces_to_dense_products(vf):
+    """T = 1, every row routed to one expert: the routed path equals the dense
+    gate/up product, SwiGLU in bf16 and the dense down product."""
+    import torch
+
+    E, H, I, k = 8, 256, 256, 4
+    gu, dn = moe_case(13, E, H, I)
+    logits = np.full((k, E), -2.0, np.float32)
+    logits[:, 5] = 3.0
+    x = S.bf16_normal(13, "moe.x1", (k, H))
+    gi, gw, gy = gather(vf, DevQ4(gu), DevQ4(dn), dev(logits), 1, dev(x), k, H)
+    assert np.all(gi == 5) and np.all(gw == 1.0)
+    Wg = DevQ4(S.Q4Matrix(gu.packed[5], gu.scales[5], gu.biases[5], 2 * I, H))
+    Wd = DevQ4(S.Q4Matrix(dn.packed[5], dn.scales[5], dn.biases[5], H, I))
+    g = torch.zeros((k, 2 * I), device="cuda")
+    vf.q4_qmv_k(Wg.struct, dev(x), k, g)
+    torch.cuda.synchronize()
+    gh = host(g).astype(np.float32)
+    gate, up = gh[:, :I], gh[:, I:]
+    h = S.f32_to_bf16((gate / (1.0 + np.exp(-gate))) * up)
+    yd = torch.zeros((k, H), device="cuda")
+    vf.q4_qmv_k(Wd.struct, dev(h), k, yd)
+    torch.cuda.synchronize()
+    assert_close(gy, host(yd), tol=1e-5, what="single expert")
+
+
+def test_ornith_shape_matches_oracle(vf):
+    """256 experts, H 2048, I 512, top-8, k = 2..9 (routes differ per row)."""
+    import torch
+
+    c = S.ORNITH_MOE
+    E, T, H, I = c["E"], c["T"], c["H"], c["I"]
+    seeds_gu, seeds_dn = S.q4_seeds(0, "ornith.gu"), S.q4_seeds(0, "ornith.dn")
+    gu_p = torch.empty((E, 2 * I, H // 8), dtype=torch.int32, device="cuda")
+    gu_s = torch.empty((E, 2 * I, H // 64), dtype=torch.int16, device="cuda")
+    gu_b = torch.empty_like(gu_s)
+    dn_p = torch.empty((E, H, I // 8), dtype=torch.int32, device="cuda")
+    dn_s = torch.empty((E, H, I // 64), dtype=torch.int16, device="cuda")
+    dn_b = torch.empty_like(dn_s)
+    vf.synth_q4(gu_p, gu_s, gu_b, seeds_gu, S.SCALE_RANGE, S.BIAS_RANGE)
+    vf.synth_q4(dn_p, dn_s, dn_b, seeds_dn, S.SCALE_RANGE, S.BIAS_RANGE)
+
+    class W:
+        pass
+
+    G, D = W(), W()
+    G.struct = B.q4_experts(gu_p, gu_s, gu_b)
+    D.struct = B.q4_experts(dn_p, dn_s, dn_b)
+    for k in (2, 9):
+        x = S.bf16_normal(0, f"ornith.x{k}", (k, H))
+        logits = S.f32_normal(0, f"ornith.l{k}", (k, E))
+        gi, gw, gy = gather(vf, G, D, dev(logits), T, dev(x), k, H)
+        oi, ow = O.route_topk(logits, T)
+        assert np.array_equal(gi, oi)
+        ref = np.zeros((k, H))
+        for r in range(k):
+            for j in range(T):
+                e = int(oi[r, j])
+                mg = S.q4_expert(0, "ornith.gu", 2 * I, H, e)
+                md = S.q4_expert(0, "ornith.dn", H, I, e)
+                gate_up = O.q4_qmv(mg.packed, mg.scales, mg.biases, x[r:r + 1])[0]
+                h = O.to_bf16(gate_up[:I] / (1.0 + np.exp(-gate_up[:I])) * gate_up[I:])
+                ref[r] += ow[r, j] * O.q4_qmv(md.packed, md.scales, md.biases, h[None, :])[0]
+        assert_close(gy, ref, what=f"ornith k={k}")
