@@ -53,6 +53,18 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   const int C = 2 * a.Hk * D + a.Hv * D;
   const bool owns_qk_tail = (h % (a.Hv / a.Hk)) == 0;
 
+  const int il = tid >> 3, l = tid & 7;
+  const int i = p * kGdnRows + il;  // value row within the head
+  float s[JPT];
+  {
+    const float* src = a.S_in + ((long long)h * D + i) * D;
+#pragma unroll
+    for (int m = 0; m < JPT / 4; ++m) {
+      const float4 v = *reinterpret_cast<const float4*>(src + 4 * l + 32 * m);
+      s[4 * m] = v.x; s[4 * m + 1] = v.y; s[4 * m + 2] = v.z; s[4 * m + 3] = v.w;
+    }
+  }
+
   // ---- 1. causal depthwise conv + SiLU for the q, k channels of QK head hq
   //         and the v channels of this CTA's value rows; slide the window.
   for (int cl = tid; cl < 2 * D + kGdnRows; cl += kGdnThreads) {
@@ -65,8 +77,13 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
 #pragma unroll
     for (int t = 0; t < 4; ++t) w[t] = a.conv_w[ch * 4 + t];
     uint16_t w0 = a.tail_in[ch], w1 = a.tail_in[C + ch], w2 = a.tail_in[2 * C + ch];
-    for (int r = 0; r < k; ++r) {
-      const uint16_t xr = a.qkv[r * a.ld_qkv + ch];
+    uint16_t xin[kGdnMaxK];
+#pragma unroll
+    for (int r = 0; r < kGdnMaxK; ++r) xin[r] = r < k ? a.qkv[r * a.ld_qkv + ch] : (uint16_t)0;
+#pragma unroll
+    for (int r = 0; r < kGdnMaxK; ++r) {
+      if (r >= k) break;
+      const uint16_t xr = xin[r];
       float acc = w[0] * bf16f(w0);
       acc = fmaf(w[1], bf16f(w1), acc);
       acc = fmaf(w[2], bf16f(w2), acc);
@@ -125,17 +142,6 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   __syncthreads();
 
   // ---- 3. delta rule over the k rows, state slice in registers
-  const int il = tid >> 3, l = tid & 7;
-  const int i = p * kGdnRows + il;  // value row within the head
-  float s[JPT];
-  {
-    const float* src = a.S_in + ((long long)h * D + i) * D;
-#pragma unroll
-    for (int m = 0; m < JPT / 4; ++m) {
-      const float4 v = *reinterpret_cast<const float4*>(src + 4 * l + 32 * m);
-      s[4 * m] = v.x; s[4 * m + 1] = v.y; s[4 * m + 2] = v.z; s[4 * m + 3] = v.w;
-    }
-  }
   for (int r = 0; r < k; ++r) {
     const float g = gs[r], beta = bs[r];
     float mk = 0.f, mq = 0.f;

@@ -11,25 +11,23 @@ namespace vk {
 constexpr int kBM = 128;           // weight rows per tile
 constexpr int kGroupsPerUnit = 4;  // 64-column groups per pipeline stage (256 columns)
 constexpr int kStages = 4;         // pipeline depth
-constexpr int kConsumerWarps = 4;  // each owns 32 weight rows (two 16-row MMA tiles)
-constexpr int kQ4Threads = (kConsumerWarps + 1) * 32;
+constexpr int kDenseWarps = 4;     // consumer warps of the dense kernel: two 16-row MMA tiles each
+constexpr int kGateUpWarps = 4;    // fused gate/up: a gate tile and its up tile per warp
+constexpr int kDownWarps = 4;      // routed down projection: two 16-row MMA tiles each
 constexpr int kQ4CtasPerSm = 2;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 
-// Dense stream-K product.
+// Dense product: RB row tiles x S K-splits, one cluster of S CTAs per tile.
 struct DenseArgs {
   const uint16_t* scales;
   const uint16_t* biases;
   const uint16_t* x;  // [k, K] bf16
   void* y;            // [k, N]
-  float* part;        // scratch: two partial tiles per CTA
-  int* cnt;           // scratch: one arrival counter per row tile, zero between calls
   int* err;
   int N, K, k, dtype;
   int KG, KC, RB;     // groups per row, 256-column chunks per row, 128-row tiles
-  long long U;        // units = RB * KC
-  int G;              // CTAs
+  int S;              // K-splits per tile (cluster size, 1..8)
 };
 
 // Routed experts.  Both kernels recompute the (cheap, deterministic) routing.
@@ -78,7 +76,7 @@ struct GdnArgs {
 };
 
 // Launchers (return the first CUDA error; *launches counts kernels launched).
-cudaError_t q4_setup_kernels();
+cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm);
 cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, cudaStream_t s);
 cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, const CUtensorMap& sgu_map,
                        const CUtensorMap& sdn_map, const MoeArgs& a, int nt, cudaStream_t s, int* launches);

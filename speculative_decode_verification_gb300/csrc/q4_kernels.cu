@@ -9,27 +9,31 @@
 // order; all (expert,row) pairs in one dispatch, one tail).
 //
 // Design (GB300, sm_103a):
-//  * One CTA = 1 producer warp + 4 consumer warps; 2 CTAs per SM.  The
+//  * A CTA is one producer warp plus four consumer warps, each owning two
+//    16-row MMA tiles of the 128-row tile; two CTAs per SM.  The
 //    producer streams 128-row x 256-column weight tiles with TMA (128-byte
-//    swizzle) into a 4-stage shared-memory ring, plus the tile's bf16 scales
-//    and biases and the activation rows with cp.async, all completing on one
-//    mbarrier per stage.  Each weight byte crosses HBM once per call.
+//    swizzle) into a 4-stage shared-memory ring, together with the tile's bf16
+//    scales and biases and the activation rows (cp.async, zero fill beyond the
+//    last row), all completing on one mbarrier per stage.  Each weight byte
+//    crosses HBM once per call.
 //  * Consumers decode each packed word once into bf16 code pairs (128 + q,
-//    exact) with one byte permute + one lop3 per pair and feed them to
+//    exact) with one shift and one lop3 per pair and feed them to
 //    mma.sync m16n8k16 as the A operand; the k activation rows are the N
-//    columns (8 per MMA, two MMA columns blocks for k > 8).  Per 64-column
-//    group the fp32 result C = sum (128+q) x is folded as
-//        acc += s*C + (b - 128 s) * sum(x)
-//    where sum(x) comes from one extra MMA with A = 1.  Products of integer
-//    codes with bf16 x are exact, accumulation is fp32.
+//    columns (8 per MMA; a second MMA column block for k > 8).  Per 64-column
+//    group the fp32 result C = sum (128 + q) x is folded as
+//        acc += s*C + (b - 128 s) * sum(x),
+//    the group sums sum(x) being added up once per stage by four consumer
+//    warps.  Products of the integer codes with bf16 x are exact; the
+//    accumulation is fp32.
 //  * Every output column is an independent dot product, the group order is
-//    fixed and the split of the K range across CTAs depends only on (N, K,
-//    SM count): row r of a width-k call is bit-identical to a width-1 call.
-//  * Dense: persistent stream-K grid; a row tile split across CTAs is
-//    reduced by the last CTA to arrive (an atomic counter, no waiting), in
-//    ascending K order.  Routed MoE: items = (distinct expert, row tile) with
-//    the full K per item; the down kernel's last arriver per 128 outputs does
-//    the fixed-order combine.
+//    fixed and the split of K across CTAs depends only on (N, K, SM count):
+//    row r of a width-k call is bit-identical to a width-1 call.
+//  * Dense: RB row tiles x S K-splits; the S CTAs of a tile form a thread
+//    block cluster and add their partial tiles through distributed shared
+//    memory in rank order (no global scratch, no atomics).
+//  * Routed MoE: items = (distinct expert, row tile) with the full K per item.
+//    The down kernel's last CTA to finish a 128-output block (an arrival
+//    counter, no waiting) combines the experts of every row in rank order.
 #include "common.cuh"
 #include "internal.h"
 
@@ -42,11 +46,19 @@ struct Q4Layout {
   static constexpr int X_BYTES = kGroupsPerUnit * NB * 128;  // [group][row][64 bf16]
   static constexpr int SB_BYTES = 2 * kBM * 8;               // scales then biases, 4 groups per row
   static constexpr int STAGE = W_BYTES + X_BYTES + SB_BYTES;
-  static constexpr int BAR_OFF = kStages * STAGE;
+  static constexpr int SX_BYTES = kGroupsPerUnit * NB * 4;   // fp32 group sums [group][row]
+  static constexpr int SX_OFF = kStages * STAGE;             // one slot per stage, after the stages
+  static constexpr int BAR_OFF = SX_OFF + kStages * SX_BYTES;
   static constexpr int MISC_OFF = BAR_OFF + 2 * kStages * 8;
-  static constexpr int MISC_BYTES = 64;
+  static constexpr int MISC_BYTES = 64 + 16 * 8;             // flags, then the producer's row-pointer table
   static constexpr int BASE_BYTES = MISC_OFF + MISC_BYTES;
   static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
+};
+
+template <int CW>
+struct Warps {
+  static constexpr int MT = kBM / 16 / CW;       // 16-row MMA tiles per consumer warp
+  static constexpr int THREADS = (CW + 1) * 32;  // + the producer warp
 };
 
 // Routing tables kept in shared memory by the MoE kernels.
@@ -58,14 +70,14 @@ struct RouteSmem {
   int U;
 };
 
-// One pipeline fill: what the producer needs to know about a tile.
+// What the producer needs to know about a tile.
 struct TileSrc {
   const CUtensorMap* map;
   int y0, y1;          // TMA row coordinate of the box(es)
   int two_boxes;       // 1: two 64-row boxes (gate rows, up rows); 0: one 128-row box
-  int row_limit;       // tile rows i with (row index within its matrix) >= limit are empty
+  int row_limit;       // tile rows whose row index within their matrix is >= limit are empty
   int mat_row0;        // matrix row of tile row 0 (for the limit test)
-  const uint16_t* scales;  // base of the scales/biases arrays addressed with global rows
+  const uint16_t* scales;  // scales/biases, addressed with the TMA row index
   const uint16_t* biases;
   int KG;
 };
@@ -77,6 +89,7 @@ __device__ __forceinline__ int tile_global_row(const TileSrc& t, int i) {
 
 // ---------------------------------------------------------------- producer
 
+// Fills one stage.  brow: the tile's activation row pointers (shared memory).
 template <int NT>
 __device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_bar, const TileSrc& t, int kc,
                                               int gcount, const uint16_t* const* brow, int nb, int lane) {
@@ -119,98 +132,158 @@ __device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_
   cp_async_mbar_arrive_noinc(full_bar);
 }
 
-// ---------------------------------------------------------------- consumer
-
-__device__ __forceinline__ uint32_t decode_pair(uint32_t v, uint32_t vs, uint32_t sel) {
-  // bf16x2 (128 + nibble 2b, 128 + nibble 2b+1) of byte b of v; vs = v >> 4
-  return and_or(prmt(v, vs, sel), 0x000F000Fu, 0x43004300u);
+// On abort the producer keeps the CTA alive until its TMA writes have landed.
+__device__ __forceinline__ void producer_drain(uint32_t bar_base, long long fills) {
+  for (long long f = (fills > kStages ? fills - kStages : 0); f < fills; ++f) {
+    const int s = (int)(f % kStages);
+    const uint32_t ph = (uint32_t)((f / kStages) & 1);
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar_base + 8 * s, ph) && clock64() - t0 < kWaitTimeoutCycles) {
+    }
+  }
 }
 
-// Accumulates one pipeline stage (gcount groups) into acc.  rbase[m] is the
-// tile row of M-tile m's first row for this warp.
-template <int NT>
-__device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, int gcount, const int (&rbase)[2], int lane,
-                                              float (&acc)[2][NT][4]) {
+// ---------------------------------------------------------------- consumer
+
+// Accumulates group G of a stage into acc for this warp's MT row tiles.
+template <int NT, int MT>
+__device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, uint32_t sx_src, int G,
+                                              const uint2 (&sw)[MT][2], const uint2 (&bw)[MT][2],
+                                              const int (&rbase)[MT], int lane, float (&acc)[MT][NT][4]) {
   using L = Q4Layout<NT>;
+  const int g = lane >> 2, c = lane & 3;
+  // B fragments: activation row 8t+g, columns 16c .. 16c+15 of the group
+  uint32_t bf[NT][8];
+  float sx[NT][2];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int b = 8 * t + g;
+    const uint32_t rowa = x_src + G * (L::NB * 128) + b * 128;
+    const uint4 xa = lds128(rowa + (((2 * c) ^ (b & 7)) << 4));
+    const uint4 xb = lds128(rowa + (((2 * c + 1) ^ (b & 7)) << 4));
+    bf[t][0] = xa.x; bf[t][1] = xa.y; bf[t][2] = xa.z; bf[t][3] = xa.w;
+    bf[t][4] = xb.x; bf[t][5] = xb.y; bf[t][6] = xb.z; bf[t][7] = xb.w;
+    const uint2 s2 = lds64(sx_src + (G * L::NB + 8 * t + 2 * c) * 4);  // sums of columns 2c, 2c+1
+    sx[t][0] = __uint_as_float(s2.x);
+    sx[t][1] = __uint_as_float(s2.y);
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    const int row = rbase[m] + g;
+    const uint32_t off = (uint32_t)((((2 * G + (c >> 1)) ^ (row & 7)) << 4) + ((c & 1) << 3));
+    const uint2 wa = lds64(w_src + row * 128 + off);        // words 2c, 2c+1 of row g
+    const uint2 wb = lds64(w_src + (row + 8) * 128 + off);  // same for row g+8
+    // Nibble pairs (p, p+4) of a word: lop3 of the word shifted by 4p bits
+    // with mask 0x000F000F and the bf16 exponent of 128 -> (128 + q_p, 128 + q_{p+4}).
+    // MMA j = 2*word + (p odd) takes pair p in k-slots (2c, 2c+1) and pair
+    // p+2 in k-slots (2c+8, 2c+9); the activation tile is stored in the
+    // matching order (see consume_stage).
+    uint32_t A[4][4];
+    {
+      const uint32_t v[4] = {wa.x, wb.x, wa.y, wb.y};  // row g word 2c, row g+8 word 2c, then word 2c+1
+      uint32_t q[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        q[i][0] = and_or(v[i], 0x000F000Fu, 0x43004300u);
+        q[i][1] = and_or(v[i] >> 4, 0x000F000Fu, 0x43004300u);
+        q[i][2] = and_or(v[i] >> 8, 0x000F000Fu, 0x43004300u);
+        q[i][3] = and_or(v[i] >> 12, 0x000F000Fu, 0x43004300u);
+      }
+#pragma unroll
+      for (int wd = 0; wd < 2; ++wd)
+#pragma unroll
+        for (int odd = 0; odd < 2; ++odd) {
+          const int j = 2 * wd + odd;
+          A[j][0] = q[2 * wd][odd];          // row g,   k-slots 2c, 2c+1
+          A[j][1] = q[2 * wd + 1][odd];      // row g+8
+          A[j][2] = q[2 * wd][odd + 2];      // row g,   k-slots 2c+8, 2c+9
+          A[j][3] = q[2 * wd + 1][odd + 2];  // row g+8
+        }
+    }
+    const uint32_t s_lo = (G & 2) ? sw[m][0].y : sw[m][0].x;
+    const uint32_t s_hi = (G & 2) ? sw[m][1].y : sw[m][1].x;
+    const uint32_t b_lo = (G & 2) ? bw[m][0].y : bw[m][0].x;
+    const uint32_t b_hi = (G & 2) ? bw[m][1].y : bw[m][1].x;
+    const float sA = (G & 1) ? bf16hi(s_lo) : bf16lo(s_lo);
+    const float sB = (G & 1) ? bf16hi(s_hi) : bf16lo(s_hi);
+    const float bA = fmaf(-128.f, sA, (G & 1) ? bf16hi(b_lo) : bf16lo(b_lo));
+    const float bB = fmaf(-128.f, sB, (G & 1) ? bf16hi(b_hi) : bf16lo(b_hi));
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float cg[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        mma_bf16_16816(cg, A[j][0], A[j][1], A[j][2], A[j][3], bf[t][2 * j], bf[t][2 * j + 1]);
+      acc[m][t][0] = fmaf(bA, sx[t][0], fmaf(sA, cg[0], acc[m][t][0]));
+      acc[m][t][1] = fmaf(bA, sx[t][1], fmaf(sA, cg[1], acc[m][t][1]));
+      acc[m][t][2] = fmaf(bB, sx[t][0], fmaf(sB, cg[2], acc[m][t][2]));
+      acc[m][t][3] = fmaf(bB, sx[t][1], fmaf(sB, cg[3], acc[m][t][3]));
+    }
+  }
+}
+
+// Accumulates one stage (gcount groups).  ok = false: the stage never filled
+// (abort) - keep the named-barrier count, skip the math.
+template <int NT, int CW>
+__device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t sx_src, int gcount,
+                                              const int (&rbase)[Warps<CW>::MT], int lane,
+                                              float (&acc)[Warps<CW>::MT][NT][4], bool ok) {
+  using L = Q4Layout<NT>;
+  constexpr int MT = Warps<CW>::MT;
   const uint32_t w_src = smem_addr(stage_ptr);
   const uint32_t x_src = w_src + L::W_BYTES;
   const uint32_t sb_src = x_src + L::X_BYTES;
   const int g = lane >> 2, c = lane & 3;
-  constexpr uint32_t ONE2 = 0x3F803F80u;  // bf16x2 (1, 1)
-
-  // scales / biases of this thread's four rows, four groups each
-  uint2 sw[2][2], bw[2][2];
+  const int w = threadIdx.x >> 5;
+  if (!ok) {
+    named_bar(2, CW * 32);
+    return;
+  }
+  // Consumer warp w < 4 prepares activation group w of the stage: the group
+  // sums (each thread its 16 values, then the four threads of a row) and, in
+  // place, the column order [0,4,2,6,1,5,3,7] within every 8-column block, the
+  // k-slot order of the decoded nibble pairs.
+  if (w < gcount) {
 #pragma unroll
-  for (int m = 0; m < 2; ++m)
+    for (int t = 0; t < NT; ++t) {
+      const int b = 8 * t + g;
+      const uint32_t rowa = x_src + w * (L::NB * 128) + b * 128;
+      const uint32_t ca = rowa + (((2 * c) ^ (b & 7)) << 4), cb = rowa + (((2 * c + 1) ^ (b & 7)) << 4);
+      const uint4 xa = lds128(ca);
+      const uint4 xb = lds128(cb);
+      float part = (bf16lo(xa.x) + bf16hi(xa.x)) + (bf16lo(xa.y) + bf16hi(xa.y));
+      part += (bf16lo(xa.z) + bf16hi(xa.z)) + (bf16lo(xa.w) + bf16hi(xa.w));
+      part += (bf16lo(xb.x) + bf16hi(xb.x)) + (bf16lo(xb.y) + bf16hi(xb.y));
+      part += (bf16lo(xb.z) + bf16hi(xb.z)) + (bf16lo(xb.w) + bf16hi(xb.w));
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (c == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(sx_src + (w * L::NB + b) * 4), "f"(part) : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ca), "r"(prmt(xa.x, xa.z, 0x5410)),
+                   "r"(prmt(xa.y, xa.w, 0x5410)), "r"(prmt(xa.x, xa.z, 0x7632)), "r"(prmt(xa.y, xa.w, 0x7632))
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cb), "r"(prmt(xb.x, xb.z, 0x5410)),
+                   "r"(prmt(xb.y, xb.w, 0x5410)), "r"(prmt(xb.x, xb.z, 0x7632)), "r"(prmt(xb.y, xb.w, 0x7632))
+                   : "memory");
+    }
+  }
+  // scales / biases of this thread's rows, four groups each
+  uint2 sw[MT][2], bw[MT][2];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = rbase[m] + g + 8 * h;
       sw[m][h] = lds64(sb_src + row * 8);
       bw[m][h] = lds64(sb_src + kBM * 8 + row * 8);
     }
-
+  named_bar(2, CW * 32);
+  if (gcount == kGroupsPerUnit) {
 #pragma unroll
-  for (int G = 0; G < kGroupsPerUnit; ++G) {
-    if (G >= gcount) break;
-    // B fragments: activation row 8t+g, columns 16c .. 16c+15 of the group
-    uint32_t bf[NT][8];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int b = 8 * t + g;
-      const uint32_t rowa = x_src + G * (L::NB * 128) + b * 128;
-      const uint4 xa = lds128(rowa + (((2 * c) ^ (b & 7)) << 4));
-      const uint4 xb = lds128(rowa + (((2 * c + 1) ^ (b & 7)) << 4));
-      bf[t][0] = xa.x; bf[t][1] = xa.y; bf[t][2] = xa.z; bf[t][3] = xa.w;
-      bf[t][4] = xb.x; bf[t][5] = xb.y; bf[t][6] = xb.z; bf[t][7] = xb.w;
-    }
-    // sum of the group's activations per column (A = 1)
-    float sx[NT][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      sx[t][0] = sx[t][1] = sx[t][2] = sx[t][3] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma_bf16_16816(sx[t], ONE2, ONE2, ONE2, ONE2, bf[t][2 * j], bf[t][2 * j + 1]);
-    }
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const int row = rbase[m] + g;
-      const uint32_t off = (uint32_t)((((2 * G + (c >> 1)) ^ (row & 7)) << 4) + ((c & 1) << 3));
-      const uint2 wa = lds64(w_src + row * 128 + off);        // words 2c, 2c+1 of row g
-      const uint2 wb = lds64(w_src + (row + 8) * 128 + off);  // same for row g+8
-      uint32_t A[4][4];
-      {
-        const uint32_t va0 = wa.x, va1 = wa.y, vb0 = wb.x, vb1 = wb.y;
-        const uint32_t sa0 = va0 >> 4, sa1 = va1 >> 4, sb0 = vb0 >> 4, sb1 = vb1 >> 4;
-        // MMA j = 2*word + half uses bytes 2*half (cols 2c,2c+1) and 2*half+1 (cols 2c+8,2c+9)
-        A[0][0] = decode_pair(va0, sa0, 0x0400); A[0][1] = decode_pair(vb0, sb0, 0x0400);
-        A[0][2] = decode_pair(va0, sa0, 0x0501); A[0][3] = decode_pair(vb0, sb0, 0x0501);
-        A[1][0] = decode_pair(va0, sa0, 0x0602); A[1][1] = decode_pair(vb0, sb0, 0x0602);
-        A[1][2] = decode_pair(va0, sa0, 0x0703); A[1][3] = decode_pair(vb0, sb0, 0x0703);
-        A[2][0] = decode_pair(va1, sa1, 0x0400); A[2][1] = decode_pair(vb1, sb1, 0x0400);
-        A[2][2] = decode_pair(va1, sa1, 0x0501); A[2][3] = decode_pair(vb1, sb1, 0x0501);
-        A[3][0] = decode_pair(va1, sa1, 0x0602); A[3][1] = decode_pair(vb1, sb1, 0x0602);
-        A[3][2] = decode_pair(va1, sa1, 0x0703); A[3][3] = decode_pair(vb1, sb1, 0x0703);
-      }
-      const uint32_t s_lo = (G & 2) ? sw[m][0].y : sw[m][0].x;
-      const uint32_t s_hi = (G & 2) ? sw[m][1].y : sw[m][1].x;
-      const uint32_t b_lo = (G & 2) ? bw[m][0].y : bw[m][0].x;
-      const uint32_t b_hi = (G & 2) ? bw[m][1].y : bw[m][1].x;
-      const float sA = (G & 1) ? bf16hi(s_lo) : bf16lo(s_lo);
-      const float sB = (G & 1) ? bf16hi(s_hi) : bf16lo(s_hi);
-      const float bA = fmaf(-128.f, sA, (G & 1) ? bf16hi(b_lo) : bf16lo(b_lo));
-      const float bB = fmaf(-128.f, sB, (G & 1) ? bf16hi(b_hi) : bf16lo(b_hi));
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        float cg[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16_16816(cg, A[j][0], A[j][1], A[j][2], A[j][3], bf[t][2 * j], bf[t][2 * j + 1]);
-        acc[m][t][0] = fmaf(bA, sx[t][0], fmaf(sA, cg[0], acc[m][t][0]));
-        acc[m][t][1] = fmaf(bA, sx[t][1], fmaf(sA, cg[1], acc[m][t][1]));
-        acc[m][t][2] = fmaf(bB, sx[t][2], fmaf(sB, cg[2], acc[m][t][2]));
-        acc[m][t][3] = fmaf(bB, sx[t][3], fmaf(sB, cg[3], acc[m][t][3]));
-      }
-    }
+    for (int G = 0; G < kGroupsPerUnit; ++G)
+      consume_group<NT, MT>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
+  } else {
+#pragma unroll 1
+    for (int G = 0; G < gcount; ++G) consume_group<NT, MT>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
   }
 }
 
@@ -224,185 +297,144 @@ __device__ __forceinline__ void store_out(void* y, int dtype, long long i, float
   }
 }
 
-template <int NT>
-__device__ __forceinline__ void zero_acc(float (&acc)[2][NT][4]) {
+template <int MT, int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[MT][NT][4]) {
 #pragma unroll
-  for (int m = 0; m < 2; ++m)
+  for (int m = 0; m < MT; ++m)
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[m][t][q] = 0.f;
 }
 
+template <int CW>
 __device__ __forceinline__ void init_barriers(uint32_t bar_base) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_base + 8 * s, 33);                        // full: producer lane 0 tx + 32 cp.async arrivals
-      mbar_init(bar_base + 8 * (kStages + s), kConsumerWarps);  // empty: one arrival per consumer warp
+      mbar_init(bar_base + 8 * s, 33);              // full: lane 0's tx arrival + 32 cp.async arrivals
+      mbar_init(bar_base + 8 * (kStages + s), CW);  // empty: one arrival per consumer warp
     }
     fence_mbar_init();
   }
 }
 
-// On abort the producer keeps the CTA alive until its TMA writes have landed.
-template <int NT>
-__device__ __forceinline__ void producer_drain(uint32_t bar_base, long long fills, volatile int* abort) {
-  for (long long f = (fills > kStages ? fills - kStages : 0); f < fills; ++f) {
-    const int s = (int)(f % kStages);
-    const uint32_t ph = (uint32_t)((f / kStages) & 1);
-    if (mbar_try_wait(bar_base + 8 * s, ph)) continue;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar_base + 8 * s, ph) && clock64() - t0 < kWaitTimeoutCycles) {
-    }
-  }
-  (void)abort;
-}
-
 // ================================================================== dense
 
-__device__ __forceinline__ int cta_of_unit(long long u, long long U, int G) {
-  return (int)(((u + 1) * (long long)G - 1) / U);
-}
-
+// Grid: RB row tiles x S K-splits; the S CTAs of a row tile form one thread
+// block cluster.  CTA s of tile rb accumulates the 256-column chunks
+// [s*KC/S, (s+1)*KC/S); the cluster adds the S partial tiles through
+// distributed shared memory in rank order, rank q finishing the consumer
+// warps w with w % S == q.  S depends only on (N, K, SM count), never on k.
 template <int NT>
-__global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
+__global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     q4_dense_kernel(const __grid_constant__ CUtensorMap wmap, const DenseArgs a) {
   using L = Q4Layout<NT>;
+  constexpr int CW = kDenseWarps, MT = Warps<CW>::MT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t bar_base = smem_addr(smem + L::BAR_OFF);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
-  volatile int* bcast = abort + 1;
-  if (threadIdx.x == 0) { *abort = 0; *bcast = 0; }
-  init_barriers(bar_base);
+  if (threadIdx.x == 0) *abort = 0;
+  init_barriers<CW>(bar_base);
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long u0 = (long long)blockIdx.x * a.U / a.G;
-  const long long u1 = (long long)(blockIdx.x + 1) * a.U / a.G;
+  const int S = a.S;
+  const int tile = blockIdx.x / S, split = blockIdx.x % S;
+  const int kc0 = split * a.KC / S, kc1 = (split + 1) * a.KC / S;
 
-  if (warp == kConsumerWarps) {
+  if (warp == CW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) tma_prefetch_desc(&wmap);
-    const uint16_t* brow[L::NB];
-#pragma unroll
-    for (int b = 0; b < L::NB; ++b) brow[b] = a.x + (long long)(b < a.k ? b : 0) * a.K;
+    const uint16_t** brow = reinterpret_cast<const uint16_t**>(smem + L::MISC_OFF + 64);
+    if (lane < L::NB) brow[lane] = a.x + (long long)(lane < a.k ? lane : 0) * a.K;
+    __syncwarp();
+    TileSrc ts;
+    ts.map = &wmap; ts.y0 = tile * kBM; ts.y1 = 0; ts.two_boxes = 0;
+    ts.row_limit = a.N; ts.mat_row0 = tile * kBM;
+    ts.scales = a.scales; ts.biases = a.biases; ts.KG = a.KG;
     long long fills = 0;
-    for (long long u = u0; u < u1; ++u, ++fills) {
+    for (int kc = kc0; kc < kc1; ++kc, ++fills) {
       const int s = (int)(fills % kStages);
       const uint32_t ph = (uint32_t)((fills / kStages) & 1);
       if (!mbar_wait(bar_base + 8 * (kStages + s), ph ^ 1, abort, a.err)) break;
-      const int tile = (int)(u / a.KC), kc = (int)(u % a.KC);
-      TileSrc ts;
-      ts.map = &wmap; ts.y0 = tile * kBM; ts.y1 = 0; ts.two_boxes = 0;
-      ts.row_limit = a.N; ts.mat_row0 = tile * kBM;
-      ts.scales = a.scales; ts.biases = a.biases; ts.KG = a.KG;
       const int gcount = min(kGroupsPerUnit, a.KG - 4 * kc);
       produce_stage<NT>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, gcount, brow, a.k, lane);
     }
-    if (*abort) producer_drain<NT>(bar_base, fills, abort);
+    if (*abort) producer_drain(bar_base, fills);
+    if (S > 1) {  // the producer warp takes part in the cluster barriers
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, c = lane & 3;
-  const int rbase[2] = {32 * warp, 32 * warp + 16};
-  float acc[2][NT][4];
-  zero_acc<NT>(acc);
+  int rbase[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) rbase[m] = 16 * (warp * MT + m);
+  float acc[MT][NT][4];
+  zero_acc<MT, NT>(acc);
   long long fills = 0;
-  int cur_tile = (int)(u0 / a.KC);
-  long long seg_start = u0;
-
-  auto flush = [&](int tile, long long s_begin, long long s_end) {
-    const long long tfirst = (long long)tile * a.KC, tlast = tfirst + a.KC - 1;
-    const int row0 = tile * kBM + 32 * warp;
-    if (s_begin == tfirst && s_end == tlast + 1) {
-      if (*abort) return;
+  for (int kc = kc0; kc < kc1; ++kc, ++fills) {
+    const int s = (int)(fills % kStages);
+    const uint32_t ph = (uint32_t)((fills / kStages) & 1);
+    const bool ok = mbar_wait(bar_base + 8 * s, ph, abort, a.err);
+    const int gcount = min(kGroupsPerUnit, a.KG - 4 * kc);
+    consume_stage<NT, CW>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase, lane,
+                          acc, ok);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
+  }
+  bool mine = true;  // does this CTA write this warp's outputs?
+  if (S > 1) {
+    // every stage has been consumed: stage 0 now holds this CTA's partial tile
+    float4* part = reinterpret_cast<float4*>(smem);
 #pragma unroll
-      for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
+      for (int t = 0; t < NT; ++t)
+        part[((warp * MT + m) * NT + t) * 32 + lane] = make_float4(acc[m][t][0], acc[m][t][1], acc[m][t][2], acc[m][t][3]);
+    cluster_sync();
+    mine = (warp % S) == split;
+    if (mine) {
+      zero_acc<MT, NT>(acc);
+      for (int q = 0; q < S; ++q) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int row = row0 + 16 * m + g + 8 * (q >> 1);
-            const int col = 8 * t + 2 * c + (q & 1);
-            if (row < a.N && col < a.k) store_out(a.y, a.dtype, (long long)col * a.N + row, acc[m][t][q]);
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const float4* src = part + ((warp * MT + m) * NT + t) * 32 + lane;
+            acc[m][t][0] += ld_dsmem_f32(&src->x, (uint32_t)q);
+            acc[m][t][1] += ld_dsmem_f32(&src->y, (uint32_t)q);
+            acc[m][t][2] += ld_dsmem_f32(&src->z, (uint32_t)q);
+            acc[m][t][3] += ld_dsmem_f32(&src->w, (uint32_t)q);
           }
-      return;
-    }
-    // partial tile: publish, count arrivals, the last arriver reduces in K order
-    constexpr int SLOT = kConsumerWarps * 2 * NT * 32 * 4;
-    const int slot = (s_begin == u0) ? 2 * blockIdx.x : 2 * blockIdx.x + 1;
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        float4* dst = reinterpret_cast<float4*>(a.part + (long long)slot * SLOT + (((warp * 2 + m) * NT + t) * 32 + lane) * 4);
-        *dst = make_float4(acc[m][t][0], acc[m][t][1], acc[m][t][2], acc[m][t][3]);
       }
-    __threadfence();
-    named_bar(1, kConsumerWarps * 32);
-    const int cfirst = cta_of_unit(tfirst, a.U, a.G), clast = cta_of_unit(tlast, a.U, a.G);
-    if (threadIdx.x == 0) {
-      int last = 0;
-      if (!*abort) {
-        const int old = atomicAdd(a.cnt + tile, 1);
-        last = (old == clast - cfirst);
-        if (last) atomicExch(a.cnt + tile, 0);
-      }
-      *bcast = last;
     }
-    named_bar(1, kConsumerWarps * 32);
-    if (!*bcast) return;
-    __threadfence();
-    float tot[2][NT][4];
-    zero_acc<NT>(tot);
-    for (int cc = cfirst; cc <= clast; ++cc) {
-      const long long cu0 = (long long)cc * a.U / a.G;
-      const int cslot = (cu0 >= tfirst) ? 2 * cc : 2 * cc + 1;
+  }
+  if (mine && !*abort) {
 #pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(
-              a.part + (long long)cslot * SLOT + (((warp * 2 + m) * NT + t) * 32 + lane) * 4));
-          tot[m][t][0] += v.x; tot[m][t][1] += v.y; tot[m][t][2] += v.z; tot[m][t][3] += v.w;
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
       for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int row = row0 + 16 * m + g + 8 * (q >> 1);
+          const int row = tile * kBM + rbase[m] + g + 8 * (q >> 1);
           const int col = 8 * t + 2 * c + (q & 1);
-          if (row < a.N && col < a.k) store_out(a.y, a.dtype, (long long)col * a.N + row, tot[m][t][q]);
+          if (row < a.N && col < a.k) store_out(a.y, a.dtype, (long long)col * a.N + row, acc[m][t][q]);
         }
-  };
-
-  for (long long u = u0; u < u1; ++u, ++fills) {
-    const int tile = (int)(u / a.KC), kc = (int)(u % a.KC);
-    if (tile != cur_tile) {
-      flush(cur_tile, seg_start, u);
-      zero_acc<NT>(acc);
-      cur_tile = tile;
-      seg_start = u;
-    }
-    const int s = (int)(fills % kStages);
-    const uint32_t ph = (uint32_t)((fills / kStages) & 1);
-    if (mbar_wait(bar_base + 8 * s, ph, abort, a.err)) {
-      const int gcount = min(kGroupsPerUnit, a.KG - 4 * kc);
-      consume_stage<NT>(smem + s * L::STAGE, gcount, rbase, lane, acc);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
   }
-  flush(cur_tile, seg_start, u1);
+  if (S > 1) cluster_sync();  // peers keep their shared memory until every rank has read it
 }
 
 // ================================================================== MoE
 
+// Top-T routing of every row, recomputed by each CTA (cheap and
+// deterministic): descending logit, equal logits -> lower index; weights =
+// softmax over the T selected logits (fp32).  Then the distinct selected
+// experts in ascending order and, per expert, the bitmask of rows.
 __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
@@ -465,8 +497,7 @@ __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
 
 // Row r and rank j of the b-th (ascending row) pair routed to expert slot u.
 __device__ __forceinline__ void pair_of(const RouteSmem* rs, const MoeArgs& a, int u, int b, int& r, int& j) {
-  const int U = rs->U;
-  if (u >= U) {  // shared expert: every row, slot T
+  if (u >= rs->U) {  // shared expert: every row, slot T
     r = b;
     j = a.T;
     return;
@@ -484,10 +515,16 @@ __device__ __forceinline__ int pairs_of(const RouteSmem* rs, const MoeArgs& a, i
   return u >= rs->U ? a.k : __popc(rs->mask[rs->ulist[u]]);
 }
 
+// GATEUP: items (expert, 64 rows of I): gate rows and up rows of the same i
+// go to the same warp (its two MMA tiles), the epilogue applies SwiGLU and
+// writes h (bf16).  Down: items (expert, 128 rows of H); partial outputs per
+// (row, rank) go to scratch and the last CTA of a 128-row block combines them.
 template <int NT, bool GATEUP>
-__global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
+__global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS, kQ4CtasPerSm)
     moe_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap smap, const MoeArgs a) {
   using L = Q4Layout<NT>;
+  constexpr int CW = GATEUP ? kGateUpWarps : kDownWarps, MT = Warps<CW>::MT;
+  static_assert(!GATEUP || MT == 2, "gate/up pairs the gate and up row tiles in one warp");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t bar_base = smem_addr(smem + L::BAR_OFF);
@@ -495,8 +532,8 @@ __global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
   volatile int* bcast = abort + 1;
   RouteSmem* rs = reinterpret_cast<RouteSmem*>(smem + L::BASE_BYTES);
   if (threadIdx.x == 0) { *abort = 0; *bcast = 0; }
-  init_barriers(bar_base);
-  route_rows(a, rs);  // contains __syncthreads
+  init_barriers<CW>(bar_base);
+  route_rows(a, rs);  // ends with __syncthreads
 
   const int TS = a.T + a.has_shared;
   if (GATEUP && blockIdx.x == 0) {
@@ -512,22 +549,23 @@ __global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
   const int KG = K / 64, KC = (KG + kGroupsPerUnit - 1) / kGroupsPerUnit;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (warp == kConsumerWarps) {
+  if (warp == CW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) { tma_prefetch_desc(&map); if (a.has_shared) tma_prefetch_desc(&smap); }
+    const uint16_t** brow = reinterpret_cast<const uint16_t**>(smem + L::MISC_OFF + 64);
     long long fills = 0;
     for (int item = blockIdx.x; item < n_items && !*abort; item += a.G) {
       const int u = item / ntiles, tile = item % ntiles;
       const bool shared = u >= rs->U;
       const int e = shared ? 0 : rs->ulist[u];
       const int nb = pairs_of(rs, a, u);
-      const uint16_t* brow[L::NB];
-#pragma unroll
-      for (int b = 0; b < L::NB; ++b) {
+      __syncwarp();
+      if (lane < L::NB) {
         int r = 0, j = 0;
-        if (b < nb) pair_of(rs, a, u, b, r, j);
-        brow[b] = GATEUP ? a.x + (long long)r * a.H : a.hbuf + ((long long)r * TS + j) * a.I;
+        if (lane < nb) pair_of(rs, a, u, lane, r, j);
+        brow[lane] = GATEUP ? a.x + (long long)r * a.H : a.hbuf + ((long long)r * TS + j) * a.I;
       }
+      __syncwarp();
       TileSrc ts;
       ts.map = shared ? &smap : &map;
       ts.KG = KG;
@@ -554,28 +592,31 @@ __global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
         produce_stage<NT>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, gcount, brow, nb, lane);
       }
     }
-    if (*abort) producer_drain<NT>(bar_base, fills, abort);
+    if (*abort) producer_drain(bar_base, fills);
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, c = lane & 3;
-  int rbase[2];
-  if (GATEUP) { rbase[0] = 16 * warp; rbase[1] = 64 + 16 * warp; }
-  else { rbase[0] = 32 * warp; rbase[1] = 32 * warp + 16; }
+  int rbase[MT];
+  if (GATEUP) { rbase[0] = 16 * warp; rbase[MT - 1] = 64 + 16 * warp; }
+  else {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) rbase[m] = 16 * (warp * MT + m);
+  }
   long long fills = 0;
   for (int item = blockIdx.x; item < n_items; item += a.G) {
     const int u = item / ntiles, tile = item % ntiles;
     const int nb = pairs_of(rs, a, u);
-    float acc[2][NT][4];
-    zero_acc<NT>(acc);
+    float acc[MT][NT][4];
+    zero_acc<MT, NT>(acc);
     for (int kc = 0; kc < KC; ++kc, ++fills) {
       const int s = (int)(fills % kStages);
       const uint32_t ph = (uint32_t)((fills / kStages) & 1);
-      if (mbar_wait(bar_base + 8 * s, ph, abort, a.err)) {
-        const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
-        consume_stage<NT>(smem + s * L::STAGE, gcount, rbase, lane, acc);
-      }
+      const bool ok = mbar_wait(bar_base + 8 * s, ph, abort, a.err);
+      const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
+      consume_stage<NT, CW>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
+                            lane, acc, ok);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
     }
@@ -599,23 +640,23 @@ __global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
           const long long p = pid[t][q & 1];
           if (p < 0) continue;
           const int i = 64 * tile + 16 * warp + g + 8 * (q >> 1);
-          const float gate = acc[0][t][q], up = acc[1][t][q];
+          const float gate = acc[0][t][q], up = acc[MT - 1][t][q];
           const float h = gate / (1.f + expf(-gate)) * up;
           a.hbuf[p * a.I + i] = f2bf16(h);
         }
     } else {
 #pragma unroll
-      for (int m = 0; m < 2; ++m)
+      for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const long long p = pid[t][q & 1];
-            const int n = kBM * tile + 32 * warp + 16 * m + g + 8 * (q >> 1);
+            const int n = kBM * tile + rbase[m] + g + 8 * (q >> 1);
             if (p >= 0 && n < a.H) a.part[p * a.H + n] = acc[m][t][q];
           }
       __threadfence();
-      named_bar(1, kConsumerWarps * 32);
+      named_bar(1, CW * 32);
       if (threadIdx.x == 0) {
         int last = 0;
         if (!*abort) {
@@ -625,11 +666,11 @@ __global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
         }
         *bcast = last;
       }
-      named_bar(1, kConsumerWarps * 32);
+      named_bar(1, CW * 32);
       if (*bcast) {
         __threadfence();
         const int n = kBM * tile + threadIdx.x;
-        if (n < a.H) {
+        if (threadIdx.x < kBM && n < a.H) {
           for (int r = 0; r < a.k; ++r) {
             float y = 0.f;
             for (int j = 0; j < a.T; ++j)
@@ -642,7 +683,7 @@ __global__ void __launch_bounds__(kQ4Threads, kQ4CtasPerSm)
             store_out(a.y, a.dtype, (long long)r * a.H + n, y);
           }
         }
-        named_bar(1, kConsumerWarps * 32);
+        named_bar(1, CW * 32);
       }
     }
   }
@@ -655,32 +696,65 @@ static size_t dense_smem() { return Q4Layout<NT>::BASE_BYTES + 1024; }
 template <int NT>
 static size_t moe_smem() { return Q4Layout<NT>::BASE_BYTES + sizeof(RouteSmem) + 1024; }
 
-cudaError_t q4_setup_kernels() {
+template <typename F>
+static cudaError_t setup_one(F* kernel, int threads, size_t smem, int* ctas_per_sm) {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(q4_dense_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dense_smem<1>()))) return e;
-  if ((e = cudaFuncSetAttribute(q4_dense_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dense_smem<2>()))) return e;
-  if ((e = cudaFuncSetAttribute(moe_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)moe_smem<1>()))) return e;
-  if ((e = cudaFuncSetAttribute(moe_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)moe_smem<2>()))) return e;
-  if ((e = cudaFuncSetAttribute(moe_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)moe_smem<1>()))) return e;
-  if ((e = cudaFuncSetAttribute(moe_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)moe_smem<2>()))) return e;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) return e;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared)))
+    return e;
+  int n = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem))) return e;
+  *ctas_per_sm = n < *ctas_per_sm ? n : *ctas_per_sm;
+  return cudaSuccess;
+}
+
+// Sets the launch attributes of every Q4 kernel and reports how many CTAs of
+// the dense and of the MoE kernels fit on one SM (the minimum over the two
+// tile widths, so that the grid - and with it the split of K across CTAs -
+// does not depend on k).
+cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm) {
+  cudaError_t e;
+  constexpr int TD = Warps<kDenseWarps>::THREADS, TG = Warps<kGateUpWarps>::THREADS, TDN = Warps<kDownWarps>::THREADS;
+  *dense_ctas_per_sm = kQ4CtasPerSm;
+  *moe_ctas_per_sm = kQ4CtasPerSm;
+  if ((e = setup_one(q4_dense_kernel<1>, TD, dense_smem<1>(), dense_ctas_per_sm))) return e;
+  if ((e = setup_one(q4_dense_kernel<2>, TD, dense_smem<2>(), dense_ctas_per_sm))) return e;
+  if ((e = setup_one(moe_kernel<1, true>, TG, moe_smem<1>(), moe_ctas_per_sm))) return e;
+  if ((e = setup_one(moe_kernel<2, true>, TG, moe_smem<2>(), moe_ctas_per_sm))) return e;
+  if ((e = setup_one(moe_kernel<1, false>, TDN, moe_smem<1>(), moe_ctas_per_sm))) return e;
+  if ((e = setup_one(moe_kernel<2, false>, TDN, moe_smem<2>(), moe_ctas_per_sm))) return e;
+  if (*dense_ctas_per_sm < 1 || *moe_ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 
 cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, cudaStream_t s) {
-  if (nt == 1) q4_dense_kernel<1><<<a.G, kQ4Threads, dense_smem<1>(), s>>>(wmap, a);
-  else q4_dense_kernel<2><<<a.G, kQ4Threads, dense_smem<2>(), s>>>(wmap, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.RB * a.S);
+  cfg.blockDim = dim3(Warps<kDenseWarps>::THREADS);
+  cfg.dynamicSmemBytes = nt == 1 ? dense_smem<1>() : dense_smem<2>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (nt == 1) return cudaLaunchKernelEx(&cfg, q4_dense_kernel<1>, wmap, a);
+  return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2>, wmap, a);
 }
 
 cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, const CUtensorMap& sgu_map,
                        const CUtensorMap& sdn_map, const MoeArgs& a, int nt, cudaStream_t s, int* launches) {
-  if (nt == 1) moe_kernel<1, true><<<a.G, kQ4Threads, moe_smem<1>(), s>>>(gu_map, sgu_map, a);
-  else moe_kernel<2, true><<<a.G, kQ4Threads, moe_smem<2>(), s>>>(gu_map, sgu_map, a);
+  constexpr int TG = Warps<kGateUpWarps>::THREADS, TDN = Warps<kDownWarps>::THREADS;
+  if (nt == 1) moe_kernel<1, true><<<a.G, TG, moe_smem<1>(), s>>>(gu_map, sgu_map, a);
+  else moe_kernel<2, true><<<a.G, TG, moe_smem<2>(), s>>>(gu_map, sgu_map, a);
   cudaError_t e = cudaGetLastError();
   if (e) return e;
   ++*launches;
-  if (nt == 1) moe_kernel<1, false><<<a.G, kQ4Threads, moe_smem<1>(), s>>>(dn_map, sdn_map, a);
-  else moe_kernel<2, false><<<a.G, kQ4Threads, moe_smem<2>(), s>>>(dn_map, sdn_map, a);
+  if (nt == 1) moe_kernel<1, false><<<a.G, TDN, moe_smem<1>(), s>>>(dn_map, sdn_map, a);
+  else moe_kernel<2, false><<<a.G, TDN, moe_smem<2>(), s>>>(dn_map, sdn_map, a);
   e = cudaGetLastError();
   if (!e) ++*launches;
   return e;

@@ -13,8 +13,8 @@
 struct verify_ctx {
   int device = 0;
   int num_sms = 0;
-  float* dense_part = nullptr;
-  int* dense_cnt = nullptr;
+  int dense_ctas_per_sm = 0;
+  int moe_ctas_per_sm = 0;
   uint16_t* moe_hbuf = nullptr;
   float* moe_part = nullptr;
   int* moe_cnt = nullptr;
@@ -30,7 +30,6 @@ constexpr int kMaxN = 1 << 20;
 constexpr int kMaxKin = 1 << 17;
 constexpr int kMaxH = 8192;
 constexpr int kMaxI = 4096;
-constexpr int kDenseSlotFloats = vk::kConsumerWarps * 2 * 2 * 32 * 4;  // NT = 2
 constexpr size_t kHbufElems = (size_t)VERIFY_MAX_K * (vk::kMaxTopK + 1) * kMaxI;
 constexpr size_t kMoePartElems = (size_t)VERIFY_MAX_K * (vk::kMaxTopK + 1) * kMaxH;
 
@@ -102,6 +101,17 @@ verify_status check_q4(verify_ctx* ctx, const verify_q4_weight* W, const char* n
   return VERIFY_OK;
 }
 
+// K-splits per row tile: the largest power of two (at most 8, the portable
+// cluster size, and at most one split per 256-column chunk) whose grid still
+// fits the GPU's CTA slots in one wave.
+// Depends only on the matrix shape and the GPU.
+int dense_splits(const verify_ctx* ctx, int RB, int KC) {
+  const int slots = ctx->dense_ctas_per_sm * ctx->num_sms;
+  int S = 1;  // powers of two pack into the GPCs without leaving a partial second wave
+  while (2 * S <= 8 && 2 * S <= KC && RB * 2 * S <= slots) S *= 2;
+  return S;
+}
+
 verify_status check_dtype(verify_ctx* ctx, int dtype, bool allow_add) {
   if (dtype == VERIFY_F32 || dtype == VERIFY_BF16 || (allow_add && dtype == VERIFY_F32_ADD)) return VERIFY_OK;
   return fail(ctx, VERIFY_EINVAL, "unsupported dtype_out%s", "");
@@ -124,15 +134,10 @@ verify_status verify_init(int device, verify_ctx** out) {
     return VERIFY_ECUDA;
   };
   if ((e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device))) return bail(e);
-  const size_t dense_part = (size_t)2 * vk::kQ4CtasPerSm * ctx->num_sms * kDenseSlotFloats * sizeof(float);
-  const size_t dense_cnt = (size_t)(kMaxN / vk::kBM) * sizeof(int);
-  if ((e = cudaMalloc(&ctx->dense_part, dense_part))) return bail(e);
-  if ((e = cudaMalloc(&ctx->dense_cnt, dense_cnt))) return bail(e);
   if ((e = cudaMalloc(&ctx->moe_hbuf, kHbufElems * sizeof(uint16_t)))) return bail(e);
   if ((e = cudaMalloc(&ctx->moe_part, kMoePartElems * sizeof(float)))) return bail(e);
   if ((e = cudaMalloc(&ctx->moe_cnt, (kMaxH / vk::kBM) * sizeof(int)))) return bail(e);
   if ((e = cudaMalloc(&ctx->err, sizeof(int)))) return bail(e);
-  if ((e = cudaMemset(ctx->dense_cnt, 0, dense_cnt))) return bail(e);
   if ((e = cudaMemset(ctx->moe_cnt, 0, (kMaxH / vk::kBM) * sizeof(int)))) return bail(e);
   if ((e = cudaMemset(ctx->err, 0, sizeof(int)))) return bail(e);
   cudaDriverEntryPointQueryResult q;
@@ -141,7 +146,7 @@ verify_status verify_init(int device, verify_ctx** out) {
       q != cudaDriverEntryPointSuccess || !fn)
     return bail(e);
   ctx->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  if ((e = vk::q4_setup_kernels())) return bail(e);
+  if ((e = vk::q4_setup_kernels(&ctx->dense_ctas_per_sm, &ctx->moe_ctas_per_sm))) return bail(e);
   if ((e = vk::gdn_setup_kernels())) return bail(e);
   if ((e = cudaDeviceSynchronize())) return bail(e);
   *out = ctx;
@@ -152,8 +157,6 @@ verify_status verify_destroy(verify_ctx* ctx) {
   if (!ctx) return VERIFY_EINVAL;
   cudaSetDevice(ctx->device);
   cudaDeviceSynchronize();
-  cudaFree(ctx->dense_part);
-  cudaFree(ctx->dense_cnt);
   cudaFree(ctx->moe_hbuf);
   cudaFree(ctx->moe_part);
   cudaFree(ctx->moe_cnt);
@@ -178,7 +181,6 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
   if (h == 0) return VERIFY_OK;
   // an aborted kernel may have left arrival counters behind: reset the scratch state
   cudaMemset(ctx->err, 0, sizeof(int));
-  cudaMemset(ctx->dense_cnt, 0, (size_t)(kMaxN / vk::kBM) * sizeof(int));
   cudaMemset(ctx->moe_cnt, 0, (kMaxH / vk::kBM) * sizeof(int));
   cudaDeviceSynchronize();
   snprintf(ctx->msg, sizeof ctx->msg, "device error code %d", h);
@@ -197,14 +199,11 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W, const uint16_
   if ((s = check_dev(ctx, y, dtype_out == VERIFY_BF16 ? 2 : 4, "y"))) return s;
 
   vk::DenseArgs a{};
-  a.scales = W->scales; a.biases = W->biases; a.x = x; a.y = y;
-  a.part = ctx->dense_part; a.cnt = ctx->dense_cnt; a.err = ctx->err;
+  a.scales = W->scales; a.biases = W->biases; a.x = x; a.y = y; a.err = ctx->err;
   a.N = W->n_out; a.K = W->k_in; a.k = k; a.dtype = dtype_out;
   a.KG = a.K / 64; a.KC = (a.KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
   a.RB = (a.N + vk::kBM - 1) / vk::kBM;
-  a.U = (long long)a.RB * a.KC;
-  const long long gmax = (long long)vk::kQ4CtasPerSm * ctx->num_sms;
-  a.G = (int)(a.U < gmax ? a.U : gmax);
+  a.S = dense_splits(ctx, a.RB, a.KC);
   CUtensorMap map;
   if ((s = make_wmap(ctx, &map, W->packed, (uint64_t)a.N, (uint64_t)a.K / 8, vk::kBM))) return s;
   cudaError_t e = vk::launch_q4_dense(map, a, k <= 8 ? 1 : 2, stream);
@@ -276,7 +275,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
-  a.G = vk::kQ4CtasPerSm * ctx->num_sms;
+  a.G = ctx->moe_ctas_per_sm * ctx->num_sms;
   int launched = 0;
   cudaError_t e = vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, stream, &launched);
   ctx->launches += launched;
