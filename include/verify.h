@@ -300,6 +300,48 @@ verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w,
                                void* out, int dtype_out,
                                struct CUstream_st* stream);
 
+
+/* --------------------------------------------------------- a verify layer */
+
+/*
+ * One hybrid verify layer ([F] section 2: every layer is a Gated DeltaNet
+ * mixer followed by a MoE FFN; 2.3: 10 routed + 1 shared expert; 2.4:
+ * zero-centred norms), applied to the k-row residual stream h (fp32 [k, H],
+ * updated in place):
+ *   xn  = bf16(rmsnorm_zc(h, norm1_w))
+ *   p   = bf16(in_proj . xn)          rows: q|k|v (C), z (Hv*dv), a (Hv), b (Hv)
+ *   o   = gdn_verify_k(p...)           bf16; state slots advance as in gdn_verify_k
+ *   h  += out_proj . o
+ *   xn2 = bf16(rmsnorm_zc(h, norm2_w))
+ *   l   = router . xn2                 fp32 [k, E+1]: E routing logits, then the
+ *                                      shared expert's gate logit
+ *   h  += q4_gather_experts_k(gate_up, down, l[:, :E], top_k, xn2,
+ *                             shared_gate_up, shared_down, l[:, E])
+ * idx_out (optional, device int32 [k, top_k]) receives the routed expert
+ * indices.  Eight kernel launches on `stream`, no host synchronisation.  Scratch
+ * activations live in the context (limits: k <= 16, H <= 8192, in_proj rows
+ * <= 32768, E + 1 <= 1024).  Weight shapes must match: in_proj [C + Hv*dv +
+ * 2*Hv, H], out_proj [H, Hv*dv], router [E + 1, H], gate_up [E, 2I, H],
+ * down [E, H, I], shared_gate_up [2I, H], shared_down [H, I].
+ */
+typedef struct {
+  verify_q4_weight in_proj;
+  verify_q4_weight out_proj;
+  verify_q4_weight router;
+  verify_q4_experts gate_up;
+  verify_q4_experts down;
+  verify_q4_weight shared_gate_up;
+  verify_q4_weight shared_down;
+  verify_gdn_params gdn;
+  const float* norm1_w; /* [H], used as 1 + w */
+  const float* norm2_w; /* [H], used as 1 + w */
+  float norm_eps;
+  int32_t top_k;
+} verify_layer;
+
+verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_state* st, float* h, int k,
+                             int32_t* idx_out, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -175,3 +175,49 @@ def to_bf16(v) -> np.ndarray:
     v = np.asarray(v, np.float64)
     f = lib().oracle_round_bf16
     return np.array([f(float(t)) for t in v.ravel()], np.uint16).reshape(v.shape)
+
+
+def stack_layer(w, h, S0, tail0, k, Hk, Hv, d, T, eps=1e-6):
+    """One hybrid verify layer on the oracle, composed of the pinned pieces
+    above in the order the layer defines ("QWEN38FLASH.md - Plan for
+    supporting Qwen/Qwen3.8-Flash-Next", section 2: a Gated DeltaNet mixer,
+    then a MoE with 10 routed + 1 shared expert; 2.4: zero-centred norms):
+
+      xn = bf16(rmsnorm_zc(h));  p = bf16(in_proj . xn) = q|k|v, z, a, b
+      o = bf16(gdn_verify(p));   h += out_proj . o
+      xn2 = bf16(rmsnorm_zc(h)); l = fp32(router . xn2)   (E logits, then the shared gate)
+      h += routed experts (top-T of l[:, :E]) + sigmoid(l[:, E]) * shared(xn2)
+
+    READING: every activation that feeds a Q4 product is rounded to bf16 (the
+    products take BF16 rows, "Flash-Next optimization transfer to Ornith and
+    Qwen 27B", table "Shared architecture"), the residual stream h stays in
+    the accumulation precision, router logits are fp32 (the routing input).
+
+    w: provider with .in_proj/.out_proj/.router/.shared_gate_up/.shared_down
+    as (packed, scales, biases), .gdn (params dict), .norm1/.norm2 (fp32) and
+    .expert(e) -> ((gate_up packed, scales, biases), (down packed, scales, biases)).
+    h: float64 [k, H].  Returns (h_out, S_snap, tail_snap, idx, logits).
+    The routed sum uses only the selected experts: top-T of the full logits,
+    then the same gather on the compacted stack of the distinct selected
+    experts (same indices, weights and order as on the full stack).
+    """
+    H = h.shape[1]
+    C = 2 * Hk * d + Hv * d
+    Z = Hv * d
+    xn = to_bf16(rmsnorm(h, w.norm1, eps, True))
+    p = to_bf16(q4_qmv(*w.in_proj, xn))
+    inp = dict(qkv=p[:, :C], z=p[:, C:C + Z], a=p[:, C + Z:C + Z + Hv], b=p[:, C + Z + Hv:C + Z + 2 * Hv])
+    o, S_snap, tail_snap = gdn_verify(Hk, Hv, d, w.gdn, S0, tail0, inp, k)
+    h = h + q4_qmv(*w.out_proj, to_bf16(o))
+    xn2 = to_bf16(rmsnorm(h, w.norm2, eps, True))
+    lg = q4_qmv(*w.router, xn2).astype(np.float32)
+    E = lg.shape[1] - 1
+    idx, _ = route_topk(lg[:, :E], T)
+    U = np.unique(idx)
+    ex = [w.expert(int(e)) for e in U]
+    gu = tuple(np.stack([x[0][i] for x in ex]) for i in range(3))
+    dn = tuple(np.stack([x[1][i] for x in ex]) for i in range(3))
+    idx_c, _, y, _ = gather_experts(gu, dn, np.ascontiguousarray(lg[:, U]), T, xn2,
+                                    shared=(w.shared_gate_up, w.shared_down), shared_logit=lg[:, E])
+    assert np.array_equal(U[idx_c], idx)
+    return h + y, S_snap, tail_snap, idx, lg

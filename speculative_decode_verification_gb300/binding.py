@@ -55,6 +55,13 @@ class GdnInputs(C.Structure):
                 ("a", C.c_void_p), ("ld_a", C.c_int64), ("b", C.c_void_p), ("ld_b", C.c_int64)]
 
 
+class Layer(C.Structure):
+    _fields_ = [("in_proj", Q4Weight), ("out_proj", Q4Weight), ("router", Q4Weight), ("gate_up", Q4Experts),
+                ("down", Q4Experts), ("shared_gate_up", Q4Weight), ("shared_down", Q4Weight),
+                ("gdn", GdnParams), ("norm1_w", C.c_void_p), ("norm2_w", C.c_void_p), ("norm_eps", C.c_float),
+                ("top_k", C.c_int32)]
+
+
 def load():
     """Loads libverify.so (raises if it has not been built)."""
     global _lib
@@ -78,6 +85,7 @@ def load():
         "gdn_commit": [C.POINTER(GdnState), i],
         "verify_rmsnorm_k": [p, p, p, f, i, i, i, p, i, p],
         "verify_synth_q4": [p, p, p, p, i64, i64, C.c_uint64, C.c_uint64, C.c_uint64, f, f, f, f, p],
+        "verify_layer_k": [p, C.POINTER(Layer), C.POINTER(GdnState), p, i, p, p],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -175,6 +183,10 @@ class Verify:
                          dtype_out: int = BF16, stream=None):
         self._check(self.lib.verify_rmsnorm_k(self.ctx, _ptr(x), _ptr(w), eps, int(bool(zero_centered)), n, k,
                                               _ptr(out), dtype_out, self._stream(stream)))
+
+    def verify_layer_k(self, layer: Layer, state: GdnState, h, k: int, idx_out=None, stream=None):
+        self._check(self.lib.verify_layer_k(self.ctx, C.byref(layer), C.byref(state), _ptr(h), k,
+                                            _ptr(idx_out), self._stream(stream)))
 
     def synth_q4(self, packed, scales, biases, seeds, scale_range, bias_range, stream=None):
         self._check(self.lib.verify_synth_q4(self.ctx, _ptr(packed), _ptr(scales), _ptr(biases),

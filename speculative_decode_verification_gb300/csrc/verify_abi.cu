@@ -19,6 +19,12 @@ struct verify_ctx {
   float* moe_part = nullptr;
   int* moe_cnt = nullptr;
   int* err = nullptr;
+  uint16_t* st_xn = nullptr;   // layer scratch: bf16 [16, 8192]
+  uint16_t* st_proj = nullptr; // bf16 [16, 32768]
+  uint16_t* st_o = nullptr;    // bf16 [16, 32768]
+  float* st_logits = nullptr;  // fp32 [16, 1024]
+  int32_t* st_idx = nullptr;   // [16, 16]
+  float* st_w = nullptr;       // [16, 16]
   int64_t launches = 0;
   char msg[512] = {0};
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -30,6 +36,7 @@ constexpr int kMaxN = 1 << 20;
 constexpr int kMaxKin = 1 << 17;
 constexpr int kMaxH = 8192;
 constexpr int kMaxI = 4096;
+constexpr int kMaxProj = 32768;
 constexpr size_t kHbufElems = (size_t)VERIFY_MAX_K * (vk::kMaxTopK + 1) * kMaxI;
 constexpr size_t kMoePartElems = (size_t)VERIFY_MAX_K * (vk::kMaxTopK + 1) * kMaxH;
 
@@ -138,6 +145,12 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = cudaMalloc(&ctx->moe_part, kMoePartElems * sizeof(float)))) return bail(e);
   if ((e = cudaMalloc(&ctx->moe_cnt, (kMaxH / vk::kBM) * sizeof(int)))) return bail(e);
   if ((e = cudaMalloc(&ctx->err, sizeof(int)))) return bail(e);
+  if ((e = cudaMalloc(&ctx->st_xn, sizeof(uint16_t) * VERIFY_MAX_K * kMaxH))) return bail(e);
+  if ((e = cudaMalloc(&ctx->st_proj, sizeof(uint16_t) * VERIFY_MAX_K * kMaxProj))) return bail(e);
+  if ((e = cudaMalloc(&ctx->st_o, sizeof(uint16_t) * VERIFY_MAX_K * kMaxProj))) return bail(e);
+  if ((e = cudaMalloc(&ctx->st_logits, sizeof(float) * VERIFY_MAX_K * 1024))) return bail(e);
+  if ((e = cudaMalloc(&ctx->st_idx, sizeof(int32_t) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
+  if ((e = cudaMalloc(&ctx->st_w, sizeof(float) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
   if ((e = cudaMemset(ctx->moe_cnt, 0, (kMaxH / vk::kBM) * sizeof(int)))) return bail(e);
   if ((e = cudaMemset(ctx->err, 0, sizeof(int)))) return bail(e);
   cudaDriverEntryPointQueryResult q;
@@ -161,6 +174,12 @@ verify_status verify_destroy(verify_ctx* ctx) {
   cudaFree(ctx->moe_part);
   cudaFree(ctx->moe_cnt);
   cudaFree(ctx->err);
+  cudaFree(ctx->st_xn);
+  cudaFree(ctx->st_proj);
+  cudaFree(ctx->st_o);
+  cudaFree(ctx->st_logits);
+  cudaFree(ctx->st_idx);
+  cudaFree(ctx->st_w);
   delete ctx;
   return VERIFY_OK;
 }
@@ -366,6 +385,48 @@ verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w, 
   if (e) return cuda_fail(ctx, e, "verify_rmsnorm_k launch");
   ctx->launches += 1;
   return VERIFY_OK;
+}
+
+verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_state* st, float* h, int k,
+                             int32_t* idx_out, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  if (!L || !st) return fail(ctx, VERIFY_EINVAL, "layer or state is NULL%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  const verify_gdn_params& g = L->gdn;
+  const int H = L->in_proj.k_in;
+  const int C = 2 * g.n_qk_heads * g.head_dim_k + g.n_v_heads * g.head_dim_v;
+  const int Z = g.n_v_heads * g.head_dim_v;
+  const int NP = C + Z + 2 * g.n_v_heads;
+  const int E = L->gate_up.n_experts;
+  if (H > kMaxH || H % 4 != 0) return fail(ctx, VERIFY_EUNSUPPORTED, "hidden size must be a multiple of 4, <= 8192%s");
+  if (L->in_proj.n_out != NP || NP > kMaxProj) return fail(ctx, VERIFY_EINVAL, "in_proj must have C + Hv*dv + 2*Hv rows%s");
+  if (L->out_proj.n_out != H || L->out_proj.k_in != Z) return fail(ctx, VERIFY_EINVAL, "out_proj must be [H, Hv*dv]%s");
+  if (L->router.n_out != E + 1 || L->router.k_in != H || E + 1 > 1024)
+    return fail(ctx, VERIFY_EINVAL, "router must be [E+1, H] (routing rows, then the shared gate row)%s");
+  verify_status s;
+  cudaStream_t sm = stream;
+  // 1. pre-mixer norm
+  if ((s = verify_rmsnorm_k(ctx, h, L->norm1_w, L->norm_eps, 1, H, k, ctx->st_xn, VERIFY_BF16, sm))) return s;
+  // 2. in_proj -> q|k|v, z, a, b
+  if ((s = q4_qmv_k(ctx, &L->in_proj, ctx->st_xn, k, ctx->st_proj, VERIFY_BF16, sm))) return s;
+  // 3. Gated DeltaNet verify
+  verify_gdn_inputs in;
+  in.qkv = ctx->st_proj; in.ld_qkv = NP;
+  in.z = ctx->st_proj + C; in.ld_z = NP;
+  in.a = ctx->st_proj + C + Z; in.ld_a = NP;
+  in.b = ctx->st_proj + C + Z + g.n_v_heads; in.ld_b = NP;
+  if ((s = gdn_verify_k(ctx, &L->gdn, st, &in, k, ctx->st_o, VERIFY_BF16, sm))) return s;
+  // 4. out_proj into the residual
+  if ((s = q4_qmv_k(ctx, &L->out_proj, ctx->st_o, k, h, VERIFY_F32_ADD, sm))) return s;
+  // 5. pre-FFN norm
+  if ((s = verify_rmsnorm_k(ctx, h, L->norm2_w, L->norm_eps, 1, H, k, ctx->st_xn, VERIFY_BF16, sm))) return s;
+  // 6. router + shared-expert gate logits
+  if ((s = q4_qmv_k(ctx, &L->router, ctx->st_xn, k, ctx->st_logits, VERIFY_F32, sm))) return s;
+  // 7. routed + shared experts into the residual
+  return q4_gather_experts_k(ctx, &L->gate_up, &L->down, ctx->st_logits, E + 1, L->top_k, ctx->st_xn, k,
+                             idx_out ? idx_out : ctx->st_idx,
+                             ctx->st_w, h, VERIFY_F32_ADD, &L->shared_gate_up, &L->shared_down, ctx->st_logits + E,
+                             sm);
 }
 
 }  // extern "C"

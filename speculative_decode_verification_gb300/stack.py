@@ -1,0 +1,103 @@
+"""A synthetic hybrid verify stack on the device: L layers of (Gated DeltaNet
+mixer -> MoE with 10 routed + 1 shared expert), random-init weights drawn by
+the seeded generator (large Q4 tensors by its device twin), one ring of GDN
+state slots per layer.  Running a verify pass is one ``verify_layer_k`` call
+per layer; committing the accepted prefix is one ``gdn_commit`` per layer.
+
+Tensor names (the seeds of the generator) are shared with the host side, so
+any weight can be re-drawn on the host bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import binding as B
+from . import synth as S
+
+
+def layer_names(l: int):
+    p = f"stack.L{l}"
+    return dict(in_proj=p + ".in_proj", out_proj=p + ".out_proj", router=p + ".router", gate_up=p + ".gate_up",
+                down=p + ".down", shared_gate_up=p + ".shared_gate_up", shared_down=p + ".shared_down",
+                gdn=p + ".gdn", norm1=p + ".norm1", norm2=p + ".norm2")
+
+
+def shapes(cfg):
+    H, d, Hk, Hv = cfg["H"], cfg["d"], cfg["n_qk_heads"], cfg["n_v_heads"]
+    C = 2 * Hk * d + Hv * d
+    NP = C + Hv * d + 2 * Hv
+    return dict(H=H, C=C, NP=NP, Z=Hv * d, E=cfg["E"], I=cfg["I"], T=cfg["T"])
+
+
+class DeviceStack:
+    """All layers' weights and GDN state slots on the current CUDA device."""
+
+    def __init__(self, vf: B.Verify, cfg, seed: int = 0, n_slots: int = 10, s_std: float = 0.02,
+                 tail_std: float = 1.0, layers: int | None = None):
+        import torch
+
+        self.vf, self.cfg, self.seed = vf, cfg, seed
+        self.n_layers = cfg["layers"] if layers is None else layers
+        sh = shapes(cfg)
+        self.sh = sh
+        H, E, I = sh["H"], sh["E"], sh["I"]
+        d, Hk, Hv = cfg["d"], cfg["n_qk_heads"], cfg["n_v_heads"]
+        self.keep = []
+        self.layers = []
+        self.states = []
+        self.state_tensors = []
+
+        def q4(name, n_out, k_in, n_experts=None):
+            e = 1 if n_experts is None else n_experts
+            shp = (e, n_out, k_in // 8) if n_experts else (n_out, k_in // 8)
+            gshp = (e, n_out, k_in // 64) if n_experts else (n_out, k_in // 64)
+            p = torch.empty(shp, dtype=torch.int32, device="cuda")
+            sc = torch.empty(gshp, dtype=torch.int16, device="cuda")
+            bi = torch.empty(gshp, dtype=torch.int16, device="cuda")
+            vf.synth_q4(p, sc, bi, S.q4_seeds(seed, name), S.SCALE_RANGE, S.BIAS_RANGE)
+            self.keep += [p, sc, bi]
+            return B.q4_experts(p, sc, bi) if n_experts else B.q4_weight(p, sc, bi)
+
+        def dev(a):
+            t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+            self.keep.append(t)
+            return t
+
+        for l in range(self.n_layers):
+            nm = layer_names(l)
+            gp = {k: dev(v) for k, v in S.gdn_params(seed, nm["gdn"], Hk, Hv, d).items()}
+            L = B.Layer()
+            L.in_proj = q4(nm["in_proj"], sh["NP"], H)
+            L.out_proj = q4(nm["out_proj"], H, sh["Z"])
+            L.router = q4(nm["router"], E + 1, H)
+            L.gate_up = q4(nm["gate_up"], 2 * I, H, E)
+            L.down = q4(nm["down"], H, I, E)
+            L.shared_gate_up = q4(nm["shared_gate_up"], 2 * I, H)
+            L.shared_down = q4(nm["shared_down"], H, I)
+            L.gdn = B.gdn_params(Hk, Hv, d, gp["conv_w"], gp["A_log"], gp["dt_bias"], gp["norm_w"])
+            L.norm1_w = dev(S.f32_uniform(seed, nm["norm1"], (H,), -0.1, 0.1)).data_ptr()
+            L.norm2_w = dev(S.f32_uniform(seed, nm["norm2"], (H,), -0.1, 0.1)).data_ptr()
+            L.norm_eps = 1e-6
+            L.top_k = sh["T"]
+            self.layers.append(L)
+            S0, t0 = S.gdn_initial_state(seed, nm["gdn"], Hk, Hv, d, s_std=s_std, tail_std=tail_std)
+            slots = [torch.zeros((Hv, d, d), dtype=torch.float32, device="cuda") for _ in range(n_slots)]
+            tails = [torch.zeros((3, sh["C"]), dtype=torch.int16, device="cuda") for _ in range(n_slots)]
+            slots[0].copy_(torch.from_numpy(S0))
+            tails[0].copy_(torch.from_numpy(t0.view(np.int16)))
+            self.state_tensors.append((slots, tails))
+            self.states.append(B.gdn_state(slots, tails, cur=0))
+
+    def verify(self, h, k: int, idx=None, stream=None):
+        """One verify pass of k rows through every layer; h (fp32 [k, H]) is
+        updated in place.  idx (optional): per-layer int32 [k, T] device
+        tensors receiving the routed expert indices."""
+        for l, (L, st) in enumerate(zip(self.layers, self.states)):
+            self.vf.verify_layer_k(L, st, h, k, None if idx is None else idx[l], stream)
+
+    def commit(self, accepted: int):
+        for st in self.states:
+            self.vf.gdn_commit(st, accepted)
+
+    def weight_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.keep)

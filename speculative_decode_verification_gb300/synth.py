@@ -240,3 +240,34 @@ def gdn_initial_state(seed: int, prefix: str, n_qk_heads: int, n_v_heads: int, d
     else:
         tail = np.zeros((conv_kernel - 1, C), np.uint16)
     return S, tail
+
+
+class HostLayerWeights:
+    """Host re-draw of one layer of the synthetic verify stack (the same named
+    tensors the device stack draws): dense matrices eagerly, experts on demand."""
+
+    def __init__(self, seed: int, l: int, H: int, NP: int, Z: int, E: int, I: int,
+                 n_qk_heads: int, n_v_heads: int, d: int):
+        p = f"stack.L{l}"
+        self.seed, self.p, self.H, self.E, self.I = seed, p, H, E, I
+        m = q4_matrix(seed, p + ".in_proj", NP, H)
+        self.in_proj = (m.packed, m.scales, m.biases)
+        m = q4_matrix(seed, p + ".out_proj", H, Z)
+        self.out_proj = (m.packed, m.scales, m.biases)
+        m = q4_matrix(seed, p + ".router", E + 1, H)
+        self.router = (m.packed, m.scales, m.biases)
+        m = q4_matrix(seed, p + ".shared_gate_up", 2 * I, H)
+        self.shared_gate_up = (m.packed, m.scales, m.biases)
+        m = q4_matrix(seed, p + ".shared_down", H, I)
+        self.shared_down = (m.packed, m.scales, m.biases)
+        self.gdn = gdn_params(seed, p + ".gdn", n_qk_heads, n_v_heads, d)
+        self.norm1 = f32_uniform(seed, p + ".norm1", (H,), -0.1, 0.1)
+        self.norm2 = f32_uniform(seed, p + ".norm2", (H,), -0.1, 0.1)
+        self._cache = {}
+
+    def expert(self, e: int):
+        if e not in self._cache:
+            g = q4_expert(self.seed, self.p + ".gate_up", 2 * self.I, self.H, e)
+            dn = q4_expert(self.seed, self.p + ".down", self.H, self.I, e)
+            self._cache[e] = ((g.packed, g.scales, g.biases), (dn.packed, dn.scales, dn.biases))
+        return self._cache[e]
