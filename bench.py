@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact width-k verify pass on GB300.
+
+Workload: the synthetic 12-layer hybrid verify stack at hidden 2560 - every
+layer a Gated DeltaNet mixer (16 QK / 48 V heads, head dim 128, per-row state
+snapshots) followed by a MoE of 512 experts (top-10 routed + 1 sigmoid-gated
+shared, intermediate 640), all projections affine Q4/group-64 with random
+weights.  One step = one verify pass of k draft rows through all 12 layers
+(every row of the hot path: dense Q4 products, routing, routed experts with
+fused gate/up + SwiGLU + combine, GDN conv/norm/gates/delta rule/gated norm
+with snapshots, layer norms and residual adds).  Accepting a prefix
+(gdn_commit) is an O(1) host pointer swap without device work; it runs in
+the end-to-end loop.
+
+Metric: verified rows/s per layer = k * layers / step time, and the achieved
+HBM bandwidth of the dominant call (the routed-expert call) against the
+measured copy bandwidth.  The step's weight reads (~3 GB at k = 9) exceed the
+129 MB L2 many times, so no flush is needed between steps.
+
+Multi-GPU: the verify pass does not shard (see DESIGN); with --gpus N every
+rank runs an independent replica and `value` sums the replicas.
+
+--impl reference times the CPU oracle (test infrastructure) on one layer of
+the same workload per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = ("12-layer hybrid verify stack, hidden 2560: GDN 16 QK/48 V heads d128 + MoE 512 experts "
+            "top-10 + shared, I 640, affine Q4/g64 weights (synthetic, seed 0)")
+EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device, self.proc, self.lines = device, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.device)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_layer_step(cfg, k, seed=0, layer=0, weights=None):
+    """One layer of the stack on the CPU oracle; returns (seconds, weights)."""
+    from oracle import oracle as O
+    from speculative_decode_verification_gb300 import synth as S
+    from speculative_decode_verification_gb300.stack import shapes
+
+    sh = shapes(cfg)
+    if weights is None:
+        weights = S.HostLayerWeights(seed, layer, sh["H"], sh["NP"], sh["Z"], sh["E"], sh["I"], cfg["n_qk_heads"],
+                                     cfg["n_v_heads"], cfg["d"])
+    S0, t0 = S.gdn_initial_state(seed, f"stack.L{layer}.gdn", cfg["n_qk_heads"], cfg["n_v_heads"], cfg["d"],
+                                 s_std=0.02, tail_std=1.0)
+    h0 = S.f32_normal(seed, f"bench.h{k}", (k, sh["H"])).astype(np.float64)
+    # draw the experts this step routes to before the clock starts (input generation)
+    t = time.perf_counter()
+    O.stack_layer(weights, h0, S0.astype(np.float64), t0, k, cfg["n_qk_heads"], cfg["n_v_heads"], cfg["d"], sh["T"])
+    return time.perf_counter() - t, weights
+
+
+def cpu_baseline(cfg, k):
+    from oracle import oracle as O
+    O.build()
+    _, w = oracle_layer_step(cfg, k)   # draws the layer's weights and the routed experts (untimed)
+    dt, _ = oracle_layer_step(cfg, k, weights=w)
+    return {"value": k / dt, "unit": "verified rows/s per layer", "cores": 1, "kind": "oracle",
+            "sample": f"one of the {cfg['layers']} layers at k={k} (full shapes), single-threaded float64 C "
+                      f"oracle, {dt:.2f} s"}
+
+
+def run_reference(args, cfg):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import oracle as O
+    O.build()
+    k = args.k
+    _, w = oracle_layer_step(cfg, k)
+    for _ in range(args.warmup):
+        oracle_layer_step(cfg, k, weights=w)
+    ts = [oracle_layer_step(cfg, k, weights=w)[0] for _ in range(args.steps)]
+    step = float(np.mean(ts))
+    value = k / step
+    line = {"metric": "verified rows/s per layer", "value": value, "unit": "verified rows/s per layer",
+            "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "k": k, "layers_per_step": 1,
+                       "note": "CPU oracle, one layer per step (bounded sample)"},
+            "cpu_baseline": {"value": value, "unit": "verified rows/s per layer", "cores": 1, "kind": "oracle",
+                             "sample": f"one layer at k={k} per step, single-threaded float64 C oracle"},
+            "e2e": {"value": value, "unit": "verified rows/s per layer", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ ours
+
+def run_ours(args, cfg):
+    import torch
+
+    from speculative_decode_verification_gb300 import binding as B
+    from speculative_decode_verification_gb300 import synth as S
+    from speculative_decode_verification_gb300.stack import DeviceStack, shapes
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (GB300)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    vf = B.Verify(local)
+    sh = shapes(cfg)
+    L, H, T = cfg["layers"], sh["H"], sh["T"]
+    ds = DeviceStack(vf, cfg, seed=0)
+    stream = torch.cuda.Stream()
+    widths = sorted(set([int(w) for w in args.widths.split(",") if w] + [args.k]))
+    hbm, peak_kind = peaks()
+    per_k, head = {}, None
+    for k in widths:
+        h0 = torch.from_numpy(S.f32_normal(0, f"bench.h{k}", (k, H))).cuda()
+        h = torch.empty_like(h0)
+        idx = [torch.zeros((k, T), dtype=torch.int32, device="cuda") for _ in range(L)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(L)]
+        with torch.cuda.stream(stream):
+            for row in ev:
+                for e in row:
+                    e.record()
+        torch.cuda.synchronize()
+        for st in ds.states:
+            st.cur, st.pending_k = 0, 0
+        def capture(events_for_layer):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for st in ds.states:
+                    st.cur, st.pending_k = 0, 0
+                with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+                    h.copy_(h0)
+                    for l, (Ly, st) in enumerate(zip(ds.layers, ds.states)):
+                        vf.set_layer_events(events_for_layer(l))
+                        vf.verify_layer_k(Ly, st, h, k, idx[l], stream.cuda_stream)
+                    vf.set_layer_events(None)
+            return graph
+
+        for st in ds.states:
+            st.cur, st.pending_k = 0, 0
+        with torch.cuda.stream(stream):
+            h.copy_(h0)
+            ds.verify(h, k, idx, stream.cuda_stream)          # warm (first launches, first touch)
+        torch.cuda.synchronize()
+        # breakdown graph: every sub-step boundary of every layer (untimed)
+        gb = capture(lambda l: ev[l])
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                gb.replay()
+        torch.cuda.synchronize()
+        names = ["norm1", "in_proj", "gdn", "out_proj", "norm2", "router", "experts"]
+        sub = {n: float(np.mean([ev[l][i].elapsed_time(ev[l][i + 1]) * 1e3 for l in range(L)]))
+               for i, n in enumerate(names)}
+        del gb
+        # timed graph: only the routed-expert call of each layer is bracketed by events
+        evm = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+        with torch.cuda.stream(stream):
+            for row in evm:
+                for e in row:
+                    e.record()
+        torch.cuda.synchronize()
+        g = capture(lambda l: [None] * 6 + evm[l])
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        sampler = ClockSampler(local) if k == args.k else None
+        if sampler:  # nvidia-smi needs a moment to start: keep the GPU busy meanwhile (untimed)
+            sampler.start()
+            t_w = time.perf_counter()
+            with torch.cuda.stream(stream):
+                while time.perf_counter() - t_w < 0.6:
+                    g.replay()
+                    stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(args.steps):
+                g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        barrier(world)
+        ms = e0.elapsed_time(e1) / args.steps
+        ms = max_over_ranks(ms, world)
+        st, code = vf.device_status()
+        if st != B.OK:
+            raise SystemExit(f"device error {code} during the benchmark")
+        moe_timed_us = float(np.mean([evm[l][0].elapsed_time(evm[l][1]) * 1e3 for l in range(L)]))
+        U = [len(np.unique(idx[l].cpu().numpy())) for l in range(L)]
+        moe_bytes = [(u + 1) * EXPERT_BYTES(H, sh["I"]) + k * H * (2 + 8) + k * (sh["E"] + 1) * 4 for u in U]
+        dense_bytes = int(0.5625 * (sh["NP"] * H + H * sh["Z"] + (sh["E"] + 1) * H))
+        gdn_bytes = cfg["n_v_heads"] * cfg["d"] ** 2 * 4 * (1 + k) + 3 * sh["C"] * 2 * (1 + k)
+        step_bytes = sum(moe_bytes) + L * (dense_bytes + gdn_bytes)
+        per_k[k] = {"rows_per_s_per_layer": k * L / (ms * 1e-3) * world, "ms_per_step": ms,
+                    "layer_us": {n: round(v, 2) for n, v in sub.items()},
+                    "distinct_experts_per_layer": float(np.mean(U)),
+                    "step_bytes": step_bytes, "step_GBs": step_bytes / (ms * 1e-3) / 1e9}
+        per_k[k]["experts_us_timed"] = moe_timed_us
+        if k == args.k:
+            moe_us = moe_timed_us
+            achieved = float(np.mean(moe_bytes)) / (moe_us * 1e-6) / 1e9
+            head = dict(ms=ms, clocks=clocks, U=float(np.mean(U)), moe_us=moe_us, moe_bytes=float(np.mean(moe_bytes)),
+                        achieved=achieved)
+        del g
+    # ---- end to end through the public API: host buffers, copies inside the timed region
+    k = args.k
+    hh = torch.from_numpy(S.f32_normal(0, f"bench.h{k}", (k, H))).pin_memory()
+    hout = torch.empty_like(hh).pin_memory()
+    hd = torch.empty((k, H), dtype=torch.float32, device="cuda")
+    for st in ds.states:
+        st.cur, st.pending_k = 0, 0
+    accepted = k // 2
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            hd.copy_(hh, non_blocking=True)
+            ds.verify(hd, k, None, stream.cuda_stream)
+            hout.copy_(hd, non_blocking=True)
+        stream.synchronize()
+        ds.commit(accepted)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world)
+    n_e2e = max(3, min(args.steps, 200))
+    launches0 = vf.launch_count()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    launches_per_step = (vf.launch_count() - launches0) // n_e2e
+    e2e_s = max_over_ranks(e2e_s, world)
+    if rank != 0:
+        return 0
+    cpu = None if args.no_cpu_baseline else cpu_baseline(cfg, k)
+    value = per_k[k]["rows_per_s_per_layer"]
+    line = {
+        "metric": "verified rows/s per layer", "value": value, "unit": "verified rows/s per layer",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "k": k, "layers": L, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (weights read per step far above 129 MB); no flush",
+                   "per_k": {str(kk): v for kk, v in per_k.items()}},
+        "roofline": {"bound": "hbm", "achieved": head["achieved"], "peak": hbm, "unit": "GB/s",
+                     "frac": head["achieved"] / hbm, "traffic": None,
+                     "kernel": "q4_gather_experts_k (routed gate/up+SwiGLU kernel, down+combine kernel)",
+                     "bytes_per_launch": head["moe_bytes"], "us_per_launch": head["moe_us"],
+                     "distinct_experts": head["U"], "peak_kind": peak_kind},
+        "clocks": head["clocks"],
+        "e2e": {"value": k * L / e2e_s * world, "unit": "verified rows/s per layer",
+                "h2d_bytes_per_step": k * H * 4, "d2h_bytes_per_step": k * H * 4,
+                "ms_per_step": e2e_s * 1e3, "path": "DeviceStack.verify -> verify_layer_k (C ABI), eager"},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--k", type=int, default=9, help="verify width of the headline number")
+    ap.add_argument("--widths", default="1,4,8,9", help="widths also measured (reported under config.per_k)")
+    ap.add_argument("--layers", type=int, default=12)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from speculative_decode_verification_gb300 import synth as S
+    cfg = dict(S.STACK)
+    cfg["layers"] = args.layers
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -342,6 +342,17 @@ typedef struct {
 verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_state* st, float* h, int k,
                              int32_t* idx_out, struct CUstream_st* stream);
 
+/*
+ * Profiling aid (no counterpart on the pages): while set, every
+ * verify_layer_k call records events[0..7] (cudaEvent_t handles created by the
+ * caller with timing enabled) on its stream - before the first norm, then
+ * after the norm, in_proj, GDN, out_proj, second norm, router and experts -
+ * so the caller can time each sub-step, also inside a captured CUDA graph.
+ * A NULL entry skips that point; events = NULL (or n = 0) switches it off.
+ * n must be 8.
+ */
+verify_status verify_set_layer_events(verify_ctx* ctx, void* const* events, int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,15 +23,17 @@ extern "C" {
 /*
  * packed[i] = low 32 bits of draw i of seed_packed        (i < n_words)
  * scales[i] = bf16(lo_s + (hi_s - lo_s) * u_i)              (i < n_groups)
- * biases[i] = bf16(lo_b + (hi_b - lo_b) * u_i)
+ * biases[i] = bf16(lo_b + (hi_b - lo_b) * u_i)                 (centered == 0)
+ *            bf16(-(scales[i] * (lo_b + (hi_b - lo_b) * u_i)))  (centered != 0)
  * with u_i = (draw i >> 40) * 2^-24 and every step an fp32 IEEE operation
- * ((hi - lo) is rounded to fp32 first), bf16 rounding to nearest-even.
+ * ((hi - lo) is rounded to fp32 first; scales[i] is the stored bf16 value),
+ * bf16 rounding to nearest-even.
  * All pointers are device memory; asynchronous on `stream`.
  */
 verify_status verify_synth_q4(verify_ctx* ctx, uint32_t* packed, uint16_t* scales, uint16_t* biases,
                               int64_t n_words, int64_t n_groups, uint64_t seed_packed, uint64_t seed_scales,
                               uint64_t seed_biases, float lo_s, float hi_s, float lo_b, float hi_b,
-                              struct CUstream_st* stream);
+                              int centered, struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }

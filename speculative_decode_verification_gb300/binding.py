@@ -84,8 +84,9 @@ def load():
         "gdn_verify_k": [p, C.POINTER(GdnParams), C.POINTER(GdnState), C.POINTER(GdnInputs), i, p, i, p],
         "gdn_commit": [C.POINTER(GdnState), i],
         "verify_rmsnorm_k": [p, p, p, f, i, i, i, p, i, p],
-        "verify_synth_q4": [p, p, p, p, i64, i64, C.c_uint64, C.c_uint64, C.c_uint64, f, f, f, f, p],
+        "verify_synth_q4": [p, p, p, p, i64, i64, C.c_uint64, C.c_uint64, C.c_uint64, f, f, f, f, i, p],
         "verify_layer_k": [p, C.POINTER(Layer), C.POINTER(GdnState), p, i, p, p],
+        "verify_set_layer_events": [p, C.POINTER(p), i],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -188,11 +189,19 @@ class Verify:
         self._check(self.lib.verify_layer_k(self.ctx, C.byref(layer), C.byref(state), _ptr(h), k,
                                             _ptr(idx_out), self._stream(stream)))
 
-    def synth_q4(self, packed, scales, biases, seeds, scale_range, bias_range, stream=None):
+    def set_layer_events(self, events):
+        """events: 8 torch.cuda.Event(enable_timing=True) (recorded once first) or None entries, or None."""
+        if events is None:
+            self._check(self.lib.verify_set_layer_events(self.ctx, None, 0))
+            return
+        arr = (C.c_void_p * 8)(*[None if e is None else e.cuda_event for e in events])
+        self._check(self.lib.verify_set_layer_events(self.ctx, arr, 8))
+
+    def synth_q4(self, packed, scales, biases, seeds, scale_range, bias_range, centered=False, stream=None):
         self._check(self.lib.verify_synth_q4(self.ctx, _ptr(packed), _ptr(scales), _ptr(biases),
                                              packed.numel(), scales.numel(), *[C.c_uint64(s) for s in seeds],
                                              scale_range[0], scale_range[1], bias_range[0], bias_range[1],
-                                             self._stream(stream)))
+                                             int(bool(centered)), self._stream(stream)))
 
 
 def gdn_params(Hk, Hv, d, conv_w, A_log, dt_bias, norm_w, q_scale=None, l2_eps=1e-6, norm_eps=1e-6,

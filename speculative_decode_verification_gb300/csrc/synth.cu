@@ -12,20 +12,24 @@ __device__ __forceinline__ uint64_t draw(uint64_t seed, uint64_t i) {
   return z ^ (z >> 31);
 }
 
-__device__ __forceinline__ uint16_t uniform_bf16(uint64_t seed, uint64_t i, float lo, float span) {
+__device__ __forceinline__ float uniform_f32(uint64_t seed, uint64_t i, float lo, float span) {
   const float u = __fmul_rn((float)(draw(seed, i) >> 40), 5.9604644775390625e-8f);  // 2^-24
-  return __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(__fmul_rn(span, u), lo)));
+  return __fadd_rn(__fmul_rn(span, u), lo);
 }
+
+__device__ __forceinline__ uint16_t to_bf16(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
 __global__ void synth_q4_kernel(uint32_t* packed, uint16_t* scales, uint16_t* biases, int64_t n_words,
                                 int64_t n_groups, uint64_t sp, uint64_t ss, uint64_t sb, float lo_s, float span_s,
-                                float lo_b, float span_b) {
+                                float lo_b, float span_b, int centered) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_words; i += stride)
     packed[i] = (uint32_t)draw(sp, (uint64_t)i);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_groups; i += stride) {
-    scales[i] = uniform_bf16(ss, (uint64_t)i, lo_s, span_s);
-    biases[i] = uniform_bf16(sb, (uint64_t)i, lo_b, span_b);
+    const uint16_t sc = to_bf16(uniform_f32(ss, (uint64_t)i, lo_s, span_s));
+    const float u = uniform_f32(sb, (uint64_t)i, lo_b, span_b);
+    scales[i] = sc;
+    biases[i] = centered ? to_bf16(-__fmul_rn(__uint_as_float((uint32_t)sc << 16), u)) : to_bf16(u);
   }
 }
 
@@ -34,12 +38,12 @@ __global__ void synth_q4_kernel(uint32_t* packed, uint16_t* scales, uint16_t* bi
 extern "C" verify_status verify_synth_q4(verify_ctx* ctx, uint32_t* packed, uint16_t* scales, uint16_t* biases,
                                          int64_t n_words, int64_t n_groups, uint64_t seed_packed,
                                          uint64_t seed_scales, uint64_t seed_biases, float lo_s, float hi_s,
-                                         float lo_b, float hi_b, struct CUstream_st* stream) {
+                                         float lo_b, float hi_b, int centered, struct CUstream_st* stream) {
   if (!ctx || !packed || !scales || !biases || n_words < 0 || n_groups < 0) return VERIFY_EINVAL;
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   synth_q4_kernel<<<sms * 8, 256, 0, stream>>>(packed, scales, biases, n_words, n_groups, seed_packed, seed_scales,
-                                               seed_biases, lo_s, hi_s - lo_s, lo_b, hi_b - lo_b);
+                                               seed_biases, lo_s, hi_s - lo_s, lo_b, hi_b - lo_b, centered);
   return cudaGetLastError() == cudaSuccess ? VERIFY_OK : VERIFY_ECUDA;
 }

@@ -26,6 +26,8 @@ struct verify_ctx {
   int32_t* st_idx = nullptr;   // [16, 16]
   float* st_w = nullptr;       // [16, 16]
   int64_t launches = 0;
+  cudaEvent_t layer_events[8] = {};
+  int n_layer_events = 0;
   char msg[512] = {0};
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
@@ -405,10 +407,18 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
     return fail(ctx, VERIFY_EINVAL, "router must be [E+1, H] (routing rows, then the shared gate row)%s");
   verify_status s;
   cudaStream_t sm = stream;
+  auto mark = [&](int i) {
+    // external record: inside stream capture this becomes an event-record node of the graph
+    if (ctx->n_layer_events == 8 && ctx->layer_events[i])
+      cudaEventRecordWithFlags(ctx->layer_events[i], sm, cudaEventRecordExternal);
+  };
+  mark(0);
   // 1. pre-mixer norm
   if ((s = verify_rmsnorm_k(ctx, h, L->norm1_w, L->norm_eps, 1, H, k, ctx->st_xn, VERIFY_BF16, sm))) return s;
+  mark(1);
   // 2. in_proj -> q|k|v, z, a, b
   if ((s = q4_qmv_k(ctx, &L->in_proj, ctx->st_xn, k, ctx->st_proj, VERIFY_BF16, sm))) return s;
+  mark(2);
   // 3. Gated DeltaNet verify
   verify_gdn_inputs in;
   in.qkv = ctx->st_proj; in.ld_qkv = NP;
@@ -416,17 +426,35 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
   in.a = ctx->st_proj + C + Z; in.ld_a = NP;
   in.b = ctx->st_proj + C + Z + g.n_v_heads; in.ld_b = NP;
   if ((s = gdn_verify_k(ctx, &L->gdn, st, &in, k, ctx->st_o, VERIFY_BF16, sm))) return s;
+  mark(3);
   // 4. out_proj into the residual
   if ((s = q4_qmv_k(ctx, &L->out_proj, ctx->st_o, k, h, VERIFY_F32_ADD, sm))) return s;
+  mark(4);
   // 5. pre-FFN norm
   if ((s = verify_rmsnorm_k(ctx, h, L->norm2_w, L->norm_eps, 1, H, k, ctx->st_xn, VERIFY_BF16, sm))) return s;
+  mark(5);
   // 6. router + shared-expert gate logits
   if ((s = q4_qmv_k(ctx, &L->router, ctx->st_xn, k, ctx->st_logits, VERIFY_F32, sm))) return s;
+  mark(6);
   // 7. routed + shared experts into the residual
-  return q4_gather_experts_k(ctx, &L->gate_up, &L->down, ctx->st_logits, E + 1, L->top_k, ctx->st_xn, k,
-                             idx_out ? idx_out : ctx->st_idx,
-                             ctx->st_w, h, VERIFY_F32_ADD, &L->shared_gate_up, &L->shared_down, ctx->st_logits + E,
-                             sm);
+  if ((s = q4_gather_experts_k(ctx, &L->gate_up, &L->down, ctx->st_logits, E + 1, L->top_k, ctx->st_xn, k,
+                               idx_out ? idx_out : ctx->st_idx, ctx->st_w, h, VERIFY_F32_ADD, &L->shared_gate_up,
+                               &L->shared_down, ctx->st_logits + E, sm)))
+    return s;
+  mark(7);
+  return VERIFY_OK;
+}
+
+verify_status verify_set_layer_events(verify_ctx* ctx, void* const* events, int n) {
+  if (!ctx) return VERIFY_EINVAL;
+  if (!events || n == 0) {
+    ctx->n_layer_events = 0;
+    return VERIFY_OK;
+  }
+  if (n != 8) return fail(ctx, VERIFY_EINVAL, "verify_set_layer_events needs 8 events%s");
+  for (int i = 0; i < 8; ++i) ctx->layer_events[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+  ctx->n_layer_events = 8;
+  return VERIFY_OK;
 }
 
 }  // extern "C"

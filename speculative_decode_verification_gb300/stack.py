@@ -54,7 +54,7 @@ class DeviceStack:
             p = torch.empty(shp, dtype=torch.int32, device="cuda")
             sc = torch.empty(gshp, dtype=torch.int16, device="cuda")
             bi = torch.empty(gshp, dtype=torch.int16, device="cuda")
-            vf.synth_q4(p, sc, bi, S.q4_seeds(seed, name), S.SCALE_RANGE, S.BIAS_RANGE)
+            vf.synth_q4(p, sc, bi, S.q4_seeds(seed, name), S.SCALE_RANGE, S.CENTERED_RANGE, centered=True)
             self.keep += [p, sc, bi]
             return B.q4_experts(p, sc, bi) if n_experts else B.q4_weight(p, sc, bi)
 

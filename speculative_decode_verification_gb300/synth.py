@@ -118,17 +118,32 @@ def q4_seeds(seed: int, name: str):
             tensor_seed(seed, name + ".biases"))
 
 
+# Centred recipe (the verify stack): bias = -scale * U(7, 8), i.e. the affine
+# form of a roughly zero-mean weight group, so that projections are not
+# dominated by a common offset and different rows route to different experts.
+CENTERED_RANGE = (7.0, 8.0)
+
+
+def q4_biases(sb: int, count: int, scales_bf16: np.ndarray, bias_range, centered: bool, start: int = 0):
+    u = uniform_f32(sb, count, *bias_range, start=start)
+    if not centered:
+        return f32_to_bf16(u)
+    return f32_to_bf16(-(bf16_to_f32(scales_bf16) * u).astype(np.float32))
+
+
 def q4_matrix(seed: int, name: str, n_out: int, k_in: int, n_experts: int | None = None,
-              scale_range=SCALE_RANGE, bias_range=BIAS_RANGE) -> Q4Matrix:
+              scale_range=SCALE_RANGE, bias_range=BIAS_RANGE, centered: bool = False) -> Q4Matrix:
     """Random-init affine Q4/g64 weights: codes U{0..15}, scales U(0.005,0.02),
-    biases U(-0.1,0.1), scales/biases stored as bf16."""
+    biases U(-0.1,0.1) (or, centered, -scale * U(7, 8)), scales/biases bf16."""
     assert k_in % 64 == 0
+    if centered:
+        bias_range = CENTERED_RANGE
     e = 1 if n_experts is None else n_experts
     sp, ss, sb = q4_seeds(seed, name)
     nw, ng = n_out * (k_in // 8), n_out * (k_in // 64)
     packed = packed_words(sp, e * nw)
     scales = f32_to_bf16(uniform_f32(ss, e * ng, *scale_range))
-    biases = f32_to_bf16(uniform_f32(sb, e * ng, *bias_range))
+    biases = q4_biases(sb, e * ng, scales, bias_range, centered)
     if n_experts is None:
         shape_w, shape_g = (n_out, k_in // 8), (n_out, k_in // 64)
     else:
@@ -138,9 +153,11 @@ def q4_matrix(seed: int, name: str, n_out: int, k_in: int, n_experts: int | None
 
 
 def q4_rows(seed: int, name: str, n_out: int, k_in: int, rows, expert: int = 0,
-            scale_range=SCALE_RANGE, bias_range=BIAS_RANGE) -> Q4Matrix:
+            scale_range=SCALE_RANGE, bias_range=BIAS_RANGE, centered: bool = False) -> Q4Matrix:
     """Re-draw only the given rows (of one expert) of a q4_matrix tensor.
     Bit-identical to slicing q4_matrix(...) but costs O(len(rows) * k_in)."""
+    if centered:
+        bias_range = CENTERED_RANGE
     sp, ss, sb = q4_seeds(seed, name)
     wpr, gpr = k_in // 8, k_in // 64
     rows = np.asarray(rows, dtype=np.int64)
@@ -151,18 +168,20 @@ def q4_rows(seed: int, name: str, n_out: int, k_in: int, rows, expert: int = 0,
         base = expert * n_out + int(n)
         packed[i] = packed_words(sp, wpr, start=base * wpr)
         scales[i] = f32_to_bf16(uniform_f32(ss, gpr, *scale_range, start=base * gpr))
-        biases[i] = f32_to_bf16(uniform_f32(sb, gpr, *bias_range, start=base * gpr))
+        biases[i] = q4_biases(sb, gpr, scales[i], bias_range, centered, start=base * gpr)
     return Q4Matrix(packed, scales, biases, len(rows), k_in)
 
 
 def q4_expert(seed: int, name: str, n_out: int, k_in: int, expert: int,
-              scale_range=SCALE_RANGE, bias_range=BIAS_RANGE) -> Q4Matrix:
+              scale_range=SCALE_RANGE, bias_range=BIAS_RANGE, centered: bool = False) -> Q4Matrix:
     """Re-draw one whole expert matrix of a q4_matrix(..., n_experts=E) stack."""
+    if centered:
+        bias_range = CENTERED_RANGE
     sp, ss, sb = q4_seeds(seed, name)
     wpr, gpr = k_in // 8, k_in // 64
     packed = packed_words(sp, n_out * wpr, start=expert * n_out * wpr)
     scales = f32_to_bf16(uniform_f32(ss, n_out * gpr, *scale_range, start=expert * n_out * gpr))
-    biases = f32_to_bf16(uniform_f32(sb, n_out * gpr, *bias_range, start=expert * n_out * gpr))
+    biases = q4_biases(sb, n_out * gpr, scales, bias_range, centered, start=expert * n_out * gpr)
     return Q4Matrix(packed.reshape(n_out, wpr), scales.reshape(n_out, gpr), biases.reshape(n_out, gpr),
                     n_out, k_in)
 
@@ -250,15 +269,15 @@ class HostLayerWeights:
                  n_qk_heads: int, n_v_heads: int, d: int):
         p = f"stack.L{l}"
         self.seed, self.p, self.H, self.E, self.I = seed, p, H, E, I
-        m = q4_matrix(seed, p + ".in_proj", NP, H)
+        m = q4_matrix(seed, p + ".in_proj", NP, H, centered=True)
         self.in_proj = (m.packed, m.scales, m.biases)
-        m = q4_matrix(seed, p + ".out_proj", H, Z)
+        m = q4_matrix(seed, p + ".out_proj", H, Z, centered=True)
         self.out_proj = (m.packed, m.scales, m.biases)
-        m = q4_matrix(seed, p + ".router", E + 1, H)
+        m = q4_matrix(seed, p + ".router", E + 1, H, centered=True)
         self.router = (m.packed, m.scales, m.biases)
-        m = q4_matrix(seed, p + ".shared_gate_up", 2 * I, H)
+        m = q4_matrix(seed, p + ".shared_gate_up", 2 * I, H, centered=True)
         self.shared_gate_up = (m.packed, m.scales, m.biases)
-        m = q4_matrix(seed, p + ".shared_down", H, I)
+        m = q4_matrix(seed, p + ".shared_down", H, I, centered=True)
         self.shared_down = (m.packed, m.scales, m.biases)
         self.gdn = gdn_params(seed, p + ".gdn", n_qk_heads, n_v_heads, d)
         self.norm1 = f32_uniform(seed, p + ".norm1", (H,), -0.1, 0.1)
@@ -267,7 +286,7 @@ class HostLayerWeights:
 
     def expert(self, e: int):
         if e not in self._cache:
-            g = q4_expert(self.seed, self.p + ".gate_up", 2 * self.I, self.H, e)
-            dn = q4_expert(self.seed, self.p + ".down", self.H, self.I, e)
+            g = q4_expert(self.seed, self.p + ".gate_up", 2 * self.I, self.H, e, centered=True)
+            dn = q4_expert(self.seed, self.p + ".down", self.H, self.I, e, centered=True)
             self._cache[e] = ((g.packed, g.scales, g.biases), (dn.packed, dn.scales, dn.biases))
         return self._cache[e]

@@ -19,7 +19,9 @@ def run():
     m = S.q4_matrix(0, "tiny.q4", 512, 512)
     x = S.bf16_normal(0, "smoke.x", (k, 512))
     y = torch.zeros((k, 512), device="cuda")
-    vf.q4_qmv_k(DevQ4(m).struct, dev(x), k, y)
+    W = DevQ4(m)  # keeps the device tensors alive while the struct points at them
+    xd = dev(x)
+    vf.q4_qmv_k(W.struct, xd, k, y)
     torch.cuda.synchronize()
     assert_close(host(y), O.q4_qmv(m.packed, m.scales, m.biases, x), what="q4_qmv_k")
     # routed experts
@@ -31,7 +33,9 @@ def run():
     idx = torch.zeros((k, T), dtype=torch.int32, device="cuda")
     w = torch.zeros((k, T), device="cuda")
     ym = torch.zeros((k, H), device="cuda")
-    vf.q4_gather_experts_k(DevQ4(gu).struct, DevQ4(dn).struct, dev(lg), E, T, dev(xm), k, idx, w, ym)
+    GU, DN = DevQ4(gu), DevQ4(dn)
+    lgd, xmd = dev(lg), dev(xm)
+    vf.q4_gather_experts_k(GU.struct, DN.struct, lgd, E, T, xmd, k, idx, w, ym)
     torch.cuda.synchronize()
     oi, _, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases), lg, T, xm)
     assert np.array_equal(host(idx), oi)
@@ -47,7 +51,7 @@ def run():
     tails = [torch.zeros((3, C), dtype=torch.int16, device="cuda") for _ in range(k + 1)]
     st = B.gdn_state(slots, tails)
     inp = S.gdn_inputs(0, "smoke.gdn", k, Hk, Hv, d)
-    di = {key: dev(v) for key, v in inp.items()}
+    di = {key: dev(v) for key, v in inp.items()}  # kept alive until the synchronize below
     o = torch.zeros((k, Hv * d), device="cuda")
     vf.gdn_verify_k(B.gdn_params(Hk, Hv, d, dp["conv_w"], dp["A_log"], dp["dt_bias"], dp["norm_w"]), st,
                     B.gdn_inputs(di["qkv"], di["z"], di["a"], di["b"]), k, o)
