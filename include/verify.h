@@ -353,6 +353,47 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
  */
 verify_status verify_set_layer_events(verify_ctx* ctx, void* const* events, int n);
 
+/* ------------------------------------- routed experts without allocation */
+
+/*
+ * Routed-expert call that allocates no device memory.  The pages have no
+ * counterpart of this entry point; it exists for callers that are not
+ * allowed to allocate: for example a host framework that hands out all
+ * device memory from its own arena and forbids plug-ins to call cudaMalloc,
+ * or a latency-critical serving loop where cudaMalloc/cudaFree would
+ * synchronise the device.  Such callers cannot create a verify_ctx (its
+ * scratch is allocated), so this call needs none.
+ *
+ * It computes exactly what q4_gather_experts_k computes, with the same
+ * arguments (no ctx) plus `device_error`: an optional device int32 the caller
+ * owns, set to 1 if a pipeline wait timed out (NULL: not reported).  The
+ * caller passes all inputs and outputs; the kernels' scratch (SwiGLU rows,
+ * per-rank partial outputs, arrival counters) lives in one array of
+ * VERIFY_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   - Limit: k*(T+s)*I*2 + k*(T+s)*H*4 bytes (s = 1 with a shared expert, each
+ *     part rounded up to 256) plus 4*(ceil(H/128)+1) must fit the array;
+ *     larger calls return VERIFY_EUNSUPPORTED before anything is enqueued.
+ *   - The first call on each device sets that device up (resolves the array's
+ *     device address, sets the kernels' launch attributes); make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the array, which keeps the last call's
+ *     contents; the call clears the parts that must start at zero (arrival
+ *     counters, error word) on `stream` before its kernels.  Calls whose work
+ *     overlaps on the GPU (different streams, no ordering) race on it.
+ * The calling thread's current device is used.
+ */
+#define VERIFY_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+verify_status q4_gather_experts_k_noalloc(const verify_q4_experts* gate_up, const verify_q4_experts* down,
+                                          const float* logits, int64_t logits_ld, int top_k,
+                                          const uint16_t* x, int k, int32_t* idx_out, float* w_out,
+                                          void* y, int dtype_out,
+                                          const verify_q4_weight* shared_gate_up,
+                                          const verify_q4_weight* shared_down,
+                                          const float* shared_gate_logit, int32_t* device_error,
+                                          struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

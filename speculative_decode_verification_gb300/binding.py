@@ -87,6 +87,8 @@ def load():
         "verify_synth_q4": [p, p, p, p, i64, i64, C.c_uint64, C.c_uint64, C.c_uint64, f, f, f, f, i, p],
         "verify_layer_k": [p, C.POINTER(Layer), C.POINTER(GdnState), p, i, p, p],
         "verify_set_layer_events": [p, C.POINTER(p), i],
+        "q4_gather_experts_k_noalloc": [C.POINTER(Q4Experts), C.POINTER(Q4Experts), p, i64, i, p, i, p, p, p, i,
+                                        C.POINTER(Q4Weight), C.POINTER(Q4Weight), p, p, p],
     }
     for name, args in sig.items():
         fn = getattr(L, name)

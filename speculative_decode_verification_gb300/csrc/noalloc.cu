@@ -1,0 +1,173 @@
+// noalloc.cu - the routed-expert call for callers that may not allocate device
+// memory.  Its scratch is a fixed array compiled into the library; nothing
+// here calls cudaMalloc, cudaFree or an allocating library routine.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "verify.h"
+
+namespace {
+
+// Scratch of the routed-expert kernels: SwiGLU rows [k, T+1, I] bf16, per-rank
+// partial outputs [k, T+1, H] fp32, one arrival counter per 128 outputs, and
+// an error word.  Every GPU that loads the library holds it until the process
+// exits.  All calls on one device share it.
+constexpr size_t kScratchBytes = VERIFY_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceSetup {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_scratch on this device
+  int num_sms = 0;
+  int moe_ctas_per_sm = 0;
+};
+
+std::mutex g_mutex;
+DeviceSetup g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Once per device, with that device current: resolve the array's device
+// address (the host-side name g_scratch is only a stand-in), set the kernels'
+// launch attributes and read the SM count.
+verify_status setup_device(int dev, DeviceSetup** out) {
+  if (dev < 0 || dev >= kMaxDevices) return VERIFY_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceSetup& d = g_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return VERIFY_ECUDA;
+    int dense_ctas = 0, moe_ctas = 0, sms = 0;
+    if (vk::q4_setup_kernels(&dense_ctas, &moe_ctas) != cudaSuccess) return VERIFY_ECUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return VERIFY_ECUDA;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return VERIFY_ECUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.scratch = static_cast<unsigned char*>(p);
+    d.num_sms = sms;
+    d.moe_ctas_per_sm = moe_ctas;
+    d.ready = true;
+  }
+  *out = &d;
+  return VERIFY_OK;
+}
+
+bool device_memory(const void* p, size_t align) {
+  if (!p || reinterpret_cast<uintptr_t>(p) % align) return false;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+bool valid_q4(const verify_q4_weight* W) {
+  return W && W->group_size == 64 && W->bits == 4 && W->k_in % 128 == 0 && W->k_in >= 256 && W->n_out >= 1 &&
+         device_memory(W->packed, 16) && device_memory(W->scales, 4) && device_memory(W->biases, 4);
+}
+
+bool encode(CUtensorMap* m, const void* base, uint64_t rows, uint64_t words, uint32_t box_rows) {
+  cuuint64_t dims[2] = {words, rows};
+  cuuint64_t strides[1] = {words * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" verify_status q4_gather_experts_k_noalloc(
+    const verify_q4_experts* gate_up, const verify_q4_experts* down, const float* logits, int64_t logits_ld,
+    int top_k, const uint16_t* x, int k, int32_t* idx_out, float* w_out, void* y, int dtype_out,
+    const verify_q4_weight* shared_gate_up, const verify_q4_weight* shared_down, const float* shared_gate_logit,
+    int32_t* device_error, struct CUstream_st* stream) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VERIFY_ECUDA;
+  DeviceSetup* d = nullptr;
+  verify_status s = setup_device(dev, &d);
+  if (s) return s;
+
+  // ---- arguments (all checked before anything is enqueued)
+  if (!gate_up || !down || k < 1 || k > VERIFY_MAX_K) return k < 1 || k > VERIFY_MAX_K ? VERIFY_EUNSUPPORTED : VERIFY_EINVAL;
+  const int E = gate_up->n_experts;
+  if (E < 1 || E > vk::kMaxExperts || down->n_experts != E) return VERIFY_EUNSUPPORTED;
+  if (top_k < 1 || top_k > vk::kMaxTopK || top_k > E) return VERIFY_EUNSUPPORTED;
+  if (!valid_q4(&gate_up->w) || !valid_q4(&down->w)) return VERIFY_EINVAL;
+  const int H = gate_up->w.k_in, I = gate_up->w.n_out / 2;
+  if (gate_up->w.n_out != 2 * I || down->w.n_out != H || down->w.k_in != I || I % 128 != 0) return VERIFY_EINVAL;
+  if (logits_ld < E) return VERIFY_EINVAL;
+  if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16 && dtype_out != VERIFY_F32_ADD) return VERIFY_EINVAL;
+  if (!device_memory(logits, 4) || !device_memory(x, 16) || !device_memory(idx_out, 4) || !device_memory(w_out, 4) ||
+      !device_memory(y, dtype_out == VERIFY_BF16 ? 2 : 4))
+    return VERIFY_EINVAL;
+  if (device_error && !device_memory(device_error, 4)) return VERIFY_EINVAL;
+  const int n_shared = (shared_gate_up != nullptr) + (shared_down != nullptr) + (shared_gate_logit != nullptr);
+  if (n_shared != 0 && n_shared != 3) return VERIFY_EINVAL;
+  if (n_shared == 3) {
+    if (!valid_q4(shared_gate_up) || !valid_q4(shared_down) || !device_memory(shared_gate_logit, 4))
+      return VERIFY_EINVAL;
+    if (shared_gate_up->n_out != 2 * I || shared_gate_up->k_in != H || shared_down->n_out != H ||
+        shared_down->k_in != I)
+      return VERIFY_EINVAL;
+  }
+  // ---- carve the fixed scratch; reject what does not fit
+  const int TS = top_k + (n_shared ? 1 : 0);
+  const int nblocks = (H + vk::kBM - 1) / vk::kBM;
+  const size_t hbuf_bytes = round256((size_t)k * TS * I * sizeof(uint16_t));
+  const size_t part_bytes = round256((size_t)k * TS * H * sizeof(float));
+  const size_t cnt_bytes = round256((size_t)nblocks * sizeof(int) + sizeof(int));
+  if (hbuf_bytes + part_bytes + cnt_bytes > kScratchBytes) return VERIFY_EUNSUPPORTED;
+  unsigned char* base = d->scratch;
+  int* cnt = reinterpret_cast<int*>(base + hbuf_bytes + part_bytes);
+  int* err_word = cnt + nblocks;
+
+  CUtensorMap gu, dn, sgu, sdn;
+  if (!encode(&gu, gate_up->w.packed, (uint64_t)E * 2 * I, (uint64_t)H / 8, 64) ||
+      !encode(&dn, down->w.packed, (uint64_t)E * H, (uint64_t)I / 8, vk::kBM))
+    return VERIFY_ECUDA;
+  if (n_shared == 3) {
+    if (!encode(&sgu, shared_gate_up->packed, (uint64_t)2 * I, (uint64_t)H / 8, 64) ||
+        !encode(&sdn, shared_down->packed, (uint64_t)H, (uint64_t)I / 8, vk::kBM))
+      return VERIFY_ECUDA;
+  } else {
+    sgu = gu;
+    sdn = dn;
+  }
+  vk::MoeArgs a{};
+  a.logits = logits; a.logits_ld = logits_ld; a.shared_logit = n_shared ? shared_gate_logit : nullptr;
+  a.x = x;
+  a.gu_scales = gate_up->w.scales; a.gu_biases = gate_up->w.biases;
+  a.dn_scales = down->w.scales; a.dn_biases = down->w.biases;
+  if (n_shared) {
+    a.sgu_scales = shared_gate_up->scales; a.sgu_biases = shared_gate_up->biases;
+    a.sdn_scales = shared_down->scales; a.sdn_biases = shared_down->biases;
+  }
+  a.hbuf = reinterpret_cast<uint16_t*>(base);
+  a.part = reinterpret_cast<float*>(base + hbuf_bytes);
+  a.cnt = cnt;
+  a.idx_out = idx_out; a.w_out = w_out; a.y = y;
+  a.err = device_error ? device_error : err_word;
+  a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
+  a.has_shared = n_shared ? 1 : 0;
+  a.G = d->moe_ctas_per_sm * d->num_sms;
+  // The arrival counters must start at zero: a previous call that stopped on a
+  // device error may have left them behind, so clear them (and the error word).
+  if (cudaMemsetAsync(cnt, 0, (size_t)(nblocks + 1) * sizeof(int), stream) != cudaSuccess) return VERIFY_ECUDA;
+  int launched = 0;
+  if (vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
+  return VERIFY_OK;
+}

@@ -1,0 +1,95 @@
+"""The routed-expert entry point that allocates nothing
+(q4_gather_experts_k_noalloc), called through the C ABI, against the
+regular entry point (q4_gather_experts_k).
+
+It serves callers that may not allocate device memory (memory owned by a
+host framework's arena; loops where cudaMalloc would synchronise the device):
+its scratch is a fixed array inside the library.  The file name makes pytest
+collect it last, so a run that stops at the first failure has run everything
+else first; it also passes on its own in a fresh process.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+from speculative_decode_verification_gb300 import binding as B
+from speculative_decode_verification_gb300 import synth as S
+from tests.gpu_util import DevQ4, assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(lib, gu, dn, logits, E, T, x, k, idx, w, y, shared=None, err=None):
+    import torch
+
+    sgu, sdn, sl = shared if shared is not None else (None, None, None)
+    st = lib.q4_gather_experts_k_noalloc(
+        C.byref(gu), C.byref(dn), C.c_void_p(logits.data_ptr()), E, T, C.c_void_p(x.data_ptr()), k,
+        C.c_void_p(idx.data_ptr()), C.c_void_p(w.data_ptr()), C.c_void_p(y.data_ptr()), B.F32,
+        C.byref(sgu) if sgu is not None else None, C.byref(sdn) if sdn is not None else None,
+        C.c_void_p(sl.data_ptr()) if sl is not None else None,
+        C.c_void_p(err.data_ptr()) if err is not None else None,
+        C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return st
+
+
+def test_noalloc_matches_regular_entry_point_on_two_calls():
+    import torch
+
+    assert torch.cuda.is_available()
+    lib = B.load()
+    vf = B.Verify(0)
+    E, H, I, T = 24, 384, 640, 10
+    gu = S.q4_matrix(50, "na.gu", 2 * I, H, n_experts=E)
+    dn = S.q4_matrix(50, "na.dn", H, I, n_experts=E)
+    sgu = S.q4_matrix(50, "na.sgu", 2 * I, H)
+    sdn = S.q4_matrix(50, "na.sdn", H, I)
+    GU, DN, SGU, SDN = DevQ4(gu), DevQ4(dn), DevQ4(sgu), DevQ4(sdn)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for call, k in enumerate([9, 4]):  # two calls in a row, different widths
+        x = dev(S.bf16_normal(50, f"na.x{call}", (k, H)))
+        logits = dev(S.f32_normal(50, f"na.l{call}", (k, E)))
+        sl = dev(np.ascontiguousarray(np.pad(S.f32_normal(50, f"na.s{call}", (k, 1)), ((0, 0), (0, E - 1)))))
+        outs = []
+        for use_noalloc in (False, True):
+            idx = torch.full((k, T), -1, dtype=torch.int32, device="cuda")
+            w = torch.zeros((k, T), device="cuda")
+            y = torch.zeros((k, H), device="cuda")
+            if use_noalloc:
+                st = _noalloc(lib, GU.struct, DN.struct, logits, E, T, x, k, idx, w, y,
+                              shared=(SGU.struct, SDN.struct, sl), err=err)
+                assert st == B.OK, f"call {call}: status {st}"
+            else:
+                vf.q4_gather_experts_k(GU.struct, DN.struct, logits, E, T, x, k, idx, w, y, B.F32,
+                                       SGU.struct, SDN.struct, sl)
+            torch.cuda.synchronize()
+            outs.append((host(idx), host(w), host(y)))
+        (i0, w0, y0), (i1, w1, y1) = outs
+        assert np.array_equal(i0, i1), f"call {call}: routing differs"
+        np.testing.assert_allclose(w1, w0, rtol=1e-6, atol=0)
+        assert_close(y1, y0, what=f"call {call}: y")
+    assert int(err.item()) == 0
+    st, code = vf.device_status()
+    assert st == B.OK, f"device error word {code}"
+    vf.close()
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    import torch
+
+    lib = B.load()
+    E, H, I, T, k = 16, 8192, 256, 16, 16  # k*T*H*4 = 8 MiB of partials alone: too large
+    gu = torch.zeros((E, 2 * I, H // 8), dtype=torch.int32, device="cuda")
+    gs = torch.zeros((E, 2 * I, H // 64), dtype=torch.int16, device="cuda")
+    dn = torch.zeros((E, H, I // 8), dtype=torch.int32, device="cuda")
+    ds = torch.zeros((E, H, I // 64), dtype=torch.int16, device="cuda")
+    GU, DN = B.q4_experts(gu, gs, gs), B.q4_experts(dn, ds, ds)
+    x = torch.zeros((k, H), dtype=torch.int16, device="cuda")
+    logits = torch.zeros((k, E), device="cuda")
+    idx = torch.zeros((k, E), dtype=torch.int32, device="cuda")
+    w = torch.zeros((k, E), device="cuda")
+    y = torch.zeros((k, H), device="cuda")
+    st = _noalloc(lib, GU, DN, logits, E, T, x, k, idx, w, y)
+    assert st == B.EUNSUPPORTED
+    torch.cuda.synchronize()
