@@ -90,6 +90,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// 8-byte copy.
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
 // 16-byte copy (L2 only); src_bytes = 0 writes zeros without reading.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -167,5 +171,18 @@ __device__ __forceinline__ float ld_dsmem_f32(const void* local_ptr, uint32_t ra
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+
+// ------------------------------------------------ programmatic dependent launch
+//
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it is still running.  Every kernel here follows one rule:
+// before griddep_wait() it reads only data that no kernel of the running
+// sequence writes (weights, parameters) or that was written at least two
+// kernels earlier (routing logits of the down kernel, the DeltaNet state
+// slot), and it writes nothing; it triggers its own dependents only after its
+// wait.  So when a kernel starts, the kernel two places before it has
+// finished.  Without the launch attribute both instructions are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 }  // namespace vk

@@ -55,39 +55,66 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
 
   const int il = tid >> 3, l = tid & 7;
   const int i = p * kGdnRows + il;  // value row within the head
+
+  // ---- before the grid dependency wait: the state slice and the conv
+  //      weights and tail (parameters, or written by an earlier verify call)
   float s[JPT];
   {
     const float* src = a.S_in + ((long long)h * D + i) * D;
 #pragma unroll
     for (int m = 0; m < JPT / 4; ++m) {
-      const float4 v = *reinterpret_cast<const float4*>(src + 4 * l + 32 * m);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * l + 32 * m));
       s[4 * m] = v.x; s[4 * m + 1] = v.y; s[4 * m + 2] = v.z; s[4 * m + 3] = v.w;
     }
   }
+  // Conv channels of this CTA: the q and k channels of QK head hq, then the v
+  // channels of its value rows; thread tid takes channels tid, tid + 128, ...
+  constexpr int NCH = 2 * D + kGdnRows;
+  constexpr int NIT = (NCH + kGdnThreads - 1) / kGdnThreads;
+  int chn[NIT];
+  float cw[NIT][4];
+  uint16_t tl[NIT][3];
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int cl = tid + it * kGdnThreads;
+    int ch = 0;
+    if (cl < D) ch = hq * D + cl;
+    else if (cl < 2 * D) ch = a.Hk * D + hq * D + (cl - D);
+    else if (cl < NCH) ch = 2 * a.Hk * D + h * D + p * kGdnRows + (cl - 2 * D);
+    chn[it] = ch;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) cw[it][t] = cl < NCH ? a.conv_w[ch * 4 + t] : 0.f;
+#pragma unroll
+    for (int t = 0; t < 3; ++t) tl[it][t] = cl < NCH ? __ldcg(a.tail_in + t * C + ch) : (uint16_t)0;
+  }
+  griddep_wait();
+  griddep_launch();
 
-  // ---- 1. causal depthwise conv + SiLU for the q, k channels of QK head hq
-  //         and the v channels of this CTA's value rows; slide the window.
-  for (int cl = tid; cl < 2 * D + kGdnRows; cl += kGdnThreads) {
-    int ch;
+  // ---- 1. causal depthwise conv + SiLU; slide the window
+  uint16_t xin[NIT][kGdnMaxK];
+#pragma unroll
+  for (int it = 0; it < NIT; ++it)
+#pragma unroll
+    for (int r = 0; r < kGdnMaxK; ++r)
+      xin[it][r] = (r < k && tid + it * kGdnThreads < NCH) ? a.qkv[r * a.ld_qkv + chn[it]] : (uint16_t)0;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int cl = tid + it * kGdnThreads;
+    if (cl >= NCH) break;
+    const int ch = chn[it];
     bool write_tail;
-    if (cl < D) { ch = hq * D + cl; write_tail = owns_qk_tail && (cl / (D / P) == p); }
-    else if (cl < 2 * D) { ch = a.Hk * D + hq * D + (cl - D); write_tail = owns_qk_tail && ((cl - D) / (D / P) == p); }
-    else { ch = 2 * a.Hk * D + h * D + p * kGdnRows + (cl - 2 * D); write_tail = true; }
-    float w[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) w[t] = a.conv_w[ch * 4 + t];
-    uint16_t w0 = a.tail_in[ch], w1 = a.tail_in[C + ch], w2 = a.tail_in[2 * C + ch];
-    uint16_t xin[kGdnMaxK];
-#pragma unroll
-    for (int r = 0; r < kGdnMaxK; ++r) xin[r] = r < k ? a.qkv[r * a.ld_qkv + ch] : (uint16_t)0;
+    if (cl < D) write_tail = owns_qk_tail && (cl / (D / P) == p);
+    else if (cl < 2 * D) write_tail = owns_qk_tail && ((cl - D) / (D / P) == p);
+    else write_tail = true;
+    uint16_t w0 = tl[it][0], w1 = tl[it][1], w2 = tl[it][2];
 #pragma unroll
     for (int r = 0; r < kGdnMaxK; ++r) {
       if (r >= k) break;
-      const uint16_t xr = xin[r];
-      float acc = w[0] * bf16f(w0);
-      acc = fmaf(w[1], bf16f(w1), acc);
-      acc = fmaf(w[2], bf16f(w2), acc);
-      acc = fmaf(w[3], bf16f(xr), acc);
+      const uint16_t xr = xin[it][r];
+      float acc = cw[it][0] * bf16f(w0);
+      acc = fmaf(cw[it][1], bf16f(w1), acc);
+      acc = fmaf(cw[it][2], bf16f(w2), acc);
+      acc = fmaf(cw[it][3], bf16f(xr), acc);
       const float cv = siluf_(acc);
       if (cl < D) qn[r][cl] = cv;
       else if (cl < 2 * D) kn[r][cl - D] = cv;
@@ -204,30 +231,32 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
 }
 
 template <int D>
-static cudaError_t launch_gdn_d(const GdnArgs& a, cudaStream_t s) {
+static cudaError_t launch_gdn_d(const GdnArgs& a, bool pdl, cudaStream_t s) {
   constexpr int P = D / kGdnRows;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.Hv * P);
   cfg.blockDim = dim3(kGdnThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = P;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, gdn_verify_kernel<D>, a);
 }
 
 cudaError_t gdn_setup_kernels() { return cudaSuccess; }
 
-cudaError_t launch_gdn(const GdnArgs& a, cudaStream_t s) {
+cudaError_t launch_gdn(const GdnArgs& a, bool pdl, cudaStream_t s) {
   switch (a.d) {
-    case 32: return launch_gdn_d<32>(a, s);
-    case 64: return launch_gdn_d<64>(a, s);
-    case 128: return launch_gdn_d<128>(a, s);
+    case 32: return launch_gdn_d<32>(a, pdl, s);
+    case 64: return launch_gdn_d<64>(a, pdl, s);
+    case 128: return launch_gdn_d<128>(a, pdl, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -237,11 +266,24 @@ cudaError_t launch_gdn(const GdnArgs& a, cudaStream_t s) {
 // out = x / sqrt(mean(x^2) + eps) * (zc ? 1 + w : w), one CTA per row.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const float* w, float eps, int zc, int n,
                                                       void* out, int dtype) {
+  constexpr int U = 8;  // loads in flight per thread
+  griddep_wait();
+  griddep_launch();
   const int r = blockIdx.x;
   const float* xr = x + (long long)r * n;
+  const int nt = blockDim.x;
   __shared__ float red[8];
   float ss = 0.f;
-  for (int c = threadIdx.x; c < n; c += blockDim.x) ss = fmaf(xr[c], xr[c], ss);
+  for (int base = 0; base < n; base += U * nt) {
+    float v[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int c = base + i * nt + threadIdx.x;
+      v[i] = c < n ? xr[c] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i) ss = fmaf(v[i], v[i], ss);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -249,18 +291,38 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const floa
   float tot = 0.f;
   for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
   const float inv = 1.f / sqrtf(tot / (float)n + eps);
-  for (int c = threadIdx.x; c < n; c += blockDim.x) {
-    const float wt = zc ? 1.f + w[c] : w[c];
-    const float v = xr[c] * inv * wt;
-    if (dtype == 1) reinterpret_cast<uint16_t*>(out)[(long long)r * n + c] = f2bf16(v);
-    else reinterpret_cast<float*>(out)[(long long)r * n + c] = v;
+  for (int base = 0; base < n; base += U * nt) {
+    float v[U], wt[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int c = base + i * nt + threadIdx.x;
+      v[i] = c < n ? xr[c] : 0.f;
+      wt[i] = c < n ? w[c] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int c = base + i * nt + threadIdx.x;
+      if (c >= n) break;
+      const float o = v[i] * inv * (zc ? 1.f + wt[i] : wt[i]);
+      if (dtype == 1) reinterpret_cast<uint16_t*>(out)[(long long)r * n + c] = f2bf16(o);
+      else reinterpret_cast<float*>(out)[(long long)r * n + c] = o;
+    }
   }
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, int n, int k, void* out, int dtype,
-                           cudaStream_t s) {
-  rmsnorm_kernel<<<k, 256, 0, s>>>(x, w, eps, zc, n, out, dtype);
-  return cudaGetLastError();
+                           bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(k);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, x, w, eps, zc, n, out, dtype);
 }
 
 }  // namespace vk

@@ -77,12 +77,15 @@ struct GdnArgs {
 
 // Launchers (return the first CUDA error; *launches counts kernels launched).
 cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm);
-cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, cudaStream_t s);
+// pdl: launch with programmatic stream serialization (the kernel may start
+// while the previous kernel on the stream runs; see griddep_wait).
+cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, bool pdl, cudaStream_t s);
 cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, const CUtensorMap& sgu_map,
-                       const CUtensorMap& sdn_map, const MoeArgs& a, int nt, cudaStream_t s, int* launches);
+                       const CUtensorMap& sdn_map, const MoeArgs& a, int nt, bool pdl, cudaStream_t s,
+                       int* launches);
 cudaError_t gdn_setup_kernels();
-cudaError_t launch_gdn(const GdnArgs& a, cudaStream_t s);
+cudaError_t launch_gdn(const GdnArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, int n, int k, void* out,
-                           int dtype, cudaStream_t s);
+                           int dtype, bool pdl, cudaStream_t s);
 
 }  // namespace vk

@@ -168,6 +168,6 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   // device error may have left them behind, so clear them (and the error word).
   if (cudaMemsetAsync(cnt, 0, (size_t)(nblocks + 1) * sizeof(int), stream) != cudaSuccess) return VERIFY_ECUDA;
   int launched = 0;
-  if (vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
+  if (vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, false, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
   return VERIFY_OK;
 }

@@ -55,6 +55,14 @@ struct Q4Layout {
   static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
 };
 
+// Where a stage holding NBL activation rows keeps them (the consumer's view).
+template <int NBL>
+struct XLayout {
+  static constexpr int NB = NBL;
+  static constexpr int W_BYTES = kBM * 128;
+  static constexpr int X_BYTES = kGroupsPerUnit * NBL * 128;
+};
+
 template <int CW>
 struct Warps {
   static constexpr int MT = kBM / 16 / CW;       // 16-row MMA tiles per consumer warp
@@ -89,47 +97,86 @@ __device__ __forceinline__ int tile_global_row(const TileSrc& t, int i) {
 
 // ---------------------------------------------------------------- producer
 
-// Fills one stage.  brow: the tile's activation row pointers (shared memory).
+// A stage is filled in three parts that all complete on its full barrier:
+// the weight tile (TMA, expected bytes), the tile's scales and biases and the
+// activation rows (cp.async, then one arrival per producer lane).  Only what
+// the consumers read is copied: scales of rows inside the matrix, activation
+// rows below nb, groups below gcount.  Anything else in the stage is stale and
+// only reaches output columns or rows that are never stored (an MMA column
+// depends on its own activation row alone).
+
+// Weight tile.  Reads only static data.
 template <int NT>
-__device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_bar, const TileSrc& t, int kc,
-                                              int gcount, const uint16_t* const* brow, int nb, int lane) {
+__device__ __forceinline__ void produce_tma(uint8_t* stage_ptr, uint32_t full_bar, const TileSrc& t, int kc) {
   using L = Q4Layout<NT>;
   const uint32_t w_dst = smem_addr(stage_ptr);
-  const uint32_t x_dst = w_dst + L::W_BYTES;
-  const uint32_t sb_dst = x_dst + L::X_BYTES;
-  if (lane == 0) {
-    mbar_arrive_expect_tx(full_bar, L::W_BYTES);
-    if (t.two_boxes) {
-      tma_load_2d(w_dst, t.map, full_bar, kc * 32, t.y0);
-      tma_load_2d(w_dst + 64 * 128, t.map, full_bar, kc * 32, t.y1);
-    } else {
-      tma_load_2d(w_dst, t.map, full_bar, kc * 32, t.y0);
+  mbar_arrive_expect_tx(full_bar, L::W_BYTES);
+  if (t.two_boxes) {
+    tma_load_2d(w_dst, t.map, full_bar, kc * 32, t.y0);
+    tma_load_2d(w_dst + 64 * 128, t.map, full_bar, kc * 32, t.y1);
+  } else {
+    tma_load_2d(w_dst, t.map, full_bar, kc * 32, t.y0);
+  }
+}
+
+// Scales and biases of the tile's rows, four groups per row: one 8-byte copy
+// per row and array when a row's groups are 8-byte aligned (K % 256 == 0),
+// else two 4-byte copies.
+template <int NT>
+__device__ __forceinline__ void produce_sb(uint8_t* stage_ptr, const TileSrc& t, int kc, int gcount, int lane) {
+  using L = Q4Layout<NT>;
+  const uint32_t sb_dst = smem_addr(stage_ptr) + L::W_BYTES + L::X_BYTES;
+  const int e0 = 4 * kc;
+  if ((t.KG & 3) == 0) {
+#pragma unroll
+    for (int idx = lane; idx < 2 * kBM; idx += 32) {
+      const int arr = idx >> 7;
+      const int row = idx & (kBM - 1);
+      const int gr = tile_global_row(t, row);
+      if (gr >= 0) cp_async8(sb_dst + arr * (kBM * 8) + row * 8, (arr ? t.biases : t.scales) + (long long)gr * t.KG + e0);
+    }
+  } else {
+#pragma unroll
+    for (int idx = lane; idx < 2 * kBM * 2; idx += 32) {
+      const int arr = idx >> 8;
+      const int row = (idx >> 1) & (kBM - 1);
+      const int word = idx & 1;
+      const int gr = tile_global_row(t, row);
+      if (gr >= 0 && 2 * word < gcount)
+        cp_async4(sb_dst + arr * (kBM * 8) + row * 8 + word * 4,
+                  (arr ? t.biases : t.scales) + (long long)gr * t.KG + e0 + 2 * word, 4u);
     }
   }
-  // scales / biases: 128 rows x 2 words (4 groups) per array
-  const int e0 = 4 * kc;
-#pragma unroll
-  for (int idx = lane; idx < 2 * kBM * 2; idx += 32) {
-    const int arr = idx >> 8;
-    const int row = (idx >> 1) & (kBM - 1);
-    const int word = idx & 1;
-    const int gr = tile_global_row(t, row);
-    const bool valid = gr >= 0 && 2 * word < gcount;
-    const uint16_t* base = arr ? t.biases : t.scales;
-    const uint16_t* src = valid ? base + (long long)gr * t.KG + e0 + 2 * word : base;
-    cp_async4(sb_dst + arr * (kBM * 8) + row * 8 + word * 4, src, valid ? 4u : 0u);
-  }
-  // activation rows: [group][row][8 chunks of 16 B], chunk index xor (row & 7)
+}
+
+// Activation rows b < nb (brow: their pointers, in shared memory), then this
+// lane's arrival once all its copies have landed.
+template <int NT>
+__device__ __forceinline__ void produce_x(uint8_t* stage_ptr, uint32_t full_bar, int kc, int gcount,
+                                          const uint16_t* const* brow, int nb, int lane) {
+  using L = Q4Layout<NT>;
+  const uint32_t x_dst = smem_addr(stage_ptr) + L::W_BYTES;
+  // [group][row][8 chunks of 16 B], chunk index xor (row & 7)
 #pragma unroll
   for (int idx = lane; idx < L::NB * 32; idx += 32) {
     const int b = idx >> 5;
+    if (b >= nb) break;
     const int G = (idx >> 3) & 3;
     const int ch = idx & 7;
-    const bool valid = b < nb && G < gcount;
-    const uint16_t* src = valid ? brow[b] + kc * 256 + G * 64 + ch * 8 : brow[0];
-    cp_async16(x_dst + G * (L::NB * 128) + b * 128 + ((ch ^ (b & 7)) << 4), src, valid ? 16u : 0u);
+    if (G < gcount)
+      cp_async16(x_dst + G * (L::NB * 128) + b * 128 + ((ch ^ (b & 7)) << 4), brow[b] + kc * 256 + G * 64 + ch * 8,
+                 16u);
   }
   cp_async_mbar_arrive_noinc(full_bar);
+}
+
+// Fills one stage.
+template <int NT>
+__device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_bar, const TileSrc& t, int kc,
+                                              int gcount, const uint16_t* const* brow, int nb, int lane) {
+  if (lane == 0) produce_tma<NT>(stage_ptr, full_bar, t, kc);
+  produce_sb<NT>(stage_ptr, t, kc, gcount, lane);
+  produce_x<NT>(stage_ptr, full_bar, kc, gcount, brow, nb, lane);
 }
 
 // On abort the producer keeps the CTA alive until its TMA writes have landed.
@@ -145,12 +192,14 @@ __device__ __forceinline__ void producer_drain(uint32_t bar_base, long long fill
 
 // ---------------------------------------------------------------- consumer
 
-// Accumulates group G of a stage into acc for this warp's MT row tiles.
-template <int NT, int MT>
+// Accumulates group G of a stage into acc for this warp's MT row tiles: NT
+// MMA column blocks (activation rows 0 .. 8 NT - 1) of a stage laid out for
+// NBL activation rows.
+template <int NT, int MT, int NBL>
 __device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, uint32_t sx_src, int G,
                                               const uint2 (&sw)[MT][2], const uint2 (&bw)[MT][2],
                                               const int (&rbase)[MT], int lane, float (&acc)[MT][NT][4]) {
-  using L = Q4Layout<NT>;
+  using L = XLayout<NBL>;
   const int g = lane >> 2, c = lane & 3;
   // B fragments: activation row 8t+g, columns 16c .. 16c+15 of the group
   uint32_t bf[NT][8];
@@ -222,13 +271,15 @@ __device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, ui
   }
 }
 
-// Accumulates one stage (gcount groups).  ok = false: the stage never filled
+// Accumulates one stage (gcount groups) for NT MMA column blocks; the stage
+// holds NBL activation rows (NBL >= 8 NT).  ok = false: the stage never filled
 // (abort) - keep the named-barrier count, skip the math.
-template <int NT, int CW>
+template <int NT, int CW, int NBL>
 __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t sx_src, int gcount,
                                               const int (&rbase)[Warps<CW>::MT], int lane,
                                               float (&acc)[Warps<CW>::MT][NT][4], bool ok) {
-  using L = Q4Layout<NT>;
+  static_assert(NBL >= 8 * NT, "stage holds too few activation rows");
+  using L = XLayout<NBL>;
   constexpr int MT = Warps<CW>::MT;
   const uint32_t w_src = smem_addr(stage_ptr);
   const uint32_t x_src = w_src + L::W_BYTES;
@@ -280,10 +331,10 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t
   if (gcount == kGroupsPerUnit) {
 #pragma unroll
     for (int G = 0; G < kGroupsPerUnit; ++G)
-      consume_group<NT, MT>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
+      consume_group<NT, MT, NBL>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
   } else {
 #pragma unroll 1
-    for (int G = 0; G < gcount; ++G) consume_group<NT, MT>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
+    for (int G = 0; G < gcount; ++G) consume_group<NT, MT, NBL>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
   }
 }
 
@@ -353,8 +404,20 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     ts.map = &wmap; ts.y0 = tile * kBM; ts.y1 = 0; ts.two_boxes = 0;
     ts.row_limit = a.N; ts.mat_row0 = tile * kBM;
     ts.scales = a.scales; ts.biases = a.biases; ts.KG = a.KG;
-    long long fills = 0;
-    for (int kc = kc0; kc < kc1; ++kc, ++fills) {
+    // The first stages' weights are static: fetch them before the previous
+    // kernel has finished (the ring is empty, no wait), the activations after.
+    const int n_pre = min(kStages, kc1 - kc0);
+    if (lane == 0)
+      for (int f = 0; f < n_pre; ++f) produce_tma<NT>(smem + f * L::STAGE, bar_base + 8 * f, ts, kc0 + f);
+    griddep_wait();
+    griddep_launch();
+    for (int f = 0; f < n_pre; ++f) {
+      const int gcount = min(kGroupsPerUnit, a.KG - 4 * (kc0 + f));
+      produce_sb<NT>(smem + f * L::STAGE, ts, kc0 + f, gcount, lane);
+      produce_x<NT>(smem + f * L::STAGE, bar_base + 8 * f, kc0 + f, gcount, brow, a.k, lane);
+    }
+    long long fills = n_pre;
+    for (int kc = kc0 + n_pre; kc < kc1; ++kc, ++fills) {
       const int s = (int)(fills % kStages);
       const uint32_t ph = (uint32_t)((fills / kStages) & 1);
       if (!mbar_wait(bar_base + 8 * (kStages + s), ph ^ 1, abort, a.err)) break;
@@ -370,6 +433,8 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
   }
 
   // -------------------------------------------------------------- consumers
+  griddep_wait();
+  griddep_launch();
   const int g = lane >> 2, c = lane & 3;
   int rbase[MT];
 #pragma unroll
@@ -382,8 +447,8 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     const uint32_t ph = (uint32_t)((fills / kStages) & 1);
     const bool ok = mbar_wait(bar_base + 8 * s, ph, abort, a.err);
     const int gcount = min(kGroupsPerUnit, a.KG - 4 * kc);
-    consume_stage<NT, CW>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase, lane,
-                          acc, ok);
+    consume_stage<NT, CW, L::NB>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
+                                 lane, acc, ok);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
   }
@@ -446,7 +511,7 @@ __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = lane + 32 * i;
-      v[i] = e < a.E ? l[e] : 0.f;
+      v[i] = e < a.E ? __ldcg(l + e) : 0.f;  // L2: may precede the grid dependency wait
     }
     uint32_t taken = 0;
     float myv = 0.f;
@@ -515,10 +580,125 @@ __device__ __forceinline__ int pairs_of(const RouteSmem* rs, const MoeArgs& a, i
   return u >= rs->U ? a.k : __popc(rs->mask[rs->ulist[u]]);
 }
 
+// y[r][n] of the routed experts in rank order (partials v[j]), then the gated
+// shared expert (partial vs).
+__device__ __forceinline__ void combine_row(const MoeArgs& a, const RouteSmem* rs, int r,
+                                            const float (&v)[kMaxTopK], float vs, int n) {
+  float y = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < a.T) y = fmaf(rs->w[r * kMaxTopK + j], v[j], y);
+  if (a.has_shared) {
+    const float sg = a.shared_logit[(long long)r * a.logits_ld];
+    const float gate = 1.f / (1.f + expf(-sg));
+    y = fmaf(gate, vs, y);
+  }
+  store_out(a.y, a.dtype, (long long)r * a.H + n, y);
+}
+
+// One item of a MoE kernel on the consumer side: the stage loop and the
+// epilogue.  NTC MMA column blocks are computed on stages laid out for NTL.
+template <int NTC, int NTL, int CW, bool GATEUP>
+__device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, uint8_t* smem, uint32_t bar_base,
+                                         volatile int* abort, volatile int* bcast, int u, int tile, int nb, int KC,
+                                         int KG, int TS, int n_experts, const int (&rbase)[Warps<CW>::MT], int lane,
+                                         long long& fills) {
+  using L = Q4Layout<NTL>;
+  constexpr int MT = Warps<CW>::MT;
+  const int warp = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
+  float acc[MT][NTC][4];
+  zero_acc<MT, NTC>(acc);
+  for (int kc = 0; kc < KC; ++kc, ++fills) {
+    const int s = (int)(fills % kStages);
+    const uint32_t ph = (uint32_t)((fills / kStages) & 1);
+    const bool ok = mbar_wait(bar_base + 8 * s, ph, abort, a.err);
+    const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
+    consume_stage<NTC, CW, L::NB>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
+                                  lane, acc, ok);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
+  }
+  // pair ids of this thread's columns
+  long long pid[NTC][2];
+#pragma unroll
+  for (int t = 0; t < NTC; ++t)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int b = 8 * t + 2 * c + q;
+      int r = 0, j = 0;
+      if (b < nb) pair_of(rs, a, u, b, r, j);
+      pid[t][q] = b < nb ? (long long)r * TS + j : -1;
+    }
+  if (GATEUP) {
+    if (*abort) return;
+#pragma unroll
+    for (int t = 0; t < NTC; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long long p = pid[t][q & 1];
+        if (p < 0) continue;
+        const int i = 64 * tile + 16 * warp + g + 8 * (q >> 1);
+        const float gate = acc[0][t][q], up = acc[MT - 1][t][q];
+        const float h = gate / (1.f + expf(-gate)) * up;
+        a.hbuf[p * a.I + i] = f2bf16(h);
+      }
+  } else {
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int t = 0; t < NTC; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const long long p = pid[t][q & 1];
+          const int n = kBM * tile + rbase[m] + g + 8 * (q >> 1);
+          if (p >= 0 && n < a.H) a.part[p * a.H + n] = acc[m][t][q];
+        }
+    __threadfence();
+    named_bar(1, CW * 32);
+    if (threadIdx.x == 0) {
+      int last = 0;
+      if (!*abort) {
+        const int old = atomicAdd(a.cnt + tile, 1);
+        last = (old == n_experts - 1);
+        if (last) atomicExch(a.cnt + tile, 0);
+      }
+      *bcast = last;
+    }
+    named_bar(1, CW * 32);
+    if (*bcast) {
+      __threadfence();
+      const int n = kBM * tile + threadIdx.x;
+      if (threadIdx.x < kBM && n < a.H) {
+        // All partials of two rows are loaded before any is used (they are
+        // independent L2 reads); the sum itself runs in rank order.
+        for (int r0 = 0; r0 < a.k; r0 += 2) {
+          const bool two = r0 + 1 < a.k;
+          const float* p0 = a.part + (long long)r0 * TS * a.H + n;
+          const float* p1 = p0 + (long long)TS * a.H;
+          float v0[kMaxTopK], v1[kMaxTopK];
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j) {
+            v0[j] = j < a.T ? __ldcg(p0 + (long long)j * a.H) : 0.f;
+            v1[j] = (two && j < a.T) ? __ldcg(p1 + (long long)j * a.H) : 0.f;
+          }
+          const float s0 = a.has_shared ? __ldcg(p0 + (long long)a.T * a.H) : 0.f;
+          const float s1 = (two && a.has_shared) ? __ldcg(p1 + (long long)a.T * a.H) : 0.f;
+          combine_row(a, rs, r0, v0, s0, n);
+          if (two) combine_row(a, rs, r0 + 1, v1, s1, n);
+        }
+      }
+      named_bar(1, CW * 32);
+    }
+  }
+}
+
 // GATEUP: items (expert, 64 rows of I): gate rows and up rows of the same i
 // go to the same warp (its two MMA tiles), the epilogue applies SwiGLU and
 // writes h (bf16).  Down: items (expert, 128 rows of H); partial outputs per
 // (row, rank) go to scratch and the last CTA of a 128-row block combines them.
+// Items are expert-major: consecutive CTAs stream consecutive slices of one
+// expert (measured much faster than block-major order, which spreads the
+// concurrent reads over all selected experts).
 template <int NT, bool GATEUP>
 __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS, kQ4CtasPerSm)
     moe_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap smap, const MoeArgs a) {
@@ -533,6 +713,13 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
   RouteSmem* rs = reinterpret_cast<RouteSmem*>(smem + L::BASE_BYTES);
   if (threadIdx.x == 0) { *abort = 0; *bcast = 0; }
   init_barriers<CW>(bar_base);
+  // Gate/up routes from logits the previous kernel wrote: wait first.  The
+  // down kernel's logits are two kernels old, so it routes (and fetches its
+  // first weights) before waiting for the gate/up kernel's h rows.
+  if (GATEUP) {
+    griddep_wait();
+    griddep_launch();
+  }
   route_rows(a, rs);  // ends with __syncthreads
 
   const int TS = a.T + a.has_shared;
@@ -554,6 +741,7 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
     if (lane == 0) { tma_prefetch_desc(&map); if (a.has_shared) tma_prefetch_desc(&smap); }
     const uint16_t** brow = reinterpret_cast<const uint16_t**>(smem + L::MISC_OFF + 64);
     long long fills = 0;
+    bool waited = GATEUP;
     for (int item = blockIdx.x; item < n_items && !*abort; item += a.G) {
       const int u = item / ntiles, tile = item % ntiles;
       const bool shared = u >= rs->U;
@@ -584,7 +772,23 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
         ts.scales = shared ? a.sdn_scales : a.dn_scales;
         ts.biases = shared ? a.sdn_biases : a.dn_biases;
       }
-      for (int kc = 0; kc < KC; ++kc, ++fills) {
+      int kc = 0;
+      if (!waited) {  // first item of the down kernel: its weights before the wait
+        waited = true;
+        const int n_pre = min(kStages, KC);
+        if (lane == 0)
+          for (int f = 0; f < n_pre; ++f) produce_tma<NT>(smem + f * L::STAGE, bar_base + 8 * f, ts, f);
+        griddep_wait();
+        griddep_launch();
+        for (int f = 0; f < n_pre; ++f) {
+          const int gcount = min(kGroupsPerUnit, KG - 4 * f);
+          produce_sb<NT>(smem + f * L::STAGE, ts, f, gcount, lane);
+          produce_x<NT>(smem + f * L::STAGE, bar_base + 8 * f, f, gcount, brow, nb, lane);
+        }
+        kc = n_pre;
+        fills = n_pre;
+      }
+      for (; kc < KC; ++kc, ++fills) {
         const int s = (int)(fills % kStages);
         const uint32_t ph = (uint32_t)((fills / kStages) & 1);
         if (!mbar_wait(bar_base + 8 * (kStages + s), ph ^ 1, abort, a.err)) break;
@@ -592,12 +796,19 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
         produce_stage<NT>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, gcount, brow, nb, lane);
       }
     }
+    if (!waited) {
+      griddep_wait();
+      griddep_launch();
+    }
     if (*abort) producer_drain(bar_base, fills);
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  const int g = lane >> 2, c = lane & 3;
+  if (!GATEUP) {
+    griddep_wait();
+    griddep_launch();
+  }
   int rbase[MT];
   if (GATEUP) { rbase[0] = 16 * warp; rbase[MT - 1] = 64 + 16 * warp; }
   else {
@@ -608,84 +819,13 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
   for (int item = blockIdx.x; item < n_items; item += a.G) {
     const int u = item / ntiles, tile = item % ntiles;
     const int nb = pairs_of(rs, a, u);
-    float acc[MT][NT][4];
-    zero_acc<MT, NT>(acc);
-    for (int kc = 0; kc < KC; ++kc, ++fills) {
-      const int s = (int)(fills % kStages);
-      const uint32_t ph = (uint32_t)((fills / kStages) & 1);
-      const bool ok = mbar_wait(bar_base + 8 * s, ph, abort, a.err);
-      const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
-      consume_stage<NT, CW>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
-                            lane, acc, ok);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
-    }
-    // pair ids of this thread's columns
-    long long pid[NT][2];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int b = 8 * t + 2 * c + q;
-        int r = 0, j = 0;
-        if (b < nb) pair_of(rs, a, u, b, r, j);
-        pid[t][q] = b < nb ? (long long)r * TS + j : -1;
-      }
-    if (GATEUP) {
-      if (*abort) continue;
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const long long p = pid[t][q & 1];
-          if (p < 0) continue;
-          const int i = 64 * tile + 16 * warp + g + 8 * (q >> 1);
-          const float gate = acc[0][t][q], up = acc[MT - 1][t][q];
-          const float h = gate / (1.f + expf(-gate)) * up;
-          a.hbuf[p * a.I + i] = f2bf16(h);
-        }
-    } else {
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const long long p = pid[t][q & 1];
-            const int n = kBM * tile + rbase[m] + g + 8 * (q >> 1);
-            if (p >= 0 && n < a.H) a.part[p * a.H + n] = acc[m][t][q];
-          }
-      __threadfence();
-      named_bar(1, CW * 32);
-      if (threadIdx.x == 0) {
-        int last = 0;
-        if (!*abort) {
-          const int old = atomicAdd(a.cnt + tile, 1);
-          last = (old == n_experts - 1);
-          if (last) atomicExch(a.cnt + tile, 0);
-        }
-        *bcast = last;
-      }
-      named_bar(1, CW * 32);
-      if (*bcast) {
-        __threadfence();
-        const int n = kBM * tile + threadIdx.x;
-        if (threadIdx.x < kBM && n < a.H) {
-          for (int r = 0; r < a.k; ++r) {
-            float y = 0.f;
-            for (int j = 0; j < a.T; ++j)
-              y = fmaf(rs->w[r * kMaxTopK + j], __ldcg(a.part + ((long long)r * TS + j) * a.H + n), y);
-            if (a.has_shared) {
-              const float sg = a.shared_logit[(long long)r * a.logits_ld];
-              const float gate = 1.f / (1.f + expf(-sg));
-              y = fmaf(gate, __ldcg(a.part + ((long long)r * TS + a.T) * a.H + n), y);
-            }
-            store_out(a.y, a.dtype, (long long)r * a.H + n, y);
-          }
-        }
-        named_bar(1, CW * 32);
-      }
-    }
+    // Most routed experts get few rows: one MMA column block then suffices.
+    if (NT == 2 && nb <= 8)
+      moe_item<1, NT, CW, GATEUP>(a, rs, smem, bar_base, abort, bcast, u, tile, nb, KC, KG, TS, n_experts, rbase,
+                                  lane, fills);
+    else
+      moe_item<NT, NT, CW, GATEUP>(a, rs, smem, bar_base, abort, bcast, u, tile, nb, KC, KG, TS, n_experts, rbase,
+                                   lane, fills);
   }
 }
 
@@ -728,34 +868,53 @@ cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm) {
   return cudaSuccess;
 }
 
-cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, cudaStream_t s) {
+cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.RB * a.S);
   cfg.blockDim = dim3(Warps<kDenseWarps>::THREADS);
   cfg.dynamicSmemBytes = nt == 1 ? dense_smem<1>() : dense_smem<2>();
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = a.S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   if (nt == 1) return cudaLaunchKernelEx(&cfg, q4_dense_kernel<1>, wmap, a);
   return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2>, wmap, a);
 }
 
+template <int NT, bool GATEUP>
+static cudaError_t launch_moe_one(const CUtensorMap& map, const CUtensorMap& smap, const MoeArgs& a, bool pdl,
+                                  cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.G);
+  cfg.blockDim = dim3(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS);
+  cfg.dynamicSmemBytes = moe_smem<NT>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, moe_kernel<NT, GATEUP>, map, smap, a);
+}
+
+// The down kernel always follows the gate/up kernel of the same call, which
+// started after everything the caller enqueued before it (or, with pdl, after
+// the kernel before it): it may overlap the gate/up kernel's tail.
 cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, const CUtensorMap& sgu_map,
-                       const CUtensorMap& sdn_map, const MoeArgs& a, int nt, cudaStream_t s, int* launches) {
-  constexpr int TG = Warps<kGateUpWarps>::THREADS, TDN = Warps<kDownWarps>::THREADS;
-  if (nt == 1) moe_kernel<1, true><<<a.G, TG, moe_smem<1>(), s>>>(gu_map, sgu_map, a);
-  else moe_kernel<2, true><<<a.G, TG, moe_smem<2>(), s>>>(gu_map, sgu_map, a);
-  cudaError_t e = cudaGetLastError();
+                       const CUtensorMap& sdn_map, const MoeArgs& a, int nt, bool pdl, cudaStream_t s,
+                       int* launches) {
+  cudaError_t e = nt == 1 ? launch_moe_one<1, true>(gu_map, sgu_map, a, pdl, s)
+                          : launch_moe_one<2, true>(gu_map, sgu_map, a, pdl, s);
   if (e) return e;
   ++*launches;
-  if (nt == 1) moe_kernel<1, false><<<a.G, TDN, moe_smem<1>(), s>>>(dn_map, sdn_map, a);
-  else moe_kernel<2, false><<<a.G, TDN, moe_smem<2>(), s>>>(dn_map, sdn_map, a);
-  e = cudaGetLastError();
+  e = nt == 1 ? launch_moe_one<1, false>(dn_map, sdn_map, a, true, s)
+              : launch_moe_one<2, false>(dn_map, sdn_map, a, true, s);
   if (!e) ++*launches;
   return e;
 }

@@ -28,6 +28,9 @@ struct verify_ctx {
   int64_t launches = 0;
   cudaEvent_t layer_events[8] = {};
   int n_layer_events = 0;
+  // Set only inside verify_layer_k: the next launch may start while the
+  // kernel before it on the stream still runs (programmatic dependent launch).
+  bool pdl = false;
   char msg[512] = {0};
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
@@ -227,7 +230,7 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W, const uint16_
   a.S = dense_splits(ctx, a.RB, a.KC);
   CUtensorMap map;
   if ((s = make_wmap(ctx, &map, W->packed, (uint64_t)a.N, (uint64_t)a.K / 8, vk::kBM))) return s;
-  cudaError_t e = vk::launch_q4_dense(map, a, k <= 8 ? 1 : 2, stream);
+  cudaError_t e = vk::launch_q4_dense(map, a, k <= 8 ? 1 : 2, ctx->pdl, stream);
   if (e) return cuda_fail(ctx, e, "q4_qmv_k launch");
   ctx->launches += 1;
   return VERIFY_OK;
@@ -298,7 +301,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   a.has_shared = n_shared ? 1 : 0;
   a.G = ctx->moe_ctas_per_sm * ctx->num_sms;
   int launched = 0;
-  cudaError_t e = vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, stream, &launched);
+  cudaError_t e = vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, ctx->pdl, stream, &launched);
   ctx->launches += launched;
   if (e) return cuda_fail(ctx, e, "q4_gather_experts_k launch");
   return VERIFY_OK;
@@ -355,7 +358,7 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p, verify_g
   a.o = o; a.err = ctx->err;
   a.Hk = Hk; a.Hv = Hv; a.d = d; a.W = p->conv_kernel; a.k = k; a.dtype = dtype_out; a.gate_act = p->gate_act;
   a.q_scale = p->q_scale; a.l2_eps = p->l2_eps; a.norm_eps = p->norm_eps;
-  cudaError_t e = vk::launch_gdn(a, stream);
+  cudaError_t e = vk::launch_gdn(a, ctx->pdl, stream);
   if (e) return cuda_fail(ctx, e, "gdn_verify_k launch");
   ctx->launches += 1;
   for (int r = 0; r <= k; ++r) st->pending[r] = pending[r];
@@ -383,7 +386,7 @@ verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w, 
   if ((s = check_dev(ctx, x, 4, "x")) || (s = check_dev(ctx, w, 4, "w")) ||
       (s = check_dev(ctx, out, dtype_out == VERIFY_BF16 ? 2 : 4, "out")))
     return s;
-  cudaError_t e = vk::launch_rmsnorm(x, w, eps, zero_centered, n, k, out, dtype_out, stream);
+  cudaError_t e = vk::launch_rmsnorm(x, w, eps, zero_centered, n, k, out, dtype_out, ctx->pdl, stream);
   if (e) return cuda_fail(ctx, e, "verify_rmsnorm_k launch");
   ctx->launches += 1;
   return VERIFY_OK;
@@ -412,13 +415,24 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
     if (ctx->n_layer_events == 8 && ctx->layer_events[i])
       cudaEventRecordWithFlags(ctx->layer_events[i], sm, cudaEventRecordExternal);
   };
+  // The layer's first kernel waits for everything enqueued before the call;
+  // each later one may start during its predecessor's tail, unless an event is
+  // recorded between the two.
+  struct PdlOff {
+    verify_ctx* c;
+    ~PdlOff() { c->pdl = false; }
+  } pdl_off{ctx};
+  auto overlap_after = [&](int i) { ctx->pdl = !(ctx->n_layer_events == 8 && ctx->layer_events[i]); };
   mark(0);
+  ctx->pdl = false;
   // 1. pre-mixer norm
   if ((s = verify_rmsnorm_k(ctx, h, L->norm1_w, L->norm_eps, 1, H, k, ctx->st_xn, VERIFY_BF16, sm))) return s;
   mark(1);
+  overlap_after(1);
   // 2. in_proj -> q|k|v, z, a, b
   if ((s = q4_qmv_k(ctx, &L->in_proj, ctx->st_xn, k, ctx->st_proj, VERIFY_BF16, sm))) return s;
   mark(2);
+  overlap_after(2);
   // 3. Gated DeltaNet verify
   verify_gdn_inputs in;
   in.qkv = ctx->st_proj; in.ld_qkv = NP;
@@ -427,15 +441,19 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
   in.b = ctx->st_proj + C + Z + g.n_v_heads; in.ld_b = NP;
   if ((s = gdn_verify_k(ctx, &L->gdn, st, &in, k, ctx->st_o, VERIFY_BF16, sm))) return s;
   mark(3);
+  overlap_after(3);
   // 4. out_proj into the residual
   if ((s = q4_qmv_k(ctx, &L->out_proj, ctx->st_o, k, h, VERIFY_F32_ADD, sm))) return s;
   mark(4);
+  overlap_after(4);
   // 5. pre-FFN norm
   if ((s = verify_rmsnorm_k(ctx, h, L->norm2_w, L->norm_eps, 1, H, k, ctx->st_xn, VERIFY_BF16, sm))) return s;
   mark(5);
+  overlap_after(5);
   // 6. router + shared-expert gate logits
   if ((s = q4_qmv_k(ctx, &L->router, ctx->st_xn, k, ctx->st_logits, VERIFY_F32, sm))) return s;
   mark(6);
+  overlap_after(6);
   // 7. routed + shared experts into the residual
   if ((s = q4_gather_experts_k(ctx, &L->gate_up, &L->down, ctx->st_logits, E + 1, L->top_k, ctx->st_xn, k,
                                idx_out ? idx_out : ctx->st_idx, ctx->st_w, h, VERIFY_F32_ADD, &L->shared_gate_up,
