@@ -186,7 +186,7 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W,
  * Limits: E <= 512, 1 <= T <= 16, 256 <= H <= 8192, 256 <= I <= 4096,
  * H % 128 == I % 128 == 0.
  * Expert weights are read once per call for every distinct selected expert
- * (the union of the rows' routes).
+ * (the union of the rows' routes).  Three kernel launches on `stream`.
  */
 verify_status q4_gather_experts_k(verify_ctx* ctx,
                                   const verify_q4_experts* gate_up,
@@ -318,7 +318,7 @@ verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w,
  *   h  += q4_gather_experts_k(gate_up, down, l[:, :E], top_k, xn2,
  *                             shared_gate_up, shared_down, l[:, E])
  * idx_out (optional, device int32 [k, top_k]) receives the routed expert
- * indices.  Eight kernel launches on `stream`, no host synchronisation.  Scratch
+ * indices.  Nine kernel launches on `stream`, no host synchronisation.  Scratch
  * activations live in the context (limits: k <= 16, H <= 8192, in_proj rows
  * <= 32768, E + 1 <= 1024).  Weight shapes must match: in_proj [C + Hv*dv +
  * 2*Hv, H], out_proj [H, Hv*dv], router [E + 1, H], gate_up [E, 2I, H],
@@ -368,18 +368,18 @@ verify_status verify_set_layer_events(verify_ctx* ctx, void* const* events, int 
  * arguments (no ctx) plus `device_error`: an optional device int32 the caller
  * owns, set to 1 if a pipeline wait timed out (NULL: not reported).  The
  * caller passes all inputs and outputs; the kernels' scratch (SwiGLU rows,
- * per-rank partial outputs, arrival counters) lives in one array of
+ * per-rank partial outputs, an error word) lives in one array of
  * VERIFY_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
  * that loads the library holds until the process exits.
  *   - Limit: k*(T+s)*I*2 + k*(T+s)*H*4 bytes (s = 1 with a shared expert, each
- *     part rounded up to 256) plus 4*(ceil(H/128)+1) must fit the array;
- *     larger calls return VERIFY_EUNSUPPORTED before anything is enqueued.
+ *     part rounded up to 256) plus 256 must fit the array; larger calls
+ *     return VERIFY_EUNSUPPORTED before anything is enqueued.
  *   - The first call on each device sets that device up (resolves the array's
  *     device address, sets the kernels' launch attributes); make that first
  *     call before any stream capture.
  *   - Every call on a device shares the array, which keeps the last call's
- *     contents; the call clears the parts that must start at zero (arrival
- *     counters, error word) on `stream` before its kernels.  Calls whose work
+ *     contents; the call clears what must start at zero (the error word, when
+ *     device_error is NULL) on `stream` before its kernels.  Calls whose work
  *     overlaps on the GPU (different streams, no ordering) race on it.
  * The calling thread's current device is used.
  */

@@ -46,7 +46,6 @@ struct MoeArgs {
   const uint16_t* sdn_biases;
   uint16_t* hbuf;             // scratch [k, TS, I] bf16 (TS = T + has_shared)
   float* part;                // scratch [k, TS, H] fp32
-  int* cnt;                   // scratch: one counter per 128-row block of H
   int32_t* idx_out;
   float* w_out;
   void* y;

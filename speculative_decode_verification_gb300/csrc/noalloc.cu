@@ -11,8 +11,7 @@
 namespace {
 
 // Scratch of the routed-expert kernels: SwiGLU rows [k, T+1, I] bf16, per-rank
-// partial outputs [k, T+1, H] fp32, one arrival counter per 128 outputs, and
-// an error word.  Every GPU that loads the library holds it until the process
+// partial outputs [k, T+1, H] fp32 and an error word.  Every GPU that loads the library holds it until the process
 // exits.  All calls on one device share it.
 constexpr size_t kScratchBytes = VERIFY_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
@@ -126,14 +125,12 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   }
   // ---- carve the fixed scratch; reject what does not fit
   const int TS = top_k + (n_shared ? 1 : 0);
-  const int nblocks = (H + vk::kBM - 1) / vk::kBM;
   const size_t hbuf_bytes = round256((size_t)k * TS * I * sizeof(uint16_t));
   const size_t part_bytes = round256((size_t)k * TS * H * sizeof(float));
-  const size_t cnt_bytes = round256((size_t)nblocks * sizeof(int) + sizeof(int));
-  if (hbuf_bytes + part_bytes + cnt_bytes > kScratchBytes) return VERIFY_EUNSUPPORTED;
+  const size_t err_bytes = 256;
+  if (hbuf_bytes + part_bytes + err_bytes > kScratchBytes) return VERIFY_EUNSUPPORTED;
   unsigned char* base = d->scratch;
-  int* cnt = reinterpret_cast<int*>(base + hbuf_bytes + part_bytes);
-  int* err_word = cnt + nblocks;
+  int* err_word = reinterpret_cast<int*>(base + hbuf_bytes + part_bytes);
 
   CUtensorMap gu, dn, sgu, sdn;
   if (!encode(&gu, gate_up->w.packed, (uint64_t)E * 2 * I, (uint64_t)H / 8, 64) ||
@@ -158,15 +155,14 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   }
   a.hbuf = reinterpret_cast<uint16_t*>(base);
   a.part = reinterpret_cast<float*>(base + hbuf_bytes);
-  a.cnt = cnt;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y;
   a.err = device_error ? device_error : err_word;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
   a.G = d->moe_ctas_per_sm * d->num_sms;
-  // The arrival counters must start at zero: a previous call that stopped on a
-  // device error may have left them behind, so clear them (and the error word).
-  if (cudaMemsetAsync(cnt, 0, (size_t)(nblocks + 1) * sizeof(int), stream) != cudaSuccess) return VERIFY_ECUDA;
+  // The error word must start at zero: a previous call may have stopped on a
+  // device error and left it set.
+  if (!device_error && cudaMemsetAsync(err_word, 0, sizeof(int), stream) != cudaSuccess) return VERIFY_ECUDA;
   int launched = 0;
   if (vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, false, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
   return VERIFY_OK;

@@ -32,8 +32,8 @@
 //    block cluster and add their partial tiles through distributed shared
 //    memory in rank order (no global scratch, no atomics).
 //  * Routed MoE: items = (distinct expert, row tile) with the full K per item.
-//    The down kernel's last CTA to finish a 128-output block (an arrival
-//    counter, no waiting) combines the experts of every row in rank order.
+//    The down kernel writes one partial output per (row, rank); a small third
+//    kernel combines every row's experts in rank order.
 #include "common.cuh"
 #include "internal.h"
 
@@ -580,27 +580,11 @@ __device__ __forceinline__ int pairs_of(const RouteSmem* rs, const MoeArgs& a, i
   return u >= rs->U ? a.k : __popc(rs->mask[rs->ulist[u]]);
 }
 
-// y[r][n] of the routed experts in rank order (partials v[j]), then the gated
-// shared expert (partial vs).
-__device__ __forceinline__ void combine_row(const MoeArgs& a, const RouteSmem* rs, int r,
-                                            const float (&v)[kMaxTopK], float vs, int n) {
-  float y = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j)
-    if (j < a.T) y = fmaf(rs->w[r * kMaxTopK + j], v[j], y);
-  if (a.has_shared) {
-    const float sg = a.shared_logit[(long long)r * a.logits_ld];
-    const float gate = 1.f / (1.f + expf(-sg));
-    y = fmaf(gate, vs, y);
-  }
-  store_out(a.y, a.dtype, (long long)r * a.H + n, y);
-}
-
 // One item of a MoE kernel on the consumer side: the stage loop and the
 // epilogue.  NTC MMA column blocks are computed on stages laid out for NTL.
 template <int NTC, int NTL, int CW, bool GATEUP>
 __device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, uint8_t* smem, uint32_t bar_base,
-                                         volatile int* abort, volatile int* bcast, int u, int tile, int nb, int KC,
+                                         volatile int* abort, int u, int tile, int nb, int KC,
                                          int KG, int TS, int n_experts, const int (&rbase)[Warps<CW>::MT], int lane,
                                          long long& fills) {
   using L = Q4Layout<NTL>;
@@ -653,49 +637,40 @@ __device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, 
           const int n = kBM * tile + rbase[m] + g + 8 * (q >> 1);
           if (p >= 0 && n < a.H) a.part[p * a.H + n] = acc[m][t][q];
         }
-    __threadfence();
-    named_bar(1, CW * 32);
-    if (threadIdx.x == 0) {
-      int last = 0;
-      if (!*abort) {
-        const int old = atomicAdd(a.cnt + tile, 1);
-        last = (old == n_experts - 1);
-        if (last) atomicExch(a.cnt + tile, 0);
-      }
-      *bcast = last;
-    }
-    named_bar(1, CW * 32);
-    if (*bcast) {
-      __threadfence();
-      const int n = kBM * tile + threadIdx.x;
-      if (threadIdx.x < kBM && n < a.H) {
-        // All partials of two rows are loaded before any is used (they are
-        // independent L2 reads); the sum itself runs in rank order.
-        for (int r0 = 0; r0 < a.k; r0 += 2) {
-          const bool two = r0 + 1 < a.k;
-          const float* p0 = a.part + (long long)r0 * TS * a.H + n;
-          const float* p1 = p0 + (long long)TS * a.H;
-          float v0[kMaxTopK], v1[kMaxTopK];
-#pragma unroll
-          for (int j = 0; j < kMaxTopK; ++j) {
-            v0[j] = j < a.T ? __ldcg(p0 + (long long)j * a.H) : 0.f;
-            v1[j] = (two && j < a.T) ? __ldcg(p1 + (long long)j * a.H) : 0.f;
-          }
-          const float s0 = a.has_shared ? __ldcg(p0 + (long long)a.T * a.H) : 0.f;
-          const float s1 = (two && a.has_shared) ? __ldcg(p1 + (long long)a.T * a.H) : 0.f;
-          combine_row(a, rs, r0, v0, s0, n);
-          if (two) combine_row(a, rs, r0 + 1, v1, s1, n);
-        }
-      }
-      named_bar(1, CW * 32);
-    }
   }
+}
+
+// y[r][n] = sum_j w[r][j] p[r][j][n] in rank order j, then + sigmoid(shared
+// gate logit) x the shared expert's partial: one thread per output, every
+// partial loaded before the sum.
+__global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
+  griddep_wait();
+  griddep_launch();
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)a.k * a.H) return;
+  const int r = (int)(i / a.H), n = (int)(i % a.H);
+  const int TS = a.T + a.has_shared;
+  const float* pr = a.part + (long long)r * TS * a.H + n;
+  float v[kMaxTopK], wj[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    v[j] = j < a.T ? __ldcg(pr + (long long)j * a.H) : 0.f;
+    wj[j] = j < a.T ? __ldcg(a.w_out + r * a.T + j) : 0.f;
+  }
+  const float vs = a.has_shared ? __ldcg(pr + (long long)a.T * a.H) : 0.f;
+  const float sg = a.has_shared ? __ldcg(a.shared_logit + (long long)r * a.logits_ld) : 0.f;
+  float y = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < a.T) y = fmaf(wj[j], v[j], y);
+  if (a.has_shared) y = fmaf(1.f / (1.f + expf(-sg)), vs, y);
+  store_out(a.y, a.dtype, (long long)r * a.H + n, y);
 }
 
 // GATEUP: items (expert, 64 rows of I): gate rows and up rows of the same i
 // go to the same warp (its two MMA tiles), the epilogue applies SwiGLU and
 // writes h (bf16).  Down: items (expert, 128 rows of H); partial outputs per
-// (row, rank) go to scratch and the last CTA of a 128-row block combines them.
+// (row, rank) go to scratch, combined by moe_combine_kernel.
 // Items are expert-major: consecutive CTAs stream consecutive slices of one
 // expert (measured much faster than block-major order, which spreads the
 // concurrent reads over all selected experts).
@@ -709,9 +684,8 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t bar_base = smem_addr(smem + L::BAR_OFF);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
-  volatile int* bcast = abort + 1;
   RouteSmem* rs = reinterpret_cast<RouteSmem*>(smem + L::BASE_BYTES);
-  if (threadIdx.x == 0) { *abort = 0; *bcast = 0; }
+  if (threadIdx.x == 0) *abort = 0;
   init_barriers<CW>(bar_base);
   // Gate/up routes from logits the previous kernel wrote: wait first.  The
   // down kernel's logits are two kernels old, so it routes (and fetches its
@@ -821,10 +795,10 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
     const int nb = pairs_of(rs, a, u);
     // Most routed experts get few rows: one MMA column block then suffices.
     if (NT == 2 && nb <= 8)
-      moe_item<1, NT, CW, GATEUP>(a, rs, smem, bar_base, abort, bcast, u, tile, nb, KC, KG, TS, n_experts, rbase,
+      moe_item<1, NT, CW, GATEUP>(a, rs, smem, bar_base, abort, u, tile, nb, KC, KG, TS, n_experts, rbase,
                                   lane, fills);
     else
-      moe_item<NT, NT, CW, GATEUP>(a, rs, smem, bar_base, abort, bcast, u, tile, nb, KC, KG, TS, n_experts, rbase,
+      moe_item<NT, NT, CW, GATEUP>(a, rs, smem, bar_base, abort, u, tile, nb, KC, KG, TS, n_experts, rbase,
                                    lane, fills);
   }
 }
@@ -903,9 +877,10 @@ static cudaError_t launch_moe_one(const CUtensorMap& map, const CUtensorMap& sma
   return cudaLaunchKernelEx(&cfg, moe_kernel<NT, GATEUP>, map, smap, a);
 }
 
-// The down kernel always follows the gate/up kernel of the same call, which
-// started after everything the caller enqueued before it (or, with pdl, after
-// the kernel before it): it may overlap the gate/up kernel's tail.
+// The down and combine kernels always follow the gate/up kernel of the same
+// call, which started after everything the caller enqueued before it (or,
+// with pdl, after the kernel before it): they may overlap their predecessor's
+// tail.
 cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, const CUtensorMap& sgu_map,
                        const CUtensorMap& sdn_map, const MoeArgs& a, int nt, bool pdl, cudaStream_t s,
                        int* launches) {
@@ -915,6 +890,18 @@ cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, con
   ++*launches;
   e = nt == 1 ? launch_moe_one<1, false>(dn_map, sdn_map, a, true, s)
               : launch_moe_one<2, false>(dn_map, sdn_map, a, true, s);
+  if (e) return e;
+  ++*launches;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(((long long)a.k * a.H + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, moe_combine_kernel, a);
   if (!e) ++*launches;
   return e;
 }

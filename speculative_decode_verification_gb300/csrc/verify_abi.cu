@@ -17,7 +17,6 @@ struct verify_ctx {
   int moe_ctas_per_sm = 0;
   uint16_t* moe_hbuf = nullptr;
   float* moe_part = nullptr;
-  int* moe_cnt = nullptr;
   int* err = nullptr;
   uint16_t* st_xn = nullptr;   // layer scratch: bf16 [16, 8192]
   uint16_t* st_proj = nullptr; // bf16 [16, 32768]
@@ -148,7 +147,6 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device))) return bail(e);
   if ((e = cudaMalloc(&ctx->moe_hbuf, kHbufElems * sizeof(uint16_t)))) return bail(e);
   if ((e = cudaMalloc(&ctx->moe_part, kMoePartElems * sizeof(float)))) return bail(e);
-  if ((e = cudaMalloc(&ctx->moe_cnt, (kMaxH / vk::kBM) * sizeof(int)))) return bail(e);
   if ((e = cudaMalloc(&ctx->err, sizeof(int)))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_xn, sizeof(uint16_t) * VERIFY_MAX_K * kMaxH))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_proj, sizeof(uint16_t) * VERIFY_MAX_K * kMaxProj))) return bail(e);
@@ -156,7 +154,6 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = cudaMalloc(&ctx->st_logits, sizeof(float) * VERIFY_MAX_K * 1024))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_idx, sizeof(int32_t) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_w, sizeof(float) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
-  if ((e = cudaMemset(ctx->moe_cnt, 0, (kMaxH / vk::kBM) * sizeof(int)))) return bail(e);
   if ((e = cudaMemset(ctx->err, 0, sizeof(int)))) return bail(e);
   cudaDriverEntryPointQueryResult q;
   void* fn = nullptr;
@@ -177,7 +174,6 @@ verify_status verify_destroy(verify_ctx* ctx) {
   cudaDeviceSynchronize();
   cudaFree(ctx->moe_hbuf);
   cudaFree(ctx->moe_part);
-  cudaFree(ctx->moe_cnt);
   cudaFree(ctx->err);
   cudaFree(ctx->st_xn);
   cudaFree(ctx->st_proj);
@@ -203,9 +199,7 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
   if ((e = cudaMemcpy(&h, ctx->err, sizeof(int), cudaMemcpyDeviceToHost))) return cuda_fail(ctx, e, "cudaMemcpy");
   if (code) *code = h;
   if (h == 0) return VERIFY_OK;
-  // an aborted kernel may have left arrival counters behind: reset the scratch state
   cudaMemset(ctx->err, 0, sizeof(int));
-  cudaMemset(ctx->moe_cnt, 0, (kMaxH / vk::kBM) * sizeof(int));
   cudaDeviceSynchronize();
   snprintf(ctx->msg, sizeof ctx->msg, "device error code %d", h);
   return VERIFY_EDEVICE;
@@ -295,7 +289,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
     a.sgu_scales = shared_gate_up->scales; a.sgu_biases = shared_gate_up->biases;
     a.sdn_scales = shared_down->scales; a.sdn_biases = shared_down->biases;
   }
-  a.hbuf = ctx->moe_hbuf; a.part = ctx->moe_part; a.cnt = ctx->moe_cnt;
+  a.hbuf = ctx->moe_hbuf; a.part = ctx->moe_part;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
