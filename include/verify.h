@@ -85,16 +85,35 @@ typedef struct verify_ctx verify_ctx;
 
 /*
  * One affine Q4 matrix with group size 64 ([T] table "Shared architecture":
- * "affine Q4, group size 64, and compatible BF16 tensors").  Layout (the
- * affine convention the MLX runtime of [T] uses):
+ * "affine Q4, group size 64, and compatible BF16 tensors"):
+ *   weight : w[n][c] = scale[n][c/64] * q[n][c] + bias[n][c/64],  q in 0..15
+ * in one of two layouts (`layout`):
+ *
+ * VERIFY_Q4_ROWS - the affine convention of the MLX runtime [T] uses; the
+ * form weights arrive in, accepted only by q4_tile:
  *   packed : uint32 [n_out, k_in/8], row-major; input column c of row n is
  *            bits 4*(c%8) .. 4*(c%8)+3 of packed[n*(k_in/8) + c/8]
  *            (lowest nibble = lowest column).
  *   scales : bf16 [n_out, k_in/64];  biases : bf16 [n_out, k_in/64]
- *   weight : w[n][c] = scales[n][c/64] * q[n][c] + biases[n][c/64]
- * Requirements: packed 16-byte aligned; scales, biases 4-byte aligned;
- * k_in % 64 == 0; group_size == 64; bits == 4.
+ *   Requirements: packed 16-byte aligned; scales, biases 2-byte aligned.
+ *
+ * VERIFY_Q4_TILED / VERIFY_Q4_TILED_GATE_UP - the library's layout, written
+ * by q4_tile, taken by every compute call: `packed` points to the tiled bytes
+ * (16-byte aligned), scales and biases are NULL (they live inside the tiles).
+ * Each (128-row tile, 256-column chunk) is one contiguous block: the tile's
+ * scales and biases, then its codes in the order the kernels consume them,
+ * so that a pipeline stage is one bulk copy and HBM is read in long runs.
+ * TILED_GATE_UP marks a fused gate/up matrix [2I, n_in] whose tiles pair 64
+ * gate rows with the 64 up rows of the same outputs.
+ *
+ * Requirements: k_in % 64 == 0, k_in >= 64; group_size == 64; bits == 4.
  */
+typedef enum {
+  VERIFY_Q4_ROWS = 0,
+  VERIFY_Q4_TILED = 1,
+  VERIFY_Q4_TILED_GATE_UP = 2
+} verify_q4_layout;
+
 typedef struct {
   const uint32_t* packed;
   const uint16_t* scales;
@@ -103,12 +122,14 @@ typedef struct {
   int32_t k_in;
   int32_t group_size; /* must be 64 */
   int32_t bits;       /* must be 4 */
+  int32_t layout;     /* verify_q4_layout */
 } verify_q4_weight;
 
 /*
- * A stack of n_experts matrices of identical shape, stored back to back:
- * packed [E, n_out, k_in/8], scales/biases [E, n_out, k_in/64].  `w` holds
- * the per-expert shape and the pointers to expert 0.
+ * A stack of n_experts matrices of identical shape, stored back to back
+ * (row layout: packed [E, n_out, k_in/8], scales/biases [E, n_out, k_in/64];
+ * tiled layout: E tiled matrices).  `w` holds the per-expert shape and the
+ * pointers to expert 0.
  */
 typedef struct {
   verify_q4_weight w;
@@ -137,6 +158,28 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
 /* Number of kernels the library launched on this ctx since verify_init. */
 int64_t verify_launch_count(const verify_ctx* ctx);
 
+/* ------------------------------------------------------------- q4_tile */
+
+/*
+ * Bytes of the tiled layout of n_experts matrices [n_out, k_in] (gate_up:
+ * the gate/up pairing, n_out = 2I with I % 64 == 0); -1 for invalid shapes.
+ * Equals the row layout's bytes when n_out % 128 == 0, plus the zero rows
+ * that complete the last 128-row tile otherwise.
+ */
+int64_t q4_tiled_bytes(int32_t n_out, int32_t k_in, int32_t n_experts, int32_t gate_up);
+
+/*
+ * Converts src (VERIFY_Q4_ROWS; n_experts matrices back to back) into the
+ * tiled layout at dst (device, 16-byte aligned, dst_bytes >= q4_tiled_bytes)
+ * on `stream`, and fills *out (a host struct) with the tiled description:
+ * packed = dst, layout = VERIFY_Q4_TILED or VERIFY_Q4_TILED_GATE_UP.  A
+ * one-time step when weights are loaded; src may be freed once the stream
+ * has passed the conversion.  Every bit of src is kept: the tiled matrix
+ * computes exactly what src describes.
+ */
+verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_experts, int32_t gate_up, void* dst,
+                      int64_t dst_bytes, verify_q4_weight* out, struct CUstream_st* stream);
+
 /* ------------------------------------------------------------ q4_qmv_k */
 
 /*
@@ -147,6 +190,7 @@ int64_t verify_launch_count(const verify_ctx* ctx);
  *
  *     y[r][n] = sum_c w[n][c] * x[r][c]      r < k, n < n_out
  *
+ * W : VERIFY_Q4_TILED.
  * x : bf16 [k, k_in] row-major, 16-byte aligned.
  * y : [k, n_out] row-major, fp32 (VERIFY_F32 / VERIFY_F32_ADD) or bf16.
  * k : 1..VERIFY_MAX_K.   Limits: n_out <= 1<<20, k_in <= 1<<17.
@@ -177,14 +221,15 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W,
  *   y[r] = sum_{j=0..T-1} wts[r][j] * p_j    (ascending j, fp32)
  *   if a shared expert is given: y[r] += sigmoid(sg[r]) * (W_sd . bf16(silu(W_sgu[0..I).x) * W_sgu[I..2I).x))
  *
- * gate_up : experts [E, 2I, H];  down : experts [E, H, I].
+ * gate_up : experts [E, 2I, H], VERIFY_Q4_TILED_GATE_UP;
+ * down    : experts [E, H, I], VERIFY_Q4_TILED.
  * logits  : fp32, row r at logits + r*logits_ld, E entries.
  * x       : bf16 [k, H].   idx_out : int32 [k, T];  w_out : fp32 [k, T].
  * y       : fp32 [k, H] (VERIFY_F32 or VERIFY_F32_ADD) or bf16.
- * shared_gate_up [2I, H], shared_down [H, I], shared_gate_logit (fp32, row r
+ * shared_gate_up [2I, H] (TILED_GATE_UP), shared_down [H, I] (TILED), shared_gate_logit (fp32, row r
  * at shared_gate_logit + r*logits_ld) may all be NULL (no shared expert).
- * Limits: E <= 512, 1 <= T <= 16, 256 <= H <= 8192, 256 <= I <= 4096,
- * H % 128 == I % 128 == 0.
+ * Limits: E <= 512, 1 <= T <= 16, 64 <= H <= 8192, 64 <= I <= 4096,
+ * H % 64 == I % 64 == 0.
  * Expert weights are read once per call for every distinct selected expert
  * (the union of the rows' routes).  Three kernel launches on `stream`.
  */
@@ -322,7 +367,8 @@ verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w,
  * activations live in the context (limits: k <= 16, H <= 8192, in_proj rows
  * <= 32768, E + 1 <= 1024).  Weight shapes must match: in_proj [C + Hv*dv +
  * 2*Hv, H], out_proj [H, Hv*dv], router [E + 1, H], gate_up [E, 2I, H],
- * down [E, H, I], shared_gate_up [2I, H], shared_down [H, I].
+ * down [E, H, I], shared_gate_up [2I, H], shared_down [H, I]; all tiled
+ * (gate_up and shared_gate_up with the gate/up pairing).
  */
 typedef struct {
   verify_q4_weight in_proj;

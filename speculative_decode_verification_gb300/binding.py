@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(PKG, "libverify.so")
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE = 0, 1, 2, 3, 4
 F32, BF16, F32_ADD = 0, 1, 2
+ROWS, TILED, TILED_GATE_UP = 0, 1, 2  # verify_q4_layout
 MAX_K = 16
 GDN_MAX_SLOTS = 17
 
@@ -30,7 +31,8 @@ class VerifyError(RuntimeError):
 
 class Q4Weight(C.Structure):
     _fields_ = [("packed", C.c_void_p), ("scales", C.c_void_p), ("biases", C.c_void_p),
-                ("n_out", C.c_int32), ("k_in", C.c_int32), ("group_size", C.c_int32), ("bits", C.c_int32)]
+                ("n_out", C.c_int32), ("k_in", C.c_int32), ("group_size", C.c_int32), ("bits", C.c_int32),
+                ("layout", C.c_int32)]
 
 
 class Q4Experts(C.Structure):
@@ -74,6 +76,8 @@ def load():
     p, i, i64, f = C.c_void_p, C.c_int, C.c_int64, C.c_float
     sig = {
         "verify_init": [i, C.POINTER(p)],
+        "q4_tiled_bytes": [C.c_int32, C.c_int32, C.c_int32, C.c_int32],
+        "q4_tile": [p, C.POINTER(Q4Weight), C.c_int32, C.c_int32, p, i64, C.POINTER(Q4Weight), p],
         "verify_destroy": [p],
         "verify_last_error": [p],
         "verify_device_status": [p, p, C.POINTER(C.c_int32)],
@@ -96,6 +100,7 @@ def load():
         fn.restype = C.c_int
     L.verify_last_error.restype = C.c_char_p
     L.verify_launch_count.restype = C.c_int64
+    L.q4_tiled_bytes.restype = C.c_int64
     _lib = L
     return L
 
@@ -105,15 +110,25 @@ def _ptr(t):
 
 
 def q4_weight(packed, scales, biases) -> Q4Weight:
-    """Q4Weight over device tensors packed [N, K/8] (int32/uint32), scales/biases [N, K/64] (bf16 bits)."""
+    """Row-layout Q4Weight over device tensors packed [N, K/8] (int32/uint32),
+    scales/biases [N, K/64] (bf16 bits).  Compute calls take its tiled form
+    (Verify.tile)."""
     n_out, k_in = packed.shape[-2], packed.shape[-1] * 8
-    return Q4Weight(packed.data_ptr(), scales.data_ptr(), biases.data_ptr(), n_out, k_in, 64, 4)
+    return Q4Weight(packed.data_ptr(), scales.data_ptr(), biases.data_ptr(), n_out, k_in, 64, 4, ROWS)
 
 
 def q4_experts(packed, scales, biases) -> Q4Experts:
-    """Q4Experts over device tensors packed [E, N, K/8], scales/biases [E, N, K/64]."""
+    """Row-layout Q4Experts over device tensors packed [E, N, K/8], scales/biases [E, N, K/64]."""
     E, n_out, k_in = packed.shape[0], packed.shape[1], packed.shape[2] * 8
-    return Q4Experts(Q4Weight(packed.data_ptr(), scales.data_ptr(), biases.data_ptr(), n_out, k_in, 64, 4), E)
+    return Q4Experts(Q4Weight(packed.data_ptr(), scales.data_ptr(), biases.data_ptr(), n_out, k_in, 64, 4, ROWS), E)
+
+
+class Tiled:
+    """A tiled Q4 matrix (or expert stack): the device buffer and its struct
+    (Q4Weight, or Q4Experts for a stack).  Keep it alive while calls use it."""
+
+    def __init__(self, buf, struct):
+        self.buf, self.struct = buf, struct
 
 
 class Verify:
@@ -198,6 +213,22 @@ class Verify:
             return
         arr = (C.c_void_p * 8)(*[None if e is None else e.cuda_event for e in events])
         self._check(self.lib.verify_set_layer_events(self.ctx, arr, 8))
+
+    def tile(self, src, gate_up: bool = False, stream=None) -> Tiled:
+        """Tiled copy of a row-layout Q4Weight or Q4Experts (q4_tile): a new
+        device buffer (torch uint8) and the struct describing it."""
+        import torch
+
+        experts = isinstance(src, Q4Experts)
+        w, E = (src.w, src.n_experts) if experts else (src, 1)
+        nbytes = int(self.lib.q4_tiled_bytes(w.n_out, w.k_in, E, int(bool(gate_up))))
+        if nbytes < 0:
+            raise VerifyError(EUNSUPPORTED, f"q4_tiled_bytes({w.n_out}, {w.k_in}, {E}, {gate_up}) rejected the shape")
+        buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        out = Q4Weight()
+        self._check(self.lib.q4_tile(self.ctx, C.byref(w), E, int(bool(gate_up)), C.c_void_p(buf.data_ptr()), nbytes,
+                                     C.byref(out), self._stream(stream)))
+        return Tiled(buf, Q4Experts(out, E) if experts else out)
 
     def synth_q4(self, packed, scales, biases, seeds, scale_range, bias_range, centered=False, stream=None):
         self._check(self.lib.verify_synth_q4(self.ctx, _ptr(packed), _ptr(scales), _ptr(biases),

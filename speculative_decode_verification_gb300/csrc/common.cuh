@@ -84,6 +84,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes (16-byte aligned, multiple of 16)
+// into shared memory, completing on an mbarrier (expected bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ------------------------------------------------------------- cp.async
 
 // 4-byte copy; src_bytes = 0 writes zeros without reading.

@@ -18,11 +18,17 @@ constexpr int kQ4CtasPerSm = 2;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 
+// Tiled weight layout (tile.cu): per (128-row tile, 256-column chunk) a block
+// of scales and biases followed by the chunk's groups of codes.
+constexpr int kTileSbBytes = 2 * kBM * 8;                                 // 2048
+constexpr int kTileGroupBytes = kBM * 32;                                 // 4096: 128 rows x 64 codes
+constexpr int kTileChunkBytes = kTileSbBytes + kGroupsPerUnit * kTileGroupBytes;  // 18432
+
 // Dense product: RB row tiles x S K-splits, one cluster of S CTAs per tile.
 struct DenseArgs {
-  const uint16_t* scales;
-  const uint16_t* biases;
-  const uint16_t* x;  // [k, K] bf16
+  const uint8_t* tiles;  // tiled weights
+  long long rt_bytes;    // bytes of one row tile
+  const uint16_t* x;     // [k, K] bf16
   void* y;            // [k, N]
   int* err;
   int N, K, k, dtype;
@@ -36,14 +42,11 @@ struct MoeArgs {
   long long logits_ld;
   const float* shared_logit;  // NULL: no shared expert
   const uint16_t* x;          // [k, H]
-  const uint16_t* gu_scales;  // [E, 2I, H/64]
-  const uint16_t* gu_biases;
-  const uint16_t* dn_scales;  // [E, H, I/64]
-  const uint16_t* dn_biases;
-  const uint16_t* sgu_scales; // shared [2I, H/64]
-  const uint16_t* sgu_biases;
-  const uint16_t* sdn_scales; // shared [H, I/64]
-  const uint16_t* sdn_biases;
+  const uint8_t* gu_tiles;    // tiled [E, 2I, H], gate/up pairing: I/64 row tiles per expert
+  const uint8_t* dn_tiles;    // tiled [E, H, I]: ceil(H/128) row tiles per expert
+  const uint8_t* sgu_tiles;   // shared expert, same layouts (NULL: none)
+  const uint8_t* sdn_tiles;
+  long long gu_rt_bytes, dn_rt_bytes;
   uint16_t* hbuf;             // scratch [k, TS, I] bf16 (TS = T + has_shared)
   float* part;                // scratch [k, TS, H] fp32
   int32_t* idx_out;
@@ -78,10 +81,13 @@ struct GdnArgs {
 cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm);
 // pdl: launch with programmatic stream serialization (the kernel may start
 // while the previous kernel on the stream runs; see griddep_wait).
-cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, bool pdl, cudaStream_t s);
-cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, const CUtensorMap& sgu_map,
-                       const CUtensorMap& sdn_map, const MoeArgs& a, int nt, bool pdl, cudaStream_t s,
-                       int* launches);
+cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s);
+cudaError_t launch_moe(const MoeArgs& a, int nt, bool pdl, cudaStream_t s, int* launches);
+// Tiled layout: bytes of E matrices [N, K] (gate_up: tiles pair gate and up rows),
+// and the conversion from the row-major layout.
+long long tiled_bytes(int N, int K, int E, bool gate_up);
+cudaError_t launch_tile(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases, uint8_t* dst, int N,
+                        int K, int E, bool gate_up, cudaStream_t s);
 cudaError_t gdn_setup_kernels();
 cudaError_t launch_gdn(const GdnArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, int n, int k, void* out,

@@ -1,8 +1,6 @@
 // noalloc.cu - the routed-expert call for callers that may not allocate device
 // memory.  Its scratch is a fixed array compiled into the library; nothing
 // here calls cudaMalloc, cudaFree or an allocating library routine.
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "internal.h"
@@ -27,7 +25,6 @@ struct DeviceSetup {
 
 std::mutex g_mutex;
 DeviceSetup g_dev[kMaxDevices];
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
@@ -44,15 +41,6 @@ verify_status setup_device(int dev, DeviceSetup** out) {
     int dense_ctas = 0, moe_ctas = 0, sms = 0;
     if (vk::q4_setup_kernels(&dense_ctas, &moe_ctas) != cudaSuccess) return VERIFY_ECUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return VERIFY_ECUDA;
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
-        return VERIFY_ECUDA;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
     d.scratch = static_cast<unsigned char*>(p);
     d.num_sms = sms;
     d.moe_ctas_per_sm = moe_ctas;
@@ -72,19 +60,15 @@ bool device_memory(const void* p, size_t align) {
   return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
 }
 
-bool valid_q4(const verify_q4_weight* W) {
-  return W && W->group_size == 64 && W->bits == 4 && W->k_in % 128 == 0 && W->k_in >= 256 && W->n_out >= 1 &&
-         device_memory(W->packed, 16) && device_memory(W->scales, 4) && device_memory(W->biases, 4);
+// A tiled operand (q4_tile) of the given layout.
+bool valid_q4(const verify_q4_weight* W, int layout) {
+  return W && W->group_size == 64 && W->bits == 4 && W->layout == layout && W->k_in % 64 == 0 && W->k_in >= 64 &&
+         W->n_out >= 1 && device_memory(W->packed, 16);
 }
 
-bool encode(CUtensorMap* m, const void* base, uint64_t rows, uint64_t words, uint32_t box_rows) {
-  cuuint64_t dims[2] = {words, rows};
-  cuuint64_t strides[1] = {words * 4};
-  cuuint32_t box[2] = {32, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+long long rt_bytes(int k_in) {
+  const long long KG = k_in / 64, KC = (KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
+  return (long long)vk::kTileSbBytes * KC + (long long)vk::kTileGroupBytes * KG;
 }
 
 }  // namespace
@@ -105,9 +89,9 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   const int E = gate_up->n_experts;
   if (E < 1 || E > vk::kMaxExperts || down->n_experts != E) return VERIFY_EUNSUPPORTED;
   if (top_k < 1 || top_k > vk::kMaxTopK || top_k > E) return VERIFY_EUNSUPPORTED;
-  if (!valid_q4(&gate_up->w) || !valid_q4(&down->w)) return VERIFY_EINVAL;
+  if (!valid_q4(&gate_up->w, VERIFY_Q4_TILED_GATE_UP) || !valid_q4(&down->w, VERIFY_Q4_TILED)) return VERIFY_EINVAL;
   const int H = gate_up->w.k_in, I = gate_up->w.n_out / 2;
-  if (gate_up->w.n_out != 2 * I || down->w.n_out != H || down->w.k_in != I || I % 128 != 0) return VERIFY_EINVAL;
+  if (gate_up->w.n_out != 2 * I || down->w.n_out != H || down->w.k_in != I || I % 64 != 0) return VERIFY_EINVAL;
   if (logits_ld < E) return VERIFY_EINVAL;
   if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16 && dtype_out != VERIFY_F32_ADD) return VERIFY_EINVAL;
   if (!device_memory(logits, 4) || !device_memory(x, 16) || !device_memory(idx_out, 4) || !device_memory(w_out, 4) ||
@@ -117,7 +101,8 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   const int n_shared = (shared_gate_up != nullptr) + (shared_down != nullptr) + (shared_gate_logit != nullptr);
   if (n_shared != 0 && n_shared != 3) return VERIFY_EINVAL;
   if (n_shared == 3) {
-    if (!valid_q4(shared_gate_up) || !valid_q4(shared_down) || !device_memory(shared_gate_logit, 4))
+    if (!valid_q4(shared_gate_up, VERIFY_Q4_TILED_GATE_UP) || !valid_q4(shared_down, VERIFY_Q4_TILED) ||
+        !device_memory(shared_gate_logit, 4))
       return VERIFY_EINVAL;
     if (shared_gate_up->n_out != 2 * I || shared_gate_up->k_in != H || shared_down->n_out != H ||
         shared_down->k_in != I)
@@ -132,27 +117,17 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   unsigned char* base = d->scratch;
   int* err_word = reinterpret_cast<int*>(base + hbuf_bytes + part_bytes);
 
-  CUtensorMap gu, dn, sgu, sdn;
-  if (!encode(&gu, gate_up->w.packed, (uint64_t)E * 2 * I, (uint64_t)H / 8, 64) ||
-      !encode(&dn, down->w.packed, (uint64_t)E * H, (uint64_t)I / 8, vk::kBM))
-    return VERIFY_ECUDA;
-  if (n_shared == 3) {
-    if (!encode(&sgu, shared_gate_up->packed, (uint64_t)2 * I, (uint64_t)H / 8, 64) ||
-        !encode(&sdn, shared_down->packed, (uint64_t)H, (uint64_t)I / 8, vk::kBM))
-      return VERIFY_ECUDA;
-  } else {
-    sgu = gu;
-    sdn = dn;
-  }
   vk::MoeArgs a{};
   a.logits = logits; a.logits_ld = logits_ld; a.shared_logit = n_shared ? shared_gate_logit : nullptr;
   a.x = x;
-  a.gu_scales = gate_up->w.scales; a.gu_biases = gate_up->w.biases;
-  a.dn_scales = down->w.scales; a.dn_biases = down->w.biases;
+  a.gu_tiles = reinterpret_cast<const uint8_t*>(gate_up->w.packed);
+  a.dn_tiles = reinterpret_cast<const uint8_t*>(down->w.packed);
   if (n_shared) {
-    a.sgu_scales = shared_gate_up->scales; a.sgu_biases = shared_gate_up->biases;
-    a.sdn_scales = shared_down->scales; a.sdn_biases = shared_down->biases;
+    a.sgu_tiles = reinterpret_cast<const uint8_t*>(shared_gate_up->packed);
+    a.sdn_tiles = reinterpret_cast<const uint8_t*>(shared_down->packed);
   }
+  a.gu_rt_bytes = rt_bytes(H);
+  a.dn_rt_bytes = rt_bytes(I);
   a.hbuf = reinterpret_cast<uint16_t*>(base);
   a.part = reinterpret_cast<float*>(base + hbuf_bytes);
   a.idx_out = idx_out; a.w_out = w_out; a.y = y;
@@ -164,6 +139,6 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   // device error and left it set.
   if (!device_error && cudaMemsetAsync(err_word, 0, sizeof(int), stream) != cudaSuccess) return VERIFY_ECUDA;
   int launched = 0;
-  if (vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, false, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
+  if (vk::launch_moe(a, k <= 8 ? 1 : 2, false, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
   return VERIFY_OK;
 }

@@ -39,26 +39,29 @@
 
 namespace vk {
 
+// A stage: [scales, biases][codes][activation rows].  The first two parts are
+// one block of the tiled weight layout (tile.cu), copied with one bulk copy.
 template <int NT>
 struct Q4Layout {
   static constexpr int NB = 8 * NT;                          // activation rows held per stage
-  static constexpr int W_BYTES = kBM * 128;                  // 128 rows x 32 packed words
+  static constexpr int SB_BYTES = kTileSbBytes;              // scales then biases, [row][4 groups]
+  static constexpr int W_BYTES = kBM * 128;                  // codes, fragment order, [group][16-row block][lane]
   static constexpr int X_BYTES = kGroupsPerUnit * NB * 128;  // [group][row][64 bf16]
-  static constexpr int SB_BYTES = 2 * kBM * 8;               // scales then biases, 4 groups per row
-  static constexpr int STAGE = W_BYTES + X_BYTES + SB_BYTES;
+  static constexpr int STAGE = SB_BYTES + W_BYTES + X_BYTES;
   static constexpr int SX_BYTES = kGroupsPerUnit * NB * 4;   // fp32 group sums [group][row]
   static constexpr int SX_OFF = kStages * STAGE;             // one slot per stage, after the stages
   static constexpr int BAR_OFF = SX_OFF + kStages * SX_BYTES;
   static constexpr int MISC_OFF = BAR_OFF + 2 * kStages * 8;
   static constexpr int MISC_BYTES = 64 + 16 * 8;             // flags, then the producer's row-pointer table
   static constexpr int BASE_BYTES = MISC_OFF + MISC_BYTES;
-  static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
+  static_assert(STAGE % 128 == 0, "stages keep 128-byte alignment");
 };
 
 // Where a stage holding NBL activation rows keeps them (the consumer's view).
 template <int NBL>
 struct XLayout {
   static constexpr int NB = NBL;
+  static constexpr int SB_BYTES = kTileSbBytes;
   static constexpr int W_BYTES = kBM * 128;
   static constexpr int X_BYTES = kGroupsPerUnit * NBL * 128;
 };
@@ -78,75 +81,23 @@ struct RouteSmem {
   int U;
 };
 
-// What the producer needs to know about a tile.
-struct TileSrc {
-  const CUtensorMap* map;
-  int y0, y1;          // TMA row coordinate of the box(es)
-  int two_boxes;       // 1: two 64-row boxes (gate rows, up rows); 0: one 128-row box
-  int row_limit;       // tile rows whose row index within their matrix is >= limit are empty
-  int mat_row0;        // matrix row of tile row 0 (for the limit test)
-  const uint16_t* scales;  // scales/biases, addressed with the TMA row index
-  const uint16_t* biases;
-  int KG;
-};
-
-__device__ __forceinline__ int tile_global_row(const TileSrc& t, int i) {
-  if (t.two_boxes) return i < 64 ? t.y0 + i : t.y1 + (i - 64);
-  return (t.mat_row0 + i < t.row_limit) ? t.y0 + i : -1;
-}
-
 // ---------------------------------------------------------------- producer
 
-// A stage is filled in three parts that all complete on its full barrier:
-// the weight tile (TMA, expected bytes), the tile's scales and biases and the
-// activation rows (cp.async, then one arrival per producer lane).  Only what
-// the consumers read is copied: scales of rows inside the matrix, activation
-// rows below nb, groups below gcount.  Anything else in the stage is stale and
-// only reaches output columns or rows that are never stored (an MMA column
-// depends on its own activation row alone).
+// A stage is filled in two parts that both complete on its full barrier: the
+// weight block (scales, biases and the gcount groups of codes: one bulk copy,
+// expected bytes) and the activation rows (cp.async, then one arrival per
+// producer lane).  Only what the consumers read is copied: activation rows
+// below nb, groups below gcount.  Anything else in the stage is stale and only
+// reaches output columns that are never stored (an MMA column depends on its
+// own activation row alone).
 
-// Weight tile.  Reads only static data.
-template <int NT>
-__device__ __forceinline__ void produce_tma(uint8_t* stage_ptr, uint32_t full_bar, const TileSrc& t, int kc) {
-  using L = Q4Layout<NT>;
-  const uint32_t w_dst = smem_addr(stage_ptr);
-  mbar_arrive_expect_tx(full_bar, L::W_BYTES);
-  if (t.two_boxes) {
-    tma_load_2d(w_dst, t.map, full_bar, kc * 32, t.y0);
-    tma_load_2d(w_dst + 64 * 128, t.map, full_bar, kc * 32, t.y1);
-  } else {
-    tma_load_2d(w_dst, t.map, full_bar, kc * 32, t.y0);
-  }
-}
-
-// Scales and biases of the tile's rows, four groups per row: one 8-byte copy
-// per row and array when a row's groups are 8-byte aligned (K % 256 == 0),
-// else two 4-byte copies.
-template <int NT>
-__device__ __forceinline__ void produce_sb(uint8_t* stage_ptr, const TileSrc& t, int kc, int gcount, int lane) {
-  using L = Q4Layout<NT>;
-  const uint32_t sb_dst = smem_addr(stage_ptr) + L::W_BYTES + L::X_BYTES;
-  const int e0 = 4 * kc;
-  if ((t.KG & 3) == 0) {
-#pragma unroll
-    for (int idx = lane; idx < 2 * kBM; idx += 32) {
-      const int arr = idx >> 7;
-      const int row = idx & (kBM - 1);
-      const int gr = tile_global_row(t, row);
-      if (gr >= 0) cp_async8(sb_dst + arr * (kBM * 8) + row * 8, (arr ? t.biases : t.scales) + (long long)gr * t.KG + e0);
-    }
-  } else {
-#pragma unroll
-    for (int idx = lane; idx < 2 * kBM * 2; idx += 32) {
-      const int arr = idx >> 8;
-      const int row = (idx >> 1) & (kBM - 1);
-      const int word = idx & 1;
-      const int gr = tile_global_row(t, row);
-      if (gr >= 0 && 2 * word < gcount)
-        cp_async4(sb_dst + arr * (kBM * 8) + row * 8 + word * 4,
-                  (arr ? t.biases : t.scales) + (long long)gr * t.KG + e0 + 2 * word, 4u);
-    }
-  }
+// Weight block kc of a row tile (tile: the row tile's first block).  Reads
+// only static data.
+__device__ __forceinline__ void produce_w(uint8_t* stage_ptr, uint32_t full_bar, const uint8_t* tile, int kc,
+                                          int gcount) {
+  const uint32_t bytes = kTileSbBytes + gcount * kTileGroupBytes;
+  mbar_arrive_expect_tx(full_bar, bytes);
+  bulk_load(smem_addr(stage_ptr), tile + (long long)kc * kTileChunkBytes, bytes, full_bar);
 }
 
 // Activation rows b < nb (brow: their pointers, in shared memory), then this
@@ -155,7 +106,7 @@ template <int NT>
 __device__ __forceinline__ void produce_x(uint8_t* stage_ptr, uint32_t full_bar, int kc, int gcount,
                                           const uint16_t* const* brow, int nb, int lane) {
   using L = Q4Layout<NT>;
-  const uint32_t x_dst = smem_addr(stage_ptr) + L::W_BYTES;
+  const uint32_t x_dst = smem_addr(stage_ptr) + L::SB_BYTES + L::W_BYTES;
   // [group][row][8 chunks of 16 B], chunk index xor (row & 7)
 #pragma unroll
   for (int idx = lane; idx < L::NB * 32; idx += 32) {
@@ -172,14 +123,13 @@ __device__ __forceinline__ void produce_x(uint8_t* stage_ptr, uint32_t full_bar,
 
 // Fills one stage.
 template <int NT>
-__device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_bar, const TileSrc& t, int kc,
+__device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_bar, const uint8_t* tile, int kc,
                                               int gcount, const uint16_t* const* brow, int nb, int lane) {
-  if (lane == 0) produce_tma<NT>(stage_ptr, full_bar, t, kc);
-  produce_sb<NT>(stage_ptr, t, kc, gcount, lane);
+  if (lane == 0) produce_w(stage_ptr, full_bar, tile, kc, gcount);
   produce_x<NT>(stage_ptr, full_bar, kc, gcount, brow, nb, lane);
 }
 
-// On abort the producer keeps the CTA alive until its TMA writes have landed.
+// On abort the producer keeps the CTA alive until its bulk copies have landed.
 __device__ __forceinline__ void producer_drain(uint32_t bar_base, long long fills) {
   for (long long f = (fills > kStages ? fills - kStages : 0); f < fills; ++f) {
     const int s = (int)(f % kStages);
@@ -218,18 +168,17 @@ __device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, ui
   }
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
-    const int row = rbase[m] + g;
-    const uint32_t off = (uint32_t)((((2 * G + (c >> 1)) ^ (row & 7)) << 4) + ((c & 1) << 3));
-    const uint2 wa = lds64(w_src + row * 128 + off);        // words 2c, 2c+1 of row g
-    const uint2 wb = lds64(w_src + (row + 8) * 128 + off);  // same for row g+8
+    // This lane's four code words of the 16-row block: rows g and g+8, words
+    // W0 (columns 16c .. 16c+7 of the group) and W1 (16c+8 .. 16c+15).
+    const uint4 w4 = lds128(w_src + ((G * 8 + (rbase[m] >> 4)) * 32 + lane) * 16);
     // Nibble pairs (p, p+4) of a word: lop3 of the word shifted by 4p bits
     // with mask 0x000F000F and the bf16 exponent of 128 -> (128 + q_p, 128 + q_{p+4}).
-    // MMA j = 2*word + (p odd) takes pair p in k-slots (2c, 2c+1) and pair
-    // p+2 in k-slots (2c+8, 2c+9); the activation tile is stored in the
-    // matching order (see consume_stage).
+    // The tiled layout orders the nibbles so that pair p of word Ww is the A
+    // fragment of MMA j = 2w + (p & 1), k-slots 2c + 8 (p >> 1) and the next,
+    // i.e. activation columns 16c + 4j + 2 (p >> 1) and the next.
     uint32_t A[4][4];
     {
-      const uint32_t v[4] = {wa.x, wb.x, wa.y, wb.y};  // row g word 2c, row g+8 word 2c, then word 2c+1
+      const uint32_t v[4] = {w4.x, w4.y, w4.z, w4.w};  // row g W0, row g+8 W0, row g W1, row g+8 W1
       uint32_t q[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -281,19 +230,17 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t
   static_assert(NBL >= 8 * NT, "stage holds too few activation rows");
   using L = XLayout<NBL>;
   constexpr int MT = Warps<CW>::MT;
-  const uint32_t w_src = smem_addr(stage_ptr);
+  const uint32_t sb_src = smem_addr(stage_ptr);
+  const uint32_t w_src = sb_src + L::SB_BYTES;
   const uint32_t x_src = w_src + L::W_BYTES;
-  const uint32_t sb_src = x_src + L::X_BYTES;
   const int g = lane >> 2, c = lane & 3;
   const int w = threadIdx.x >> 5;
   if (!ok) {
     named_bar(2, CW * 32);
     return;
   }
-  // Consumer warp w < 4 prepares activation group w of the stage: the group
-  // sums (each thread its 16 values, then the four threads of a row) and, in
-  // place, the column order [0,4,2,6,1,5,3,7] within every 8-column block, the
-  // k-slot order of the decoded nibble pairs.
+  // Consumer warp w < 4 adds up activation group w of the stage: each thread
+  // its 16 values, then the four threads of a row.
   if (w < gcount) {
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -309,12 +256,6 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
       if (c == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(sx_src + (w * L::NB + b) * 4), "f"(part) : "memory");
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ca), "r"(prmt(xa.x, xa.z, 0x5410)),
-                   "r"(prmt(xa.y, xa.w, 0x5410)), "r"(prmt(xa.x, xa.z, 0x7632)), "r"(prmt(xa.y, xa.w, 0x7632))
-                   : "memory");
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(cb), "r"(prmt(xb.x, xb.z, 0x5410)),
-                   "r"(prmt(xb.y, xb.w, 0x5410)), "r"(prmt(xb.x, xb.z, 0x7632)), "r"(prmt(xb.y, xb.w, 0x7632))
-                   : "memory");
     }
   }
   // scales / biases of this thread's rows, four groups each
@@ -378,7 +319,7 @@ __device__ __forceinline__ void init_barriers(uint32_t bar_base) {
 // warps w with w % S == q.  S depends only on (N, K, SM count), never on k.
 template <int NT>
 __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
-    q4_dense_kernel(const __grid_constant__ CUtensorMap wmap, const DenseArgs a) {
+    q4_dense_kernel(const DenseArgs a) {
   using L = Q4Layout<NT>;
   constexpr int CW = kDenseWarps, MT = Warps<CW>::MT;
   extern __shared__ uint8_t smem_raw[];
@@ -396,26 +337,21 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) tma_prefetch_desc(&wmap);
     const uint16_t** brow = reinterpret_cast<const uint16_t**>(smem + L::MISC_OFF + 64);
     if (lane < L::NB) brow[lane] = a.x + (long long)(lane < a.k ? lane : 0) * a.K;
     __syncwarp();
-    TileSrc ts;
-    ts.map = &wmap; ts.y0 = tile * kBM; ts.y1 = 0; ts.two_boxes = 0;
-    ts.row_limit = a.N; ts.mat_row0 = tile * kBM;
-    ts.scales = a.scales; ts.biases = a.biases; ts.KG = a.KG;
+    const uint8_t* ts = a.tiles + (long long)tile * a.rt_bytes;
     // The first stages' weights are static: fetch them before the previous
     // kernel has finished (the ring is empty, no wait), the activations after.
     const int n_pre = min(kStages, kc1 - kc0);
     if (lane == 0)
-      for (int f = 0; f < n_pre; ++f) produce_tma<NT>(smem + f * L::STAGE, bar_base + 8 * f, ts, kc0 + f);
+      for (int f = 0; f < n_pre; ++f)
+        produce_w(smem + f * L::STAGE, bar_base + 8 * f, ts, kc0 + f, min(kGroupsPerUnit, a.KG - 4 * (kc0 + f)));
     griddep_wait();
     griddep_launch();
-    for (int f = 0; f < n_pre; ++f) {
-      const int gcount = min(kGroupsPerUnit, a.KG - 4 * (kc0 + f));
-      produce_sb<NT>(smem + f * L::STAGE, ts, kc0 + f, gcount, lane);
-      produce_x<NT>(smem + f * L::STAGE, bar_base + 8 * f, kc0 + f, gcount, brow, a.k, lane);
-    }
+    for (int f = 0; f < n_pre; ++f)
+      produce_x<NT>(smem + f * L::STAGE, bar_base + 8 * f, kc0 + f, min(kGroupsPerUnit, a.KG - 4 * (kc0 + f)), brow,
+                    a.k, lane);
     long long fills = n_pre;
     for (int kc = kc0 + n_pre; kc < kc1; ++kc, ++fills) {
       const int s = (int)(fills % kStages);
@@ -676,7 +612,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
 // concurrent reads over all selected experts).
 template <int NT, bool GATEUP>
 __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS, kQ4CtasPerSm)
-    moe_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ CUtensorMap smap, const MoeArgs a) {
+    moe_kernel(const MoeArgs a) {
   using L = Q4Layout<NT>;
   constexpr int CW = GATEUP ? kGateUpWarps : kDownWarps, MT = Warps<CW>::MT;
   static_assert(!GATEUP || MT == 2, "gate/up pairs the gate and up row tiles in one warp");
@@ -712,7 +648,6 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) { tma_prefetch_desc(&map); if (a.has_shared) tma_prefetch_desc(&smap); }
     const uint16_t** brow = reinterpret_cast<const uint16_t**>(smem + L::MISC_OFF + 64);
     long long fills = 0;
     bool waited = GATEUP;
@@ -728,37 +663,21 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
         brow[lane] = GATEUP ? a.x + (long long)r * a.H : a.hbuf + ((long long)r * TS + j) * a.I;
       }
       __syncwarp();
-      TileSrc ts;
-      ts.map = shared ? &smap : &map;
-      ts.KG = KG;
-      if (GATEUP) {
-        ts.two_boxes = 1;
-        ts.y0 = (shared ? 0 : e * 2 * a.I) + 64 * tile;
-        ts.y1 = ts.y0 + a.I;
-        ts.row_limit = 0; ts.mat_row0 = 0;
-        ts.scales = shared ? a.sgu_scales : a.gu_scales;
-        ts.biases = shared ? a.sgu_biases : a.gu_biases;
-      } else {
-        ts.two_boxes = 0;
-        ts.y0 = (shared ? 0 : e * a.H) + kBM * tile;
-        ts.y1 = 0;
-        ts.row_limit = a.H; ts.mat_row0 = kBM * tile;
-        ts.scales = shared ? a.sdn_scales : a.dn_scales;
-        ts.biases = shared ? a.sdn_biases : a.dn_biases;
-      }
+      const uint8_t* ts =
+          GATEUP ? (shared ? a.sgu_tiles : a.gu_tiles + (long long)e * (a.I / 64) * a.gu_rt_bytes) + tile * a.gu_rt_bytes
+                 : (shared ? a.sdn_tiles : a.dn_tiles + (long long)e * ((a.H + kBM - 1) / kBM) * a.dn_rt_bytes) +
+                       tile * a.dn_rt_bytes;
       int kc = 0;
       if (!waited) {  // first item of the down kernel: its weights before the wait
         waited = true;
         const int n_pre = min(kStages, KC);
         if (lane == 0)
-          for (int f = 0; f < n_pre; ++f) produce_tma<NT>(smem + f * L::STAGE, bar_base + 8 * f, ts, f);
+          for (int f = 0; f < n_pre; ++f)
+            produce_w(smem + f * L::STAGE, bar_base + 8 * f, ts, f, min(kGroupsPerUnit, KG - 4 * f));
         griddep_wait();
         griddep_launch();
-        for (int f = 0; f < n_pre; ++f) {
-          const int gcount = min(kGroupsPerUnit, KG - 4 * f);
-          produce_sb<NT>(smem + f * L::STAGE, ts, f, gcount, lane);
-          produce_x<NT>(smem + f * L::STAGE, bar_base + 8 * f, f, gcount, brow, nb, lane);
-        }
+        for (int f = 0; f < n_pre; ++f)
+          produce_x<NT>(smem + f * L::STAGE, bar_base + 8 * f, f, min(kGroupsPerUnit, KG - 4 * f), brow, nb, lane);
         kc = n_pre;
         fills = n_pre;
       }
@@ -842,7 +761,7 @@ cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm) {
   return cudaSuccess;
 }
 
-cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt, bool pdl, cudaStream_t s) {
+cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.RB * a.S);
   cfg.blockDim = dim3(Warps<kDenseWarps>::THREADS);
@@ -857,13 +776,12 @@ cudaError_t launch_q4_dense(const CUtensorMap& wmap, const DenseArgs& a, int nt,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  if (nt == 1) return cudaLaunchKernelEx(&cfg, q4_dense_kernel<1>, wmap, a);
-  return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2>, wmap, a);
+  if (nt == 1) return cudaLaunchKernelEx(&cfg, q4_dense_kernel<1>, a);
+  return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2>, a);
 }
 
 template <int NT, bool GATEUP>
-static cudaError_t launch_moe_one(const CUtensorMap& map, const CUtensorMap& smap, const MoeArgs& a, bool pdl,
-                                  cudaStream_t s) {
+static cudaError_t launch_moe_one(const MoeArgs& a, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.G);
   cfg.blockDim = dim3(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS);
@@ -874,22 +792,18 @@ static cudaError_t launch_moe_one(const CUtensorMap& map, const CUtensorMap& sma
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, moe_kernel<NT, GATEUP>, map, smap, a);
+  return cudaLaunchKernelEx(&cfg, moe_kernel<NT, GATEUP>, a);
 }
 
 // The down and combine kernels always follow the gate/up kernel of the same
 // call, which started after everything the caller enqueued before it (or,
 // with pdl, after the kernel before it): they may overlap their predecessor's
 // tail.
-cudaError_t launch_moe(const CUtensorMap& gu_map, const CUtensorMap& dn_map, const CUtensorMap& sgu_map,
-                       const CUtensorMap& sdn_map, const MoeArgs& a, int nt, bool pdl, cudaStream_t s,
-                       int* launches) {
-  cudaError_t e = nt == 1 ? launch_moe_one<1, true>(gu_map, sgu_map, a, pdl, s)
-                          : launch_moe_one<2, true>(gu_map, sgu_map, a, pdl, s);
+cudaError_t launch_moe(const MoeArgs& a, int nt, bool pdl, cudaStream_t s, int* launches) {
+  cudaError_t e = nt == 1 ? launch_moe_one<1, true>(a, pdl, s) : launch_moe_one<2, true>(a, pdl, s);
   if (e) return e;
   ++*launches;
-  e = nt == 1 ? launch_moe_one<1, false>(dn_map, sdn_map, a, true, s)
-              : launch_moe_one<2, false>(dn_map, sdn_map, a, true, s);
+  e = nt == 1 ? launch_moe_one<1, false>(a, true, s) : launch_moe_one<2, false>(a, true, s);
   if (e) return e;
   ++*launches;
   cudaLaunchConfig_t cfg = {};

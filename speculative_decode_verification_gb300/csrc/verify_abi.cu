@@ -1,8 +1,6 @@
 // verify_abi.cu - the C ABI declared in include/verify.h: context and scratch,
 // argument validation (all done before anything is launched), TMA
 // descriptors, launches on the caller's stream, GDN slot bookkeeping.
-#include <cudaTypedefs.h>
-
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -31,7 +29,6 @@ struct verify_ctx {
   // kernel before it on the stream still runs (programmatic dependent launch).
   bool pdl = false;
   char msg[512] = {0};
-  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
 
 namespace {
@@ -82,34 +79,29 @@ verify_status use_device(verify_ctx* ctx) {
   return VERIFY_OK;
 }
 
-// Packed-weight TMA map: uint32 [rows, words], box 32 words x box_rows, 128B swizzle.
-verify_status make_wmap(verify_ctx* ctx, CUtensorMap* m, const void* base, uint64_t rows, uint64_t words,
-                        uint32_t box_rows) {
-  cuuint64_t dims[2] = {words, rows};
-  cuuint64_t strides[1] = {words * 4};
-  cuuint32_t box[2] = {32, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = ctx->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(ctx->msg, sizeof ctx->msg, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return VERIFY_ECUDA;
-  }
-  return VERIFY_OK;
+bool valid_shape(int32_t n_out, int32_t k_in) {
+  return n_out >= 1 && n_out <= kMaxN && k_in >= 64 && k_in % 64 == 0 && k_in <= kMaxKin;
 }
 
-verify_status check_q4(verify_ctx* ctx, const verify_q4_weight* W, const char* name) {
+// A compute operand: tiled layout (`layout`), in device memory.
+verify_status check_q4(verify_ctx* ctx, const verify_q4_weight* W, const char* name, int layout = VERIFY_Q4_TILED) {
   if (!W) return fail(ctx, VERIFY_EINVAL, "%s is NULL", name);
   if (W->group_size != 64 || W->bits != 4) return fail(ctx, VERIFY_EUNSUPPORTED, "%s: only 4-bit, group 64", name);
-  if (W->k_in % 128 != 0 || W->k_in < 256 || W->k_in > kMaxKin)
-    return fail(ctx, VERIFY_EUNSUPPORTED, "%s: k_in must be a multiple of 128 in [256, 131072]", name);
-  if (W->n_out < 1 || W->n_out > kMaxN) return fail(ctx, VERIFY_EUNSUPPORTED, "%s: n_out out of range", name);
-  verify_status s;
-  if ((s = check_dev(ctx, W->packed, 16, "packed"))) return s;
-  if ((s = check_dev(ctx, W->scales, 4, "scales"))) return s;
-  if ((s = check_dev(ctx, W->biases, 4, "biases"))) return s;
-  return VERIFY_OK;
+  if (W->layout != layout)
+    return fail(ctx, VERIFY_EINVAL,
+                layout == VERIFY_Q4_TILED_GATE_UP ? "%s: expected the gate/up tiled layout (q4_tile with gate_up)"
+                                                  : "%s: expected the tiled layout (q4_tile)",
+                name);
+  if (!valid_shape(W->n_out, W->k_in))
+    return fail(ctx, VERIFY_EUNSUPPORTED, "%s: n_out in 1..2^20, k_in a multiple of 64 in [64, 131072]", name);
+  if (layout == VERIFY_Q4_TILED_GATE_UP && W->n_out % 128 != 0)
+    return fail(ctx, VERIFY_EUNSUPPORTED, "%s: gate/up rows must be 2I with I a multiple of 64", name);
+  return check_dev(ctx, W->packed, 16, name);
+}
+
+long long rt_bytes(int k_in) {
+  const long long KG = k_in / 64, KC = (KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
+  return (long long)vk::kTileSbBytes * KC + (long long)vk::kTileGroupBytes * KG;
 }
 
 // K-splits per row tile: the largest power of two (at most 8, the portable
@@ -155,12 +147,6 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = cudaMalloc(&ctx->st_idx, sizeof(int32_t) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_w, sizeof(float) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
   if ((e = cudaMemset(ctx->err, 0, sizeof(int)))) return bail(e);
-  cudaDriverEntryPointQueryResult q;
-  void* fn = nullptr;
-  if ((e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q)) ||
-      q != cudaDriverEntryPointSuccess || !fn)
-    return bail(e);
-  ctx->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   if ((e = vk::q4_setup_kernels(&ctx->dense_ctas_per_sm, &ctx->moe_ctas_per_sm))) return bail(e);
   if ((e = vk::gdn_setup_kernels())) return bail(e);
   if ((e = cudaDeviceSynchronize())) return bail(e);
@@ -205,6 +191,38 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
   return VERIFY_EDEVICE;
 }
 
+int64_t q4_tiled_bytes(int32_t n_out, int32_t k_in, int32_t n_experts, int32_t gate_up) {
+  if (!valid_shape(n_out, k_in) || n_experts < 1 || (gate_up && n_out % 128 != 0)) return -1;
+  return vk::tiled_bytes(n_out, k_in, n_experts, gate_up != 0);
+}
+
+verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_experts, int32_t gate_up, void* dst,
+                      int64_t dst_bytes, verify_q4_weight* out, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (!src || !out) return fail(ctx, VERIFY_EINVAL, "src or out is NULL%s");
+  if (src->layout != VERIFY_Q4_ROWS) return fail(ctx, VERIFY_EINVAL, "src must have the row layout%s");
+  if (src->group_size != 64 || src->bits != 4) return fail(ctx, VERIFY_EUNSUPPORTED, "only 4-bit, group 64%s");
+  const int64_t need = q4_tiled_bytes(src->n_out, src->k_in, n_experts, gate_up);
+  if (need < 0) return fail(ctx, VERIFY_EUNSUPPORTED, "shape or n_experts out of range%s");
+  if (dst_bytes < need) return fail(ctx, VERIFY_EINVAL, "dst_bytes is smaller than q4_tiled_bytes%s");
+  if ((s = check_dev(ctx, src->packed, 4, "packed"))) return s;
+  if ((s = check_dev(ctx, src->scales, 2, "scales"))) return s;
+  if ((s = check_dev(ctx, src->biases, 2, "biases"))) return s;
+  if ((s = check_dev(ctx, dst, 16, "dst"))) return s;
+  cudaError_t e = vk::launch_tile(src->packed, src->scales, src->biases, static_cast<uint8_t*>(dst), src->n_out,
+                                  src->k_in, n_experts, gate_up != 0, stream);
+  if (e) return cuda_fail(ctx, e, "q4_tile launch");
+  ctx->launches += 1;
+  *out = *src;
+  out->packed = static_cast<const uint32_t*>(dst);
+  out->scales = nullptr;
+  out->biases = nullptr;
+  out->layout = gate_up ? VERIFY_Q4_TILED_GATE_UP : VERIFY_Q4_TILED;
+  return VERIFY_OK;
+}
+
 verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W, const uint16_t* x, int k, void* y,
                        int dtype_out, struct CUstream_st* stream) {
   if (!ctx) return VERIFY_EINVAL;
@@ -217,14 +235,13 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W, const uint16_
   if ((s = check_dev(ctx, y, dtype_out == VERIFY_BF16 ? 2 : 4, "y"))) return s;
 
   vk::DenseArgs a{};
-  a.scales = W->scales; a.biases = W->biases; a.x = x; a.y = y; a.err = ctx->err;
+  a.tiles = reinterpret_cast<const uint8_t*>(W->packed); a.rt_bytes = rt_bytes(W->k_in);
+  a.x = x; a.y = y; a.err = ctx->err;
   a.N = W->n_out; a.K = W->k_in; a.k = k; a.dtype = dtype_out;
   a.KG = a.K / 64; a.KC = (a.KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
   a.RB = (a.N + vk::kBM - 1) / vk::kBM;
   a.S = dense_splits(ctx, a.RB, a.KC);
-  CUtensorMap map;
-  if ((s = make_wmap(ctx, &map, W->packed, (uint64_t)a.N, (uint64_t)a.K / 8, vk::kBM))) return s;
-  cudaError_t e = vk::launch_q4_dense(map, a, k <= 8 ? 1 : 2, ctx->pdl, stream);
+  cudaError_t e = vk::launch_q4_dense(a, k <= 8 ? 1 : 2, ctx->pdl, stream);
   if (e) return cuda_fail(ctx, e, "q4_qmv_k launch");
   ctx->launches += 1;
   return VERIFY_OK;
@@ -244,13 +261,13 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   if (E < 1 || E > vk::kMaxExperts || down->n_experts != E)
     return fail(ctx, VERIFY_EUNSUPPORTED, "n_experts must match and be in 1..512%s");
   if (top_k < 1 || top_k > vk::kMaxTopK || top_k > E) return fail(ctx, VERIFY_EUNSUPPORTED, "top_k out of range%s");
-  if ((s = check_q4(ctx, &gate_up->w, "gate_up"))) return s;
+  if ((s = check_q4(ctx, &gate_up->w, "gate_up", VERIFY_Q4_TILED_GATE_UP))) return s;
   if ((s = check_q4(ctx, &down->w, "down"))) return s;
   const int H = gate_up->w.k_in, I = gate_up->w.n_out / 2;
   if (gate_up->w.n_out != 2 * I || down->w.n_out != H || down->w.k_in != I)
     return fail(ctx, VERIFY_EINVAL, "expert shapes must be gate_up [2I, H], down [H, I]%s");
-  if (H > kMaxH || I > kMaxI || I % 128 != 0)
-    return fail(ctx, VERIFY_EUNSUPPORTED, "H <= 8192, I <= 4096, multiples of 128%s");
+  if (H > kMaxH || I > kMaxI || I % 64 != 0)
+    return fail(ctx, VERIFY_EUNSUPPORTED, "H <= 8192, I <= 4096, multiples of 64%s");
   if (logits_ld < E) return fail(ctx, VERIFY_EINVAL, "logits_ld < n_experts%s");
   if ((s = check_dtype(ctx, dtype_out, true))) return s;
   if ((s = check_dev(ctx, logits, 4, "logits"))) return s;
@@ -262,7 +279,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   if (n_shared != 0 && n_shared != 3)
     return fail(ctx, VERIFY_EINVAL, "shared expert: give all of gate_up, down and gate logit, or none%s");
   if (n_shared == 3) {
-    if ((s = check_q4(ctx, shared_gate_up, "shared_gate_up"))) return s;
+    if ((s = check_q4(ctx, shared_gate_up, "shared_gate_up", VERIFY_Q4_TILED_GATE_UP))) return s;
     if ((s = check_q4(ctx, shared_down, "shared_down"))) return s;
     if (shared_gate_up->n_out != 2 * I || shared_gate_up->k_in != H || shared_down->n_out != H ||
         shared_down->k_in != I)
@@ -270,32 +287,24 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
     if ((s = check_dev(ctx, shared_gate_logit, 4, "shared_gate_logit"))) return s;
   }
 
-  CUtensorMap gu, dn, sgu, sdn;
-  if ((s = make_wmap(ctx, &gu, gate_up->w.packed, (uint64_t)E * 2 * I, (uint64_t)H / 8, 64))) return s;
-  if ((s = make_wmap(ctx, &dn, down->w.packed, (uint64_t)E * H, (uint64_t)I / 8, vk::kBM))) return s;
-  if (n_shared == 3) {
-    if ((s = make_wmap(ctx, &sgu, shared_gate_up->packed, (uint64_t)2 * I, (uint64_t)H / 8, 64))) return s;
-    if ((s = make_wmap(ctx, &sdn, shared_down->packed, (uint64_t)H, (uint64_t)I / 8, vk::kBM))) return s;
-  } else {
-    sgu = gu;
-    sdn = dn;
-  }
   vk::MoeArgs a{};
   a.logits = logits; a.logits_ld = logits_ld; a.shared_logit = n_shared ? shared_gate_logit : nullptr;
   a.x = x;
-  a.gu_scales = gate_up->w.scales; a.gu_biases = gate_up->w.biases;
-  a.dn_scales = down->w.scales; a.dn_biases = down->w.biases;
+  a.gu_tiles = reinterpret_cast<const uint8_t*>(gate_up->w.packed);
+  a.dn_tiles = reinterpret_cast<const uint8_t*>(down->w.packed);
   if (n_shared) {
-    a.sgu_scales = shared_gate_up->scales; a.sgu_biases = shared_gate_up->biases;
-    a.sdn_scales = shared_down->scales; a.sdn_biases = shared_down->biases;
+    a.sgu_tiles = reinterpret_cast<const uint8_t*>(shared_gate_up->packed);
+    a.sdn_tiles = reinterpret_cast<const uint8_t*>(shared_down->packed);
   }
+  a.gu_rt_bytes = rt_bytes(H);
+  a.dn_rt_bytes = rt_bytes(I);
   a.hbuf = ctx->moe_hbuf; a.part = ctx->moe_part;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
   a.G = ctx->moe_ctas_per_sm * ctx->num_sms;
   int launched = 0;
-  cudaError_t e = vk::launch_moe(gu, dn, sgu, sdn, a, k <= 8 ? 1 : 2, ctx->pdl, stream, &launched);
+  cudaError_t e = vk::launch_moe(a, k <= 8 ? 1 : 2, ctx->pdl, stream, &launched);
   ctx->launches += launched;
   if (e) return cuda_fail(ctx, e, "q4_gather_experts_k launch");
   return VERIFY_OK;

@@ -33,7 +33,7 @@ class DeviceStack:
     """All layers' weights and GDN state slots on the current CUDA device."""
 
     def __init__(self, vf: B.Verify, cfg, seed: int = 0, n_slots: int = 10, s_std: float = 0.02,
-                 tail_std: float = 1.0, layers: int | None = None):
+                 tail_std: float = 1.0, layers: int | None = None, keep_rows: bool = False):
         import torch
 
         self.vf, self.cfg, self.seed = vf, cfg, seed
@@ -43,11 +43,13 @@ class DeviceStack:
         H, E, I = sh["H"], sh["E"], sh["I"]
         d, Hk, Hv = cfg["d"], cfg["n_qk_heads"], cfg["n_v_heads"]
         self.keep = []
+        self.rows = []  # with keep_rows: the row-layout (packed, scales, biases) of every Q4 tensor, in draw order
         self.layers = []
         self.states = []
         self.state_tensors = []
 
-        def q4(name, n_out, k_in, n_experts=None):
+        def q4(name, n_out, k_in, n_experts=None, gate_up=False):
+            # drawn in the row layout, kept only in the tiled layout
             e = 1 if n_experts is None else n_experts
             shp = (e, n_out, k_in // 8) if n_experts else (n_out, k_in // 8)
             gshp = (e, n_out, k_in // 64) if n_experts else (n_out, k_in // 64)
@@ -55,8 +57,14 @@ class DeviceStack:
             sc = torch.empty(gshp, dtype=torch.int16, device="cuda")
             bi = torch.empty(gshp, dtype=torch.int16, device="cuda")
             vf.synth_q4(p, sc, bi, S.q4_seeds(seed, name), S.SCALE_RANGE, S.CENTERED_RANGE, centered=True)
-            self.keep += [p, sc, bi]
-            return B.q4_experts(p, sc, bi) if n_experts else B.q4_weight(p, sc, bi)
+            rows = B.q4_experts(p, sc, bi) if n_experts else B.q4_weight(p, sc, bi)
+            t = vf.tile(rows, gate_up=gate_up)
+            torch.cuda.synchronize()
+            if keep_rows:
+                self.rows.append((p, sc, bi))
+            del p, sc, bi
+            self.keep.append(t.buf)
+            return t.struct
 
         def dev(a):
             t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
@@ -70,9 +78,9 @@ class DeviceStack:
             L.in_proj = q4(nm["in_proj"], sh["NP"], H)
             L.out_proj = q4(nm["out_proj"], H, sh["Z"])
             L.router = q4(nm["router"], E + 1, H)
-            L.gate_up = q4(nm["gate_up"], 2 * I, H, E)
+            L.gate_up = q4(nm["gate_up"], 2 * I, H, E, gate_up=True)
             L.down = q4(nm["down"], H, I, E)
-            L.shared_gate_up = q4(nm["shared_gate_up"], 2 * I, H)
+            L.shared_gate_up = q4(nm["shared_gate_up"], 2 * I, H, gate_up=True)
             L.shared_down = q4(nm["shared_down"], H, I)
             L.gdn = B.gdn_params(Hk, Hv, d, gp["conv_w"], gp["A_log"], gp["dt_bias"], gp["norm_w"])
             L.norm1_w = dev(S.f32_uniform(seed, nm["norm1"], (H,), -0.1, 0.1)).data_ptr()

@@ -30,14 +30,17 @@ def host(t, dtype=None):
 
 
 class DevQ4:
-    """A Q4Matrix (synth) copied to the device, with its library struct."""
+    """A Q4Matrix (synth) copied to the device in the row layout (`rows`), and
+    its tiled form for the compute calls (`struct`, kept alive by `tiled`)."""
 
-    def __init__(self, m):
+    def __init__(self, vf, m, gate_up=False):
         self.packed, self.scales, self.biases = dev(m.packed), dev(m.scales), dev(m.biases)
         if m.packed.ndim == 3:
-            self.struct = B.q4_experts(self.packed, self.scales, self.biases)
+            self.rows = B.q4_experts(self.packed, self.scales, self.biases)
         else:
-            self.struct = B.q4_weight(self.packed, self.scales, self.biases)
+            self.rows = B.q4_weight(self.packed, self.scales, self.biases)
+        self.tiled = vf.tile(self.rows, gate_up=gate_up)
+        self.struct = self.tiled.struct
 
 
 def rel_err(gpu, ref):

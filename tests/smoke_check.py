@@ -19,7 +19,7 @@ def run():
     m = S.q4_matrix(0, "tiny.q4", 512, 512)
     x = S.bf16_normal(0, "smoke.x", (k, 512))
     y = torch.zeros((k, 512), device="cuda")
-    W = DevQ4(m)  # keeps the device tensors alive while the struct points at them
+    W = DevQ4(vf, m)  # keeps the device tensors alive while the struct points at them
     xd = dev(x)
     vf.q4_qmv_k(W.struct, xd, k, y)
     torch.cuda.synchronize()
@@ -33,7 +33,7 @@ def run():
     idx = torch.zeros((k, T), dtype=torch.int32, device="cuda")
     w = torch.zeros((k, T), device="cuda")
     ym = torch.zeros((k, H), device="cuda")
-    GU, DN = DevQ4(gu), DevQ4(dn)
+    GU, DN = DevQ4(vf, gu, True), DevQ4(vf, dn)
     lgd, xmd = dev(lg), dev(xm)
     vf.q4_gather_experts_k(GU.struct, DN.struct, lgd, E, T, xmd, k, idx, w, ym)
     torch.cuda.synchronize()

@@ -61,10 +61,25 @@ def test_small_moe_matches_oracle(vf, k):
     logits = S.f32_normal(10, f"moe.l{k}", (k, E))
     oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
                                      logits, T, x)
-    gi, gw, gy = gather(vf, DevQ4(gu), DevQ4(dn), dev(logits), T, dev(x), k, H)
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(logits), T, dev(x), k, H)
     assert np.array_equal(gi, oi)
     np.testing.assert_allclose(gw, ow, rtol=1e-5, atol=1e-6)
     assert_close(gy, oy, what=f"k={k}")
+
+
+@pytest.mark.parametrize("k", [3, 9])
+def test_moe_with_k_not_a_multiple_of_128(vf, k):
+    """H = 320 and I = 192: partial 256-column chunks on both products and a
+    ragged last 128-row tile of the down product."""
+    E, H, I, T = 12, 320, 192, 3
+    gu, dn = moe_case(12, E, H, I)
+    x = S.bf16_normal(12, f"moe.r.x{k}", (k, H))
+    logits = S.f32_normal(12, f"moe.r.l{k}", (k, E))
+    oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
+                                     logits, T, x)
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(logits), T, dev(x), k, H)
+    assert np.array_equal(gi, oi)
+    assert_close(gy, oy, what=f"H=320 I=192 k={k}")
 
 
 def test_shared_expert_and_ragged_down(vf):
@@ -83,8 +98,8 @@ def test_shared_expert_and_ragged_down(vf):
     # the shared gate logit is read at row stride logits_ld = E: store it in a [k, E] array
     slm = np.zeros((k, E), np.float32)
     slm[:, 0] = sl
-    gi, gw, gy = gather(vf, DevQ4(gu), DevQ4(dn), dev(logits), T, dev(x), k, H,
-                        shared=(DevQ4(sgu), DevQ4(sdn), dev(slm)))
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(logits), T, dev(x), k, H,
+                        shared=(DevQ4(vf, sgu, True), DevQ4(vf, sdn), dev(slm)))
     assert np.array_equal(gi, oi)
     assert_close(gy, oy, what="shared")
 
@@ -92,7 +107,7 @@ def test_shared_expert_and_ragged_down(vf):
 def test_width_k_rows_bit_identical_to_width_1(vf):
     E, H, I, T = 32, 512, 256, 8
     gu, dn = moe_case(12, E, H, I)
-    G, D = DevQ4(gu), DevQ4(dn)
+    G, D = DevQ4(vf, gu, True), DevQ4(vf, dn)
     x = S.bf16_normal(12, "moe.xb", (9, H))
     logits = S.f32_normal(12, "moe.lb", (9, E))
     _, _, y9 = gather(vf, G, D, dev(logits), T, dev(x), 9, H)
@@ -111,10 +126,10 @@ def test_single_expert_reduces_to_dense_products(vf):
     logits = np.full((k, E), -2.0, np.float32)
     logits[:, 5] = 3.0
     x = S.bf16_normal(13, "moe.x1", (k, H))
-    gi, gw, gy = gather(vf, DevQ4(gu), DevQ4(dn), dev(logits), 1, dev(x), k, H)
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(logits), 1, dev(x), k, H)
     assert np.all(gi == 5) and np.all(gw == 1.0)
-    Wg = DevQ4(S.Q4Matrix(gu.packed[5], gu.scales[5], gu.biases[5], 2 * I, H))
-    Wd = DevQ4(S.Q4Matrix(dn.packed[5], dn.scales[5], dn.biases[5], H, I))
+    Wg = DevQ4(vf, S.Q4Matrix(gu.packed[5], gu.scales[5], gu.biases[5], 2 * I, H))
+    Wd = DevQ4(vf, S.Q4Matrix(dn.packed[5], dn.scales[5], dn.biases[5], H, I))
     g = torch.zeros((k, 2 * I), device="cuda")
     vf.q4_qmv_k(Wg.struct, dev(x), k, g)
     torch.cuda.synchronize()
@@ -143,12 +158,8 @@ def test_ornith_shape_matches_oracle(vf):
     vf.synth_q4(gu_p, gu_s, gu_b, seeds_gu, S.SCALE_RANGE, S.BIAS_RANGE)
     vf.synth_q4(dn_p, dn_s, dn_b, seeds_dn, S.SCALE_RANGE, S.BIAS_RANGE)
 
-    class W:
-        pass
-
-    G, D = W(), W()
-    G.struct = B.q4_experts(gu_p, gu_s, gu_b)
-    D.struct = B.q4_experts(dn_p, dn_s, dn_b)
+    G = vf.tile(B.q4_experts(gu_p, gu_s, gu_b), gate_up=True)
+    D = vf.tile(B.q4_experts(dn_p, dn_s, dn_b))
     for k in (2, 9):
         x = S.bf16_normal(0, f"ornith.x{k}", (k, H))
         logits = S.f32_normal(0, f"ornith.l{k}", (k, E))

@@ -41,7 +41,7 @@ def run_qmv(vf, W, x_dev, k, N, dtype=B.F32, y=None):
 def test_tiny_projection_matches_oracle_widths_1_to_4(vf):
     """512 x 512, k = 1..4, seed 0 (the tiny workload)."""
     m = S.q4_matrix(0, "tiny.q4", 512, 512)
-    W = DevQ4(m)
+    W = DevQ4(vf, m)
     for k in range(1, 5):
         x = S.bf16_normal(0, f"tiny.x{k}", (k, 512))
         ref = O.q4_qmv(m.packed, m.scales, m.biases, x)
@@ -49,11 +49,12 @@ def test_tiny_projection_matches_oracle_widths_1_to_4(vf):
         assert_close(y, ref, what=f"k={k}")
 
 
-@pytest.mark.parametrize("N,K", [(1, 256), (96, 2560), (100, 640), (129, 1152), (300, 512), (1000, 2048)])
+@pytest.mark.parametrize("N,K", [(1, 256), (96, 2560), (100, 640), (129, 1152), (300, 512), (1000, 2048),
+                                 (200, 576), (130, 192), (5, 64)])
 @pytest.mark.parametrize("k", [1, 5, 9, 16])
 def test_ragged_shapes_match_oracle(vf, N, K, k):
     m = S.q4_matrix(1, f"rag.{N}.{K}", N, K)
-    W = DevQ4(m)
+    W = DevQ4(vf, m)
     x = S.bf16_normal(1, f"rag.x.{N}.{K}.{k}", (k, K))
     ref = O.q4_qmv(m.packed, m.scales, m.biases, x)
     y = host(run_qmv(vf, W, dev(x), k, N))
@@ -63,7 +64,7 @@ def test_ragged_shapes_match_oracle(vf, N, K, k):
 @pytest.mark.parametrize("N,K", [(512, 512), (100, 640), (1000, 2048), (5120, 5120)])
 def test_width_k_rows_bit_identical_to_width_1(vf, N, K):
     m = S.q4_matrix(2, f"bit.{N}.{K}", N, K)
-    W = DevQ4(m)
+    W = DevQ4(vf, m)
     x = S.bf16_normal(2, f"bit.x.{N}.{K}", (16, K))
     xd = dev(x)
     singles = [host(run_qmv(vf, W, dev(x[r:r + 1]), 1, N))[0] for r in range(16)]
@@ -83,7 +84,7 @@ def test_exact_integer_case_is_bitwise(vf):
     biases = S.f32_to_bf16((rng.integers(-1, 2, size=(N, K // 64)) * 0.0625).astype(np.float32))
     x = S.f32_to_bf16(rng.integers(-2, 3, size=(k, K)).astype(np.float32))
     ref = O.q4_qmv(packed, scales, biases, x)
-    W = DevQ4(S.Q4Matrix(packed, scales, biases, N, K))
+    W = DevQ4(vf, S.Q4Matrix(packed, scales, biases, N, K))
     y = host(run_qmv(vf, W, dev(x), k, N))
     assert np.array_equal(y.astype(np.float64), ref)
 
@@ -92,7 +93,7 @@ def test_bf16_and_accumulate_outputs(vf):
     import torch
 
     m = S.q4_matrix(3, "dt.q4", 640, 1024)
-    W = DevQ4(m)
+    W = DevQ4(vf, m)
     x = dev(S.bf16_normal(3, "dt.x", (7, 1024)))
     y32 = host(run_qmv(vf, W, x, 7, 640))
     y16 = host(run_qmv(vf, W, x, 7, 640, dtype=B.BF16), np.uint16)
@@ -115,7 +116,8 @@ def test_dense_full_size_sampled_rows(vf, N, K):
     scales = torch.empty((N, K // 64), dtype=torch.int16, device="cuda")
     biases = torch.empty((N, K // 64), dtype=torch.int16, device="cuda")
     vf.synth_q4(packed, scales, biases, (sp, ss, sb), S.SCALE_RANGE, S.BIAS_RANGE)
-    W = B.q4_weight(packed, scales, biases)
+    Wt = vf.tile(B.q4_weight(packed, scales, biases))
+    W = Wt.struct
     x = S.bf16_normal(0, name + ".x", (9, K))
     rows = np.unique(np.concatenate([[0, N - 1], np.random.default_rng(N + K).integers(0, N, 46)]))
     sub = S.q4_rows(0, name, N, K, rows)
@@ -139,7 +141,7 @@ def test_argument_errors_are_reported_before_launch(vf):
     import torch
 
     m = S.q4_matrix(4, "err.q4", 128, 512)
-    W = DevQ4(m)
+    W = DevQ4(vf, m)
     x = dev(S.bf16_normal(4, "err.x", (2, 512)))
     y = torch.zeros((2, 128), device="cuda")
     before = vf.launch_count()
@@ -153,12 +155,15 @@ def test_argument_errors_are_reported_before_launch(vf):
     with pytest.raises(B.VerifyError) as e:
         vf.q4_qmv_k(W.struct, hx, 2, y)
     assert e.value.status == B.EINVAL
-    bad = B.Q4Weight(W.struct.packed, W.struct.scales, W.struct.biases, 128, 576, 64, 4)
+    bad = B.Q4Weight(W.struct.packed, None, None, 128, 520, 64, 4, B.TILED)  # k_in % 64 != 0
     with pytest.raises(B.VerifyError) as e:
         vf.q4_qmv_k(bad, x, 2, y)
     assert e.value.status == B.EUNSUPPORTED
-    bad = B.Q4Weight(W.struct.packed, W.struct.scales, W.struct.biases, 128, 512, 32, 4)
+    bad = B.Q4Weight(W.struct.packed, None, None, 128, 512, 32, 4, B.TILED)  # group 32
     with pytest.raises(B.VerifyError) as e:
         vf.q4_qmv_k(bad, x, 2, y)
     assert e.value.status == B.EUNSUPPORTED
+    with pytest.raises(B.VerifyError) as e:  # the row layout is only an input of q4_tile
+        vf.q4_qmv_k(W.rows, x, 2, y)
+    assert e.value.status == B.EINVAL
     assert vf.launch_count() == before

@@ -1,5 +1,5 @@
 """GPU parity of a full hybrid verify layer stack (verify_layer_k: GDN mixer
-then routed + shared MoE, 8 kernels per layer) against the oracle's
+then routed + shared MoE, 9 kernels per layer) against the oracle's
 composition of its pinned pieces.
 
 Pages: "QWEN38FLASH.md - Plan for supporting Qwen/Qwen3.8-Flash-Next" section 2
@@ -156,18 +156,18 @@ def test_stack_rows_equal_single_row_steps(vf):
 def test_device_weights_match_host_redraw(vf):
     """The stack's weights drawn on the device (centred recipe) are the host
     generator's bits: the oracle side re-draws exactly what the GPU uses."""
-    ds = DeviceStack(vf, SMALL, seed=3, layers=1)
+    ds = DeviceStack(vf, SMALL, seed=3, layers=1, keep_rows=True)
     sh = shapes(SMALL)
     w = S.HostLayerWeights(3, 0, sh["H"], sh["NP"], sh["Z"], sh["E"], sh["I"], SMALL["n_qk_heads"],
                            SMALL["n_v_heads"], SMALL["d"])
-    # keep: 4 GDN parameter tensors, then (packed, scales, biases) of in_proj,
-    # out_proj, router, gate_up, down, shared gate/up, shared down
-    dev_t = ds.keep
-    assert np.array_equal(host(dev_t[4]).view(np.uint32), w.in_proj[0])
-    assert np.array_equal(host(dev_t[5]).view(np.uint16), w.in_proj[1])
-    assert np.array_equal(host(dev_t[6]).view(np.uint16), w.in_proj[2])
+    # rows: (packed, scales, biases) of in_proj, out_proj, router, gate_up, down,
+    # shared gate/up, shared down
+    ip, _, _, gup = ds.rows[0], ds.rows[1], ds.rows[2], ds.rows[3]
+    assert np.array_equal(host(ip[0]).view(np.uint32), w.in_proj[0])
+    assert np.array_equal(host(ip[1]).view(np.uint16), w.in_proj[1])
+    assert np.array_equal(host(ip[2]).view(np.uint16), w.in_proj[2])
     gu, dn = w.expert(5)
-    assert np.array_equal(host(dev_t[13][5]).view(np.uint32), gu[0])
-    assert np.array_equal(host(dev_t[14][5]).view(np.uint16), gu[1])
-    assert np.array_equal(host(dev_t[15][5]).view(np.uint16), gu[2])
+    assert np.array_equal(host(gup[0][5]).view(np.uint32), gu[0])
+    assert np.array_equal(host(gup[1][5]).view(np.uint16), gu[1])
+    assert np.array_equal(host(gup[2][5]).view(np.uint16), gu[2])
     assert np.all(w.in_proj[2].view(np.int16) < 0)  # centred biases are negative

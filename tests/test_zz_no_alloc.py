@@ -45,7 +45,7 @@ def test_noalloc_matches_regular_entry_point_on_two_calls():
     dn = S.q4_matrix(50, "na.dn", H, I, n_experts=E)
     sgu = S.q4_matrix(50, "na.sgu", 2 * I, H)
     sdn = S.q4_matrix(50, "na.sdn", H, I)
-    GU, DN, SGU, SDN = DevQ4(gu), DevQ4(dn), DevQ4(sgu), DevQ4(sdn)
+    GU, DN, SGU, SDN = DevQ4(vf, gu, True), DevQ4(vf, dn), DevQ4(vf, sgu, True), DevQ4(vf, sdn)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for call, k in enumerate([9, 4]):  # two calls in a row, different widths
         x = dev(S.bf16_normal(50, f"na.x{call}", (k, H)))
@@ -80,11 +80,11 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
 
     lib = B.load()
     E, H, I, T, k = 16, 8192, 256, 16, 16  # k*T*H*4 = 8 MiB of partials alone: too large
-    gu = torch.zeros((E, 2 * I, H // 8), dtype=torch.int32, device="cuda")
-    gs = torch.zeros((E, 2 * I, H // 64), dtype=torch.int16, device="cuda")
-    dn = torch.zeros((E, H, I // 8), dtype=torch.int32, device="cuda")
-    ds = torch.zeros((E, H, I // 64), dtype=torch.int16, device="cuda")
-    GU, DN = B.q4_experts(gu, gs, gs), B.q4_experts(dn, ds, ds)
+    # tiled operands of the right shapes (the call stops at the size check)
+    gu = torch.zeros(int(lib.q4_tiled_bytes(2 * I, H, E, 1)), dtype=torch.uint8, device="cuda")
+    dn = torch.zeros(int(lib.q4_tiled_bytes(H, I, E, 0)), dtype=torch.uint8, device="cuda")
+    GU = B.Q4Experts(B.Q4Weight(gu.data_ptr(), None, None, 2 * I, H, 64, 4, B.TILED_GATE_UP), E)
+    DN = B.Q4Experts(B.Q4Weight(dn.data_ptr(), None, None, H, I, 64, 4, B.TILED), E)
     x = torch.zeros((k, H), dtype=torch.int16, device="cuda")
     logits = torch.zeros((k, E), device="cuda")
     idx = torch.zeros((k, E), dtype=torch.int32, device="cuda")
