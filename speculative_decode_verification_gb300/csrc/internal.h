@@ -14,7 +14,9 @@ constexpr int kStages = 4;         // pipeline depth
 constexpr int kDenseWarps = 4;     // consumer warps of the dense kernel: two 16-row MMA tiles each
 constexpr int kGateUpWarps = 4;    // fused gate/up: a gate tile and its up tile per warp
 constexpr int kDownWarps = 4;      // routed down projection: two 16-row MMA tiles each
-constexpr int kQ4CtasPerSm = 2;
+constexpr int kQ4CtasPerSm = 2;    // dense kernels
+constexpr int kMoeCtasPerSm = 3;   // routed-expert kernels: 8 activation rows per stage, three stages
+constexpr int kMoeStages = 3;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 
@@ -82,7 +84,7 @@ cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm);
 // pdl: launch with programmatic stream serialization (the kernel may start
 // while the previous kernel on the stream runs; see griddep_wait).
 cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s);
-cudaError_t launch_moe(const MoeArgs& a, int nt, bool pdl, cudaStream_t s, int* launches);
+cudaError_t launch_moe(const MoeArgs& a, bool pdl, cudaStream_t s, int* launches);
 // Tiled layout: bytes of E matrices [N, K] (gate_up: tiles pair gate and up rows),
 // and the conversion from the row-major layout.
 long long tiled_bytes(int N, int K, int E, bool gate_up);

@@ -139,6 +139,6 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   // device error and left it set.
   if (!device_error && cudaMemsetAsync(err_word, 0, sizeof(int), stream) != cudaSuccess) return VERIFY_ECUDA;
   int launched = 0;
-  if (vk::launch_moe(a, k <= 8 ? 1 : 2, false, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
+  if (vk::launch_moe(a, false, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
   return VERIFY_OK;
 }

@@ -41,17 +41,18 @@ namespace vk {
 
 // A stage: [scales, biases][codes][activation rows].  The first two parts are
 // one block of the tiled weight layout (tile.cu), copied with one bulk copy.
-template <int NT>
+template <int NT, int ST = kStages>
 struct Q4Layout {
+  static constexpr int STAGES = ST;                          // pipeline depth
   static constexpr int NB = 8 * NT;                          // activation rows held per stage
   static constexpr int SB_BYTES = kTileSbBytes;              // scales then biases, [row][4 groups]
   static constexpr int W_BYTES = kBM * 128;                  // codes, fragment order, [group][16-row block][lane]
   static constexpr int X_BYTES = kGroupsPerUnit * NB * 128;  // [group][row][64 bf16]
   static constexpr int STAGE = SB_BYTES + W_BYTES + X_BYTES;
   static constexpr int SX_BYTES = kGroupsPerUnit * NB * 4;   // fp32 group sums [group][row]
-  static constexpr int SX_OFF = kStages * STAGE;             // one slot per stage, after the stages
-  static constexpr int BAR_OFF = SX_OFF + kStages * SX_BYTES;
-  static constexpr int MISC_OFF = BAR_OFF + 2 * kStages * 8;
+  static constexpr int SX_OFF = ST * STAGE;                  // one slot per stage, after the stages
+  static constexpr int BAR_OFF = SX_OFF + ST * SX_BYTES;
+  static constexpr int MISC_OFF = BAR_OFF + 2 * ST * 8;
   static constexpr int MISC_BYTES = 64 + 16 * 8;             // flags, then the producer's row-pointer table
   static constexpr int BASE_BYTES = MISC_OFF + MISC_BYTES;
   static_assert(STAGE % 128 == 0, "stages keep 128-byte alignment");
@@ -76,9 +77,11 @@ struct Warps {
 struct RouteSmem {
   uint32_t mask[kMaxExperts];      // bit r set: row r selected the expert
   int16_t ulist[kMaxExperts];      // distinct selected experts, ascending
+  int16_t vlist[2 * kMaxExperts + 2];  // work units: expert slot u (< U, or U = shared) | row chunk << 12
   int32_t idx[16 * kMaxTopK];      // [r][j]
   float w[16 * kMaxTopK];          // [r][j]
   int U;
+  int V;
 };
 
 // ---------------------------------------------------------------- producer
@@ -130,10 +133,11 @@ __device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_
 }
 
 // On abort the producer keeps the CTA alive until its bulk copies have landed.
+template <int ST = kStages>
 __device__ __forceinline__ void producer_drain(uint32_t bar_base, long long fills) {
-  for (long long f = (fills > kStages ? fills - kStages : 0); f < fills; ++f) {
-    const int s = (int)(f % kStages);
-    const uint32_t ph = (uint32_t)((f / kStages) & 1);
+  for (long long f = (fills > ST ? fills - ST : 0); f < fills; ++f) {
+    const int s = (int)(f % ST);
+    const uint32_t ph = (uint32_t)((f / ST) & 1);
     const long long t0 = clock64();
     while (!mbar_try_wait(bar_base + 8 * s, ph) && clock64() - t0 < kWaitTimeoutCycles) {
     }
@@ -299,12 +303,12 @@ __device__ __forceinline__ void zero_acc(float (&acc)[MT][NT][4]) {
       for (int q = 0; q < 4; ++q) acc[m][t][q] = 0.f;
 }
 
-template <int CW>
+template <int CW, int ST = kStages>
 __device__ __forceinline__ void init_barriers(uint32_t bar_base) {
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_base + 8 * s, 33);              // full: lane 0's tx arrival + 32 cp.async arrivals
-      mbar_init(bar_base + 8 * (kStages + s), CW);  // empty: one arrival per consumer warp
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(bar_base + 8 * s, 33);         // full: lane 0's tx arrival + 32 cp.async arrivals
+      mbar_init(bar_base + 8 * (ST + s), CW);  // empty: one arrival per consumer warp
     }
     fence_mbar_init();
   }
@@ -492,6 +496,26 @@ __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
       running += __popc(bal);
     }
     if (lane == 0) rs->U = running;
+    __syncwarp();
+    // Work units: (expert slot u, chunk of 8 of its rows), the chunks of one
+    // expert adjacent so that its weights are read back to back (L2).  Slot
+    // U is the shared expert (every row).
+    const int slots = running + (a.has_shared ? 1 : 0);
+    int vrun = 0;
+    for (int base = 0; base < slots; base += 32) {
+      const int u = base + lane;
+      int nch = 0;
+      if (u < slots) nch = ((u < running ? __popc(rs->mask[rs->ulist[u]]) : a.k) + 7) >> 3;
+      int incl = nch;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      for (int c = 0; c < nch; ++c) rs->vlist[vrun + incl - nch + c] = (int16_t)(u | (c << 12));
+      vrun += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) rs->V = vrun;
   }
   __syncthreads();
 }
@@ -517,38 +541,36 @@ __device__ __forceinline__ int pairs_of(const RouteSmem* rs, const MoeArgs& a, i
 }
 
 // One item of a MoE kernel on the consumer side: the stage loop and the
-// epilogue.  NTC MMA column blocks are computed on stages laid out for NTL.
-template <int NTC, int NTL, int CW, bool GATEUP>
+// epilogue.  The item covers rows 8 rc .. 8 rc + nb - 1 of expert slot u.
+template <int CW, bool GATEUP, int ST>
 __device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, uint8_t* smem, uint32_t bar_base,
-                                         volatile int* abort, int u, int tile, int nb, int KC,
-                                         int KG, int TS, int n_experts, const int (&rbase)[Warps<CW>::MT], int lane,
-                                         long long& fills) {
-  using L = Q4Layout<NTL>;
+                                         volatile int* abort, int u, int rc, int tile, int nb, int KC, int KG, int TS,
+                                         const int (&rbase)[Warps<CW>::MT], int lane, long long& fills) {
+  using L = Q4Layout<1, ST>;
   constexpr int MT = Warps<CW>::MT;
   const int warp = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
-  float acc[MT][NTC][4];
-  zero_acc<MT, NTC>(acc);
+  float acc[MT][1][4];
+  zero_acc<MT, 1>(acc);
   for (int kc = 0; kc < KC; ++kc, ++fills) {
-    const int s = (int)(fills % kStages);
-    const uint32_t ph = (uint32_t)((fills / kStages) & 1);
+    const int s = (int)(fills % ST);
+    const uint32_t ph = (uint32_t)((fills / ST) & 1);
     const bool ok = mbar_wait(bar_base + 8 * s, ph, abort, a.err);
     const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
-    consume_stage<NTC, CW, L::NB>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
-                                  lane, acc, ok);
+    consume_stage<1, CW, L::NB>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
+                                lane, acc, ok);
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
+    if (lane == 0) mbar_arrive(bar_base + 8 * (ST + s));
   }
   // pair ids of this thread's columns
-  long long pid[NTC][2];
+  long long pid[1][2];
 #pragma unroll
-  for (int t = 0; t < NTC; ++t)
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int b = 8 * t + 2 * c + q;
-      int r = 0, j = 0;
-      if (b < nb) pair_of(rs, a, u, b, r, j);
-      pid[t][q] = b < nb ? (long long)r * TS + j : -1;
-    }
+  for (int q = 0; q < 2; ++q) {
+    const int b = 2 * c + q;
+    int r = 0, j = 0;
+    if (b < nb) pair_of(rs, a, u, 8 * rc + b, r, j);
+    pid[0][q] = b < nb ? (long long)r * TS + j : -1;
+  }
+  constexpr int NTC = 1;
   if (GATEUP) {
     if (*abort) return;
 #pragma unroll
@@ -610,10 +632,11 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
 // Items are expert-major: consecutive CTAs stream consecutive slices of one
 // expert (measured much faster than block-major order, which spreads the
 // concurrent reads over all selected experts).
-template <int NT, bool GATEUP>
-__global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS, kQ4CtasPerSm)
+template <bool GATEUP>
+__global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS, kMoeCtasPerSm)
     moe_kernel(const MoeArgs a) {
-  using L = Q4Layout<NT>;
+  constexpr int ST = kMoeStages;
+  using L = Q4Layout<1, ST>;
   constexpr int CW = GATEUP ? kGateUpWarps : kDownWarps, MT = Warps<CW>::MT;
   static_assert(!GATEUP || MT == 2, "gate/up pairs the gate and up row tiles in one warp");
   extern __shared__ uint8_t smem_raw[];
@@ -622,7 +645,7 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
   RouteSmem* rs = reinterpret_cast<RouteSmem*>(smem + L::BASE_BYTES);
   if (threadIdx.x == 0) *abort = 0;
-  init_barriers<CW>(bar_base);
+  init_barriers<CW, ST>(bar_base);
   // Gate/up routes from logits the previous kernel wrote: wait first.  The
   // down kernel's logits are two kernels old, so it routes (and fetches its
   // first weights) before waiting for the gate/up kernel's h rows.
@@ -639,9 +662,8 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
       a.w_out[i] = rs->w[(i / a.T) * kMaxTopK + i % a.T];
     }
   }
-  const int n_experts = rs->U + a.has_shared;
   const int ntiles = GATEUP ? a.I / 64 : (a.H + kBM - 1) / kBM;
-  const int n_items = n_experts * ntiles;
+  const int n_items = rs->V * ntiles;
   const int K = GATEUP ? a.H : a.I;
   const int KG = K / 64, KC = (KG + kGroupsPerUnit - 1) / kGroupsPerUnit;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -652,14 +674,15 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
     long long fills = 0;
     bool waited = GATEUP;
     for (int item = blockIdx.x; item < n_items && !*abort; item += a.G) {
-      const int u = item / ntiles, tile = item % ntiles;
+      const int unit = rs->vlist[item / ntiles], tile = item % ntiles;
+      const int u = unit & 0xFFF, rc = unit >> 12;
       const bool shared = u >= rs->U;
       const int e = shared ? 0 : rs->ulist[u];
-      const int nb = pairs_of(rs, a, u);
+      const int nb = min(8, pairs_of(rs, a, u) - 8 * rc);
       __syncwarp();
       if (lane < L::NB) {
         int r = 0, j = 0;
-        if (lane < nb) pair_of(rs, a, u, lane, r, j);
+        if (lane < nb) pair_of(rs, a, u, 8 * rc + lane, r, j);
         brow[lane] = GATEUP ? a.x + (long long)r * a.H : a.hbuf + ((long long)r * TS + j) * a.I;
       }
       __syncwarp();
@@ -670,30 +693,30 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
       int kc = 0;
       if (!waited) {  // first item of the down kernel: its weights before the wait
         waited = true;
-        const int n_pre = min(kStages, KC);
+        const int n_pre = min(ST, KC);
         if (lane == 0)
           for (int f = 0; f < n_pre; ++f)
             produce_w(smem + f * L::STAGE, bar_base + 8 * f, ts, f, min(kGroupsPerUnit, KG - 4 * f));
         griddep_wait();
         griddep_launch();
         for (int f = 0; f < n_pre; ++f)
-          produce_x<NT>(smem + f * L::STAGE, bar_base + 8 * f, f, min(kGroupsPerUnit, KG - 4 * f), brow, nb, lane);
+          produce_x<1>(smem + f * L::STAGE, bar_base + 8 * f, f, min(kGroupsPerUnit, KG - 4 * f), brow, nb, lane);
         kc = n_pre;
         fills = n_pre;
       }
       for (; kc < KC; ++kc, ++fills) {
-        const int s = (int)(fills % kStages);
-        const uint32_t ph = (uint32_t)((fills / kStages) & 1);
-        if (!mbar_wait(bar_base + 8 * (kStages + s), ph ^ 1, abort, a.err)) break;
+        const int s = (int)(fills % ST);
+        const uint32_t ph = (uint32_t)((fills / ST) & 1);
+        if (!mbar_wait(bar_base + 8 * (ST + s), ph ^ 1, abort, a.err)) break;
         const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
-        produce_stage<NT>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, gcount, brow, nb, lane);
+        produce_stage<1>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, gcount, brow, nb, lane);
       }
     }
     if (!waited) {
       griddep_wait();
       griddep_launch();
     }
-    if (*abort) producer_drain(bar_base, fills);
+    if (*abort) producer_drain<ST>(bar_base, fills);
     return;
   }
 
@@ -710,15 +733,10 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
   }
   long long fills = 0;
   for (int item = blockIdx.x; item < n_items; item += a.G) {
-    const int u = item / ntiles, tile = item % ntiles;
-    const int nb = pairs_of(rs, a, u);
-    // Most routed experts get few rows: one MMA column block then suffices.
-    if (NT == 2 && nb <= 8)
-      moe_item<1, NT, CW, GATEUP>(a, rs, smem, bar_base, abort, u, tile, nb, KC, KG, TS, n_experts, rbase,
-                                  lane, fills);
-    else
-      moe_item<NT, NT, CW, GATEUP>(a, rs, smem, bar_base, abort, u, tile, nb, KC, KG, TS, n_experts, rbase,
-                                   lane, fills);
+    const int unit = rs->vlist[item / ntiles], tile = item % ntiles;
+    const int u = unit & 0xFFF, rc = unit >> 12;
+    const int nb = min(8, pairs_of(rs, a, u) - 8 * rc);
+    moe_item<CW, GATEUP, ST>(a, rs, smem, bar_base, abort, u, rc, tile, nb, KC, KG, TS, rbase, lane, fills);
   }
 }
 
@@ -727,7 +745,7 @@ __global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THR
 template <int NT>
 static size_t dense_smem() { return Q4Layout<NT>::BASE_BYTES + 1024; }
 template <int NT>
-static size_t moe_smem() { return Q4Layout<NT>::BASE_BYTES + sizeof(RouteSmem) + 1024; }
+static size_t moe_smem() { return Q4Layout<NT, kMoeStages>::BASE_BYTES + sizeof(RouteSmem) + 1024; }
 
 template <typename F>
 static cudaError_t setup_one(F* kernel, int threads, size_t smem, int* ctas_per_sm) {
@@ -750,13 +768,11 @@ cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm) {
   cudaError_t e;
   constexpr int TD = Warps<kDenseWarps>::THREADS, TG = Warps<kGateUpWarps>::THREADS, TDN = Warps<kDownWarps>::THREADS;
   *dense_ctas_per_sm = kQ4CtasPerSm;
-  *moe_ctas_per_sm = kQ4CtasPerSm;
   if ((e = setup_one(q4_dense_kernel<1>, TD, dense_smem<1>(), dense_ctas_per_sm))) return e;
   if ((e = setup_one(q4_dense_kernel<2>, TD, dense_smem<2>(), dense_ctas_per_sm))) return e;
-  if ((e = setup_one(moe_kernel<1, true>, TG, moe_smem<1>(), moe_ctas_per_sm))) return e;
-  if ((e = setup_one(moe_kernel<2, true>, TG, moe_smem<2>(), moe_ctas_per_sm))) return e;
-  if ((e = setup_one(moe_kernel<1, false>, TDN, moe_smem<1>(), moe_ctas_per_sm))) return e;
-  if ((e = setup_one(moe_kernel<2, false>, TDN, moe_smem<2>(), moe_ctas_per_sm))) return e;
+  *moe_ctas_per_sm = kMoeCtasPerSm;
+  if ((e = setup_one(moe_kernel<true>, TG, moe_smem<1>(), moe_ctas_per_sm))) return e;
+  if ((e = setup_one(moe_kernel<false>, TDN, moe_smem<1>(), moe_ctas_per_sm))) return e;
   if (*dense_ctas_per_sm < 1 || *moe_ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
@@ -780,30 +796,30 @@ cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s
   return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2>, a);
 }
 
-template <int NT, bool GATEUP>
+template <bool GATEUP>
 static cudaError_t launch_moe_one(const MoeArgs& a, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.G);
   cfg.blockDim = dim3(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS);
-  cfg.dynamicSmemBytes = moe_smem<NT>();
+  cfg.dynamicSmemBytes = moe_smem<1>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, moe_kernel<NT, GATEUP>, a);
+  return cudaLaunchKernelEx(&cfg, moe_kernel<GATEUP>, a);
 }
 
 // The down and combine kernels always follow the gate/up kernel of the same
 // call, which started after everything the caller enqueued before it (or,
 // with pdl, after the kernel before it): they may overlap their predecessor's
 // tail.
-cudaError_t launch_moe(const MoeArgs& a, int nt, bool pdl, cudaStream_t s, int* launches) {
-  cudaError_t e = nt == 1 ? launch_moe_one<1, true>(a, pdl, s) : launch_moe_one<2, true>(a, pdl, s);
+cudaError_t launch_moe(const MoeArgs& a, bool pdl, cudaStream_t s, int* launches) {
+  cudaError_t e = launch_moe_one<true>(a, pdl, s);
   if (e) return e;
   ++*launches;
-  e = nt == 1 ? launch_moe_one<1, false>(a, true, s) : launch_moe_one<2, false>(a, true, s);
+  e = launch_moe_one<false>(a, true, s);
   if (e) return e;
   ++*launches;
   cudaLaunchConfig_t cfg = {};

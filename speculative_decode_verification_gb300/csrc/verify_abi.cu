@@ -304,7 +304,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   a.has_shared = n_shared ? 1 : 0;
   a.G = ctx->moe_ctas_per_sm * ctx->num_sms;
   int launched = 0;
-  cudaError_t e = vk::launch_moe(a, k <= 8 ? 1 : 2, ctx->pdl, stream, &launched);
+  cudaError_t e = vk::launch_moe(a, ctx->pdl, stream, &launched);
   ctx->launches += launched;
   if (e) return cuda_fail(ctx, e, "q4_gather_experts_k launch");
   return VERIFY_OK;
