@@ -453,25 +453,55 @@ __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
       const int e = lane + 32 * i;
       v[i] = e < a.E ? __ldcg(l + e) : 0.f;  // L2: may precede the grid dependency wait
     }
-    uint32_t taken = 0;
+    // Order-preserving keys (0 = no expert; -0 counts as +0), then this lane's
+    // four best in descending order (equal keys: lower index first).  A round
+    // takes the warp maximum key and, among the lanes holding it, the lowest
+    // expert index; only the winning lane advances its list.
+    uint32_t key[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const uint32_t b = __float_as_uint(v[i] == 0.f ? 0.f : v[i]);
+      key[i] = (lane + 32 * i < a.E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+    }
+    uint32_t taken = 0, tk[4];
+    int ti[4];
+    auto refill = [&]() {
+      tk[0] = tk[1] = tk[2] = tk[3] = 0u;
+      ti[0] = ti[1] = ti[2] = ti[3] = 0;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const uint32_t kv = ((taken >> i) & 1u) ? 0u : key[i];
+        if (kv > tk[3]) {
+          if (kv > tk[2]) {
+            tk[3] = tk[2]; ti[3] = ti[2];
+            if (kv > tk[1]) {
+              tk[2] = tk[1]; ti[2] = ti[1];
+              if (kv > tk[0]) { tk[1] = tk[0]; ti[1] = ti[0]; tk[0] = kv; ti[0] = i; }
+              else { tk[1] = kv; ti[1] = i; }
+            } else { tk[2] = kv; ti[2] = i; }
+          } else { tk[3] = kv; ti[3] = i; }
+        }
+      }
+    };
+    refill();
     float myv = 0.f;
     int mye = -1;
     for (int j = 0; j < a.T; ++j) {
-      float bv = 0.f;
-      int be = -1;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = lane + 32 * i;
-        if (e < a.E && !((taken >> i) & 1u) && (be < 0 || v[i] > bv)) { bv = v[i]; be = e; }
+      const uint32_t m = __reduce_max_sync(0xffffffffu, tk[0]);
+      const uint32_t we =
+          __reduce_min_sync(0xffffffffu, tk[0] == m ? (uint32_t)(lane + 32 * ti[0]) : 0xffffffffu);
+      if (lane == (int)(we & 31u)) {
+        taken |= 1u << ti[0];
+        tk[0] = tk[1]; ti[0] = ti[1];
+        tk[1] = tk[2]; ti[1] = ti[2];
+        tk[2] = tk[3]; ti[2] = ti[3];
+        tk[3] = 0u;
+        if (tk[0] == 0u) refill();  // four taken from this lane: look at the rest
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be))) { bv = ov; be = oe; }
+      if (lane == j) {
+        myv = __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
+        mye = (int)we;
       }
-      if (lane == (be & 31)) taken |= 1u << (be >> 5);
-      if (lane == j) { myv = bv; mye = be; }
     }
     const float top = __shfl_sync(0xffffffffu, myv, 0);
     const float ex = lane < a.T ? expf(myv - top) : 0.f;

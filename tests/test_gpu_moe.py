@@ -67,6 +67,27 @@ def test_small_moe_matches_oracle(vf, k):
     assert_close(gy, oy, what=f"k={k}")
 
 
+def test_routing_ties_and_crowded_lanes(vf):
+    """Top-16 of 512 with many equal logits (ties -> lower expert index) and a
+    row whose largest logits all sit at experts 3, 35, 67, ... (one lane of
+    the warp holds every winner): indices equal the oracle's bit for bit."""
+    E, H, I, T, k = 512, 256, 128, 16, 6
+    gu, dn = moe_case(14, E, H, I)
+    x = S.bf16_normal(14, "moe.t.x", (k, H))
+    lg = np.round(S.f32_normal(14, "moe.t.l", (k, E)) * 2.0) / 2.0  # coarse grid: many ties
+    lg[1, :] = 0.0
+    lg[2, 3::32] = 5.0 + np.arange(16, dtype=np.float32) / 64.0  # 16 winners in one lane
+    lg[3, 3::32] = 7.0  # 16 equal winners in one lane
+    lg[4, :] = -0.0
+    lg = lg.astype(np.float32)
+    oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
+                                     lg, T, x)
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(lg), T, dev(x), k, H)
+    assert np.array_equal(gi, oi)
+    np.testing.assert_allclose(gw, ow, rtol=1e-5, atol=1e-6)
+    assert_close(gy, oy, what="ties")
+
+
 @pytest.mark.parametrize("k", [3, 9])
 def test_moe_with_k_not_a_multiple_of_128(vf, k):
     """H = 320 and I = 192: partial 256-column chunks on both products and a
