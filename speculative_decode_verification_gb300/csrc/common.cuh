@@ -175,6 +175,18 @@ __device__ __forceinline__ float ld_dsmem_f32(const void* local_ptr, uint32_t ra
   return v;
 }
 
+// 16-byte load from the same offset in the shared memory of cluster rank `rank`.
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const void* local_ptr, uint32_t rank) {
+  uint32_t a = smem_addr(local_ptr), ra;
+  float4 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
+
 // Named barrier among `threads` threads (id 0 is __syncthreads').
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

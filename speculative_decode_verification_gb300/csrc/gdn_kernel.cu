@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   __shared__ float ys[kGdnMaxK][kGdnRows];
   __shared__ float gs[kGdnMaxK], bs[kGdnMaxK], kq[kGdnMaxK];
   __shared__ float ss_part[kGdnMaxK];
+  __shared__ float ss_all[kGdnMaxK][D / kGdnRows];
+  __shared__ float inv_s[kGdnMaxK];
 
   const int p = (int)cluster_rank();
   const int h = blockIdx.x / P;
@@ -208,21 +210,42 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   __syncthreads();
 
   // ---- 4. gated RMSNorm over the head's D value rows (cluster-wide sum)
+  // The output gates do not depend on the sum: load them first.
+  float act[2], nw[2];
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int e = tid + h2 * kGdnThreads;
+    act[h2] = 0.f;
+    nw[h2] = 0.f;
+    if (e < k * kGdnRows) {
+      const int r = e / kGdnRows, iv = p * kGdnRows + e % kGdnRows;
+      const float zz = bf16f(a.z[r * a.ld_z + h * D + iv]);
+      act[h2] = a.gate_act == 1 ? siluf_(zz) : sigmoidf_(zz);
+      nw[h2] = a.norm_w[iv];
+    }
+  }
   if (tid < k) {
     float ss = 0.f;
     for (int t = 0; t < kGdnRows; ++t) ss = fmaf(ys[tid][t], ys[tid][t], ss);
     ss_part[tid] = ss;
   }
   cluster_sync();
-  for (int e = tid; e < k * kGdnRows; e += kGdnThreads) {
-    const int r = e / kGdnRows, ii = e % kGdnRows;
+  // one remote load per (row, rank), all in flight together; then the sum in rank order
+  if (tid < k * P) ss_all[tid / P][tid % P] = ld_dsmem_f32(&ss_part[tid / P], (uint32_t)(tid % P));
+  __syncthreads();
+  if (tid < k) {
     float tot = 0.f;
-    for (int q = 0; q < P; ++q) tot += ld_dsmem_f32(&ss_part[r], (uint32_t)q);
-    const float inv = 1.f / sqrtf(tot / (float)D + a.norm_eps);
+    for (int q = 0; q < P; ++q) tot += ss_all[tid][q];
+    inv_s[tid] = 1.f / sqrtf(tot / (float)D + a.norm_eps);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int e = tid + h2 * kGdnThreads;
+    if (e >= k * kGdnRows) break;
+    const int r = e / kGdnRows, ii = e % kGdnRows;
     const int iv = p * kGdnRows + ii;
-    const float zz = bf16f(a.z[r * a.ld_z + h * D + iv]);
-    const float act = a.gate_act == 1 ? siluf_(zz) : sigmoidf_(zz);
-    const float ov = ys[r][ii] * inv * a.norm_w[iv] * act;
+    const float ov = ys[r][ii] * inv_s[r] * nw[h2] * act[h2];
     const long long oi = (long long)r * a.Hv * D + h * D + iv;
     if (a.dtype == 1) reinterpret_cast<uint16_t*>(a.o)[oi] = f2bf16(ov);
     else reinterpret_cast<float*>(a.o)[oi] = ov;

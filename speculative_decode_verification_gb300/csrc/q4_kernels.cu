@@ -404,17 +404,32 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     cluster_sync();
     mine = (warp % S) == split;
     if (mine) {
+      // Sum the S partial tiles in rank order.  The next rank's four-float
+      // loads are issued before this rank's adds, so the remote-load latency
+      // is paid about once rather than once per value.
       zero_acc<MT, NT>(acc);
+      float4 cur[MT][NT], nxt[MT][NT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) cur[m][t] = ld_dsmem_f32x4(part + ((warp * MT + m) * NT + t) * 32 + lane, 0u);
       for (int q = 0; q < S; ++q) {
+        if (q + 1 < S) {
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+              nxt[m][t] = ld_dsmem_f32x4(part + ((warp * MT + m) * NT + t) * 32 + lane, (uint32_t)(q + 1));
+        }
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            const float4* src = part + ((warp * MT + m) * NT + t) * 32 + lane;
-            acc[m][t][0] += ld_dsmem_f32(&src->x, (uint32_t)q);
-            acc[m][t][1] += ld_dsmem_f32(&src->y, (uint32_t)q);
-            acc[m][t][2] += ld_dsmem_f32(&src->z, (uint32_t)q);
-            acc[m][t][3] += ld_dsmem_f32(&src->w, (uint32_t)q);
+            acc[m][t][0] += cur[m][t].x;
+            acc[m][t][1] += cur[m][t].y;
+            acc[m][t][2] += cur[m][t].z;
+            acc[m][t][3] += cur[m][t].w;
+            cur[m][t] = nxt[m][t];
           }
       }
     }
