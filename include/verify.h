@@ -231,7 +231,8 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W,
  * Limits: E <= 512, 1 <= T <= 16, 64 <= H <= 8192, 64 <= I <= 4096,
  * H % 64 == I % 64 == 0.
  * Expert weights are read once per call for every distinct selected expert
- * (the union of the rows' routes).  Three kernel launches on `stream`.
+ * (the union of the rows' routes).  Two kernel launches on `stream`: the routed
+ * experts (gate/up and down items in one kernel), then the combine.
  */
 verify_status q4_gather_experts_k(verify_ctx* ctx,
                                   const verify_q4_experts* gate_up,
@@ -363,7 +364,7 @@ verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w,
  *   h  += q4_gather_experts_k(gate_up, down, l[:, :E], top_k, xn2,
  *                             shared_gate_up, shared_down, l[:, E])
  * idx_out (optional, device int32 [k, top_k]) receives the routed expert
- * indices.  Nine kernel launches on `stream`, no host synchronisation.  Scratch
+ * indices.  Eight kernel launches on `stream`, no host synchronisation.  Scratch
  * activations live in the context (limits: k <= 16, H <= 8192, in_proj rows
  * <= 32768, E + 1 <= 1024).  Weight shapes must match: in_proj [C + Hv*dv +
  * 2*Hv, H], out_proj [H, Hv*dv], router [E + 1, H], gate_up [E, 2I, H],

@@ -192,6 +192,26 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Bounded wait until *p >= target (an acquire load, so what the writers
+// published before counting is visible after).  false on abort or timeout.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort, int* err) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  if (v >= target) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (*abort) return false;
+    __nanosleep(64);
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (clock64() - t0 > kWaitTimeoutCycles) {
+      *abort = 1;
+      record_error(err, VERIFY_DEV_ETIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------ programmatic dependent launch
 //
 // A kernel launched with programmatic stream serialization may start while

@@ -17,6 +17,7 @@ constexpr int kDownWarps = 4;      // routed down projection: two 16-row MMA til
 constexpr int kQ4CtasPerSm = 2;    // dense kernels
 constexpr int kMoeCtasPerSm = 3;   // routed-expert kernels: 8 activation rows per stage, three stages
 constexpr int kMoeStages = 3;
+constexpr int kMoeUnits = 2 * 512 + 2;  // work units of one call: (expert, chunk of 8 rows), at most
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 
@@ -51,6 +52,8 @@ struct MoeArgs {
   long long gu_rt_bytes, dn_rt_bytes;
   uint16_t* hbuf;             // scratch [k, TS, I] bf16 (TS = T + has_shared)
   float* part;                // scratch [k, TS, H] fp32
+  int* work;                  // scratch: next work item (0 before a call; the combine kernel resets it)
+  int* done;                  // scratch [kMoeUnits]: gate/up tiles written per unit (reset likewise)
   int32_t* idx_out;
   float* w_out;
   void* y;

@@ -9,7 +9,8 @@
 namespace {
 
 // Scratch of the routed-expert kernels: SwiGLU rows [k, T+1, I] bf16, per-rank
-// partial outputs [k, T+1, H] fp32 and an error word.  Every GPU that loads the library holds it until the process
+// partial outputs [k, T+1, H] fp32, an error word and the work-scheduling
+// counters.  Every GPU that loads the library holds it until the process
 // exits.  All calls on one device share it.
 constexpr size_t kScratchBytes = VERIFY_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
@@ -112,8 +113,8 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   const int TS = top_k + (n_shared ? 1 : 0);
   const size_t hbuf_bytes = round256((size_t)k * TS * I * sizeof(uint16_t));
   const size_t part_bytes = round256((size_t)k * TS * H * sizeof(float));
-  const size_t err_bytes = 256;
-  if (hbuf_bytes + part_bytes + err_bytes > kScratchBytes) return VERIFY_EUNSUPPORTED;
+  const size_t word_bytes = round256((size_t)(2 + vk::kMoeUnits) * sizeof(int));  // error word, work counter, unit counts
+  if (hbuf_bytes + part_bytes + word_bytes > kScratchBytes) return VERIFY_EUNSUPPORTED;
   unsigned char* base = d->scratch;
   int* err_word = reinterpret_cast<int*>(base + hbuf_bytes + part_bytes);
 
@@ -130,14 +131,17 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   a.dn_rt_bytes = rt_bytes(I);
   a.hbuf = reinterpret_cast<uint16_t*>(base);
   a.part = reinterpret_cast<float*>(base + hbuf_bytes);
+  a.work = err_word + 1;
+  a.done = err_word + 2;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y;
   a.err = device_error ? device_error : err_word;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
   a.G = d->moe_ctas_per_sm * d->num_sms;
-  // The error word must start at zero: a previous call may have stopped on a
-  // device error and left it set.
-  if (!device_error && cudaMemsetAsync(err_word, 0, sizeof(int), stream) != cudaSuccess) return VERIFY_ECUDA;
+  // The error word and the scheduling counters must start at zero: a previous
+  // call may have stopped on a device error and left them set.
+  if (cudaMemsetAsync(err_word, 0, (size_t)(2 + vk::kMoeUnits) * sizeof(int), stream) != cudaSuccess)
+    return VERIFY_ECUDA;
   int launched = 0;
   if (vk::launch_moe(a, false, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;
   return VERIFY_OK;

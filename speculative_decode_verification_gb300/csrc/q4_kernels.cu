@@ -9,31 +9,34 @@
 // order; all (expert,row) pairs in one dispatch, one tail).
 //
 // Design (GB300, sm_103a):
-//  * A CTA is one producer warp plus four consumer warps, each owning two
-//    16-row MMA tiles of the 128-row tile; two CTAs per SM.  The
-//    producer streams 128-row x 256-column weight tiles with TMA (128-byte
-//    swizzle) into a 4-stage shared-memory ring, together with the tile's bf16
-//    scales and biases and the activation rows (cp.async, zero fill beyond the
-//    last row), all completing on one mbarrier per stage.  Each weight byte
-//    crosses HBM once per call.
-//  * Consumers decode each packed word once into bf16 code pairs (128 + q,
-//    exact) with one shift and one lop3 per pair and feed them to
-//    mma.sync m16n8k16 as the A operand; the k activation rows are the N
-//    columns (8 per MMA; a second MMA column block for k > 8).  Per 64-column
-//    group the fp32 result C = sum (128 + q) x is folded as
+//  * Weights are read in the tiled layout of tile.cu: per (128-row tile,
+//    256-column chunk) one contiguous block of scales, biases and codes in MMA
+//    fragment order.  A CTA is one producer warp plus four consumer warps.  The
+//    producer fills a ring of stages in shared memory: one bulk copy per weight
+//    block and cp.async of the activation rows, both completing on the stage's
+//    mbarrier.  Each weight byte crosses HBM once per call.
+//  * Consumers read each fragment with one 16-byte shared load, decode the
+//    nibbles to bf16 code values 128 + q (exact) with one lop3 per pair and
+//    feed them to mma.sync m16n8k16 as the A operand; the k activation rows
+//    are the N columns (8 per MMA; a second column block for k > 8).  Per
+//    64-column group the fp32 result C = sum (128 + q) x is folded as
 //        acc += s*C + (b - 128 s) * sum(x),
-//    the group sums sum(x) being added up once per stage by four consumer
-//    warps.  Products of the integer codes with bf16 x are exact; the
-//    accumulation is fp32.
+//    the group sums sum(x) added up once per stage.  Products of the integer
+//    codes with bf16 x are exact; the accumulation is fp32.
 //  * Every output column is an independent dot product, the group order is
 //    fixed and the split of K across CTAs depends only on (N, K, SM count):
 //    row r of a width-k call is bit-identical to a width-1 call.
-//  * Dense: RB row tiles x S K-splits; the S CTAs of a tile form a thread
-//    block cluster and add their partial tiles through distributed shared
-//    memory in rank order (no global scratch, no atomics).
-//  * Routed MoE: items = (distinct expert, row tile) with the full K per item.
-//    The down kernel writes one partial output per (row, rank); a small third
-//    kernel combines every row's experts in rank order.
+//  * Dense: two CTAs per SM, four stages; RB row tiles x S K-splits, the S
+//    CTAs of a tile form a thread block cluster and add their partial tiles
+//    through distributed shared memory in rank order (no global scratch, no
+//    atomics).
+//  * Routed MoE: three CTAs per SM, three stages of 8 activation rows.  One
+//    kernel routes every row in every CTA, then works through items: first
+//    the gate/up items (expert, row chunk, 64 gate + 64 up rows; SwiGLU into
+//    the h rows), then the down items (expert, row chunk, 128 output rows;
+//    one partial output per (row, rank)).  A down item starts once every
+//    gate/up item of its unit is counted done.  A second small kernel combines
+//    every row's experts in rank order.
 #include "common.cuh"
 #include "internal.h"
 
@@ -649,6 +652,10 @@ __device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, 
 __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
   griddep_wait();
   griddep_launch();
+  if (blockIdx.x == 0) {  // the routed-expert kernel is done: reset its work counter and unit counts
+    for (int i = threadIdx.x; i < kMoeUnits; i += blockDim.x) a.done[i] = 0;
+    if (threadIdx.x == 0) *a.work = 0;
+  }
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)a.k * a.H) return;
   const int r = (int)(i / a.H), n = (int)(i % a.H);
@@ -670,118 +677,146 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
   store_out(a.y, a.dtype, (long long)r * a.H + n, y);
 }
 
-// GATEUP: items (expert, 64 rows of I): gate rows and up rows of the same i
-// go to the same warp (its two MMA tiles), the epilogue applies SwiGLU and
-// writes h (bf16).  Down: items (expert, 128 rows of H); partial outputs per
-// (row, rank) go to scratch, combined by moe_combine_kernel.
-// Items are expert-major: consecutive CTAs stream consecutive slices of one
-// expert (measured much faster than block-major order, which spreads the
-// concurrent reads over all selected experts).
-template <bool GATEUP>
-__global__ void __launch_bounds__(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS, kMoeCtasPerSm)
-    moe_kernel(const MoeArgs a) {
+// The routed-expert products as one persistent kernel (a third kernel, the
+// combine, follows).  Work items, handed out in order by an atomic counter:
+//   [0, n_gu)         gate/up items (unit v, 64 outputs of I): gate rows and
+//                     up rows of the same outputs go to the same warp, the
+//                     epilogue applies SwiGLU and writes h (bf16) for the
+//                     unit's rows, then counts the item in done[v];
+//   [n_gu, n_gu+n_dn) down items (unit v, 128 rows of H): one fp32 partial
+//                     per (row, rank); its h rows are read only once
+//                     done[v] == I / 64, all gate/up tiles of the unit.
+// A unit is (distinct expert or the shared expert, chunk of up to 8 of its
+// rows).  Items are unit-major: concurrent CTAs stream consecutive slices of
+// one expert.  A down item is handed out only after every gate/up item, and
+// a handed-out item belongs to a running CTA, so every wait ends (bounded).
+__device__ __forceinline__ void moe_decode(const MoeArgs& a, const RouteSmem* rs, int item, int n_gu, int ntg,
+                                           int ntd, bool& gu, int& v, int& u, int& rc, int& tile, int& nb) {
+  gu = item < n_gu;
+  const int rel = gu ? item : item - n_gu;
+  const int nt = gu ? ntg : ntd;
+  v = rel / nt;
+  tile = rel % nt;
+  const int unit = rs->vlist[v];
+  u = unit & 0xFFF;
+  rc = unit >> 12;
+  nb = min(8, pairs_of(rs, a, u) - 8 * rc);
+}
+
+__global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) moe_kernel(const MoeArgs a) {
+  static_assert(kGateUpWarps == kDownWarps, "both item kinds share one CTA shape");
   constexpr int ST = kMoeStages;
   using L = Q4Layout<1, ST>;
-  constexpr int CW = GATEUP ? kGateUpWarps : kDownWarps, MT = Warps<CW>::MT;
-  static_assert(!GATEUP || MT == 2, "gate/up pairs the gate and up row tiles in one warp");
+  constexpr int CW = kGateUpWarps, MT = Warps<CW>::MT;
+  static_assert(MT == 2, "gate/up pairs the gate and up row tiles in one warp");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t bar_base = smem_addr(smem + L::BAR_OFF);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
+  volatile int* slot_item = abort + 4;  // item id of the item starting in stage s (-1: no more work)
   RouteSmem* rs = reinterpret_cast<RouteSmem*>(smem + L::BASE_BYTES);
   if (threadIdx.x == 0) *abort = 0;
   init_barriers<CW, ST>(bar_base);
-  // Gate/up routes from logits the previous kernel wrote: wait first.  The
-  // down kernel's logits are two kernels old, so it routes (and fetches its
-  // first weights) before waiting for the gate/up kernel's h rows.
-  if (GATEUP) {
-    griddep_wait();
-    griddep_launch();
-  }
+  griddep_wait();  // the routing logits come from the kernel before
+  griddep_launch();
   route_rows(a, rs);  // ends with __syncthreads
 
   const int TS = a.T + a.has_shared;
-  if (GATEUP && blockIdx.x == 0) {
+  if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < a.k * a.T; i += blockDim.x) {
       a.idx_out[i] = rs->idx[(i / a.T) * kMaxTopK + i % a.T];
       a.w_out[i] = rs->w[(i / a.T) * kMaxTopK + i % a.T];
     }
   }
-  const int ntiles = GATEUP ? a.I / 64 : (a.H + kBM - 1) / kBM;
-  const int n_items = rs->V * ntiles;
-  const int K = GATEUP ? a.H : a.I;
-  const int KG = K / 64, KC = (KG + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  const int ntg = a.I / 64, ntd = (a.H + kBM - 1) / kBM;
+  const int n_gu = rs->V * ntg, n_all = n_gu + rs->V * ntd;
+  const int KGg = a.H / 64, KCg = (KGg + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  const int KGd = a.I / 64, KCd = (KGd + kGroupsPerUnit - 1) / kGroupsPerUnit;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
     const uint16_t** brow = reinterpret_cast<const uint16_t**>(smem + L::MISC_OFF + 64);
     long long fills = 0;
-    bool waited = GATEUP;
-    for (int item = blockIdx.x; item < n_items && !*abort; item += a.G) {
-      const int unit = rs->vlist[item / ntiles], tile = item % ntiles;
-      const int u = unit & 0xFFF, rc = unit >> 12;
+    // The first item of every CTA is its block id: consecutive blocks sit on
+    // distinct SMs, so when there are few items the heavy gate/up items do
+    // not share an SM.  Later items come from the counter, in order.
+    int next = blockIdx.x;
+    for (;;) {
+      const int item = next;
+      const int s0 = (int)(fills % ST);
+      if (!mbar_wait(bar_base + 8 * (ST + s0), (uint32_t)(((fills / ST) & 1) ^ 1), abort, a.err)) break;
+      if (item >= n_all || *abort) {
+        // end mark: a stage without data whose item id tells the consumers to stop
+        if (lane == 0) {
+          slot_item[s0] = -1;
+          mbar_arrive_expect_tx(bar_base + 8 * s0, 0);
+        }
+        cp_async_mbar_arrive_noinc(bar_base + 8 * s0);
+        ++fills;
+        break;
+      }
+      if (lane == 0) next = a.G + atomicAdd(a.work, 1);  // the item after this one, fetched early
+      bool gu;
+      int v, u, rc, tile, nb;
+      moe_decode(a, rs, item, n_gu, ntg, ntd, gu, v, u, rc, tile, nb);
       const bool shared = u >= rs->U;
       const int e = shared ? 0 : rs->ulist[u];
-      const int nb = min(8, pairs_of(rs, a, u) - 8 * rc);
       __syncwarp();
       if (lane < L::NB) {
         int r = 0, j = 0;
         if (lane < nb) pair_of(rs, a, u, 8 * rc + lane, r, j);
-        brow[lane] = GATEUP ? a.x + (long long)r * a.H : a.hbuf + ((long long)r * TS + j) * a.I;
+        brow[lane] = gu ? a.x + (long long)r * a.H : a.hbuf + ((long long)r * TS + j) * a.I;
       }
       __syncwarp();
       const uint8_t* ts =
-          GATEUP ? (shared ? a.sgu_tiles : a.gu_tiles + (long long)e * (a.I / 64) * a.gu_rt_bytes) + tile * a.gu_rt_bytes
-                 : (shared ? a.sdn_tiles : a.dn_tiles + (long long)e * ((a.H + kBM - 1) / kBM) * a.dn_rt_bytes) +
-                       tile * a.dn_rt_bytes;
+          gu ? (shared ? a.sgu_tiles : a.gu_tiles + (long long)e * ntg * a.gu_rt_bytes) + tile * a.gu_rt_bytes
+             : (shared ? a.sdn_tiles : a.dn_tiles + (long long)e * ntd * a.dn_rt_bytes) + tile * a.dn_rt_bytes;
+      const int KG = gu ? KGg : KGd, KC = gu ? KCg : KCd;
       int kc = 0;
-      if (!waited) {  // first item of the down kernel: its weights before the wait
-        waited = true;
-        const int n_pre = min(ST, KC);
-        if (lane == 0)
-          for (int f = 0; f < n_pre; ++f)
-            produce_w(smem + f * L::STAGE, bar_base + 8 * f, ts, f, min(kGroupsPerUnit, KG - 4 * f));
-        griddep_wait();
-        griddep_launch();
-        for (int f = 0; f < n_pre; ++f)
-          produce_x<1>(smem + f * L::STAGE, bar_base + 8 * f, f, min(kGroupsPerUnit, KG - 4 * f), brow, nb, lane);
-        kc = n_pre;
-        fills = n_pre;
+      if (!gu) {
+        int ok = 1;
+        if (lane == 0) ok = wait_count(a.done + v, ntg, abort, a.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
       for (; kc < KC; ++kc, ++fills) {
         const int s = (int)(fills % ST);
         const uint32_t ph = (uint32_t)((fills / ST) & 1);
-        if (!mbar_wait(bar_base + 8 * (ST + s), ph ^ 1, abort, a.err)) break;
-        const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
-        produce_stage<1>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, gcount, brow, nb, lane);
+        if (kc > 0 && !mbar_wait(bar_base + 8 * (ST + s), ph ^ 1, abort, a.err)) break;
+        if (kc == 0 && lane == 0) slot_item[s] = item;
+        produce_stage<1>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, min(kGroupsPerUnit, KG - 4 * kc), brow, nb,
+                         lane);
       }
-    }
-    if (!waited) {
-      griddep_wait();
-      griddep_launch();
+      next = __shfl_sync(0xffffffffu, next, 0);
+      if (*abort) break;
     }
     if (*abort) producer_drain<ST>(bar_base, fills);
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  if (!GATEUP) {
-    griddep_wait();
-    griddep_launch();
-  }
-  int rbase[MT];
-  if (GATEUP) { rbase[0] = 16 * warp; rbase[MT - 1] = 64 + 16 * warp; }
-  else {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) rbase[m] = 16 * (warp * MT + m);
-  }
   long long fills = 0;
-  for (int item = blockIdx.x; item < n_items; item += a.G) {
-    const int unit = rs->vlist[item / ntiles], tile = item % ntiles;
-    const int u = unit & 0xFFF, rc = unit >> 12;
-    const int nb = min(8, pairs_of(rs, a, u) - 8 * rc);
-    moe_item<CW, GATEUP, ST>(a, rs, smem, bar_base, abort, u, rc, tile, nb, KC, KG, TS, rbase, lane, fills);
+  for (;;) {
+    const int s = (int)(fills % ST);
+    if (!mbar_wait(bar_base + 8 * s, (uint32_t)((fills / ST) & 1), abort, a.err)) break;
+    const int item = slot_item[s];
+    if (item < 0) break;
+    bool gu;
+    int v, u, rc, tile, nb;
+    moe_decode(a, rs, item, n_gu, ntg, ntd, gu, v, u, rc, tile, nb);
+    if (gu) {
+      const int rbase[MT] = {16 * warp, 64 + 16 * warp};
+      moe_item<CW, true, ST>(a, rs, smem, bar_base, abort, u, rc, tile, nb, KCg, KGg, TS, rbase, lane, fills);
+      // publish this tile of the unit's h rows
+      named_bar(3, CW * 32);
+      if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(a.done + v, 1);
+      }
+    } else {
+      const int rbase[MT] = {16 * (warp * MT), 16 * (warp * MT + 1)};
+      moe_item<CW, false, ST>(a, rs, smem, bar_base, abort, u, rc, tile, nb, KCd, KGd, TS, rbase, lane, fills);
+    }
   }
 }
 
@@ -811,13 +846,12 @@ static cudaError_t setup_one(F* kernel, int threads, size_t smem, int* ctas_per_
 // does not depend on k).
 cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm) {
   cudaError_t e;
-  constexpr int TD = Warps<kDenseWarps>::THREADS, TG = Warps<kGateUpWarps>::THREADS, TDN = Warps<kDownWarps>::THREADS;
+  constexpr int TD = Warps<kDenseWarps>::THREADS, TG = Warps<kGateUpWarps>::THREADS;
   *dense_ctas_per_sm = kQ4CtasPerSm;
   if ((e = setup_one(q4_dense_kernel<1>, TD, dense_smem<1>(), dense_ctas_per_sm))) return e;
   if ((e = setup_one(q4_dense_kernel<2>, TD, dense_smem<2>(), dense_ctas_per_sm))) return e;
   *moe_ctas_per_sm = kMoeCtasPerSm;
-  if ((e = setup_one(moe_kernel<true>, TG, moe_smem<1>(), moe_ctas_per_sm))) return e;
-  if ((e = setup_one(moe_kernel<false>, TDN, moe_smem<1>(), moe_ctas_per_sm))) return e;
+  if ((e = setup_one(moe_kernel, TG, moe_smem<1>(), moe_ctas_per_sm))) return e;
   if (*dense_ctas_per_sm < 1 || *moe_ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
@@ -841,32 +875,26 @@ cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s
   return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2>, a);
 }
 
-template <bool GATEUP>
-static cudaError_t launch_moe_one(const MoeArgs& a, bool pdl, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.G);
-  cfg.blockDim = dim3(Warps<GATEUP ? kGateUpWarps : kDownWarps>::THREADS);
-  cfg.dynamicSmemBytes = moe_smem<1>();
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, moe_kernel<GATEUP>, a);
-}
-
-// The down and combine kernels always follow the gate/up kernel of the same
-// call, which started after everything the caller enqueued before it (or,
-// with pdl, after the kernel before it): they may overlap their predecessor's
-// tail.
+// The combine kernel follows the routed-expert kernel of the same call, which
+// started after everything the caller enqueued before it (or, with pdl,
+// during the tail of the kernel before it).
 cudaError_t launch_moe(const MoeArgs& a, bool pdl, cudaStream_t s, int* launches) {
-  cudaError_t e = launch_moe_one<true>(a, pdl, s);
-  if (e) return e;
-  ++*launches;
-  e = launch_moe_one<false>(a, true, s);
-  if (e) return e;
-  ++*launches;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.G);
+    cfg.blockDim = dim3(Warps<kGateUpWarps>::THREADS);
+    cfg.dynamicSmemBytes = moe_smem<1>();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, moe_kernel, a);
+    if (e) return e;
+    ++*launches;
+  }
+  cudaError_t e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(((long long)a.k * a.H + 255) / 256));
   cfg.blockDim = dim3(256);

@@ -16,6 +16,7 @@ struct verify_ctx {
   uint16_t* moe_hbuf = nullptr;
   float* moe_part = nullptr;
   int* err = nullptr;
+  int* moe_sched = nullptr;  // routed-expert scheduling: work counter, then one count per unit
   uint16_t* st_xn = nullptr;   // layer scratch: bf16 [16, 8192]
   uint16_t* st_proj = nullptr; // bf16 [16, 32768]
   uint16_t* st_o = nullptr;    // bf16 [16, 32768]
@@ -140,6 +141,8 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = cudaMalloc(&ctx->moe_hbuf, kHbufElems * sizeof(uint16_t)))) return bail(e);
   if ((e = cudaMalloc(&ctx->moe_part, kMoePartElems * sizeof(float)))) return bail(e);
   if ((e = cudaMalloc(&ctx->err, sizeof(int)))) return bail(e);
+  if ((e = cudaMalloc(&ctx->moe_sched, (1 + vk::kMoeUnits) * sizeof(int)))) return bail(e);
+  if ((e = cudaMemset(ctx->moe_sched, 0, (1 + vk::kMoeUnits) * sizeof(int)))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_xn, sizeof(uint16_t) * VERIFY_MAX_K * kMaxH))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_proj, sizeof(uint16_t) * VERIFY_MAX_K * kMaxProj))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_o, sizeof(uint16_t) * VERIFY_MAX_K * kMaxProj))) return bail(e);
@@ -161,6 +164,7 @@ verify_status verify_destroy(verify_ctx* ctx) {
   cudaFree(ctx->moe_hbuf);
   cudaFree(ctx->moe_part);
   cudaFree(ctx->err);
+  cudaFree(ctx->moe_sched);
   cudaFree(ctx->st_xn);
   cudaFree(ctx->st_proj);
   cudaFree(ctx->st_o);
@@ -186,6 +190,7 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
   if (code) *code = h;
   if (h == 0) return VERIFY_OK;
   cudaMemset(ctx->err, 0, sizeof(int));
+  cudaMemset(ctx->moe_sched, 0, (1 + vk::kMoeUnits) * sizeof(int));  // an aborted call may leave counts behind
   cudaDeviceSynchronize();
   snprintf(ctx->msg, sizeof ctx->msg, "device error code %d", h);
   return VERIFY_EDEVICE;
@@ -299,6 +304,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   a.gu_rt_bytes = rt_bytes(H);
   a.dn_rt_bytes = rt_bytes(I);
   a.hbuf = ctx->moe_hbuf; a.part = ctx->moe_part;
+  a.work = ctx->moe_sched; a.done = ctx->moe_sched + 1;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;

@@ -61,7 +61,10 @@ def test_small_moe_matches_oracle(vf, k):
     logits = S.f32_normal(10, f"moe.l{k}", (k, E))
     oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
                                      logits, T, x)
-    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(logits), T, dev(x), k, H)
+    gud, dnd = DevQ4(vf, gu, True), DevQ4(vf, dn)
+    before = vf.launch_count()
+    gi, gw, gy = gather(vf, gud, dnd, dev(logits), T, dev(x), k, H)
+    assert vf.launch_count() - before == 2  # the routed experts kernel, then the combine
     assert np.array_equal(gi, oi)
     np.testing.assert_allclose(gw, ow, rtol=1e-5, atol=1e-6)
     assert_close(gy, oy, what=f"k={k}")

@@ -78,7 +78,9 @@ def check_layers(vf, cfg, seed, k, layers, h_name):
                                                   cfg["n_qk_heads"], cfg["n_v_heads"], cfg["d"], sh["T"])
         hd = torch.from_numpy(h.astype(np.float32)).cuda()
         idx = torch.zeros((k, sh["T"]), dtype=torch.int32, device="cuda")
+        before = vf.launch_count()
         vf.verify_layer_k(ds.layers[l], ds.states[l], hd, k, idx)
+        assert vf.launch_count() - before == 8  # norm, in_proj, GDN, out_proj, norm, router, experts, combine
         torch.cuda.synchronize()
         st = ds.states[l]
         S_last = host(ds.state_tensors[l][0][st.pending[k]])
