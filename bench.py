@@ -44,6 +44,33 @@ WORKLOAD = ("12-layer hybrid verify stack, hidden 2560: GDN 16 QK/48 V heads d12
 EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
 
 
+# DRAM traffic of the routed-expert kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum) of both layers of a 2-layer
+# stack at k = 9: 422.035456 MB over two launches whose algorithmic bytes sum to
+# 2 x 206226468.  Expert traffic grows with the distinct experts read, like the
+# algorithmic bytes, so a full launch's traffic is this ratio times its bytes.
+# The figure holds only for the kernel sources it was taken on; any change to
+# them reports null until the kernel is captured again.
+MOE_TRAFFIC_RATIO = 422.035456e6 / (2 * 206226468.0)
+MOE_TRAFFIC_SOURCES = {
+    "q4_kernels.cu": "daf7b9f96161c02ac87208ac82013c666a6e2c6f327eb70c3e4791eb694391e4",
+    "common.cuh": "ac5aa05db48a72a18577a5db7c1b26c1b88c76c3390aef39744a8dd5e3539166",
+    "internal.h": "7df581318f3629a9eae499d2617e4719382be12e36505847a741700d3f1e63a8",
+}
+
+
+def moe_traffic(bytes_per_launch):
+    """DRAM bytes per routed-expert launch, or None once the kernel changed."""
+    import hashlib
+
+    csrc = os.path.join(ROOT, "speculative_decode_verification_gb300", "csrc")
+    for name, digest in MOE_TRAFFIC_SOURCES.items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    return MOE_TRAFFIC_RATIO * bytes_per_launch
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -361,7 +388,8 @@ def run_ours(args, cfg):
                    "l2": "inputs larger than L2 (weights read per step far above 129 MB); no flush",
                    "per_k": {str(kk): v for kk, v in per_k.items()}},
         "roofline": {"bound": "hbm", "achieved": head["achieved"], "peak": hbm, "unit": "GB/s",
-                     "frac": head["achieved"] / hbm, "traffic": None,
+                     "frac": head["achieved"] / hbm, "traffic": moe_traffic(head["moe_bytes"]),
+                     "traffic_unit": "DRAM bytes per launch (ncu read + write of a 2-layer capture, scaled)",
                      "kernel": "q4_gather_experts_k (fused routed gate/up+SwiGLU and down kernel, then the combine kernel)",
                      "bytes_per_launch": head["moe_bytes"], "us_per_launch": head["moe_us"],
                      "distinct_experts": head["U"], "peak_kind": peak_kind},
