@@ -54,7 +54,7 @@ EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
 MOE_TRAFFIC_RATIO = 422.035456e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
     "q4_kernels.cu": "daf7b9f96161c02ac87208ac82013c666a6e2c6f327eb70c3e4791eb694391e4",
-    "common.cuh": "ac5aa05db48a72a18577a5db7c1b26c1b88c76c3390aef39744a8dd5e3539166",
+    "common.cuh": "905057bb3ceb5a22b2467509b74e8de32e62c9a15cee8a0db03be6eaf6c9724a",
     "internal.h": "7df581318f3629a9eae499d2617e4719382be12e36505847a741700d3f1e63a8",
 }
 

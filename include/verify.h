@@ -415,18 +415,19 @@ verify_status verify_set_layer_events(verify_ctx* ctx, void* const* events, int 
  * arguments (no ctx) plus `device_error`: an optional device int32 the caller
  * owns, set to 1 if a pipeline wait timed out (NULL: not reported).  The
  * caller passes all inputs and outputs; the kernels' scratch (SwiGLU rows,
- * per-rank partial outputs, an error word) lives in one array of
+ * per-rank partial outputs, an error word, the expert kernel's item counter
+ * and per-unit counts) lives in one array of
  * VERIFY_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
  * that loads the library holds until the process exits.
  *   - Limit: k*(T+s)*I*2 + k*(T+s)*H*4 bytes (s = 1 with a shared expert, each
- *     part rounded up to 256) plus 256 must fit the array; larger calls
+ *     part rounded up to 256) plus 4352 must fit the array; larger calls
  *     return VERIFY_EUNSUPPORTED before anything is enqueued.
  *   - The first call on each device sets that device up (resolves the array's
  *     device address, sets the kernels' launch attributes); make that first
  *     call before any stream capture.
  *   - Every call on a device shares the array, which keeps the last call's
- *     contents; the call clears what must start at zero (the error word, when
- *     device_error is NULL) on `stream` before its kernels.  Calls whose work
+ *     contents; the call clears what must start at zero (the error word and
+ *     the counters) on `stream` before its kernels.  Calls whose work
  *     overlaps on the GPU (different streams, no ordering) race on it.
  * The calling thread's current device is used.
  */

@@ -218,8 +218,8 @@ __device__ __forceinline__ bool wait_count(const int* p, int target, volatile in
 // the kernel before it is still running.  Every kernel here follows one rule:
 // before griddep_wait() it reads only data that no kernel of the running
 // sequence writes (weights, parameters) or that was written at least two
-// kernels earlier (routing logits of the down kernel, the DeltaNet state
-// slot), and it writes nothing; it triggers its own dependents only after its
+// kernels earlier (the DeltaNet state slot, written by the layer's previous
+// call), and it writes nothing; it triggers its own dependents only after its
 // wait.  So when a kernel starts, the kernel two places before it has
 // finished.  Without the launch attribute both instructions are no-ops.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -1,5 +1,5 @@
 """GPU parity of a full hybrid verify layer stack (verify_layer_k: GDN mixer
-then routed + shared MoE, 9 kernels per layer) against the oracle's
+then routed + shared MoE, 8 kernels per layer) against the oracle's
 composition of its pinned pieces.
 
 Pages: "QWEN38FLASH.md - Plan for supporting Qwen/Qwen3.8-Flash-Next" section 2
