@@ -98,12 +98,14 @@ struct RouteSmem {
 // own activation row alone).
 
 // Weight block kc of a row tile (tile: the row tile's first block).  Reads
-// only static data.
+// only static data, with the evict-first L2 policy (every weight byte is read
+// once per call).
 __device__ __forceinline__ void produce_w(uint8_t* stage_ptr, uint32_t full_bar, const uint8_t* tile, int kc,
                                           int gcount) {
   const uint32_t bytes = kTileSbBytes + gcount * kTileGroupBytes;
   mbar_arrive_expect_tx(full_bar, bytes);
-  bulk_load(smem_addr(stage_ptr), tile + (long long)kc * kTileChunkBytes, bytes, full_bar);
+  bulk_load_hint(smem_addr(stage_ptr), tile + (long long)kc * kTileChunkBytes, bytes, full_bar,
+                 l2_evict_first_policy());
 }
 
 // Activation rows b < nb (brow: their pointers, in shared memory), then this
@@ -454,116 +456,161 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
 
 // ================================================================== MoE
 
-// Top-T routing of every row, recomputed by each CTA (cheap and
-// deterministic): descending logit, equal logits -> lower index; weights =
-// softmax over the T selected logits (fp32).  Then the distinct selected
-// experts in ascending order and, per expert, the bitmask of rows.
+// Top-T routing of every row, recomputed by each CTA (deterministic):
+// descending logit, equal logits -> lower index; weights = softmax over the T
+// selected logits (fp32).  Then the distinct selected experts in ascending
+// order, per expert the bitmask of rows, and the work units.
+//
+// One warp takes R rows at once, interleaved so that their latencies overlap.
+// A logit becomes an order-preserving key (0 = no expert; -0 counts as +0).
+// Each lane keeps its four best keys in descending order (equal keys: lower
+// index first), updated with compares and selects rather than branches.  A
+// round takes the warp maximum key and, among the lanes holding it, the lowest
+// expert index; the winning lane shifts its list and, once its four are taken,
+// rescans its remaining keys (rare).
+template <int R>
+__device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs, const int (&row)[R], int lane) {
+  constexpr int NI = kMaxExperts / 32;
+  constexpr uint32_t FULL = 0xffffffffu;
+  uint32_t key[R][NI];
+  {
+    float v[R][NI];
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      const float* l = a.logits + (long long)(row[q] < 0 ? 0 : row[q]) * a.logits_ld;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int e = lane + 32 * i;
+        v[q][i] = (row[q] >= 0 && e < a.E) ? __ldcg(l + e) : 0.f;  // L2: written by the kernel before
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const uint32_t b = __float_as_uint(v[q][i] == 0.f ? 0.f : v[q][i]);
+        key[q][i] = (row[q] >= 0 && lane + 32 * i < a.E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+      }
+  }
+  uint32_t taken[R], tk[R][4];
+  int ti[R][4];
+  // this lane's four best keys not yet taken, descending
+  auto scan = [&](int q) {
+    uint32_t k0 = 0u, k1 = 0u, k2 = 0u, k3 = 0u;
+    int i0 = 0, i1 = 0, i2 = 0, i3 = 0;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const uint32_t kv = ((taken[q] >> i) & 1u) ? 0u : key[q][i];
+      const bool c0 = kv > k0, c1 = kv > k1, c2 = kv > k2, c3 = kv > k3;  // c0 => c1 => c2 => c3
+      k3 = c2 ? k2 : (c3 ? kv : k3);
+      i3 = c2 ? i2 : (c3 ? i : i3);
+      k2 = c1 ? k1 : (c2 ? kv : k2);
+      i2 = c1 ? i1 : (c2 ? i : i2);
+      k1 = c0 ? k0 : (c1 ? kv : k1);
+      i1 = c0 ? i0 : (c1 ? i : i1);
+      k0 = c0 ? kv : k0;
+      i0 = c0 ? i : i0;
+    }
+    tk[q][0] = k0; tk[q][1] = k1; tk[q][2] = k2; tk[q][3] = k3;
+    ti[q][0] = i0; ti[q][1] = i1; ti[q][2] = i2; ti[q][3] = i3;
+  };
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    taken[q] = 0u;
+    scan(q);
+  }
+  float myv[R];
+  int mye[R];
+#pragma unroll
+  for (int q = 0; q < R; ++q) { myv[q] = 0.f; mye[q] = -1; }
+  for (int j = 0; j < a.T; ++j) {
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      if (row[q] < 0) continue;  // warp-uniform
+      const uint32_t m = __reduce_max_sync(FULL, tk[q][0]);
+      const uint32_t we = __reduce_min_sync(FULL, tk[q][0] == m ? (uint32_t)(lane + 32 * ti[q][0]) : FULL);
+      const bool win = lane == (int)(we & 31u);
+      taken[q] |= win ? (1u << ti[q][0]) : 0u;
+      tk[q][0] = win ? tk[q][1] : tk[q][0]; ti[q][0] = win ? ti[q][1] : ti[q][0];
+      tk[q][1] = win ? tk[q][2] : tk[q][1]; ti[q][1] = win ? ti[q][2] : ti[q][1];
+      tk[q][2] = win ? tk[q][3] : tk[q][2]; ti[q][2] = win ? ti[q][3] : ti[q][2];
+      tk[q][3] = win ? 0u : tk[q][3];
+      if (win && tk[q][0] == 0u) scan(q);  // four taken from this lane: look at the rest
+      if (lane == j) {
+        myv[q] = __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
+        mye[q] = (int)we;
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    if (row[q] < 0) continue;
+    const float top = __shfl_sync(FULL, myv[q], 0);
+    const float ex = lane < a.T ? expf(myv[q] - top) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(FULL, sum, off);
+    sum = __shfl_sync(FULL, sum, 0);
+    if (lane < a.T) {
+      rs->idx[row[q] * kMaxTopK + lane] = mye[q];
+      rs->w[row[q] * kMaxTopK + lane] = ex / sum;
+      atomicOr(&rs->mask[mye[q]], 1u << row[q]);
+    }
+  }
+}
+
+// Routes rows 0 .. k-1 into rs (every thread of the CTA calls it; ends with
+// __syncthreads).  Warp w takes rows w and w + nwarps of each group of
+// 2 nwarps rows, so up to ten rows need a single pass.
 __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
+  constexpr int R = 2;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
   for (int e = tid; e < a.E; e += nthr) rs->mask[e] = 0u;
   __syncthreads();
-  for (int r = warp; r < a.k; r += nwarps) {
-    const float* l = a.logits + (long long)r * a.logits_ld;
-    float v[kMaxExperts / 32];
+  for (int base = 0; base < a.k; base += R * nwarps) {
+    int row[R];
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < a.E ? __ldcg(l + e) : 0.f;  // L2: may precede the grid dependency wait
+    for (int q = 0; q < R; ++q) {
+      const int r = base + warp + q * nwarps;
+      row[q] = r < a.k ? r : -1;
     }
-    // Order-preserving keys (0 = no expert; -0 counts as +0), then this lane's
-    // four best in descending order (equal keys: lower index first).  A round
-    // takes the warp maximum key and, among the lanes holding it, the lowest
-    // expert index; only the winning lane advances its list.
-    uint32_t key[kMaxExperts / 32];
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const uint32_t b = __float_as_uint(v[i] == 0.f ? 0.f : v[i]);
-      key[i] = (lane + 32 * i < a.E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
-    }
-    uint32_t taken = 0, tk[4];
-    int ti[4];
-    auto refill = [&]() {
-      tk[0] = tk[1] = tk[2] = tk[3] = 0u;
-      ti[0] = ti[1] = ti[2] = ti[3] = 0;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const uint32_t kv = ((taken >> i) & 1u) ? 0u : key[i];
-        if (kv > tk[3]) {
-          if (kv > tk[2]) {
-            tk[3] = tk[2]; ti[3] = ti[2];
-            if (kv > tk[1]) {
-              tk[2] = tk[1]; ti[2] = ti[1];
-              if (kv > tk[0]) { tk[1] = tk[0]; ti[1] = ti[0]; tk[0] = kv; ti[0] = i; }
-              else { tk[1] = kv; ti[1] = i; }
-            } else { tk[2] = kv; ti[2] = i; }
-          } else { tk[3] = kv; ti[3] = i; }
-        }
-      }
-    };
-    refill();
-    float myv = 0.f;
-    int mye = -1;
-    for (int j = 0; j < a.T; ++j) {
-      const uint32_t m = __reduce_max_sync(0xffffffffu, tk[0]);
-      const uint32_t we =
-          __reduce_min_sync(0xffffffffu, tk[0] == m ? (uint32_t)(lane + 32 * ti[0]) : 0xffffffffu);
-      if (lane == (int)(we & 31u)) {
-        taken |= 1u << ti[0];
-        tk[0] = tk[1]; ti[0] = ti[1];
-        tk[1] = tk[2]; ti[1] = ti[2];
-        tk[2] = tk[3]; ti[2] = ti[3];
-        tk[3] = 0u;
-        if (tk[0] == 0u) refill();  // four taken from this lane: look at the rest
-      }
-      if (lane == j) {
-        myv = __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
-        mye = (int)we;
-      }
-    }
-    const float top = __shfl_sync(0xffffffffu, myv, 0);
-    const float ex = lane < a.T ? expf(myv - top) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    sum = __shfl_sync(0xffffffffu, sum, 0);
-    if (lane < a.T) {
-      rs->idx[r * kMaxTopK + lane] = mye;
-      rs->w[r * kMaxTopK + lane] = ex / sum;
-      atomicOr(&rs->mask[mye], 1u << r);
-    }
+    if (row[0] >= 0) route_warp_rows<R>(a, rs, row, lane);
   }
   __syncthreads();
   if (warp == 0) {
-    int running = 0;
-    for (int base = 0; base < a.E; base += 32) {
-      const int e = base + lane;
-      const bool f = e < a.E && rs->mask[e] != 0u;
-      const uint32_t bal = __ballot_sync(0xffffffffu, f);
-      if (f) rs->ulist[running + __popc(bal & ((1u << lane) - 1u))] = (int16_t)e;
-      running += __popc(bal);
-    }
-    if (lane == 0) rs->U = running;
-    __syncwarp();
-    // Work units: (expert slot u, chunk of 8 of its rows), the chunks of one
-    // expert adjacent so that its weights are read back to back (L2).  Slot
-    // U is the shared expert (every row).
-    const int slots = running + (a.has_shared ? 1 : 0);
-    int vrun = 0;
-    for (int base = 0; base < slots; base += 32) {
-      const int u = base + lane;
-      int nch = 0;
-      if (u < slots) nch = ((u < running ? __popc(rs->mask[rs->ulist[u]]) : a.k) + 7) >> 3;
-      int incl = nch;
+    // One pass over the masks gives the distinct experts (ascending) and the
+    // work units: (expert slot u, chunk c of 8 of its rows), the chunks of one
+    // expert adjacent so that its weights are read back to back.  At most 16
+    // rows, so an expert has one chunk, or two when more than 8 rows chose it.
+    constexpr int NI = kMaxExperts / 32;
+    uint32_t mk[NI];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += t;
+    for (int i = 0; i < NI; ++i) mk[i] = (lane + 32 * i < a.E) ? rs->mask[lane + 32 * i] : 0u;
+    const uint32_t lt = (1u << lane) - 1u;
+    int running = 0, vrun = 0;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const bool f = mk[i] != 0u, two = __popc(mk[i]) > 8;
+      const uint32_t bf = __ballot_sync(0xffffffffu, f), b2 = __ballot_sync(0xffffffffu, two);
+      if (f) {
+        const int u = running + __popc(bf & lt);
+        const int vp = vrun + __popc(bf & lt) + __popc(b2 & lt);
+        rs->ulist[u] = (int16_t)(lane + 32 * i);
+        rs->vlist[vp] = (int16_t)u;
+        if (two) rs->vlist[vp + 1] = (int16_t)(u | (1 << 12));
       }
-      for (int c = 0; c < nch; ++c) rs->vlist[vrun + incl - nch + c] = (int16_t)(u | (c << 12));
-      vrun += __shfl_sync(0xffffffffu, incl, 31);
+      running += __popc(bf);
+      vrun += __popc(bf) + __popc(b2);
     }
-    if (lane == 0) rs->V = vrun;
+    if (lane == 0) {
+      if (a.has_shared) {  // slot U: the shared expert, every row
+        for (int c = 0; c < (a.k + 7) / 8; ++c) rs->vlist[vrun + c] = (int16_t)(running | (c << 12));
+        vrun += (a.k + 7) / 8;
+      }
+      rs->U = running;
+      rs->V = vrun;
+    }
   }
   __syncthreads();
 }
@@ -756,7 +803,6 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
         ++fills;
         break;
       }
-      if (lane == 0) next = a.G + atomicAdd(a.work, 1);  // the item after this one, fetched early
       bool gu;
       int v, u, rc, tile, nb;
       moe_decode(a, rs, item, n_gu, ntg, ntd, gu, v, u, rc, tile, nb);
@@ -787,6 +833,10 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
         produce_stage<1>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, min(kGroupsPerUnit, KG - 4 * kc), brow, nb,
                          lane);
       }
+      // The next item, fetched once this item's stages are all issued: an
+      // atomic still in flight would hold up this lane's next barrier arrival
+      // (a release), and at the start every CTA fetches at once.
+      if (lane == 0) next = a.G + atomicAdd(a.work, 1);
       next = __shfl_sync(0xffffffffu, next, 0);
       if (*abort) break;
     }
