@@ -524,23 +524,31 @@ __device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs,
 #pragma unroll
   for (int q = 0; q < R; ++q) { myv[q] = 0.f; mye[q] = -1; }
   for (int j = 0; j < a.T; ++j) {
+    // the R rows' reductions back to back (independent), then the updates
+    uint32_t m[R], we[R];
+#pragma unroll
+    for (int q = 0; q < R; ++q) m[q] = __reduce_max_sync(FULL, tk[q][0]);
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+      we[q] = __reduce_min_sync(FULL, tk[q][0] == m[q] ? (uint32_t)(lane + 32 * ti[q][0]) : FULL);
+    bool rescan[R];
 #pragma unroll
     for (int q = 0; q < R; ++q) {
-      if (row[q] < 0) continue;  // warp-uniform
-      const uint32_t m = __reduce_max_sync(FULL, tk[q][0]);
-      const uint32_t we = __reduce_min_sync(FULL, tk[q][0] == m ? (uint32_t)(lane + 32 * ti[q][0]) : FULL);
-      const bool win = lane == (int)(we & 31u);
+      const bool win = row[q] >= 0 && lane == (int)(we[q] & 31u);
       taken[q] |= win ? (1u << ti[q][0]) : 0u;
       tk[q][0] = win ? tk[q][1] : tk[q][0]; ti[q][0] = win ? ti[q][1] : ti[q][0];
       tk[q][1] = win ? tk[q][2] : tk[q][1]; ti[q][1] = win ? ti[q][2] : ti[q][1];
       tk[q][2] = win ? tk[q][3] : tk[q][2]; ti[q][2] = win ? ti[q][3] : ti[q][2];
       tk[q][3] = win ? 0u : tk[q][3];
-      if (win && tk[q][0] == 0u) scan(q);  // four taken from this lane: look at the rest
+      rescan[q] = win && tk[q][0] == 0u;  // four taken from this lane: look at the rest
       if (lane == j) {
-        myv[q] = __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
-        mye[q] = (int)we;
+        myv[q] = __uint_as_float((m[q] & 0x80000000u) ? (m[q] & 0x7fffffffu) : ~m[q]);
+        mye[q] = (int)we[q];
       }
     }
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+      if (rescan[q]) scan(q);
   }
 #pragma unroll
   for (int q = 0; q < R; ++q) {
@@ -559,15 +567,14 @@ __device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs,
   }
 }
 
-// Routes rows 0 .. k-1 into rs (every thread of the CTA calls it; ends with
-// __syncthreads).  Warp w takes rows w and w + nwarps of each group of
-// 2 nwarps rows, so up to ten rows need a single pass.
+// Routes rows 0 .. k-1 into rs (every thread of the CTA calls it, after
+// rs->mask has been zeroed and a CTA barrier; ends with __syncthreads).  Warp
+// w takes rows w and w + nwarps of each group of 2 nwarps rows, so up to ten
+// rows need a single pass.
 __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
   constexpr int R = 2;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
-  for (int e = tid; e < a.E; e += nthr) rs->mask[e] = 0u;
-  __syncthreads();
   for (int base = 0; base < a.k; base += R * nwarps) {
     int row[R];
 #pragma unroll
@@ -583,26 +590,43 @@ __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
     // work units: (expert slot u, chunk c of 8 of its rows), the chunks of one
     // expert adjacent so that its weights are read back to back.  At most 16
     // rows, so an expert has one chunk, or two when more than 8 rows chose it.
-    constexpr int NI = kMaxExperts / 32;
-    uint32_t mk[NI];
+    // Lane l takes experts 16 l .. 16 l + 15: it counts its experts and units,
+    // a warp scan gives its first slots, then it writes its own entries.
+    constexpr int PER = kMaxExperts / 32;
+    uint32_t mk[PER];
+    const uint4* m4 = reinterpret_cast<const uint4*>(rs->mask + PER * lane);
 #pragma unroll
-    for (int i = 0; i < NI; ++i) mk[i] = (lane + 32 * i < a.E) ? rs->mask[lane + 32 * i] : 0u;
-    const uint32_t lt = (1u << lane) - 1u;
-    int running = 0, vrun = 0;
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const bool f = mk[i] != 0u, two = __popc(mk[i]) > 8;
-      const uint32_t bf = __ballot_sync(0xffffffffu, f), b2 = __ballot_sync(0xffffffffu, two);
-      if (f) {
-        const int u = running + __popc(bf & lt);
-        const int vp = vrun + __popc(bf & lt) + __popc(b2 & lt);
-        rs->ulist[u] = (int16_t)(lane + 32 * i);
-        rs->vlist[vp] = (int16_t)u;
-        if (two) rs->vlist[vp + 1] = (int16_t)(u | (1 << 12));
-      }
-      running += __popc(bf);
-      vrun += __popc(bf) + __popc(b2);
+    for (int i = 0; i < PER / 4; ++i) {
+      const uint4 t = m4[i];
+      mk[4 * i] = t.x; mk[4 * i + 1] = t.y; mk[4 * i + 2] = t.z; mk[4 * i + 3] = t.w;
     }
+    int nf = 0, nv = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      nf += mk[i] != 0u;
+      nv += (mk[i] != 0u) + (__popc(mk[i]) > 8);
+    }
+    const int packed = nf | (nv << 16);  // nf <= 512, so the halves never carry into each other
+    int incl = packed;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    int u = (incl - packed) & 0xFFFF, vp = (incl - packed) >> 16;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if (mk[i] != 0u) {
+        rs->ulist[u] = (int16_t)(PER * lane + i);
+        rs->vlist[vp] = (int16_t)u;
+        if (__popc(mk[i]) > 8) rs->vlist[++vp] = (int16_t)(u | (1 << 12));
+        ++u;
+        ++vp;
+      }
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    const int running = tot & 0xFFFF;
+    int vrun = tot >> 16;
     if (lane == 0) {
       if (a.has_shared) {  // slot U: the shared expert, every row
         for (int c = 0; c < (a.k + 7) / 8; ++c) rs->vlist[vrun + c] = (int16_t)(running | (c << 12));
@@ -762,8 +786,11 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
   volatile int* slot_item = abort + 4;  // item id of the item starting in stage s (-1: no more work)
   RouteSmem* rs = reinterpret_cast<RouteSmem*>(smem + L::BASE_BYTES);
+  static_assert(L::BASE_BYTES % 16 == 0, "the routing tables are read with 16-byte loads");
   if (threadIdx.x == 0) *abort = 0;
   init_barriers<CW, ST>(bar_base);
+  for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) rs->mask[e] = 0u;  // shared memory only
+  __syncthreads();
   griddep_wait();  // the routing logits come from the kernel before
   griddep_launch();
   route_rows(a, rs);  // ends with __syncthreads
