@@ -469,7 +469,8 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
 // expert index; the winning lane shifts its list and, once its four are taken,
 // rescans its remaining keys (rare).
 template <int R>
-__device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs, const int (&row)[R], int lane) {
+__device__ __forceinline__ void route_warp_rows(const float* logits, long long ld, int E, int T, RouteSmem* rs,
+                                                const int (&row)[R], int lane) {
   constexpr int NI = kMaxExperts / 32;
   constexpr uint32_t FULL = 0xffffffffu;
   uint32_t key[R][NI];
@@ -477,11 +478,11 @@ __device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs,
     float v[R][NI];
 #pragma unroll
     for (int q = 0; q < R; ++q) {
-      const float* l = a.logits + (long long)(row[q] < 0 ? 0 : row[q]) * a.logits_ld;
+      const float* l = logits + (long long)(row[q] < 0 ? 0 : row[q]) * ld;
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
         const int e = lane + 32 * i;
-        v[q][i] = (row[q] >= 0 && e < a.E) ? __ldcg(l + e) : 0.f;  // L2: written by the kernel before
+        v[q][i] = (row[q] >= 0 && e < E) ? __ldcg(l + e) : 0.f;  // L2: written by the kernel before
       }
     }
 #pragma unroll
@@ -489,7 +490,7 @@ __device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs,
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
         const uint32_t b = __float_as_uint(v[q][i] == 0.f ? 0.f : v[q][i]);
-        key[q][i] = (row[q] >= 0 && lane + 32 * i < a.E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+        key[q][i] = (row[q] >= 0 && lane + 32 * i < E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
       }
   }
   uint32_t taken[R], tk[R][4];
@@ -523,7 +524,7 @@ __device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs,
   int mye[R];
 #pragma unroll
   for (int q = 0; q < R; ++q) { myv[q] = 0.f; mye[q] = -1; }
-  for (int j = 0; j < a.T; ++j) {
+  for (int j = 0; j < T; ++j) {
     // the R rows' reductions back to back (independent), then the updates
     uint32_t m[R], we[R];
 #pragma unroll
@@ -554,12 +555,12 @@ __device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs,
   for (int q = 0; q < R; ++q) {
     if (row[q] < 0) continue;
     const float top = __shfl_sync(FULL, myv[q], 0);
-    const float ex = lane < a.T ? expf(myv[q] - top) : 0.f;
+    const float ex = lane < T ? expf(myv[q] - top) : 0.f;
     float sum = ex;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(FULL, sum, off);
     sum = __shfl_sync(FULL, sum, 0);
-    if (lane < a.T) {
+    if (lane < T) {
       rs->idx[row[q] * kMaxTopK + lane] = mye[q];
       rs->w[row[q] * kMaxTopK + lane] = ex / sum;
       atomicOr(&rs->mask[mye[q]], 1u << row[q]);
@@ -571,18 +572,18 @@ __device__ __forceinline__ void route_warp_rows(const MoeArgs& a, RouteSmem* rs,
 // rs->mask has been zeroed and a CTA barrier; ends with __syncthreads).  Warp
 // w takes rows w and w + nwarps of each group of 2 nwarps rows, so up to ten
 // rows need a single pass.
-__device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
+__device__ void route_rows(const float* logits, long long ld, int E, int T, int k, int has_shared, RouteSmem* rs) {
   constexpr int R = 2;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
-  for (int base = 0; base < a.k; base += R * nwarps) {
+  for (int base = 0; base < k; base += R * nwarps) {
     int row[R];
 #pragma unroll
     for (int q = 0; q < R; ++q) {
       const int r = base + warp + q * nwarps;
-      row[q] = r < a.k ? r : -1;
+      row[q] = r < k ? r : -1;
     }
-    if (row[0] >= 0) route_warp_rows<R>(a, rs, row, lane);
+    if (row[0] >= 0) route_warp_rows<R>(logits, ld, E, T, rs, row, lane);
   }
   __syncthreads();
   if (warp == 0) {
@@ -600,13 +601,13 @@ __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
       const uint4 t = m4[i];
       mk[4 * i] = t.x; mk[4 * i + 1] = t.y; mk[4 * i + 2] = t.z; mk[4 * i + 3] = t.w;
     }
-    int nf = 0, nv = 0;
+    uint32_t fm = 0u, tm = 0u;  // bit i: expert 16 l + i selected; selected by more than 8 rows
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      nf += mk[i] != 0u;
-      nv += (mk[i] != 0u) + (__popc(mk[i]) > 8);
+      fm |= (mk[i] != 0u ? 1u : 0u) << i;
+      tm |= (__popc(mk[i]) > 8 ? 1u : 0u) << i;
     }
-    const int packed = nf | (nv << 16);  // nf <= 512, so the halves never carry into each other
+    const int packed = __popc(fm) | ((__popc(fm) + __popc(tm)) << 16);  // the halves never carry
     int incl = packed;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -614,23 +615,20 @@ __device__ void route_rows(const MoeArgs& a, RouteSmem* rs) {
       if (lane >= off) incl += t;
     }
     int u = (incl - packed) & 0xFFFF, vp = (incl - packed) >> 16;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      if (mk[i] != 0u) {
-        rs->ulist[u] = (int16_t)(PER * lane + i);
-        rs->vlist[vp] = (int16_t)u;
-        if (__popc(mk[i]) > 8) rs->vlist[++vp] = (int16_t)(u | (1 << 12));
-        ++u;
-        ++vp;
-      }
+    for (; fm; fm &= fm - 1u) {
+      const int i = __ffs(fm) - 1;
+      rs->ulist[u] = (int16_t)(PER * lane + i);
+      rs->vlist[vp++] = (int16_t)u;
+      if ((tm >> i) & 1u) rs->vlist[vp++] = (int16_t)(u | (1 << 12));
+      ++u;
     }
     const int tot = __shfl_sync(0xffffffffu, incl, 31);
     const int running = tot & 0xFFFF;
     int vrun = tot >> 16;
     if (lane == 0) {
-      if (a.has_shared) {  // slot U: the shared expert, every row
-        for (int c = 0; c < (a.k + 7) / 8; ++c) rs->vlist[vrun + c] = (int16_t)(running | (c << 12));
-        vrun += (a.k + 7) / 8;
+      if (has_shared) {  // slot U: the shared expert, every row
+        for (int c = 0; c < (k + 7) / 8; ++c) rs->vlist[vrun + c] = (int16_t)(running | (c << 12));
+        vrun += (k + 7) / 8;
       }
       rs->U = running;
       rs->V = vrun;
@@ -793,7 +791,7 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
   __syncthreads();
   griddep_wait();  // the routing logits come from the kernel before
   griddep_launch();
-  route_rows(a, rs);  // ends with __syncthreads
+  route_rows(a.logits, a.logits_ld, a.E, a.T, a.k, a.has_shared, rs);  // ends with __syncthreads
 
   const int TS = a.T + a.has_shared;
   if (blockIdx.x == 0) {
