@@ -286,50 +286,47 @@ cudaError_t launch_gdn(const GdnArgs& a, bool pdl, cudaStream_t s) {
 
 // ------------------------------------------------------------------ glue
 
-// out = x / sqrt(mean(x^2) + eps) * (zc ? 1 + w : w), one CTA per row.
+// out = x / sqrt(mean(x^2) + eps) * (zc ? 1 + w : w), one CTA of 256 threads
+// per row.  Thread t holds elements t, t + 256, ... (VPT of them, n <= 256 VPT)
+// in registers; the weights are static and are loaded before the dependency wait.
+template <int VPT>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const float* w, float eps, int zc, int n,
                                                       void* out, int dtype) {
-  constexpr int U = 8;  // loads in flight per thread
+  const int nt = blockDim.x, tid = threadIdx.x;
+  float wt[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * nt + tid;
+    wt[i] = c < n ? (zc ? 1.f + w[c] : w[c]) : 0.f;
+  }
   griddep_wait();
   griddep_launch();
   const int r = blockIdx.x;
   const float* xr = x + (long long)r * n;
-  const int nt = blockDim.x;
   __shared__ float red[8];
-  float ss = 0.f;
-  for (int base = 0; base < n; base += U * nt) {
-    float v[U];
+  float v[VPT];
 #pragma unroll
-    for (int i = 0; i < U; ++i) {
-      const int c = base + i * nt + threadIdx.x;
-      v[i] = c < n ? xr[c] : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < U; ++i) ss = fmaf(v[i], v[i], ss);
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * nt + tid;
+    v[i] = c < n ? xr[c] : 0.f;
   }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) ss = fmaf(v[i], v[i], ss);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
   __syncthreads();
   float tot = 0.f;
   for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
   const float inv = 1.f / sqrtf(tot / (float)n + eps);
-  for (int base = 0; base < n; base += U * nt) {
-    float v[U], wt[U];
 #pragma unroll
-    for (int i = 0; i < U; ++i) {
-      const int c = base + i * nt + threadIdx.x;
-      v[i] = c < n ? xr[c] : 0.f;
-      wt[i] = c < n ? w[c] : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < U; ++i) {
-      const int c = base + i * nt + threadIdx.x;
-      if (c >= n) break;
-      const float o = v[i] * inv * (zc ? 1.f + wt[i] : wt[i]);
-      if (dtype == 1) reinterpret_cast<uint16_t*>(out)[(long long)r * n + c] = f2bf16(o);
-      else reinterpret_cast<float*>(out)[(long long)r * n + c] = o;
-    }
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * nt + tid;
+    if (c >= n) break;
+    const float o = v[i] * inv * wt[i];
+    if (dtype == 1) reinterpret_cast<uint16_t*>(out)[(long long)r * n + c] = f2bf16(o);
+    else reinterpret_cast<float*>(out)[(long long)r * n + c] = o;
   }
 }
 
@@ -345,7 +342,11 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, in
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, rmsnorm_kernel, x, w, eps, zc, n, out, dtype);
+  if (n <= 256 * 4) return cudaLaunchKernelEx(&cfg, rmsnorm_kernel<4>, x, w, eps, zc, n, out, dtype);
+  if (n <= 256 * 8) return cudaLaunchKernelEx(&cfg, rmsnorm_kernel<8>, x, w, eps, zc, n, out, dtype);
+  if (n <= 256 * 16) return cudaLaunchKernelEx(&cfg, rmsnorm_kernel<16>, x, w, eps, zc, n, out, dtype);
+  if (n <= 256 * 32) return cudaLaunchKernelEx(&cfg, rmsnorm_kernel<32>, x, w, eps, zc, n, out, dtype);
+  return cudaLaunchKernelEx(&cfg, rmsnorm_kernel<64>, x, w, eps, zc, n, out, dtype);  // n <= 16384
 }
 
 }  // namespace vk

@@ -372,7 +372,8 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     if (*abort) producer_drain(bar_base, fills);
     if (S > 1) {  // the producer warp takes part in the cluster barriers
       cluster_sync();
-      cluster_sync();
+      cluster_arrive();
+      cluster_wait();
     }
     return;
   }
@@ -397,7 +398,12 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_base + 8 * (kStages + s));
   }
-  bool mine = true;  // does this CTA write this warp's outputs?
+  // Which of this warp's row tiles does this CTA write?  With S > 1, 16-row
+  // tile mt of the 128-row tile belongs to rank mt % S, which sums the S
+  // partial tiles in rank order.
+  bool mine[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) mine[m] = S == 1 || ((warp * MT + m) % S) == split;
   if (S > 1) {
     // every stage has been consumed: stage 0 now holds this CTA's partial tile
     float4* part = reinterpret_cast<float4*>(smem);
@@ -407,39 +413,35 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
       for (int t = 0; t < NT; ++t)
         part[((warp * MT + m) * NT + t) * 32 + lane] = make_float4(acc[m][t][0], acc[m][t][1], acc[m][t][2], acc[m][t][3]);
     cluster_sync();
-    mine = (warp % S) == split;
-    if (mine) {
-      // Sum the S partial tiles in rank order.  The next rank's four-float
-      // loads are issued before this rank's adds, so the remote-load latency
-      // is paid about once rather than once per value.
-      zero_acc<MT, NT>(acc);
-      float4 cur[MT][NT], nxt[MT][NT];
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
+    for (int m = 0; m < MT; ++m) {
+      if (!mine[m]) continue;  // warp-uniform
+      // all S ranks' four-float loads in flight at once, then the adds in rank order
+      float4 pv[kMaxSplits][NT];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) cur[m][t] = ld_dsmem_f32x4(part + ((warp * MT + m) * NT + t) * 32 + lane, 0u);
-      for (int q = 0; q < S; ++q) {
-        if (q + 1 < S) {
+      for (int q = 0; q < kMaxSplits; ++q)
 #pragma unroll
-          for (int m = 0; m < MT; ++m)
+        for (int t = 0; t < NT; ++t)
+          if (q < S) pv[q][t] = ld_dsmem_f32x4(part + ((warp * MT + m) * NT + t) * 32 + lane, (uint32_t)q);
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
-              nxt[m][t] = ld_dsmem_f32x4(part + ((warp * MT + m) * NT + t) * 32 + lane, (uint32_t)(q + 1));
-        }
+      for (int t = 0; t < NT; ++t) {
+        acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            acc[m][t][0] += cur[m][t].x;
-            acc[m][t][1] += cur[m][t].y;
-            acc[m][t][2] += cur[m][t].z;
-            acc[m][t][3] += cur[m][t].w;
-            cur[m][t] = nxt[m][t];
+        for (int q = 0; q < kMaxSplits; ++q)
+          if (q < S) {
+            acc[m][t][0] += pv[q][t].x;
+            acc[m][t][1] += pv[q][t].y;
+            acc[m][t][2] += pv[q][t].z;
+            acc[m][t][3] += pv[q][t].w;
           }
       }
     }
+    cluster_arrive();  // this CTA has read its peers' partial tiles
   }
-  if (mine && !*abort) {
+  if (!*abort) {
+    // y += result: every old value is loaded before the first store, so that
+    // the loads overlap instead of waiting behind the stores
+    float old[MT][NT][4];
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -448,10 +450,25 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
         for (int q = 0; q < 4; ++q) {
           const int row = tile * kBM + rbase[m] + g + 8 * (q >> 1);
           const int col = 8 * t + 2 * c + (q & 1);
-          if (row < a.N && col < a.k) store_out(a.y, a.dtype, (long long)col * a.N + row, acc[m][t][q]);
+          old[m][t][q] = (a.dtype == 2 && mine[m] && row < a.N && col < a.k)
+                             ? reinterpret_cast<const float*>(a.y)[(long long)col * a.N + row]
+                             : 0.f;
+        }
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int row = tile * kBM + rbase[m] + g + 8 * (q >> 1);
+          const int col = 8 * t + 2 * c + (q & 1);
+          if (!mine[m] || row >= a.N || col >= a.k) continue;
+          const long long i = (long long)col * a.N + row;
+          if (a.dtype == 2) reinterpret_cast<float*>(a.y)[i] = old[m][t][q] + acc[m][t][q];
+          else store_out(a.y, a.dtype, i, acc[m][t][q]);
         }
   }
-  if (S > 1) cluster_sync();  // peers keep their shared memory until every rank has read it
+  if (S > 1) cluster_wait();  // peers keep their shared memory until every rank has read it
 }
 
 // ================================================================== MoE
@@ -738,12 +755,15 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
   }
   const float vs = a.has_shared ? __ldcg(pr + (long long)a.T * a.H) : 0.f;
   const float sg = a.has_shared ? __ldcg(a.shared_logit + (long long)r * a.logits_ld) : 0.f;
+  // y += result: the old value is loaded with the partials
+  const float yo = a.dtype == 2 ? reinterpret_cast<const float*>(a.y)[(long long)r * a.H + n] : 0.f;
   float y = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j)
     if (j < a.T) y = fmaf(wj[j], v[j], y);
   if (a.has_shared) y = fmaf(1.f / (1.f + expf(-sg)), vs, y);
-  store_out(a.y, a.dtype, (long long)r * a.H + n, y);
+  if (a.dtype == 2) reinterpret_cast<float*>(a.y)[(long long)r * a.H + n] = yo + y;
+  else store_out(a.y, a.dtype, (long long)r * a.H + n, y);
 }
 
 // The routed-expert products as one persistent kernel (a third kernel, the

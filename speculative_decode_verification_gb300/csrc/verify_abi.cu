@@ -112,7 +112,7 @@ long long rt_bytes(int k_in) {
 int dense_splits(const verify_ctx* ctx, int RB, int KC) {
   const int slots = ctx->dense_ctas_per_sm * ctx->num_sms;
   int S = 1;  // powers of two pack into the GPCs without leaving a partial second wave
-  while (2 * S <= 8 && 2 * S <= KC && RB * 2 * S <= slots) S *= 2;
+  while (2 * S <= vk::kMaxSplits && 2 * S <= KC && RB * 2 * S <= slots) S *= 2;
   return S;
 }
 
