@@ -26,25 +26,33 @@
 
 namespace vk {
 
-constexpr int kGdnRows = 16;      // value rows per CTA
-constexpr int kGdnThreads = 128;  // 8 threads per value row
+constexpr int kGdnRows = 16;  // value rows per CTA
 constexpr int kGdnMaxK = 16;
+
+// Threads per value row: each holds D / TPR state columns (a multiple of 4).
+template <int D>
+struct GdnShape {
+  static constexpr int TPR = D >= 64 ? 16 : 8;
+  static constexpr int THREADS = kGdnRows * TPR;  // 256 for D >= 64
+  static constexpr int NV4 = D / TPR / 4;         // float4 groups of state columns per thread
+  static constexpr int P = D / kGdnRows;          // CTAs per head (cluster size)
+};
 
 __device__ __forceinline__ float sigmoidf_(float t) { return 1.f / (1.f + expf(-t)); }
 __device__ __forceinline__ float siluf_(float t) { return t / (1.f + expf(-t)); }
 __device__ __forceinline__ float softplusf_(float t) { return fmaxf(t, 0.f) + log1pf(expf(-fabsf(t))); }
 
 template <int D>
-__global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a) {
-  constexpr int P = D / kGdnRows;   // CTAs per head (cluster size)
-  constexpr int JPT = D / 8;        // state columns per thread
+__global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const GdnArgs a) {
+  using SH = GdnShape<D>;
+  constexpr int TPR = SH::TPR, NT = SH::THREADS, NV4 = SH::NV4, P = SH::P;
   __shared__ __align__(16) float qn[kGdnMaxK][D];
   __shared__ __align__(16) float kn[kGdnMaxK][D];
   __shared__ float vs[kGdnMaxK][kGdnRows];
   __shared__ float ys[kGdnMaxK][kGdnRows];
   __shared__ float gs[kGdnMaxK], bs[kGdnMaxK], kq[kGdnMaxK];
   __shared__ float ss_part[kGdnMaxK];
-  __shared__ float ss_all[kGdnMaxK][D / kGdnRows];
+  __shared__ float ss_all[kGdnMaxK][P];
   __shared__ float inv_s[kGdnMaxK];
 
   const int p = (int)cluster_rank();
@@ -55,30 +63,31 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   const int C = 2 * a.Hk * D + a.Hv * D;
   const bool owns_qk_tail = (h % (a.Hv / a.Hk)) == 0;
 
-  const int il = tid >> 3, l = tid & 7;
+  // thread (il, l): value row il of this CTA, state columns 4 l + 4 TPR m + e
+  const int il = tid / TPR, l = tid % TPR;
   const int i = p * kGdnRows + il;  // value row within the head
 
   // ---- before the grid dependency wait: the state slice and the conv
   //      weights and tail (parameters, or written by an earlier verify call)
-  float s[JPT];
+  float s[4 * NV4];
   {
     const float* src = a.S_in + ((long long)h * D + i) * D;
 #pragma unroll
-    for (int m = 0; m < JPT / 4; ++m) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * l + 32 * m));
+    for (int m = 0; m < NV4; ++m) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * l + 4 * TPR * m));
       s[4 * m] = v.x; s[4 * m + 1] = v.y; s[4 * m + 2] = v.z; s[4 * m + 3] = v.w;
     }
   }
   // Conv channels of this CTA: the q and k channels of QK head hq, then the v
-  // channels of its value rows; thread tid takes channels tid, tid + 128, ...
+  // channels of its value rows; thread tid takes channels tid, tid + NT, ...
   constexpr int NCH = 2 * D + kGdnRows;
-  constexpr int NIT = (NCH + kGdnThreads - 1) / kGdnThreads;
+  constexpr int NIT = (NCH + NT - 1) / NT;
   int chn[NIT];
   float cw[NIT][4];
   uint16_t tl[NIT][3];
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
-    const int cl = tid + it * kGdnThreads;
+    const int cl = tid + it * NT;
     int ch = 0;
     if (cl < D) ch = hq * D + cl;
     else if (cl < 2 * D) ch = a.Hk * D + hq * D + (cl - D);
@@ -98,10 +107,16 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   for (int it = 0; it < NIT; ++it)
 #pragma unroll
     for (int r = 0; r < kGdnMaxK; ++r)
-      xin[it][r] = (r < k && tid + it * kGdnThreads < NCH) ? a.qkv[r * a.ld_qkv + chn[it]] : (uint16_t)0;
+      xin[it][r] = (r < k && tid + it * NT < NCH) ? a.qkv[r * a.ld_qkv + chn[it]] : (uint16_t)0;
+  // gate inputs, loaded with the conv inputs
+  float av = 0.f, bv = 0.f;
+  if (tid < k) {
+    av = bf16f(a.a[tid * a.ld_a + h]);
+    bv = bf16f(a.b[tid * a.ld_b + h]);
+  }
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
-    const int cl = tid + it * kGdnThreads;
+    const int cl = tid + it * NT;
     if (cl >= NCH) break;
     const int ch = chn[it];
     bool write_tail;
@@ -131,17 +146,15 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   }
   // ---- gates
   if (tid < k) {
-    const int r = tid;
-    const float av = bf16f(a.a[r * a.ld_a + h]), bv = bf16f(a.b[r * a.ld_b + h]);
-    bs[r] = sigmoidf_(bv);
-    gs[r] = expf(-expf(a.A_log[h]) * softplusf_(av + a.dt_bias[h]));
+    bs[tid] = sigmoidf_(bv);
+    gs[tid] = expf(-expf(a.A_log[h]) * softplusf_(av + a.dt_bias[h]));
   }
   __syncthreads();
 
-  // ---- 2. L2 norms of q and k per row (warp w: rows w, w+4, ...), k.q
+  // ---- 2. L2 norms of q and k per row (warp w: rows w, w + NT/32, ...), k.q
   {
     const int warp = tid >> 5, lane = tid & 31;
-    for (int r = warp; r < k; r += kGdnThreads / 32) {
+    for (int r = warp; r < k; r += NT / 32) {
       float sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int j = lane; j < D; j += 32) {
@@ -175,9 +188,9 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
     const float g = gs[r], beta = bs[r];
     float mk = 0.f, mq = 0.f;
 #pragma unroll
-    for (int m = 0; m < JPT / 4; ++m) {
-      const float4 kv = *reinterpret_cast<const float4*>(&kn[r][4 * l + 32 * m]);
-      const float4 qv = *reinterpret_cast<const float4*>(&qn[r][4 * l + 32 * m]);
+    for (int m = 0; m < NV4; ++m) {
+      const float4 kv = *reinterpret_cast<const float4*>(&kn[r][4 * l + 4 * TPR * m]);
+      const float4 qv = *reinterpret_cast<const float4*>(&qn[r][4 * l + 4 * TPR * m]);
       const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
       const float qq[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
@@ -189,7 +202,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
       }
     }
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) {
+    for (int off = TPR / 2; off > 0; off >>= 1) {  // the TPR threads of this value row
       mk += __shfl_xor_sync(0xffffffffu, mk, off);
       mq += __shfl_xor_sync(0xffffffffu, mq, off);
     }
@@ -197,13 +210,14 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
     const float y = fmaf(delta, kq[r], mq);  // (S + delta k^T) q = S q + delta (k.q)
     float* dst = a.S_out[r] + ((long long)h * D + i) * D;
 #pragma unroll
-    for (int m = 0; m < JPT / 4; ++m) {
-      const float4 kv = *reinterpret_cast<const float4*>(&kn[r][4 * l + 32 * m]);
+    for (int m = 0; m < NV4; ++m) {
+      const float4 kv = *reinterpret_cast<const float4*>(&kn[r][4 * l + 4 * TPR * m]);
       s[4 * m] = fmaf(delta, kv.x, s[4 * m]);
       s[4 * m + 1] = fmaf(delta, kv.y, s[4 * m + 1]);
       s[4 * m + 2] = fmaf(delta, kv.z, s[4 * m + 2]);
       s[4 * m + 3] = fmaf(delta, kv.w, s[4 * m + 3]);
-      *reinterpret_cast<float4*>(dst + 4 * l + 32 * m) = make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]);
+      *reinterpret_cast<float4*>(dst + 4 * l + 4 * TPR * m) =
+          make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]);
     }
     if (l == 0) ys[r][il] = y;
   }
@@ -211,10 +225,11 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
 
   // ---- 4. gated RMSNorm over the head's D value rows (cluster-wide sum)
   // The output gates do not depend on the sum: load them first.
-  float act[2], nw[2];
+  constexpr int EPT = (kGdnMaxK * kGdnRows + NT - 1) / NT;  // outputs per thread
+  float act[EPT], nw[EPT];
 #pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int e = tid + h2 * kGdnThreads;
+  for (int h2 = 0; h2 < EPT; ++h2) {
+    const int e = tid + h2 * NT;
     act[h2] = 0.f;
     nw[h2] = 0.f;
     if (e < k * kGdnRows) {
@@ -232,6 +247,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   cluster_sync();
   // one remote load per (row, rank), all in flight together; then the sum in rank order
   if (tid < k * P) ss_all[tid / P][tid % P] = ld_dsmem_f32(&ss_part[tid / P], (uint32_t)(tid % P));
+  cluster_arrive();  // this CTA has read its peers' sums
   __syncthreads();
   if (tid < k) {
     float tot = 0.f;
@@ -240,8 +256,8 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
   }
   __syncthreads();
 #pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int e = tid + h2 * kGdnThreads;
+  for (int h2 = 0; h2 < EPT; ++h2) {
+    const int e = tid + h2 * NT;
     if (e >= k * kGdnRows) break;
     const int r = e / kGdnRows, ii = e % kGdnRows;
     const int iv = p * kGdnRows + ii;
@@ -250,15 +266,15 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_verify_kernel(const GdnArgs a
     if (a.dtype == 1) reinterpret_cast<uint16_t*>(a.o)[oi] = f2bf16(ov);
     else reinterpret_cast<float*>(a.o)[oi] = ov;
   }
-  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+  cluster_wait();  // keep this CTA's shared memory alive until every peer has read it
 }
 
 template <int D>
 static cudaError_t launch_gdn_d(const GdnArgs& a, bool pdl, cudaStream_t s) {
-  constexpr int P = D / kGdnRows;
+  constexpr int P = GdnShape<D>::P;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.Hv * P);
-  cfg.blockDim = dim3(kGdnThreads);
+  cfg.blockDim = dim3(GdnShape<D>::THREADS);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
