@@ -405,7 +405,9 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
 #pragma unroll
   for (int m = 0; m < MT; ++m) mine[m] = S == 1 || ((warp * MT + m) % S) == split;
   if (S > 1) {
-    // every stage has been consumed: stage 0 now holds this CTA's partial tile
+    // Stage 0 now holds this CTA's partial tile: once every consumer warp is
+    // done with the last stage, which may itself be stage 0.
+    named_bar(2, CW * 32);
     float4* part = reinterpret_cast<float4*>(smem);
 #pragma unroll
     for (int m = 0; m < MT; ++m)
