@@ -98,6 +98,11 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
 #pragma unroll
     for (int t = 0; t < 3; ++t) tl[it][t] = cl < NCH ? __ldcg(a.tail_in + t * C + ch) : (uint16_t)0;
   }
+  // gated RMSNorm: output e = tid + NT h2 is (row e / 16, value row e % 16)
+  constexpr int EPT = (kGdnMaxK * kGdnRows + NT - 1) / NT;  // outputs per thread
+  float nw[EPT];
+#pragma unroll
+  for (int h2 = 0; h2 < EPT; ++h2) nw[h2] = a.norm_w[p * kGdnRows + (tid + h2 * NT) % kGdnRows];
   griddep_wait();
   griddep_launch();
 
@@ -108,6 +113,12 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
 #pragma unroll
     for (int r = 0; r < kGdnMaxK; ++r)
       xin[it][r] = (r < k && tid + it * NT < NCH) ? a.qkv[r * a.ld_qkv + chn[it]] : (uint16_t)0;
+  uint16_t zin[EPT];
+#pragma unroll
+  for (int h2 = 0; h2 < EPT; ++h2) {
+    const int e = tid + h2 * NT;
+    zin[h2] = e < k * kGdnRows ? a.z[(e / kGdnRows) * a.ld_z + h * D + p * kGdnRows + e % kGdnRows] : (uint16_t)0;
+  }
   // gate inputs, loaded with the conv inputs
   float av = 0.f, bv = 0.f;
   if (tid < k) {
@@ -224,20 +235,12 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
   __syncthreads();
 
   // ---- 4. gated RMSNorm over the head's D value rows (cluster-wide sum)
-  // The output gates do not depend on the sum: load them first.
-  constexpr int EPT = (kGdnMaxK * kGdnRows + NT - 1) / NT;  // outputs per thread
-  float act[EPT], nw[EPT];
+  // The output gates do not depend on the sum: compute them first.
+  float act[EPT];
 #pragma unroll
   for (int h2 = 0; h2 < EPT; ++h2) {
-    const int e = tid + h2 * NT;
-    act[h2] = 0.f;
-    nw[h2] = 0.f;
-    if (e < k * kGdnRows) {
-      const int r = e / kGdnRows, iv = p * kGdnRows + e % kGdnRows;
-      const float zz = bf16f(a.z[r * a.ld_z + h * D + iv]);
-      act[h2] = a.gate_act == 1 ? siluf_(zz) : sigmoidf_(zz);
-      nw[h2] = a.norm_w[iv];
-    }
+    const float zz = bf16f(zin[h2]);
+    act[h2] = a.gate_act == 1 ? siluf_(zz) : sigmoidf_(zz);
   }
   if (tid < k) {
     float ss = 0.f;
