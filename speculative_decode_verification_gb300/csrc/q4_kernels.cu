@@ -768,8 +768,9 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
   else store_out(a.y, a.dtype, (long long)r * a.H + n, y);
 }
 
-// The routed-expert products as one persistent kernel (a third kernel, the
-// combine, follows).  Work items, handed out in order by an atomic counter:
+// The routed-expert products as one persistent kernel (a second kernel, the
+// combine, follows).  Work items, in order: CTA b takes item b first, later
+// items come from a global counter (item G, G + 1, ...):
 //   [0, n_gu)         gate/up items (unit v, 64 outputs of I): gate rows and
 //                     up rows of the same outputs go to the same warp, the
 //                     epilogue applies SwiGLU and writes h (bf16) for the
@@ -779,8 +780,9 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
 //                     done[v] == I / 64, all gate/up tiles of the unit.
 // A unit is (distinct expert or the shared expert, chunk of up to 8 of its
 // rows).  Items are unit-major: concurrent CTAs stream consecutive slices of
-// one expert.  A down item is handed out only after every gate/up item, and
-// a handed-out item belongs to a running CTA, so every wait ends (bounded).
+// one expert.  Every gate/up item comes before every down item, and each is
+// held by a running CTA that depends on nothing to finish it, so every wait
+// of a down item ends (bounded).
 __device__ __forceinline__ void moe_decode(const MoeArgs& a, const RouteSmem* rs, int item, int n_gu, int ntg,
                                            int ntd, bool& gu, int& v, int& u, int& rc, int& tile, int& nb) {
   gu = item < n_gu;
