@@ -406,6 +406,150 @@ def run_ours(args, cfg):
     return 0
 
 
+def run_kernels(args):
+    """Each hot-path kernel alone on its own configuration.  A timed batch is
+    R back-to-back calls between two CUDA events on the launching stream,
+    rotating over enough weight copies or input sets that a batch touches more
+    than 3 x L2, so no call finds its inputs in L2; per-call time = batch
+    time / R, median of --steps batches after --warmup.  One JSON line per
+    (kernel, config, k), then a summary line.  Not the bench contract line: a
+    per-kernel roofline table."""
+    import torch
+    from speculative_decode_verification_gb300 import binding as B
+    from speculative_decode_verification_gb300 import synth as S
+
+    vf = B.Verify(0)
+    hbm, peak_kind = peaks()
+    stream = torch.cuda.Stream()
+    L2 = 129 << 20
+    keep = []
+
+    def q4(name, n_out, k_in, n_experts=None, gate_up=False):
+        e = 1 if n_experts is None else n_experts
+        shp = (e, n_out, k_in // 8) if n_experts else (n_out, k_in // 8)
+        gshp = (e, n_out, k_in // 64) if n_experts else (n_out, k_in // 64)
+        p = torch.empty(shp, dtype=torch.int32, device="cuda")
+        sc = torch.empty(gshp, dtype=torch.int16, device="cuda")
+        bi = torch.empty(gshp, dtype=torch.int16, device="cuda")
+        vf.synth_q4(p, sc, bi, S.q4_seeds(0, name), S.SCALE_RANGE, S.BIAS_RANGE, centered=False)
+        rows = B.q4_experts(p, sc, bi) if n_experts else B.q4_weight(p, sc, bi)
+        t = vf.tile(rows, gate_up=gate_up)
+        torch.cuda.synchronize()
+        del p, sc, bi
+        keep.append(t.buf)
+        return t.struct
+
+    def dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        keep.append(t)
+        return t
+
+    def time_calls(calls, R=40):
+        """calls: the rotation set (callables).  Median per-call microseconds."""
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for it in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                e0.record()
+                for i in range(R):
+                    calls[(it * R + i) % len(calls)]()
+                e1.record()
+            e1.synchronize()
+            if it >= args.warmup:
+                ts.append(e0.elapsed_time(e1) * 1e3 / R)
+        return float(np.median(ts))
+
+    lines = []
+
+    def emit(kernel, config, k, us, nbytes, extra=None):
+        d = {"kernel": kernel, "config": config, "k": k, "us": round(us, 3), "bytes": int(nbytes),
+             "GBs": round(nbytes / us / 1e3, 1), "frac": round(nbytes / us / 1e3 / hbm, 4), "peak": hbm,
+             "peak_kind": peak_kind}
+        if extra:
+            d.update(extra)
+        lines.append(d)
+        print(json.dumps(d), flush=True)
+
+    widths = [int(w) for w in args.widths.split(",") if w]
+    kmax = max(widths)
+    # a1: dense Q4 products, the dense configuration's shapes; copies rotated
+    for (N, K) in S.DENSE_SHAPES:
+        wbytes = 0.5625 * N * K
+        n_copies = int(np.ceil(3 * L2 / wbytes)) + 1
+        Ws = [q4(f"kbench.dense.{N}x{K}.c{c}", N, K) for c in range(n_copies)]
+        x = dev(S.bf16_normal(0, f"kbench.x.{K}", (kmax, K)).view(np.int16))
+        y = torch.empty((kmax, N), dtype=torch.float32, device="cuda")
+        t1 = None
+        for k in widths:
+            us = time_calls([(lambda W=W, k=k: vf.q4_qmv_k(W, x, k, y, B.F32, stream.cuda_stream)) for W in Ws])
+            t1 = us if k == 1 else t1
+            emit("q4_qmv_k", f"dense {N}x{K}", k, us, wbytes + 2 * k * K + 4 * k * N,
+                 {"t_over_t1": round(us / t1, 3) if t1 else None, "copies": n_copies})
+        del Ws
+        keep.clear()
+        torch.cuda.empty_cache()
+    # a2-a4: routed experts, the Ornith-shaped configuration (no shared expert);
+    # the expert weights (453 MB) exceed 3 x L2; 8 input sets rotated
+    m = S.ORNITH_MOE
+    E, T, H, I = m["E"], m["T"], m["H"], m["I"]
+    gu = q4("kbench.moe.gu", 2 * I, H, E, gate_up=True)
+    dn = q4("kbench.moe.dn", H, I, E)
+    for k in widths:
+        sets = []
+        for r in range(8):
+            logits = dev(S.f32_normal(0, f"kbench.moe.l{k}.{r}", (k, E)))
+            x = dev(S.bf16_normal(0, f"kbench.moe.x{k}.{r}", (k, H)).view(np.int16))
+            idx = torch.zeros((k, T), dtype=torch.int32, device="cuda")
+            w = torch.zeros((k, T), dtype=torch.float32, device="cuda")
+            y = torch.zeros((k, H), dtype=torch.float32, device="cuda")
+            keep.extend([idx, w, y])
+            sets.append((logits, x, idx, w, y))
+        us = time_calls([(lambda st=st, k=k: vf.q4_gather_experts_k(gu, dn, st[0], E, T, st[1], k, st[2], st[3], st[4],
+                                                                     B.F32, stream=stream.cuda_stream))
+                         for st in sets])
+        U = float(np.mean([np.unique(st[2].cpu().numpy()).size for st in sets]))
+        emit("q4_gather_experts_k", f"experts E{E} T{T} H{H} I{I}", k, us,
+             U * 3 * H * I * 0.5625 + k * H * (2 + 4) + k * E * 4, {"distinct_experts": U})
+    del gu, dn
+    keep.clear()
+    torch.cuda.empty_cache()
+    # a5-a7: the GDN verify step, the Flash-Next-shaped configuration; 8 state
+    # rings and input sets rotated
+    g = S.FLASH_GDN
+    Hk, Hv, d = g["n_qk_heads"], g["n_v_heads"], g["d"]
+    C = 2 * Hk * d + Hv * d
+    gp = {key: dev(v) for key, v in S.gdn_params(0, "kbench.gdn", Hk, Hv, d).items()}
+    params = B.gdn_params(Hk, Hv, d, gp["conv_w"], gp["A_log"], gp["dt_bias"], gp["norm_w"])
+    S0, t0 = S.gdn_initial_state(0, "kbench.gdn", Hk, Hv, d, s_std=0.02, tail_std=1.0)
+    rings = []
+    for r in range(8):
+        slots = [dev(S0) if s == 0 else torch.zeros((Hv, d, d), dtype=torch.float32, device="cuda")
+                 for s in range(kmax + 1)]
+        tails = [dev(t0.view(np.int16)) if s == 0 else torch.zeros((3, C), dtype=torch.int16, device="cuda")
+                 for s in range(kmax + 1)]
+        keep.extend(slots + tails)
+        rings.append((slots, tails))
+    for k in widths:
+        calls = []
+        for r, (slots, tails) in enumerate(rings):
+            inp = {key: dev(v.view(np.int16) if v.dtype == np.uint16 else v)
+                   for key, v in S.gdn_inputs(0, f"kbench.gdn.{k}.{r}", k, Hk, Hv, d).items()}
+            o = torch.empty((k, Hv * d), dtype=torch.float32, device="cuda")
+            keep.append(o)
+            gi = B.gdn_inputs(inp["qkv"], inp["z"], inp["a"], inp["b"])
+
+            def call(slots=slots, tails=tails, gi=gi, o=o, k=k):
+                vf.gdn_verify_k(params, B.gdn_state(slots, tails, cur=0), gi, k, o, B.F32, stream.cuda_stream)
+
+            calls.append(call)
+        us = time_calls(calls)
+        nbytes = Hv * d * d * 4 * (1 + k) + 3 * C * 2 * (1 + k) + k * (C + Hv * d + 2 * Hv) * 2 + k * Hv * d * 4
+        emit("gdn_verify_k", f"gdn Hk{Hk} Hv{Hv} d{d}", k, us, nbytes)
+    print(json.dumps({"summary": "per-kernel roofline: back-to-back calls, weights or inputs rotated over > 3 x L2",
+                      "n": len(lines), "peak": hbm, "peak_kind": peak_kind}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -416,12 +560,16 @@ def main():
     ap.add_argument("--widths", default="1,4,8,9", help="widths also measured (reported under config.per_k)")
     ap.add_argument("--layers", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels", action="store_true",
+                    help="time each hot-path kernel alone on its own configuration instead (JSON line per kernel)")
     args = ap.parse_args()
     from speculative_decode_verification_gb300 import synth as S
     cfg = dict(S.STACK)
     cfg["layers"] = args.layers
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.kernels:
+        return run_kernels(args)
     return run_ours(args, cfg)
 
 

@@ -85,6 +85,8 @@ struct GdnArgs {
 
 // Launchers (return the first CUDA error; *launches counts kernels launched).
 cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm);
+// max_clusters[S], S = 1 .. kMaxSplits: dense-kernel clusters of S CTAs resident at once.
+cudaError_t q4_dense_cluster_limits(int* max_clusters);
 // pdl: launch with programmatic stream serialization (the kernel may start
 // while the previous kernel on the stream runs; see griddep_wait).
 cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s);

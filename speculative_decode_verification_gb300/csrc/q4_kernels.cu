@@ -955,6 +955,37 @@ cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm) {
   return cudaSuccess;
 }
 
+// For every cluster size S = 1 .. kMaxSplits: how many clusters of S dense
+// CTAs the GPU runs at once (the smaller of the two column-block widths, so
+// that the split of K, chosen from it, does not depend on k).
+cudaError_t q4_dense_cluster_limits(int* max_clusters) {
+  constexpr int TD = Warps<kDenseWarps>::THREADS;
+  max_clusters[0] = 0;
+  for (int S = 1; S <= kMaxSplits; ++S) {
+    int best = 1 << 30;
+    for (int nt = 1; nt <= 2; ++nt) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(S * 64);
+      cfg.blockDim = dim3(TD);
+      cfg.dynamicSmemBytes = nt == 1 ? dense_smem<1>() : dense_smem<2>();
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = S;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      cudaError_t e = nt == 1 ? cudaOccupancyMaxActiveClusters(&n, q4_dense_kernel<1>, &cfg)
+                              : cudaOccupancyMaxActiveClusters(&n, q4_dense_kernel<2>, &cfg);
+      if (e) return e;
+      best = n < best ? n : best;
+    }
+    max_clusters[S] = best;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.RB * a.S);

@@ -12,6 +12,7 @@ struct verify_ctx {
   int device = 0;
   int num_sms = 0;
   int dense_ctas_per_sm = 0;
+  int dense_max_clusters[vk::kMaxSplits + 1] = {};  // clusters of S dense CTAs resident at once
   int moe_ctas_per_sm = 0;
   uint16_t* moe_hbuf = nullptr;
   float* moe_part = nullptr;
@@ -105,14 +106,14 @@ long long rt_bytes(int k_in) {
   return (long long)vk::kTileSbBytes * KC + (long long)vk::kTileGroupBytes * KG;
 }
 
-// K-splits per row tile: the largest power of two (at most 8, the portable
-// cluster size, and at most one split per 256-column chunk) whose grid still
-// fits the GPU's CTA slots in one wave.
-// Depends only on the matrix shape and the GPU.
+// K-splits per row tile: the largest S (at most 8, the portable cluster
+// size, and at most one split per 256-column chunk) whose RB clusters of S
+// CTAs all run at once on this GPU (one wave), by the occupancy of clusters
+// of that size.  Depends only on the matrix shape and the GPU.
 int dense_splits(const verify_ctx* ctx, int RB, int KC) {
-  const int slots = ctx->dense_ctas_per_sm * ctx->num_sms;
-  int S = 1;  // powers of two pack into the GPCs without leaving a partial second wave
-  while (2 * S <= vk::kMaxSplits && 2 * S <= KC && RB * 2 * S <= slots) S *= 2;
+  int S = 1;
+  for (int s = 2; s <= vk::kMaxSplits && s <= KC; ++s)
+    if (RB <= ctx->dense_max_clusters[s]) S = s;
   return S;
 }
 
@@ -151,6 +152,7 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = cudaMalloc(&ctx->st_w, sizeof(float) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
   if ((e = cudaMemset(ctx->err, 0, sizeof(int)))) return bail(e);
   if ((e = vk::q4_setup_kernels(&ctx->dense_ctas_per_sm, &ctx->moe_ctas_per_sm))) return bail(e);
+  if ((e = vk::q4_dense_cluster_limits(ctx->dense_max_clusters))) return bail(e);
   if ((e = vk::gdn_setup_kernels())) return bail(e);
   if ((e = cudaDeviceSynchronize())) return bail(e);
   *out = ctx;
