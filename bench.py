@@ -231,7 +231,7 @@ def run_ours(args, cfg):
     vf = B.Verify(local)
     sh = shapes(cfg)
     L, H, T = cfg["layers"], sh["H"], sh["T"]
-    ds = DeviceStack(vf, cfg, seed=0)
+    ds = DeviceStack(vf, cfg, seed=0, n_slots=max(10, max(int(w) for w in args.widths.split(',') if w) + 1, args.k + 1))
     stream = torch.cuda.Stream()
     widths = sorted(set([int(w) for w in args.widths.split(",") if w] + [args.k]))
     hbm, peak_kind = peaks()
@@ -557,7 +557,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--k", type=int, default=9, help="verify width of the headline number")
-    ap.add_argument("--widths", default="1,4,8,9", help="widths also measured (reported under config.per_k)")
+    ap.add_argument("--widths", default="1,4,8,9,16", help="widths also measured (reported under config.per_k)")
     ap.add_argument("--layers", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernels", action="store_true",

@@ -68,7 +68,7 @@ def check_layers(vf, cfg, seed, k, layers, h_name):
     import torch
 
     sh = shapes(cfg)
-    ds = DeviceStack(vf, cfg, seed=seed, layers=layers)
+    ds = DeviceStack(vf, cfg, seed=seed, layers=layers, n_slots=max(10, k + 1))
     h = S.f32_normal(seed, h_name, (k, sh["H"])).astype(np.float64)
     compared = 0
     for l in range(layers):
@@ -113,7 +113,7 @@ def check_layers(vf, cfg, seed, k, layers, h_name):
     return compared
 
 
-@pytest.mark.parametrize("k", [1, 4, 9])
+@pytest.mark.parametrize("k", [1, 4, 9, 16])
 def test_small_stack_layers_match_oracle(vf, k):
     assert check_layers(vf, SMALL, 1, k, SMALL["layers"], f"stack.h{k}") > 0
 
@@ -125,13 +125,13 @@ def test_flash_next_stack_layers_match_oracle(vf):
     assert check_layers(vf, cfg, 0, 9, cfg["layers"], "stack.full.h") >= 9 * cfg["layers"] // 2
 
 
-def test_stack_rows_equal_single_row_steps(vf):
+@pytest.mark.parametrize("k", [9, 16])
+def test_stack_rows_equal_single_row_steps(vf, k):
     """Row r of a k-row verify through the whole stack is bit-identical to a
     1-row verify started from the states after r rows (every layer)."""
     import torch
 
-    k = 9
-    ds = DeviceStack(vf, SMALL, seed=2)
+    ds = DeviceStack(vf, SMALL, seed=2, n_slots=k + 1)
     h0 = S.f32_normal(2, "stack.rows", (k, SMALL["H"]))
     h = torch.from_numpy(h0.copy()).cuda()
     ds.verify(h, k)
