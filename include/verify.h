@@ -158,6 +158,15 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
 /* Number of kernels the library launched on this ctx since verify_init. */
 int64_t verify_launch_count(const verify_ctx* ctx);
 
+/* Test aid for failure detection: launches one kernel on `stream` whose two
+ * bounded waits are made to run out - a pipeline barrier that nothing arrives
+ * on and a counter that nothing increments - through the same wait code and
+ * limit (about 2 s at full clock) as the verify kernels.  The kernel then
+ * returns; it neither hangs nor faults.  Afterwards verify_device_status
+ * reports VERIFY_EDEVICE with code 1 (and clears it), and the context stays
+ * usable.  One kernel launch. */
+verify_status verify_selftest_stuck_wait(verify_ctx* ctx, struct CUstream_st* stream);
+
 /* ------------------------------------------------------------- q4_tile */
 
 /*

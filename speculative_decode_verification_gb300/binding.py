@@ -82,6 +82,7 @@ def load():
         "verify_last_error": [p],
         "verify_device_status": [p, p, C.POINTER(C.c_int32)],
         "verify_launch_count": [p],
+        "verify_selftest_stuck_wait": [p, p],
         "q4_qmv_k": [p, C.POINTER(Q4Weight), p, i, p, i, p],
         "q4_gather_experts_k": [p, C.POINTER(Q4Experts), C.POINTER(Q4Experts), p, i64, i, p, i, p, p, p, i,
                                 C.POINTER(Q4Weight), C.POINTER(Q4Weight), p, p],
@@ -165,6 +166,10 @@ class Verify:
 
     def launch_count(self) -> int:
         return int(self.lib.verify_launch_count(self.ctx))
+
+    def selftest_stuck_wait(self, stream=None):
+        """Launches the stuck-wait probe (verify_selftest_stuck_wait)."""
+        self._check(self.lib.verify_selftest_stuck_wait(self.ctx, self._stream(stream)))
 
     def device_status(self, stream=None):
         code = C.c_int32(0)

@@ -97,6 +97,9 @@ long long tiled_bytes(int N, int K, int E, bool gate_up);
 cudaError_t launch_tile(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases, uint8_t* dst, int N,
                         int K, int E, bool gate_up, cudaStream_t s);
 cudaError_t gdn_setup_kernels();
+// One kernel whose two bounded waits (a barrier and a counter that nothing
+// completes) run out and record VERIFY_DEV_ETIMEOUT in *err.
+cudaError_t launch_stuck_wait_probe(int* err, cudaStream_t s);
 cudaError_t launch_gdn(const GdnArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, int n, int k, void* out,
                            int dtype, bool pdl, cudaStream_t s);

@@ -198,6 +198,16 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
   return VERIFY_EDEVICE;
 }
 
+verify_status verify_selftest_stuck_wait(verify_ctx* ctx, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s = use_device(ctx);
+  if (s) return s;
+  cudaError_t e = vk::launch_stuck_wait_probe(ctx->err, stream);
+  if (e) return cuda_fail(ctx, e, "stuck-wait probe launch");
+  ctx->launches += 1;
+  return VERIFY_OK;
+}
+
 int64_t q4_tiled_bytes(int32_t n_out, int32_t k_in, int32_t n_experts, int32_t gate_up) {
   if (!valid_shape(n_out, k_in) || n_experts < 1 || (gate_up && n_out % 128 != 0)) return -1;
   return vk::tiled_bytes(n_out, k_in, n_experts, gate_up != 0);
