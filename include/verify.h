@@ -342,6 +342,11 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p,
  */
 verify_status gdn_commit(verify_gdn_state* st, int accepted);
 
+/* gdn_commit(&states[l], accepted) for l = 0 .. n_states - 1, all or nothing:
+ * every state is checked first (VERIFY_EINVAL, nothing changed, if any would
+ * be rejected).  Host-only. */
+verify_status gdn_commit_all(verify_gdn_state* states, int n_states, int accepted);
+
 /* --------------------------------------------------------- layer glue */
 
 /*
@@ -397,6 +402,17 @@ typedef struct {
 
 verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_state* st, float* h, int k,
                              int32_t* idx_out, struct CUstream_st* stream);
+
+/*
+ * A verify pass of k rows through n_layers layers in one call: verify_layer_k
+ * on (layers[l], states[l]) for l = 0 .. n_layers - 1, in order, on `stream`,
+ * h updated in place.  idx_out (optional, device int32) receives layer l's
+ * routed indices at idx_out + l * k * layers[l].top_k.  Returns the first
+ * failing layer's status; the layers before it have been enqueued and their
+ * states advanced.  8 * n_layers kernel launches, no host synchronisation.
+ */
+verify_status verify_stack_k(verify_ctx* ctx, const verify_layer* layers, verify_gdn_state* states, int n_layers,
+                             float* h, int k, int32_t* idx_out, struct CUstream_st* stream);
 
 /*
  * Profiling aid (no counterpart on the pages): while set, every

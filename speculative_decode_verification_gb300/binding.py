@@ -91,6 +91,8 @@ def load():
         "verify_rmsnorm_k": [p, p, p, f, i, i, i, p, i, p],
         "verify_synth_q4": [p, p, p, p, i64, i64, C.c_uint64, C.c_uint64, C.c_uint64, f, f, f, f, i, p],
         "verify_layer_k": [p, C.POINTER(Layer), C.POINTER(GdnState), p, i, p, p],
+        "verify_stack_k": [p, C.POINTER(Layer), C.POINTER(GdnState), i, p, i, p, p],
+        "gdn_commit_all": [C.POINTER(GdnState), i, i],
         "verify_set_layer_events": [p, C.POINTER(p), i],
         "q4_gather_experts_k_noalloc": [C.POINTER(Q4Experts), C.POINTER(Q4Experts), p, i64, i, p, i, p, p, p, i,
                                         C.POINTER(Q4Weight), C.POINTER(Q4Weight), p, p, p],
@@ -210,6 +212,17 @@ class Verify:
     def verify_layer_k(self, layer: Layer, state: GdnState, h, k: int, idx_out=None, stream=None):
         self._check(self.lib.verify_layer_k(self.ctx, C.byref(layer), C.byref(state), _ptr(h), k,
                                             _ptr(idx_out), self._stream(stream)))
+
+    def verify_stack_k(self, layers, states, h, k: int, idx_out=None, stream=None):
+        """One verify pass through every layer (verify_stack_k): layers and
+        states are ctypes arrays of Layer and GdnState."""
+        self._check(self.lib.verify_stack_k(self.ctx, layers, states, len(layers), _ptr(h), k,
+                                            _ptr(idx_out) if idx_out is not None else None, self._stream(stream)))
+
+    def gdn_commit_all(self, states, accepted: int):
+        st = self.lib.gdn_commit_all(states, len(states), accepted)
+        if st != OK:
+            raise VerifyError(st, f"gdn_commit_all({accepted}) rejected")
 
     def set_layer_events(self, events):
         """events: 8 torch.cuda.Event(enable_timing=True) (recorded once first) or None entries, or None."""

@@ -396,6 +396,17 @@ verify_status gdn_commit(verify_gdn_state* st, int accepted) {
   return VERIFY_OK;
 }
 
+verify_status gdn_commit_all(verify_gdn_state* states, int n_states, int accepted) {
+  if (!states || n_states < 1) return VERIFY_EINVAL;
+  for (int l = 0; l < n_states; ++l)
+    if (states[l].pending_k <= 0 || accepted < 0 || accepted > states[l].pending_k) return VERIFY_EINVAL;
+  for (int l = 0; l < n_states; ++l) {
+    states[l].cur = states[l].pending[accepted];
+    states[l].pending_k = 0;
+  }
+  return VERIFY_OK;
+}
+
 verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w, float eps, int zero_centered, int n,
                                int k, void* out, int dtype_out, struct CUstream_st* stream) {
   if (!ctx) return VERIFY_EINVAL;
@@ -481,6 +492,19 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
                                &L->shared_down, ctx->st_logits + E, sm)))
     return s;
   mark(7);
+  return VERIFY_OK;
+}
+
+verify_status verify_stack_k(verify_ctx* ctx, const verify_layer* layers, verify_gdn_state* states, int n_layers,
+                             float* h, int k, int32_t* idx_out, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  if (!layers || !states || n_layers < 1) return fail(ctx, VERIFY_EINVAL, "layers, states or n_layers invalid%s");
+  int32_t* idx = idx_out;
+  for (int l = 0; l < n_layers; ++l) {
+    verify_status s = verify_layer_k(ctx, &layers[l], &states[l], h, k, idx, stream);
+    if (s) return s;
+    if (idx) idx += (long long)k * layers[l].top_k;
+  }
   return VERIFY_OK;
 }
 

@@ -33,10 +33,12 @@ class DeviceStack:
     """All layers' weights and GDN state slots on the current CUDA device."""
 
     def __init__(self, vf: B.Verify, cfg, seed: int = 0, n_slots: int = 10, s_std: float = 0.02,
-                 tail_std: float = 1.0, layers: int | None = None, keep_rows: bool = False):
+                 tail_std: float = 1.0, layers: int | None = None, keep_rows: bool = False, graphs: bool = True):
         import torch
 
         self.vf, self.cfg, self.seed = vf, cfg, seed
+        self.use_graphs = graphs
+        self._graphs = {}
         self.n_layers = cfg["layers"] if layers is None else layers
         sh = shapes(cfg)
         self.sh = sh
@@ -44,8 +46,10 @@ class DeviceStack:
         d, Hk, Hv = cfg["d"], cfg["n_qk_heads"], cfg["n_v_heads"]
         self.keep = []
         self.rows = []  # with keep_rows: the row-layout (packed, scales, biases) of every Q4 tensor, in draw order
-        self.layers = []
-        self.states = []
+        # ctypes arrays, passed whole to verify_stack_k / gdn_commit_all; indexing
+        # gives views that write through (e.g. resetting one layer's cur)
+        self.layers = (B.Layer * self.n_layers)()
+        self.states = (B.GdnState * self.n_layers)()
         self.state_tensors = []
 
         def q4(name, n_out, k_in, n_experts=None, gate_up=False):
@@ -87,25 +91,57 @@ class DeviceStack:
             L.norm2_w = dev(S.f32_uniform(seed, nm["norm2"], (H,), -0.1, 0.1)).data_ptr()
             L.norm_eps = 1e-6
             L.top_k = sh["T"]
-            self.layers.append(L)
+            self.layers[l] = L
             S0, t0 = S.gdn_initial_state(seed, nm["gdn"], Hk, Hv, d, s_std=s_std, tail_std=tail_std)
             slots = [torch.zeros((Hv, d, d), dtype=torch.float32, device="cuda") for _ in range(n_slots)]
             tails = [torch.zeros((3, sh["C"]), dtype=torch.int16, device="cuda") for _ in range(n_slots)]
             slots[0].copy_(torch.from_numpy(S0))
             tails[0].copy_(torch.from_numpy(t0.view(np.int16)))
             self.state_tensors.append((slots, tails))
-            self.states.append(B.gdn_state(slots, tails, cur=0))
+            self.states[l] = B.gdn_state(slots, tails, cur=0)
 
     def verify(self, h, k: int, idx=None, stream=None):
         """One verify pass of k rows through every layer; h (fp32 [k, H]) is
         updated in place.  idx (optional): per-layer int32 [k, T] device
         tensors receiving the routed expert indices."""
+        if idx is None:
+            if self.use_graphs:
+                self._verify_graphed(h, k, stream)
+            else:  # one call for the whole pass
+                self.vf.verify_stack_k(self.layers, self.states, h, k, None, stream)
+            return
         for l, (L, st) in enumerate(zip(self.layers, self.states)):
-            self.vf.verify_layer_k(L, st, h, k, None if idx is None else idx[l], stream)
+            self.vf.verify_layer_k(L, st, h, k, idx[l], stream)
+
+    def _verify_graphed(self, h, k: int, stream=None):
+        """verify_stack_k through a CUDA graph: captured once per (k, h buffer,
+        every layer's current slot and pending count) and replayed after.  Which
+        slots a pass writes depends only on those, so a replay does what the
+        call would.  The capture runs the host side of the call (checks, slot
+        bookkeeping) without running kernels; its resulting states are restored
+        before every replay."""
+        import ctypes
+
+        import torch
+
+        key = (k, h.data_ptr(), tuple((int(st.cur), int(st.pending_k)) for st in self.states))
+        ent = self._graphs.get(key)
+        if ent is None:
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+                self.vf.verify_stack_k(self.layers, self.states, h, k, None, cap.cuda_stream)
+            ent = (g, bytes(self.states))
+            self._graphs[key] = ent
+        g, post = ent
+        ctypes.memmove(ctypes.addressof(self.states), post, len(post))
+        run = torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream()
+        with torch.cuda.stream(run):
+            g.replay()
 
     def commit(self, accepted: int):
-        for st in self.states:
-            self.vf.gdn_commit(st, accepted)
+        self.vf.gdn_commit_all(self.states, accepted)
 
     def weight_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.keep)
