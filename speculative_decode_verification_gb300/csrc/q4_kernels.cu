@@ -404,6 +404,21 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
   bool mine[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) mine[m] = S == 1 || ((warp * MT + m) % S) == split;
+  // y += result: the old values this CTA adds to, loaded now so that the
+  // loads overlap the cluster reduction
+  float old[MT][NT][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int row = tile * kBM + rbase[m] + g + 8 * (q >> 1);
+        const int col = 8 * t + 2 * c + (q & 1);
+        old[m][t][q] = (a.dtype == 2 && mine[m] && row < a.N && col < a.k)
+                           ? reinterpret_cast<const float*>(a.y)[(long long)col * a.N + row]
+                           : 0.f;
+      }
   if (S > 1) {
     // Stage 0 now holds this CTA's partial tile: once every consumer warp is
     // done with the last stage, which may itself be stage 0.
@@ -441,21 +456,6 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     cluster_arrive();  // this CTA has read its peers' partial tiles
   }
   if (!*abort) {
-    // y += result: every old value is loaded before the first store, so that
-    // the loads overlap instead of waiting behind the stores
-    float old[MT][NT][4];
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int row = tile * kBM + rbase[m] + g + 8 * (q >> 1);
-          const int col = 8 * t + 2 * c + (q & 1);
-          old[m][t][q] = (a.dtype == 2 && mine[m] && row < a.N && col < a.k)
-                             ? reinterpret_cast<const float*>(a.y)[(long long)col * a.N + row]
-                             : 0.f;
-        }
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -738,15 +738,20 @@ __device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, 
 // gate logit) x the shared expert's partial: one thread per output, every
 // partial loaded before the sum.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
+  // Before the dependency wait: the old residual (y += result) and the shared
+  // expert's gate logit, written at least two kernels earlier.
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = i < (long long)a.k * a.H;
+  const int r = live ? (int)(i / a.H) : 0, n = live ? (int)(i % a.H) : 0;
+  const float yo = live && a.dtype == 2 ? reinterpret_cast<const float*>(a.y)[(long long)r * a.H + n] : 0.f;
+  const float sg = live && a.has_shared ? __ldcg(a.shared_logit + (long long)r * a.logits_ld) : 0.f;
   griddep_wait();
   griddep_launch();
   if (blockIdx.x == 0) {  // the routed-expert kernel is done: reset its work counter and unit counts
     for (int i = threadIdx.x; i < kMoeUnits; i += blockDim.x) a.done[i] = 0;
     if (threadIdx.x == 0) *a.work = 0;
   }
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long long)a.k * a.H) return;
-  const int r = (int)(i / a.H), n = (int)(i % a.H);
+  if (!live) return;
   const int TS = a.T + a.has_shared;
   const float* pr = a.part + (long long)r * TS * a.H + n;
   float v[kMaxTopK], wj[kMaxTopK];
@@ -756,9 +761,6 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
     wj[j] = j < a.T ? __ldcg(a.w_out + r * a.T + j) : 0.f;
   }
   const float vs = a.has_shared ? __ldcg(pr + (long long)a.T * a.H) : 0.f;
-  const float sg = a.has_shared ? __ldcg(a.shared_logit + (long long)r * a.logits_ld) : 0.f;
-  // y += result: the old value is loaded with the partials
-  const float yo = a.dtype == 2 ? reinterpret_cast<const float*>(a.y)[(long long)r * a.H + n] : 0.f;
   float y = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j)
