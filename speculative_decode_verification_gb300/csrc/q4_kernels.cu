@@ -30,7 +30,7 @@
 //    CTAs of a tile form a thread block cluster and add their partial tiles
 //    through distributed shared memory in rank order (no global scratch, no
 //    atomics).
-//  * Routed MoE: three CTAs per SM, three stages of 8 activation rows.  One
+//  * Routed MoE: four CTAs per SM, two stages of 8 activation rows.  One
 //    kernel routes every row in every CTA, then works through items: first
 //    the gate/up items (expert, row chunk, 64 gate + 64 up rows; SwiGLU into
 //    the h rows), then the down items (expert, row chunk, 128 output rows;
