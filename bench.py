@@ -46,16 +46,16 @@ EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
 
 # DRAM traffic of the routed-expert kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum) of both layers of a 2-layer
-# stack at k = 9: 421.42 MB over two launches whose algorithmic bytes sum to
+# stack at k = 9: 421.35 MB over two launches whose algorithmic bytes sum to
 # 2 x 206226468.  Expert traffic grows with the distinct experts read, like the
 # algorithmic bytes, so a full launch's traffic is this ratio times its bytes.
 # The figure holds only for the kernel sources it was taken on; any change to
 # them reports null until the kernel is captured again.
-MOE_TRAFFIC_RATIO = 421.424896e6 / (2 * 206226468.0)
+MOE_TRAFFIC_RATIO = 421.352192e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
-    "q4_kernels.cu": "a3d7c5f3f092a2d893fd30cfbacd1ff2669331da9740658ae1f23e0356d4a60d",
+    "q4_kernels.cu": "57a118ba33e5126b1cdb1649197abaf82766f15181213a9caf04d8a7291091d9",
     "common.cuh": "42f3979950afca5ad7b600502ccd7937295ffb64a1af497afd0962771f07ea98",
-    "internal.h": "381069902166ee42ad382fd4bd6eaac23180a94e1aca3fd650ec65c477b02d89",
+    "internal.h": "1e523d20c52f700e7160133693d6b731c6f50ddce0a152587f30cc0f134010ea",
 }
 
 
