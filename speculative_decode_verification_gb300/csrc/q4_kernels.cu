@@ -154,7 +154,7 @@ __device__ __forceinline__ void producer_drain(uint32_t bar_base, long long fill
 // Accumulates group G of a stage into acc for this warp's MT row tiles: NT
 // MMA column blocks (activation rows 0 .. 8 NT - 1) of a stage laid out for
 // NBL activation rows.
-template <int NT, int MT, int NBL>
+template <int NT, int MT, int NBL, bool MMASUM = false>
 __device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, uint32_t sx_src, int G,
                                               const uint2 (&sw)[MT][2], const uint2 (&bw)[MT][2],
                                               const int (&rbase)[MT], int lane, float (&acc)[MT][NT][4]) {
@@ -171,9 +171,18 @@ __device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, ui
     const uint4 xb = lds128(rowa + (((2 * c + 1) ^ (b & 7)) << 4));
     bf[t][0] = xa.x; bf[t][1] = xa.y; bf[t][2] = xa.z; bf[t][3] = xa.w;
     bf[t][4] = xb.x; bf[t][5] = xb.y; bf[t][6] = xb.z; bf[t][7] = xb.w;
-    const uint2 s2 = lds64(sx_src + (G * L::NB + 8 * t + 2 * c) * 4);  // sums of columns 2c, 2c+1
-    sx[t][0] = __uint_as_float(s2.x);
-    sx[t][1] = __uint_as_float(s2.y);
+    if (MMASUM) {  // sums of activation rows 8t + 2c, 8t + 2c + 1: an MMA with A = 1
+      float cs[4] = {0.f, 0.f, 0.f, 0.f};
+      constexpr uint32_t ONE2 = 0x3F803F80u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_bf16_16816(cs, ONE2, ONE2, ONE2, ONE2, bf[t][2 * j], bf[t][2 * j + 1]);
+      sx[t][0] = cs[0];
+      sx[t][1] = cs[1];
+    } else {
+      const uint2 s2 = lds64(sx_src + (G * L::NB + 8 * t + 2 * c) * 4);  // sums of columns 2c, 2c+1
+      sx[t][0] = __uint_as_float(s2.x);
+      sx[t][1] = __uint_as_float(s2.y);
+    }
   }
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
@@ -231,8 +240,11 @@ __device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, ui
 
 // Accumulates one stage (gcount groups) for NT MMA column blocks; the stage
 // holds NBL activation rows (NBL >= 8 NT).  ok = false: the stage never filled
-// (abort) - keep the named-barrier count, skip the math.
-template <int NT, int CW, int NBL>
+// (abort) - keep the named-barrier count, skip the math.  The activation
+// group sums come either from consumer warp w < 4 adding up group w once per
+// stage (then a named barrier), or with MMASUM from one MMA with an all-ones
+// A operand in every warp, with no barrier (the routed-expert kernel).
+template <int NT, int CW, int NBL, bool MMASUM = false>
 __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t sx_src, int gcount,
                                               const int (&rbase)[Warps<CW>::MT], int lane,
                                               float (&acc)[Warps<CW>::MT][NT][4], bool ok) {
@@ -245,12 +257,12 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t
   const int g = lane >> 2, c = lane & 3;
   const int w = threadIdx.x >> 5;
   if (!ok) {
-    named_bar(2, CW * 32);
+    if (!MMASUM) named_bar(2, CW * 32);
     return;
   }
   // Consumer warp w < 4 adds up activation group w of the stage: each thread
   // its 16 values, then the four threads of a row.
-  if (w < gcount) {
+  if (!MMASUM && w < gcount) {
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int b = 8 * t + g;
@@ -277,14 +289,14 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t
       sw[m][h] = lds64(sb_src + row * 8);
       bw[m][h] = lds64(sb_src + kBM * 8 + row * 8);
     }
-  named_bar(2, CW * 32);
+  if (!MMASUM) named_bar(2, CW * 32);
   if (gcount == kGroupsPerUnit) {
 #pragma unroll
     for (int G = 0; G < kGroupsPerUnit; ++G)
-      consume_group<NT, MT, NBL>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
+      consume_group<NT, MT, NBL, MMASUM>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
   } else {
 #pragma unroll 1
-    for (int G = 0; G < gcount; ++G) consume_group<NT, MT, NBL>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
+    for (int G = 0; G < gcount; ++G) consume_group<NT, MT, NBL, MMASUM>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
   }
 }
 
@@ -692,7 +704,7 @@ __device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, 
     const uint32_t ph = (uint32_t)((fills / ST) & 1);
     const bool ok = mbar_wait(bar_base + 8 * s, ph, abort, a.err);
     const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
-    consume_stage<1, CW, L::NB>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
+    consume_stage<1, CW, L::NB, true>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
                                 lane, acc, ok);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_base + 8 * (ST + s));
