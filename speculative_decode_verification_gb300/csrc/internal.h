@@ -15,7 +15,7 @@ constexpr int kDenseWarps = 4;     // consumer warps of the dense kernel: two 16
 constexpr int kGateUpWarps = 4;    // fused gate/up: a gate tile and its up tile per warp
 constexpr int kDownWarps = 4;      // routed down projection: two 16-row MMA tiles each
 constexpr int kQ4CtasPerSm = 2;    // dense kernels
-constexpr int kMaxSplits = 8;       // K-splits of a dense row tile (one cluster; the portable cluster size)
+constexpr int kMaxSplits = 16;      // K-splits of a dense row tile (one cluster; 16 = largest non-portable size)
 constexpr int kMoeCtasPerSm = 4;   // routed-expert kernel: 8 activation rows per stage, two stages
 constexpr int kMoeStages = 2;
 constexpr int kMoeUnits = 2 * 512 + 2;  // work units of one call: (expert, chunk of 8 rows), at most

@@ -445,24 +445,27 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (!mine[m]) continue;  // warp-uniform
-      // all S ranks' four-float loads in flight at once, then the adds in rank order
-      float4 pv[kMaxSplits][NT];
+      // up to 8 ranks' four-float loads in flight at once, then their adds; in rank order
+      constexpr int QB = 8;
 #pragma unroll
-      for (int q = 0; q < kMaxSplits; ++q)
+      for (int t = 0; t < NT; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
+      for (int q0 = 0; q0 < S; q0 += QB) {
+        float4 pv[QB][NT];
+#pragma unroll
+        for (int q = 0; q < QB; ++q)
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            if (q0 + q < S) pv[q][t] = ld_dsmem_f32x4(part + ((warp * MT + m) * NT + t) * 32 + lane, (uint32_t)(q0 + q));
 #pragma unroll
         for (int t = 0; t < NT; ++t)
-          if (q < S) pv[q][t] = ld_dsmem_f32x4(part + ((warp * MT + m) * NT + t) * 32 + lane, (uint32_t)q);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxSplits; ++q)
-          if (q < S) {
-            acc[m][t][0] += pv[q][t].x;
-            acc[m][t][1] += pv[q][t].y;
-            acc[m][t][2] += pv[q][t].z;
-            acc[m][t][3] += pv[q][t].w;
-          }
+          for (int q = 0; q < QB; ++q)
+            if (q0 + q < S) {
+              acc[m][t][0] += pv[q][t].x;
+              acc[m][t][1] += pv[q][t].y;
+              acc[m][t][2] += pv[q][t].z;
+              acc[m][t][3] += pv[q][t].w;
+            }
       }
     }
     cluster_arrive();  // this CTA has read its peers' partial tiles
@@ -963,6 +966,9 @@ cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm) {
   *dense_ctas_per_sm = kQ4CtasPerSm;
   if ((e = setup_one(q4_dense_kernel<1>, TD, dense_smem<1>(), dense_ctas_per_sm))) return e;
   if ((e = setup_one(q4_dense_kernel<2>, TD, dense_smem<2>(), dense_ctas_per_sm))) return e;
+  // clusters of up to 16 CTAs (sizes above 8 are not portable)
+  if ((e = cudaFuncSetAttribute(q4_dense_kernel<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1))) return e;
+  if ((e = cudaFuncSetAttribute(q4_dense_kernel<2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1))) return e;
   *moe_ctas_per_sm = kMoeCtasPerSm;
   if ((e = setup_one(moe_kernel, TG, moe_smem<1>(), moe_ctas_per_sm))) return e;
   if (*dense_ctas_per_sm < 1 || *moe_ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -992,7 +998,12 @@ cudaError_t q4_dense_cluster_limits(int* max_clusters) {
       int n = 0;
       cudaError_t e = nt == 1 ? cudaOccupancyMaxActiveClusters(&n, q4_dense_kernel<1>, &cfg)
                               : cudaOccupancyMaxActiveClusters(&n, q4_dense_kernel<2>, &cfg);
-      if (e) return e;
+      if (e && S > 8) {  // a GPU without clusters this large: never chosen
+        (void)cudaGetLastError();
+        n = 0;
+      } else if (e) {
+        return e;
+      }
       best = n < best ? n : best;
     }
     max_clusters[S] = best;

@@ -106,10 +106,10 @@ long long rt_bytes(int k_in) {
   return (long long)vk::kTileSbBytes * KC + (long long)vk::kTileGroupBytes * KG;
 }
 
-// K-splits per row tile: the largest S (at most 8, the portable cluster
-// size, and at most one split per 256-column chunk) whose RB clusters of S
-// CTAs all run at once on this GPU (one wave), by the occupancy of clusters
-// of that size.  Depends only on the matrix shape and the GPU.
+// K-splits per row tile: the largest S (at most 16, the largest cluster,
+// and at most one split per 256-column chunk) whose RB clusters of S CTAs all
+// run at once on this GPU (one wave), by the occupancy of clusters of that
+// size.  Depends only on the matrix shape and the GPU.
 int dense_splits(const verify_ctx* ctx, int RB, int KC) {
   int S = 1;
   for (int s = 2; s <= vk::kMaxSplits && s <= KC; ++s)
