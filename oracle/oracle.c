@@ -18,7 +18,8 @@
  * invariants, not against this file): q4 nibble order and group indexing,
  * exact integer products, top-k order/ties and softmax identities, the
  * single-expert special case, the delta-rule identities (zero state, unit
- * gates, beta = 0, decay 1/2), conv taps, norms.
+ * gates, beta = 0, decay 1/2), conv taps, norms, greedy acceptance
+ * (hand-worked cases, numpy's argmax, the serial-decoding identity).
  */
 #include <math.h>
 #include <stdint.h>
@@ -350,5 +351,43 @@ int oracle_rmsnorm(const double* x, const float* w, double eps, int zero_centere
       out[(int64_t)r * n + c] = xr[c] * inv * wt;
     }
   }
+  return 0;
+}
+
+/* ------------------------------------------------------ greedy acceptance */
+
+/*
+ * Greedy acceptance of one verify block ([R] "What it is": the block runs the
+ * pending token and the drafts in one pass; "Acceptance": a draft stands when
+ * the token chosen from the previous row's logits equals it, and in greedy
+ * mode the output is token for token what serial decoding gives).
+ *
+ * Row 0 of the block is the pending token, rows 1..k-1 are the drafts
+ * d_1..d_{k-1}, given as draft[0..k-2].  Greedy choice of row r:
+ *   t_r = argmax_v logits[r][v]
+ * READING (the pages are silent): among equal maxima the lowest index wins;
+ * -0 and +0 are equal; a NaN ranks above every number (so the first NaN
+ * wins), which is numpy's argmax.  Then
+ *   m = number of leading drafts with d_{r+1} == t_r  (0 <= m <= k-1),
+ *   a = m + 1 rows stand (the pending token's row always does),
+ *   the next pending token is t_m.
+ * out: int32 [2 + k] = { a, t_m, t_0, ..., t_{k-1} }.
+ */
+int oracle_accept_greedy(const float* logits, int64_t ld, int V, int k, const int32_t* draft,
+                         int32_t* out) {
+  if (V < 1 || k < 1 || (k > 1 && !draft)) return 1;
+  for (int r = 0; r < k; ++r) {
+    const float* l = logits + (int64_t)r * ld;
+    int best = 0;
+    for (int v = 1; v < V; ++v) {
+      const int bn = isnan(l[best]), vn = isnan(l[v]);
+      if (!bn && (vn || l[v] > l[best])) best = v;
+    }
+    out[2 + r] = best;
+  }
+  int m = 0;
+  while (m < k - 1 && draft[m] == out[2 + m]) ++m;
+  out[0] = m + 1;
+  out[1] = out[2 + m];
   return 0;
 }

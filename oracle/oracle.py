@@ -46,10 +46,11 @@ def lib():
         L.oracle_gdn_verify.argtypes = [i, i, i, i, i, d, d, d, i, p, p, p, p, p, p,
                                         p, i64, p, i64, p, i64, p, i64, i, p, p, p, p]
         L.oracle_rmsnorm.argtypes = [p, p, d, i, i, i, p]
+        L.oracle_accept_greedy.argtypes = [p, i64, i, i, p, p]
         L.oracle_round_bf16.argtypes = [d]
         L.oracle_round_bf16.restype = C.c_uint16
         for f in ("oracle_q4_qmv", "oracle_route_topk", "oracle_gather_experts",
-                  "oracle_gdn_verify", "oracle_rmsnorm"):
+                  "oracle_gdn_verify", "oracle_rmsnorm", "oracle_accept_greedy"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -168,6 +169,21 @@ def rmsnorm(x, w, eps=1e-6, zero_centered=True):
     _check(lib().oracle_rmsnorm(_ptr(x), _ptr(w), float(eps), int(bool(zero_centered)), n, k, _ptr(out)),
            "oracle_rmsnorm")
     return out
+
+
+def accept_greedy(logits, draft):
+    """Greedy acceptance of a verify block: logits fp32 [k, V] (row 0 the
+    pending token's, rows 1..k-1 the drafts'), draft int32 [k-1].
+    Returns (a, next_token, t) with t the k greedy choices."""
+    logits = _c(np.atleast_2d(logits), np.float32)
+    k, V = logits.shape
+    draft = _c(np.asarray(draft).reshape(-1), np.int32)
+    if draft.size != k - 1:
+        raise ValueError("draft must hold k - 1 tokens")
+    out = np.zeros(2 + k, np.int32)
+    _check(lib().oracle_accept_greedy(_ptr(logits), V, V, k, _ptr(draft) if k > 1 else None, _ptr(out)),
+           "oracle_accept_greedy")
+    return int(out[0]), int(out[1]), out[2:].copy()
 
 
 def to_bf16(v) -> np.ndarray:
