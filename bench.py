@@ -54,8 +54,8 @@ EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
 MOE_TRAFFIC_RATIO = 423.830272e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
     "q4_kernels.cu": "fec6bb1e38dd162e2c457a22b389b21886b22895ea205503cf21fee6e0fa0bd0",
-    "common.cuh": "42f3979950afca5ad7b600502ccd7937295ffb64a1af497afd0962771f07ea98",
-    "internal.h": "a75b831d620009fcd85e155b83e3056940054bf5d893357dd20fcdd5469defc9",
+    "common.cuh": "249c762d042e43ac9c4c4d180b4ceee3ec2cba7f6f77f10aca9458f16499efa2",
+    "internal.h": "de05c6ac68a4402989803601246e06496a2f1014865c41001652f0c1d43ab657",
 }
 
 

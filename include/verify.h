@@ -13,13 +13,17 @@
  *   gdn_verify_k        k-row Gated DeltaNet step with per-row state snapshots
  *   gdn_commit          accepted-prefix rollback by slot (pointer) swap
  *   verify_rmsnorm_k    the layer glue norm used by a full verify layer
+ *   verify_accept_greedy greedy acceptance of the block on the device, fused
+ *                       with the commit of every GDN state (gdn_commit_dev:
+ *                       the same commit for any sampler's accepted count)
  *
  * Sources (pages, cited by title and section):
  *   [T]  "Flash-Next optimization transfer to Ornith and Qwen 27B":
  *        table "Shared architecture and implemented paths" and section
  *        "Exact verification kernels and benchmark admission".
  *   [R]  "Red Lite dev45 - speculative decoding with the Qwen3-Next MTP block":
- *        section "What it is" (2-row verify) and "Tried and kept or not".
+ *        sections "What it is" (2-row verify), "Acceptance" and "Tried and
+ *        kept or not".
  *   [F]  "QWEN38FLASH.md - Plan for supporting Qwen/Qwen3.8-Flash-Next":
  *        section 2.1 "Gated DeltaNet (GDN)", 2.3 "MoE", 2.4 (norm forms),
  *        3.1 (KDA -> GDN adaptations), 5.1 (GDN kernel list).
@@ -152,7 +156,9 @@ const char* verify_last_error(const verify_ctx* ctx);
 /* Synchronises `stream`, reads and clears the device error word.  Returns
  * VERIFY_OK if no kernel reported a problem since the last check, else
  * VERIFY_EDEVICE with *code (if non-NULL) set to the first error code:
- * 1 = pipeline wait timed out, 2 = expert index out of range. */
+ * 1 = pipeline wait timed out, 2 = expert index out of range, 3 = a device
+ * commit found no matching verify pending (nothing committed), 4 = a
+ * device-held committed slot outside 0 .. n_slots-1 (the verify wrote nothing). */
 verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, int32_t* code);
 
 /* Number of kernels the library launched on this ctx since verify_init. */
@@ -288,6 +294,16 @@ typedef struct {
  * pending_k == k; gdn_commit turns one of them into `cur`.
  * The caller fills S_slots/conv_slots/n_slots/cur once (n_slots >= k+1 for
  * every verify) and then only reads the struct.
+ *
+ * Device-held commit (dev != NULL, set by gdn_state_to_device): the committed
+ * slot lives in device memory, dev[0] = committed slot, dev[1] = rows of the
+ * verify still pending (0: none), so that an accept and commit on the device
+ * (verify_accept_greedy, gdn_commit_dev) need no host round trip and a
+ * captured CUDA graph of verify + accept stays valid from step to step.  The
+ * kernels then read and advance dev; the host fields cur, pending_k and
+ * pending are not used, and the host commits reject the state.  Slots are used
+ * in the same order as with a host-held commit: the state after the first r
+ * rows goes to slot r-1 + (r-1 >= cur), the r-th slot other than cur.
  */
 typedef struct {
   float* S_slots[VERIFY_GDN_MAX_SLOTS];
@@ -296,6 +312,7 @@ typedef struct {
   int32_t cur;
   int32_t pending_k;
   int32_t pending[VERIFY_GDN_MAX_SLOTS];
+  int32_t* dev; /* NULL, or device int32 [2] as above */
 } verify_gdn_state;
 
 /* Inputs of a width-k GDN call: bf16, row r of each at ptr + r*ld.  qkv has
@@ -325,6 +342,8 @@ typedef struct {
  * o : [k, n_v_heads*head_dim_v] fp32 or bf16 (VERIFY_F32 / VERIFY_BF16).
  * Requires n_slots >= k+1, all slot pointers 16-byte aligned.
  * A second verify without a commit in between starts again from `cur`.
+ * With a device-held commit (st->dev) the kernel takes cur from dev[0] when
+ * it runs, every one of the n_slots slots must be valid, and dev[1] becomes k.
  */
 verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p,
                            verify_gdn_state* st, const verify_gdn_inputs* in,
@@ -337,8 +356,8 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p,
  * Makes the state after the first `accepted` rows of the last verify current:
  * cur = pending[accepted]; accepted = 0 keeps the pre-verify state.
  * Host-only, O(1), touches no device memory and launches nothing.
- * Errors: VERIFY_EINVAL if nothing is pending (a second commit) or accepted
- * is outside 0..pending_k.
+ * Errors: VERIFY_EINVAL if nothing is pending (a second commit), accepted
+ * is outside 0..pending_k, or the state's commit is device-held.
  */
 verify_status gdn_commit(verify_gdn_state* st, int accepted);
 
@@ -346,6 +365,67 @@ verify_status gdn_commit(verify_gdn_state* st, int accepted);
  * every state is checked first (VERIFY_EINVAL, nothing changed, if any would
  * be rejected).  Host-only. */
 verify_status gdn_commit_all(verify_gdn_state* states, int n_states, int accepted);
+
+/* ------------------------------------------ acceptance and commit on device */
+
+/*
+ * Moves the committed slot of states[0 .. n_states-1] to the device: dev is
+ * caller-owned device memory of int32 [n_states][2]; states[l].dev becomes
+ * dev + 2*l, holding {states[l].cur, 0}.  A verify still pending on the host
+ * is dropped (as a second verify would drop it).  Copies on `stream` and
+ * synchronises it.  VERIFY_EINVAL: NULL or misaligned dev, a state already on
+ * the device, a cur outside 0 .. n_slots-1.
+ */
+verify_status gdn_state_to_device(verify_ctx* ctx, verify_gdn_state* states, int n_states, int32_t* dev,
+                                  struct CUstream_st* stream);
+
+/*
+ * Back to a host-held commit: synchronises `stream`, copies each dev[0] into
+ * cur, sets pending_k = 0 (a verify pending on the device is dropped) and
+ * dev = NULL.  VERIFY_EINVAL if a state is not on the device or holds an
+ * invalid slot (then nothing changes).
+ */
+verify_status gdn_state_to_host(verify_ctx* ctx, verify_gdn_state* states, int n_states,
+                                struct CUstream_st* stream);
+
+/*
+ * Rollback by slot swap on the device ([R] "What it is": a rejected draft is
+ * undone by swapping the DeltaNet state pointers with the snapshots), with the
+ * accepted row count read from device memory (*accepted, any sampler's):
+ * for every state, all or nothing, cur <- accepted == 0 ? cur
+ * : accepted-1 + (accepted-1 >= cur), and nothing is pending afterwards.  The
+ * states must have consecutive dev words (states[l].dev == states[0].dev + 2l,
+ * as gdn_state_to_device sets them).  Errors found on the host return
+ * VERIFY_EINVAL before the launch; on the device, a state with no verify
+ * pending or accepted outside 0 .. pending rows commits nothing and records
+ * device error 3.  One kernel launch.
+ */
+verify_status gdn_commit_dev(verify_ctx* ctx, const verify_gdn_state* states, int n_states,
+                             const int32_t* accepted, struct CUstream_st* stream);
+
+/*
+ * Greedy acceptance of a width-k verify block, fused with the commit
+ * ([R] "What it is": the pending token and the drafts run as the rows of one
+ * pass; "Acceptance": a draft stands when the token chosen from the previous
+ * row's logits equals it, so greedy verification gives serial decoding's
+ * tokens exactly).  Inputs:
+ *   logits : device fp32 [k, V], row r at logits + r*ld: the target's logits
+ *            after row r (row 0 the pending token, row r >= 1 draft d_r);
+ *   draft  : device int32 [k-1], draft[r-1] = d_r (may be NULL when k == 1).
+ * Computes t_r = argmax_v logits[r][v] (lowest index among equal maxima,
+ * -0 == +0, a NaN above every number: numpy's argmax), m = the number of
+ * leading drafts with d_{r+1} == t_r, and writes
+ *   result : device int32 [2 + k] = { a = m + 1, t_m, t_0, ..., t_{k-1} }
+ * (a rows stand; t_m is the next pending token).  If n_states > 0 it then
+ * commits a on every state as gdn_commit_dev does, which also requires each
+ * state's pending rows to equal k (else device error 3, nothing committed).
+ * Limits: 1 <= k <= 16, 1 <= V <= 2^30, ld >= V.  Rows that are 16-byte
+ * aligned (logits aligned, ld % 4 == 0) are read as float4.  One kernel
+ * launch; the ctx's scratch serialises calls on one ctx (one stream at a time).
+ */
+verify_status verify_accept_greedy(verify_ctx* ctx, const float* logits, int64_t ld, int V, int k,
+                                   const int32_t* draft, int32_t* result, const verify_gdn_state* states,
+                                   int n_states, struct CUstream_st* stream);
 
 /* --------------------------------------------------------- layer glue */
 

@@ -49,7 +49,7 @@ class GdnParams(C.Structure):
 class GdnState(C.Structure):
     _fields_ = [("S_slots", C.c_void_p * GDN_MAX_SLOTS), ("conv_slots", C.c_void_p * GDN_MAX_SLOTS),
                 ("n_slots", C.c_int32), ("cur", C.c_int32), ("pending_k", C.c_int32),
-                ("pending", C.c_int32 * GDN_MAX_SLOTS)]
+                ("pending", C.c_int32 * GDN_MAX_SLOTS), ("dev", C.c_void_p)]
 
 
 class GdnInputs(C.Structure):
@@ -94,6 +94,10 @@ def load():
         "verify_stack_k": [p, C.POINTER(Layer), C.POINTER(GdnState), i, p, i, p, p],
         "gdn_commit_all": [C.POINTER(GdnState), i, i],
         "verify_set_layer_events": [p, C.POINTER(p), i],
+        "gdn_state_to_device": [p, C.POINTER(GdnState), i, p, p],
+        "gdn_state_to_host": [p, C.POINTER(GdnState), i, p],
+        "gdn_commit_dev": [p, C.POINTER(GdnState), i, p, p],
+        "verify_accept_greedy": [p, p, i64, i, i, p, p, C.POINTER(GdnState), i, p],
         "q4_gather_experts_k_noalloc": [C.POINTER(Q4Experts), C.POINTER(Q4Experts), p, i64, i, p, i, p, p, p, i,
                                         C.POINTER(Q4Weight), C.POINTER(Q4Weight), p, p, p],
     }
@@ -223,6 +227,28 @@ class Verify:
         st = self.lib.gdn_commit_all(states, len(states), accepted)
         if st != OK:
             raise VerifyError(st, f"gdn_commit_all({accepted}) rejected")
+
+    def gdn_state_to_device(self, states, dev, stream=None):
+        """Moves the committed slot of every state (a ctypes array of GdnState)
+        to the device words dev (int32 [len(states), 2]); synchronises."""
+        self._check(self.lib.gdn_state_to_device(self.ctx, states, len(states), _ptr(dev), self._stream(stream)))
+
+    def gdn_state_to_host(self, states, stream=None):
+        self._check(self.lib.gdn_state_to_host(self.ctx, states, len(states), self._stream(stream)))
+
+    def gdn_commit_dev(self, states, accepted, stream=None):
+        """Commits the device-held int32 accepted (a 1-element tensor) on every state."""
+        self._check(self.lib.gdn_commit_dev(self.ctx, states, len(states), _ptr(accepted), self._stream(stream)))
+
+    def accept_greedy(self, logits, k: int, draft, result, states=None, stream=None):
+        """Greedy acceptance of a width-k block (verify_accept_greedy): logits
+        fp32 [k, V] (row stride logits.stride(0)), draft int32 [k-1], result
+        int32 [2 + k]; commits on the device-held states if given."""
+        n = 0 if states is None else len(states)
+        self._check(self.lib.verify_accept_greedy(
+            self.ctx, _ptr(logits), logits.stride(0), logits.shape[1], k,
+            _ptr(draft) if draft is not None and k > 1 else None, _ptr(result),
+            states if n else None, n, self._stream(stream)))
 
     def set_layer_events(self, events):
         """events: 8 torch.cuda.Event(enable_timing=True) (recorded once first) or None entries, or None."""

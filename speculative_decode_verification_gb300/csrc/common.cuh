@@ -14,6 +14,8 @@
 
 #define VERIFY_DEV_ETIMEOUT 1
 #define VERIFY_DEV_EINDEX 2
+#define VERIFY_DEV_ESEQUENCE 3  // device commit without a matching verify pending
+#define VERIFY_DEV_ESLOT 4      // device-held committed slot outside 0 .. n_slots-1
 
 namespace vk {
 

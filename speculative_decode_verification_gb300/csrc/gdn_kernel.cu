@@ -67,11 +67,26 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
   const int il = tid / TPR, l = tid % TPR;
   const int i = p * kGdnRows + il;  // value row within the head
 
+  // Committed slot.  A device-held one was written by a commit at least two
+  // launches before this one (the layer's first launch waits for all earlier
+  // work), so it may be read before the dependency wait.  Every CTA reads the
+  // same word; an invalid slot makes all of them leave before writing anything.
+  int cur = a.cur;
+  if (a.dev_state) {
+    cur = __ldcg(a.dev_state);
+    if (cur < 0 || cur >= a.n_slots) {
+      if (blockIdx.x == 0 && tid == 0) record_error(a.err, VERIFY_DEV_ESLOT);
+      return;
+    }
+  }
+  const float* S_in = a.S_slots[cur];
+  const uint16_t* tail_in = a.tail_slots[cur];
+
   // ---- before the grid dependency wait: the state slice and the conv
   //      weights and tail (parameters, or written by an earlier verify call)
   float s[4 * NV4];
   {
-    const float* src = a.S_in + ((long long)h * D + i) * D;
+    const float* src = S_in + ((long long)h * D + i) * D;
 #pragma unroll
     for (int m = 0; m < NV4; ++m) {
       const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * l + 4 * TPR * m));
@@ -96,7 +111,7 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
 #pragma unroll
     for (int t = 0; t < 4; ++t) cw[it][t] = cl < NCH ? a.conv_w[ch * 4 + t] : 0.f;
 #pragma unroll
-    for (int t = 0; t < 3; ++t) tl[it][t] = cl < NCH ? __ldcg(a.tail_in + t * C + ch) : (uint16_t)0;
+    for (int t = 0; t < 3; ++t) tl[it][t] = cl < NCH ? __ldcg(tail_in + t * C + ch) : (uint16_t)0;
   }
   // gated RMSNorm: output e = tid + NT h2 is (row e / 16, value row e % 16)
   constexpr int EPT = (kGdnMaxK * kGdnRows + NT - 1) / NT;  // outputs per thread
@@ -105,6 +120,7 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
   for (int h2 = 0; h2 < EPT; ++h2) nw[h2] = a.norm_w[p * kGdnRows + (tid + h2 * NT) % kGdnRows];
   griddep_wait();
   griddep_launch();
+  if (a.dev_state && blockIdx.x == 0 && tid == 0) a.dev_state[1] = k;
 
   // ---- 1. causal depthwise conv + SiLU; slide the window
   uint16_t xin[NIT][kGdnMaxK];
@@ -149,9 +165,10 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
       else vs[r][cl - 2 * D] = cv;
       w0 = w1; w1 = w2; w2 = xr;
       if (write_tail) {
-        a.tail_out[r][ch] = w0;
-        a.tail_out[r][C + ch] = w1;
-        a.tail_out[r][2 * C + ch] = w2;
+        uint16_t* to = a.tail_slots[r + (r >= cur)];
+        to[ch] = w0;
+        to[C + ch] = w1;
+        to[2 * C + ch] = w2;
       }
     }
   }
@@ -219,7 +236,7 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
     }
     const float delta = (vs[r][il] - mk) * beta;
     const float y = fmaf(delta, kq[r], mq);  // (S + delta k^T) q = S q + delta (k.q)
-    float* dst = a.S_out[r] + ((long long)h * D + i) * D;
+    float* dst = a.S_slots[r + (r >= cur)] + ((long long)h * D + i) * D;
 #pragma unroll
     for (int m = 0; m < NV4; ++m) {
       const float4 kv = *reinterpret_cast<const float4*>(&kn[r][4 * l + 4 * TPR * m]);

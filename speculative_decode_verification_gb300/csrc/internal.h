@@ -64,11 +64,17 @@ struct MoeArgs {
   int G;
 };
 
+// State slots: S_slots[s] fp32 [Hv, dv, dk], tail_slots[s] bf16 [W-1, C].  The
+// kernel reads slot cur and writes the state after row r to slot r + (r >= cur),
+// the r+1-th slot other than cur in ascending order.  cur is the argument, or,
+// with dev_state, dev_state[0] read when the kernel runs (written by a device
+// commit at least two launches earlier); the kernel then stores k in
+// dev_state[1] (the rows now pending).
 struct GdnArgs {
-  const float* S_in;          // [Hv, dv, dk]
-  const uint16_t* tail_in;    // [W-1, C]
-  float* S_out[17];           // slot receiving the state after row r (r < k)
-  uint16_t* tail_out[17];
+  float* S_slots[17];
+  uint16_t* tail_slots[17];
+  int n_slots, cur;
+  int* dev_state;
   const uint16_t* qkv; long long ld_qkv;
   const uint16_t* z;   long long ld_z;
   const uint16_t* a;   long long ld_a;
@@ -103,5 +109,29 @@ cudaError_t launch_stuck_wait_probe(int* err, cudaStream_t s);
 cudaError_t launch_gdn(const GdnArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, int n, int k, void* out,
                            int dtype, bool pdl, cudaStream_t s);
+
+// Greedy acceptance fused with the device commit (V > 0), or the device
+// commit alone of the accepted count *accepted (V == 0, one CTA).
+struct AcceptArgs {
+  const float* logits;        // [k, V], row r at logits + r * ld
+  long long ld;
+  int V, k;
+  int vec;                    // rows are 16-byte aligned: float4 loads
+  int blocks_per_row;
+  const int* draft;           // [k-1]
+  int* result;                // [2 + k]
+  const int* accepted;        // V == 0: the accepted row count
+  int* dev_state;             // [n_states][2] {committed slot, pending rows}
+  int n_states;
+  int need_k;                 // > 0: every state's pending rows must equal it
+  unsigned long long* best;   // scratch [kMaxAcceptK], zero between calls
+  unsigned int* ticket;       // scratch, zero between calls
+  int* err;
+};
+constexpr int kMaxAcceptK = 16;
+constexpr int kAcceptThreads = 256;
+// Grid of the acceptance kernel: CTAs per logits row.
+int accept_blocks_per_row(int V, int k, int num_sms);
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 
 }  // namespace vk

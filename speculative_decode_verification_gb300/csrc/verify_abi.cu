@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "verify.h"
@@ -24,6 +25,8 @@ struct verify_ctx {
   float* st_logits = nullptr;  // fp32 [16, 1024]
   int32_t* st_idx = nullptr;   // [16, 16]
   float* st_w = nullptr;       // [16, 16]
+  unsigned long long* acc_best = nullptr;  // greedy acceptance: per-row argmax keys, then the ticket
+  unsigned int* acc_ticket = nullptr;
   int64_t launches = 0;
   cudaEvent_t layer_events[8] = {};
   int n_layer_events = 0;
@@ -151,6 +154,9 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = cudaMalloc(&ctx->st_idx, sizeof(int32_t) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_w, sizeof(float) * VERIFY_MAX_K * vk::kMaxTopK))) return bail(e);
   if ((e = cudaMemset(ctx->err, 0, sizeof(int)))) return bail(e);
+  if ((e = cudaMalloc(&ctx->acc_best, sizeof(unsigned long long) * (vk::kMaxAcceptK + 1)))) return bail(e);
+  if ((e = cudaMemset(ctx->acc_best, 0, sizeof(unsigned long long) * (vk::kMaxAcceptK + 1)))) return bail(e);
+  ctx->acc_ticket = reinterpret_cast<unsigned int*>(ctx->acc_best + vk::kMaxAcceptK);
   if ((e = vk::q4_setup_kernels(&ctx->dense_ctas_per_sm, &ctx->moe_ctas_per_sm))) return bail(e);
   if ((e = vk::q4_dense_cluster_limits(ctx->dense_max_clusters))) return bail(e);
   if ((e = vk::gdn_setup_kernels())) return bail(e);
@@ -173,6 +179,7 @@ verify_status verify_destroy(verify_ctx* ctx) {
   cudaFree(ctx->st_logits);
   cudaFree(ctx->st_idx);
   cudaFree(ctx->st_w);
+  cudaFree(ctx->acc_best);
   delete ctx;
   return VERIFY_OK;
 }
@@ -193,6 +200,7 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
   if (h == 0) return VERIFY_OK;
   cudaMemset(ctx->err, 0, sizeof(int));
   cudaMemset(ctx->moe_sched, 0, (1 + vk::kMoeUnits) * sizeof(int));  // an aborted call may leave counts behind
+  cudaMemset(ctx->acc_best, 0, sizeof(unsigned long long) * (vk::kMaxAcceptK + 1));
   cudaDeviceSynchronize();
   snprintf(ctx->msg, sizeof ctx->msg, "device error code %d", h);
   return VERIFY_EDEVICE;
@@ -345,7 +353,8 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p, verify_g
   if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16) return fail(ctx, VERIFY_EINVAL, "dtype_out F32 or BF16%s");
   if (st->n_slots < k + 1 || st->n_slots > VERIFY_GDN_MAX_SLOTS)
     return fail(ctx, VERIFY_EINVAL, "n_slots must be in k+1..17%s");
-  if (st->cur < 0 || st->cur >= st->n_slots) return fail(ctx, VERIFY_EINVAL, "cur is not a slot%s");
+  if (!st->dev && (st->cur < 0 || st->cur >= st->n_slots)) return fail(ctx, VERIFY_EINVAL, "cur is not a slot%s");
+  if (st->dev && (s = check_dev(ctx, st->dev, 8, "state dev words"))) return s;
   const int d = p->head_dim_k, Hk = p->n_qk_heads, Hv = p->n_v_heads;
   const int C = 2 * Hk * d + Hv * d;
   if (in->ld_qkv < C || in->ld_z < (int64_t)Hv * d || in->ld_a < Hv || in->ld_b < Hv)
@@ -357,22 +366,30 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p, verify_g
       (s = check_dev(ctx, o, dtype_out == VERIFY_BF16 ? 2 : 4, "o")))
     return s;
 
+  // Slots in use: cur, then the state after row r in slot r + (r >= cur), the
+  // free slots in ascending order.  With a device-held commit cur is known only
+  // on the device, so every slot must be valid.
   int pending[VERIFY_GDN_MAX_SLOTS];
-  pending[0] = st->cur;
-  for (int sl = 0, r = 1; sl < st->n_slots && r <= k; ++sl)
-    if (sl != st->cur) pending[r++] = sl;
-  for (int r = 0; r <= k; ++r) {
-    if ((s = check_dev(ctx, st->S_slots[pending[r]], 16, "S slot"))) return s;
-    if ((s = check_dev(ctx, st->conv_slots[pending[r]], 2, "conv slot"))) return s;
+  const int n_used = st->dev ? st->n_slots : k + 1;
+  if (st->dev) {
+    for (int sl = 0; sl < n_used; ++sl) pending[sl] = sl;
+  } else {
+    pending[0] = st->cur;
+    for (int r = 0; r < k; ++r) pending[r + 1] = r + (r >= st->cur ? 1 : 0);
+  }
+  for (int u = 0; u < n_used; ++u) {
+    if ((s = check_dev(ctx, st->S_slots[pending[u]], 16, "S slot"))) return s;
+    if ((s = check_dev(ctx, st->conv_slots[pending[u]], 2, "conv slot"))) return s;
   }
 
   vk::GdnArgs a{};
-  a.S_in = st->S_slots[st->cur];
-  a.tail_in = st->conv_slots[st->cur];
-  for (int r = 0; r < k; ++r) {
-    a.S_out[r] = st->S_slots[pending[r + 1]];
-    a.tail_out[r] = st->conv_slots[pending[r + 1]];
+  for (int sl = 0; sl < st->n_slots; ++sl) {
+    a.S_slots[sl] = st->S_slots[sl];
+    a.tail_slots[sl] = st->conv_slots[sl];
   }
+  a.n_slots = st->n_slots;
+  a.cur = st->dev ? 0 : st->cur;
+  a.dev_state = st->dev;
   a.qkv = in->qkv; a.ld_qkv = in->ld_qkv; a.z = in->z; a.ld_z = in->ld_z;
   a.a = in->a; a.ld_a = in->ld_a; a.b = in->b; a.ld_b = in->ld_b;
   a.conv_w = p->conv_w; a.A_log = p->A_log; a.dt_bias = p->dt_bias; a.norm_w = p->norm_w;
@@ -382,13 +399,15 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p, verify_g
   cudaError_t e = vk::launch_gdn(a, ctx->pdl, stream);
   if (e) return cuda_fail(ctx, e, "gdn_verify_k launch");
   ctx->launches += 1;
-  for (int r = 0; r <= k; ++r) st->pending[r] = pending[r];
-  st->pending_k = k;
+  if (!st->dev) {
+    for (int r = 0; r <= k; ++r) st->pending[r] = pending[r];
+    st->pending_k = k;
+  }
   return VERIFY_OK;
 }
 
 verify_status gdn_commit(verify_gdn_state* st, int accepted) {
-  if (!st) return VERIFY_EINVAL;
+  if (!st || st->dev) return VERIFY_EINVAL;
   if (st->pending_k <= 0) return VERIFY_EINVAL;
   if (accepted < 0 || accepted > st->pending_k) return VERIFY_EINVAL;
   st->cur = st->pending[accepted];
@@ -399,11 +418,124 @@ verify_status gdn_commit(verify_gdn_state* st, int accepted) {
 verify_status gdn_commit_all(verify_gdn_state* states, int n_states, int accepted) {
   if (!states || n_states < 1) return VERIFY_EINVAL;
   for (int l = 0; l < n_states; ++l)
-    if (states[l].pending_k <= 0 || accepted < 0 || accepted > states[l].pending_k) return VERIFY_EINVAL;
+    if (states[l].dev || states[l].pending_k <= 0 || accepted < 0 || accepted > states[l].pending_k)
+      return VERIFY_EINVAL;
   for (int l = 0; l < n_states; ++l) {
     states[l].cur = states[l].pending[accepted];
     states[l].pending_k = 0;
   }
+  return VERIFY_OK;
+}
+
+// The dev words of states[0 .. n-1] are consecutive int32 pairs in device memory.
+static verify_status check_dev_states(verify_ctx* ctx, const verify_gdn_state* states, int n_states) {
+  if (!states || n_states < 1) return fail(ctx, VERIFY_EINVAL, "states is NULL or n_states < 1%s");
+  verify_status s;
+  if ((s = check_dev(ctx, states[0].dev, 8, "state dev words"))) return s;
+  for (int l = 1; l < n_states; ++l)
+    if (states[l].dev != states[0].dev + 2 * l)
+      return fail(ctx, VERIFY_EINVAL, "the states' dev words must be consecutive pairs%s");
+  return VERIFY_OK;
+}
+
+verify_status gdn_state_to_device(verify_ctx* ctx, verify_gdn_state* states, int n_states, int32_t* dev,
+                                  struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (!states || n_states < 1 || n_states > (1 << 20)) return fail(ctx, VERIFY_EINVAL, "states or n_states invalid%s");
+  if ((s = check_dev(ctx, dev, 8, "dev"))) return s;
+  std::vector<int32_t> words(2 * (size_t)n_states);
+  for (int l = 0; l < n_states; ++l) {
+    if (states[l].dev) return fail(ctx, VERIFY_EINVAL, "a state is already on the device%s");
+    if (states[l].n_slots < 2 || states[l].n_slots > VERIFY_GDN_MAX_SLOTS || states[l].cur < 0 ||
+        states[l].cur >= states[l].n_slots)
+      return fail(ctx, VERIFY_EINVAL, "a state's cur or n_slots is invalid%s");
+    words[2 * l] = states[l].cur;
+    words[2 * l + 1] = 0;
+  }
+  cudaError_t e = cudaMemcpyAsync(dev, words.data(), words.size() * sizeof(int32_t), cudaMemcpyHostToDevice, stream);
+  if (!e) e = cudaStreamSynchronize(stream);
+  if (e) return cuda_fail(ctx, e, "gdn_state_to_device copy");
+  for (int l = 0; l < n_states; ++l) {
+    states[l].dev = dev + 2 * l;
+    states[l].pending_k = 0;
+  }
+  return VERIFY_OK;
+}
+
+verify_status gdn_state_to_host(verify_ctx* ctx, verify_gdn_state* states, int n_states, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if ((s = check_dev_states(ctx, states, n_states))) return s;
+  std::vector<int32_t> words(2 * (size_t)n_states);
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (!e) e = cudaMemcpy(words.data(), states[0].dev, words.size() * sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e) return cuda_fail(ctx, e, "gdn_state_to_host copy");
+  for (int l = 0; l < n_states; ++l)
+    if (words[2 * l] < 0 || words[2 * l] >= states[l].n_slots)
+      return fail(ctx, VERIFY_EINVAL, "a device-held committed slot is invalid%s");
+  for (int l = 0; l < n_states; ++l) {
+    states[l].cur = words[2 * l];
+    states[l].pending_k = 0;
+    states[l].dev = nullptr;
+  }
+  return VERIFY_OK;
+}
+
+verify_status gdn_commit_dev(verify_ctx* ctx, const verify_gdn_state* states, int n_states, const int32_t* accepted,
+                             struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if ((s = check_dev_states(ctx, states, n_states))) return s;
+  if ((s = check_dev(ctx, accepted, 4, "accepted"))) return s;
+  vk::AcceptArgs a{};
+  a.V = 0;
+  a.k = 1;
+  a.accepted = accepted;
+  a.dev_state = states[0].dev;
+  a.n_states = n_states;
+  a.need_k = 0;
+  a.err = ctx->err;
+  cudaError_t e = vk::launch_accept(a, stream);
+  if (e) return cuda_fail(ctx, e, "gdn_commit_dev launch");
+  ctx->launches += 1;
+  return VERIFY_OK;
+}
+
+verify_status verify_accept_greedy(verify_ctx* ctx, const float* logits, int64_t ld, int V, int k,
+                                   const int32_t* draft, int32_t* result, const verify_gdn_state* states,
+                                   int n_states, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (k < 1 || k > vk::kMaxAcceptK) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if (V < 1 || V > (1 << 30)) return fail(ctx, VERIFY_EUNSUPPORTED, "V must be in 1..2^30%s");
+  if (ld < V) return fail(ctx, VERIFY_EINVAL, "ld must be >= V%s");
+  if ((s = check_dev(ctx, logits, 4, "logits")) || (s = check_dev(ctx, result, 4, "result"))) return s;
+  if (k > 1 && (s = check_dev(ctx, draft, 4, "draft"))) return s;
+  if (n_states < 0) return fail(ctx, VERIFY_EINVAL, "n_states < 0%s");
+  if (n_states > 0 && (s = check_dev_states(ctx, states, n_states))) return s;
+  vk::AcceptArgs a{};
+  a.logits = logits;
+  a.ld = ld;
+  a.V = V;
+  a.k = k;
+  a.vec = aligned(logits, 16) && ld % 4 == 0;
+  a.blocks_per_row = vk::accept_blocks_per_row(V, k, ctx->num_sms);
+  a.draft = draft;
+  a.result = result;
+  a.dev_state = n_states > 0 ? states[0].dev : nullptr;
+  a.n_states = n_states;
+  a.need_k = k;
+  a.best = ctx->acc_best;
+  a.ticket = ctx->acc_ticket;
+  a.err = ctx->err;
+  cudaError_t e = vk::launch_accept(a, stream);
+  if (e) return cuda_fail(ctx, e, "verify_accept_greedy launch");
+  ctx->launches += 1;
   return VERIFY_OK;
 }
 

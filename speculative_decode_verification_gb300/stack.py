@@ -2,7 +2,9 @@
 mixer -> MoE with 10 routed + 1 shared expert), random-init weights drawn by
 the seeded generator (large Q4 tensors by its device twin), one ring of GDN
 state slots per layer.  Running a verify pass is one ``verify_layer_k`` call
-per layer; committing the accepted prefix is one ``gdn_commit`` per layer.
+per layer; committing the accepted prefix is one ``gdn_commit`` per layer, or,
+with the committed slots held on the device (``to_device``), one acceptance
+kernel that also commits (``verify_accept``), with no host round trip.
 
 Tensor names (the seeds of the generator) are shared with the host side, so
 any weight can be re-drawn on the host bit for bit.
@@ -39,6 +41,7 @@ class DeviceStack:
         self.vf, self.cfg, self.seed = vf, cfg, seed
         self.use_graphs = graphs
         self._graphs = {}
+        self.dev_words = None  # int32 [layers, 2] once the committed slots live on the device
         self.n_layers = cfg["layers"] if layers is None else layers
         sh = shapes(cfg)
         self.sh = sh
@@ -124,24 +127,79 @@ class DeviceStack:
 
         import torch
 
-        key = (k, h.data_ptr(), tuple((int(st.cur), int(st.pending_k)) for st in self.states))
+        if self.dev_words is not None:  # the kernels read the committed slots themselves
+            key = (k, h.data_ptr(), "dev")
+        else:
+            key = (k, h.data_ptr(), tuple((int(st.cur), int(st.pending_k)) for st in self.states))
         ent = self._graphs.get(key)
         if ent is None:
-            g = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream()
-            cap.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
-                self.vf.verify_stack_k(self.layers, self.states, h, k, None, cap.cuda_stream)
-            ent = (g, bytes(self.states))
-            self._graphs[key] = ent
+            ent = self._capture(key, lambda st: self.vf.verify_stack_k(self.layers, self.states, h, k, None, st))
         g, post = ent
         ctypes.memmove(ctypes.addressof(self.states), post, len(post))
         run = torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream()
         with torch.cuda.stream(run):
             g.replay()
 
+    def _capture(self, key, enqueue):
+        import torch
+
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+            enqueue(cap.cuda_stream)
+        ent = (g, bytes(self.states))
+        self._graphs[key] = ent
+        return ent
+
     def commit(self, accepted: int):
         self.vf.gdn_commit_all(self.states, accepted)
+
+    # ------------------------------------------------ device-held commits
+
+    def to_device(self):
+        """Moves every layer's committed slot to the device: from here on the
+        verify kernels read it there and only device commits change it."""
+        import torch
+
+        words = torch.zeros((self.n_layers, 2), dtype=torch.int32, device="cuda")
+        self.vf.gdn_state_to_device(self.states, words)
+        self.dev_words = words
+        self._graphs.clear()
+
+    def to_host(self):
+        self.vf.gdn_state_to_host(self.states)
+        self.dev_words = None
+        self._graphs.clear()
+
+    def commit_dev(self, accepted, stream=None):
+        """Commits the device-held int32 count `accepted` on every layer."""
+        self.vf.gdn_commit_dev(self.states, accepted, stream)
+
+    def verify_accept(self, h, k: int, logits, draft, result, stream=None):
+        """A verify pass, then greedy acceptance of the block against `logits`
+        (fp32 [k, V], the target's logits of the k rows) and `draft` (int32
+        [k-1]) with the commit of every layer, all on the device: `result`
+        (int32 [2 + k]) receives the accepted rows, the next token and the k
+        greedy choices.  With graphs, one replay per call."""
+        import torch
+
+        if self.dev_words is None:
+            raise RuntimeError("verify_accept needs device-held commits: call to_device() first")
+
+        def enqueue(st):
+            self.vf.verify_stack_k(self.layers, self.states, h, k, None, st)
+            self.vf.accept_greedy(logits, k, draft, result, states=self.states, stream=st)
+
+        if not self.use_graphs:
+            enqueue(stream if stream else torch.cuda.current_stream().cuda_stream)
+            return
+        key = ("accept", k, h.data_ptr(), logits.data_ptr(), logits.stride(0), logits.shape[1],
+               None if draft is None else draft.data_ptr(), result.data_ptr())
+        g, _ = self._graphs.get(key) or self._capture(key, enqueue)
+        run = torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream()
+        with torch.cuda.stream(run):
+            g.replay()
 
     def weight_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.keep)

@@ -217,6 +217,19 @@ FLASH_GDN = dict(n_qk_heads=16, n_v_heads=48, d=128, conv_kernel=4)
 STACK = dict(layers=12, H=2560, E=512, T=10, I=640, n_qk_heads=16, n_v_heads=48, d=128,
              conv_kernel=4)
 
+# Flash-Next vocabulary (padded): the width of the target's logits per row.
+FLASH_VOCAB = 248_320
+
+
+def vocab_logits(seed: int, name: str, k: int, V: int, levels: int = 0) -> np.ndarray:
+    """Target logits fp32 [k, V] ~ N(0, 1); with levels > 0 rounded to
+    multiples of 1/levels, so that equal maxima occur."""
+    x = f32_normal(seed, name, (k, V))
+    if levels > 0:
+        x = (np.round(x.astype(np.float64) * levels) / levels).astype(np.float32)
+    return x
+
+
 # Tiny workload: one 512x512 projection and a 2/2-head, d=32 GDN step.
 TINY_Q4 = (512, 512)
 TINY_GDN = dict(n_qk_heads=2, n_v_heads=2, d=32, conv_kernel=4)

@@ -57,9 +57,31 @@ def run():
                     B.gdn_inputs(di["qkv"], di["z"], di["a"], di["b"]), k, o)
     vf.gdn_commit(st, 2)
     torch.cuda.synchronize()
-    oo, oS, _ = O.gdn_verify(Hk, Hv, d, p, S0.astype(np.float64), t0, inp, k)
+    oo, oS, ot = O.gdn_verify(Hk, Hv, d, p, S0.astype(np.float64), t0, inp, k)
     assert_close(host(o), oo, what="gdn_verify_k")
     assert_close(host(slots[st.cur]), oS[1], what="gdn_commit state")
+    # greedy acceptance on the device, fused with a device-held commit
+    arr = (B.GdnState * 1)()
+    arr[0] = st
+    words = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    vf.gdn_state_to_device(arr, words)
+    vf.gdn_verify_k(B.gdn_params(Hk, Hv, d, dp["conv_w"], dp["A_log"], dp["dt_bias"], dp["norm_w"]), arr[0],
+                    B.gdn_inputs(di["qkv"], di["z"], di["a"], di["b"]), k, o)
+    V = 3000
+    lx = S.vocab_logits(0, "smoke.logits", k, V, 4)
+    _, _, t = O.accept_greedy(lx, np.zeros(k - 1, np.int32))
+    draft = t[: k - 1].copy()
+    draft[2] = (t[2] + 1) % V  # two drafts stand
+    a, nxt, _ = O.accept_greedy(lx, draft)
+    res = torch.zeros(2 + k, dtype=torch.int32, device="cuda")
+    lxd, drd = dev(lx), dev(draft)
+    vf.accept_greedy(lxd, k, drd, res, states=arr)
+    torch.cuda.synchronize()
+    assert host(res).tolist() == [a, nxt] + t.tolist(), "verify_accept_greedy"
+    c = st.cur  # the slot the device verify started from
+    assert a == 3 and host(words).tolist() == [[2 + (2 >= c), 0]], "device commit"
+    _, oS2, _ = O.gdn_verify(Hk, Hv, d, p, oS[1], ot[1], inp, k)
+    assert_close(host(slots[2 + (2 >= c)]), oS2[2], what="device-committed state")
     status, code = vf.device_status()
     assert status == B.OK, f"device error word {code}"
     vf.close()
