@@ -377,6 +377,7 @@ def run_ours(args, cfg):
     launches_per_step = launches_per_pass  # the timed steps replay graphs of the same kernels
     e2e_s = max_over_ranks(float(np.median(e2e_t)), world)
     e2e_mean_s = max_over_ranks(float(np.mean(e2e_t)), world)
+    loop = device_loop(args, ds, vf, stream, k, H, world)
     if rank != 0:
         return 0
     cpu = None if args.no_cpu_baseline else cpu_baseline(cfg, k)
@@ -402,17 +403,97 @@ def run_ours(args, cfg):
                 "path": "DeviceStack.verify (one CUDA graph replay of verify_stack_k per state configuration)"},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
+        "device_loop": loop,
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
+def device_loop(args, ds, vf, stream, k, H, world):
+    """Decode steps with acceptance and commit on the device: per step the
+    host copies the k input rows in, one graph replay runs the verify pass and
+    verify_accept_greedy (greedy choice over a 248,320-entry vocabulary,
+    accepted prefix, commit of every layer's state), and the host reads back
+    the result (accepted rows, next token, the k choices).  The target logits
+    are synthetic and fixed: N(0, 1) with one planted winner per row (logit
+    100 at a seeded token), and the drafts follow the winners up to row
+    k // 2, so k // 2 + 1 rows stand every step and the next token is known by
+    construction.  The LM head that would produce the logits is not part of
+    the pass.  Reported beside the headline, not in it."""
+    import torch
+
+    from speculative_decode_verification_gb300 import synth as S
+
+    V = S.FLASH_VOCAB
+    x = S.vocab_logits(0, f"bench.loop.logits{k}", k, V, 0)
+    t = (S.uniform_f32(S.tensor_seed(0, f"bench.loop.winners{k}"), k, 0.0, 1.0) * V).astype(np.int64) % V
+    x[np.arange(k), t] = 100.0
+    m = min(k // 2, k - 1)
+    draft = t[: k - 1].astype(np.int32)
+    if m < k - 1:
+        draft[m] = (t[m] + 1) % V
+    a_want, next_want = m + 1, int(t[m])
+    logits = torch.from_numpy(x).cuda()
+    dd = torch.from_numpy(np.concatenate([draft, [0]]).astype(np.int32)).cuda()
+    res = torch.zeros(2 + k, dtype=torch.int32, device="cuda")
+    hh = torch.from_numpy(S.f32_normal(0, f"bench.h{k}", (k, H))).pin_memory()
+    rout = torch.empty(2 + k, dtype=torch.int32).pin_memory()
+    hd = torch.empty((k, H), dtype=torch.float32, device="cuda")
+    for st in ds.states:
+        st.cur, st.pending_k = 0, 0
+    ds.to_device()
+
+    def step():
+        with torch.cuda.stream(stream):
+            hd.copy_(hh, non_blocking=True)
+            ds.verify_accept(hd, k, logits, dd, res, stream.cuda_stream)
+            rout.copy_(res, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier(world)
+    ts = []
+    for _ in range(max(3, min(args.steps, 200))):
+        t0 = time.perf_counter()
+        step()
+        ts.append(time.perf_counter() - t0)
+        if int(rout[0]) != a_want or int(rout[1]) != next_want:
+            raise SystemExit(f"device acceptance gave {rout[:2].tolist()}, expected {[a_want, next_want]}")
+    # device-timed replays of the same graph (input rows refreshed on the device each step)
+    h0 = hd.clone()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_dev = max(3, min(args.steps, 500))
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(n_dev):
+            hd.copy_(h0)
+            ds.verify_accept(hd, k, logits, dd, res, stream.cuda_stream)
+        e1.record()
+    torch.cuda.synchronize()
+    dev_ms = e0.elapsed_time(e1) / n_dev
+    ds.to_host()
+    st, code = vf.device_status()
+    if st != 0:
+        raise SystemExit(f"device error {code} in the device loop")
+    host_s = max_over_ranks(float(np.median(ts)), world)
+    dev_ms = max_over_ranks(dev_ms, world)
+    L = ds.n_layers
+    return {"k": k, "V": V, "accepted_rows": a_want, "steps": len(ts),
+            "ms_per_step": host_s * 1e3, "verified_rows_per_s_per_layer": k * L / host_s * world,
+            "device_ms_per_step": dev_ms,
+            "h2d_bytes_per_step": k * H * 4, "d2h_bytes_per_step": (2 + k) * 4,
+            "statistic": "median of per-step host times; device time from CUDA events over back-to-back replays",
+            "path": "DeviceStack.verify_accept: one graph replay of verify_stack_k + verify_accept_greedy "
+                    "(device-held commits)"}
+
+
 def run_kernels(args):
     """Each hot-path kernel alone on its own configuration.  A timed batch is
-    R back-to-back calls between two CUDA events on the launching stream,
-    rotating over enough weight copies or input sets that a batch touches more
-    than 3 x L2, so no call finds its inputs in L2; per-call time = batch
-    time / R, median of --steps batches after --warmup.  One JSON line per
+    one replay of a CUDA graph of R back-to-back calls between two CUDA events
+    on the launching stream, rotating over enough weight copies or input sets
+    that a batch touches more than 3 x L2, so no call finds its inputs in L2;
+    per-call time = batch time / R, median of --steps batches after --warmup.  One JSON line per
     (kernel, config, k), then a summary line.  Not the bench contract line: a
     per-kernel roofline table."""
     import torch
@@ -446,18 +527,29 @@ def run_kernels(args):
         return t
 
     def time_calls(calls, R=40):
-        """calls: the rotation set (callables).  Median per-call microseconds."""
+        """calls: the rotation set (callables).  One CUDA graph holds R >= len(calls)
+        back-to-back calls cycling through the set (no host work between the
+        kernels); per-call time = replay time / R, median over replays."""
+        R = max(R, len(calls))
+        with torch.cuda.stream(stream):
+            for c in calls:  # first launches outside the capture
+                c()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(R):
+                calls[i % len(calls)]()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ts = []
         for it in range(args.warmup + args.steps):
             with torch.cuda.stream(stream):
                 e0.record()
-                for i in range(R):
-                    calls[(it * R + i) % len(calls)]()
+                g.replay()
                 e1.record()
             e1.synchronize()
             if it >= args.warmup:
                 ts.append(e0.elapsed_time(e1) * 1e3 / R)
+        del g
         return float(np.median(ts))
 
     lines = []
@@ -546,6 +638,27 @@ def run_kernels(args):
         us = time_calls(calls)
         nbytes = Hv * d * d * 4 * (1 + k) + 3 * C * 2 * (1 + k) + k * (C + Hv * d + 2 * Hv) * 2 + k * Hv * d * 4
         emit("gdn_verify_k", f"gdn Hk{Hk} Hv{Hv} d{d}", k, us, nbytes)
+    del rings
+    keep.clear()
+    torch.cuda.empty_cache()
+    # next row: greedy acceptance over the Flash-Next vocabulary (no states to
+    # commit); logits sets rotated over > 3 x L2
+    V = S.FLASH_VOCAB
+    for k in widths:
+        n_sets = int(np.ceil(3 * L2 / (k * V * 4))) + 1
+        base = torch.from_numpy(S.vocab_logits(0, f"kbench.accept.{k}", k, V, 0)).cuda()
+        sets = []
+        for r in range(n_sets):
+            lg = base.roll(r, dims=1).contiguous()  # same values, other positions
+            res = torch.zeros(2 + k, dtype=torch.int32, device="cuda")
+            sets.append((lg, res))
+        dft = torch.zeros(max(k - 1, 1), dtype=torch.int32, device="cuda")
+        us = time_calls([(lambda st=st, k=k: vf.accept_greedy(st[0], k, dft, st[1], stream=stream.cuda_stream))
+                         for st in sets])
+        emit("verify_accept_greedy", f"accept V{V}", k, us, k * V * 4 + 4 * (k - 1) + 4 * (k + 2),
+             {"sets": n_sets})
+        del sets, base
+        torch.cuda.empty_cache()
     print(json.dumps({"summary": "per-kernel roofline: back-to-back calls, weights or inputs rotated over > 3 x L2",
                       "n": len(lines), "peak": hbm, "peak_kind": peak_kind}), flush=True)
     return 0

@@ -136,22 +136,26 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptArgs
 
   // ---- last CTA: every other CTA's atomicMax happened before its ticket
   __threadfence();
-  __shared__ int t[kMaxAcceptK];
   __shared__ int acc_sh;
-  if (tid < p.k) {
-    const unsigned long long b = atomicExch(p.best + tid, 0ull);  // read and reset for the next call
-    t[tid] = (int)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+  if (w == 0) {  // lane r < k: row r's winner and draft d_{r+1}, then one ballot
+    int t = 0;
+    bool match = false;
+    if (lane < p.k) {
+      const int d = lane < p.k - 1 ? __ldcg(p.draft + lane) : 0;
+      const unsigned long long b = atomicExch(p.best + lane, 0ull);  // read and reset for the next call
+      t = (int)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+      match = lane < p.k - 1 && d == t;
+      p.result[2 + lane] = t;
+    }
+    const int m = __ffs(~__ballot_sync(0xffffffffu, match)) - 1;  // leading drafts that stand
+    const int tm = __shfl_sync(0xffffffffu, t, m);
+    if (lane == 0) {
+      p.result[0] = m + 1;
+      p.result[1] = tm;
+      acc_sh = m + 1;
+      *p.ticket = 0u;
+    }
   }
-  __syncthreads();
-  if (tid == 0) {
-    int m = 0;
-    while (m < p.k - 1 && __ldcg(p.draft + m) == t[m]) ++m;
-    p.result[0] = m + 1;
-    p.result[1] = t[m];
-    acc_sh = m + 1;
-    *p.ticket = 0u;
-  }
-  if (tid < p.k) p.result[2 + tid] = t[tid];
   __syncthreads();
   if (p.n_states > 0) commit_states(p, acc_sh);
 }
