@@ -231,7 +231,8 @@ def run_ours(args, cfg):
     vf = B.Verify(local)
     sh = shapes(cfg)
     L, H, T = cfg["layers"], sh["H"], sh["T"]
-    ds = DeviceStack(vf, cfg, seed=0, n_slots=max(10, max(int(w) for w in args.widths.split(',') if w) + 1, args.k + 1))
+    ds = DeviceStack(vf, cfg, seed=0, n_slots=max(10, max(int(w) for w in args.widths.split(',') if w) + 1, args.k + 1),
+                     vocab=S.FLASH_VOCAB)
     stream = torch.cuda.Stream()
     widths = sorted(set([int(w) for w in args.widths.split(",") if w] + [args.k]))
     hbm, peak_kind = peaks()
@@ -462,16 +463,45 @@ def device_loop(args, ds, vf, stream, k, H, world):
             raise SystemExit(f"device acceptance gave {rout[:2].tolist()}, expected {[a_want, next_want]}")
     # device-timed replays of the same graph (input rows refreshed on the device each step)
     h0 = hd.clone()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_dev = max(3, min(args.steps, 500))
-    with torch.cuda.stream(stream):
-        e0.record()
-        for _ in range(n_dev):
-            hd.copy_(h0)
-            ds.verify_accept(hd, k, logits, dd, res, stream.cuda_stream)
-        e1.record()
-    torch.cuda.synchronize()
-    dev_ms = e0.elapsed_time(e1) / n_dev
+
+    def device_ms(run):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(n_dev):
+                hd.copy_(h0)
+                run()
+            e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n_dev
+
+    dev_ms = device_ms(lambda: ds.verify_accept(hd, k, logits, dd, res, stream.cuda_stream))
+    # the same loop with the target head in the graph: final norm, the Q4 LM
+    # head over the full vocabulary (357.6 MB of weights), acceptance, commit
+    sel = None
+    if ds.vocab:
+        def step_sel():
+            with torch.cuda.stream(stream):
+                hd.copy_(hh, non_blocking=True)
+                ds.verify_select_accept(hd, k, dd, res, stream.cuda_stream)
+                rout.copy_(res, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(args.warmup):
+            step_sel()
+        ts_sel, acc = [], []
+        for _ in range(max(3, min(args.steps, 200))):
+            t0 = time.perf_counter()
+            step_sel()
+            ts_sel.append(time.perf_counter() - t0)
+            acc.append(int(rout[0]))
+        sel_dev = device_ms(lambda: ds.verify_select_accept(hd, k, dd, res, stream.cuda_stream))
+        sel_s = max_over_ranks(float(np.median(ts_sel)), world)
+        sel = {"ms_per_step": sel_s * 1e3, "device_ms_per_step": max_over_ranks(sel_dev, world),
+               "lm_head_bytes": int(0.5625 * V * H), "accepted_rows_mean": float(np.mean(acc)),
+               "path": "DeviceStack.verify_select_accept: verify_stack_k + final norm + q4_qmv_k LM head + "
+                       "verify_accept_greedy in one graph"}
     ds.to_host()
     st, code = vf.device_status()
     if st != 0:
@@ -485,7 +515,8 @@ def device_loop(args, ds, vf, stream, k, H, world):
             "h2d_bytes_per_step": k * H * 4, "d2h_bytes_per_step": (2 + k) * 4,
             "statistic": "median of per-step host times; device time from CUDA events over back-to-back replays",
             "path": "DeviceStack.verify_accept: one graph replay of verify_stack_k + verify_accept_greedy "
-                    "(device-held commits)"}
+                    "(device-held commits)",
+            "with_lm_head": sel}
 
 
 def run_kernels(args):
@@ -566,7 +597,7 @@ def run_kernels(args):
     widths = [int(w) for w in args.widths.split(",") if w]
     kmax = max(widths)
     # a1: dense Q4 products, the dense configuration's shapes; copies rotated
-    for (N, K) in S.DENSE_SHAPES:
+    for (N, K) in S.DENSE_SHAPES + [S.LM_HEAD]:
         wbytes = 0.5625 * N * K
         n_copies = int(np.ceil(3 * L2 / wbytes)) + 1
         Ws = [q4(f"kbench.dense.{N}x{K}.c{c}", N, K) for c in range(n_copies)]
@@ -576,7 +607,8 @@ def run_kernels(args):
         for k in widths:
             us = time_calls([(lambda W=W, k=k: vf.q4_qmv_k(W, x, k, y, B.F32, stream.cuda_stream)) for W in Ws])
             t1 = us if k == 1 else t1
-            emit("q4_qmv_k", f"dense {N}x{K}", k, us, wbytes + 2 * k * K + 4 * k * N,
+            emit("q4_qmv_k", f"dense {N}x{K}" + (" (LM head)" if (N, K) == S.LM_HEAD else ""), k, us,
+                 wbytes + 2 * k * K + 4 * k * N,
                  {"t_over_t1": round(us / t1, 3) if t1 else None, "copies": n_copies})
         del Ws
         keep.clear()

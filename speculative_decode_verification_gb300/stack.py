@@ -35,7 +35,8 @@ class DeviceStack:
     """All layers' weights and GDN state slots on the current CUDA device."""
 
     def __init__(self, vf: B.Verify, cfg, seed: int = 0, n_slots: int = 10, s_std: float = 0.02,
-                 tail_std: float = 1.0, layers: int | None = None, keep_rows: bool = False, graphs: bool = True):
+                 tail_std: float = 1.0, layers: int | None = None, keep_rows: bool = False, graphs: bool = True,
+                 vocab: int = 0):
         import torch
 
         self.vf, self.cfg, self.seed = vf, cfg, seed
@@ -102,6 +103,13 @@ class DeviceStack:
             tails[0].copy_(torch.from_numpy(t0.view(np.int16)))
             self.state_tensors.append((slots, tails))
             self.states[l] = B.gdn_state(slots, tails, cur=0)
+        # target head (vocab > 0): final zero-centred norm and a Q4 LM head [vocab, H]
+        self.vocab = vocab
+        if vocab:
+            self.final_norm_w = dev(S.f32_uniform(seed, "stack.final_norm", (H,), -0.1, 0.1))
+            self.lm_head = q4("stack.lm_head", vocab, H)
+            self.xn = torch.zeros((16, H), dtype=torch.int16, device="cuda")
+            self.logits = torch.zeros((16, vocab), dtype=torch.float32, device="cuda")
 
     def verify(self, h, k: int, idx=None, stream=None):
         """One verify pass of k rows through every layer; h (fp32 [k, H]) is
@@ -175,6 +183,44 @@ class DeviceStack:
     def commit_dev(self, accepted, stream=None):
         """Commits the device-held int32 count `accepted` on every layer."""
         self.vf.gdn_commit_dev(self.states, accepted, stream)
+
+    def select(self, h, k: int, stream=None):
+        """Target logits of the k rows of h: final norm (bf16 rows), then the Q4
+        LM head; returns the fp32 [k, vocab] view of the logits buffer."""
+        import torch
+
+        st = stream if stream else torch.cuda.current_stream().cuda_stream
+        H = self.sh["H"]
+        self.vf.verify_rmsnorm_k(h, self.final_norm_w, 1e-6, True, H, k, self.xn, B.BF16, st)
+        lg = self.logits[:k]
+        self.vf.q4_qmv_k(self.lm_head, self.xn, k, lg, B.F32, st)
+        return lg
+
+    def verify_select_accept(self, h, k: int, draft, result, stream=None):
+        """The whole target side of a decode step on the device: the verify
+        pass, the final norm and LM head over the full vocabulary, greedy
+        acceptance of `draft` (int32 [k-1]) and the commit of every layer.
+        `result` (int32 [2 + k]) receives the accepted rows, the next token and
+        the k greedy choices.  Needs vocab > 0 and device-held commits; with
+        graphs, one replay per call."""
+        import torch
+
+        if self.dev_words is None or not self.vocab:
+            raise RuntimeError("verify_select_accept needs vocab > 0 and to_device()")
+
+        def enqueue(st):
+            self.vf.verify_stack_k(self.layers, self.states, h, k, None, st)
+            lg = self.select(h, k, st)
+            self.vf.accept_greedy(lg, k, draft, result, states=self.states, stream=st)
+
+        if not self.use_graphs:
+            enqueue(stream if stream else torch.cuda.current_stream().cuda_stream)
+            return
+        key = ("select", k, h.data_ptr(), None if draft is None else draft.data_ptr(), result.data_ptr())
+        g, _ = self._graphs.get(key) or self._capture(key, enqueue)
+        run = torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream()
+        with torch.cuda.stream(run):
+            g.replay()
 
     def verify_accept(self, h, k: int, logits, draft, result, stream=None):
         """A verify pass, then greedy acceptance of the block against `logits`

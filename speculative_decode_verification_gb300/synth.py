@@ -217,8 +217,10 @@ FLASH_GDN = dict(n_qk_heads=16, n_v_heads=48, d=128, conv_kernel=4)
 STACK = dict(layers=12, H=2560, E=512, T=10, I=640, n_qk_heads=16, n_v_heads=48, d=128,
              conv_kernel=4)
 
-# Flash-Next vocabulary (padded): the width of the target's logits per row.
+# Flash-Next vocabulary (padded): the width of the target's logits per row,
+# and the Q4 LM head that makes them from the hidden-2560 rows (n_out, k_in).
 FLASH_VOCAB = 248_320
+LM_HEAD = (FLASH_VOCAB, 2560)
 
 
 def vocab_logits(seed: int, name: str, k: int, V: int, levels: int = 0) -> np.ndarray:

@@ -328,3 +328,100 @@ def test_stack_device_loop_equals_host_loop(vf, k):
     assert len(dev_st._graphs) == 1  # one capture served every step
     dev_st.to_host()
     assert [int(s.cur) for s in dev_st.states] == [int(s.cur) for s in host_st.states]
+
+
+# ------------------------------------------- token selection at the target
+
+@pytest.mark.parametrize("k", [1, 4, 9])
+def test_token_selection_over_a_q4_lm_head(vf, k):
+    """GPU token selection over the full vocabulary: the Q4 LM head
+    (q4_qmv_k at N = 248,320, hidden 256 here so that the oracle computes
+    every logit) and then greedy acceptance on the device.  The argmax is
+    decided on fp32 logits on both sides (the oracle's float64 sums rounded
+    to fp32); a row whose two largest oracle logits lie within twice the
+    product tolerance may resolve either way, and then the GPU's choice must
+    be one of the near-maximal tokens."""
+    import torch
+
+    from tests.gpu_util import DevQ4, assert_close
+
+    V, H = S.FLASH_VOCAB, 256
+    m = S.q4_matrix(7, "select.lm_head", V, H, centered=True)
+    W = DevQ4(vf, m)
+    x = S.bf16_normal(7, f"select.x{k}", (k, H))
+    y = torch.zeros((k, V), dtype=torch.float32, device="cuda")
+    vf.q4_qmv_k(W.struct, dev(x), k, y, B.F32)
+    ref = O.q4_qmv(m.packed, m.scales, m.biases, x)
+    torch.cuda.synchronize()
+    assert_close(host(y), ref, what="LM head logits")
+    ref32 = ref.astype(np.float32)
+    _, _, t_o = O.accept_greedy(ref32, np.zeros(k - 1, np.int32))
+    tol = 2e-3 * float(np.sqrt(np.mean(ref * ref)))
+    decisive = []
+    for r in range(k):
+        top2 = np.partition(ref[r], -2)[-2:]
+        decisive.append(top2[1] - top2[0] > tol)
+    assert sum(decisive) >= k - 1
+    n_lead = next((r for r, dcs in enumerate(decisive) if not dcs), k)  # rows decided without doubt
+    m_acc = max(0, min(n_lead - 1, k - 1))
+    draft = _drafts(t_o, m_acc, V, np.random.default_rng(k))
+    a, nxt, _ = O.accept_greedy(ref32, draft)
+    res = torch.zeros(2 + k, dtype=torch.int32, device="cuda")
+    vf.accept_greedy(y, k, dev(draft) if k > 1 else None, res)
+    torch.cuda.synchronize()
+    got = host(res)
+    for r in range(k):
+        if decisive[r]:
+            assert got[2 + r] == t_o[r], f"row {r}"
+        else:
+            assert ref[r, got[2 + r]] >= ref[r].max() - tol, f"row {r}: not a near-maximal token"
+    if all(decisive[: m_acc + 1]):
+        assert got[0] == a and got[1] == nxt
+
+
+def test_stack_select_accept_graph_equals_eager_composition(vf):
+    """The whole target side of a decode step as one graph replay (verify,
+    final norm, Q4 LM head over the full vocabulary, device acceptance and
+    commit) gives bit for bit what the same calls give launched one by one
+    with host commits, step after step."""
+    import torch
+
+    from speculative_decode_verification_gb300.stack import DeviceStack
+
+    cfg = dict(layers=2, H=256, E=16, T=4, I=256, n_qk_heads=2, n_v_heads=4, d=64, conv_kernel=4)
+    k, V = 5, S.FLASH_VOCAB
+    a_st = DeviceStack(vf, cfg, seed=9, n_slots=k + 1, vocab=V, graphs=False)
+    b_st = DeviceStack(vf, cfg, seed=9, n_slots=k + 1, vocab=V)
+    b_st.to_device()
+    h_a = torch.zeros((k, cfg["H"]), dtype=torch.float32, device="cuda")
+    h_b = torch.zeros_like(h_a)
+    draft = torch.zeros(k - 1, dtype=torch.int32, device="cuda")
+    res_a = torch.zeros(2 + k, dtype=torch.int32, device="cuda")
+    res_b = torch.zeros_like(res_a)
+    for step in range(4):
+        h0 = torch.from_numpy(S.f32_normal(9, f"select.h.{step}", (k, cfg["H"])))
+        h_a.copy_(h0)
+        h_b.copy_(h0)
+        # drafts: the eager side's own choices up to row `step`, so that the
+        # accepted count varies from step to step
+        a_st.verify(h_a, k)
+        lg = a_st.select(h_a, k)
+        vf.accept_greedy(lg, k, None if k == 1 else draft, res_a)
+        torch.cuda.synchronize()
+        t = host(res_a)[2:]
+        d = t[: k - 1].copy()
+        if step < k - 1:
+            d[step] = (t[step] + 1) % V
+        draft.copy_(torch.from_numpy(d))
+        vf.accept_greedy(lg, k, draft, res_a)
+        torch.cuda.synchronize()
+        a = int(host(res_a)[0])
+        assert a == min(step, k - 1) + 1
+        a_st.commit(a)
+        b_st.verify_select_accept(h_b, k, draft, res_b)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(h_a).view(np.uint32), host(h_b).view(np.uint32)), f"step {step}"
+        assert np.array_equal(host(res_a), host(res_b)), f"step {step}"
+        w = host(b_st.dev_words)
+        assert [int(x) for x in w[:, 0]] == [int(s.cur) for s in a_st.states]
+    assert len(b_st._graphs) == 1

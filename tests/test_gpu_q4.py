@@ -104,9 +104,10 @@ def test_bf16_and_accumulate_outputs(vf):
     assert np.array_equal(yadd, want.astype(np.float32))
 
 
-@pytest.mark.parametrize("N,K", S.DENSE_SHAPES)
+@pytest.mark.parametrize("N,K", S.DENSE_SHAPES + [S.LM_HEAD])
 def test_dense_full_size_sampled_rows(vf, N, K):
-    """The Qwen-27B-shaped projections at full size, weights drawn on the
+    """The Qwen-27B-shaped projections and the Flash-Next-shaped LM head
+    (248,320 x 2560, the full vocabulary) at full size, weights drawn on the
     device; the oracle recomputes 48 sampled output rows drawn on the host."""
     import torch
 
