@@ -391,3 +391,129 @@ int oracle_accept_greedy(const float* logits, int64_t ld, int V, int k, const in
   out[1] = out[2 + m];
   return 0;
 }
+
+/* ------------------------------------------------------- attention verify */
+
+/* IEEE binary16 bit pattern -> value (exact). */
+static double f16_value(uint16_t h) {
+  const int sign = h >> 15, ex = (h >> 10) & 31, frac = h & 1023;
+  double v;
+  if (ex == 0) v = ldexp((double)frac, -24);
+  else if (ex == 31) v = frac ? NAN : INFINITY;
+  else v = ldexp((double)(1024 + frac), ex - 25);
+  return sign ? -v : v;
+}
+
+/* value -> nearest binary16 (ties to even), rounded once from float64. */
+uint16_t oracle_round_f16(double v) {
+  if (isnan(v)) return 0x7E00;
+  const uint16_t sign = signbit(v) ? 0x8000 : 0;
+  const double a = fabs(v);
+  if (a == 0.0) return sign;
+  if (isinf(a) || a >= 65520.0) return sign | 0x7C00;  /* 65520: halfway past 65504 */
+  int ex;
+  frexp(a, &ex);
+  int E = ex - 1;                                       /* 2^E <= a < 2^(E+1) */
+  if (E < -14) return sign | (uint16_t)nearbyint(ldexp(a, 24));  /* subnormal, quantum 2^-24 */
+  double r = nearbyint(ldexp(a, 10 - E));               /* 1024 <= r <= 2048 */
+  if (r >= 2048.0) { r = 1024.0; ++E; }
+  if (E > 15) return sign | 0x7C00;
+  return sign | (uint16_t)(((E + 15) << 10) | ((int)r - 1024));
+}
+
+/*
+ * Rotary position embedding of one head vector at position pos, on its first
+ * rope_dim entries ([F] 2.2: partial RoPE, rope dim 64 of 256, theta 1e7).
+ * READING (the pages name only the dims and the base): the rotate-half
+ * pairing, entry i with entry i + rope_dim/2, at angle pos * theta^(-2i/rope_dim);
+ * entries from rope_dim on pass through.
+ */
+static void rope(const double* x, double* y, int D, int rope_dim, double theta, double pos) {
+  const int half = rope_dim / 2;
+  for (int i = 0; i < D; ++i) y[i] = x[i];
+  for (int i = 0; i < half; ++i) {
+    const double ang = pos * pow(theta, -2.0 * i / rope_dim);
+    const double c = cos(ang), s = sin(ang);
+    y[i] = x[i] * c - x[i + half] * s;
+    y[i + half] = x[i + half] * c + x[i] * s;
+  }
+}
+
+/*
+ * Width-k attention verify over a KV cache ([R] "What it is": attention runs
+ * per row, row r seeing the earlier rows' keys and values, and rejected rows
+ * are overwritten later; [T] "Exact verification kernels": each row keeps its
+ * serial KV window; [F] 2.2: grouped-query attention, 24 query and 2 KV heads
+ * of dim 256, partial RoPE, a sigmoid gate on the output, an F16 cache).
+ *
+ * Row r of the block is the token at absolute position P + r.  Its key and
+ * value (kn, vn) are appended to the cache: the key after RoPE at P + r, both
+ * rounded to binary16 (k_app, v_app).  Its query (after RoPE at P + r)
+ * attends to cache positions 0 .. P-1 and the block's rows 0 .. r, with score
+ * q.key / sqrt(D) and a softmax over that window; query head h reads KV head
+ * h / (Hq / Hkv) (READING: contiguous groups).  Output:
+ *   o[r][h][:] = (sum_j p_j value_j) * sigmoid(gate[r][h][:]).
+ * READING: the per-head query/key norms of the lineage are applied before
+ * this step (q and k arrive normalised); the sparse indexer of [F] 2.2 is not
+ * modelled: below its 2048-token budget QSA is dense attention, which this is.
+ *
+ * q, gate: bf16 [k, Hq, D]; kn, vn: bf16 [k, Hkv, D]; Kc, Vc: binary16
+ * [Hkv, cap, D] with positions 0 .. P-1 valid.  o: float64 [k, Hq, D];
+ * k_app, v_app: binary16 [k, Hkv, D].
+ */
+int oracle_attn_verify(int Hq, int Hkv, int D, int rope_dim, double theta, int P, int k, int64_t cap,
+                       const uint16_t* q, const uint16_t* kn, const uint16_t* vn, const uint16_t* gate,
+                       const uint16_t* Kc, const uint16_t* Vc, double* o, uint16_t* k_app,
+                       uint16_t* v_app) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv || D < 2 || rope_dim < 0 || rope_dim > D || rope_dim % 2 || P < 0 ||
+      k < 1 || (int64_t)P > cap)
+    return 1;
+  const int G = Hq / Hkv;
+  double* x = (double*)malloc(sizeof(double) * D);
+  double* y = (double*)malloc(sizeof(double) * D);
+  double* s = (double*)malloc(sizeof(double) * ((size_t)P + k));
+  double* acc = (double*)malloc(sizeof(double) * D);
+  if (!x || !y || !s || !acc) return 2;
+  /* the block's keys and values, as the cache holds them */
+  for (int r = 0; r < k; ++r)
+    for (int h = 0; h < Hkv; ++h) {
+      const int64_t off = ((int64_t)r * Hkv + h) * D;
+      for (int i = 0; i < D; ++i) x[i] = bf16_value(kn[off + i]);
+      rope(x, y, D, rope_dim, theta, (double)P + r);
+      for (int i = 0; i < D; ++i) {
+        k_app[off + i] = oracle_round_f16(y[i]);
+        v_app[off + i] = oracle_round_f16(bf16_value(vn[off + i]));
+      }
+    }
+  const double scale = 1.0 / sqrt((double)D);
+  for (int r = 0; r < k; ++r)
+    for (int h = 0; h < Hq; ++h) {
+      const int hk = h / G;
+      const int64_t qo = ((int64_t)r * Hq + h) * D;
+      for (int i = 0; i < D; ++i) x[i] = bf16_value(q[qo + i]);
+      rope(x, y, D, rope_dim, theta, (double)P + r);
+      const int n = P + r + 1;  /* the row's window */
+      double mx = -INFINITY;
+      for (int j = 0; j < n; ++j) {
+        const uint16_t* key = j < P ? Kc + ((int64_t)hk * cap + j) * D : k_app + ((int64_t)(j - P) * Hkv + hk) * D;
+        double dot = 0.0;
+        for (int i = 0; i < D; ++i) dot += y[i] * f16_value(key[i]);
+        s[j] = dot * scale;
+        if (s[j] > mx) mx = s[j];
+      }
+      double sum = 0.0;
+      for (int i = 0; i < D; ++i) acc[i] = 0.0;
+      for (int j = 0; j < n; ++j) {
+        const double p = exp(s[j] - mx);
+        sum += p;
+        const uint16_t* val = j < P ? Vc + ((int64_t)hk * cap + j) * D : v_app + ((int64_t)(j - P) * Hkv + hk) * D;
+        for (int i = 0; i < D; ++i) acc[i] += p * f16_value(val[i]);
+      }
+      for (int i = 0; i < D; ++i) o[qo + i] = acc[i] / sum * sigmoid(bf16_value(gate[qo + i]));
+    }
+  free(x);
+  free(y);
+  free(s);
+  free(acc);
+  return 0;
+}

@@ -47,10 +47,13 @@ def lib():
                                         p, i64, p, i64, p, i64, p, i64, i, p, p, p, p]
         L.oracle_rmsnorm.argtypes = [p, p, d, i, i, i, p]
         L.oracle_accept_greedy.argtypes = [p, i64, i, i, p, p]
+        L.oracle_attn_verify.argtypes = [i, i, i, i, d, i, i, i64, p, p, p, p, p, p, p, p, p]
+        L.oracle_round_f16.argtypes = [d]
+        L.oracle_round_f16.restype = C.c_uint16
         L.oracle_round_bf16.argtypes = [d]
         L.oracle_round_bf16.restype = C.c_uint16
         for f in ("oracle_q4_qmv", "oracle_route_topk", "oracle_gather_experts",
-                  "oracle_gdn_verify", "oracle_rmsnorm", "oracle_accept_greedy"):
+                  "oracle_gdn_verify", "oracle_rmsnorm", "oracle_accept_greedy", "oracle_attn_verify"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -184,6 +187,29 @@ def accept_greedy(logits, draft):
     _check(lib().oracle_accept_greedy(_ptr(logits), V, V, k, _ptr(draft) if k > 1 else None, _ptr(out)),
            "oracle_accept_greedy")
     return int(out[0]), int(out[1]), out[2:].copy()
+
+
+def round_f16(v: float) -> int:
+    return int(lib().oracle_round_f16(float(v)))
+
+
+def attn_verify(Hq, Hkv, D, P, q, kn, vn, gate, Kc, Vc, rope_dim=64, theta=1e7):
+    """Width-k attention verify over a binary16 KV cache.  q, gate: bf16 bits
+    [k, Hq, D]; kn, vn: bf16 bits [k, Hkv, D]; Kc, Vc: binary16 bits
+    [Hkv, cap, D] (positions 0..P-1 valid).  Returns o float64 [k, Hq, D] and
+    the appended rows k_app, v_app (binary16 bits [k, Hkv, D])."""
+    q, gate = _c(q, np.uint16), _c(gate, np.uint16)
+    kn, vn = _c(kn, np.uint16), _c(vn, np.uint16)
+    Kc, Vc = _c(Kc, np.uint16), _c(Vc, np.uint16)
+    k = q.shape[0]
+    cap = Kc.shape[1]
+    o = np.zeros((k, Hq, D), np.float64)
+    k_app = np.zeros((k, Hkv, D), np.uint16)
+    v_app = np.zeros((k, Hkv, D), np.uint16)
+    _check(lib().oracle_attn_verify(Hq, Hkv, D, rope_dim, float(theta), P, k, cap, _ptr(q), _ptr(kn), _ptr(vn),
+                                    _ptr(gate), _ptr(Kc), _ptr(Vc), _ptr(o), _ptr(k_app), _ptr(v_app)),
+           "oracle_attn_verify")
+    return o, k_app, v_app
 
 
 def to_bf16(v) -> np.ndarray:

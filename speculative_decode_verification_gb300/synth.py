@@ -196,6 +196,12 @@ def f32_normal(seed: int, name: str, shape, mean=0.0, std=1.0) -> np.ndarray:
     return normal_f32(tensor_seed(seed, name), n, mean, std).reshape(shape)
 
 
+def f16_normal(seed: int, name: str, shape, mean=0.0, std=1.0) -> np.ndarray:
+    """N(mean, std) rounded to IEEE binary16 (nearest-even), as bit patterns."""
+    n = int(np.prod(shape))
+    return normal_f32(tensor_seed(seed, name), n, mean, std).astype(np.float16).view(np.uint16).reshape(shape)
+
+
 def f32_uniform(seed: int, name: str, shape, lo, hi) -> np.ndarray:
     n = int(np.prod(shape))
     return uniform_f32(tensor_seed(seed, name), n, lo, hi).reshape(shape)
@@ -230,6 +236,30 @@ def vocab_logits(seed: int, name: str, k: int, V: int, levels: int = 0) -> np.nd
     if levels > 0:
         x = (np.round(x.astype(np.float64) * levels) / levels).astype(np.float32)
     return x
+
+
+# Flash-Next-shaped attention layer (QSA below its sparse budget = dense GQA):
+# 24 query heads, 2 KV heads, head dim 256, RoPE on the first 64 dims, base 1e7.
+FLASH_ATTN = dict(n_q_heads=24, n_kv_heads=2, d=256, rope_dim=64, theta=1e7)
+
+
+def attn_inputs(seed: int, prefix: str, k: int, Hq: int, Hkv: int, D: int):
+    """The block's query, gate, key and value rows (bf16 bits): q and k with
+    entries ~ N(0, 1) (unit-rms rows, as after the per-head norms), v and the
+    gate ~ N(0, 1)."""
+    return dict(q=bf16_normal(seed, prefix + ".q", (k, Hq, D)), gate=bf16_normal(seed, prefix + ".gate", (k, Hq, D)),
+                k=bf16_normal(seed, prefix + ".k", (k, Hkv, D)), v=bf16_normal(seed, prefix + ".v", (k, Hkv, D)))
+
+
+def attn_cache(seed: int, prefix: str, Hkv: int, cap: int, D: int, P: int):
+    """A KV cache of capacity cap with P valid positions (binary16 bits
+    [Hkv, cap, D], N(0, 1) keys and values; positions from P on zero)."""
+    K = np.zeros((Hkv, cap, D), np.uint16)
+    V = np.zeros((Hkv, cap, D), np.uint16)
+    if P:
+        K[:, :P] = f16_normal(seed, prefix + ".K", (Hkv, P, D))
+        V[:, :P] = f16_normal(seed, prefix + ".V", (Hkv, P, D))
+    return K, V
 
 
 # Tiny workload: one 512x512 projection and a 2/2-head, d=32 GDN step.
