@@ -13,6 +13,8 @@
  *   gdn_verify_k        k-row Gated DeltaNet step with per-row state snapshots
  *   gdn_commit          accepted-prefix rollback by slot (pointer) swap
  *   verify_rmsnorm_k    the layer glue norm used by a full verify layer
+ *   attn_verify_k       width-k grouped-query attention over an F16 KV cache
+ *                       (attn_commit: the cache's rollback)
  *   verify_accept_greedy greedy acceptance of the block on the device, fused
  *                       with the commit of every GDN state (gdn_commit_dev:
  *                       the same commit for any sampler's accepted count)
@@ -426,6 +428,86 @@ verify_status gdn_commit_dev(verify_ctx* ctx, const verify_gdn_state* states, in
 verify_status verify_accept_greedy(verify_ctx* ctx, const float* logits, int64_t ld, int V, int k,
                                    const int32_t* draft, int32_t* result, const verify_gdn_state* states,
                                    int n_states, struct CUstream_st* stream);
+
+/* ---------------------------------------------------- attention verify */
+
+/*
+ * Grouped-query attention of a verify layer ([F] 2.2: 24 query and 2 KV
+ * heads of dim 256, RoPE on the first 64 dims with base 1e7, a sigmoid gate on
+ * the output, an F16 KV cache; below its 2048-token sparse budget QSA is this
+ * dense attention).
+ */
+typedef struct {
+  int32_t n_q_heads, n_kv_heads; /* n_q_heads a multiple of n_kv_heads */
+  int32_t head_dim;              /* 128 or 256 */
+  int32_t rope_dim;              /* even, <= head_dim: the rotated leading dims */
+  float rope_theta;
+} verify_attn_params;
+
+/*
+ * KV cache of one attention layer, caller-allocated: K and V are binary16
+ * [n_kv_heads, capacity, head_dim]; positions 0 .. len-1 are committed.
+ * split (a multiple of 32, >= 32) fixes how the key positions are cut for
+ * the split-KV kernel: [s*split, (s+1)*split).  Results are bit-identical
+ * across widths (row r of a width-k call == a width-1 call at len + r) for
+ * one split value.  work: caller device memory of attn_workspace_bytes(...)
+ * bytes (partial results and the rotation table).  After attn_verify_k(k)
+ * the block's keys and values sit at len .. len+k-1 and pending_k == k;
+ * attn_commit(a) makes a of them committed (len += a); the others are
+ * overwritten by the next verify.
+ */
+typedef struct {
+  uint16_t* K;
+  uint16_t* V;
+  int64_t capacity;
+  int32_t len;
+  int32_t split;
+  int32_t pending_k;
+  void* work;
+  int64_t work_bytes;
+} verify_kv_cache;
+
+/* Inputs of a width-k attention call, bf16, row r at ptr + r*ld: q and gate
+ * [n_q_heads*head_dim] (head-major), k and v [n_kv_heads*head_dim]. */
+typedef struct {
+  const uint16_t* q;    int64_t ld_q;
+  const uint16_t* gate; int64_t ld_gate;
+  const uint16_t* k;    int64_t ld_k;
+  const uint16_t* v;    int64_t ld_v;
+} verify_attn_inputs;
+
+/* Workspace bytes attn_verify_k needs for a cache of `capacity` positions cut
+ * by `split`, for widths up to max_k (0 for bad arguments). */
+int64_t attn_workspace_bytes(const verify_attn_params* p, int64_t capacity, int32_t split, int32_t max_k);
+
+/*
+ * Width-k attention verify ([R] "What it is": attention runs per row, row r
+ * seeing the earlier rows' K/V; [T] "Exact verification kernels": each row's
+ * serial KV window).  Row r is the token at position P + r, P = cache->len:
+ *   key_r = rope(k[r], P + r) and v[r], rounded to binary16, are written to
+ *   the cache at position P + r (every KV head);
+ *   for query head h (KV head h / (n_q_heads / n_kv_heads)):
+ *     s_j = rope(q[r][h], P + r) . K[j] / sqrt(head_dim),  j = 0 .. P + r
+ *     o[r][h*head_dim + i] = (sum_j softmax(s)_j V[j][i]) * sigmoid(gate[r][h*head_dim + i])
+ * rope(x, pos) rotates the pair (x_i, x_{i+rope_dim/2}) by the angle
+ * pos * theta^(-2i/rope_dim) for i < rope_dim/2; other dims pass through.
+ * o: [k, n_q_heads*head_dim], VERIFY_F32 or VERIFY_BF16 (row stride
+ * n_q_heads*head_dim).  Three kernel launches (append, split partials,
+ * combine).  Limits: 1 <= k <= 16, k * n_q_heads / n_kv_heads <= 256,
+ * len + k <= capacity.  Arithmetic: rotation angles in float64, the
+ * rotation in fp32; q.K and p.V on the tensor cores with binary16 operands and
+ * fp32 sums, the scaled query and the probabilities each carried as a pair of
+ * binary16 values (hi + lo), so that the cache's binary16 values are the only
+ * rounding of note.
+ */
+verify_status attn_verify_k(verify_ctx* ctx, const verify_attn_params* p, verify_kv_cache* cache,
+                            const verify_attn_inputs* in, int k, void* o, int dtype_out,
+                            struct CUstream_st* stream);
+
+/* Rollback of the cache: len += accepted (0 .. pending_k), nothing pending
+ * afterwards.  Host-only.  VERIFY_EINVAL if nothing is pending or accepted is
+ * out of range. */
+verify_status attn_commit(verify_kv_cache* cache, int accepted);
 
 /* --------------------------------------------------------- layer glue */
 

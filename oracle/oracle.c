@@ -395,13 +395,25 @@ int oracle_accept_greedy(const float* logits, int64_t ld, int V, int k, const in
 /* ------------------------------------------------------- attention verify */
 
 /* IEEE binary16 bit pattern -> value (exact). */
-static double f16_value(uint16_t h) {
+static double f16_decode(uint16_t h) {
   const int sign = h >> 15, ex = (h >> 10) & 31, frac = h & 1023;
   double v;
   if (ex == 0) v = ldexp((double)frac, -24);
   else if (ex == 31) v = frac ? NAN : INFINITY;
   else v = ldexp((double)(1024 + frac), ex - 25);
   return sign ? -v : v;
+}
+
+/* The same through a table of all 65536 patterns (long caches decode each
+ * value many times). */
+static double f16_table[65536];
+static int f16_table_ready = 0;
+static double f16_value(uint16_t h) {
+  if (!f16_table_ready) {
+    for (int i = 0; i < 65536; ++i) f16_table[i] = f16_decode((uint16_t)i);
+    f16_table_ready = 1;
+  }
+  return f16_table[h];
 }
 
 /* value -> nearest binary16 (ties to even), rounded once from float64. */

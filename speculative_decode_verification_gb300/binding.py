@@ -57,6 +57,21 @@ class GdnInputs(C.Structure):
                 ("a", C.c_void_p), ("ld_a", C.c_int64), ("b", C.c_void_p), ("ld_b", C.c_int64)]
 
 
+class AttnParams(C.Structure):
+    _fields_ = [("n_q_heads", C.c_int32), ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("rope_dim", C.c_int32), ("rope_theta", C.c_float)]
+
+
+class KvCache(C.Structure):
+    _fields_ = [("K", C.c_void_p), ("V", C.c_void_p), ("capacity", C.c_int64), ("len", C.c_int32),
+                ("split", C.c_int32), ("pending_k", C.c_int32), ("work", C.c_void_p), ("work_bytes", C.c_int64)]
+
+
+class AttnInputs(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("ld_q", C.c_int64), ("gate", C.c_void_p), ("ld_gate", C.c_int64),
+                ("k", C.c_void_p), ("ld_k", C.c_int64), ("v", C.c_void_p), ("ld_v", C.c_int64)]
+
+
 class Layer(C.Structure):
     _fields_ = [("in_proj", Q4Weight), ("out_proj", Q4Weight), ("router", Q4Weight), ("gate_up", Q4Experts),
                 ("down", Q4Experts), ("shared_gate_up", Q4Weight), ("shared_down", Q4Weight),
@@ -94,6 +109,9 @@ def load():
         "verify_stack_k": [p, C.POINTER(Layer), C.POINTER(GdnState), i, p, i, p, p],
         "gdn_commit_all": [C.POINTER(GdnState), i, i],
         "verify_set_layer_events": [p, C.POINTER(p), i],
+        "attn_workspace_bytes": [C.POINTER(AttnParams), i64, C.c_int32, C.c_int32],
+        "attn_verify_k": [p, C.POINTER(AttnParams), C.POINTER(KvCache), C.POINTER(AttnInputs), i, p, i, p],
+        "attn_commit": [C.POINTER(KvCache), i],
         "gdn_state_to_device": [p, C.POINTER(GdnState), i, p, p],
         "gdn_state_to_host": [p, C.POINTER(GdnState), i, p],
         "gdn_commit_dev": [p, C.POINTER(GdnState), i, p, p],
@@ -108,6 +126,7 @@ def load():
     L.verify_last_error.restype = C.c_char_p
     L.verify_launch_count.restype = C.c_int64
     L.q4_tiled_bytes.restype = C.c_int64
+    L.attn_workspace_bytes.restype = C.c_int64
     _lib = L
     return L
 
@@ -228,6 +247,16 @@ class Verify:
         if st != OK:
             raise VerifyError(st, f"gdn_commit_all({accepted}) rejected")
 
+    def attn_verify_k(self, params: AttnParams, cache: KvCache, inputs: AttnInputs, k: int, o,
+                      dtype_out: int = F32, stream=None):
+        self._check(self.lib.attn_verify_k(self.ctx, C.byref(params), C.byref(cache), C.byref(inputs), k,
+                                           _ptr(o), dtype_out, self._stream(stream)))
+
+    def attn_commit(self, cache: KvCache, accepted: int):
+        st = self.lib.attn_commit(C.byref(cache), accepted)
+        if st != OK:
+            raise VerifyError(st, f"attn_commit({accepted}) rejected")
+
     def gdn_state_to_device(self, states, dev, stream=None):
         """Moves the committed slot of every state (a ctypes array of GdnState)
         to the device words dev (int32 [len(states), 2]); synchronises."""
@@ -298,6 +327,27 @@ def gdn_state(S_slots, conv_slots, cur=0) -> GdnState:
     st.cur = cur
     st.pending_k = 0
     return st
+
+
+def attn_params(Hq, Hkv, D, rope_dim=64, theta=1e7) -> AttnParams:
+    return AttnParams(Hq, Hkv, D, rope_dim, theta)
+
+
+def attn_workspace_bytes(params: AttnParams, capacity: int, split: int, max_k: int) -> int:
+    return int(load().attn_workspace_bytes(C.byref(params), capacity, split, max_k))
+
+
+def kv_cache(K, V, work, length=0, split=256) -> KvCache:
+    """K, V: int16 device tensors [Hkv, capacity, D] (binary16 bits); work: a
+    device buffer of attn_workspace_bytes(...) bytes."""
+    return KvCache(K.data_ptr(), V.data_ptr(), K.shape[1], length, split, 0, work.data_ptr(),
+                   work.numel() * work.element_size())
+
+
+def attn_inputs(q, gate, k, v) -> AttnInputs:
+    """Row-major [rows, heads * D] (or [rows, heads, D]) bf16 tensors."""
+    return AttnInputs(q.data_ptr(), q.stride(0), gate.data_ptr(), gate.stride(0), k.data_ptr(), k.stride(0),
+                      v.data_ptr(), v.stride(0))
 
 
 def gdn_inputs(qkv, z, a, b) -> GdnInputs:

@@ -110,6 +110,32 @@ cudaError_t launch_gdn(const GdnArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, int n, int k, void* out,
                            int dtype, bool pdl, cudaStream_t s);
 
+// Width-k grouped-query attention over a binary16 KV cache: append (the
+// block's rotated keys and values into the cache, the rotation table), split
+// partials (one CTA per (M group, key split, KV head)), combine.
+struct AttnArgs {
+  const uint16_t* q;    long long ld_q;
+  const uint16_t* gate; long long ld_gate;
+  const uint16_t* kin;  long long ld_k;
+  const uint16_t* vin;  long long ld_v;
+  uint16_t* K;          // [Hkv, cap, D]
+  uint16_t* V;
+  long long cap;
+  int Hq, Hkv, D, rope_dim;
+  float theta;
+  int P, k, split;
+  int nsplit;           // ceil((P + k) / split)
+  int n_mtiles;         // ceil(k * Hq / Hkv / 16): 16 (row, head) pairs per tile
+  float2* rot;          // [k][rope_dim / 2] (cos, sin) at positions P + r
+  float* part_o;        // [Hkv][nsplit][16 n_mtiles][D] unnormalised outputs
+  float2* part_ml;      // [Hkv][nsplit][16 n_mtiles] (running max, sum)
+  void* o;              // [k, Hq * D]
+  int dtype;
+};
+constexpr int kAttnMaxM = 256;   // k * (Hq / Hkv) per call
+cudaError_t attn_setup_kernels();
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s, int* launches);
+
 // Greedy acceptance fused with the device commit (V > 0), or the device
 // commit alone of the accepted count *accepted (V == 0, one CTA).
 struct AcceptArgs {

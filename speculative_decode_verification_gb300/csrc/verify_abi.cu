@@ -160,6 +160,7 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = vk::q4_setup_kernels(&ctx->dense_ctas_per_sm, &ctx->moe_ctas_per_sm))) return bail(e);
   if ((e = vk::q4_dense_cluster_limits(ctx->dense_max_clusters))) return bail(e);
   if ((e = vk::gdn_setup_kernels())) return bail(e);
+  if ((e = vk::attn_setup_kernels())) return bail(e);
   if ((e = cudaDeviceSynchronize())) return bail(e);
   *out = ctx;
   return VERIFY_OK;
@@ -536,6 +537,92 @@ verify_status verify_accept_greedy(verify_ctx* ctx, const float* logits, int64_t
   cudaError_t e = vk::launch_accept(a, stream);
   if (e) return cuda_fail(ctx, e, "verify_accept_greedy launch");
   ctx->launches += 1;
+  return VERIFY_OK;
+}
+
+// ------------------------------------------------------------ attention
+
+// Workspace of one attention call: the rotation table, then (max, sum) and the
+// unnormalised outputs of every (KV head, split, pair), each 256-byte aligned.
+struct AttnWork {
+  long long rot, ml, po, total;
+};
+static AttnWork attn_work(const verify_attn_params* p, long long nsplit, int k) {
+  auto up = [](long long b) { return (b + 255) / 256 * 256; };
+  const long long G = p->n_q_heads / p->n_kv_heads;
+  const long long Mpad = (k * G + 15) / 16 * 16;
+  AttnWork w;
+  w.rot = 0;
+  w.ml = up((long long)k * (p->rope_dim / 2) * 8);
+  w.po = w.ml + up(p->n_kv_heads * nsplit * Mpad * 8);
+  w.total = w.po + up(p->n_kv_heads * nsplit * Mpad * (long long)p->head_dim * 4);
+  return w;
+}
+
+static bool attn_params_ok(const verify_attn_params* p) {
+  return p && p->n_q_heads >= 1 && p->n_kv_heads >= 1 && p->n_q_heads % p->n_kv_heads == 0 &&
+         p->n_q_heads <= 1024 && (p->head_dim == 128 || p->head_dim == 256) && p->rope_dim >= 0 &&
+         p->rope_dim <= p->head_dim && p->rope_dim % 2 == 0 && p->rope_theta > 0.f;
+}
+
+int64_t attn_workspace_bytes(const verify_attn_params* p, int64_t capacity, int32_t split, int32_t max_k) {
+  if (!attn_params_ok(p) || capacity < 1 || split < 32 || split % 32 || max_k < 1 || max_k > VERIFY_MAX_K)
+    return 0;
+  return attn_work(p, (capacity + split - 1) / split, max_k).total;
+}
+
+verify_status attn_verify_k(verify_ctx* ctx, const verify_attn_params* p, verify_kv_cache* cache,
+                            const verify_attn_inputs* in, int k, void* o, int dtype_out, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (!p || !cache || !in) return fail(ctx, VERIFY_EINVAL, "params, cache or inputs is NULL%s");
+  if (!attn_params_ok(p))
+    return fail(ctx, VERIFY_EUNSUPPORTED, "attention: head_dim 128 or 256, n_q_heads a multiple of n_kv_heads, "
+                                          "even rope_dim <= head_dim%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  const int G = p->n_q_heads / p->n_kv_heads, D = p->head_dim;
+  if (k * G > vk::kAttnMaxM) return fail(ctx, VERIFY_EUNSUPPORTED, "k * n_q_heads / n_kv_heads must be <= 256%s");
+  if (cache->split < 32 || cache->split % 32) return fail(ctx, VERIFY_EINVAL, "split must be a multiple of 32%s");
+  if (cache->len < 0 || cache->capacity < 1 || (int64_t)cache->len + k > cache->capacity)
+    return fail(ctx, VERIFY_EINVAL, "len + k must be <= capacity%s");
+  const long long nsplit = ((long long)cache->len + k + cache->split - 1) / cache->split;
+  if (nsplit > 65535) return fail(ctx, VERIFY_EUNSUPPORTED, "more than 65535 key splits: use a larger split%s");
+  if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16) return fail(ctx, VERIFY_EINVAL, "dtype_out F32 or BF16%s");
+  if (in->ld_q < (int64_t)p->n_q_heads * D || in->ld_gate < (int64_t)p->n_q_heads * D ||
+      in->ld_k < (int64_t)p->n_kv_heads * D || in->ld_v < (int64_t)p->n_kv_heads * D)
+    return fail(ctx, VERIFY_EINVAL, "an input row stride is smaller than its row%s");
+  const AttnWork w = attn_work(p, nsplit, k);
+  if (cache->work_bytes < w.total) return fail(ctx, VERIFY_EINVAL, "cache workspace too small%s");
+  if ((s = check_dev(ctx, cache->K, 16, "K cache")) || (s = check_dev(ctx, cache->V, 16, "V cache")) ||
+      (s = check_dev(ctx, cache->work, 256, "workspace")) || (s = check_dev(ctx, in->q, 2, "q")) ||
+      (s = check_dev(ctx, in->gate, 2, "gate")) || (s = check_dev(ctx, in->k, 2, "k")) ||
+      (s = check_dev(ctx, in->v, 2, "v")) || (s = check_dev(ctx, o, dtype_out == VERIFY_BF16 ? 2 : 4, "o")))
+    return s;
+  vk::AttnArgs a{};
+  a.q = in->q; a.ld_q = in->ld_q; a.gate = in->gate; a.ld_gate = in->ld_gate;
+  a.kin = in->k; a.ld_k = in->ld_k; a.vin = in->v; a.ld_v = in->ld_v;
+  a.K = cache->K; a.V = cache->V; a.cap = cache->capacity;
+  a.Hq = p->n_q_heads; a.Hkv = p->n_kv_heads; a.D = D; a.rope_dim = p->rope_dim; a.theta = p->rope_theta;
+  a.P = cache->len; a.k = k; a.split = cache->split; a.nsplit = (int)nsplit;
+  a.n_mtiles = (k * G + 15) / 16;
+  char* base = static_cast<char*>(cache->work);
+  a.rot = reinterpret_cast<float2*>(base + w.rot);
+  a.part_ml = reinterpret_cast<float2*>(base + w.ml);
+  a.part_o = reinterpret_cast<float*>(base + w.po);
+  a.o = o; a.dtype = dtype_out == VERIFY_BF16 ? 1 : 0;
+  int launched = 0;
+  cudaError_t e = vk::launch_attn(a, stream, &launched);
+  ctx->launches += launched;
+  if (e) return cuda_fail(ctx, e, "attn_verify_k launch");
+  cache->pending_k = k;
+  return VERIFY_OK;
+}
+
+verify_status attn_commit(verify_kv_cache* cache, int accepted) {
+  if (!cache || cache->pending_k <= 0 || accepted < 0 || accepted > cache->pending_k) return VERIFY_EINVAL;
+  cache->len += accepted;
+  cache->pending_k = 0;
   return VERIFY_OK;
 }
 

@@ -253,12 +253,19 @@ def attn_inputs(seed: int, prefix: str, k: int, Hq: int, Hkv: int, D: int):
 
 def attn_cache(seed: int, prefix: str, Hkv: int, cap: int, D: int, P: int):
     """A KV cache of capacity cap with P valid positions (binary16 bits
-    [Hkv, cap, D], N(0, 1) keys and values; positions from P on zero)."""
+    [Hkv, cap, D], N(0, 1) keys and values; positions from P on zero).  Long
+    caches are drawn from numpy's PCG64 stream seeded by the tensor name (the
+    SplitMix64 Box-Muller stream is too slow for 10^8 values on the host)."""
     K = np.zeros((Hkv, cap, D), np.uint16)
     V = np.zeros((Hkv, cap, D), np.uint16)
     if P:
-        K[:, :P] = f16_normal(seed, prefix + ".K", (Hkv, P, D))
-        V[:, :P] = f16_normal(seed, prefix + ".V", (Hkv, P, D))
+        if Hkv * P * D <= 1 << 20:
+            K[:, :P] = f16_normal(seed, prefix + ".K", (Hkv, P, D))
+            V[:, :P] = f16_normal(seed, prefix + ".V", (Hkv, P, D))
+        else:
+            for X, nm in ((K, ".K"), (V, ".V")):
+                rng = np.random.default_rng(tensor_seed(seed, prefix + nm))
+                X[:, :P] = rng.standard_normal((Hkv, P, D), dtype=np.float32).astype(np.float16).view(np.uint16)
     return K, V
 
 

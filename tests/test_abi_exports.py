@@ -62,3 +62,21 @@ def test_commit_bookkeeping_on_host(lib):
 def test_null_context_is_rejected(lib):
     assert lib.q4_qmv_k(None, None, None, 1, None, 0, None) == 1
     assert lib.verify_last_error(None) == b"null context"
+
+
+def test_attention_cache_bookkeeping_on_host(lib):
+    from speculative_decode_verification_gb300 import binding as B
+
+    c = B.KvCache()
+    c.capacity, c.len, c.split, c.pending_k = 100, 10, 32, 0
+    assert lib.attn_commit(C.byref(c), 0) == B.EINVAL  # nothing pending
+    c.pending_k = 4
+    assert lib.attn_commit(C.byref(c), 5) == B.EINVAL
+    assert lib.attn_commit(C.byref(c), 3) == B.OK
+    assert c.len == 13 and c.pending_k == 0
+    p = B.attn_params(24, 2, 256)
+    # rotation table, then (max, sum) and outputs of 2 heads x 4 splits x 16 pairs
+    want = 256 + 2 * 4 * 16 * 8 + 2 * 4 * 16 * 256 * 4
+    assert B.attn_workspace_bytes(p, 1024, 256, 1) == want
+    assert B.attn_workspace_bytes(p, 1024, 250, 1) == 0  # split not a multiple of 32
+    assert B.attn_workspace_bytes(B.attn_params(24, 5, 256), 1024, 256, 1) == 0
