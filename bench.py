@@ -596,8 +596,13 @@ def run_kernels(args):
 
     widths = [int(w) for w in args.widths.split(",") if w]
     kmax = max(widths)
-    # a1: dense Q4 products, the dense configuration's shapes; copies rotated
-    for (N, K) in S.DENSE_SHAPES + [S.LM_HEAD]:
+    only = set(args.only.split(",")) if args.only else None
+
+    def want(name):
+        return only is None or name in only
+
+    # a1: dense Q4 products, the dense configuration's shapes and the LM head; copies rotated
+    for (N, K) in [sh for sh in S.DENSE_SHAPES if want("dense")] + ([S.LM_HEAD] if want("lm_head") else []):
         wbytes = 0.5625 * N * K
         n_copies = int(np.ceil(3 * L2 / wbytes)) + 1
         Ws = [q4(f"kbench.dense.{N}x{K}.c{c}", N, K) for c in range(n_copies)]
@@ -617,9 +622,9 @@ def run_kernels(args):
     # the expert weights (453 MB) exceed 3 x L2; 8 input sets rotated
     m = S.ORNITH_MOE
     E, T, H, I = m["E"], m["T"], m["H"], m["I"]
-    gu = q4("kbench.moe.gu", 2 * I, H, E, gate_up=True)
-    dn = q4("kbench.moe.dn", H, I, E)
-    for k in widths:
+    gu = q4("kbench.moe.gu", 2 * I, H, E, gate_up=True) if want("experts") else None
+    dn = q4("kbench.moe.dn", H, I, E) if want("experts") else None
+    for k in (widths if want("experts") else []):
         sets = []
         for r in range(8):
             logits = dev(S.f32_normal(0, f"kbench.moe.l{k}.{r}", (k, E)))
@@ -647,14 +652,14 @@ def run_kernels(args):
     params = B.gdn_params(Hk, Hv, d, gp["conv_w"], gp["A_log"], gp["dt_bias"], gp["norm_w"])
     S0, t0 = S.gdn_initial_state(0, "kbench.gdn", Hk, Hv, d, s_std=0.02, tail_std=1.0)
     rings = []
-    for r in range(8):
+    for r in range(8 if want("gdn") else 0):
         slots = [dev(S0) if s == 0 else torch.zeros((Hv, d, d), dtype=torch.float32, device="cuda")
                  for s in range(kmax + 1)]
         tails = [dev(t0.view(np.int16)) if s == 0 else torch.zeros((3, C), dtype=torch.int16, device="cuda")
                  for s in range(kmax + 1)]
         keep.extend(slots + tails)
         rings.append((slots, tails))
-    for k in widths:
+    for k in (widths if want("gdn") else []):
         calls = []
         for r, (slots, tails) in enumerate(rings):
             inp = {key: dev(v.view(np.int16) if v.dtype == np.uint16 else v)
@@ -676,7 +681,7 @@ def run_kernels(args):
     # next row: greedy acceptance over the Flash-Next vocabulary (no states to
     # commit); logits sets rotated over > 3 x L2
     V = S.FLASH_VOCAB
-    for k in widths:
+    for k in (widths if want("accept") else []):
         n_sets = int(np.ceil(3 * L2 / (k * V * 4))) + 1
         base = torch.from_numpy(S.vocab_logits(0, f"kbench.accept.{k}", k, V, 0)).cuda()
         sets = []
@@ -690,6 +695,42 @@ def run_kernels(args):
         emit("verify_accept_greedy", f"accept V{V}", k, us, k * V * 4 + 4 * (k - 1) + 4 * (k + 2),
              {"sets": n_sets})
         del sets, base
+        torch.cuda.empty_cache()
+    # next row: width-k attention verify at the Flash-Next attention shape over
+    # caches of 4,096 and 65,536 positions; caches rotated over > 3 x L2
+    ac = S.FLASH_ATTN
+    Hq, Hkv, D = ac["n_q_heads"], ac["n_kv_heads"], ac["d"]
+    params = B.attn_params(Hq, Hkv, D, ac["rope_dim"], ac["theta"])
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    for P in ((4096, 65536) if want("attn") else ()):
+        cap = P + kmax
+        cache_bytes = 2 * Hkv * cap * D * 2
+        n_c = int(np.ceil(3 * L2 / cache_bytes)) + 1
+        split = B.attn_default_split(cap)
+        nb = B.attn_workspace_bytes(params, cap, split, kmax)
+        caches = []
+        for _ in range(n_c):
+            Kc = torch.randn((Hkv, cap, D), generator=gen, device="cuda").half().view(torch.int16)
+            Vc = torch.randn((Hkv, cap, D), generator=gen, device="cuda").half().view(torch.int16)
+            wk = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            caches.append((Kc, Vc, wk))
+        for k in widths:
+            ins = {n: dev(S.bf16_normal(0, f"kbench.attn.{n}{k}", (k, (Hq if n in "qg" else Hkv) * D)).view(np.int16))
+                   for n in ("q", "g", "k", "v")}
+            ai = B.attn_inputs(ins["q"], ins["g"], ins["k"], ins["v"])
+            o = torch.empty((k, Hq * D), dtype=torch.float32, device="cuda")
+            calls = []
+            for (Kc, Vc, wk) in caches:
+                kc = B.kv_cache(Kc, Vc, wk, P, split)
+                keep.append(kc)
+                calls.append(lambda kc=kc, k=k: vf.attn_verify_k(params, kc, ai, k, o, B.F32, stream.cuda_stream))
+            us = time_calls(calls)
+            flops = sum(4.0 * Hq * D * (P + r + 1) for r in range(k))
+            emit("attn_verify_k", f"attn Hq{Hq} Hkv{Hkv} D{D} P{P}", k, us,
+                 2 * Hkv * (P + k) * D * 2 + k * (2 * Hq * D * 2 + 2 * Hkv * D * 2 + Hq * D * 4),
+                 {"tflops": round(flops / us / 1e6, 2), "caches": n_c, "split": split})
+        del caches
         torch.cuda.empty_cache()
     print(json.dumps({"summary": "per-kernel roofline: back-to-back calls, weights or inputs rotated over > 3 x L2",
                       "n": len(lines), "peak": hbm, "peak_kind": peak_kind}), flush=True)
@@ -706,6 +747,8 @@ def main():
     ap.add_argument("--widths", default="1,4,8,9,16", help="widths also measured (reported under config.per_k)")
     ap.add_argument("--layers", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="",
+                    help="with --kernels: comma list of dense,lm_head,experts,gdn,accept,attn (default all)")
     ap.add_argument("--kernels", action="store_true",
                     help="time each hot-path kernel alone on its own configuration instead (JSON line per kernel)")
     args = ap.parse_args()

@@ -476,6 +476,10 @@ typedef struct {
   const uint16_t* v;    int64_t ld_v;
 } verify_attn_inputs;
 
+/* A split for a cache of `capacity` positions: about 128 key splits per KV
+ * head at full length (a multiple of 32, at least 32). */
+int32_t attn_default_split(int64_t capacity);
+
 /* Workspace bytes attn_verify_k needs for a cache of `capacity` positions cut
  * by `split`, for widths up to max_k (0 for bad arguments). */
 int64_t attn_workspace_bytes(const verify_attn_params* p, int64_t capacity, int32_t split, int32_t max_k);

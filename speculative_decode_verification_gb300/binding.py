@@ -110,6 +110,7 @@ def load():
         "gdn_commit_all": [C.POINTER(GdnState), i, i],
         "verify_set_layer_events": [p, C.POINTER(p), i],
         "attn_workspace_bytes": [C.POINTER(AttnParams), i64, C.c_int32, C.c_int32],
+        "attn_default_split": [i64],
         "attn_verify_k": [p, C.POINTER(AttnParams), C.POINTER(KvCache), C.POINTER(AttnInputs), i, p, i, p],
         "attn_commit": [C.POINTER(KvCache), i],
         "gdn_state_to_device": [p, C.POINTER(GdnState), i, p, p],
@@ -335,6 +336,10 @@ def attn_params(Hq, Hkv, D, rope_dim=64, theta=1e7) -> AttnParams:
 
 def attn_workspace_bytes(params: AttnParams, capacity: int, split: int, max_k: int) -> int:
     return int(load().attn_workspace_bytes(C.byref(params), capacity, split, max_k))
+
+
+def attn_default_split(capacity: int) -> int:
+    return int(load().attn_default_split(capacity))
 
 
 def kv_cache(K, V, work, length=0, split=256) -> KvCache:

@@ -5,9 +5,9 @@
 // sees the earlier rows' keys and values).
 //
 // Three launches:
-//  1. append: the block's keys (rotated at P + r, angles in float64) and
-//     values go into the cache at P + r as binary16; CTA (r, 0) also writes
-//     the (cos, sin) table of row r for the queries.
+//  1. append: the block's keys (rotated at P + r) and values go into the
+//     cache at P + r as binary16; the queries are rotated and scaled by
+//     1/sqrt(D) and kept as binary16 pairs hi + lo.
 //  2. partials: CTA (M group, split s, KV head) takes 2 tiles of 16
 //     (row, query head) pairs of that KV head's group and the key positions
 //     [s*split, (s+1)*split) of the window, 32 at a time through a
@@ -15,10 +15,10 @@
 //     the tensor cores (mma.sync m16n8k16, binary16 operands, fp32 sums; the
 //     query and the probabilities each as a binary16 pair hi + lo, two MMAs
 //     against the same key or value fragment, so that only the cache's own
-//     binary16 rounding remains), masks
-//     positions after each row's own (P + r), keeps the running max and sum,
-//     and accumulates P V for its half of the head dim.  Both warps of a tile
-//     compute the same S.
+//     binary16 rounding remains).  Each warp of a tile sums S over its half of
+//     the head dim and the halves are added through shared memory; then both
+//     mask positions after each row's own (P + r), keep the running max and
+//     sum, and accumulate P V for their own half of the head dim.
 //  3. combine: per (row, query head) the splits that hold the row's window are
 //     merged in ascending order and gated.
 //
@@ -29,8 +29,10 @@
 // splits past it are skipped.
 //
 // Bound: the cache read, 2 * Hkv * D * 2 bytes per position (2 KB at the
-// Flash-Next shape), with the work of k * Hq / Hkv query rows per key; at long
-// windows and k ~ 9 the mma.sync pipe, not HBM, is the limit.
+// Flash-Next shape), with 4 * k * Hq * D flops per key position.  The hi + lo
+// pairs double the tensor work, and at k ~ 9 the mma.sync pipe, not HBM, is
+// the limit: a capture at 65,536 positions shows the tensor pipe 37% busy,
+// stalled on MMA dependencies, with DRAM 12% busy.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -42,6 +44,7 @@ namespace vk {
 namespace {
 
 constexpr int kBN = 32;        // key positions per sub-tile
+constexpr int kNS = kBN / 8;   // 8-position n-tiles of S per sub-tile
 constexpr int kMT = 2;         // tiles of 16 (row, head) pairs per CTA
 constexpr int kThreads = 128;  // 4 warps: (tile, D half)
 
@@ -78,24 +81,51 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 __device__ __forceinline__ uint32_t pack_half2(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // ---------------------------------------------------------------- append
+// x rotated at pos on its first rope_dim entries, entry e.  The angle
+// pos * inv_freq[j] is formed and reduced modulo 2 pi in float64 (two float64
+// operations: the device's float64 rate is low), then sin and cos of the
+// reduced angle in fp32, the rotation in float64.
+__device__ __forceinline__ double rope_entry(const uint16_t* x, int e, int rope_dim, const double* inv_freq,
+                                             long long pos) {
+  const int half = rope_dim / 2;
+  double y = (double)bf16f(x[e]);
+  if (e < rope_dim) {
+    const int j = e < half ? e : e - half;
+    constexpr double kTwoPi = 6.283185307179586;
+    const double ang = (double)pos * inv_freq[j];
+    const float red = (float)fma(-kTwoPi, rint(ang * (1.0 / kTwoPi)), ang);
+    float sn, cs;
+    sincosf(red, &sn, &cs);
+    y = e < half ? y * cs - (double)bf16f(x[e + half]) * sn : y * cs + (double)bf16f(x[e - half]) * sn;
+  }
+  return y;
+}
+
+// CTA (r, h): h < Hkv appends KV head h's key and value of row r to the cache;
+// h >= Hkv rotates and scales query head h - Hkv of row r into its binary16
+// pair (hi, lo).
 __global__ void attn_append_kernel(const AttnArgs a) {
-  const int r = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
-  const int half = a.rope_dim / 2;
+  const int r = blockIdx.x, h = blockIdx.y;
   const long long pos = (long long)a.P + r;
-  const uint16_t* kr = a.kin + (long long)r * a.ld_k + (long long)h * a.D;
-  const uint16_t* vr = a.vin + (long long)r * a.ld_v + (long long)h * a.D;
-  for (int e = i; e < a.D; e += blockDim.x) {
-    double y = (double)bf16f(kr[e]);
-    if (e < a.rope_dim) {
-      const int j = e < half ? e : e - half;
-      double sn, cs;
-      sincos((double)pos * pow((double)a.theta, -2.0 * j / a.rope_dim), &sn, &cs);
-      y = e < half ? y * cs - (double)bf16f(kr[e + half]) * sn : y * cs + (double)bf16f(kr[e - half]) * sn;
-      if (h == 0 && e < half) a.rot[r * half + e] = make_float2((float)cs, (float)sn);
+  if (h < a.Hkv) {
+    const uint16_t* kr = a.kin + (long long)r * a.ld_k + (long long)h * a.D;
+    const uint16_t* vr = a.vin + (long long)r * a.ld_v + (long long)h * a.D;
+    for (int e = threadIdx.x; e < a.D; e += blockDim.x) {
+      const long long dst = ((long long)h * a.cap + pos) * a.D + e;
+      a.K[dst] = __half_as_ushort(__double2half(rope_entry(kr, e, a.rope_dim, a.inv_freq, pos)));
+      a.V[dst] = __half_as_ushort(__float2half_rn(bf16f(vr[e])));
     }
-    const long long dst = ((long long)h * a.cap + pos) * a.D + e;
-    a.K[dst] = __half_as_ushort(__double2half(y));
-    a.V[dst] = __half_as_ushort(__float2half_rn(bf16f(vr[e])));
+    return;
+  }
+  const int hq = h - a.Hkv;
+  const uint16_t* qr = a.q + (long long)r * a.ld_q + (long long)hq * a.D;
+  const double scale = 1.0 / sqrt((double)a.D);
+  for (int e = threadIdx.x; e < a.D; e += blockDim.x) {
+    const double y = rope_entry(qr, e, a.rope_dim, a.inv_freq, pos) * scale;
+    const __half hi = __double2half(y);
+    const long long dst = ((long long)r * a.Hq + hq) * a.D + e;
+    a.qh[dst] = __half_as_ushort(hi);
+    a.ql[dst] = __half_as_ushort(__double2half(y - (double)__half2float(hi)));
   }
 }
 
@@ -134,30 +164,20 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
     }
     cp_async_commit();
   };
-  load_sub(0, 0);
-
-  // queries of this CTA's 32 (row, head) pairs: rotated at P + r, scaled by
-  // 1/sqrt(D), held as two binary16 parts hi + lo (about 22 significant bits;
-  // zeros past M)
-  const float scale = 1.f / sqrtf((float)D);
-  const int half = a.rope_dim / 2;
-  for (int e = tid; e < kMT * 16 * D; e += kThreads) {
-    const int mm = e / D, i = e % D, m = m0 + mm;
-    float y = 0.f;
-    if (m < M) {
-      const int r = m / G, hq = hk * G + m % G;
-      const uint16_t* qr = a.q + (long long)r * a.ld_q + (long long)hq * D;
-      y = bf16f(qr[i]);
-      if (i < a.rope_dim) {
-        const float2 cs = a.rot[r * half + (i < half ? i : i - half)];
-        y = i < half ? fmaf(y, cs.x, -bf16f(qr[i + half]) * cs.y) : fmaf(y, cs.x, bf16f(qr[i - half]) * cs.y);
-      }
+  // queries of this CTA's 32 (row, head) pairs, rotated at P + r and scaled by
+  // 1/sqrt(D) by the append kernel: two binary16 parts hi + lo (about 22
+  // significant bits; zeros past M).  They travel with the first key tile.
+  {
+    constexpr int QCH = kMT * 16 * (D / 8);
+    for (int q = tid; q < 2 * QCH; q += kThreads) {
+      const int part = q / QCH, cc = q % QCH;
+      const int mm = cc / (D / 8), col = (cc % (D / 8)) * 8, m = m0 + mm;
+      const bool ok = m < M;
+      const long long row = ok ? (long long)(m / G) * a.Hq + hk * G + m % G : 0;
+      cp_async16(smem_addr((part ? Qlo : Qs) + mm * LD + col), (part ? a.ql : a.qh) + row * D + col, ok ? 16u : 0u);
     }
-    const float ys = y * scale;
-    const __half hi = __float2half_rn(ys);
-    Qs[mm * LD + i] = __half_as_ushort(hi);
-    Qlo[mm * LD + i] = __half_as_ushort(__float2half_rn(ys - __half2float(hi)));
   }
+  load_sub(0, 0);
 
   const int mt = w >> 1, dh = w & 1;
   const int mrow = m0 + mt * 16;         // first pair of this warp's tile
@@ -172,8 +192,10 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
 #pragma unroll
   for (int nt = 0; nt < NTO; ++nt) o_acc[nt][0] = o_acc[nt][1] = o_acc[nt][2] = o_acc[nt][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  const uint32_t q_base = smem_addr(Qs + (mt * 16 + (lane & 15)) * LD + (lane >> 4) * 8);
+  // this warp's D half of the query fragments
+  const uint32_t q_base = smem_addr(Qs + (mt * 16 + (lane & 15)) * LD + dh * (D / 2) + (lane >> 4) * 8);
   const uint32_t qlo_base = q_base + SM::Q_BYTES;
+  __shared__ float xs[4][kNS * 4][32];  // partial scores of each warp, in fragment order
 
   for (int sub = 0; sub < nsub; ++sub) {
     if (sub + 1 < nsub) {
@@ -186,32 +208,53 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
     if (live) {
       const uint16_t* Ks = KVs + ((sub & 1) * 2) * kBN * LD;
       const uint16_t* Vs = Ks + kBN * LD;
-      // S = Q K^T: 16 pairs x 32 positions
-      float sacc[4][4];
+      // S = Q K^T: 16 pairs x kBN positions.  Each warp of the tile sums over
+      // its D half (hi and lo query parts in separate accumulators), then the
+      // two halves are added through shared memory, half 0 first.
+      float sh[kNS][4], sl[kNS][4];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+      for (int nt = 0; nt < kNS; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
       // lanes 0-7 / 8-15: rows of n-tile 2j at columns +0 / +8; lanes 16-31: n-tile 2j+1
-      const uint32_t k_base = smem_addr(Ks + ((lane >> 4) * 8 + (lane & 7)) * LD + ((lane >> 3) & 1) * 8);
+      const uint32_t k_base =
+          smem_addr(Ks + ((lane >> 4) * 8 + (lane & 7)) * LD + dh * (D / 2) + ((lane >> 3) & 1) * 8);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
+      for (int kk = 0; kk < D / 32; ++kk) {
+        uint32_t a0, a1, a2, a3, l0, l1, l2, l3, b[2 * kNS];
         ldsm_x4(q_base + kk * 32, a0, a1, a2, a3);
         ldsm_x4(qlo_base + kk * 32, l0, l1, l2, l3);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(k_base + j * 16 * LD * 2 + kk * 32, b0, b1, b2, b3);
-          mma_f16(sacc[2 * j], a0, a1, a2, a3, b0, b1);
-          mma_f16(sacc[2 * j], l0, l1, l2, l3, b0, b1);
-          mma_f16(sacc[2 * j + 1], a0, a1, a2, a3, b2, b3);
-          mma_f16(sacc[2 * j + 1], l0, l1, l2, l3, b2, b3);
-        }
+        for (int j = 0; j < kNS / 2; ++j)
+          ldsm_x4(k_base + j * 16 * LD * 2 + kk * 32, b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+#pragma unroll
+        for (int nt = 0; nt < kNS; ++nt) mma_f16(sh[nt], a0, a1, a2, a3, b[2 * nt], b[2 * nt + 1]);
+#pragma unroll
+        for (int nt = 0; nt < kNS; ++nt) mma_f16(sl[nt], l0, l1, l2, l3, b[2 * nt], b[2 * nt + 1]);
       }
+      float sacc[kNS][4];
+#pragma unroll
+      for (int nt = 0; nt < kNS; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float part = sh[nt][e] + sl[nt][e];
+          xs[w][nt * 4 + e][lane] = part;
+          sacc[nt][e] = part;
+        }
+      if (mt == 0) named_bar(1, 64);  // the tile's two warps (constant ids)
+      else named_bar(2, 64);
+#pragma unroll
+      for (int nt = 0; nt < kNS; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float other = xs[w ^ 1][nt * 4 + e][lane];
+          sacc[nt][e] = dh == 0 ? sacc[nt][e] + other : other + sacc[nt][e];
+        }
       // mask, running max and sum; p rounded to binary16 feeds P V and the sum
       const int pbase = pos0 + sub * kBN;
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < kNS; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int ri = e >> 1, pos = pbase + nt * 8 + 2 * c + (e & 1);
@@ -229,10 +272,10 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
         msub[ri] = mn == -INFINITY ? 0.f : mn;
         m_run[ri] = mn;
       }
-      uint32_t pa[4][2], pl[4][2];  // p as binary16 pairs hi, lo: [n-tile][row g / g + 8]
+      uint32_t pa[kNS][2], pl[kNS][2];  // p as binary16 pairs hi, lo: [n-tile][row g / g + 8]
       float ps[2] = {0.f, 0.f};
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < kNS; ++nt)
 #pragma unroll
         for (int ri = 0; ri < 2; ++ri) {
           const float p0 = expf(sacc[nt][2 * ri] - msub[ri]), p1 = expf(sacc[nt][2 * ri + 1] - msub[ri]);
@@ -259,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
       // 16 positions of a k-step, lanes 16-31 the same for the next n-tile
       const uint32_t v_base = smem_addr(Vs + (lane & 15) * LD + dh * (D / 2) + (lane >> 4) * 8);
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
+      for (int kk = 0; kk < kBN / 16; ++kk) {
         const uint32_t a0 = pa[2 * kk][0], a1 = pa[2 * kk][1], a2 = pa[2 * kk + 1][0], a3 = pa[2 * kk + 1][1];
         const uint32_t l0 = pl[2 * kk][0], l1 = pl[2 * kk][1], l2 = pl[2 * kk + 1][0], l3 = pl[2 * kk + 1][1];
 #pragma unroll
@@ -292,26 +335,67 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
 }
 
 // ---------------------------------------------------------------- combine
-__global__ void attn_combine_kernel(const AttnArgs a) {
+// One CTA per (row, query head).  The splits holding the row's window are
+// merged in ascending order: weights exp(m_j - max) go to shared memory in
+// chunks, and each thread sums its dims over the chunk, eight loads in
+// flight, adding in split order.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineChunk = 1024;
+
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const AttnArgs a) {
+  __shared__ float fs[kCombineChunk], ls[kCombineChunk];
+  __shared__ float red[kCombineThreads / 32];
   const int G = a.Hq / a.Hkv, Mpad = 16 * a.n_mtiles;
   const int r = blockIdx.x / a.Hq, hq = blockIdx.x % a.Hq, hk = hq / G;
   const int m = r * G + hq % G;
   const int nsr = (a.P + r + a.split) / a.split;  // splits holding positions 0 .. P + r
-  float mstar = -INFINITY;
-  for (int j = 0; j < nsr; ++j) mstar = fmaxf(mstar, a.part_ml[(long long)(hk * a.nsplit + j) * Mpad + m].x);
-  for (int i = threadIdx.x; i < a.D; i += blockDim.x) {
-    float acc = 0.f, l = 0.f;
-    for (int j = 0; j < nsr; ++j) {
-      const long long row = (long long)(hk * a.nsplit + j) * Mpad + m;
-      const float2 ml = a.part_ml[row];
-      if (ml.x == -INFINITY) continue;
-      const float f = expf(ml.x - mstar);
-      acc = fmaf(a.part_o[row * a.D + i], f, acc);
-      l = fmaf(ml.y, f, l);
+  const long long row0 = (long long)hk * a.nsplit * Mpad + m;  // split j at row0 + j * Mpad
+  const int tid = threadIdx.x;
+  float mx = -INFINITY;
+  for (int j = tid; j < nsr; j += kCombineThreads) mx = fmaxf(mx, a.part_ml[row0 + (long long)j * Mpad].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  float mstar = red[0];
+#pragma unroll
+  for (int i = 1; i < kCombineThreads / 32; ++i) mstar = fmaxf(mstar, red[i]);
+  constexpr int U = 8;
+  float acc[2] = {0.f, 0.f}, l = 0.f;  // dims tid and tid + 256 (head_dim <= 512)
+  for (int c0 = 0; c0 < nsr; c0 += kCombineChunk) {
+    const int n = min(kCombineChunk, nsr - c0);
+    __syncthreads();
+    for (int j = tid; j < n; j += kCombineThreads) {
+      const float2 ml = a.part_ml[row0 + (long long)(c0 + j) * Mpad];
+      fs[j] = ml.x == -INFINITY ? 0.f : expf(ml.x - mstar);
+      ls[j] = ml.y;
     }
+    __syncthreads();
+    for (int j = 0; j < n; ++j) l = fmaf(ls[j], fs[j], l);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = tid + h * kCombineThreads;
+      if (i >= a.D) break;
+      const float* src = a.part_o + (row0 + (long long)c0 * Mpad) * a.D + i;
+      const long long stride = (long long)Mpad * a.D;
+      int j = 0;
+      for (; j + U <= n; j += U) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = __ldcs(src + (j + u) * stride);
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[h] = fmaf(x[u], fs[j + u], acc[h]);
+      }
+      for (; j < n; ++j) acc[h] = fmaf(__ldcs(src + j * stride), fs[j], acc[h]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = tid + h * kCombineThreads;
+    if (i >= a.D) break;
     const long long oi = (long long)r * a.Hq * a.D + (long long)hq * a.D + i;
     const float gt = bf16f(a.gate[(long long)r * a.ld_gate + (long long)hq * a.D + i]);
-    const float y = acc / l * (1.f / (1.f + expf(-gt)));
+    const float y = acc[h] / l * (1.f / (1.f + expf(-gt)));
     if (a.dtype == 1) reinterpret_cast<uint16_t*>(a.o)[oi] = f2bf16(y);
     else reinterpret_cast<float*>(a.o)[oi] = y;
   }
@@ -319,7 +403,7 @@ __global__ void attn_combine_kernel(const AttnArgs a) {
 
 template <int D>
 cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s, int* launches) {
-  attn_append_kernel<<<dim3(a.k, a.Hkv), 256, 0, s>>>(a);
+  attn_append_kernel<<<dim3(a.k, a.Hkv + a.Hq), 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e) return e;
   ++*launches;
@@ -327,7 +411,7 @@ cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s, int* launches) {
   attn_partial_kernel<D><<<grid, kThreads, AttnSmem<D>::BYTES, s>>>(a);
   if ((e = cudaGetLastError())) return e;
   ++*launches;
-  attn_combine_kernel<<<a.k * a.Hq, 256, 0, s>>>(a);
+  attn_combine_kernel<<<a.k * a.Hq, kCombineThreads, 0, s>>>(a);
   if ((e = cudaGetLastError())) return e;
   ++*launches;
   return cudaSuccess;

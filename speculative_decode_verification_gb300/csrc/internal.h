@@ -122,11 +122,12 @@ struct AttnArgs {
   uint16_t* V;
   long long cap;
   int Hq, Hkv, D, rope_dim;
-  float theta;
+  double inv_freq[128];  // theta^(-2j / rope_dim), j < rope_dim / 2, computed on the host in float64
   int P, k, split;
   int nsplit;           // ceil((P + k) / split)
   int n_mtiles;         // ceil(k * Hq / Hkv / 16): 16 (row, head) pairs per tile
-  float2* rot;          // [k][rope_dim / 2] (cos, sin) at positions P + r
+  uint16_t* qh;         // [k][Hq][D] binary16: rotated, scaled queries (hi part)
+  uint16_t* ql;         // the remainders (lo part)
   float* part_o;        // [Hkv][nsplit][16 n_mtiles][D] unnormalised outputs
   float2* part_ml;      // [Hkv][nsplit][16 n_mtiles] (running max, sum)
   void* o;              // [k, Hq * D]

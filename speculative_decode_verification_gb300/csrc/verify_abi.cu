@@ -1,6 +1,7 @@
 // verify_abi.cu - the C ABI declared in include/verify.h: context and scratch,
 // argument validation (all done before anything is launched), TMA
 // descriptors, launches on the caller's stream, GDN slot bookkeeping.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -542,18 +543,20 @@ verify_status verify_accept_greedy(verify_ctx* ctx, const float* logits, int64_t
 
 // ------------------------------------------------------------ attention
 
-// Workspace of one attention call: the rotation table, then (max, sum) and the
-// unnormalised outputs of every (KV head, split, pair), each 256-byte aligned.
+// Workspace of one attention call: the rotated queries (hi and lo binary16
+// parts), then (max, sum) and the unnormalised outputs of every (KV head,
+// split, pair), each 256-byte aligned.
 struct AttnWork {
-  long long rot, ml, po, total;
+  long long qh, ql, ml, po, total;
 };
 static AttnWork attn_work(const verify_attn_params* p, long long nsplit, int k) {
   auto up = [](long long b) { return (b + 255) / 256 * 256; };
   const long long G = p->n_q_heads / p->n_kv_heads;
   const long long Mpad = (k * G + 15) / 16 * 16;
   AttnWork w;
-  w.rot = 0;
-  w.ml = up((long long)k * (p->rope_dim / 2) * 8);
+  w.qh = 0;
+  w.ql = up((long long)k * p->n_q_heads * p->head_dim * 2);
+  w.ml = w.ql + up((long long)k * p->n_q_heads * p->head_dim * 2);
   w.po = w.ml + up(p->n_kv_heads * nsplit * Mpad * 8);
   w.total = w.po + up(p->n_kv_heads * nsplit * Mpad * (long long)p->head_dim * 4);
   return w;
@@ -563,6 +566,13 @@ static bool attn_params_ok(const verify_attn_params* p) {
   return p && p->n_q_heads >= 1 && p->n_kv_heads >= 1 && p->n_q_heads % p->n_kv_heads == 0 &&
          p->n_q_heads <= 1024 && (p->head_dim == 128 || p->head_dim == 256) && p->rope_dim >= 0 &&
          p->rope_dim <= p->head_dim && p->rope_dim % 2 == 0 && p->rope_theta > 0.f;
+}
+
+int32_t attn_default_split(int64_t capacity) {
+  if (capacity < 1) return 32;
+  const int64_t per = (capacity + 127) / 128;
+  const int64_t s = (per + 31) / 32 * 32;
+  return (int32_t)(s < 32 ? 32 : (s > (1 << 20) ? (1 << 20) : s));
 }
 
 int64_t attn_workspace_bytes(const verify_attn_params* p, int64_t capacity, int32_t split, int32_t max_k) {
@@ -603,11 +613,13 @@ verify_status attn_verify_k(verify_ctx* ctx, const verify_attn_params* p, verify
   a.q = in->q; a.ld_q = in->ld_q; a.gate = in->gate; a.ld_gate = in->ld_gate;
   a.kin = in->k; a.ld_k = in->ld_k; a.vin = in->v; a.ld_v = in->ld_v;
   a.K = cache->K; a.V = cache->V; a.cap = cache->capacity;
-  a.Hq = p->n_q_heads; a.Hkv = p->n_kv_heads; a.D = D; a.rope_dim = p->rope_dim; a.theta = p->rope_theta;
+  a.Hq = p->n_q_heads; a.Hkv = p->n_kv_heads; a.D = D; a.rope_dim = p->rope_dim;
+  for (int j = 0; j < p->rope_dim / 2; ++j) a.inv_freq[j] = pow((double)p->rope_theta, -2.0 * j / p->rope_dim);
   a.P = cache->len; a.k = k; a.split = cache->split; a.nsplit = (int)nsplit;
   a.n_mtiles = (k * G + 15) / 16;
   char* base = static_cast<char*>(cache->work);
-  a.rot = reinterpret_cast<float2*>(base + w.rot);
+  a.qh = reinterpret_cast<uint16_t*>(base + w.qh);
+  a.ql = reinterpret_cast<uint16_t*>(base + w.ql);
   a.part_ml = reinterpret_cast<float2*>(base + w.ml);
   a.part_o = reinterpret_cast<float*>(base + w.po);
   a.o = o; a.dtype = dtype_out == VERIFY_BF16 ? 1 : 0;
