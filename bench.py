@@ -703,7 +703,8 @@ def run_kernels(args):
     params = B.attn_params(Hq, Hkv, D, ac["rope_dim"], ac["theta"])
     gen = torch.Generator(device="cuda")
     gen.manual_seed(0)
-    for P in ((4096, 65536) if want("attn") else ()):
+    attn_ps = [int(x) for x in args.attn_p.split(",") if x]
+    for P in (attn_ps if want("attn") else ()):
         cap = P + kmax
         cache_bytes = 2 * Hkv * cap * D * 2
         n_c = int(np.ceil(3 * L2 / cache_bytes)) + 1
@@ -749,6 +750,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
                     help="with --kernels: comma list of dense,lm_head,experts,gdn,accept,attn (default all)")
+    ap.add_argument("--attn-p", default="4096,65536",
+                    help="with --kernels: cached positions of the attention rows (comma list)")
     ap.add_argument("--kernels", action="store_true",
                     help="time each hot-path kernel alone on its own configuration instead (JSON line per kernel)")
     args = ap.parse_args()
