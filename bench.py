@@ -55,7 +55,7 @@ MOE_TRAFFIC_RATIO = 423.830272e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
     "q4_kernels.cu": "fec6bb1e38dd162e2c457a22b389b21886b22895ea205503cf21fee6e0fa0bd0",
     "common.cuh": "249c762d042e43ac9c4c4d180b4ceee3ec2cba7f6f77f10aca9458f16499efa2",
-    "internal.h": "de05c6ac68a4402989803601246e06496a2f1014865c41001652f0c1d43ab657",
+    "internal.h": "159b5d8572666eea0459b20616e0abb7866e251170f8c15654798b807f4d9174",
 }
 
 
