@@ -1,7 +1,7 @@
 /*
  * verify.h - C ABI of the exact width-k verification pass (one GB300, sm_103a).
  *
- * A speculative-decoding verify pass runs a block of k draft rows (k = 1..16;
+ * A speculative-decoding verify pass runs a block of k draft rows (k = 1..32;
  * the pages measure 1..9) through the target model in one pass and must give,
  * row for row, what k ordinary one-row steps give.  This library provides the
  * data-parallel hot path of that pass for hybrid Gated-DeltaNet / MoE models:
@@ -84,8 +84,9 @@ typedef enum {
   VERIFY_F32_ADD = 2  /* y(fp32) += result: the residual add of a verify layer */
 } verify_dtype;
 
-#define VERIFY_MAX_K 16          /* widest verify block any call accepts */
-#define VERIFY_GDN_MAX_SLOTS 17  /* VERIFY_MAX_K + 1 state slots */
+#define VERIFY_MAX_K 32          /* widest verify block any call accepts */
+#define VERIFY_PASS_K 16         /* rows per pass: wider blocks run as two passes */
+#define VERIFY_GDN_MAX_SLOTS 33  /* VERIFY_MAX_K + 1 state slots */
 
 typedef struct verify_ctx verify_ctx;
 
@@ -211,7 +212,9 @@ verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_ex
  * x : bf16 [k, k_in] row-major, 16-byte aligned.
  * y : [k, n_out] row-major, fp32 (VERIFY_F32 / VERIFY_F32_ADD) or bf16.
  * k : 1..VERIFY_MAX_K.   Limits: n_out <= 1<<20, k_in <= 1<<17.
- * Each packed weight is read from HBM once per call for all k rows.
+ * Each packed weight is read from HBM once per pass of up to VERIFY_PASS_K
+ * rows: k <= 16 is one launch, 17..32 two launches (rows 0..15, then the
+ * rest), each row computed as in a width-1 call.
  */
 verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W,
                        const uint16_t* x, int k, void* y, int dtype_out,
@@ -247,9 +250,11 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W,
  * at shared_gate_logit + r*logits_ld) may all be NULL (no shared expert).
  * Limits: E <= 512, 1 <= T <= 16, 64 <= H <= 8192, 64 <= I <= 4096,
  * H % 64 == I % 64 == 0.
- * Expert weights are read once per call for every distinct selected expert
- * (the union of the rows' routes).  Two kernel launches on `stream`: the routed
- * experts (gate/up and down items in one kernel), then the combine.
+ * Expert weights are read once per pass of up to VERIFY_PASS_K rows for
+ * every distinct expert the pass selects (the union of its rows' routes).
+ * Two kernel launches per pass on `stream`: the routed experts (gate/up and
+ * down items in one kernel), then the combine; k in 17..32 runs two passes
+ * (rows 0..15, then the rest).
  */
 verify_status q4_gather_experts_k(verify_ctx* ctx,
                                   const verify_q4_experts* gate_up,
@@ -342,7 +347,9 @@ typedef struct {
  * The state (S and conv window) after row r is written to slot pending[r+1]
  * (the free slots in ascending index order); slot cur is only read.
  * o : [k, n_v_heads*head_dim_v] fp32 or bf16 (VERIFY_F32 / VERIFY_BF16).
- * Requires n_slots >= k+1, all slot pointers 16-byte aligned.
+ * Requires n_slots >= k+1, all slot pointers 16-byte aligned.  One launch for
+ * k <= 16; k in 17..32 adds a second launch that continues from the snapshot
+ * after row 15 (the state carries over exactly).
  * A second verify without a commit in between starts again from `cur`.
  * With a device-held commit (st->dev) the kernel takes cur from dev[0] when
  * it runs, every one of the n_slots slots must be valid, and dev[1] becomes k.
@@ -421,7 +428,7 @@ verify_status gdn_commit_dev(verify_ctx* ctx, const verify_gdn_state* states, in
  * (a rows stand; t_m is the next pending token).  If n_states > 0 it then
  * commits a on every state as gdn_commit_dev does, which also requires each
  * state's pending rows to equal k (else device error 3, nothing committed).
- * Limits: 1 <= k <= 16, 1 <= V <= 2^30, ld >= V.  Rows that are 16-byte
+ * Limits: 1 <= k <= 32, 1 <= V <= 2^30, ld >= V.  Rows that are 16-byte
  * aligned (logits aligned, ld % 4 == 0) are read as float4.  One kernel
  * launch; the ctx's scratch serialises calls on one ctx (one stream at a time).
  */
@@ -497,7 +504,7 @@ int64_t attn_workspace_bytes(const verify_attn_params* p, int64_t capacity, int3
  * pos * theta^(-2i/rope_dim) for i < rope_dim/2; other dims pass through.
  * o: [k, n_q_heads*head_dim], VERIFY_F32 or VERIFY_BF16 (row stride
  * n_q_heads*head_dim).  Three kernel launches (append, split partials,
- * combine).  Limits: 1 <= k <= 16, k * n_q_heads / n_kv_heads <= 256,
+ * combine).  Limits: 1 <= k <= 32, k * n_q_heads / n_kv_heads <= 512,
  * len + k <= capacity.  Arithmetic: rotation angles in float64, the
  * rotation in fp32; q.K and p.V on the tensor cores with binary16 operands and
  * fp32 sums, the scaled query and the probabilities each carried as a pair of
@@ -544,8 +551,10 @@ verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w,
  *   h  += q4_gather_experts_k(gate_up, down, l[:, :E], top_k, xn2,
  *                             shared_gate_up, shared_down, l[:, E])
  * idx_out (optional, device int32 [k, top_k]) receives the routed expert
- * indices.  Eight kernel launches on `stream`, no host synchronisation.  Scratch
- * activations live in the context (limits: k <= 16, H <= 8192, in_proj rows
+ * indices.  Eight kernel launches on `stream` for k <= 16 (fourteen for
+ * 17..32: the products, the DeltaNet step and the experts run two passes),
+ * no host synchronisation.  Scratch
+ * activations live in the context (limits: k <= 32, H <= 8192, in_proj rows
  * <= 32768, E + 1 <= 1024).  Weight shapes must match: in_proj [C + Hv*dv +
  * 2*Hv, H], out_proj [H, Hv*dv], router [E + 1, H], gate_up [E, 2I, H],
  * down [E, H, I], shared_gate_up [2I, H], shared_down [H, I]; all tiled
@@ -575,7 +584,8 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
  * h updated in place.  idx_out (optional, device int32) receives layer l's
  * routed indices at idx_out + l * k * layers[l].top_k.  Returns the first
  * failing layer's status; the layers before it have been enqueued and their
- * states advanced.  8 * n_layers kernel launches, no host synchronisation.
+ * states advanced.  verify_layer_k's launches per layer, no host
+ * synchronisation.
  */
 verify_status verify_stack_k(verify_ctx* ctx, const verify_layer* layers, verify_gdn_state* states, int n_layers,
                              float* h, int k, int32_t* idx_out, struct CUstream_st* stream);
@@ -610,7 +620,7 @@ verify_status verify_set_layer_events(verify_ctx* ctx, void* const* events, int 
  * and per-unit counts) lives in one array of
  * VERIFY_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
  * that loads the library holds until the process exits.
- *   - Limit: k*(T+s)*I*2 + k*(T+s)*H*4 bytes (s = 1 with a shared expert, each
+ *   - Limit: k <= VERIFY_PASS_K (one pass); k*(T+s)*I*2 + k*(T+s)*H*4 bytes (s = 1 with a shared expert, each
  *     part rounded up to 256) plus 4352 must fit the array; larger calls
  *     return VERIFY_EUNSUPPORTED before anything is enqueued.
  *   - The first call on each device sets that device up (resolves the array's

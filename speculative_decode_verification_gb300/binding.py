@@ -17,8 +17,9 @@ LIB_PATH = os.path.join(PKG, "libverify.so")
 OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE = 0, 1, 2, 3, 4
 F32, BF16, F32_ADD = 0, 1, 2
 ROWS, TILED, TILED_GATE_UP = 0, 1, 2  # verify_q4_layout
-MAX_K = 16
-GDN_MAX_SLOTS = 17
+MAX_K = 32
+PASS_K = 16
+GDN_MAX_SLOTS = 33
 
 _lib = None
 

@@ -79,8 +79,10 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
       return;
     }
   }
-  const float* S_in = a.S_slots[cur];
-  const uint16_t* tail_in = a.tail_slots[cur];
+  // this launch starts from the state after the block's first r0 rows
+  const int in_slot = a.r0 == 0 ? cur : (a.r0 - 1) + (a.r0 - 1 >= cur ? 1 : 0);
+  const float* S_in = a.S_slots[in_slot];
+  const uint16_t* tail_in = a.tail_slots[in_slot];
 
   // ---- before the grid dependency wait: the state slice and the conv
   //      weights and tail (parameters, or written by an earlier verify call)
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
   for (int h2 = 0; h2 < EPT; ++h2) nw[h2] = a.norm_w[p * kGdnRows + (tid + h2 * NT) % kGdnRows];
   griddep_wait();
   griddep_launch();
-  if (a.dev_state && blockIdx.x == 0 && tid == 0) a.dev_state[1] = k;
+  if (a.dev_state && blockIdx.x == 0 && tid == 0) a.dev_state[1] = a.r0 + k;
 
   // ---- 1. causal depthwise conv + SiLU; slide the window
   uint16_t xin[NIT][kGdnMaxK];
@@ -165,7 +167,8 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
       else vs[r][cl - 2 * D] = cv;
       w0 = w1; w1 = w2; w2 = xr;
       if (write_tail) {
-        uint16_t* to = a.tail_slots[r + (r >= cur)];
+        const int rr = a.r0 + r;
+        uint16_t* to = a.tail_slots[rr + (rr >= cur)];
         to[ch] = w0;
         to[C + ch] = w1;
         to[2 * C + ch] = w2;
@@ -236,7 +239,8 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
     }
     const float delta = (vs[r][il] - mk) * beta;
     const float y = fmaf(delta, kq[r], mq);  // (S + delta k^T) q = S q + delta (k.q)
-    float* dst = a.S_slots[r + (r >= cur)] + ((long long)h * D + i) * D;
+    const int rr = a.r0 + r;
+    float* dst = a.S_slots[rr + (rr >= cur)] + ((long long)h * D + i) * D;
 #pragma unroll
     for (int m = 0; m < NV4; ++m) {
       const float4 kv = *reinterpret_cast<const float4*>(&kn[r][4 * l + 4 * TPR * m]);

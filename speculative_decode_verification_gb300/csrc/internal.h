@@ -66,15 +66,17 @@ struct MoeArgs {
 
 // State slots: S_slots[s] fp32 [Hv, dv, dk], tail_slots[s] bf16 [W-1, C].  The
 // kernel reads slot cur and writes the state after row r to slot r + (r >= cur),
-// the r+1-th slot other than cur in ascending order.  cur is the argument, or,
+// the r+1-th slot other than cur in ascending order (r counted from the
+// block's first row: a launch with r0 > 0 continues from the slot of row r0-1).  cur is the argument, or,
 // with dev_state, dev_state[0] read when the kernel runs (written by a device
 // commit at least two launches earlier); the kernel then stores k in
 // dev_state[1] (the rows now pending).
 struct GdnArgs {
-  float* S_slots[17];
-  uint16_t* tail_slots[17];
+  float* S_slots[33];
+  uint16_t* tail_slots[33];
   int n_slots, cur;
   int* dev_state;
+  int r0;  // block row of this launch's first row: it starts from the state after r0 rows
   const uint16_t* qkv; long long ld_qkv;
   const uint16_t* z;   long long ld_z;
   const uint16_t* a;   long long ld_a;
@@ -133,7 +135,7 @@ struct AttnArgs {
   void* o;              // [k, Hq * D]
   int dtype;
 };
-constexpr int kAttnMaxM = 256;   // k * (Hq / Hkv) per call
+constexpr int kAttnMaxM = 512;   // k * (Hq / Hkv) per call
 cudaError_t attn_setup_kernels();
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s, int* launches);
 
@@ -155,7 +157,7 @@ struct AcceptArgs {
   unsigned int* ticket;       // scratch, zero between calls
   int* err;
 };
-constexpr int kMaxAcceptK = 16;
+constexpr int kMaxAcceptK = 32;
 constexpr int kAcceptThreads = 256;
 // Grid of the acceptance kernel: CTAs per logits row.
 int accept_blocks_per_row(int V, int k, int num_sms);

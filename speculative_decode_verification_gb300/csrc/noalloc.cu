@@ -86,7 +86,7 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   if (s) return s;
 
   // ---- arguments (all checked before anything is enqueued)
-  if (!gate_up || !down || k < 1 || k > VERIFY_MAX_K) return k < 1 || k > VERIFY_MAX_K ? VERIFY_EUNSUPPORTED : VERIFY_EINVAL;
+  if (!gate_up || !down || k < 1 || k > VERIFY_PASS_K) return k < 1 || k > VERIFY_PASS_K ? VERIFY_EUNSUPPORTED : VERIFY_EINVAL;
   const int E = gate_up->n_experts;
   if (E < 1 || E > vk::kMaxExperts || down->n_experts != E) return VERIFY_EUNSUPPORTED;
   if (top_k < 1 || top_k > vk::kMaxTopK || top_k > E) return VERIFY_EUNSUPPORTED;

@@ -255,7 +255,7 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W, const uint16_
   if (!ctx) return VERIFY_EINVAL;
   verify_status s;
   if ((s = use_device(ctx))) return s;
-  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..32%s");
   if ((s = check_q4(ctx, W, "W"))) return s;
   if ((s = check_dtype(ctx, dtype_out, true))) return s;
   if ((s = check_dev(ctx, x, 16, "x"))) return s;
@@ -263,14 +263,22 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W, const uint16_
 
   vk::DenseArgs a{};
   a.tiles = reinterpret_cast<const uint8_t*>(W->packed); a.rt_bytes = rt_bytes(W->k_in);
-  a.x = x; a.y = y; a.err = ctx->err;
-  a.N = W->n_out; a.K = W->k_in; a.k = k; a.dtype = dtype_out;
+  a.err = ctx->err;
+  a.N = W->n_out; a.K = W->k_in; a.dtype = dtype_out;
   a.KG = a.K / 64; a.KC = (a.KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
   a.RB = (a.N + vk::kBM - 1) / vk::kBM;
   a.S = dense_splits(ctx, a.RB, a.KC);
-  cudaError_t e = vk::launch_q4_dense(a, k <= 8 ? 1 : 2, ctx->pdl, stream);
-  if (e) return cuda_fail(ctx, e, "q4_qmv_k launch");
-  ctx->launches += 1;
+  const size_t y_elem = dtype_out == VERIFY_BF16 ? 2 : 4;
+  // passes of up to VERIFY_PASS_K rows; rows are independent, so each is
+  // computed exactly as in a width-1 call
+  for (int r0 = 0; r0 < k; r0 += VERIFY_PASS_K) {
+    a.k = k - r0 < VERIFY_PASS_K ? k - r0 : VERIFY_PASS_K;
+    a.x = x + (size_t)r0 * a.K;
+    a.y = static_cast<char*>(y) + (size_t)r0 * a.N * y_elem;
+    cudaError_t e = vk::launch_q4_dense(a, a.k <= 8 ? 1 : 2, ctx->pdl, stream);
+    if (e) return cuda_fail(ctx, e, "q4_qmv_k launch");
+    ctx->launches += 1;
+  }
   return VERIFY_OK;
 }
 
@@ -283,7 +291,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   verify_status s;
   if ((s = use_device(ctx))) return s;
   if (!gate_up || !down) return fail(ctx, VERIFY_EINVAL, "expert stacks are NULL%s");
-  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..32%s");
   const int E = gate_up->n_experts;
   if (E < 1 || E > vk::kMaxExperts || down->n_experts != E)
     return fail(ctx, VERIFY_EUNSUPPORTED, "n_experts must match and be in 1..512%s");
@@ -328,13 +336,26 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   a.hbuf = ctx->moe_hbuf; a.part = ctx->moe_part;
   a.work = ctx->moe_sched; a.done = ctx->moe_sched + 1;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;
-  a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
+  a.E = E; a.T = top_k; a.H = H; a.I = I; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
   a.G = ctx->moe_ctas_per_sm * ctx->num_sms;
-  int launched = 0;
-  cudaError_t e = vk::launch_moe(a, ctx->pdl, stream, &launched);
-  ctx->launches += launched;
-  if (e) return cuda_fail(ctx, e, "q4_gather_experts_k launch");
+  const size_t y_elem = dtype_out == VERIFY_BF16 ? 2 : 4;
+  // passes of up to VERIFY_PASS_K rows (each row's routing, experts and
+  // combine depend on that row alone); a later pass's kernels write the
+  // shared scratch only after their dependency wait
+  for (int r0 = 0; r0 < k; r0 += VERIFY_PASS_K) {
+    a.k = k - r0 < VERIFY_PASS_K ? k - r0 : VERIFY_PASS_K;
+    a.logits = logits + (size_t)r0 * logits_ld;
+    a.shared_logit = n_shared ? shared_gate_logit + (size_t)r0 * logits_ld : nullptr;
+    a.x = x + (size_t)r0 * H;
+    a.idx_out = idx_out + (size_t)r0 * top_k;
+    a.w_out = w_out + (size_t)r0 * top_k;
+    a.y = static_cast<char*>(y) + (size_t)r0 * H * y_elem;
+    int launched = 0;
+    cudaError_t e = vk::launch_moe(a, ctx->pdl, stream, &launched);
+    ctx->launches += launched;
+    if (e) return cuda_fail(ctx, e, "q4_gather_experts_k launch");
+  }
   return VERIFY_OK;
 }
 
@@ -344,7 +365,7 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p, verify_g
   verify_status s;
   if ((s = use_device(ctx))) return s;
   if (!p || !st || !in) return fail(ctx, VERIFY_EINVAL, "params, state or inputs is NULL%s");
-  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..32%s");
   if (p->n_qk_heads < 1 || p->n_v_heads < 1 || p->n_v_heads % p->n_qk_heads != 0)
     return fail(ctx, VERIFY_EUNSUPPORTED, "n_v_heads must be a positive multiple of n_qk_heads%s");
   if (p->head_dim_k != p->head_dim_v ||
@@ -354,7 +375,7 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p, verify_g
   if (p->gate_act != 0 && p->gate_act != 1) return fail(ctx, VERIFY_EINVAL, "gate_act must be 0 or 1%s");
   if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16) return fail(ctx, VERIFY_EINVAL, "dtype_out F32 or BF16%s");
   if (st->n_slots < k + 1 || st->n_slots > VERIFY_GDN_MAX_SLOTS)
-    return fail(ctx, VERIFY_EINVAL, "n_slots must be in k+1..17%s");
+    return fail(ctx, VERIFY_EINVAL, "n_slots must be in k+1..33%s");
   if (!st->dev && (st->cur < 0 || st->cur >= st->n_slots)) return fail(ctx, VERIFY_EINVAL, "cur is not a slot%s");
   if (st->dev && (s = check_dev(ctx, st->dev, 8, "state dev words"))) return s;
   const int d = p->head_dim_k, Hk = p->n_qk_heads, Hv = p->n_v_heads;
@@ -392,15 +413,29 @@ verify_status gdn_verify_k(verify_ctx* ctx, const verify_gdn_params* p, verify_g
   a.n_slots = st->n_slots;
   a.cur = st->dev ? 0 : st->cur;
   a.dev_state = st->dev;
+  a.r0 = 0;
   a.qkv = in->qkv; a.ld_qkv = in->ld_qkv; a.z = in->z; a.ld_z = in->ld_z;
   a.a = in->a; a.ld_a = in->ld_a; a.b = in->b; a.ld_b = in->ld_b;
   a.conv_w = p->conv_w; a.A_log = p->A_log; a.dt_bias = p->dt_bias; a.norm_w = p->norm_w;
   a.o = o; a.err = ctx->err;
   a.Hk = Hk; a.Hv = Hv; a.d = d; a.W = p->conv_kernel; a.k = k; a.dtype = dtype_out; a.gate_act = p->gate_act;
   a.q_scale = p->q_scale; a.l2_eps = p->l2_eps; a.norm_eps = p->norm_eps;
-  cudaError_t e = vk::launch_gdn(a, ctx->pdl, stream);
-  if (e) return cuda_fail(ctx, e, "gdn_verify_k launch");
-  ctx->launches += 1;
+  // rows 0..15, then (k > 16) a continuation from the snapshot after row 15;
+  // it reads that snapshot before its dependency wait, so it is launched
+  // after the first pass has finished (no dependent launch)
+  const size_t o_elem = dtype_out == VERIFY_BF16 ? 2 : 4;
+  for (int r0 = 0; r0 < k; r0 += VERIFY_PASS_K) {
+    a.r0 = r0;
+    a.k = k - r0 < VERIFY_PASS_K ? k - r0 : VERIFY_PASS_K;
+    a.qkv = in->qkv + (size_t)r0 * in->ld_qkv;
+    a.z = in->z + (size_t)r0 * in->ld_z;
+    a.a = in->a + (size_t)r0 * in->ld_a;
+    a.b = in->b + (size_t)r0 * in->ld_b;
+    a.o = static_cast<char*>(o) + (size_t)r0 * Hv * d * o_elem;
+    cudaError_t e = vk::launch_gdn(a, r0 == 0 && ctx->pdl, stream);
+    if (e) return cuda_fail(ctx, e, "gdn_verify_k launch");
+    ctx->launches += 1;
+  }
   if (!st->dev) {
     for (int r = 0; r <= k; ++r) st->pending[r] = pending[r];
     st->pending_k = k;
@@ -513,7 +548,7 @@ verify_status verify_accept_greedy(verify_ctx* ctx, const float* logits, int64_t
   if (!ctx) return VERIFY_EINVAL;
   verify_status s;
   if ((s = use_device(ctx))) return s;
-  if (k < 1 || k > vk::kMaxAcceptK) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if (k < 1 || k > vk::kMaxAcceptK) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..32%s");
   if (V < 1 || V > (1 << 30)) return fail(ctx, VERIFY_EUNSUPPORTED, "V must be in 1..2^30%s");
   if (ld < V) return fail(ctx, VERIFY_EINVAL, "ld must be >= V%s");
   if ((s = check_dev(ctx, logits, 4, "logits")) || (s = check_dev(ctx, result, 4, "result"))) return s;
@@ -590,9 +625,9 @@ verify_status attn_verify_k(verify_ctx* ctx, const verify_attn_params* p, verify
   if (!attn_params_ok(p))
     return fail(ctx, VERIFY_EUNSUPPORTED, "attention: head_dim 128 or 256, n_q_heads a multiple of n_kv_heads, "
                                           "even rope_dim <= head_dim%s");
-  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..32%s");
   const int G = p->n_q_heads / p->n_kv_heads, D = p->head_dim;
-  if (k * G > vk::kAttnMaxM) return fail(ctx, VERIFY_EUNSUPPORTED, "k * n_q_heads / n_kv_heads must be <= 256%s");
+  if (k * G > vk::kAttnMaxM) return fail(ctx, VERIFY_EUNSUPPORTED, "k * n_q_heads / n_kv_heads must be <= 512%s");
   if (cache->split < 32 || cache->split % 32) return fail(ctx, VERIFY_EINVAL, "split must be a multiple of 32%s");
   if (cache->len < 0 || cache->capacity < 1 || (int64_t)cache->len + k > cache->capacity)
     return fail(ctx, VERIFY_EINVAL, "len + k must be <= capacity%s");
@@ -659,7 +694,7 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
                              int32_t* idx_out, struct CUstream_st* stream) {
   if (!ctx) return VERIFY_EINVAL;
   if (!L || !st) return fail(ctx, VERIFY_EINVAL, "layer or state is NULL%s");
-  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..16%s");
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..32%s");
   const verify_gdn_params& g = L->gdn;
   const int H = L->in_proj.k_in;
   const int C = 2 * g.n_qk_heads * g.head_dim_k + g.n_v_heads * g.head_dim_v;

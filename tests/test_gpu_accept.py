@@ -79,6 +79,8 @@ CASES = [
     (1, S.FLASH_VOCAB, 0, 0, 0),
     (9, S.FLASH_VOCAB, 0, 0, 0),
     (16, S.FLASH_VOCAB, 16, 0, 0),
+    (32, S.FLASH_VOCAB, 4, 0, 0),
+    (32, 777, 0, 3, 1),
 ]
 
 
@@ -133,11 +135,11 @@ def test_repeated_calls_leave_no_state(vf):
 def test_k_out_of_range_rejected(vf):
     import torch
 
-    lg = torch.zeros((17, 8), dtype=torch.float32, device="cuda")
-    res = torch.zeros(19, dtype=torch.int32, device="cuda")
-    d = torch.zeros(16, dtype=torch.int32, device="cuda")
+    lg = torch.zeros((33, 8), dtype=torch.float32, device="cuda")
+    res = torch.zeros(35, dtype=torch.int32, device="cuda")
+    d = torch.zeros(32, dtype=torch.int32, device="cuda")
     with pytest.raises(B.VerifyError) as e:
-        vf.accept_greedy(lg, 17, d, res)
+        vf.accept_greedy(lg, 33, d, res)
     assert e.value.status == B.EUNSUPPORTED
 
 
@@ -159,7 +161,8 @@ def _dev_cur(words):
     return int(host(words)[0, 0])
 
 
-@pytest.mark.parametrize("shape,k", [((2, 4, 64), 1), ((2, 4, 64), 4), ((2, 4, 64), 16), ((16, 48, 128), 9)])
+@pytest.mark.parametrize("shape,k", [((2, 4, 64), 1), ((2, 4, 64), 4), ((2, 4, 64), 16), ((2, 4, 64), 32),
+                                     ((16, 48, 128), 9)])
 def test_device_commit_equals_host_commit(vf, shape, k):
     """The same verify + commit sequence, once with host-held and once with
     device-held commits: outputs, committed slots and their contents agree
@@ -167,8 +170,8 @@ def test_device_commit_equals_host_commit(vf, shape, k):
     import torch
 
     Hk, Hv, d = shape
-    A = Layer(21, Hk, Hv, d, n_slots=17, s_std=0.02, tail_std=1.0)
-    Bl, arr, words = _device_layer(21, Hk, Hv, d)
+    A = Layer(21, Hk, Hv, d, n_slots=33, s_std=0.02, tail_std=1.0)
+    Bl, arr, words = _device_layer(21, Hk, Hv, d, n_slots=33)
     vf.gdn_state_to_device(arr, words)
     assert _dev_cur(words) == 0
     rng = np.random.default_rng(k)

@@ -89,13 +89,14 @@ CASES = [
     (24, 2, 256, 1000, 4, 256),
     (24, 2, 256, 2047, 16, 512),
     (6, 1, 256, 700, 9, 32),
+    (24, 2, 256, 500, 32, 256),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"H{c[0]}_{c[1]}_D{c[2]}_P{c[3]}_k{c[4]}_s{c[5]}" for c in CASES])
 def test_attn_matches_oracle(vf, case):
     Hq, Hkv, D, P, k, split = case
-    cache = Cache(20, f"attn.{Hq}.{D}.{P}", Hq, Hkv, D, P + k + 3, P, split)
+    cache = Cache(20, f"attn.{Hq}.{D}.{P}", Hq, Hkv, D, P + k + 3, P, split, max_k=max(16, k))
     inp = S.attn_inputs(20, f"attn.in.{Hq}.{P}.{k}", k, Hq, Hkv, D)
     o = cache.verify(vf, inp, k)
     oo, k_app, v_app = cache.oracle(inp, P)

@@ -91,11 +91,12 @@ def test_tiny_step_matches_oracle(vf, gate_act):
         assert np.array_equal(t_r, ot[r])
 
 
-@pytest.mark.parametrize("k", [1, 4, 9, 16])
+@pytest.mark.parametrize("k", [1, 4, 9, 16, 17, 32])
 def test_flash_shape_matches_oracle(vf, k):
-    """16/48 heads, d = 128, S0 ~ N(0, 0.02^2), conv tail ~ N(0,1)."""
+    """16/48 heads, d = 128, S0 ~ N(0, 0.02^2), conv tail ~ N(0,1).  k > 16
+    runs as two launches, the second continuing from row 15's snapshot."""
     c = S.FLASH_GDN
-    L = Layer(3, c["n_qk_heads"], c["n_v_heads"], c["d"], n_slots=17, s_std=0.02, tail_std=1.0)
+    L = Layer(3, c["n_qk_heads"], c["n_v_heads"], c["d"], n_slots=33, s_std=0.02, tail_std=1.0)
     inp = S.gdn_inputs(3, f"flash.gdn.{k}", k, c["n_qk_heads"], c["n_v_heads"], c["d"])
     o = L.verify(vf, inp, k)
     oo, oS, ot = L.oracle(inp, k)
@@ -106,12 +107,12 @@ def test_flash_shape_matches_oracle(vf, k):
         assert np.array_equal(t_r, ot[r])
 
 
-def test_k_rows_bit_identical_to_sequential_single_rows(vf):
+@pytest.mark.parametrize("k", [9, 32])
+def test_k_rows_bit_identical_to_sequential_single_rows(vf, k):
     """Row r of a k-row call equals a 1-row call started from the snapshot
     after r rows: outputs and states, bit for bit."""
     c = S.FLASH_GDN
-    k = 9
-    L = Layer(4, c["n_qk_heads"], c["n_v_heads"], c["d"], s_std=0.02, tail_std=1.0)
+    L = Layer(4, c["n_qk_heads"], c["n_v_heads"], c["d"], n_slots=k + 1, s_std=0.02, tail_std=1.0)
     inp = S.gdn_inputs(4, "seq.gdn", k, c["n_qk_heads"], c["n_v_heads"], c["d"])
     o = L.verify(vf, inp, k)
     snaps = [L.slot(L.state.pending[r + 1]) for r in range(k)]
@@ -127,12 +128,12 @@ def test_k_rows_bit_identical_to_sequential_single_rows(vf):
         S_prev, t_prev = S1, t1
 
 
-@pytest.mark.parametrize("k", [4, 8, 9])
+@pytest.mark.parametrize("k", [4, 8, 9, 20])
 def test_rollback_to_every_accepted_prefix(vf, k):
     """verify(k) + commit(a) leaves exactly the state of a fresh verify(a), for
     every a in 0..k; a = 0 keeps the pre-verify state."""
     c = S.FLASH_GDN
-    L = Layer(5, c["n_qk_heads"], c["n_v_heads"], c["d"], s_std=0.02, tail_std=1.0)
+    L = Layer(5, c["n_qk_heads"], c["n_v_heads"], c["d"], n_slots=max(10, k + 1), s_std=0.02, tail_std=1.0)
     inp = S.gdn_inputs(5, f"rb.gdn.{k}", k, c["n_qk_heads"], c["n_v_heads"], c["d"])
     for a in range(k + 1):
         L.reset()

@@ -53,7 +53,7 @@ def moe_case(seed, E, H, I):
     return gu, dn
 
 
-@pytest.mark.parametrize("k", [1, 2, 5, 9, 16])
+@pytest.mark.parametrize("k", [1, 2, 5, 9, 16, 25, 32])
 def test_small_moe_matches_oracle(vf, k):
     E, H, I, T = 16, 256, 256, 4
     gu, dn = moe_case(10, E, H, I)
@@ -64,7 +64,8 @@ def test_small_moe_matches_oracle(vf, k):
     gud, dnd = DevQ4(vf, gu, True), DevQ4(vf, dn)
     before = vf.launch_count()
     gi, gw, gy = gather(vf, gud, dnd, dev(logits), T, dev(x), k, H)
-    assert vf.launch_count() - before == 2  # the routed experts kernel, then the combine
+    # the routed experts kernel, then the combine, per pass of up to 16 rows
+    assert vf.launch_count() - before == 2 * ((k + 15) // 16)
     assert np.array_equal(gi, oi)
     np.testing.assert_allclose(gw, ow, rtol=1e-5, atol=1e-6)
     assert_close(gy, oy, what=f"k={k}")
@@ -200,3 +201,18 @@ def test_ornith_shape_matches_oracle(vf):
                 h = O.to_bf16(gate_up[:I] / (1.0 + np.exp(-gate_up[:I])) * gate_up[I:])
                 ref[r] += ow[r, j] * O.q4_qmv(md.packed, md.scales, md.biases, h[None, :])[0]
         assert_close(gy, ref, what=f"ornith k={k}")
+
+
+def test_width_32_rows_equal_single_rows(vf):
+    """A 32-row call runs as two 16-row passes: every row's indices, weights
+    and output equal a 1-row call on that row, bit for bit."""
+    E, H, I, T, k = 64, 256, 256, 8, 32
+    gu, dn = moe_case(15, E, H, I)
+    x = S.bf16_normal(15, "moe.w32.x", (k, H))
+    logits = S.f32_normal(15, "moe.w32.l", (k, E))
+    gud, dnd = DevQ4(vf, gu, True), DevQ4(vf, dn)
+    gi, gw, gy = gather(vf, gud, dnd, dev(logits), T, dev(x), k, H)
+    for r in (0, 7, 15, 16, 24, 31):
+        i1, w1, y1 = gather(vf, gud, dnd, dev(logits[r:r + 1]), T, dev(x[r:r + 1]), 1, H)
+        assert np.array_equal(i1[0], gi[r]) and np.array_equal(w1[0].view(np.uint32), gw[r].view(np.uint32))
+        assert np.array_equal(y1[0].view(np.uint32), gy[r].view(np.uint32)), f"row {r}"

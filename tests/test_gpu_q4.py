@@ -51,7 +51,7 @@ def test_tiny_projection_matches_oracle_widths_1_to_4(vf):
 
 @pytest.mark.parametrize("N,K", [(1, 256), (96, 2560), (100, 640), (129, 1152), (300, 512), (1000, 2048),
                                  (200, 576), (130, 192), (5, 64)])
-@pytest.mark.parametrize("k", [1, 5, 9, 16])
+@pytest.mark.parametrize("k", [1, 5, 9, 16, 32])
 def test_ragged_shapes_match_oracle(vf, N, K, k):
     m = S.q4_matrix(1, f"rag.{N}.{K}", N, K)
     W = DevQ4(vf, m)
@@ -65,10 +65,10 @@ def test_ragged_shapes_match_oracle(vf, N, K, k):
 def test_width_k_rows_bit_identical_to_width_1(vf, N, K):
     m = S.q4_matrix(2, f"bit.{N}.{K}", N, K)
     W = DevQ4(vf, m)
-    x = S.bf16_normal(2, f"bit.x.{N}.{K}", (16, K))
+    x = S.bf16_normal(2, f"bit.x.{N}.{K}", (32, K))
     xd = dev(x)
-    singles = [host(run_qmv(vf, W, dev(x[r:r + 1]), 1, N))[0] for r in range(16)]
-    for k in (2, 4, 8, 9, 16):
+    singles = [host(run_qmv(vf, W, dev(x[r:r + 1]), 1, N))[0] for r in range(32)]
+    for k in (2, 4, 8, 9, 16, 17, 32):
         y = host(run_qmv(vf, W, xd, k, N))
         for r in range(k):
             assert np.array_equal(y[r].view(np.uint32), singles[r].view(np.uint32)), f"k={k} row {r}"
@@ -150,7 +150,7 @@ def test_argument_errors_are_reported_before_launch(vf):
         vf.q4_qmv_k(W.struct, x, 0, y)
     assert e.value.status == B.EUNSUPPORTED
     with pytest.raises(B.VerifyError) as e:
-        vf.q4_qmv_k(W.struct, x, 17, y)
+        vf.q4_qmv_k(W.struct, x, 33, y)  # wider than VERIFY_MAX_K
     assert e.value.status == B.EUNSUPPORTED
     hx = torch.zeros((2, 512), dtype=torch.int16)  # host memory
     with pytest.raises(B.VerifyError) as e:

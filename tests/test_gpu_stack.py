@@ -80,7 +80,9 @@ def check_layers(vf, cfg, seed, k, layers, h_name):
         idx = torch.zeros((k, sh["T"]), dtype=torch.int32, device="cuda")
         before = vf.launch_count()
         vf.verify_layer_k(ds.layers[l], ds.states[l], hd, k, idx)
-        assert vf.launch_count() - before == 8  # norm, in_proj, GDN, out_proj, norm, router, experts, combine
+        # norm, in_proj, GDN, out_proj, norm, router, experts, combine; above 16
+        # rows the products, the GDN step and the experts run two passes
+        assert vf.launch_count() - before == (8 if k <= 16 else 14)
         torch.cuda.synchronize()
         st = ds.states[l]
         S_last = host(ds.state_tensors[l][0][st.pending[k]])
@@ -113,7 +115,7 @@ def check_layers(vf, cfg, seed, k, layers, h_name):
     return compared
 
 
-@pytest.mark.parametrize("k", [1, 4, 9, 16])
+@pytest.mark.parametrize("k", [1, 4, 9, 16, 32])
 def test_small_stack_layers_match_oracle(vf, k):
     assert check_layers(vf, SMALL, 1, k, SMALL["layers"], f"stack.h{k}") > 0
 
@@ -125,7 +127,7 @@ def test_flash_next_stack_layers_match_oracle(vf):
     assert check_layers(vf, cfg, 0, 9, cfg["layers"], "stack.full.h") >= 9 * cfg["layers"] // 2
 
 
-@pytest.mark.parametrize("k", [9, 16])
+@pytest.mark.parametrize("k", [9, 16, 32])
 def test_stack_rows_equal_single_row_steps(vf, k):
     """Row r of a k-row verify through the whole stack is bit-identical to a
     1-row verify started from the states after r rows (every layer)."""
