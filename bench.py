@@ -55,7 +55,7 @@ MOE_TRAFFIC_RATIO = 423.830272e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
     "q4_kernels.cu": "fec6bb1e38dd162e2c457a22b389b21886b22895ea205503cf21fee6e0fa0bd0",
     "common.cuh": "249c762d042e43ac9c4c4d180b4ceee3ec2cba7f6f77f10aca9458f16499efa2",
-    "internal.h": "159b5d8572666eea0459b20616e0abb7866e251170f8c15654798b807f4d9174",
+    "internal.h": "79c9ee68c1438d371ed1db836a1bf4d26bf3e0372c26f83f19e8087682ddb69e",
 }
 
 
@@ -745,7 +745,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--k", type=int, default=9, help="verify width of the headline number")
-    ap.add_argument("--widths", default="1,4,8,9,16", help="widths also measured (reported under config.per_k)")
+    ap.add_argument("--widths", default="1,4,8,9,16,32", help="widths also measured (reported under config.per_k)")
     ap.add_argument("--layers", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
