@@ -21,6 +21,7 @@
 //     sum, and accumulate P V for their own half of the head dim.
 //  3. combine: per (row, query head) the splits that hold the row's window are
 //     merged in ascending order and gated.
+// Launches 2 and 3 are programmatic dependents of the one before.
 //
 // Exactness: a row's arithmetic depends only on its own query, its window and
 // the absolute cut of key positions (split and the 32-position sub-tiles), not
@@ -105,6 +106,7 @@ __device__ __forceinline__ double rope_entry(const uint16_t* x, int e, int rope_
 // h >= Hkv rotates and scales query head h - Hkv of row r into its binary16
 // pair (hi, lo).
 __global__ void attn_append_kernel(const AttnArgs a) {
+  griddep_launch();  // the split kernel may start its prefetch of committed positions
   const int r = blockIdx.x, h = blockIdx.y;
   const long long pos = (long long)a.P + r;
   if (h < a.Hkv) {
@@ -164,9 +166,17 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
     }
     cp_async_commit();
   };
+  // Launched as a programmatic dependent of the append kernel: a first
+  // sub-tile of positions committed before this call (written at least two
+  // launches back) is fetched before the dependency wait; the queries and the
+  // block's own keys and values after it.
+  const bool early = pos0 + kBN <= a.P;
+  if (early) load_sub(0, 0);
+  griddep_wait();
+  griddep_launch();
   // queries of this CTA's 32 (row, head) pairs, rotated at P + r and scaled by
   // 1/sqrt(D) by the append kernel: two binary16 parts hi + lo (about 22
-  // significant bits; zeros past M).  They travel with the first key tile.
+  // significant bits; zeros past M).
   {
     constexpr int QCH = kMT * 16 * (D / 8);
     for (int q = tid; q < 2 * QCH; q += kThreads) {
@@ -177,7 +187,8 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a
       cp_async16(smem_addr((part ? Qlo : Qs) + mm * LD + col), (part ? a.ql : a.qh) + row * D + col, ok ? 16u : 0u);
     }
   }
-  load_sub(0, 0);
+  if (early) cp_async_commit();  // the queries as a group of their own
+  else load_sub(0, 0);           // the queries travel with the first tile
 
   const int mt = w >> 1, dh = w & 1;
   const int mrow = m0 + mt * 16;         // first pair of this warp's tile
@@ -351,6 +362,15 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const Att
   const int nsr = (a.P + r + a.split) / a.split;  // splits holding positions 0 .. P + r
   const long long row0 = (long long)hk * a.nsplit * Mpad + m;  // split j at row0 + j * Mpad
   const int tid = threadIdx.x;
+  // the gate is an input of the call: read it before the dependency wait
+  float gt[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = tid + h * kCombineThreads;
+    gt[h] = i < a.D ? bf16f(a.gate[(long long)r * a.ld_gate + (long long)hq * a.D + i]) : 0.f;
+  }
+  griddep_wait();
+  griddep_launch();
   float mx = -INFINITY;
   for (int j = tid; j < nsr; j += kCombineThreads) mx = fmaxf(mx, a.part_ml[row0 + (long long)j * Mpad].x);
 #pragma unroll
@@ -394,8 +414,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const Att
     const int i = tid + h * kCombineThreads;
     if (i >= a.D) break;
     const long long oi = (long long)r * a.Hq * a.D + (long long)hq * a.D + i;
-    const float gt = bf16f(a.gate[(long long)r * a.ld_gate + (long long)hq * a.D + i]);
-    const float y = acc[h] / l * (1.f / (1.f + expf(-gt)));
+    const float y = acc[h] / l * (1.f / (1.f + expf(-gt[h])));
     if (a.dtype == 1) reinterpret_cast<uint16_t*>(a.o)[oi] = f2bf16(y);
     else reinterpret_cast<float*>(a.o)[oi] = y;
   }
@@ -407,12 +426,25 @@ cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s, int* launches) {
   cudaError_t e = cudaGetLastError();
   if (e) return e;
   ++*launches;
-  const dim3 grid((a.n_mtiles + kMT - 1) / kMT, a.nsplit, a.Hkv);
-  attn_partial_kernel<D><<<grid, kThreads, AttnSmem<D>::BYTES, s>>>(a);
-  if ((e = cudaGetLastError())) return e;
+  // the partial and combine kernels are programmatic dependents: each may
+  // start while the kernel before it finishes, and waits before reading its
+  // results
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.n_mtiles + kMT - 1) / kMT, a.nsplit, a.Hkv);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = AttnSmem<D>::BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, attn_partial_kernel<D>, a))) return e;
   ++*launches;
-  attn_combine_kernel<<<a.k * a.Hq, kCombineThreads, 0, s>>>(a);
-  if ((e = cudaGetLastError())) return e;
+  cfg.gridDim = dim3(a.k * a.Hq);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  if ((e = cudaLaunchKernelEx(&cfg, attn_combine_kernel, a))) return e;
   ++*launches;
   return cudaSuccess;
 }
