@@ -82,6 +82,20 @@ def run():
     assert a == 3 and host(words).tolist() == [[2 + (2 >= c), 0]], "device commit"
     _, oS2, _ = O.gdn_verify(Hk, Hv, d, p, oS[1], ot[1], inp, k)
     assert_close(host(slots[2 + (2 >= c)]), oS2[2], what="device-committed state")
+    # width-k attention over a small binary16 cache
+    Hq, Hkv, D, P = 4, 2, 128, 37
+    Kc, Vc = S.attn_cache(0, "smoke.attn", Hkv, P + k, D, P)
+    ai = S.attn_inputs(0, "smoke.attn.in", k, Hq, Hkv, D)
+    Kd, Vd = dev(Kc), dev(Vc)
+    ap = B.attn_params(Hq, Hkv, D)
+    work = torch.empty(B.attn_workspace_bytes(ap, P + k, 32, k), dtype=torch.uint8, device="cuda")
+    kc = B.kv_cache(Kd, Vd, work, P, 32)
+    aid = {key: dev(v.reshape(k, -1)) for key, v in ai.items()}
+    ao = torch.zeros((k, Hq * D), device="cuda")
+    vf.attn_verify_k(ap, kc, B.attn_inputs(aid["q"], aid["gate"], aid["k"], aid["v"]), k, ao)
+    torch.cuda.synchronize()
+    oo_attn, _, _ = O.attn_verify(Hq, Hkv, D, P, ai["q"], ai["k"], ai["v"], ai["gate"], Kc, Vc)
+    assert_close(host(ao), oo_attn.reshape(k, -1), what="attn_verify_k")
     status, code = vf.device_status()
     assert status == B.OK, f"device error word {code}"
     vf.close()
