@@ -484,7 +484,7 @@ typedef struct {
 } verify_attn_inputs;
 
 /* A split for a cache of `capacity` positions: about 128 key splits per KV
- * head at full length (a multiple of 32, at least 32). */
+ * head at full length, a multiple of 32 and at least 128. */
 int32_t attn_default_split(int64_t capacity);
 
 /* Workspace bytes attn_verify_k needs for a cache of `capacity` positions cut

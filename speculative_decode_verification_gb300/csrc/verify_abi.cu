@@ -603,11 +603,13 @@ static bool attn_params_ok(const verify_attn_params* p) {
          p->rope_dim <= p->head_dim && p->rope_dim % 2 == 0 && p->rope_theta > 0.f;
 }
 
+// About 128 key splits per KV head at full length, and at least 128
+// positions per split (a sweep at 4,096 and 65,536 positions, k = 1 and 9).
 int32_t attn_default_split(int64_t capacity) {
-  if (capacity < 1) return 32;
+  if (capacity < 1) return 128;
   const int64_t per = (capacity + 127) / 128;
   const int64_t s = (per + 31) / 32 * 32;
-  return (int32_t)(s < 32 ? 32 : (s > (1 << 20) ? (1 << 20) : s));
+  return (int32_t)(s < 128 ? 128 : (s > (1 << 20) ? (1 << 20) : s));
 }
 
 int64_t attn_workspace_bytes(const verify_attn_params* p, int64_t capacity, int32_t split, int32_t max_k) {
