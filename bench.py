@@ -240,7 +240,8 @@ def run_ours(args, cfg):
     for k in widths:
         h0 = torch.from_numpy(S.f32_normal(0, f"bench.h{k}", (k, H))).cuda()
         h = torch.empty_like(h0)
-        idx = [torch.zeros((k, T), dtype=torch.int32, device="cuda") for _ in range(L)]
+        idx_all = torch.zeros((L, k, T), dtype=torch.int32, device="cuda")
+        idx = [idx_all[l] for l in range(L)]
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(L)]
         with torch.cuda.stream(stream):
             for row in ev:
@@ -256,10 +257,13 @@ def run_ours(args, cfg):
                     st.cur, st.pending_k = 0, 0
                 with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
                     h.copy_(h0)
-                    for l, (Ly, st) in enumerate(zip(ds.layers, ds.states)):
-                        vf.set_layer_events(events_for_layer(l))
-                        vf.verify_layer_k(Ly, st, h, k, idx[l], stream.cuda_stream)
-                    vf.set_layer_events(None)
+                    if events_for_layer is None:  # the public one-call pass
+                        vf.verify_stack_k(ds.layers, ds.states, h, k, idx_all, stream.cuda_stream)
+                    else:
+                        for l, (Ly, st) in enumerate(zip(ds.layers, ds.states)):
+                            vf.set_layer_events(events_for_layer(l))
+                            vf.verify_layer_k(Ly, st, h, k, idx[l], stream.cuda_stream)
+                        vf.set_layer_events(None)
             return graph
 
         for st in ds.states:
@@ -268,7 +272,9 @@ def run_ours(args, cfg):
             h.copy_(h0)
             lc0 = vf.launch_count()
             ds.verify(h, k, idx, stream.cuda_stream)          # warm (first launches, first touch)
-            launches_per_pass = vf.launch_count() - lc0       # our kernels in one verify pass (eager)
+            n_launch = vf.launch_count() - lc0                # our kernels in one verify pass (eager)
+            if k == args.k:
+                launches_per_pass = n_launch
         torch.cuda.synchronize()
         # breakdown graph: every sub-step boundary of every layer (untimed)
         gb = capture(lambda l: ev[l])
@@ -281,9 +287,10 @@ def run_ours(args, cfg):
         sub = {n: float(np.mean([ev[l][i].elapsed_time(ev[l][i + 1]) * 1e3 for l in range(L)]))
                for i, n in enumerate(names)}
         del gb
-        # timed graph: the verify step alone (an event between two kernels stops the
-        # second from overlapping the first, so the step carries none)
-        g = capture(lambda l: None)
+        # timed graph: the verify step alone, one verify_stack_k call (an event
+        # between two kernels stops the second from overlapping the first, so
+        # the step carries none)
+        g = capture(None)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):

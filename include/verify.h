@@ -585,7 +585,10 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
  * routed indices at idx_out + l * k * layers[l].top_k.  Returns the first
  * failing layer's status; the layers before it have been enqueued and their
  * states advanced.  verify_layer_k's launches per layer, no host
- * synchronisation.
+ * synchronisation.  Layer 0's first kernel waits for everything enqueued
+ * before the call; each later layer's first kernel is a programmatic
+ * dependent of the layer before (it reads only its weights before its
+ * dependency wait).
  */
 verify_status verify_stack_k(verify_ctx* ctx, const verify_layer* layers, verify_gdn_state* states, int n_layers,
                              float* h, int k, int32_t* idx_out, struct CUstream_st* stream);

@@ -34,6 +34,10 @@ struct verify_ctx {
   // Set only inside verify_layer_k: the next launch may start while the
   // kernel before it on the stream still runs (programmatic dependent launch).
   bool pdl = false;
+  // Set by verify_stack_k for layers after the first: the layer's first kernel
+  // may overlap the previous layer's last one (it reads only static data
+  // before its dependency wait).
+  bool chain_layer = false;
   char msg[512] = {0};
 };
 
@@ -715,16 +719,17 @@ verify_status verify_layer_k(verify_ctx* ctx, const verify_layer* L, verify_gdn_
     if (ctx->n_layer_events == 8 && ctx->layer_events[i])
       cudaEventRecordWithFlags(ctx->layer_events[i], sm, cudaEventRecordExternal);
   };
-  // The layer's first kernel waits for everything enqueued before the call;
-  // each later one may start during its predecessor's tail, unless an event is
-  // recorded between the two.
+  // The layer's first kernel waits for everything enqueued before the call
+  // (inside verify_stack_k, layers after the first chain to the previous
+  // layer instead); each later one may start during its predecessor's tail,
+  // unless an event is recorded between the two.
   struct PdlOff {
     verify_ctx* c;
     ~PdlOff() { c->pdl = false; }
   } pdl_off{ctx};
   auto overlap_after = [&](int i) { ctx->pdl = !(ctx->n_layer_events == 8 && ctx->layer_events[i]); };
   mark(0);
-  ctx->pdl = false;
+  ctx->pdl = ctx->chain_layer && !(ctx->n_layer_events == 8 && ctx->layer_events[0]);
   // 1. pre-mixer norm
   if ((s = verify_rmsnorm_k(ctx, h, L->norm1_w, L->norm_eps, 1, H, k, ctx->st_xn, VERIFY_BF16, sm))) return s;
   mark(1);
@@ -769,7 +774,9 @@ verify_status verify_stack_k(verify_ctx* ctx, const verify_layer* layers, verify
   if (!layers || !states || n_layers < 1) return fail(ctx, VERIFY_EINVAL, "layers, states or n_layers invalid%s");
   int32_t* idx = idx_out;
   for (int l = 0; l < n_layers; ++l) {
+    ctx->chain_layer = l > 0;
     verify_status s = verify_layer_k(ctx, &layers[l], &states[l], h, k, idx, stream);
+    ctx->chain_layer = false;
     if (s) return s;
     if (idx) idx += (long long)k * layers[l].top_k;
   }
