@@ -183,3 +183,16 @@ def test_argument_errors(vf):
     o = torch.zeros((1, 24 * 256), device="cuda")
     with pytest.raises(B.VerifyError):
         vf.attn_verify_k(small, c2, B.attn_inputs(d["q"], d["gate"], d["k"], d["v"]), 1, o)  # workspace too small
+
+
+@pytest.mark.parametrize("rope_dim,theta", [(0, 1e7), (128, 1e4), (32, 5e5)])
+def test_rope_dim_variants(vf, rope_dim, theta):
+    """No rotation, full rotation (rope_dim = head_dim) and a narrow band,
+    at another base: outputs and appended keys against the oracle."""
+    Hq, Hkv, D, P, k = 8, 2, 128, 300, 9
+    cache = Cache(26, f"rd.{rope_dim}", Hq, Hkv, D, P + k, P, 64, rope_dim=rope_dim, theta=theta)
+    inp = S.attn_inputs(26, f"rd.in.{rope_dim}", k, Hq, Hkv, D)
+    o = cache.verify(vf, inp, k)
+    oo, k_app, v_app = cache.oracle(inp, P)
+    assert_close(o, oo.reshape(k, -1), what=f"rope_dim={rope_dim}")
+    _check_appended(cache, P, k, k_app, v_app)
