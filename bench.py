@@ -53,9 +53,9 @@ EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
 # them reports null until the kernel is captured again.
 MOE_TRAFFIC_RATIO = 423.830272e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
-    "q4_kernels.cu": "fec6bb1e38dd162e2c457a22b389b21886b22895ea205503cf21fee6e0fa0bd0",
+    "q4_kernels.cu": "e0c27f19fe5ac111744c11abf6e218398ab77b9a9f90a8d402364cab98e7be92",
     "common.cuh": "249c762d042e43ac9c4c4d180b4ceee3ec2cba7f6f77f10aca9458f16499efa2",
-    "internal.h": "79c9ee68c1438d371ed1db836a1bf4d26bf3e0372c26f83f19e8087682ddb69e",
+    "internal.h": "ad24c5d3d06bbb017f43bbc27b7628d9fdcc31aaa44027c2c684c26918761823",
 }
 
 
@@ -504,11 +504,14 @@ def device_loop(args, ds, vf, stream, k, H, world):
             ts_sel.append(time.perf_counter() - t0)
             acc.append(int(rout[0]))
         sel_dev = device_ms(lambda: ds.verify_select_accept(hd, k, dd, res, stream.cuda_stream))
+        unf_dev = device_ms(lambda: ds.verify_select_accept(hd, k, dd, res, stream.cuda_stream, fused=False))
         sel_s = max_over_ranks(float(np.median(ts_sel)), world)
         sel = {"ms_per_step": sel_s * 1e3, "device_ms_per_step": max_over_ranks(sel_dev, world),
+               "device_ms_per_step_unfused": max_over_ranks(unf_dev, world),
                "lm_head_bytes": int(0.5625 * V * H), "accepted_rows_mean": float(np.mean(acc)),
-               "path": "DeviceStack.verify_select_accept: verify_stack_k + final norm + q4_qmv_k LM head + "
-                       "verify_accept_greedy in one graph"}
+               "path": "DeviceStack.verify_select_accept: verify_stack_k + final norm + verify_lm_head_accept "
+                       "(the LM head with its argmax epilogue, acceptance and commit) in one graph; unfused: "
+                       "q4_qmv_k logits then verify_accept_greedy"}
     ds.to_host()
     st, code = vf.device_status()
     if st != 0:

@@ -436,6 +436,25 @@ verify_status verify_accept_greedy(verify_ctx* ctx, const float* logits, int64_t
                                    const int32_t* draft, int32_t* result, const verify_gdn_state* states,
                                    int n_states, struct CUstream_st* stream);
 
+/*
+ * GPU token selection at the target, fused ([T] table "Shared architecture":
+ * greedy proposals use a compact vocabulary, target verification the full
+ * one; [R] "Acceptance"): the LM head product y = W . x[r] (as q4_qmv_k
+ * computes it) with an argmax epilogue, so the logits never reach memory,
+ * then greedy acceptance and the commit as verify_accept_greedy does.
+ *   W     : VERIFY_Q4_TILED [V, H], V = vocabulary (n_out <= 2^20).
+ *   x     : bf16 [k, H] (the final-normed rows), 16-byte aligned.
+ *   draft, result, states, n_states: as verify_accept_greedy.
+ * The choices equal those of q4_qmv_k followed by verify_accept_greedy on its
+ * fp32 output, bit for bit.  One launch per pass of up to 16 rows (17..32 rows:
+ * two passes), whose epilogue merges each row's argmax key with a 64-bit
+ * atomicMax, then a one-CTA launch for the accepted prefix and the commit.
+ * Shares the acceptance scratch of the ctx with verify_accept_greedy.
+ */
+verify_status verify_lm_head_accept(verify_ctx* ctx, const verify_q4_weight* W, const uint16_t* x, int k,
+                                    const int32_t* draft, int32_t* result, const verify_gdn_state* states,
+                                    int n_states, struct CUstream_st* stream);
+
 /* ---------------------------------------------------- attention verify */
 
 /*

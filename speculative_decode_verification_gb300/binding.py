@@ -118,6 +118,7 @@ def load():
         "gdn_state_to_host": [p, C.POINTER(GdnState), i, p],
         "gdn_commit_dev": [p, C.POINTER(GdnState), i, p, p],
         "verify_accept_greedy": [p, p, i64, i, i, p, p, C.POINTER(GdnState), i, p],
+        "verify_lm_head_accept": [p, C.POINTER(Q4Weight), p, i, p, p, C.POINTER(GdnState), i, p],
         "q4_gather_experts_k_noalloc": [C.POINTER(Q4Experts), C.POINTER(Q4Experts), p, i64, i, p, i, p, p, p, i,
                                         C.POINTER(Q4Weight), C.POINTER(Q4Weight), p, p, p],
     }
@@ -279,6 +280,15 @@ class Verify:
         self._check(self.lib.verify_accept_greedy(
             self.ctx, _ptr(logits), logits.stride(0), logits.shape[1], k,
             _ptr(draft) if draft is not None and k > 1 else None, _ptr(result),
+            states if n else None, n, self._stream(stream)))
+
+    def lm_head_accept(self, W: Q4Weight, x, k: int, draft, result, states=None, stream=None):
+        """The Q4 LM head with its argmax epilogue, then greedy acceptance and
+        the commit (verify_lm_head_accept): x bf16 [k, H], draft int32
+        [k-1], result int32 [2 + k]."""
+        n = 0 if states is None else len(states)
+        self._check(self.lib.verify_lm_head_accept(
+            self.ctx, C.byref(W), _ptr(x), k, _ptr(draft) if draft is not None and k > 1 else None, _ptr(result),
             states if n else None, n, self._stream(stream)))
 
     def set_layer_events(self, events):

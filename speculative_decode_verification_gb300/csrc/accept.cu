@@ -18,33 +18,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "argmax.cuh"
 #include "common.cuh"
 #include "internal.h"
 
 namespace vk {
 namespace {
-
-__device__ __forceinline__ unsigned long long argmax_key(float f, int v) {
-  uint32_t u = __float_as_uint(f);
-  uint32_t key;
-  if (f != f) {
-    key = 0xFFFFFFFFu;  // NaN ranks above every number
-  } else {
-    if (f == 0.f) u = 0u;  // -0 == +0
-    key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  }
-  return ((unsigned long long)key << 32) | (0xFFFFFFFFu - (uint32_t)v);
-}
-
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
-  return a > b ? a : b;
-}
-
-// Slot that becomes committed when `a` rows of the pending verify stand: the
-// state after the first a rows was written to slot a-1 + (a-1 >= cur).
-__device__ __forceinline__ int committed_slot(int cur, int a) {
-  return a == 0 ? cur : (a - 1) + ((a - 1) >= cur ? 1 : 0);
-}
 
 // Commits `acc` rows on every state, all or nothing (one CTA, all threads).
 __device__ void commit_states(const AcceptArgs& p, int acc) {
@@ -67,6 +46,34 @@ __device__ void commit_states(const AcceptArgs& p, int acc) {
   }
 }
 
+// The k winners (read and reset), the accepted prefix by one warp ballot, the
+// result, then the commit; ticket: also reset the ticket.  One CTA, all threads.
+__device__ void finish(const AcceptArgs& p, bool ticket) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  __shared__ int acc_sh;
+  if (w == 0) {  // lane r < k: row r's winner and draft d_{r+1}, then one ballot
+    int t = 0;
+    bool match = false;
+    if (lane < p.k) {
+      const int d = lane < p.k - 1 ? __ldcg(p.draft + lane) : 0;
+      const unsigned long long b = atomicExch(p.best + lane, 0ull);  // read and reset for the next call
+      t = argmax_index(b);
+      match = lane < p.k - 1 && d == t;
+      p.result[2 + lane] = t;
+    }
+    const int m = __ffs(~__ballot_sync(0xffffffffu, match)) - 1;  // leading drafts that stand
+    const int tm = __shfl_sync(0xffffffffu, t, m);
+    if (lane == 0) {
+      p.result[0] = m + 1;
+      p.result[1] = tm;
+      acc_sh = m + 1;
+      if (ticket) *p.ticket = 0u;
+    }
+  }
+  __syncthreads();
+  if (p.n_states > 0) commit_states(p, acc_sh);
+}
+
 __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptArgs p) {
   constexpr int NW = kAcceptThreads / 32;
   __shared__ unsigned long long warp_best[NW];
@@ -76,6 +83,10 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptArgs
   if (p.V == 0) {  // commit only
     const int acc = __ldcg(p.accepted);
     commit_states(p, acc);
+    return;
+  }
+  if (p.V < 0) {  // the keys were merged by the LM head's argmax epilogue
+    finish(p, false);
     return;
   }
 
@@ -136,28 +147,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(const AcceptArgs
 
   // ---- last CTA: every other CTA's atomicMax happened before its ticket
   __threadfence();
-  __shared__ int acc_sh;
-  if (w == 0) {  // lane r < k: row r's winner and draft d_{r+1}, then one ballot
-    int t = 0;
-    bool match = false;
-    if (lane < p.k) {
-      const int d = lane < p.k - 1 ? __ldcg(p.draft + lane) : 0;
-      const unsigned long long b = atomicExch(p.best + lane, 0ull);  // read and reset for the next call
-      t = (int)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
-      match = lane < p.k - 1 && d == t;
-      p.result[2 + lane] = t;
-    }
-    const int m = __ffs(~__ballot_sync(0xffffffffu, match)) - 1;  // leading drafts that stand
-    const int tm = __shfl_sync(0xffffffffu, t, m);
-    if (lane == 0) {
-      p.result[0] = m + 1;
-      p.result[1] = tm;
-      acc_sh = m + 1;
-      *p.ticket = 0u;
-    }
-  }
-  __syncthreads();
-  if (p.n_states > 0) commit_states(p, acc_sh);
+  finish(p, true);
 }
 
 }  // namespace
@@ -171,7 +161,7 @@ int accept_blocks_per_row(int V, int k, int num_sms) {
 }
 
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
-  const int grid = a.V == 0 ? 1 : a.k * a.blocks_per_row;
+  const int grid = a.V <= 0 ? 1 : a.k * a.blocks_per_row;
   accept_kernel<<<grid, kAcceptThreads, 0, s>>>(a);
   return cudaGetLastError();
 }

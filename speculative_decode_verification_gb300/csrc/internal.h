@@ -37,7 +37,12 @@ struct DenseArgs {
   int* err;
   int N, K, k, dtype;
   int KG, KC, RB;     // groups per row, 256-column chunks per row, 128-row tiles
-  int S;              // K-splits per tile (cluster size, 1..8)
+  int S;              // K-splits per tile (cluster size, 1..16)
+  // Argmax epilogue (the LM head's greedy choice; y unused): per output
+  // column r (block row r0 + r) the 64-bit argmax key over the N outputs is
+  // merged into best[r0 + r] (zero before the first pass).
+  unsigned long long* best;
+  int r0;
 };
 
 // Routed experts.  Both kernels recompute the (cheap, deterministic) routing.
@@ -98,6 +103,8 @@ cudaError_t q4_dense_cluster_limits(int* max_clusters);
 // pdl: launch with programmatic stream serialization (the kernel may start
 // while the previous kernel on the stream runs; see griddep_wait).
 cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s);
+// The same product with the argmax epilogue (one pass of up to 16 rows).
+cudaError_t launch_q4_dense_argmax(const DenseArgs& a, int nt, cudaStream_t s);
 cudaError_t launch_moe(const MoeArgs& a, bool pdl, cudaStream_t s, int* launches);
 // Tiled layout: bytes of E matrices [N, K] (gate_up: tiles pair gate and up rows),
 // and the conversion from the row-major layout.
@@ -139,8 +146,10 @@ constexpr int kAttnMaxM = 512;   // k * (Hq / Hkv) per call
 cudaError_t attn_setup_kernels();
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s, int* launches);
 
-// Greedy acceptance fused with the device commit (V > 0), or the device
-// commit alone of the accepted count *accepted (V == 0, one CTA).
+// Greedy acceptance fused with the device commit (V > 0), the device commit
+// alone of the accepted count *accepted (V == 0, one CTA), or the acceptance
+// and commit from keys already merged in best (V < 0, one CTA: after the LM
+// head's argmax epilogue).
 struct AcceptArgs {
   const float* logits;        // [k, V], row r at logits + r * ld
   long long ld;

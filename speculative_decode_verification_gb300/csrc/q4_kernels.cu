@@ -37,6 +37,7 @@
 //    one partial output per (row, rank)).  A down item starts once every
 //    gate/up item of its unit is counted done.  A second small kernel combines
 //    every row's experts in rank order.
+#include "argmax.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -333,12 +334,51 @@ __device__ __forceinline__ void init_barriers(uint32_t bar_base) {
 
 // ================================================================== dense
 
-// Grid: RB row tiles x S K-splits; the S CTAs of a row tile form one thread
-// block cluster.  CTA s of tile rb accumulates the 256-column chunks
-// [s*KC/S, (s+1)*KC/S); the cluster adds the S partial tiles through
-// distributed shared memory in rank order, rank q finishing the consumer
-// warps w with w % S == q.  S depends only on (N, K, SM count), never on k.
-template <int NT>
+// Argmax epilogue of the dense product (the LM head's greedy choice): each
+// consumer warp takes the largest key of its output rows per column, the CTA
+// merges its warps in shared memory and each column with one 64-bit atomicMax
+// (no fence, no ticket: a one-CTA launch of the acceptance kernel reads the
+// merged keys after this kernel).  Consumer threads only; the keys are those
+// of the fp32 values the plain product would store.
+template <int NT, int MT>
+__device__ void dense_argmax_epilogue(const DenseArgs& a, const float (&acc)[MT][NT][4], const bool (&mine)[MT],
+                                      int tile, const int (&rbase)[MT], int warp, int lane, uint8_t* scratch,
+                                      bool aborted) {
+  constexpr int CW = kDenseWarps, NTH = CW * 32;
+  constexpr uint32_t FULL = 0xffffffffu;
+  const int g = lane >> 2, c = lane & 3;
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(scratch);  // [CW][16]
+  unsigned long long kb[NT][2];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) kb[t][0] = kb[t][1] = 0ull;
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int row = tile * kBM + rbase[m] + g + 8 * (q >> 1);
+        const int col = 8 * t + 2 * c + (q & 1);
+        if (mine[m] && row < a.N && col < a.k) kb[t][q & 1] = umax64(kb[t][q & 1], argmax_key(acc[m][t][q], row));
+      }
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) kb[t][e] = umax64(kb[t][e], __shfl_xor_sync(FULL, kb[t][e], off));
+      if (g == 0) red[warp * 16 + 8 * t + 2 * c + e] = kb[t][e];
+    }
+  named_bar(2, NTH);
+  if (warp == 0 && lane < a.k && !aborted) {
+    unsigned long long mk = 0ull;
+#pragma unroll
+    for (int w = 0; w < CW; ++w) mk = umax64(mk, red[w * 16 + lane]);
+    if (mk) atomicMax(a.best + a.r0 + lane, mk);
+  }
+}
+
+template <int NT, bool ARGMAX = false>
 __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     q4_dense_kernel(const DenseArgs a) {
   using L = Q4Layout<NT>;
@@ -470,7 +510,10 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
     }
     cluster_arrive();  // this CTA has read its peers' partial tiles
   }
-  if (!*abort) {
+  if constexpr (ARGMAX) {
+    // stage 1's space is free (stage 0 may still hold the partial tile peers read)
+    dense_argmax_epilogue<NT, MT>(a, acc, mine, tile, rbase, warp, lane, smem + L::STAGE, *abort != 0);
+  } else if (!*abort) {
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -969,6 +1012,15 @@ cudaError_t q4_setup_kernels(int* dense_ctas_per_sm, int* moe_ctas_per_sm) {
   // clusters of up to 16 CTAs (sizes above 8 are not portable)
   if ((e = cudaFuncSetAttribute(q4_dense_kernel<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1))) return e;
   if ((e = cudaFuncSetAttribute(q4_dense_kernel<2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1))) return e;
+  // the argmax-epilogue instances (LM head): same shape, their occupancy checked alike
+  int argmax_ctas = kQ4CtasPerSm;
+  if ((e = setup_one(q4_dense_kernel<1, true>, TD, dense_smem<1>(), &argmax_ctas))) return e;
+  if ((e = setup_one(q4_dense_kernel<2, true>, TD, dense_smem<2>(), &argmax_ctas))) return e;
+  if ((e = cudaFuncSetAttribute(q4_dense_kernel<1, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
+    return e;
+  if ((e = cudaFuncSetAttribute(q4_dense_kernel<2, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)))
+    return e;
+  if (argmax_ctas < *dense_ctas_per_sm) return cudaErrorInvalidConfiguration;
   *moe_ctas_per_sm = kMoeCtasPerSm;
   if ((e = setup_one(moe_kernel, TG, moe_smem<1>(), moe_ctas_per_sm))) return e;
   if (*dense_ctas_per_sm < 1 || *moe_ctas_per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -1028,6 +1080,23 @@ cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s
   cfg.numAttrs = pdl ? 2 : 1;
   if (nt == 1) return cudaLaunchKernelEx(&cfg, q4_dense_kernel<1>, a);
   return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2>, a);
+}
+
+cudaError_t launch_q4_dense_argmax(const DenseArgs& a, int nt, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.RB * a.S);
+  cfg.blockDim = dim3(Warps<kDenseWarps>::THREADS);
+  cfg.dynamicSmemBytes = nt == 1 ? dense_smem<1>() : dense_smem<2>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (nt == 1) return cudaLaunchKernelEx(&cfg, q4_dense_kernel<1, true>, a);
+  return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2, true>, a);
 }
 
 // The combine kernel follows the routed-expert kernel of the same call, which

@@ -580,6 +580,52 @@ verify_status verify_accept_greedy(verify_ctx* ctx, const float* logits, int64_t
   return VERIFY_OK;
 }
 
+verify_status verify_lm_head_accept(verify_ctx* ctx, const verify_q4_weight* W, const uint16_t* x, int k,
+                                    const int32_t* draft, int32_t* result, const verify_gdn_state* states,
+                                    int n_states, struct CUstream_st* stream) {
+  if (!ctx) return VERIFY_EINVAL;
+  verify_status s;
+  if ((s = use_device(ctx))) return s;
+  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..32%s");
+  if ((s = check_q4(ctx, W, "W"))) return s;
+  if ((s = check_dev(ctx, x, 16, "x")) || (s = check_dev(ctx, result, 4, "result"))) return s;
+  if (k > 1 && (s = check_dev(ctx, draft, 4, "draft"))) return s;
+  if (n_states < 0) return fail(ctx, VERIFY_EINVAL, "n_states < 0%s");
+  if (n_states > 0 && (s = check_dev_states(ctx, states, n_states))) return s;
+  vk::DenseArgs a{};
+  a.tiles = reinterpret_cast<const uint8_t*>(W->packed); a.rt_bytes = rt_bytes(W->k_in);
+  a.err = ctx->err;
+  a.N = W->n_out; a.K = W->k_in; a.dtype = VERIFY_F32;
+  a.KG = a.K / 64; a.KC = (a.KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
+  a.RB = (a.N + vk::kBM - 1) / vk::kBM;
+  a.S = dense_splits(ctx, a.RB, a.KC);  // as q4_qmv_k: the same fp32 outputs
+  a.best = ctx->acc_best;
+  for (int r0 = 0; r0 < k; r0 += VERIFY_PASS_K) {
+    a.k = k - r0 < VERIFY_PASS_K ? k - r0 : VERIFY_PASS_K;
+    a.r0 = r0;
+    a.x = x + (size_t)r0 * a.K;
+    cudaError_t e = vk::launch_q4_dense_argmax(a, a.k <= 8 ? 1 : 2, stream);
+    if (e) return cuda_fail(ctx, e, "verify_lm_head_accept launch");
+    ctx->launches += 1;
+  }
+  // then one CTA: the accepted prefix from the merged keys, the result, the commit
+  vk::AcceptArgs f{};
+  f.V = -1;
+  f.k = k;
+  f.draft = draft;
+  f.result = result;
+  f.dev_state = n_states > 0 ? states[0].dev : nullptr;
+  f.n_states = n_states;
+  f.need_k = k;
+  f.best = ctx->acc_best;
+  f.ticket = ctx->acc_ticket;
+  f.err = ctx->err;
+  cudaError_t e = vk::launch_accept(f, stream);
+  if (e) return cuda_fail(ctx, e, "verify_lm_head_accept finish launch");
+  ctx->launches += 1;
+  return VERIFY_OK;
+}
+
 // ------------------------------------------------------------ attention
 
 // Workspace of one attention call: the rotated queries (hi and lo binary16

@@ -196,13 +196,15 @@ class DeviceStack:
         self.vf.q4_qmv_k(self.lm_head, self.xn, k, lg, B.F32, st)
         return lg
 
-    def verify_select_accept(self, h, k: int, draft, result, stream=None):
+    def verify_select_accept(self, h, k: int, draft, result, stream=None, fused: bool = True):
         """The whole target side of a decode step on the device: the verify
         pass, the final norm and LM head over the full vocabulary, greedy
         acceptance of `draft` (int32 [k-1]) and the commit of every layer.
         `result` (int32 [2 + k]) receives the accepted rows, the next token and
-        the k greedy choices.  Needs vocab > 0 and device-held commits; with
-        graphs, one replay per call."""
+        the k greedy choices.  fused: the LM head's argmax epilogue does the
+        acceptance (verify_lm_head_accept; the logits never reach memory), else
+        the logits are written and verify_accept_greedy reads them.  Needs
+        vocab > 0 and device-held commits; with graphs, one replay per call."""
         import torch
 
         if self.dev_words is None or not self.vocab:
@@ -210,13 +212,18 @@ class DeviceStack:
 
         def enqueue(st):
             self.vf.verify_stack_k(self.layers, self.states, h, k, None, st)
-            lg = self.select(h, k, st)
-            self.vf.accept_greedy(lg, k, draft, result, states=self.states, stream=st)
+            if fused:
+                H = self.sh["H"]
+                self.vf.verify_rmsnorm_k(h, self.final_norm_w, 1e-6, True, H, k, self.xn, B.BF16, st)
+                self.vf.lm_head_accept(self.lm_head, self.xn, k, draft, result, states=self.states, stream=st)
+            else:
+                lg = self.select(h, k, st)
+                self.vf.accept_greedy(lg, k, draft, result, states=self.states, stream=st)
 
         if not self.use_graphs:
             enqueue(stream if stream else torch.cuda.current_stream().cuda_stream)
             return
-        key = ("select", k, h.data_ptr(), None if draft is None else draft.data_ptr(), result.data_ptr())
+        key = ("select", fused, k, h.data_ptr(), None if draft is None else draft.data_ptr(), result.data_ptr())
         g, _ = self._graphs.get(key) or self._capture(key, enqueue)
         run = torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream()
         with torch.cuda.stream(run):

@@ -428,3 +428,67 @@ def test_stack_select_accept_graph_equals_eager_composition(vf):
         w = host(b_st.dev_words)
         assert [int(x) for x in w[:, 0]] == [int(s.cur) for s in a_st.states]
     assert len(b_st._graphs) == 1
+
+
+@pytest.mark.parametrize("V,H,k", [(S.FLASH_VOCAB, 256, 1), (S.FLASH_VOCAB, 256, 9), (S.FLASH_VOCAB, 256, 32),
+                                   (1000, 512, 16), (333, 1024, 5)])
+def test_lm_head_accept_equals_product_then_accept(vf, V, H, k):
+    """verify_lm_head_accept (the LM head with its argmax epilogue) gives bit
+    for bit what q4_qmv_k followed by verify_accept_greedy gives, for
+    several accepted prefixes."""
+    import torch
+
+    from tests.gpu_util import DevQ4
+
+    m = S.q4_matrix(31, f"lmf.{V}.{H}", V, H, centered=True)
+    W = DevQ4(vf, m)
+    x = dev(S.bf16_normal(31, f"lmf.x.{k}", (k, H)))
+    y = torch.zeros((k, V), dtype=torch.float32, device="cuda")
+    vf.q4_qmv_k(W.struct, x, k, y, B.F32)
+    res_a = torch.zeros(2 + k, dtype=torch.int32, device="cuda")
+    res_b = torch.full((2 + k,), -5, dtype=torch.int32, device="cuda")
+    draft = torch.zeros(max(k - 1, 1), dtype=torch.int32, device="cuda")
+    vf.accept_greedy(y, k, None if k == 1 else draft, res_a)
+    torch.cuda.synchronize()
+    t = host(res_a)[2:]
+    for mm in sorted({0, k // 2, k - 1}):
+        d = _drafts(t, mm, V, np.random.default_rng(mm))
+        if k > 1:
+            draft[: k - 1].copy_(torch.from_numpy(d))
+        vf.accept_greedy(y, k, None if k == 1 else draft, res_a)
+        vf.lm_head_accept(W.struct, x, k, None if k == 1 else draft, res_b)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(res_a), host(res_b)), f"m={mm}"
+        assert host(res_b)[0] == mm + 1
+
+
+def test_stack_fused_and_unfused_target_steps_agree(vf):
+    """One graph per step of the whole target side, with the fused LM-head
+    acceptance and with the logits written and read back: the same results,
+    residuals and committed slots, step after step."""
+    import torch
+
+    from speculative_decode_verification_gb300.stack import DeviceStack
+
+    cfg = dict(layers=2, H=256, E=16, T=4, I=256, n_qk_heads=2, n_v_heads=4, d=64, conv_kernel=4)
+    k, V = 9, 50000
+    a_st = DeviceStack(vf, cfg, seed=12, n_slots=k + 1, vocab=V)
+    b_st = DeviceStack(vf, cfg, seed=12, n_slots=k + 1, vocab=V)
+    a_st.to_device()
+    b_st.to_device()
+    h_a = torch.zeros((k, cfg["H"]), dtype=torch.float32, device="cuda")
+    h_b = torch.zeros_like(h_a)
+    draft = torch.zeros(k - 1, dtype=torch.int32, device="cuda")
+    res_a = torch.zeros(2 + k, dtype=torch.int32, device="cuda")
+    res_b = torch.zeros_like(res_a)
+    for step in range(4):
+        h0 = torch.from_numpy(S.f32_normal(12, f"fused.h.{step}", (k, cfg["H"])))
+        h_a.copy_(h0)
+        h_b.copy_(h0)
+        draft.copy_(torch.from_numpy(S.f32_uniform(12, f"fused.d.{step}", (k - 1,), 0, V).astype(np.int32)))
+        a_st.verify_select_accept(h_a, k, draft, res_a, fused=False)
+        b_st.verify_select_accept(h_b, k, draft, res_b, fused=True)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(res_a), host(res_b)), f"step {step}"
+        assert np.array_equal(host(h_a).view(np.uint32), host(h_b).view(np.uint32))
+        assert np.array_equal(host(a_st.dev_words), host(b_st.dev_words))
