@@ -312,6 +312,17 @@ def run_ours(args, cfg):
                 g.replay()
             e1.record()
         torch.cuda.synchronize()
+        # per-step spread: after the timed steps, an event after each of up to
+        # 200 more replays (a graph boundary already orders them)
+        n_pct = max(3, min(args.steps, 200))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_pct + 1)]
+        with torch.cuda.stream(stream):
+            evs[0].record()
+            for i in range(n_pct):
+                g.replay()
+                evs[i + 1].record()
+        torch.cuda.synchronize()
+        step_ms = np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(n_pct)])
         # the routed-expert call's own duration: a second graph of the same step
         # with events around that call in every layer, replayed right after the
         # timed steps (durations averaged over layers and replays)
@@ -344,6 +355,7 @@ def run_ours(args, cfg):
         gdn_bytes = cfg["n_v_heads"] * cfg["d"] ** 2 * 4 * (1 + k) + 3 * sh["C"] * 2 * (1 + k)
         step_bytes = sum(moe_bytes) + L * (dense_bytes + gdn_bytes)
         per_k[k] = {"rows_per_s_per_layer": k * L / (ms * 1e-3) * world, "ms_per_step": ms,
+                    "ms_per_step_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 4) for q in (10, 50, 90)],
                     "layer_us": {n: round(v, 2) for n, v in sub.items()},
                     "distinct_experts_per_layer": float(np.mean(U)),
                     "step_bytes": step_bytes, "step_GBs": step_bytes / (ms * 1e-3) / 1e9}
