@@ -175,6 +175,23 @@ def oracle_layer_step(cfg, k, seed=0, layer=0, weights=None):
     return time.perf_counter() - t, weights
 
 
+def host_cpu():
+    """The host CPU's model and logical core count, read at run time."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    import platform
+
+    return f"{model or platform.processor() or platform.machine()} ({os.cpu_count()} logical cores)"
+
+
 def cpu_baseline(cfg, k):
     from oracle import oracle as O
     O.build()
@@ -182,7 +199,7 @@ def cpu_baseline(cfg, k):
     dt, _ = oracle_layer_step(cfg, k, weights=w)
     return {"value": k / dt, "unit": "verified rows/s per layer", "cores": 1, "kind": "oracle",
             "sample": f"one of the {cfg['layers']} layers at k={k} (full shapes), single-threaded float64 C "
-                      f"oracle, {dt:.2f} s"}
+                      f"oracle, {dt:.2f} s", "host": host_cpu()}
 
 
 def run_reference(args, cfg):
@@ -205,7 +222,8 @@ def run_reference(args, cfg):
             "config": {"workload": WORKLOAD, "k": k, "layers_per_step": 1,
                        "note": "CPU oracle, one layer per step (bounded sample)"},
             "cpu_baseline": {"value": value, "unit": "verified rows/s per layer", "cores": 1, "kind": "oracle",
-                             "sample": f"one layer at k={k} per step, single-threaded float64 C oracle"},
+                             "sample": f"one layer at k={k} per step, single-threaded float64 C oracle",
+                             "host": host_cpu()},
             "e2e": {"value": value, "unit": "verified rows/s per layer", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
