@@ -19,7 +19,11 @@
  * exact integer products, top-k order/ties and softmax identities, the
  * single-expert special case, the delta-rule identities (zero state, unit
  * gates, beta = 0, decay 1/2), conv taps, norms, greedy acceptance
- * (hand-worked cases, numpy's argmax, the serial-decoding identity).
+ * (hand-worked cases, numpy's argmax, the serial-decoding identity), the
+ * attention verify (binary16 rounding against numpy's cast, one-key and
+ * zero-query closed forms, RoPE of one-hot keys, relative-position
+ * invariance, the two-key score gap, k rows against k single-row steps, the
+ * query-head grouping).
  */
 #include <math.h>
 #include <stdint.h>
