@@ -119,23 +119,24 @@ def test_dense_full_size_sampled_rows(vf, N, K):
     vf.synth_q4(packed, scales, biases, (sp, ss, sb), S.SCALE_RANGE, S.BIAS_RANGE)
     Wt = vf.tile(B.q4_weight(packed, scales, biases))
     W = Wt.struct
-    x = S.bf16_normal(0, name + ".x", (9, K))
+    x = S.bf16_normal(0, name + ".x", (32, K))
     rows = np.unique(np.concatenate([[0, N - 1], np.random.default_rng(N + K).integers(0, N, 46)]))
     sub = S.q4_rows(0, name, N, K, rows)
     # the device generator reproduces the host draw bit for bit
     assert np.array_equal(host(packed[rows.tolist()]).view(np.uint32), sub.packed)
     assert np.array_equal(host(scales[rows.tolist()]).view(np.uint16), sub.scales)
     ref = O.q4_qmv(sub.packed, sub.scales, sub.biases, x)
-    for k in S.DENSE_WIDTHS:
+    for k in S.DENSE_WIDTHS + [16, 32]:
         y = torch.zeros((k, N), dtype=torch.float32, device="cuda")
         vf.q4_qmv_k(W, dev(x[:k]), k, y, B.F32)
         torch.cuda.synchronize()
         assert_close(host(y)[:, rows], ref[:k], what=f"{name} k={k}")
-        if k == 9:
+        if k in (9, 32):  # a row of the second column block, and one of the second pass
+            r = k - 1
             y1 = torch.zeros((1, N), dtype=torch.float32, device="cuda")
-            vf.q4_qmv_k(W, dev(x[8:9]), 1, y1, B.F32)
+            vf.q4_qmv_k(W, dev(x[r:r + 1]), 1, y1, B.F32)
             torch.cuda.synchronize()
-            assert torch.equal(y[8], y1[0])
+            assert torch.equal(y[r], y1[0])
 
 
 def test_argument_errors_are_reported_before_launch(vf):
