@@ -192,38 +192,63 @@ def host_cpu():
     return f"{model or platform.processor() or platform.machine()} ({os.cpu_count()} logical cores)"
 
 
-def cpu_baseline(cfg, k):
+def oracle_mode(threaded):
+    """Selects the oracle build (OpenMP over all host cores, or the plain
+    single-threaded one); returns the threads it uses (None: no OpenMP build)."""
     from oracle import oracle as O
     O.build()
-    _, w = oracle_layer_step(cfg, k)   # draws the layer's weights and the routed experts (untimed)
-    dt, _ = oracle_layer_step(cfg, k, weights=w)
-    return {"value": k / dt, "unit": "verified rows/s per layer", "cores": 1, "kind": "oracle",
-            "sample": f"one of the {cfg['layers']} layers at k={k} (full shapes), single-threaded float64 C "
-                      f"oracle, {dt:.2f} s", "host": host_cpu()}
+    if threaded and O.build_threaded() is None:
+        return None
+    return O.use_threads(threaded)
+
+
+def cpu_baseline(cfg, k, runs=5):
+    """One full-shape layer at width k on the oracle, both modes: the median of
+    `runs` timed runs after one warm-up (which also draws the layer's weights
+    and routed experts, untimed)."""
+    _, w = oracle_layer_step(cfg, k)
+    out = {}
+    for threaded in (False, True):
+        n = oracle_mode(threaded)
+        if n is None:
+            continue
+        oracle_layer_step(cfg, k, weights=w)
+        ts = [oracle_layer_step(cfg, k, weights=w)[0] for _ in range(runs)]
+        out[threaded] = (n, float(np.median(ts)))
+    oracle_mode(False)
+    n1, t1 = out[False]
+    single = {"value": k / t1, "unit": "verified rows/s per layer", "cores": 1, "ms_per_layer": t1 * 1e3}
+    nt, tt = out.get(True, out[False])
+    return {"value": k / tt, "unit": "verified rows/s per layer", "cores": nt, "kind": "oracle",
+            "sample": f"one of the {cfg['layers']} layers at k={k} (full shapes), float64 C oracle "
+                      f"({'OpenMP over output rows, ' + str(nt) + ' threads' if True in out else 'single thread'}), "
+                      f"median of {runs} runs after one warm-up, {tt * 1e3:.0f} ms per layer",
+            "statistic": f"median of {runs}", "host": host_cpu(), "single_thread": single}
 
 
 def run_reference(args, cfg):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from oracle import oracle as O
-    O.build()
     k = args.k
-    _, w = oracle_layer_step(cfg, k)
+    _, w = oracle_layer_step(cfg, k)    # draws the weights and routed experts (untimed)
+    nt = oracle_mode(True) or oracle_mode(False)
     for _ in range(args.warmup):
         oracle_layer_step(cfg, k, weights=w)
     ts = [oracle_layer_step(cfg, k, weights=w)[0] for _ in range(args.steps)]
-    step = float(np.mean(ts))
+    step = float(np.median(ts))
     value = k / step
+    sample = (f"one full-shape layer at k={k} per step, float64 C oracle on {nt} host threads "
+              f"(OpenMP over output rows), median of {args.steps} steps")
     line = {"metric": "verified rows/s per layer", "value": value, "unit": "verified rows/s per layer",
             "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "ms_per_step": step * 1e3, "ms_per_step_mean": float(np.mean(ts)) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "k": k, "layers_per_step": 1,
                        "note": "CPU oracle, one layer per step (bounded sample)"},
-            "cpu_baseline": {"value": value, "unit": "verified rows/s per layer", "cores": 1, "kind": "oracle",
-                             "sample": f"one layer at k={k} per step, single-threaded float64 C oracle",
-                             "host": host_cpu()},
+            "cpu_baseline": {"value": value, "unit": "verified rows/s per layer", "cores": nt, "kind": "oracle",
+                             "sample": sample, "host": host_cpu()},
             "e2e": {"value": value, "unit": "verified rows/s per layer", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -231,6 +256,22 @@ def run_reference(args, cfg):
 
 
 # ------------------------------------------------------------------ ours
+
+def time_steps(graph, stream, steps):
+    """Mean ms per replay of `graph` over `steps` back-to-back replays, from
+    CUDA events recorded on the replay stream (synchronised on both sides)."""
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(steps):
+            graph.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
 
 def run_ours(args, cfg):
     import torch
@@ -254,8 +295,8 @@ def run_ours(args, cfg):
     stream = torch.cuda.Stream()
     widths = sorted(set([int(w) for w in args.widths.split(",") if w] + [args.k]))
     hbm, peak_kind = peaks()
-    per_k, head = {}, None
-    for k in widths:
+    per_k, head, timed = {}, None, {}
+    for k in widths:  # set-up and untimed measurements per width; the timed trials follow
         h0 = torch.from_numpy(S.f32_normal(0, f"bench.h{k}", (k, H))).cuda()
         h = torch.empty_like(h0)
         idx_all = torch.zeros((L, k, T), dtype=torch.int32, device="cuda")
@@ -314,24 +355,9 @@ def run_ours(args, cfg):
             for _ in range(args.warmup):
                 g.replay()
         torch.cuda.synchronize()
-        barrier(world)
-        sampler = ClockSampler(local) if k == args.k else None
-        if sampler:  # nvidia-smi needs a moment to start: keep the GPU busy meanwhile (untimed)
-            sampler.start()
-            t_w = time.perf_counter()
-            with torch.cuda.stream(stream):
-                while time.perf_counter() - t_w < 0.6:
-                    g.replay()
-                    stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record()
-            for _ in range(args.steps):
-                g.replay()
-            e1.record()
-        torch.cuda.synchronize()
-        # per-step spread: after the timed steps, an event after each of up to
-        # 200 more replays (a graph boundary already orders them)
+        timed[k] = g
+        # per-step spread: an event after each of up to 200 replays (a graph
+        # boundary already orders them)
         n_pct = max(3, min(args.steps, 200))
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_pct + 1)]
         with torch.cuda.stream(stream):
@@ -342,8 +368,8 @@ def run_ours(args, cfg):
         torch.cuda.synchronize()
         step_ms = np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(n_pct)])
         # the routed-expert call's own duration: a second graph of the same step
-        # with events around that call in every layer, replayed right after the
-        # timed steps (durations averaged over layers and replays)
+        # with events around that call in every layer (durations averaged over
+        # layers and replays)
         evm = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
         with torch.cuda.stream(stream):
             for row in evm:
@@ -359,31 +385,55 @@ def run_ours(args, cfg):
             stream.synchronize()
             moe_samples += [evm[l][0].elapsed_time(evm[l][1]) * 1e3 for l in range(L)]
         del gm
-        clocks = sampler.stop() if sampler else None
-        barrier(world)
-        ms = e0.elapsed_time(e1) / args.steps
-        ms = max_over_ranks(ms, world)
-        st, code = vf.device_status()
-        if st != B.OK:
-            raise SystemExit(f"device error {code} during the benchmark")
         moe_timed_us = float(np.mean(moe_samples))
         U = [len(np.unique(idx[l].cpu().numpy())) for l in range(L)]
         moe_bytes = [(u + 1) * EXPERT_BYTES(H, sh["I"]) + k * H * (2 + 8) + k * (sh["E"] + 1) * 4 for u in U]
         dense_bytes = int(0.5625 * (sh["NP"] * H + H * sh["Z"] + (sh["E"] + 1) * H))
         gdn_bytes = cfg["n_v_heads"] * cfg["d"] ** 2 * 4 * (1 + k) + 3 * sh["C"] * 2 * (1 + k)
         step_bytes = sum(moe_bytes) + L * (dense_bytes + gdn_bytes)
-        per_k[k] = {"rows_per_s_per_layer": k * L / (ms * 1e-3) * world, "ms_per_step": ms,
-                    "ms_per_step_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 4) for q in (10, 50, 90)],
+        per_k[k] = {"ms_per_step_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 4) for q in (10, 50, 90)],
                     "layer_us": {n: round(v, 2) for n, v in sub.items()},
                     "distinct_experts_per_layer": float(np.mean(U)),
-                    "step_bytes": step_bytes, "step_GBs": step_bytes / (ms * 1e-3) / 1e9}
+                    "step_bytes": step_bytes}
         per_k[k]["experts_us_timed"] = moe_timed_us
         if k == args.k:
             moe_us = moe_timed_us
             achieved = float(np.mean(moe_bytes)) / (moe_us * 1e-6) / 1e9
-            head = dict(ms=ms, clocks=clocks, U=float(np.mean(U)), moe_us=moe_us, moe_bytes=float(np.mean(moe_bytes)),
-                        achieved=achieved)
-        del g
+            head = dict(U=float(np.mean(U)), moe_us=moe_us, moe_bytes=float(np.mean(moe_bytes)), achieved=achieved)
+    # The timed trials, back to back with the clock sampler running: the
+    # widths ascending, descending, then ascending again (the pages' protocol
+    # reverses the order on the second trial).  Each trial of a width is W
+    # warm-up replays and exactly `steps` timed replays; the headline keeps
+    # trial 1, and each width also reports its three trials and their median.
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_w = time.perf_counter()  # nvidia-smi needs a moment to start: keep the GPU busy meanwhile (untimed)
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t_w < 0.6:
+            timed[widths[0]].replay()
+            stream.synchronize()
+    for order in (widths, widths[::-1], widths):
+        for k in order:
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    timed[k].replay()
+            torch.cuda.synchronize()
+            barrier(world)
+            per_k[k].setdefault("ms_per_step_trials", []).append(
+                max_over_ranks(time_steps(timed[k], stream, args.steps), world))
+    clocks = sampler.stop()
+    for k in widths:
+        tr = per_k[k]["ms_per_step_trials"]
+        ms, ms3 = tr[0], float(np.median(tr))
+        per_k[k].update({"rows_per_s_per_layer": k * L / (ms * 1e-3) * world, "ms_per_step": ms,
+                         "step_GBs": per_k[k]["step_bytes"] / (ms * 1e-3) / 1e9, "ms_per_step_median3": ms3,
+                         "rows_per_s_per_layer_median3": k * L / (ms3 * 1e-3) * world})
+    head["ms"] = per_k[args.k]["ms_per_step"]
+    head["clocks"] = clocks
+    st, code = vf.device_status()
+    if st != B.OK:
+        raise SystemExit(f"device error {code} during the benchmark")
+    del timed
     # ---- end to end through the public API: host buffers, copies inside the timed region
     k = args.k
     hh = torch.from_numpy(S.f32_normal(0, f"bench.h{k}", (k, H))).pin_memory()
@@ -430,7 +480,7 @@ def run_ours(args, cfg):
         "roofline": {"bound": "hbm", "achieved": head["achieved"], "peak": hbm, "unit": "GB/s",
                      "frac": head["achieved"] / hbm, "traffic": moe_traffic(head["moe_bytes"]),
                      "traffic_unit": "DRAM bytes per launch (ncu read + write of a 2-layer capture, scaled)",
-                     "kernel": "q4_gather_experts_k (fused routed gate/up+SwiGLU and down kernel, then the combine kernel)",
+                     "kernel": "q4_gather_experts_k (routing kernel, fused routed gate/up+SwiGLU and down kernel, combine kernel)",
                      "bytes_per_launch": head["moe_bytes"], "us_per_launch": head["moe_us"],
                      "distinct_experts": head["U"], "peak_kind": peak_kind},
         "clocks": head["clocks"],
@@ -781,7 +831,7 @@ def run_kernels(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--k", type=int, default=9, help="verify width of the headline number")

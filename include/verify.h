@@ -635,15 +635,18 @@ verify_status verify_set_layer_events(verify_ctx* ctx, void* const* events, int 
  * scratch is allocated), so this call needs none.
  *
  * It computes exactly what q4_gather_experts_k computes, with the same
- * arguments (no ctx) plus `device_error`: an optional device int32 the caller
- * owns, set to 1 if a pipeline wait timed out (NULL: not reported).  The
+ * arguments (no ctx) and the same shape rules and status codes, plus
+ * `device_error`: an optional device int32 the caller owns, set to 1 if a
+ * pipeline wait timed out.  With `device_error` NULL a timeout is not
+ * reported anywhere, and idx_out, w_out and y are then undefined: callers
+ * that must know pass a word (and zero it before the call).  The
  * caller passes all inputs and outputs; the kernels' scratch (SwiGLU rows,
  * per-rank partial outputs, an error word, the expert kernel's item counter
  * and per-unit counts) lives in one array of
  * VERIFY_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU
  * that loads the library holds until the process exits.
  *   - Limit: k <= VERIFY_PASS_K (one pass); k*(T+s)*I*2 + k*(T+s)*H*4 bytes (s = 1 with a shared expert, each
- *     part rounded up to 256) plus 4352 must fit the array; larger calls
+ *     part rounded up to 256) plus 5376 must fit the array; larger calls
  *     return VERIFY_EUNSUPPORTED before anything is enqueued.
  *   - The first call on each device sets that device up (resolves the array's
  *     device address, sets the kernels' launch attributes); make that first

@@ -24,11 +24,36 @@
  * zero-query closed forms, RoPE of one-hot keys, relative-position
  * invariance, the two-key score gap, k rows against k single-row steps, the
  * query-head grouping).
+ *
+ * Timing only: compiled with -fopenmp (a second library beside the plain
+ * one), the output rows of each Q4 product are spread over the host cores.
+ * Every output is still the same sequential float64 sum, so that build gives
+ * bit-identical results; the plain build is single-threaded.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the products may use (1 in the plain build). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+static int thread_index(void) {
+#ifdef _OPENMP
+  return omp_get_thread_num();
+#else
+  return 0;
+#endif
+}
 
 /* ------------------------------------------------------------ bf16 helpers */
 
@@ -89,9 +114,12 @@ static double q4_weight(const uint32_t* packed, const uint16_t* scales,
 int oracle_q4_qmv(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases,
                   int n_out, int k_in, const uint16_t* x, int64_t ldx, int k, double* y) {
   if (k_in % 64 != 0 || n_out < 0 || k < 0) return 1;
-  double* w = (double*)malloc(sizeof(double) * (size_t)k_in);
-  if (!w) return 2;
+  /* one dequantised row per thread */
+  double* w_all = (double*)malloc(sizeof(double) * (size_t)k_in * (size_t)oracle_num_threads());
+  if (!w_all) return 2;
+#pragma omp parallel for schedule(static)
   for (int64_t n = 0; n < n_out; ++n) {
+    double* w = w_all + (size_t)thread_index() * (size_t)k_in;
     for (int c = 0; c < k_in; ++c) w[c] = q4_weight(packed, scales, biases, k_in, n, c);
     for (int r = 0; r < k; ++r) {
       double acc = 0.0;
@@ -99,7 +127,7 @@ int oracle_q4_qmv(const uint32_t* packed, const uint16_t* scales, const uint16_t
       y[(int64_t)r * n_out + n] = acc;
     }
   }
-  free(w);
+  free(w_all);
   return 0;
 }
 

@@ -19,24 +19,52 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
+LIB_OMP = os.path.join(HERE, "liboracle_omp.so")  # the same source with -fopenmp, for timing only
 
-_lib = None
+_libs = {}
+_threaded = False
+
+
+def _compile(out, extra):
+    if not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(SRC):
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", *extra,
+                               "-o", tmp, SRC, "-lm"])
+        os.replace(tmp, out)
+    return out
 
 
 def build(force: bool = False) -> str:
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
-        tmp = LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-                               "-o", tmp, SRC, "-lm"])
-        os.replace(tmp, LIB)
-    return LIB
+    if force:
+        for f in (LIB, LIB_OMP):
+            if os.path.exists(f):
+                os.remove(f)
+    return _compile(LIB, [])
+
+
+def build_threaded():
+    """The OpenMP build (None if this host's gcc cannot build it)."""
+    try:
+        return _compile(LIB_OMP, ["-fopenmp"])
+    except (subprocess.CalledProcessError, OSError):
+        return None
+
+
+def use_threads(on: bool) -> int:
+    """Timing only: route every call below through the OpenMP build (on) or
+    the plain single-threaded one; returns the threads the products use.
+    Results are bit-identical either way."""
+    global _threaded
+    if on and build_threaded() is None:
+        raise RuntimeError("the OpenMP build of the oracle is not available on this host")
+    _threaded = bool(on)
+    return int(lib().oracle_num_threads())
 
 
 def lib():
-    global _lib
-    if _lib is None:
-        build()
-        L = C.CDLL(LIB)
+    key = "omp" if _threaded else "plain"
+    if key not in _libs:
+        L = C.CDLL(build_threaded() if _threaded else build())
         p = C.c_void_p
         i, i64, d = C.c_int, C.c_int64, C.c_double
         L.oracle_q4_qmv.argtypes = [p, p, p, i, i, p, i64, i, p]
@@ -52,11 +80,13 @@ def lib():
         L.oracle_round_f16.restype = C.c_uint16
         L.oracle_round_bf16.argtypes = [d]
         L.oracle_round_bf16.restype = C.c_uint16
+        L.oracle_num_threads.argtypes = []
         for f in ("oracle_q4_qmv", "oracle_route_topk", "oracle_gather_experts",
-                  "oracle_gdn_verify", "oracle_rmsnorm", "oracle_accept_greedy", "oracle_attn_verify"):
+                  "oracle_gdn_verify", "oracle_rmsnorm", "oracle_accept_greedy", "oracle_attn_verify",
+                  "oracle_num_threads"):
             getattr(L, f).restype = C.c_int
-        _lib = L
-    return _lib
+        _libs[key] = L
+    return _libs[key]
 
 
 def _ptr(a):

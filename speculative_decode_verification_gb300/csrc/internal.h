@@ -19,6 +19,11 @@ constexpr int kMaxSplits = 16;      // K-splits of a dense row tile (one cluster
 constexpr int kMoeCtasPerSm = 4;   // routed-expert kernel: 8 activation rows per stage, two stages
 constexpr int kMoeStages = 2;
 constexpr int kMoeUnits = 2 * 512 + 2;  // work units of one call: (expert, chunk of 8 rows), at most
+constexpr int kMoeSmSlots = 256;        // per-SM arrival counters of the routed-expert kernel (SM ids below this)
+// Scheduling words of the routed-expert kernel, zero between calls: the
+// gate/up item counter, the down item counter, one arrival counter per SM,
+// then one gate/up tile count per unit.
+constexpr int kMoeSchedWords = 2 + kMoeSmSlots + kMoeUnits;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 
@@ -58,16 +63,24 @@ struct MoeArgs {
   long long gu_rt_bytes, dn_rt_bytes;
   uint16_t* hbuf;             // scratch [k, TS, I] bf16 (TS = T + has_shared)
   float* part;                // scratch [k, TS, H] fp32
-  int* work;                  // scratch: next work item (0 before a call; the combine kernel resets it)
-  int* done;                  // scratch [kMoeUnits]: gate/up tiles written per unit (reset likewise)
+  int* work;                  // scratch [kMoeSchedWords] (zero before a call; the combine kernel resets it):
+                              // gate/up counter, down counter, per-SM arrivals, then the unit counts
+  int* done;                  // = work + 2 + kMoeSmSlots: gate/up tiles written per unit
   int32_t* idx_out;
   float* w_out;
   void* y;
   int* err;
   int E, T, H, I, k, dtype;
   int has_shared;
-  int G;
+  int G;                      // CTAs of the routed-expert kernel
+  int n_sm;                   // SMs of the GPU
 };
+
+// Shape rules of the routed-expert call, shared by q4_gather_experts_k and
+// its no-allocation twin so that both accept the same calls: 0 (fine) or the
+// verify_status to return, with a message.
+int moe_shape_status(int k, int max_k, int E_gate_up, int E_down, int top_k, int gu_n_out, int gu_k_in,
+                     int dn_n_out, int dn_k_in, const char** msg);
 
 // State slots: S_slots[s] fp32 [Hv, dv, dk], tail_slots[s] bf16 [W-1, C].  The
 // kernel reads slot cur and writes the state after row r to slot r + (r >= cur),

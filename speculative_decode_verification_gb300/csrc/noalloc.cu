@@ -10,7 +10,7 @@ namespace {
 
 // Scratch of the routed-expert kernels: SwiGLU rows [k, T+1, I] bf16, per-rank
 // partial outputs [k, T+1, H] fp32, an error word and the work-scheduling
-// counters.  Every GPU that loads the library holds it until the process
+// words (item counters, per-SM arrival counters, per-unit counts).  Every GPU that loads the library holds it until the process
 // exits.  All calls on one device share it.
 constexpr size_t kScratchBytes = VERIFY_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
@@ -85,14 +85,16 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   verify_status s = setup_device(dev, &d);
   if (s) return s;
 
-  // ---- arguments (all checked before anything is enqueued)
-  if (!gate_up || !down || k < 1 || k > VERIFY_PASS_K) return k < 1 || k > VERIFY_PASS_K ? VERIFY_EUNSUPPORTED : VERIFY_EINVAL;
+  // ---- arguments (all checked before anything is enqueued); the shape rules
+  // are those of q4_gather_experts_k, with k limited to one pass
+  if (!gate_up || !down) return VERIFY_EINVAL;
   const int E = gate_up->n_experts;
-  if (E < 1 || E > vk::kMaxExperts || down->n_experts != E) return VERIFY_EUNSUPPORTED;
-  if (top_k < 1 || top_k > vk::kMaxTopK || top_k > E) return VERIFY_EUNSUPPORTED;
+  const char* why = "";
+  if (int rule = vk::moe_shape_status(k, VERIFY_PASS_K, E, down->n_experts, top_k, gate_up->w.n_out,
+                                      gate_up->w.k_in, down->w.n_out, down->w.k_in, &why))
+    return (verify_status)rule;
   if (!valid_q4(&gate_up->w, VERIFY_Q4_TILED_GATE_UP) || !valid_q4(&down->w, VERIFY_Q4_TILED)) return VERIFY_EINVAL;
   const int H = gate_up->w.k_in, I = gate_up->w.n_out / 2;
-  if (gate_up->w.n_out != 2 * I || down->w.n_out != H || down->w.k_in != I || I % 64 != 0) return VERIFY_EINVAL;
   if (logits_ld < E) return VERIFY_EINVAL;
   if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16 && dtype_out != VERIFY_F32_ADD) return VERIFY_EINVAL;
   if (!device_memory(logits, 4) || !device_memory(x, 16) || !device_memory(idx_out, 4) || !device_memory(w_out, 4) ||
@@ -113,7 +115,7 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   const int TS = top_k + (n_shared ? 1 : 0);
   const size_t hbuf_bytes = round256((size_t)k * TS * I * sizeof(uint16_t));
   const size_t part_bytes = round256((size_t)k * TS * H * sizeof(float));
-  const size_t word_bytes = round256((size_t)(2 + vk::kMoeUnits) * sizeof(int));  // error word, work counter, unit counts
+  const size_t word_bytes = round256((size_t)(1 + vk::kMoeSchedWords) * sizeof(int));  // error word, scheduling words
   if (hbuf_bytes + part_bytes + word_bytes > kScratchBytes) return VERIFY_EUNSUPPORTED;
   unsigned char* base = d->scratch;
   int* err_word = reinterpret_cast<int*>(base + hbuf_bytes + part_bytes);
@@ -132,15 +134,16 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   a.hbuf = reinterpret_cast<uint16_t*>(base);
   a.part = reinterpret_cast<float*>(base + hbuf_bytes);
   a.work = err_word + 1;
-  a.done = err_word + 2;
+  a.done = a.work + 2 + vk::kMoeSmSlots;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y;
   a.err = device_error ? device_error : err_word;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
   a.G = d->moe_ctas_per_sm * d->num_sms;
-  // The error word and the scheduling counters must start at zero: a previous
+  a.n_sm = d->num_sms;
+  // The error word and the scheduling words must start at zero: a previous
   // call may have stopped on a device error and left them set.
-  if (cudaMemsetAsync(err_word, 0, (size_t)(2 + vk::kMoeUnits) * sizeof(int), stream) != cudaSuccess)
+  if (cudaMemsetAsync(err_word, 0, (size_t)(1 + vk::kMoeSchedWords) * sizeof(int), stream) != cudaSuccess)
     return VERIFY_ECUDA;
   int launched = 0;
   if (vk::launch_moe(a, false, stream, &launched) != cudaSuccess) return VERIFY_ECUDA;

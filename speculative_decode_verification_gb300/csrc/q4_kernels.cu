@@ -30,13 +30,16 @@
 //    CTAs of a tile form a thread block cluster and add their partial tiles
 //    through distributed shared memory in rank order (no global scratch, no
 //    atomics).
-//  * Routed MoE: four CTAs per SM, two stages of 8 activation rows.  One
-//    kernel routes every row in every CTA, then works through items: first
-//    the gate/up items (expert, row chunk, 64 gate + 64 up rows; SwiGLU into
-//    the h rows), then the down items (expert, row chunk, 128 output rows;
+//  * Routed MoE: a one-CTA kernel routes every row (a warp per row) and
+//    writes the routes.  Then four CTAs per SM, two stages of 8 activation
+//    rows: each CTA reads the routes, builds the list of work units and works
+//    through items: first the gate/up items (expert, row chunk, 64 gate + 64
+//    up rows; SwiGLU into the h rows), then the down items (expert, row chunk, 128 output rows;
 //    one partial output per (row, rank)).  A down item starts once every
-//    gate/up item of its unit is counted done.  A second small kernel combines
-//    every row's experts in rank order.
+//    gate/up item of its unit is counted done; the items come from two
+//    in-order counters such that every such wait ends without assuming
+//    that all CTAs are resident.  A second small kernel combines every row's
+//    experts in rank order.
 #include "argmax.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -83,7 +86,6 @@ struct RouteSmem {
   int16_t ulist[kMaxExperts];      // distinct selected experts, ascending
   int16_t vlist[2 * kMaxExperts + 2];  // work units: expert slot u (< U, or U = shared) | row chunk << 12
   int32_t idx[16 * kMaxTopK];      // [r][j]
-  float w[16 * kMaxTopK];          // [r][j]
   int U;
   int V;
 };
@@ -533,10 +535,8 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
 
 // ================================================================== MoE
 
-// Top-T routing of every row, recomputed by each CTA (deterministic):
-// descending logit, equal logits -> lower index; weights = softmax over the T
-// selected logits (fp32).  Then the distinct selected experts in ascending
-// order, per expert the bitmask of rows, and the work units.
+// Top-T routing (deterministic): descending logit, equal logits -> lower
+// index; weights = softmax over the T selected logits (fp32).
 //
 // One warp takes R rows at once, interleaved so that their latencies overlap.
 // A logit becomes an order-preserving key (0 = no expert; -0 counts as +0).
@@ -546,8 +546,8 @@ __global__ void __launch_bounds__(Warps<kDenseWarps>::THREADS, kQ4CtasPerSm)
 // expert index; the winning lane shifts its list and, once its four are taken,
 // rescans its remaining keys (rare).
 template <int R>
-__device__ __forceinline__ void route_warp_rows(const float* logits, long long ld, int E, int T, RouteSmem* rs,
-                                                const int (&row)[R], int lane) {
+__device__ __forceinline__ void route_warp_rows(const float* logits, long long ld, int E, int T, const int (&row)[R],
+                                                int lane, int (&e_out)[R], float (&w_out)[R]) {
   constexpr int NI = kMaxExperts / 32;
   constexpr uint32_t FULL = 0xffffffffu;
   uint32_t key[R][NI];
@@ -630,37 +630,48 @@ __device__ __forceinline__ void route_warp_rows(const float* logits, long long l
   }
 #pragma unroll
   for (int q = 0; q < R; ++q) {
-    if (row[q] < 0) continue;
     const float top = __shfl_sync(FULL, myv[q], 0);
     const float ex = lane < T ? expf(myv[q] - top) : 0.f;
     float sum = ex;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(FULL, sum, off);
     sum = __shfl_sync(FULL, sum, 0);
-    if (lane < T) {
-      rs->idx[row[q] * kMaxTopK + lane] = mye[q];
-      rs->w[row[q] * kMaxTopK + lane] = ex / sum;
-      atomicOr(&rs->mask[mye[q]], 1u << row[q]);
-    }
+    e_out[q] = mye[q];
+    w_out[q] = ex / sum;
   }
 }
 
-// Routes rows 0 .. k-1 into rs (every thread of the CTA calls it, after
-// rs->mask has been zeroed and a CTA barrier; ends with __syncthreads).  Warp
-// w takes rows w and w + nwarps of each group of 2 nwarps rows, so up to ten
-// rows need a single pass.
-__device__ void route_rows(const float* logits, long long ld, int E, int T, int k, int has_shared, RouteSmem* rs) {
-  constexpr int R = 2;
+// The routing of a call, once: warp r routes row r (up to 16 rows) and lane
+// j < T writes the row's j-th expert and weight to idx_out / w_out, which the
+// expert kernel and the combine then read.
+__global__ void __launch_bounds__(32 * 16) moe_route_kernel(const MoeArgs a) {
+  griddep_wait();  // the routing logits come from the kernel before
+  griddep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= a.k) return;
+  const int row[1] = {warp};
+  int e[1];
+  float w[1];
+  route_warp_rows<1>(a.logits, a.logits_ld, a.E, a.T, row, lane, e, w);
+  if (lane < a.T) {
+    a.idx_out[warp * a.T + lane] = e[0];
+    a.w_out[warp * a.T + lane] = w[0];
+  }
+}
+
+// Reads the routes of rows 0 .. k-1 (idx, [k, T], written by the routing
+// kernel) into rs: per row its experts, per expert the bitmask of its rows.
+// Then one pass over the masks gives the distinct experts and the work units.
+// Every thread of the CTA calls it, after rs->mask has been zeroed and a CTA
+// barrier; it ends with __syncthreads.
+__device__ void load_routes(const int32_t* idx, int T, int k, int has_shared, RouteSmem* rs) {
   const int tid = threadIdx.x, nthr = blockDim.x;
-  const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
-  for (int base = 0; base < k; base += R * nwarps) {
-    int row[R];
-#pragma unroll
-    for (int q = 0; q < R; ++q) {
-      const int r = base + warp + q * nwarps;
-      row[q] = r < k ? r : -1;
-    }
-    if (row[0] >= 0) route_warp_rows<R>(logits, ld, E, T, rs, row, lane);
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int t = tid; t < k * T; t += nthr) {
+    const int r = t / T, j = t - r * T;
+    const int e = __ldcg(idx + t);  // L2: written by the kernel before
+    rs->idx[r * kMaxTopK + j] = e;
+    atomicOr(&rs->mask[e], 1u << r);
   }
   __syncthreads();
   if (warp == 0) {
@@ -805,9 +816,8 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
   const float sg = live && a.has_shared ? __ldcg(a.shared_logit + (long long)r * a.logits_ld) : 0.f;
   griddep_wait();
   griddep_launch();
-  if (blockIdx.x == 0) {  // the routed-expert kernel is done: reset its work counter and unit counts
-    for (int i = threadIdx.x; i < kMoeUnits; i += blockDim.x) a.done[i] = 0;
-    if (threadIdx.x == 0) *a.work = 0;
+  if (blockIdx.x == 0) {  // the routed-expert kernel is done: reset its counters and unit counts
+    for (int i = threadIdx.x; i < kMoeSchedWords; i += blockDim.x) a.work[i] = 0;
   }
   if (!live) return;
   const int TS = a.T + a.has_shared;
@@ -829,8 +839,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
 }
 
 // The routed-expert products as one persistent kernel (a second kernel, the
-// combine, follows).  Work items, in order: CTA b takes item b first, later
-// items come from a global counter (item G, G + 1, ...):
+// combine, follows).  Work items:
 //   [0, n_gu)         gate/up items (unit v, 64 outputs of I): gate rows and
 //                     up rows of the same outputs go to the same warp, the
 //                     epilogue applies SwiGLU and writes h (bf16) for the
@@ -840,9 +849,21 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
 //                     done[v] == I / 64, all gate/up tiles of the unit.
 // A unit is (distinct expert or the shared expert, chunk of up to 8 of its
 // rows).  Items are unit-major: concurrent CTAs stream consecutive slices of
-// one expert.  Every gate/up item comes before every down item, and each is
-// held by a running CTA that depends on nothing to finish it, so every wait
-// of a down item ends (bounded).
+// one expert.  Gate/up items come in order from one counter, down items from
+// a second; a CTA draws from the gate/up counter while it has items, except
+// that its first draw may go to the down counter: only the first
+// ceil(est / n_sm) CTAs to arrive on an SM start on a gate/up item (est: an
+// upper bound of the gate/up item count), so that when gate/up items are
+// fewer than the CTAs they fall on distinct SMs.  The first CTA on every SM
+// always starts on the gate/up counter.
+// Progress without co-residency: a gate/up item waits for nothing.  A down
+// item of unit v waits for v's gate/up items; each of those is claimed by a
+// CTA that is running (claims happen at run time) or unclaimed.  If one is
+// unclaimed, the gate/up counter is not exhausted, and the first CTA of the
+// waiting CTA's SM (which arrived before it, so it runs) still draws from
+// that counter: it never waits while gate/up items remain.  So every
+// gate/up item is eventually claimed and done, and every wait ends, however
+// many CTAs are resident (bounded waits besides).
 __device__ __forceinline__ void moe_decode(const MoeArgs& a, const RouteSmem* rs, int item, int n_gu, int ntg,
                                            int ntd, bool& gu, int& v, int& u, int& rc, int& tile, int& nb) {
   gu = item < n_gu;
@@ -873,31 +894,49 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
   init_barriers<CW, ST>(bar_base);
   for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) rs->mask[e] = 0u;  // shared memory only
   __syncthreads();
-  griddep_wait();  // the routing logits come from the kernel before
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The first draw: this CTA's arrival slot on its SM, then the gate/up or
+  // the down counter (read as an item once the routes give n_gu).  Issued
+  // before the dependency wait, so that the two atomics' latency overlaps it:
+  // the scheduling words are touched only by this kernel and its combine,
+  // and the combine that last reset them ran at least two kernels back.
+  bool first_gu = true;
+  int first_raw = 0;
+  if (warp == CW && lane == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const int est = (min(a.k * a.T, a.E) + a.has_shared) * (a.I / 64);
+    if (smid < (unsigned)kMoeSmSlots) first_gu = (long long)atomicAdd(a.work + 2 + smid, 1) * a.n_sm < est;
+    first_raw = atomicAdd(a.work + (first_gu ? 0 : 1), 1);
+  }
+  griddep_wait();  // the routes come from the routing kernel before
   griddep_launch();
-  route_rows(a.logits, a.logits_ld, a.E, a.T, a.k, a.has_shared, rs);  // ends with __syncthreads
+  load_routes(a.idx_out, a.T, a.k, a.has_shared, rs);  // ends with __syncthreads
 
   const int TS = a.T + a.has_shared;
-  if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < a.k * a.T; i += blockDim.x) {
-      a.idx_out[i] = rs->idx[(i / a.T) * kMaxTopK + i % a.T];
-      a.w_out[i] = rs->w[(i / a.T) * kMaxTopK + i % a.T];
-    }
-  }
   const int ntg = a.I / 64, ntd = (a.H + kBM - 1) / kBM;
   const int n_gu = rs->V * ntg, n_all = n_gu + rs->V * ntd;
   const int KGg = a.H / 64, KCg = (KGg + kGroupsPerUnit - 1) / kGroupsPerUnit;
   const int KGd = a.I / 64, KCd = (KGd + kGroupsPerUnit - 1) / kGroupsPerUnit;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
     const uint16_t** brow = reinterpret_cast<const uint16_t**>(smem + L::MISC_OFF + 64);
     long long fills = 0;
-    // The first item of every CTA is its block id: consecutive blocks sit on
-    // distinct SMs, so when there are few items the heavy gate/up items do
-    // not share an SM.  Later items come from the counter, in order.
-    int next = blockIdx.x;
+    // lane 0 draws; gu_open: the gate/up counter may still hold items
+    bool gu_open = true;
+    int next = 0;
+    if (lane == 0) {
+      if (!first_gu) {
+        next = n_gu + first_raw;
+      } else if (first_raw < n_gu) {
+        next = first_raw;
+      } else {
+        gu_open = false;
+        next = n_gu + atomicAdd(a.work + 1, 1);
+      }
+    }
+    next = __shfl_sync(0xffffffffu, next, 0);
     for (;;) {
       const int item = next;
       const int s0 = (int)(fills % ST);
@@ -944,8 +983,15 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
       }
       // The next item, fetched once this item's stages are all issued: an
       // atomic still in flight would hold up this lane's next barrier arrival
-      // (a release), and at the start every CTA fetches at once.
-      if (lane == 0) next = a.G + atomicAdd(a.work, 1);
+      // (a release).  Gate/up items first, while there are any.
+      if (lane == 0) {
+        int i = n_gu;
+        if (gu_open) {
+          i = atomicAdd(a.work, 1);
+          gu_open = i < n_gu;
+        }
+        next = i < n_gu ? i : n_gu + atomicAdd(a.work + 1, 1);
+      }
       next = __shfl_sync(0xffffffffu, next, 0);
       if (*abort) break;
     }
@@ -1099,21 +1145,35 @@ cudaError_t launch_q4_dense_argmax(const DenseArgs& a, int nt, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, q4_dense_kernel<2, true>, a);
 }
 
-// The combine kernel follows the routed-expert kernel of the same call, which
-// started after everything the caller enqueued before it (or, with pdl,
-// during the tail of the kernel before it).
+// Three kernels: the routing kernel (after everything the caller enqueued
+// before it, or, with pdl, during the tail of the kernel before it), then the
+// routed-expert kernel and the combine, each a programmatic dependent of the
+// kernel before it.  The expert kernel's first draw, before its dependency
+// wait, touches scheduling words that the previous call's combine reset: that
+// combine ran before the routing kernel, two kernels back.
 cudaError_t launch_moe(const MoeArgs& a, bool pdl, cudaStream_t s, int* launches) {
+  cudaLaunchAttribute pdl_attr[1];
+  pdl_attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl_attr[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(32 * a.k);
+    cfg.stream = s;
+    cfg.attrs = pdl_attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, moe_route_kernel, a);
+    if (e) return e;
+    ++*launches;
+  }
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.G);
     cfg.blockDim = dim3(Warps<kGateUpWarps>::THREADS);
     cfg.dynamicSmemBytes = moe_smem<1>();
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.attrs = pdl_attr;
+    cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, moe_kernel, a);
     if (e) return e;
     ++*launches;

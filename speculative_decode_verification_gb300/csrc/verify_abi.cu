@@ -19,7 +19,7 @@ struct verify_ctx {
   uint16_t* moe_hbuf = nullptr;
   float* moe_part = nullptr;
   int* err = nullptr;
-  int* moe_sched = nullptr;  // routed-expert scheduling: work counter, then one count per unit
+  int* moe_sched = nullptr;  // routed-expert scheduling words (vk::kMoeSchedWords), zero between calls
   uint16_t* st_xn = nullptr;   // layer scratch: bf16 [16, 8192]
   uint16_t* st_proj = nullptr; // bf16 [16, 32768]
   uint16_t* st_o = nullptr;    // bf16 [16, 32768]
@@ -132,6 +132,36 @@ verify_status check_dtype(verify_ctx* ctx, int dtype, bool allow_add) {
 
 }  // namespace
 
+namespace vk {
+
+int moe_shape_status(int k, int max_k, int E_gate_up, int E_down, int top_k, int gu_n_out, int gu_k_in,
+                     int dn_n_out, int dn_k_in, const char** msg) {
+  if (k < 1 || k > max_k) {
+    *msg = max_k == VERIFY_PASS_K ? "k must be in 1..16%s" : "k must be in 1..32%s";
+    return VERIFY_EUNSUPPORTED;
+  }
+  if (E_gate_up < 1 || E_gate_up > kMaxExperts || E_down != E_gate_up) {
+    *msg = "n_experts must match and be in 1..512%s";
+    return VERIFY_EUNSUPPORTED;
+  }
+  if (top_k < 1 || top_k > kMaxTopK || top_k > E_gate_up) {
+    *msg = "top_k out of range%s";
+    return VERIFY_EUNSUPPORTED;
+  }
+  const int H = gu_k_in, I = gu_n_out / 2;
+  if (gu_n_out != 2 * I || dn_n_out != H || dn_k_in != I) {
+    *msg = "expert shapes must be gate_up [2I, H], down [H, I]%s";
+    return VERIFY_EINVAL;
+  }
+  if (H > kMaxH || I > kMaxI || I % 64 != 0) {
+    *msg = "H <= 8192, I <= 4096, multiples of 64%s";
+    return VERIFY_EUNSUPPORTED;
+  }
+  return VERIFY_OK;
+}
+
+}  // namespace vk
+
 extern "C" {
 
 verify_status verify_init(int device, verify_ctx** out) {
@@ -150,8 +180,8 @@ verify_status verify_init(int device, verify_ctx** out) {
   if ((e = cudaMalloc(&ctx->moe_hbuf, kHbufElems * sizeof(uint16_t)))) return bail(e);
   if ((e = cudaMalloc(&ctx->moe_part, kMoePartElems * sizeof(float)))) return bail(e);
   if ((e = cudaMalloc(&ctx->err, sizeof(int)))) return bail(e);
-  if ((e = cudaMalloc(&ctx->moe_sched, (1 + vk::kMoeUnits) * sizeof(int)))) return bail(e);
-  if ((e = cudaMemset(ctx->moe_sched, 0, (1 + vk::kMoeUnits) * sizeof(int)))) return bail(e);
+  if ((e = cudaMalloc(&ctx->moe_sched, vk::kMoeSchedWords * sizeof(int)))) return bail(e);
+  if ((e = cudaMemset(ctx->moe_sched, 0, vk::kMoeSchedWords * sizeof(int)))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_xn, sizeof(uint16_t) * VERIFY_MAX_K * kMaxH))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_proj, sizeof(uint16_t) * VERIFY_MAX_K * kMaxProj))) return bail(e);
   if ((e = cudaMalloc(&ctx->st_o, sizeof(uint16_t) * VERIFY_MAX_K * kMaxProj))) return bail(e);
@@ -205,7 +235,7 @@ verify_status verify_device_status(verify_ctx* ctx, struct CUstream_st* stream, 
   if (code) *code = h;
   if (h == 0) return VERIFY_OK;
   cudaMemset(ctx->err, 0, sizeof(int));
-  cudaMemset(ctx->moe_sched, 0, (1 + vk::kMoeUnits) * sizeof(int));  // an aborted call may leave counts behind
+  cudaMemset(ctx->moe_sched, 0, vk::kMoeSchedWords * sizeof(int));  // an aborted call may leave counts behind
   cudaMemset(ctx->acc_best, 0, sizeof(unsigned long long) * (vk::kMaxAcceptK + 1));
   cudaDeviceSynchronize();
   snprintf(ctx->msg, sizeof ctx->msg, "device error code %d", h);
@@ -295,18 +325,14 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   verify_status s;
   if ((s = use_device(ctx))) return s;
   if (!gate_up || !down) return fail(ctx, VERIFY_EINVAL, "expert stacks are NULL%s");
-  if (k < 1 || k > VERIFY_MAX_K) return fail(ctx, VERIFY_EUNSUPPORTED, "k must be in 1..32%s");
   const int E = gate_up->n_experts;
-  if (E < 1 || E > vk::kMaxExperts || down->n_experts != E)
-    return fail(ctx, VERIFY_EUNSUPPORTED, "n_experts must match and be in 1..512%s");
-  if (top_k < 1 || top_k > vk::kMaxTopK || top_k > E) return fail(ctx, VERIFY_EUNSUPPORTED, "top_k out of range%s");
+  const char* why = "";
+  if (int rule = vk::moe_shape_status(k, VERIFY_MAX_K, E, down->n_experts, top_k, gate_up->w.n_out, gate_up->w.k_in,
+                                      down->w.n_out, down->w.k_in, &why))
+    return fail(ctx, (verify_status)rule, why);
   if ((s = check_q4(ctx, &gate_up->w, "gate_up", VERIFY_Q4_TILED_GATE_UP))) return s;
   if ((s = check_q4(ctx, &down->w, "down"))) return s;
   const int H = gate_up->w.k_in, I = gate_up->w.n_out / 2;
-  if (gate_up->w.n_out != 2 * I || down->w.n_out != H || down->w.k_in != I)
-    return fail(ctx, VERIFY_EINVAL, "expert shapes must be gate_up [2I, H], down [H, I]%s");
-  if (H > kMaxH || I > kMaxI || I % 64 != 0)
-    return fail(ctx, VERIFY_EUNSUPPORTED, "H <= 8192, I <= 4096, multiples of 64%s");
   if (logits_ld < E) return fail(ctx, VERIFY_EINVAL, "logits_ld < n_experts%s");
   if ((s = check_dtype(ctx, dtype_out, true))) return s;
   if ((s = check_dev(ctx, logits, 4, "logits"))) return s;
@@ -338,11 +364,12 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   a.gu_rt_bytes = rt_bytes(H);
   a.dn_rt_bytes = rt_bytes(I);
   a.hbuf = ctx->moe_hbuf; a.part = ctx->moe_part;
-  a.work = ctx->moe_sched; a.done = ctx->moe_sched + 1;
+  a.work = ctx->moe_sched; a.done = ctx->moe_sched + 2 + vk::kMoeSmSlots;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
   a.G = ctx->moe_ctas_per_sm * ctx->num_sms;
+  a.n_sm = ctx->num_sms;
   const size_t y_elem = dtype_out == VERIFY_BF16 ? 2 : 4;
   // passes of up to VERIFY_PASS_K rows (each row's routing, experts and
   // combine depend on that row alone); a later pass's kernels write the

@@ -107,6 +107,38 @@ def test_flash_shape_matches_oracle(vf, k):
         assert np.array_equal(t_r, ot[r])
 
 
+@pytest.mark.parametrize("k", range(1, 10))
+def test_flash_shape_every_width_with_random_rollback(vf, k):
+    """Flash-Next shape at every width k = 1..9: output and every row's
+    snapshot against the oracle, then a commit of a seeded random accepted
+    prefix a in 0..k, whose state must be the oracle's state after a rows
+    and, bit for bit, the state a fresh verify(a) leaves."""
+    c = S.FLASH_GDN
+    L = Layer(8, c["n_qk_heads"], c["n_v_heads"], c["d"], n_slots=10, s_std=0.02, tail_std=1.0)
+    inp = S.gdn_inputs(8, f"wr.gdn.{k}", k, c["n_qk_heads"], c["n_v_heads"], c["d"])
+    o = L.verify(vf, inp, k)
+    oo, oS, ot = L.oracle(inp, k)
+    assert_close(o, oo, what=f"o, k={k}")
+    for r in range(k):
+        S_r, t_r = L.slot(L.state.pending[r + 1])
+        assert_close(S_r, oS[r], what=f"S after row {r}, k={k}")
+        assert np.array_equal(t_r, ot[r])
+    a = int(S.draws(S.tensor_seed(8, f"wr.accept.{k}"), 0, 1)[0] % np.uint64(k + 1))
+    vf.gdn_commit(L.state, a)
+    got = L.slot(L.state.cur)
+    if a == 0:
+        assert L.state.cur == 0
+        assert np.array_equal(got[0], L.S0) and np.array_equal(got[1], L.tail0)
+        return
+    assert_close(got[0], oS[a - 1], what=f"committed state, k={k}, a={a}")
+    assert np.array_equal(got[1], ot[a - 1])
+    L.reset()
+    L.verify(vf, {key: v[:a] for key, v in inp.items()}, a)
+    want = L.slot(L.state.pending[a])
+    assert np.array_equal(got[0].view(np.uint32), want[0].view(np.uint32)), f"k={k}, a={a}"
+    assert np.array_equal(got[1], want[1])
+
+
 @pytest.mark.parametrize("k", [9, 32])
 def test_k_rows_bit_identical_to_sequential_single_rows(vf, k):
     """Row r of a k-row call equals a 1-row call started from the snapshot

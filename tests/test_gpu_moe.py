@@ -64,8 +64,8 @@ def test_small_moe_matches_oracle(vf, k):
     gud, dnd = DevQ4(vf, gu, True), DevQ4(vf, dn)
     before = vf.launch_count()
     gi, gw, gy = gather(vf, gud, dnd, dev(logits), T, dev(x), k, H)
-    # the routed experts kernel, then the combine, per pass of up to 16 rows
-    assert vf.launch_count() - before == 2 * ((k + 15) // 16)
+    # the routing kernel, the routed experts kernel, then the combine, per pass of up to 16 rows
+    assert vf.launch_count() - before == 3 * ((k + 15) // 16)
     assert np.array_equal(gi, oi)
     np.testing.assert_allclose(gw, ow, rtol=1e-5, atol=1e-6)
     assert_close(gy, oy, what=f"k={k}")
@@ -168,7 +168,9 @@ def test_single_expert_reduces_to_dense_products(vf):
 
 
 def test_ornith_shape_matches_oracle(vf):
-    """256 experts, H 2048, I 512, top-8, k = 2..9 (routes differ per row)."""
+    """256 experts, H 2048, I 512, top-8, at every width k = 2..9 (routes
+    differ per row); then every row of the 9-row call against a 1-row call
+    on that row, bit for bit."""
     import torch
 
     c = S.ORNITH_MOE
@@ -185,22 +187,34 @@ def test_ornith_shape_matches_oracle(vf):
 
     G = vf.tile(B.q4_experts(gu_p, gu_s, gu_b), gate_up=True)
     D = vf.tile(B.q4_experts(dn_p, dn_s, dn_b))
-    for k in (2, 9):
+    experts = {}
+
+    def expert(e):
+        if e not in experts:
+            experts[e] = (S.q4_expert(0, "ornith.gu", 2 * I, H, e), S.q4_expert(0, "ornith.dn", H, I, e))
+        return experts[e]
+
+    for k in range(2, 10):
         x = S.bf16_normal(0, f"ornith.x{k}", (k, H))
         logits = S.f32_normal(0, f"ornith.l{k}", (k, E))
         gi, gw, gy = gather(vf, G, D, dev(logits), T, dev(x), k, H)
         oi, ow = O.route_topk(logits, T)
         assert np.array_equal(gi, oi)
+        np.testing.assert_allclose(gw, ow, rtol=1e-5, atol=1e-6)
         ref = np.zeros((k, H))
         for r in range(k):
             for j in range(T):
-                e = int(oi[r, j])
-                mg = S.q4_expert(0, "ornith.gu", 2 * I, H, e)
-                md = S.q4_expert(0, "ornith.dn", H, I, e)
+                mg, md = expert(int(oi[r, j]))
                 gate_up = O.q4_qmv(mg.packed, mg.scales, mg.biases, x[r:r + 1])[0]
                 h = O.to_bf16(gate_up[:I] / (1.0 + np.exp(-gate_up[:I])) * gate_up[I:])
                 ref[r] += ow[r, j] * O.q4_qmv(md.packed, md.scales, md.biases, h[None, :])[0]
         assert_close(gy, ref, what=f"ornith k={k}")
+        if k == 9:
+            for r in range(k):
+                i1, w1, y1 = gather(vf, G, D, dev(logits[r:r + 1]), T, dev(x[r:r + 1]), 1, H)
+                assert np.array_equal(i1[0], gi[r])
+                assert np.array_equal(w1[0].view(np.uint32), gw[r].view(np.uint32)), f"ornith weights row {r}"
+                assert np.array_equal(y1[0].view(np.uint32), gy[r].view(np.uint32)), f"ornith row {r}"
 
 
 def test_width_32_rows_equal_single_rows(vf):
@@ -216,3 +230,33 @@ def test_width_32_rows_equal_single_rows(vf):
         i1, w1, y1 = gather(vf, gud, dnd, dev(logits[r:r + 1]), T, dev(x[r:r + 1]), 1, H)
         assert np.array_equal(i1[0], gi[r]) and np.array_equal(w1[0].view(np.uint32), gw[r].view(np.uint32))
         assert np.array_equal(y1[0].view(np.uint32), gy[r].view(np.uint32)), f"row {r}"
+
+
+@pytest.mark.parametrize("k", [1, 9])
+def test_progress_beside_a_concurrent_kernel(vf, k):
+    """The expert kernel's down items wait for their unit's gate/up items.  With
+    another stream's long matmuls holding SMs, not every expert CTA is
+    resident at once; the call must still finish without a wait running out
+    (the device error word stays clear) and give a solo run's result bit for
+    bit.  k = 1 has fewer gate/up items than CTAs."""
+    import torch
+
+    E, H, I, T = 64, 1024, 512, 8
+    gu, dn = moe_case(16, E, H, I)
+    G, D = DevQ4(vf, gu, True), DevQ4(vf, dn)
+    x = dev(S.bf16_normal(16, f"moe.cc.x{k}", (k, H)))
+    logits = dev(S.f32_normal(16, f"moe.cc.l{k}", (k, E)))
+    ref = gather(vf, G, D, logits, T, x, k, H)
+    a = torch.randn((8192, 8192), device="cuda", dtype=torch.bfloat16)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        with torch.cuda.stream(side):
+            for _ in range(8):
+                a = torch.matmul(a, a) * 1e-4
+        got = gather(vf, G, D, logits, T, x, k, H)
+        for g, r in zip(got, ref):
+            assert np.array_equal(g.view(np.uint32), r.view(np.uint32))
+    torch.cuda.synchronize()
+    st, code = vf.device_status()
+    assert st == B.OK, f"device error word {code}"

@@ -1,5 +1,5 @@
 """GPU parity of a full hybrid verify layer stack (verify_layer_k: GDN mixer
-then routed + shared MoE, 8 kernels per layer) against the oracle's
+then routed + shared MoE, 9 kernels per layer) against the oracle's
 composition of its pinned pieces.
 
 Pages: "QWEN38FLASH.md - Plan for supporting Qwen/Qwen3.8-Flash-Next" section 2
@@ -80,9 +80,9 @@ def check_layers(vf, cfg, seed, k, layers, h_name):
         idx = torch.zeros((k, sh["T"]), dtype=torch.int32, device="cuda")
         before = vf.launch_count()
         vf.verify_layer_k(ds.layers[l], ds.states[l], hd, k, idx)
-        # norm, in_proj, GDN, out_proj, norm, router, experts, combine; above 16
-        # rows the products, the GDN step and the experts run two passes
-        assert vf.launch_count() - before == (8 if k <= 16 else 14)
+        # norm, in_proj, GDN, out_proj, norm, router, routing, experts, combine;
+        # above 16 rows the products, the GDN step and the experts run two passes
+        assert vf.launch_count() - before == (9 if k <= 16 else 16)
         torch.cuda.synchronize()
         st = ds.states[l]
         S_last = host(ds.state_tensors[l][0][st.pending[k]])

@@ -1,0 +1,238 @@
+"""Stage-by-stage parity of the full-size hybrid verify stack (hidden 2560,
+GDN 16/48/128, 512 experts top-10 + shared, I = 640, twelve layers) at the
+single-kernel tolerance, max |gpu - oracle| <= 1e-3 * rms(oracle).
+
+Each layer runs stage by stage through the public entry points, and the
+oracle piece of every stage gets the GPU's own input of that stage (the same
+bf16 rows): the pre-mixer norm, the in-projection, the Gated DeltaNet step
+(output, every row's state snapshot and conv window), the out-projection and
+its residual add, the pre-MoE norm, the router, and the routed + shared
+experts with their residual add.  Routing indices are compared bit for bit
+with the oracle's top-k of the GPU's logits (descending, ties to the lower
+index).  Each stage is run with fp32 output for the comparison and with the
+bf16 output the layer uses, which must be the fp32 value rounded to nearest
+even.  Finally one ``verify_layer_k`` call from the same input must give the
+staged chain's residual, routes and snapshots bit for bit, so the fused
+layer inherits the stage checks.
+
+Pages: "QWEN38FLASH.md - Plan for supporting Qwen/Qwen3.8-Flash-Next"
+section 2 (the layer: Gated DeltaNet mixer, then MoE of 10 routed + 1
+sigmoid-gated shared expert; zero-centred norms), "Flash-Next optimization
+transfer to Ornith and Qwen 27B", "Exact verification kernels" (agreement with
+serial results).
+"""
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from speculative_decode_verification_gb300 import binding as B
+from speculative_decode_verification_gb300 import synth as S
+from speculative_decode_verification_gb300.stack import DeviceStack, shapes
+from tests.gpu_util import assert_close, host
+
+pytestmark = pytest.mark.gpu
+
+CFG = dict(S.STACK)
+SEED = 0
+K_MAX = 9
+
+
+@pytest.fixture(scope="module")
+def vf():
+    import torch
+
+    assert torch.cuda.is_available()
+    v = B.Verify(0)
+    yield v
+    st, code = v.device_status()
+    assert st == B.OK, f"device error word {code}"
+    v.close()
+
+
+@pytest.fixture(scope="module")
+def stack(vf):
+    return DeviceStack(vf, CFG, seed=SEED, n_slots=K_MAX + 1, graphs=False)
+
+
+_host_layers = {}
+
+
+def host_layer(l):
+    if l not in _host_layers:
+        sh = shapes(CFG)
+        _host_layers[l] = S.HostLayerWeights(SEED, l, sh["H"], sh["NP"], sh["Z"], sh["E"], sh["I"],
+                                             CFG["n_qk_heads"], CFG["n_v_heads"], CFG["d"])
+    return _host_layers[l]
+
+
+def rne(a32):
+    return S.f32_to_bf16(np.asarray(a32, np.float32))
+
+
+def bits16(t):
+    return host(t).view(np.uint16)
+
+
+def stage_pair(run, shape):
+    """Runs one stage with fp32 output and with bf16 output; the bf16 result
+    must be the fp32 result rounded to nearest even."""
+    import torch
+
+    y32 = torch.zeros(shape, dtype=torch.float32, device="cuda")
+    y16 = torch.zeros(shape, dtype=torch.int16, device="cuda")
+    run(y32, B.F32)
+    run(y16, B.BF16)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(y16), rne(host(y32))), "bf16 output is not the rounded fp32 output"
+    return y32, y16
+
+
+def check_layer_stages(vf, ds, l, h_dev, k):
+    """Layer l from the device residual h_dev (fp32 [k, H], updated in place),
+    every stage against the oracle from the GPU's own stage input."""
+    import torch
+
+    sh = shapes(CFG)
+    H, C, Z, NP, E, T, I = sh["H"], sh["C"], sh["Z"], sh["NP"], sh["E"], sh["T"], sh["I"]
+    Hk, Hv, d = CFG["n_qk_heads"], CFG["n_v_heads"], CFG["d"]
+    L, st = ds.layers[l], ds.states[l]
+    w = host_layer(l)
+    h_in = host(h_dev).copy()
+    where = f"layer {l}, k={k}"
+
+    # 1. pre-mixer norm
+    xn32, xn = stage_pair(lambda y, dt: vf.verify_rmsnorm_k(h_dev, w_ptr(L.norm1_w), L.norm_eps, True, H, k, y, dt),
+                          (k, H))
+    assert_close(host(xn32), O.rmsnorm(h_in, w.norm1, 1e-6, True), what=f"norm1, {where}")
+    # 2. in-projection
+    p32, p = stage_pair(lambda y, dt: vf.q4_qmv_k(L.in_proj, xn, k, y, dt), (k, NP))
+    assert_close(host(p32), O.q4_qmv(*w.in_proj, bits16(xn)), what=f"in_proj, {where}")
+    # 3. Gated DeltaNet step, from the layer's initial state
+    S0, t0 = S.gdn_initial_state(SEED, f"stack.L{l}.gdn", Hk, Hv, d, s_std=0.02, tail_std=1.0)
+    gi = B.gdn_inputs(p[:, :C], p[:, C:C + Z], p[:, C + Z:C + Z + Hv], p[:, C + Z + Hv:])
+    o32, o = stage_pair(lambda y, dt: vf.gdn_verify_k(L.gdn, st, gi, k, y, dt), (k, Z))
+    ph = bits16(p)
+    inp = dict(qkv=ph[:, :C], z=ph[:, C:C + Z], a=ph[:, C + Z:C + Z + Hv], b=ph[:, C + Z + Hv:])
+    o_ref, S_ref, t_ref = O.gdn_verify(Hk, Hv, d, w.gdn, S0.astype(np.float64), t0, inp, k)
+    assert_close(host(o32), o_ref, what=f"GDN output, {where}")
+    slots, tails = ds.state_tensors[l]
+    snaps = []
+    for r in range(k):
+        s_r = host(slots[st.pending[r + 1]]).copy()
+        t_r = bits16(tails[st.pending[r + 1]]).copy()
+        assert_close(s_r, S_ref[r], what=f"GDN state after row {r}, {where}")
+        assert np.array_equal(t_r, t_ref[r]), f"conv window after row {r}, {where}"
+        snaps.append((s_r, t_r))
+    # 4. out-projection, then its residual add (fp32, elementwise)
+    out32 = torch.zeros((k, H), dtype=torch.float32, device="cuda")
+    vf.q4_qmv_k(L.out_proj, o, k, out32, B.F32)
+    vf.q4_qmv_k(L.out_proj, o, k, h_dev, B.F32_ADD)
+    torch.cuda.synchronize()
+    assert_close(host(out32), O.q4_qmv(*w.out_proj, bits16(o)), what=f"out_proj, {where}")
+    h_mid = host(h_dev).copy()
+    assert np.array_equal(h_mid, (h_in + host(out32)).astype(np.float32)), f"mixer residual add, {where}"
+    # 5. pre-MoE norm
+    xn2_32, xn2 = stage_pair(
+        lambda y, dt: vf.verify_rmsnorm_k(h_dev, w_ptr(L.norm2_w), L.norm_eps, True, H, k, y, dt), (k, H))
+    assert_close(host(xn2_32), O.rmsnorm(h_mid, w.norm2, 1e-6, True), what=f"norm2, {where}")
+    # 6. router (E routing logits, then the shared expert's gate logit)
+    lg = torch.zeros((k, E + 1), dtype=torch.float32, device="cuda")
+    vf.q4_qmv_k(L.router, xn2, k, lg, B.F32)
+    torch.cuda.synchronize()
+    lgh = host(lg).copy()
+    x2h = bits16(xn2)
+    assert_close(lgh, O.q4_qmv(*w.router, x2h), what=f"router, {where}")
+    # 7. routed + shared experts from the GPU's logits and rows
+    idx = torch.zeros((k, T), dtype=torch.int32, device="cuda")
+    wts = torch.zeros((k, T), dtype=torch.float32, device="cuda")
+    y32 = torch.zeros((k, H), dtype=torch.float32, device="cuda")
+    args = (L.gate_up, L.down, lg, E + 1, T, xn2, k, idx, wts)
+    shared = dict(shared_gate_up=L.shared_gate_up, shared_down=L.shared_down, shared_gate_logit=lg[:, E:])
+    vf.q4_gather_experts_k(*args, y32, B.F32, **shared)
+    vf.q4_gather_experts_k(*args, h_dev, B.F32_ADD, **shared)
+    torch.cuda.synchronize()
+    idx_ref, w_ref = O.route_topk(lgh[:, :E], T)
+    gidx = host(idx).copy()
+    assert np.array_equal(gidx, idx_ref), f"routing indices, {where}"
+    np.testing.assert_allclose(host(wts), w_ref, rtol=1e-5, atol=1e-6, err_msg=f"routing weights, {where}")
+    U = np.unique(idx_ref)
+    ex = [w.expert(int(e)) for e in U]
+    gu = tuple(np.stack([x[0][i] for x in ex]) for i in range(3))
+    dn = tuple(np.stack([x[1][i] for x in ex]) for i in range(3))
+    idx_c, _, y_ref, _ = O.gather_experts(gu, dn, np.ascontiguousarray(lgh[:, U]), T, x2h,
+                                          shared=(w.shared_gate_up, w.shared_down), shared_logit=lgh[:, E])
+    assert np.array_equal(U[idx_c], idx_ref)
+    assert_close(host(y32), y_ref, what=f"experts, {where}")
+    h_out = host(h_dev).copy()
+    assert np.array_equal(h_out, (h_mid + host(y32)).astype(np.float32)), f"MoE residual add, {where}"
+
+    # the fused layer call from the same input gives the staged chain bit for bit
+    h_layer = torch.from_numpy(h_in).cuda()
+    idx_layer = torch.zeros((k, T), dtype=torch.int32, device="cuda")
+    vf.verify_layer_k(L, st, h_layer, k, idx_layer)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(h_layer).view(np.uint32), h_out.view(np.uint32)), f"verify_layer_k residual, {where}"
+    assert np.array_equal(host(idx_layer), gidx), f"verify_layer_k routes, {where}"
+    for r in range(k):
+        assert np.array_equal(host(slots[st.pending[r + 1]]).view(np.uint32), snaps[r][0].view(np.uint32)), \
+            f"verify_layer_k state after row {r}, {where}"
+        assert np.array_equal(bits16(tails[st.pending[r + 1]]), snaps[r][1]), \
+            f"verify_layer_k conv window after row {r}, {where}"
+    return gidx
+
+
+def w_ptr(addr):
+    """A device pointer held in a Layer struct, passed on as is."""
+    class _P:
+        def data_ptr(self):
+            return addr
+    return _P()
+
+
+@pytest.mark.parametrize("k", [1, 4, 8, 9])
+def test_full_stack_stage_by_stage(vf, stack, k):
+    """All twelve layers at hidden 2560; rows 0..k-1 of one seeded block, so
+    every width sees the same first rows."""
+    import torch
+
+    h0 = S.f32_normal(SEED, "stack.stages.h", (K_MAX, shapes(CFG)["H"]))[:k]
+    h = torch.from_numpy(np.ascontiguousarray(h0)).cuda()
+    routed = set()
+    for l in range(CFG["layers"]):
+        idx = check_layer_stages(vf, stack, l, h, k)
+        routed.update(int(e) for e in idx.ravel())
+    # the rows route to different experts (the workload's premise)
+    assert len(routed) > CFG["T"]
+
+
+def test_stack_experts_width_k_equals_width_1(vf, stack):
+    """The stack's routed + shared expert call (512 experts, top-10, I 640,
+    hidden 2560) at k = 9: every row equals a 1-row call on that row, bit
+    for bit (routes, weights and output)."""
+    import torch
+
+    sh = shapes(CFG)
+    H, E, T = sh["H"], sh["E"], sh["T"]
+    L = stack.layers[0]
+    k = K_MAX
+    xh = S.bf16_normal(SEED, "stack.ew.x", (k, H))
+    lgh = S.f32_normal(SEED, "stack.ew.l", (k, E + 1))
+
+    def call(rows):
+        x = torch.from_numpy(np.ascontiguousarray(xh[rows]).view(np.int16)).cuda()
+        lg = torch.from_numpy(np.ascontiguousarray(lgh[rows])).cuda()
+        n = len(rows)
+        idx = torch.zeros((n, T), dtype=torch.int32, device="cuda")
+        w = torch.zeros((n, T), dtype=torch.float32, device="cuda")
+        y = torch.zeros((n, H), dtype=torch.float32, device="cuda")
+        vf.q4_gather_experts_k(L.gate_up, L.down, lg, E + 1, T, x, n, idx, w, y, B.F32, L.shared_gate_up,
+                               L.shared_down, lg[:, E:])
+        torch.cuda.synchronize()
+        return host(idx), host(w), host(y)
+
+    gi, gw, gy = call(list(range(k)))
+    for r in range(k):
+        i1, w1, y1 = call([r])
+        assert np.array_equal(i1[0], gi[r])
+        assert np.array_equal(w1[0].view(np.uint32), gw[r].view(np.uint32)), f"weights row {r}"
+        assert np.array_equal(y1[0].view(np.uint32), gy[r].view(np.uint32)), f"row {r}"

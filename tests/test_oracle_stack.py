@@ -206,3 +206,23 @@ def test_mixer_output_reaches_the_residual_through_out_proj(k):
     swapped = dict(inp, z=p[:, :Z], qkv=np.concatenate([p[:, Z:C], p[:, C:C + Z]], axis=1))
     o_bad, _, _ = O.gdn_verify(CFG["n_qk_heads"], Hv, CFG["d"], w.gdn, S0, t0, swapped, k)
     assert not np.allclose(_bf(O.to_bf16(o_bad)), want)
+
+
+def test_threaded_oracle_build_is_bit_identical():
+    """The OpenMP build (timing only) spreads output rows over the cores but
+    sums every output in the same order: a whole layer gives the same bits."""
+    k = 3
+    w = Layer()
+    h, S0, t0 = _inputs(6, k)
+    O.use_threads(False)
+    want = _run(w, h, S0, t0, k)
+    try:
+        if O.build_threaded() is None:
+            pytest.skip("no OpenMP build of the oracle on this host")
+        n = O.use_threads(True)
+        got = _run(w, h, S0, t0, k)
+    finally:
+        O.use_threads(False)
+    assert n >= 1
+    for g, r in zip(got, want):
+        assert np.array_equal(np.asarray(g), np.asarray(r))
