@@ -627,7 +627,7 @@ def run_kernels(args):
     L2 = 129 << 20
     keep = []
 
-    def q4(name, n_out, k_in, n_experts=None, gate_up=False):
+    def q4(name, n_out, k_in, n_experts=None, gate_up=False, down=False):
         e = 1 if n_experts is None else n_experts
         shp = (e, n_out, k_in // 8) if n_experts else (n_out, k_in // 8)
         gshp = (e, n_out, k_in // 64) if n_experts else (n_out, k_in // 64)
@@ -636,7 +636,7 @@ def run_kernels(args):
         bi = torch.empty(gshp, dtype=torch.int16, device="cuda")
         vf.synth_q4(p, sc, bi, S.q4_seeds(0, name), S.SCALE_RANGE, S.BIAS_RANGE, centered=False)
         rows = B.q4_experts(p, sc, bi) if n_experts else B.q4_weight(p, sc, bi)
-        t = vf.tile(rows, gate_up=gate_up)
+        t = vf.tile(rows, gate_up=gate_up, down=down)
         torch.cuda.synchronize()
         del p, sc, bi
         keep.append(t.buf)
@@ -691,6 +691,39 @@ def run_kernels(args):
     def want(name):
         return only is None or name in only
 
+    # the tiny configuration: one 512 x 512 projection at k = 1..4 and a
+    # 2/2-head, d = 32 GDN step at k = 2.  Its 147 KB of weights are rotated
+    # over 8 copies and stay in L2: these rows measure latency, not bandwidth.
+    if want("tiny"):
+        N = K = 512
+        Ws = [q4(f"kbench.tiny.c{c}", N, K) for c in range(8)]
+        x = dev(S.bf16_normal(0, "kbench.tiny.x", (4, K)).view(np.int16))
+        y = torch.empty((4, N), dtype=torch.float32, device="cuda")
+        for k in (1, 2, 3, 4):
+            us = time_calls([(lambda W=W, k=k: vf.q4_qmv_k(W, x, k, y, B.F32, stream.cuda_stream)) for W in Ws])
+            emit("q4_qmv_k", f"tiny {N}x{K}", k, us, 0.5625 * N * K + 2 * k * K + 4 * k * N, {"l2_resident": True})
+        Hk, Hv, d, k = 2, 2, 32, 2
+        C = 2 * Hk * d + Hv * d
+        gp = {key: dev(v) for key, v in S.gdn_params(0, "kbench.tiny.gdn", Hk, Hv, d).items()}
+        params = B.gdn_params(Hk, Hv, d, gp["conv_w"], gp["A_log"], gp["dt_bias"], gp["norm_w"])
+        calls = []
+        for r in range(8):
+            slots = [torch.zeros((Hv, d, d), dtype=torch.float32, device="cuda") for _ in range(k + 1)]
+            tails = [torch.zeros((3, C), dtype=torch.int16, device="cuda") for _ in range(k + 1)]
+            inp = {key: dev(v.view(np.int16) if v.dtype == np.uint16 else v)
+                   for key, v in S.gdn_inputs(0, f"kbench.tiny.gdn.{r}", k, Hk, Hv, d).items()}
+            o = torch.empty((k, Hv * d), dtype=torch.float32, device="cuda")
+            keep.extend(slots + tails + [o])
+            gi = B.gdn_inputs(inp["qkv"], inp["z"], inp["a"], inp["b"])
+            calls.append(lambda slots=slots, tails=tails, gi=gi, o=o:
+                         vf.gdn_verify_k(params, B.gdn_state(slots, tails, cur=0), gi, k, o, B.F32, stream.cuda_stream))
+        us = time_calls(calls)
+        emit("gdn_verify_k", f"tiny gdn Hk{Hk} Hv{Hv} d{d}", k, us,
+             Hv * d * d * 4 * (1 + k) + 3 * C * 2 * (1 + k) + k * (C + Hv * d + 2 * Hv) * 2 + k * Hv * d * 4,
+             {"l2_resident": True})
+        del Ws
+        keep.clear()
+        torch.cuda.empty_cache()
     # a1: dense Q4 products, the dense configuration's shapes and the LM head; copies rotated
     for (N, K) in [sh for sh in S.DENSE_SHAPES if want("dense")] + ([S.LM_HEAD] if want("lm_head") else []):
         wbytes = 0.5625 * N * K
@@ -713,7 +746,7 @@ def run_kernels(args):
     m = S.ORNITH_MOE
     E, T, H, I = m["E"], m["T"], m["H"], m["I"]
     gu = q4("kbench.moe.gu", 2 * I, H, E, gate_up=True) if want("experts") else None
-    dn = q4("kbench.moe.dn", H, I, E) if want("experts") else None
+    dn = q4("kbench.moe.dn", H, I, E, down=True) if want("experts") else None
     for k in (widths if want("experts") else []):
         sets = []
         for r in range(8):
@@ -839,7 +872,7 @@ def main():
     ap.add_argument("--layers", type=int, default=12)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="",
-                    help="with --kernels: comma list of dense,lm_head,experts,gdn,accept,attn (default all)")
+                    help="with --kernels: comma list of tiny,dense,lm_head,experts,gdn,accept,attn (default all)")
     ap.add_argument("--attn-p", default="4096,65536",
                     help="with --kernels: cached positions of the attention rows (comma list)")
     ap.add_argument("--kernels", action="store_true",

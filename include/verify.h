@@ -104,22 +104,38 @@ typedef struct verify_ctx verify_ctx;
  *   scales : bf16 [n_out, k_in/64];  biases : bf16 [n_out, k_in/64]
  *   Requirements: packed 16-byte aligned; scales, biases 2-byte aligned.
  *
- * VERIFY_Q4_TILED / VERIFY_Q4_TILED_GATE_UP - the library's layout, written
- * by q4_tile, taken by every compute call: `packed` points to the tiled bytes
- * (16-byte aligned), scales and biases are NULL (they live inside the tiles).
- * Each (128-row tile, 256-column chunk) is one contiguous block: the tile's
- * scales and biases, then its codes in the order the kernels consume them,
- * so that a pipeline stage is one bulk copy and HBM is read in long runs.
- * TILED_GATE_UP marks a fused gate/up matrix [2I, n_in] whose tiles pair 64
- * gate rows with the 64 up rows of the same outputs.
+ * VERIFY_Q4_TILED / VERIFY_Q4_TILED_GATE_UP / VERIFY_Q4_TILED_DOWN - the
+ * library's layouts, written by q4_tile, taken by the compute calls:
+ * `packed` points to the tiled bytes (16-byte aligned), scales and biases
+ * are NULL (they live inside the tiles).  Each (128-row tile, column chunk)
+ * is one contiguous block: the tile's scales and biases, then its codes in
+ * the order the kernels consume them, so that a pipeline stage is one bulk
+ * copy and HBM is read in long runs.
+ *   TILED         - dense products (q4_qmv_k, the LM head): 256-column
+ *                   chunks.
+ *   TILED_GATE_UP - routed and shared experts' fused gate/up matrix
+ *                   [2I, n_in], whose tiles pair 64 gate rows with the 64 up
+ *                   rows of the same outputs; 128-column chunks.
+ *   TILED_DOWN    - routed and shared experts' down matrix; 128-column
+ *                   chunks.
+ * The experts' smaller blocks let their kernel keep a deeper pipeline in
+ * the same shared memory.
  *
  * Requirements: k_in % 64 == 0, k_in >= 64; group_size == 64; bits == 4.
  */
 typedef enum {
   VERIFY_Q4_ROWS = 0,
   VERIFY_Q4_TILED = 1,
-  VERIFY_Q4_TILED_GATE_UP = 2
+  VERIFY_Q4_TILED_GATE_UP = 2,
+  VERIFY_Q4_TILED_DOWN = 3
 } verify_q4_layout;
+
+/* What a matrix is tiled for (q4_tile, q4_tiled_bytes). */
+typedef enum {
+  VERIFY_TILE_DENSE = 0,   /* -> VERIFY_Q4_TILED */
+  VERIFY_TILE_GATE_UP = 1, /* -> VERIFY_Q4_TILED_GATE_UP (n_out = 2I, I % 64 == 0) */
+  VERIFY_TILE_DOWN = 2     /* -> VERIFY_Q4_TILED_DOWN */
+} verify_tile_kind;
 
 typedef struct {
   const uint32_t* packed;
@@ -179,23 +195,24 @@ verify_status verify_selftest_stuck_wait(verify_ctx* ctx, struct CUstream_st* st
 /* ------------------------------------------------------------- q4_tile */
 
 /*
- * Bytes of the tiled layout of n_experts matrices [n_out, k_in] (gate_up:
- * the gate/up pairing, n_out = 2I with I % 64 == 0); -1 for invalid shapes.
- * Equals the row layout's bytes when n_out % 128 == 0, plus the zero rows
- * that complete the last 128-row tile otherwise.
+ * Bytes of the tiled layout (kind: verify_tile_kind) of n_experts matrices
+ * [n_out, k_in]; -1 for invalid shapes or kind.  Equals the row layout's
+ * bytes when n_out % 128 == 0, plus the zero rows that complete the last
+ * 128-row tile otherwise.
  */
-int64_t q4_tiled_bytes(int32_t n_out, int32_t k_in, int32_t n_experts, int32_t gate_up);
+int64_t q4_tiled_bytes(int32_t n_out, int32_t k_in, int32_t n_experts, int32_t kind);
 
 /*
  * Converts src (VERIFY_Q4_ROWS; n_experts matrices back to back) into the
- * tiled layout at dst (device, 16-byte aligned, dst_bytes >= q4_tiled_bytes)
- * on `stream`, and fills *out (a host struct) with the tiled description:
- * packed = dst, layout = VERIFY_Q4_TILED or VERIFY_Q4_TILED_GATE_UP.  A
- * one-time step when weights are loaded; src may be freed once the stream
- * has passed the conversion.  Every bit of src is kept: the tiled matrix
- * computes exactly what src describes.
+ * tiled layout of `kind` (verify_tile_kind) at dst (device, 16-byte aligned,
+ * dst_bytes >= q4_tiled_bytes) on `stream`, and fills *out (a host struct)
+ * with the tiled description: packed = dst, layout = VERIFY_Q4_TILED,
+ * VERIFY_Q4_TILED_GATE_UP or VERIFY_Q4_TILED_DOWN.  A one-time step when
+ * weights are loaded; src may be freed once the stream has passed the
+ * conversion.  Every bit of src is kept: the tiled matrix computes exactly
+ * what src describes.  Returns VERIFY_EUNSUPPORTED for an unknown kind.
  */
-verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_experts, int32_t gate_up, void* dst,
+verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_experts, int32_t kind, void* dst,
                       int64_t dst_bytes, verify_q4_weight* out, struct CUstream_st* stream);
 
 /* ------------------------------------------------------------ q4_qmv_k */
@@ -242,11 +259,11 @@ verify_status q4_qmv_k(verify_ctx* ctx, const verify_q4_weight* W,
  *   if a shared expert is given: y[r] += sigmoid(sg[r]) * (W_sd . bf16(silu(W_sgu[0..I).x) * W_sgu[I..2I).x))
  *
  * gate_up : experts [E, 2I, H], VERIFY_Q4_TILED_GATE_UP;
- * down    : experts [E, H, I], VERIFY_Q4_TILED.
+ * down    : experts [E, H, I], VERIFY_Q4_TILED_DOWN.
  * logits  : fp32, row r at logits + r*logits_ld, E entries.
  * x       : bf16 [k, H].   idx_out : int32 [k, T];  w_out : fp32 [k, T].
  * y       : fp32 [k, H] (VERIFY_F32 or VERIFY_F32_ADD) or bf16.
- * shared_gate_up [2I, H] (TILED_GATE_UP), shared_down [H, I] (TILED), shared_gate_logit (fp32, row r
+ * shared_gate_up [2I, H] (TILED_GATE_UP), shared_down [H, I] (TILED_DOWN), shared_gate_logit (fp32, row r
  * at shared_gate_logit + r*logits_ld) may all be NULL (no shared expert).
  * Limits: E <= 512, 1 <= T <= 16, 64 <= H <= 8192, 64 <= I <= 4096,
  * H % 64 == I % 64 == 0.
@@ -577,7 +594,8 @@ verify_status verify_rmsnorm_k(verify_ctx* ctx, const float* x, const float* w,
  * <= 32768, E + 1 <= 1024).  Weight shapes must match: in_proj [C + Hv*dv +
  * 2*Hv, H], out_proj [H, Hv*dv], router [E + 1, H], gate_up [E, 2I, H],
  * down [E, H, I], shared_gate_up [2I, H], shared_down [H, I]; all tiled
- * (gate_up and shared_gate_up with the gate/up pairing).
+ * (gate_up and shared_gate_up as VERIFY_Q4_TILED_GATE_UP, down and
+ * shared_down as VERIFY_Q4_TILED_DOWN, the rest VERIFY_Q4_TILED).
  */
 typedef struct {
   verify_q4_weight in_proj;

@@ -16,7 +16,8 @@ LIB_PATH = os.path.join(PKG, "libverify.so")
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE = 0, 1, 2, 3, 4
 F32, BF16, F32_ADD = 0, 1, 2
-ROWS, TILED, TILED_GATE_UP = 0, 1, 2  # verify_q4_layout
+ROWS, TILED, TILED_GATE_UP, TILED_DOWN = 0, 1, 2, 3  # verify_q4_layout
+TILE_DENSE, TILE_GATE_UP, TILE_DOWN = 0, 1, 2  # verify_tile_kind
 MAX_K = 32
 PASS_K = 16
 GDN_MAX_SLOTS = 33
@@ -299,19 +300,24 @@ class Verify:
         arr = (C.c_void_p * 8)(*[None if e is None else e.cuda_event for e in events])
         self._check(self.lib.verify_set_layer_events(self.ctx, arr, 8))
 
-    def tile(self, src, gate_up: bool = False, stream=None) -> Tiled:
+    def tile(self, src, gate_up: bool = False, down: bool = False, stream=None) -> Tiled:
         """Tiled copy of a row-layout Q4Weight or Q4Experts (q4_tile): a new
-        device buffer (torch uint8) and the struct describing it."""
+        device buffer (torch uint8) and the struct describing it.  gate_up:
+        an expert gate/up matrix; down: an expert down matrix; neither: a
+        dense product's matrix."""
         import torch
 
+        if gate_up and down:
+            raise ValueError("a matrix is tiled as gate/up or as down, not both")
+        kind = TILE_GATE_UP if gate_up else TILE_DOWN if down else TILE_DENSE
         experts = isinstance(src, Q4Experts)
         w, E = (src.w, src.n_experts) if experts else (src, 1)
-        nbytes = int(self.lib.q4_tiled_bytes(w.n_out, w.k_in, E, int(bool(gate_up))))
+        nbytes = int(self.lib.q4_tiled_bytes(w.n_out, w.k_in, E, kind))
         if nbytes < 0:
-            raise VerifyError(EUNSUPPORTED, f"q4_tiled_bytes({w.n_out}, {w.k_in}, {E}, {gate_up}) rejected the shape")
+            raise VerifyError(EUNSUPPORTED, f"q4_tiled_bytes({w.n_out}, {w.k_in}, {E}, {kind}) rejected the shape")
         buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         out = Q4Weight()
-        self._check(self.lib.q4_tile(self.ctx, C.byref(w), E, int(bool(gate_up)), C.c_void_p(buf.data_ptr()), nbytes,
+        self._check(self.lib.q4_tile(self.ctx, C.byref(w), E, kind, C.c_void_p(buf.data_ptr()), nbytes,
                                      C.byref(out), self._stream(stream)))
         return Tiled(buf, Q4Experts(out, E) if experts else out)
 

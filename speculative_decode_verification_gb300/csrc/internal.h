@@ -16,8 +16,9 @@ constexpr int kGateUpWarps = 4;    // fused gate/up: a gate tile and its up tile
 constexpr int kDownWarps = 4;      // routed down projection: two 16-row MMA tiles each
 constexpr int kQ4CtasPerSm = 2;    // dense kernels
 constexpr int kMaxSplits = 16;      // K-splits of a dense row tile (one cluster; 16 = largest non-portable size)
-constexpr int kMoeCtasPerSm = 4;   // routed-expert kernel: 8 activation rows per stage, two stages
-constexpr int kMoeStages = 2;
+constexpr int kMoeCtasPerSm = 4;   // routed-expert kernel: 8 activation rows per stage, four stages
+constexpr int kMoeStages = 4;
+constexpr int kExpertGroups = 2;   // routed experts: 64-column groups per stage (128 columns)
 constexpr int kMoeUnits = 2 * 512 + 2;  // work units of one call: (expert, chunk of 8 rows), at most
 constexpr int kMoeSmSlots = 256;        // per-SM arrival counters of the routed-expert kernel (SM ids below this)
 // Scheduling words of the routed-expert kernel, zero between calls: the
@@ -27,11 +28,25 @@ constexpr int kMoeSchedWords = 2 + kMoeSmSlots + kMoeUnits;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 
-// Tiled weight layout (tile.cu): per (128-row tile, 256-column chunk) a block
-// of scales and biases followed by the chunk's groups of codes.
-constexpr int kTileSbBytes = 2 * kBM * 8;                                 // 2048
+// Tiled weight layouts (tile.cu): per (128-row tile, chunk of G 64-column
+// groups) a block of scales and biases followed by the chunk's groups of
+// codes.  Dense matrices: G = kGroupsPerUnit (256 columns); routed and shared
+// experts: G = kExpertGroups (128 columns).
 constexpr int kTileGroupBytes = kBM * 32;                                 // 4096: 128 rows x 64 codes
-constexpr int kTileChunkBytes = kTileSbBytes + kGroupsPerUnit * kTileGroupBytes;  // 18432
+__host__ __device__ constexpr int tile_sb_bytes(int groups) { return 2 * kBM * 2 * groups; }
+__host__ __device__ constexpr int tile_chunk_bytes(int groups) {
+  return tile_sb_bytes(groups) + groups * kTileGroupBytes;
+}
+constexpr int kTileSbBytes = tile_sb_bytes(kGroupsPerUnit);               // 2048
+constexpr int kTileChunkBytes = tile_chunk_bytes(kGroupsPerUnit);         // 18432
+// Groups per chunk of a tiled layout (verify_q4_layout), 0 if not tiled.
+__host__ __device__ constexpr int layout_groups(int layout) {
+  return layout == 1 ? kGroupsPerUnit : (layout == 2 || layout == 3) ? kExpertGroups : 0;
+}
+// Bytes of one 128-row tile of a tiled matrix with k_in columns.
+__host__ __device__ constexpr long long tile_row_bytes(int k_in, int groups) {
+  return (long long)tile_sb_bytes(groups) * ((k_in / 64 + groups - 1) / groups) + (long long)kTileGroupBytes * (k_in / 64);
+}
 
 // Dense product: RB row tiles x S K-splits, one cluster of S CTAs per tile.
 struct DenseArgs {
@@ -119,11 +134,12 @@ cudaError_t launch_q4_dense(const DenseArgs& a, int nt, bool pdl, cudaStream_t s
 // The same product with the argmax epilogue (one pass of up to 16 rows).
 cudaError_t launch_q4_dense_argmax(const DenseArgs& a, int nt, cudaStream_t s);
 cudaError_t launch_moe(const MoeArgs& a, bool pdl, cudaStream_t s, int* launches);
-// Tiled layout: bytes of E matrices [N, K] (gate_up: tiles pair gate and up rows),
-// and the conversion from the row-major layout.
-long long tiled_bytes(int N, int K, int E, bool gate_up);
+// Tiled layouts: bytes of E matrices [N, K] of a tile kind (0 dense, 1
+// gate/up: tiles pair gate and up rows, 2 expert down), and the conversion
+// from the row-major layout.
+long long tiled_bytes(int N, int K, int E, int kind);
 cudaError_t launch_tile(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases, uint8_t* dst, int N,
-                        int K, int E, bool gate_up, cudaStream_t s);
+                        int K, int E, int kind, cudaStream_t s);
 cudaError_t gdn_setup_kernels();
 // One kernel whose two bounded waits (a barrier and a counter that nothing
 // completes) run out and record VERIFY_DEV_ETIMEOUT in *err.

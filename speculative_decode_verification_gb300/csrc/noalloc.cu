@@ -67,10 +67,6 @@ bool valid_q4(const verify_q4_weight* W, int layout) {
          W->n_out >= 1 && device_memory(W->packed, 16);
 }
 
-long long rt_bytes(int k_in) {
-  const long long KG = k_in / 64, KC = (KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
-  return (long long)vk::kTileSbBytes * KC + (long long)vk::kTileGroupBytes * KG;
-}
 
 }  // namespace
 
@@ -93,7 +89,7 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   if (int rule = vk::moe_shape_status(k, VERIFY_PASS_K, E, down->n_experts, top_k, gate_up->w.n_out,
                                       gate_up->w.k_in, down->w.n_out, down->w.k_in, &why))
     return (verify_status)rule;
-  if (!valid_q4(&gate_up->w, VERIFY_Q4_TILED_GATE_UP) || !valid_q4(&down->w, VERIFY_Q4_TILED)) return VERIFY_EINVAL;
+  if (!valid_q4(&gate_up->w, VERIFY_Q4_TILED_GATE_UP) || !valid_q4(&down->w, VERIFY_Q4_TILED_DOWN)) return VERIFY_EINVAL;
   const int H = gate_up->w.k_in, I = gate_up->w.n_out / 2;
   if (logits_ld < E) return VERIFY_EINVAL;
   if (dtype_out != VERIFY_F32 && dtype_out != VERIFY_BF16 && dtype_out != VERIFY_F32_ADD) return VERIFY_EINVAL;
@@ -104,7 +100,7 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   const int n_shared = (shared_gate_up != nullptr) + (shared_down != nullptr) + (shared_gate_logit != nullptr);
   if (n_shared != 0 && n_shared != 3) return VERIFY_EINVAL;
   if (n_shared == 3) {
-    if (!valid_q4(shared_gate_up, VERIFY_Q4_TILED_GATE_UP) || !valid_q4(shared_down, VERIFY_Q4_TILED) ||
+    if (!valid_q4(shared_gate_up, VERIFY_Q4_TILED_GATE_UP) || !valid_q4(shared_down, VERIFY_Q4_TILED_DOWN) ||
         !device_memory(shared_gate_logit, 4))
       return VERIFY_EINVAL;
     if (shared_gate_up->n_out != 2 * I || shared_gate_up->k_in != H || shared_down->n_out != H ||
@@ -129,8 +125,8 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
     a.sgu_tiles = reinterpret_cast<const uint8_t*>(shared_gate_up->packed);
     a.sdn_tiles = reinterpret_cast<const uint8_t*>(shared_down->packed);
   }
-  a.gu_rt_bytes = rt_bytes(H);
-  a.dn_rt_bytes = rt_bytes(I);
+  a.gu_rt_bytes = vk::tile_row_bytes(H, vk::kExpertGroups);
+  a.dn_rt_bytes = vk::tile_row_bytes(I, vk::kExpertGroups);
   a.hbuf = reinterpret_cast<uint16_t*>(base);
   a.part = reinterpret_cast<float*>(base + hbuf_bytes);
   a.work = err_word + 1;

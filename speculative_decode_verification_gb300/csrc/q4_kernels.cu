@@ -47,16 +47,18 @@
 namespace vk {
 
 // A stage: [scales, biases][codes][activation rows].  The first two parts are
-// one block of the tiled weight layout (tile.cu), copied with one bulk copy.
-template <int NT, int ST = kStages>
+// one block of a tiled weight layout (tile.cu: GPU 64-column groups per
+// block), copied with one bulk copy.
+template <int NT, int ST = kStages, int GPU = kGroupsPerUnit>
 struct Q4Layout {
   static constexpr int STAGES = ST;                          // pipeline depth
+  static constexpr int GROUPS = GPU;                         // 64-column groups per stage
   static constexpr int NB = 8 * NT;                          // activation rows held per stage
-  static constexpr int SB_BYTES = kTileSbBytes;              // scales then biases, [row][4 groups]
-  static constexpr int W_BYTES = kBM * 128;                  // codes, fragment order, [group][16-row block][lane]
-  static constexpr int X_BYTES = kGroupsPerUnit * NB * 128;  // [group][row][64 bf16]
+  static constexpr int SB_BYTES = tile_sb_bytes(GPU);        // scales then biases, [row][GPU groups]
+  static constexpr int W_BYTES = GPU * kTileGroupBytes;      // codes, fragment order, [group][16-row block][lane]
+  static constexpr int X_BYTES = GPU * NB * 128;             // [group][row][64 bf16]
   static constexpr int STAGE = SB_BYTES + W_BYTES + X_BYTES;
-  static constexpr int SX_BYTES = kGroupsPerUnit * NB * 4;   // fp32 group sums [group][row]
+  static constexpr int SX_BYTES = GPU * NB * 4;              // fp32 group sums [group][row]
   static constexpr int SX_OFF = ST * STAGE;                  // one slot per stage, after the stages
   static constexpr int BAR_OFF = SX_OFF + ST * SX_BYTES;
   static constexpr int MISC_OFF = BAR_OFF + 2 * ST * 8;
@@ -65,13 +67,14 @@ struct Q4Layout {
   static_assert(STAGE % 128 == 0, "stages keep 128-byte alignment");
 };
 
-// Where a stage holding NBL activation rows keeps them (the consumer's view).
-template <int NBL>
+// Where a stage of GPU groups holding NBL activation rows keeps them (the
+// consumer's view).
+template <int NBL, int GPU = kGroupsPerUnit>
 struct XLayout {
   static constexpr int NB = NBL;
-  static constexpr int SB_BYTES = kTileSbBytes;
-  static constexpr int W_BYTES = kBM * 128;
-  static constexpr int X_BYTES = kGroupsPerUnit * NBL * 128;
+  static constexpr int SB_BYTES = tile_sb_bytes(GPU);
+  static constexpr int W_BYTES = GPU * kTileGroupBytes;
+  static constexpr int X_BYTES = GPU * NBL * 128;
 };
 
 template <int CW>
@@ -100,44 +103,45 @@ struct RouteSmem {
 // reaches output columns that are never stored (an MMA column depends on its
 // own activation row alone).
 
-// Weight block kc of a row tile (tile: the row tile's first block).  Reads
-// only static data, with the evict-first L2 policy (every weight byte is read
-// once per call).
+// Weight block kc of a row tile (tile: the row tile's first block; GPU
+// groups per block).  Reads only static data, with the evict-first L2 policy
+// (every weight byte is read once per call).
+template <int GPU = kGroupsPerUnit>
 __device__ __forceinline__ void produce_w(uint8_t* stage_ptr, uint32_t full_bar, const uint8_t* tile, int kc,
                                           int gcount) {
-  const uint32_t bytes = kTileSbBytes + gcount * kTileGroupBytes;
+  const uint32_t bytes = tile_sb_bytes(GPU) + gcount * kTileGroupBytes;
   mbar_arrive_expect_tx(full_bar, bytes);
-  bulk_load_hint(smem_addr(stage_ptr), tile + (long long)kc * kTileChunkBytes, bytes, full_bar,
+  bulk_load_hint(smem_addr(stage_ptr), tile + (long long)kc * tile_chunk_bytes(GPU), bytes, full_bar,
                  l2_evict_first_policy());
 }
 
 // Activation rows b < nb (brow: their pointers, in shared memory), then this
 // lane's arrival once all its copies have landed.
-template <int NT>
+template <int NT, int GPU = kGroupsPerUnit>
 __device__ __forceinline__ void produce_x(uint8_t* stage_ptr, uint32_t full_bar, int kc, int gcount,
                                           const uint16_t* const* brow, int nb, int lane) {
-  using L = Q4Layout<NT>;
+  using L = XLayout<8 * NT, GPU>;
   const uint32_t x_dst = smem_addr(stage_ptr) + L::SB_BYTES + L::W_BYTES;
   // [group][row][8 chunks of 16 B], chunk index xor (row & 7)
 #pragma unroll
-  for (int idx = lane; idx < L::NB * 32; idx += 32) {
-    const int b = idx >> 5;
+  for (int idx = lane; idx < L::NB * 8 * GPU; idx += 32) {
+    const int b = idx / (8 * GPU);
     if (b >= nb) break;
-    const int G = (idx >> 3) & 3;
+    const int G = (idx >> 3) % GPU;
     const int ch = idx & 7;
     if (G < gcount)
-      cp_async16(x_dst + G * (L::NB * 128) + b * 128 + ((ch ^ (b & 7)) << 4), brow[b] + kc * 256 + G * 64 + ch * 8,
-                 16u);
+      cp_async16(x_dst + G * (L::NB * 128) + b * 128 + ((ch ^ (b & 7)) << 4),
+                 brow[b] + kc * (64 * GPU) + G * 64 + ch * 8, 16u);
   }
   cp_async_mbar_arrive_noinc(full_bar);
 }
 
 // Fills one stage.
-template <int NT>
+template <int NT, int GPU = kGroupsPerUnit>
 __device__ __forceinline__ void produce_stage(uint8_t* stage_ptr, uint32_t full_bar, const uint8_t* tile, int kc,
                                               int gcount, const uint16_t* const* brow, int nb, int lane) {
-  if (lane == 0) produce_w(stage_ptr, full_bar, tile, kc, gcount);
-  produce_x<NT>(stage_ptr, full_bar, kc, gcount, brow, nb, lane);
+  if (lane == 0) produce_w<GPU>(stage_ptr, full_bar, tile, kc, gcount);
+  produce_x<NT, GPU>(stage_ptr, full_bar, kc, gcount, brow, nb, lane);
 }
 
 // On abort the producer keeps the CTA alive until its bulk copies have landed.
@@ -157,11 +161,11 @@ __device__ __forceinline__ void producer_drain(uint32_t bar_base, long long fill
 // Accumulates group G of a stage into acc for this warp's MT row tiles: NT
 // MMA column blocks (activation rows 0 .. 8 NT - 1) of a stage laid out for
 // NBL activation rows.
-template <int NT, int MT, int NBL, bool MMASUM = false>
+template <int NT, int MT, int NBL, bool MMASUM = false, int GPU = kGroupsPerUnit>
 __device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, uint32_t sx_src, int G,
                                               const uint2 (&sw)[MT][2], const uint2 (&bw)[MT][2],
                                               const int (&rbase)[MT], int lane, float (&acc)[MT][NT][4]) {
-  using L = XLayout<NBL>;
+  using L = XLayout<NBL, GPU>;
   const int g = lane >> 2, c = lane & 3;
   // B fragments: activation row 8t+g, columns 16c .. 16c+15 of the group
   uint32_t bf[NT][8];
@@ -247,12 +251,13 @@ __device__ __forceinline__ void consume_group(uint32_t w_src, uint32_t x_src, ui
 // group sums come either from consumer warp w < 4 adding up group w once per
 // stage (then a named barrier), or with MMASUM from one MMA with an all-ones
 // A operand in every warp, with no barrier (the routed-expert kernel).
-template <int NT, int CW, int NBL, bool MMASUM = false>
+template <int NT, int CW, int NBL, bool MMASUM = false, int GPU = kGroupsPerUnit>
 __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t sx_src, int gcount,
                                               const int (&rbase)[Warps<CW>::MT], int lane,
                                               float (&acc)[Warps<CW>::MT][NT][4], bool ok) {
   static_assert(NBL >= 8 * NT, "stage holds too few activation rows");
-  using L = XLayout<NBL>;
+  static_assert(MMASUM || GPU == 4, "per-warp group sums need one consumer warp per group");
+  using L = XLayout<NBL, GPU>;
   constexpr int MT = Warps<CW>::MT;
   const uint32_t sb_src = smem_addr(stage_ptr);
   const uint32_t w_src = sb_src + L::SB_BYTES;
@@ -282,24 +287,32 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage_ptr, uint32_t
       if (c == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(sx_src + (w * L::NB + b) * 4), "f"(part) : "memory");
     }
   }
-  // scales / biases of this thread's rows, four groups each
+  // scales / biases of this thread's rows, GPU groups each ([row][GPU] bf16;
+  // with two groups the pair sits in .x)
   uint2 sw[MT][2], bw[MT][2];
 #pragma unroll
   for (int m = 0; m < MT; ++m)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = rbase[m] + g + 8 * h;
-      sw[m][h] = lds64(sb_src + row * 8);
-      bw[m][h] = lds64(sb_src + kBM * 8 + row * 8);
+      if (GPU == 4) {
+        sw[m][h] = lds64(sb_src + row * 8);
+        bw[m][h] = lds64(sb_src + kBM * 8 + row * 8);
+      } else {
+        static_assert(GPU == 4 || GPU == 2, "two or four groups per stage");
+        sw[m][h] = make_uint2(lds32(sb_src + row * 4), 0u);
+        bw[m][h] = make_uint2(lds32(sb_src + kBM * 4 + row * 4), 0u);
+      }
     }
   if (!MMASUM) named_bar(2, CW * 32);
-  if (gcount == kGroupsPerUnit) {
+  if (gcount == GPU) {
 #pragma unroll
-    for (int G = 0; G < kGroupsPerUnit; ++G)
-      consume_group<NT, MT, NBL, MMASUM>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
+    for (int G = 0; G < GPU; ++G)
+      consume_group<NT, MT, NBL, MMASUM, GPU>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
   } else {
 #pragma unroll 1
-    for (int G = 0; G < gcount; ++G) consume_group<NT, MT, NBL, MMASUM>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
+    for (int G = 0; G < gcount; ++G)
+      consume_group<NT, MT, NBL, MMASUM, GPU>(w_src, x_src, sx_src, G, sw, bw, rbase, lane, acc);
   }
 }
 
@@ -747,11 +760,11 @@ __device__ __forceinline__ int pairs_of(const RouteSmem* rs, const MoeArgs& a, i
 
 // One item of a MoE kernel on the consumer side: the stage loop and the
 // epilogue.  The item covers rows 8 rc .. 8 rc + nb - 1 of expert slot u.
-template <int CW, bool GATEUP, int ST>
+template <int CW, bool GATEUP, int ST, int GPU>
 __device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, uint8_t* smem, uint32_t bar_base,
                                          volatile int* abort, int u, int rc, int tile, int nb, int KC, int KG, int TS,
                                          const int (&rbase)[Warps<CW>::MT], int lane, long long& fills) {
-  using L = Q4Layout<1, ST>;
+  using L = Q4Layout<1, ST, GPU>;
   constexpr int MT = Warps<CW>::MT;
   const int warp = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
   float acc[MT][1][4];
@@ -760,9 +773,9 @@ __device__ __forceinline__ void moe_item(const MoeArgs& a, const RouteSmem* rs, 
     const int s = (int)(fills % ST);
     const uint32_t ph = (uint32_t)((fills / ST) & 1);
     const bool ok = mbar_wait(bar_base + 8 * s, ph, abort, a.err);
-    const int gcount = min(kGroupsPerUnit, KG - 4 * kc);
-    consume_stage<1, CW, L::NB, true>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount, rbase,
-                                lane, acc, ok);
+    const int gcount = min(GPU, KG - GPU * kc);
+    consume_stage<1, CW, L::NB, true, GPU>(smem + s * L::STAGE, smem_addr(smem + L::SX_OFF + s * L::SX_BYTES), gcount,
+                                           rbase, lane, acc, ok);
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_base + 8 * (ST + s));
   }
@@ -879,8 +892,8 @@ __device__ __forceinline__ void moe_decode(const MoeArgs& a, const RouteSmem* rs
 
 __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) moe_kernel(const MoeArgs a) {
   static_assert(kGateUpWarps == kDownWarps, "both item kinds share one CTA shape");
-  constexpr int ST = kMoeStages;
-  using L = Q4Layout<1, ST>;
+  constexpr int ST = kMoeStages, GPU = kExpertGroups;
+  using L = Q4Layout<1, ST, GPU>;
   constexpr int CW = kGateUpWarps, MT = Warps<CW>::MT;
   static_assert(MT == 2, "gate/up pairs the gate and up row tiles in one warp");
   extern __shared__ uint8_t smem_raw[];
@@ -916,8 +929,8 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
   const int TS = a.T + a.has_shared;
   const int ntg = a.I / 64, ntd = (a.H + kBM - 1) / kBM;
   const int n_gu = rs->V * ntg, n_all = n_gu + rs->V * ntd;
-  const int KGg = a.H / 64, KCg = (KGg + kGroupsPerUnit - 1) / kGroupsPerUnit;
-  const int KGd = a.I / 64, KCd = (KGd + kGroupsPerUnit - 1) / kGroupsPerUnit;
+  const int KGg = a.H / 64, KCg = (KGg + GPU - 1) / GPU;
+  const int KGd = a.I / 64, KCd = (KGd + GPU - 1) / GPU;
 
   if (warp == CW) {
     // ------------------------------------------------------------ producer
@@ -978,8 +991,8 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
         const uint32_t ph = (uint32_t)((fills / ST) & 1);
         if (kc > 0 && !mbar_wait(bar_base + 8 * (ST + s), ph ^ 1, abort, a.err)) break;
         if (kc == 0 && lane == 0) slot_item[s] = item;
-        produce_stage<1>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, min(kGroupsPerUnit, KG - 4 * kc), brow, nb,
-                         lane);
+        produce_stage<1, GPU>(smem + s * L::STAGE, bar_base + 8 * s, ts, kc, min(GPU, KG - GPU * kc), brow, nb,
+                              lane);
       }
       // The next item, fetched once this item's stages are all issued: an
       // atomic still in flight would hold up this lane's next barrier arrival
@@ -1011,7 +1024,7 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
     moe_decode(a, rs, item, n_gu, ntg, ntd, gu, v, u, rc, tile, nb);
     if (gu) {
       const int rbase[MT] = {16 * warp, 64 + 16 * warp};
-      moe_item<CW, true, ST>(a, rs, smem, bar_base, abort, u, rc, tile, nb, KCg, KGg, TS, rbase, lane, fills);
+      moe_item<CW, true, ST, GPU>(a, rs, smem, bar_base, abort, u, rc, tile, nb, KCg, KGg, TS, rbase, lane, fills);
       // publish this tile of the unit's h rows
       named_bar(3, CW * 32);
       if (threadIdx.x == 0) {
@@ -1020,7 +1033,7 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
       }
     } else {
       const int rbase[MT] = {16 * (warp * MT), 16 * (warp * MT + 1)};
-      moe_item<CW, false, ST>(a, rs, smem, bar_base, abort, u, rc, tile, nb, KCd, KGd, TS, rbase, lane, fills);
+      moe_item<CW, false, ST, GPU>(a, rs, smem, bar_base, abort, u, rc, tile, nb, KCd, KGd, TS, rbase, lane, fills);
     }
   }
 }
@@ -1030,7 +1043,7 @@ __global__ void __launch_bounds__(Warps<kGateUpWarps>::THREADS, kMoeCtasPerSm) m
 template <int NT>
 static size_t dense_smem() { return Q4Layout<NT>::BASE_BYTES + 1024; }
 template <int NT>
-static size_t moe_smem() { return Q4Layout<NT, kMoeStages>::BASE_BYTES + sizeof(RouteSmem) + 1024; }
+static size_t moe_smem() { return Q4Layout<NT, kMoeStages, kExpertGroups>::BASE_BYTES + sizeof(RouteSmem) + 1024; }
 
 template <typename F>
 static cudaError_t setup_one(F* kernel, int threads, size_t smem, int* ctas_per_sm) {

@@ -99,8 +99,9 @@ verify_status check_q4(verify_ctx* ctx, const verify_q4_weight* W, const char* n
   if (W->group_size != 64 || W->bits != 4) return fail(ctx, VERIFY_EUNSUPPORTED, "%s: only 4-bit, group 64", name);
   if (W->layout != layout)
     return fail(ctx, VERIFY_EINVAL,
-                layout == VERIFY_Q4_TILED_GATE_UP ? "%s: expected the gate/up tiled layout (q4_tile with gate_up)"
-                                                  : "%s: expected the tiled layout (q4_tile)",
+                layout == VERIFY_Q4_TILED_GATE_UP ? "%s: expected the gate/up tiled layout (q4_tile, VERIFY_TILE_GATE_UP)"
+                : layout == VERIFY_Q4_TILED_DOWN  ? "%s: expected the expert down layout (q4_tile, VERIFY_TILE_DOWN)"
+                                                  : "%s: expected the dense tiled layout (q4_tile, VERIFY_TILE_DENSE)",
                 name);
   if (!valid_shape(W->n_out, W->k_in))
     return fail(ctx, VERIFY_EUNSUPPORTED, "%s: n_out in 1..2^20, k_in a multiple of 64 in [64, 131072]", name);
@@ -109,10 +110,8 @@ verify_status check_q4(verify_ctx* ctx, const verify_q4_weight* W, const char* n
   return check_dev(ctx, W->packed, 16, name);
 }
 
-long long rt_bytes(int k_in) {
-  const long long KG = k_in / 64, KC = (KG + vk::kGroupsPerUnit - 1) / vk::kGroupsPerUnit;
-  return (long long)vk::kTileSbBytes * KC + (long long)vk::kTileGroupBytes * KG;
-}
+// bytes of one 128-row tile of a matrix with k_in columns in the dense layout
+long long rt_bytes(int k_in) { return vk::tile_row_bytes(k_in, vk::kGroupsPerUnit); }
 
 // K-splits per row tile: the largest S (at most 16, the largest cluster,
 // and at most one split per 256-column chunk) whose RB clusters of S CTAs all
@@ -252,12 +251,13 @@ verify_status verify_selftest_stuck_wait(verify_ctx* ctx, struct CUstream_st* st
   return VERIFY_OK;
 }
 
-int64_t q4_tiled_bytes(int32_t n_out, int32_t k_in, int32_t n_experts, int32_t gate_up) {
-  if (!valid_shape(n_out, k_in) || n_experts < 1 || (gate_up && n_out % 128 != 0)) return -1;
-  return vk::tiled_bytes(n_out, k_in, n_experts, gate_up != 0);
+int64_t q4_tiled_bytes(int32_t n_out, int32_t k_in, int32_t n_experts, int32_t kind) {
+  if (kind != VERIFY_TILE_DENSE && kind != VERIFY_TILE_GATE_UP && kind != VERIFY_TILE_DOWN) return -1;
+  if (!valid_shape(n_out, k_in) || n_experts < 1 || (kind == VERIFY_TILE_GATE_UP && n_out % 128 != 0)) return -1;
+  return vk::tiled_bytes(n_out, k_in, n_experts, kind);
 }
 
-verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_experts, int32_t gate_up, void* dst,
+verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_experts, int32_t kind, void* dst,
                       int64_t dst_bytes, verify_q4_weight* out, struct CUstream_st* stream) {
   if (!ctx) return VERIFY_EINVAL;
   verify_status s;
@@ -265,7 +265,9 @@ verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_ex
   if (!src || !out) return fail(ctx, VERIFY_EINVAL, "src or out is NULL%s");
   if (src->layout != VERIFY_Q4_ROWS) return fail(ctx, VERIFY_EINVAL, "src must have the row layout%s");
   if (src->group_size != 64 || src->bits != 4) return fail(ctx, VERIFY_EUNSUPPORTED, "only 4-bit, group 64%s");
-  const int64_t need = q4_tiled_bytes(src->n_out, src->k_in, n_experts, gate_up);
+  if (kind != VERIFY_TILE_DENSE && kind != VERIFY_TILE_GATE_UP && kind != VERIFY_TILE_DOWN)
+    return fail(ctx, VERIFY_EUNSUPPORTED, "unknown tile kind%s");
+  const int64_t need = q4_tiled_bytes(src->n_out, src->k_in, n_experts, kind);
   if (need < 0) return fail(ctx, VERIFY_EUNSUPPORTED, "shape or n_experts out of range%s");
   if (dst_bytes < need) return fail(ctx, VERIFY_EINVAL, "dst_bytes is smaller than q4_tiled_bytes%s");
   if ((s = check_dev(ctx, src->packed, 4, "packed"))) return s;
@@ -273,14 +275,16 @@ verify_status q4_tile(verify_ctx* ctx, const verify_q4_weight* src, int32_t n_ex
   if ((s = check_dev(ctx, src->biases, 2, "biases"))) return s;
   if ((s = check_dev(ctx, dst, 16, "dst"))) return s;
   cudaError_t e = vk::launch_tile(src->packed, src->scales, src->biases, static_cast<uint8_t*>(dst), src->n_out,
-                                  src->k_in, n_experts, gate_up != 0, stream);
+                                  src->k_in, n_experts, kind, stream);
   if (e) return cuda_fail(ctx, e, "q4_tile launch");
   ctx->launches += 1;
   *out = *src;
   out->packed = static_cast<const uint32_t*>(dst);
   out->scales = nullptr;
   out->biases = nullptr;
-  out->layout = gate_up ? VERIFY_Q4_TILED_GATE_UP : VERIFY_Q4_TILED;
+  out->layout = kind == VERIFY_TILE_GATE_UP ? VERIFY_Q4_TILED_GATE_UP
+                : kind == VERIFY_TILE_DOWN  ? VERIFY_Q4_TILED_DOWN
+                                            : VERIFY_Q4_TILED;
   return VERIFY_OK;
 }
 
@@ -331,7 +335,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
                                       down->w.n_out, down->w.k_in, &why))
     return fail(ctx, (verify_status)rule, why);
   if ((s = check_q4(ctx, &gate_up->w, "gate_up", VERIFY_Q4_TILED_GATE_UP))) return s;
-  if ((s = check_q4(ctx, &down->w, "down"))) return s;
+  if ((s = check_q4(ctx, &down->w, "down", VERIFY_Q4_TILED_DOWN))) return s;
   const int H = gate_up->w.k_in, I = gate_up->w.n_out / 2;
   if (logits_ld < E) return fail(ctx, VERIFY_EINVAL, "logits_ld < n_experts%s");
   if ((s = check_dtype(ctx, dtype_out, true))) return s;
@@ -345,7 +349,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
     return fail(ctx, VERIFY_EINVAL, "shared expert: give all of gate_up, down and gate logit, or none%s");
   if (n_shared == 3) {
     if ((s = check_q4(ctx, shared_gate_up, "shared_gate_up", VERIFY_Q4_TILED_GATE_UP))) return s;
-    if ((s = check_q4(ctx, shared_down, "shared_down"))) return s;
+    if ((s = check_q4(ctx, shared_down, "shared_down", VERIFY_Q4_TILED_DOWN))) return s;
     if (shared_gate_up->n_out != 2 * I || shared_gate_up->k_in != H || shared_down->n_out != H ||
         shared_down->k_in != I)
       return fail(ctx, VERIFY_EINVAL, "shared expert shape differs from the routed experts%s");
@@ -361,8 +365,8 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
     a.sgu_tiles = reinterpret_cast<const uint8_t*>(shared_gate_up->packed);
     a.sdn_tiles = reinterpret_cast<const uint8_t*>(shared_down->packed);
   }
-  a.gu_rt_bytes = rt_bytes(H);
-  a.dn_rt_bytes = rt_bytes(I);
+  a.gu_rt_bytes = vk::tile_row_bytes(H, vk::kExpertGroups);
+  a.dn_rt_bytes = vk::tile_row_bytes(I, vk::kExpertGroups);
   a.hbuf = ctx->moe_hbuf; a.part = ctx->moe_part;
   a.work = ctx->moe_sched; a.done = ctx->moe_sched + 2 + vk::kMoeSmSlots;
   a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;

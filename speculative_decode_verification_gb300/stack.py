@@ -56,7 +56,7 @@ class DeviceStack:
         self.states = (B.GdnState * self.n_layers)()
         self.state_tensors = []
 
-        def q4(name, n_out, k_in, n_experts=None, gate_up=False):
+        def q4(name, n_out, k_in, n_experts=None, gate_up=False, down=False):
             # drawn in the row layout, kept only in the tiled layout
             e = 1 if n_experts is None else n_experts
             shp = (e, n_out, k_in // 8) if n_experts else (n_out, k_in // 8)
@@ -66,7 +66,7 @@ class DeviceStack:
             bi = torch.empty(gshp, dtype=torch.int16, device="cuda")
             vf.synth_q4(p, sc, bi, S.q4_seeds(seed, name), S.SCALE_RANGE, S.CENTERED_RANGE, centered=True)
             rows = B.q4_experts(p, sc, bi) if n_experts else B.q4_weight(p, sc, bi)
-            t = vf.tile(rows, gate_up=gate_up)
+            t = vf.tile(rows, gate_up=gate_up, down=down)
             torch.cuda.synchronize()
             if keep_rows:
                 self.rows.append((p, sc, bi))
@@ -87,9 +87,9 @@ class DeviceStack:
             L.out_proj = q4(nm["out_proj"], H, sh["Z"])
             L.router = q4(nm["router"], E + 1, H)
             L.gate_up = q4(nm["gate_up"], 2 * I, H, E, gate_up=True)
-            L.down = q4(nm["down"], H, I, E)
+            L.down = q4(nm["down"], H, I, E, down=True)
             L.shared_gate_up = q4(nm["shared_gate_up"], 2 * I, H, gate_up=True)
-            L.shared_down = q4(nm["shared_down"], H, I)
+            L.shared_down = q4(nm["shared_down"], H, I, down=True)
             L.gdn = B.gdn_params(Hk, Hv, d, gp["conv_w"], gp["A_log"], gp["dt_bias"], gp["norm_w"])
             L.norm1_w = dev(S.f32_uniform(seed, nm["norm1"], (H,), -0.1, 0.1)).data_ptr()
             L.norm2_w = dev(S.f32_uniform(seed, nm["norm2"], (H,), -0.1, 0.1)).data_ptr()

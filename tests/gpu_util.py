@@ -31,15 +31,16 @@ def host(t, dtype=None):
 
 class DevQ4:
     """A Q4Matrix (synth) copied to the device in the row layout (`rows`), and
-    its tiled form for the compute calls (`struct`, kept alive by `tiled`)."""
+    its tiled form for the compute calls (`struct`, kept alive by `tiled`):
+    gate_up / down for an expert's gate/up or down matrix, else dense."""
 
-    def __init__(self, vf, m, gate_up=False):
+    def __init__(self, vf, m, gate_up=False, down=False):
         self.packed, self.scales, self.biases = dev(m.packed), dev(m.scales), dev(m.biases)
         if m.packed.ndim == 3:
             self.rows = B.q4_experts(self.packed, self.scales, self.biases)
         else:
             self.rows = B.q4_weight(self.packed, self.scales, self.biases)
-        self.tiled = vf.tile(self.rows, gate_up=gate_up)
+        self.tiled = vf.tile(self.rows, gate_up=gate_up, down=down)
         self.struct = self.tiled.struct
 
 

@@ -33,7 +33,7 @@ def run():
     idx = torch.zeros((k, T), dtype=torch.int32, device="cuda")
     w = torch.zeros((k, T), device="cuda")
     ym = torch.zeros((k, H), device="cuda")
-    GU, DN = DevQ4(vf, gu, True), DevQ4(vf, dn)
+    GU, DN = DevQ4(vf, gu, True), DevQ4(vf, dn, down=True)
     lgd, xmd = dev(lg), dev(xm)
     vf.q4_gather_experts_k(GU.struct, DN.struct, lgd, E, T, xmd, k, idx, w, ym)
     torch.cuda.synchronize()

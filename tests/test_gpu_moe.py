@@ -61,7 +61,7 @@ def test_small_moe_matches_oracle(vf, k):
     logits = S.f32_normal(10, f"moe.l{k}", (k, E))
     oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
                                      logits, T, x)
-    gud, dnd = DevQ4(vf, gu, True), DevQ4(vf, dn)
+    gud, dnd = DevQ4(vf, gu, True), DevQ4(vf, dn, down=True)
     before = vf.launch_count()
     gi, gw, gy = gather(vf, gud, dnd, dev(logits), T, dev(x), k, H)
     # the routing kernel, the routed experts kernel, then the combine, per pass of up to 16 rows
@@ -86,7 +86,7 @@ def test_routing_ties_and_crowded_lanes(vf):
     lg = lg.astype(np.float32)
     oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
                                      lg, T, x)
-    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(lg), T, dev(x), k, H)
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn, down=True), dev(lg), T, dev(x), k, H)
     assert np.array_equal(gi, oi)
     np.testing.assert_allclose(gw, ow, rtol=1e-5, atol=1e-6)
     assert_close(gy, oy, what="ties")
@@ -102,7 +102,7 @@ def test_moe_with_k_not_a_multiple_of_128(vf, k):
     logits = S.f32_normal(12, f"moe.r.l{k}", (k, E))
     oi, ow, oy, _ = O.gather_experts((gu.packed, gu.scales, gu.biases), (dn.packed, dn.scales, dn.biases),
                                      logits, T, x)
-    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(logits), T, dev(x), k, H)
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn, down=True), dev(logits), T, dev(x), k, H)
     assert np.array_equal(gi, oi)
     assert_close(gy, oy, what=f"H=320 I=192 k={k}")
 
@@ -123,8 +123,8 @@ def test_shared_expert_and_ragged_down(vf):
     # the shared gate logit is read at row stride logits_ld = E: store it in a [k, E] array
     slm = np.zeros((k, E), np.float32)
     slm[:, 0] = sl
-    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(logits), T, dev(x), k, H,
-                        shared=(DevQ4(vf, sgu, True), DevQ4(vf, sdn), dev(slm)))
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn, down=True), dev(logits), T, dev(x), k, H,
+                        shared=(DevQ4(vf, sgu, True), DevQ4(vf, sdn, down=True), dev(slm)))
     assert np.array_equal(gi, oi)
     assert_close(gy, oy, what="shared")
 
@@ -132,7 +132,7 @@ def test_shared_expert_and_ragged_down(vf):
 def test_width_k_rows_bit_identical_to_width_1(vf):
     E, H, I, T = 32, 512, 256, 8
     gu, dn = moe_case(12, E, H, I)
-    G, D = DevQ4(vf, gu, True), DevQ4(vf, dn)
+    G, D = DevQ4(vf, gu, True), DevQ4(vf, dn, down=True)
     x = S.bf16_normal(12, "moe.xb", (9, H))
     logits = S.f32_normal(12, "moe.lb", (9, E))
     _, _, y9 = gather(vf, G, D, dev(logits), T, dev(x), 9, H)
@@ -151,7 +151,7 @@ def test_single_expert_reduces_to_dense_products(vf):
     logits = np.full((k, E), -2.0, np.float32)
     logits[:, 5] = 3.0
     x = S.bf16_normal(13, "moe.x1", (k, H))
-    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn), dev(logits), 1, dev(x), k, H)
+    gi, gw, gy = gather(vf, DevQ4(vf, gu, True), DevQ4(vf, dn, down=True), dev(logits), 1, dev(x), k, H)
     assert np.all(gi == 5) and np.all(gw == 1.0)
     Wg = DevQ4(vf, S.Q4Matrix(gu.packed[5], gu.scales[5], gu.biases[5], 2 * I, H))
     Wd = DevQ4(vf, S.Q4Matrix(dn.packed[5], dn.scales[5], dn.biases[5], H, I))
@@ -186,7 +186,7 @@ def test_ornith_shape_matches_oracle(vf):
     vf.synth_q4(dn_p, dn_s, dn_b, seeds_dn, S.SCALE_RANGE, S.BIAS_RANGE)
 
     G = vf.tile(B.q4_experts(gu_p, gu_s, gu_b), gate_up=True)
-    D = vf.tile(B.q4_experts(dn_p, dn_s, dn_b))
+    D = vf.tile(B.q4_experts(dn_p, dn_s, dn_b), down=True)
     experts = {}
 
     def expert(e):
@@ -224,7 +224,7 @@ def test_width_32_rows_equal_single_rows(vf):
     gu, dn = moe_case(15, E, H, I)
     x = S.bf16_normal(15, "moe.w32.x", (k, H))
     logits = S.f32_normal(15, "moe.w32.l", (k, E))
-    gud, dnd = DevQ4(vf, gu, True), DevQ4(vf, dn)
+    gud, dnd = DevQ4(vf, gu, True), DevQ4(vf, dn, down=True)
     gi, gw, gy = gather(vf, gud, dnd, dev(logits), T, dev(x), k, H)
     for r in (0, 7, 15, 16, 24, 31):
         i1, w1, y1 = gather(vf, gud, dnd, dev(logits[r:r + 1]), T, dev(x[r:r + 1]), 1, H)
@@ -243,7 +243,7 @@ def test_progress_beside_a_concurrent_kernel(vf, k):
 
     E, H, I, T = 64, 1024, 512, 8
     gu, dn = moe_case(16, E, H, I)
-    G, D = DevQ4(vf, gu, True), DevQ4(vf, dn)
+    G, D = DevQ4(vf, gu, True), DevQ4(vf, dn, down=True)
     x = dev(S.bf16_normal(16, f"moe.cc.x{k}", (k, H)))
     logits = dev(S.f32_normal(16, f"moe.cc.l{k}", (k, E)))
     ref = gather(vf, G, D, logits, T, x, k, H)

@@ -2,9 +2,10 @@
 host description of the format, on shapes with a ragged last row tile, a
 partial last column chunk, the gate/up pairing and expert stacks.
 
-Format (include/verify.h, q4_tile): per (128-row tile, 256-column chunk) one
-block = scales [128 rows][4 groups] bf16, biases likewise, then for each
-group present: for 16-row block b and lane L = 4g + c the words
+Format (include/verify.h, q4_tile): per (128-row tile, chunk of G 64-column
+groups; G = 4 for dense products, 2 for the experts' gate/up and down
+matrices) one block = scales [128 rows][G groups] bf16, biases likewise,
+then for each group present: for 16-row block b and lane L = 4g + c the words
 (row 16b+g W0, row 16b+g+8 W0, row 16b+g W1, row 16b+g+8 W1), where Ww holds
 columns 16c + 8w .. 16c + 8w + 7 of the group with nibble p taken from
 column 16c + 8w + sigma(p), sigma = (0 4 2 6 1 5 3 7).  Rows past the matrix
@@ -30,10 +31,10 @@ def permute_word(u):
     return out
 
 
-def tile_host(packed, scales, biases, N, K, gate_up):
+def tile_host(packed, scales, biases, N, K, gate_up, GR=4):
     """Tiled bytes of one matrix [N, K] (row layout: packed uint32 [N, K/8],
-    scales/biases uint16 [N, K/64])."""
-    KG, KC, KW = K // 64, (K // 64 + 3) // 4, K // 8
+    scales/biases uint16 [N, K/64]), GR groups per chunk."""
+    KG, KC, KW = K // 64, (K // 64 + GR - 1) // GR, K // 8
     RT = N // 128 if gate_up else (N + 127) // 128
     out = bytearray()
     for rt in range(RT):
@@ -42,13 +43,13 @@ def tile_host(packed, scales, biases, N, K, gate_up):
         else:
             rows = [rt * 128 + i if rt * 128 + i < N else -1 for i in range(128)]
         for kc in range(KC):
-            gcount = min(4, KG - 4 * kc)
-            sb = np.zeros((2, 128, 4), np.uint16)
+            gcount = min(GR, KG - GR * kc)
+            sb = np.zeros((2, 128, GR), np.uint16)
             for i, r in enumerate(rows):
                 if r >= 0:
                     for G in range(gcount):
-                        sb[0, i, G] = scales[r, 4 * kc + G]
-                        sb[1, i, G] = biases[r, 4 * kc + G]
+                        sb[0, i, G] = scales[r, GR * kc + G]
+                        sb[1, i, G] = biases[r, GR * kc + G]
             out += sb.tobytes()
             for G in range(gcount):
                 blk = np.zeros((8, 32, 4), np.uint32)
@@ -56,7 +57,7 @@ def tile_host(packed, scales, biases, N, K, gate_up):
                     for lane in range(32):
                         g, c = lane >> 2, lane & 3
                         r0, r1 = rows[16 * b + g], rows[16 * b + g + 8]
-                        wi = 8 * (4 * kc + G) + 2 * c
+                        wi = 8 * (GR * kc + G) + 2 * c
                         w = lambda r, o: permute_word(packed[r, wi + o]) if r >= 0 else 0  # noqa: E731
                         blk[b, lane] = [w(r0, 0), w(r1, 0), w(r0, 1), w(r1, 1)]
                 out += blk.tobytes()
@@ -70,25 +71,30 @@ def vf():
     v.close()
 
 
-@pytest.mark.parametrize("N,K,E,gate_up", [(200, 576, 1, False), (128, 256, 1, False), (384, 192, 2, True),
-                                           (130, 640, 2, False)])
-def test_tiled_bytes_match_the_format(vf, N, K, E, gate_up):
+@pytest.mark.parametrize("N,K,E,kind", [(200, 576, 1, B.TILE_DENSE), (128, 256, 1, B.TILE_DENSE),
+                                        (384, 192, 2, B.TILE_GATE_UP), (130, 640, 2, B.TILE_DENSE),
+                                        (256, 448, 3, B.TILE_GATE_UP), (130, 640, 2, B.TILE_DOWN),
+                                        (200, 576, 1, B.TILE_DOWN), (384, 64, 1, B.TILE_DOWN)])
+def test_tiled_bytes_match_the_format(vf, N, K, E, kind):
     import torch
 
     m = S.q4_matrix(7, f"tile.{N}.{K}", N, K, n_experts=E if E > 1 else None)
     keep = (dev(m.packed), dev(m.scales), dev(m.biases))  # alive while the struct points at them
     W = B.q4_experts(*keep) if E > 1 else B.q4_weight(*keep)
-    t = vf.tile(W, gate_up=gate_up)
+    gate_up = kind == B.TILE_GATE_UP
+    t = vf.tile(W, gate_up=gate_up, down=kind == B.TILE_DOWN)
     torch.cuda.synchronize()
     got = host(t.buf).tobytes()
     P = m.packed.reshape(E, N, K // 8)
     Sc = m.scales.reshape(E, N, K // 64)
     Bi = m.biases.reshape(E, N, K // 64)
-    want = b"".join(tile_host(P[e], Sc[e], Bi[e], N, K, gate_up) for e in range(E))
-    assert len(got) == len(want) == vf.lib.q4_tiled_bytes(N, K, E, int(gate_up))
+    GR = 4 if kind == B.TILE_DENSE else 2
+    want = b"".join(tile_host(P[e], Sc[e], Bi[e], N, K, gate_up, GR) for e in range(E))
+    assert len(got) == len(want) == vf.lib.q4_tiled_bytes(N, K, E, kind)
     assert got == want
     s = t.struct.w if E > 1 else t.struct
-    assert s.layout == (B.TILED_GATE_UP if gate_up else B.TILED) and not s.scales and not s.biases
+    layout = {B.TILE_DENSE: B.TILED, B.TILE_GATE_UP: B.TILED_GATE_UP, B.TILE_DOWN: B.TILED_DOWN}[kind]
+    assert s.layout == layout and not s.scales and not s.biases
     del keep
 
 
@@ -112,3 +118,8 @@ def test_tile_rejects_bad_arguments(vf):
     st = vf.lib.q4_tile(vf.ctx, C.byref(W), 1, 0, C.c_void_p(small.data_ptr()), 16, C.byref(out), None)
     assert st == B.EINVAL  # dst smaller than q4_tiled_bytes
     assert vf.lib.q4_tiled_bytes(128, 100, 1, 0) == -1
+    assert vf.lib.q4_tiled_bytes(128, 256, 1, 3) == -1  # no such tile kind
+    with pytest.raises(B.VerifyError) as e:  # the experts' down layout is not a dense operand
+        vf.q4_qmv_k(vf.tile(W, down=True).struct, torch.zeros((1, 256), dtype=torch.int16, device="cuda"), 1,
+                    torch.zeros((1, 128), device="cuda"))
+    assert e.value.status == B.EINVAL

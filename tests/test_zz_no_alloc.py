@@ -54,7 +54,8 @@ def test_noalloc_matches_regular_entry_point_on_two_calls():
     dn = S.q4_matrix(50, "na.dn", H, I, n_experts=E)
     sgu = S.q4_matrix(50, "na.sgu", 2 * I, H)
     sdn = S.q4_matrix(50, "na.sdn", H, I)
-    GU, DN, SGU, SDN = DevQ4(vf, gu, True), DevQ4(vf, dn), DevQ4(vf, sgu, True), DevQ4(vf, sdn)
+    GU, DN, SGU, SDN = (DevQ4(vf, gu, True), DevQ4(vf, dn, down=True), DevQ4(vf, sgu, True),
+                        DevQ4(vf, sdn, down=True))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for call, (k, dtype, with_shared) in enumerate(CASES):
         x = dev(S.bf16_normal(50, f"na.x{call}", (k, H)))
@@ -100,10 +101,10 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     lib = B.load()
     E, H, I, T, k = 16, 8192, 256, 16, 16  # k*T*H*4 = 8 MiB of partials alone: too large
     # tiled operands of the right shapes (the call stops at the size check)
-    gu = torch.zeros(int(lib.q4_tiled_bytes(2 * I, H, E, 1)), dtype=torch.uint8, device="cuda")
-    dn = torch.zeros(int(lib.q4_tiled_bytes(H, I, E, 0)), dtype=torch.uint8, device="cuda")
+    gu = torch.zeros(int(lib.q4_tiled_bytes(2 * I, H, E, B.TILE_GATE_UP)), dtype=torch.uint8, device="cuda")
+    dn = torch.zeros(int(lib.q4_tiled_bytes(H, I, E, B.TILE_DOWN)), dtype=torch.uint8, device="cuda")
     GU = B.Q4Experts(B.Q4Weight(gu.data_ptr(), None, None, 2 * I, H, 64, 4, B.TILED_GATE_UP), E)
-    DN = B.Q4Experts(B.Q4Weight(dn.data_ptr(), None, None, H, I, 64, 4, B.TILED), E)
+    DN = B.Q4Experts(B.Q4Weight(dn.data_ptr(), None, None, H, I, 64, 4, B.TILED_DOWN), E)
     x = torch.zeros((k, H), dtype=torch.int16, device="cuda")
     logits = torch.zeros((k, E), device="cuda")
     idx = torch.zeros((k, E), dtype=torch.int32, device="cuda")
@@ -127,7 +128,7 @@ def test_noalloc_applies_the_regular_shape_rules(H, I, k):
     gu = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     dn = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     GU = B.Q4Experts(B.Q4Weight(gu.data_ptr(), None, None, 2 * I, H, 64, 4, B.TILED_GATE_UP), E)
-    DN = B.Q4Experts(B.Q4Weight(dn.data_ptr(), None, None, H, I, 64, 4, B.TILED), E)
+    DN = B.Q4Experts(B.Q4Weight(dn.data_ptr(), None, None, H, I, 64, 4, B.TILED_DOWN), E)
     x = torch.zeros((k, H), dtype=torch.int16, device="cuda")
     logits = torch.zeros((k, E), device="cuda")
     idx = torch.zeros((k, T), dtype=torch.int32, device="cuda")
