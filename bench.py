@@ -46,16 +46,17 @@ EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
 
 # DRAM traffic of the routed-expert kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum) of both layers of a 2-layer
-# stack at k = 9: 421.35 MB over two launches whose algorithmic bytes sum to
-# 2 x 206226468.  Expert traffic grows with the distinct experts read, like the
-# algorithmic bytes, so a full launch's traffic is this ratio times its bytes.
-# The figure holds only for the kernel sources it was taken on; any change to
-# them reports null until the kernel is captured again.
-MOE_TRAFFIC_RATIO = 423.830272e6 / (2 * 206226468.0)
+# stack at k = 9: 412.19 MB read and 5.98 MB written over two launches whose
+# algorithmic bytes sum to 2 x 206226468.  Expert traffic grows with the
+# distinct experts read, like the algorithmic bytes, so a full launch's
+# traffic is this ratio times its bytes.  The figure holds only for the
+# kernel sources it was taken on; any change to them reports null until the
+# kernel is captured again.
+MOE_TRAFFIC_RATIO = 418.17472e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
-    "q4_kernels.cu": "e0c27f19fe5ac111744c11abf6e218398ab77b9a9f90a8d402364cab98e7be92",
-    "common.cuh": "249c762d042e43ac9c4c4d180b4ceee3ec2cba7f6f77f10aca9458f16499efa2",
-    "internal.h": "ad24c5d3d06bbb017f43bbc27b7628d9fdcc31aaa44027c2c684c26918761823",
+    "q4_kernels.cu": "7c2684ed52c90a824ba00ea4c146d3ad0c4be127b4851875a351b2b4b438ad35",
+    "common.cuh": "3c7de14039580caf156b44b6e1c560f4cc81b8c0cb9346e712921c24b6aafcfd",
+    "internal.h": "4c192abe46cbaf6257ad563a1d289d447c040ff68ace2f8baa723d2a49c93924",
 }
 
 

@@ -73,6 +73,45 @@ def bits16(t):
     return host(t).view(np.uint16)
 
 
+def _bf_ulp(v):
+    """Spacing of bf16 values at |v| (float64)."""
+    e = np.floor(np.log2(np.maximum(np.abs(v), 1e-30)))
+    return np.exp2(e - 7)
+
+
+def down_column(m, i):
+    """Column i of a row-layout Q4 matrix (packed, scales, biases), float64."""
+    packed, scales, biases = m
+    q = (packed[:, i // 8].astype(np.uint64) >> np.uint64(4 * (i % 8))) & np.uint64(15)
+    sc = (scales[:, i // 64].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    bi = (biases[:, i // 64].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return sc * q.astype(np.float64) + bi
+
+
+def swiglu_tie_envelope(w, x2h, lgh, idx_ref, w_ref, E, I):
+    """Per output, the most that a different rounding direction of the SwiGLU
+    row's near-tie elements can move the expert output.  h = bf16(silu(g) u)
+    is rounded independently on each side from fp32 (GPU) and float64
+    (oracle) g and u; where the exact value lies within 1e-5 of its size of
+    a rounding midpoint, both directions are correct.  Each such element i of
+    the pair (row r, rank j, expert e) moves output n by at most
+    |weight| |W_d[e][n, i]| ulp(h_i)."""
+    k, H = x2h.shape[0], w.H
+    env = np.zeros((k, H))
+    for r in range(k):
+        pairs = [(w.expert(int(idx_ref[r, j])), w_ref[r, j]) for j in range(idx_ref.shape[1])]
+        pairs.append(((w.shared_gate_up, w.shared_down), 1.0 / (1.0 + np.exp(-float(lgh[r, E])))))
+        for (gu, dn), wt in pairs:
+            out = O.q4_qmv(*gu, x2h[r:r + 1])[0]
+            g, u = out[:I], out[I:]
+            h = g / (1.0 + np.exp(-g)) * u
+            ulp = _bf_ulp(h)
+            frac = h / ulp - np.floor(h / ulp)
+            for i in np.nonzero(np.abs(frac - 0.5) * ulp <= 1e-5 * np.abs(h))[0]:
+                env[r] += abs(wt) * np.abs(down_column(dn, int(i))) * ulp[i]
+    return env
+
+
 def stage_pair(run, shape):
     """Runs one stage with fp32 output and with bf16 output; the bf16 result
     must be the fp32 result rounded to nearest even."""
@@ -162,7 +201,13 @@ def check_layer_stages(vf, ds, l, h_dev, k):
     idx_c, _, y_ref, _ = O.gather_experts(gu, dn, np.ascontiguousarray(lgh[:, U]), T, x2h,
                                           shared=(w.shared_gate_up, w.shared_down), shared_logit=lgh[:, E])
     assert np.array_equal(U[idx_c], idx_ref)
-    assert_close(host(y32), y_ref, what=f"experts, {where}")
+    yg = host(y32).astype(np.float64)
+    tol = 1e-3 * np.sqrt(np.mean(y_ref * y_ref))
+    if np.max(np.abs(yg - y_ref)) > tol:
+        # within 1e-3 rms once the SwiGLU row's near-tie roundings are allowed either way
+        env = swiglu_tie_envelope(w, x2h, lgh, idx_ref, w_ref, E, I)
+        worst = np.max(np.abs(yg - y_ref) - env)
+        assert worst <= tol, f"experts, {where}: |gpu-oracle| exceeds 1e-3 rms plus the tie envelope by {worst:.3e}"
     h_out = host(h_dev).copy()
     assert np.array_equal(h_out, (h_mid + host(y32)).astype(np.float32)), f"MoE residual add, {where}"
 
