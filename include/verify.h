@@ -519,8 +519,9 @@ typedef struct {
   const uint16_t* v;    int64_t ld_v;
 } verify_attn_inputs;
 
-/* A split for a cache of `capacity` positions: about 128 key splits per KV
- * head at full length, a multiple of 32 and at least 128. */
+/* A split for a cache of `capacity` positions: about 74 key splits per KV
+ * head at full length (with two KV heads, one wave of one CTA per SM), a
+ * multiple of 64 and at least 128. */
 int32_t attn_default_split(int64_t capacity);
 
 /* Workspace bytes attn_verify_k needs for a cache of `capacity` positions cut

@@ -8,32 +8,28 @@
 //  1. append: the block's keys (rotated at P + r) and values go into the
 //     cache at P + r as binary16; the queries are rotated and scaled by
 //     1/sqrt(D) and kept as binary16 pairs hi + lo.
-//  2. partials: CTA (M group, split s, KV head) takes 2 tiles of 16
-//     (row, query head) pairs of that KV head's group and the key positions
-//     [s*split, (s+1)*split) of the window, 32 at a time through a
-//     double-buffered cp.async ring.  Warp (tile, D half) computes S = Q K^T on
-//     the tensor cores (mma.sync m16n8k16, binary16 operands, fp32 sums; the
+//  2. partials: CTA (M tile, split s, KV head) takes 128 (row, query head)
+//     pairs of that KV head's group and the key positions [s*split,
+//     (s+1)*split) of the window, 64 at a time.  S = Q K^T and O += P V run on
+//     the tcgen05 tensor cores with fp32 accumulators in tensor memory (the
 //     query and the probabilities each as a binary16 pair hi + lo, two MMAs
-//     against the same key or value fragment, so that only the cache's own
-//     binary16 rounding remains).  Each warp of a tile sums S over its half of
-//     the head dim and the halves are added through shared memory; then both
-//     mask positions after each row's own (P + r), keep the running max and
-//     sum, and accumulate P V for their own half of the head dim.
+//     against the same key or value tile, so that only the cache's own
+//     binary16 rounding remains); each thread owns one pair's row of S and O,
+//     masks positions after the pair's own (P + r) and keeps the running max
+//     and sum.
 //  3. combine: per (row, query head) the splits that hold the row's window are
 //     merged in ascending order and gated.
 // Launches 2 and 3 are programmatic dependents of the one before.
 //
 // Exactness: a row's arithmetic depends only on its own query, its window and
-// the absolute cut of key positions (split and the 32-position sub-tiles), not
+// the absolute cut of key positions (split and the 64-position sub-tiles), not
 // on k or the other rows, so row r of a width-k call equals a width-1 call at
 // P + r bit for bit.  Positions past a row's window add exact zeros, and
 // splits past it are skipped.
 //
 // Bound: the cache read, 2 * Hkv * D * 2 bytes per position (2 KB at the
-// Flash-Next shape), with 4 * k * Hq * D flops per key position.  The hi + lo
-// pairs double the tensor work, and at k ~ 9 the mma.sync pipe, not HBM, is
-// the limit: a capture at 65,536 positions shows the tensor pipe 37% busy,
-// stalled on MMA dependencies, with DRAM 12% busy.
+// Flash-Next shape), with 4 * k * Hq * D flops per key position (twice that
+// on the tensor cores with the hi + lo pairs, and M padded to 128 pairs).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -44,41 +40,10 @@
 namespace vk {
 namespace {
 
-constexpr int kBN = 32;        // key positions per sub-tile
-constexpr int kNS = kBN / 8;   // 8-position n-tiles of S per sub-tile
-constexpr int kMT = 2;         // tiles of 16 (row, head) pairs per CTA
-constexpr int kThreads = 128;  // 4 warps: (tile, D half)
-
-template <int D>
-struct AttnSmem {
-  static constexpr int LD = D + 8;  // halves per row: 16 B of padding keeps ldmatrix conflict-free
-  static constexpr int Q_BYTES = kMT * 16 * LD * 2;         // one of the query's hi / lo parts
-  static constexpr int KV_BYTES = kBN * LD * 2;
-  static constexpr int BYTES = 2 * Q_BYTES + 2 * 2 * KV_BYTES;  // q hi, q lo, 2 stages of (K, V)
-};
-
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ uint32_t pack_half2(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // ---------------------------------------------------------------- append
@@ -132,217 +97,261 @@ __global__ void attn_append_kernel(const AttnArgs a) {
 }
 
 // ---------------------------------------------------------------- partials
-template <int D>
-__global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnArgs a) {
-  using SM = AttnSmem<D>;
-  constexpr int LD = SM::LD;
-  constexpr int NTO = D / 16;  // 8-wide output tiles per D half
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);                  // q hi
-  uint16_t* Qlo = reinterpret_cast<uint16_t*>(smem + SM::Q_BYTES);   // q - q hi
-  uint16_t* KVs = reinterpret_cast<uint16_t*>(smem + 2 * SM::Q_BYTES);
+// CTA (M tile, split s, KV head): the 128 (row, query head) pairs m0 .. m0+127
+// of that KV head's group against the key positions [s*split, (s+1)*split),
+// 64 at a time.  Thread t holds pair m0 + t: TMEM lane t.
+//   S = Q K^T   tcgen05, M 128 x N 64, K = D in steps of 16: the query's
+//               binary16 hi part, then its lo part, into one fp32 TMEM tile;
+//   softmax     each thread reads its row of S from TMEM, masks positions
+//               after its own (P + r), keeps the running max and sum, and
+//               writes p as binary16 hi and lo parts to shared memory;
+//   O += P V    tcgen05, M 128 x N D, K = 64 in steps of 16 (V MN-major),
+//               O an fp32 TMEM tile, rescaled by exp(m_old - m_new) in place
+//               (tcgen05.ld / st) when a row's max rises.
+// Operands are in the canonical no-swizzle layouts (core matrices of 8 rows x
+// 16 B): Q, K and P K-major, V MN-major, filled with 16-byte cp.async or
+// stores.  Each load of the next key or value tile is issued as soon as the
+// MMA that read the previous one has completed.  One CTA per SM (about
+// 224 KB of shared memory at D = 256).
+constexpr int kTcM = 128;        // pairs per CTA (TMEM lanes)
+constexpr int kTcN = 64;         // key positions per sub-tile
+constexpr int kTcThreads = 128;  // thread t <-> TMEM lane t
 
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int g = lane >> 2, c = lane & 3;
+template <int D>
+struct TcSmem {
+  static constexpr int Q_BYTES = kTcM * D * 2;    // one of the query's hi / lo parts
+  static constexpr int KV_BYTES = kTcN * D * 2;
+  static constexpr int P_BYTES = kTcM * kTcN * 2;  // one of p's hi / lo parts
+  static constexpr int QH = 0, QL = Q_BYTES, K = 2 * Q_BYTES, V = K + KV_BYTES, PH = V + KV_BYTES,
+                       PL = PH + P_BYTES;
+  static constexpr int BYTES = PL + P_BYTES;
+  static constexpr uint32_t TMEM_COLS = D > 128 ? 512 : 256;  // S at column 0, O at O_COL
+  static constexpr uint32_t O_COL = D > 128 ? 256 : 128;
+};
+
+// Byte offset of element (row, kidx) of a K-major operand with R rows:
+// per k-step of 16, [row / 8][k half][row % 8][8 elements].
+template <int R>
+__device__ __forceinline__ uint32_t kmajor_off(int row, int kidx) {
+  return (uint32_t)((kidx >> 4) * (R * 32) + (row >> 3) * 256 + ((kidx >> 3) & 1) * 128 + (row & 7) * 16 +
+                    (kidx & 7) * 2);
+}
+// Byte offset of value (key, d) in the MN-major value tile: [key / 8][d / 8][key % 8][8 d].
+template <int D>
+__device__ __forceinline__ uint32_t vmajor_off(int key, int d) {
+  return (uint32_t)(((key >> 3) * (D / 8) + (d >> 3)) * 128 + (key & 7) * 16 + (d & 7) * 2);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_partial_kernel(const AttnArgs a) {
+  using L = TcSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ __align__(8) uint64_t bars[2];  // S tile done, O tile done
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  volatile int* abort = &abort_flag;
+  const uint32_t sb = smem_addr(smem);
+  const uint32_t bar_s = smem_addr(&bars[0]), bar_o = smem_addr(&bars[1]);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int s = blockIdx.y, hk = blockIdx.z;
   const int G = a.Hq / a.Hkv, M = a.k * G, Mpad = 16 * a.n_mtiles;
-  const int m0 = blockIdx.x * (kMT * 16);
+  const int m0 = blockIdx.x * kTcM;
   const int end = a.P + a.k;  // positions held by the cache after the append
   const int pos0 = s * a.split;
   const int pos_end = min(pos0 + a.split, end);
-  const int nsub = (pos_end - pos0 + kBN - 1) / kBN;
+  const int nsub = (pos_end - pos0 + kTcN - 1) / kTcN;
 
-  auto load_sub = [&](int sub, int stage) {
-    const int p0 = pos0 + sub * kBN;
-    constexpr int CH = kBN * (D / 8);  // 16-byte chunks per K or V sub-tile
-    for (int q = tid; q < 2 * CH; q += kThreads) {
-      const int which = q / CH, cc = q % CH;
-      const int row = cc / (D / 8), col = (cc % (D / 8)) * 8;
-      const int pos = p0 + row;
+  // keys and values of sub-tile `sub` (zero fill past the cache's end)
+  auto load_kv = [&](int sub, bool values) {
+    constexpr int CH = kTcN * (D / 8);
+    for (int q = tid; q < CH; q += kTcThreads) {
+      const int row = q / (D / 8), d0 = (q % (D / 8)) * 8;
+      const int pos = pos0 + sub * kTcN + row;
       const bool ok = pos < end;
-      const uint16_t* src = (which ? a.V : a.K) + ((long long)hk * a.cap + (ok ? pos : 0)) * D + col;
-      uint16_t* dst = KVs + ((stage * 2 + which) * kBN + row) * LD + col;
-      cp_async16(smem_addr(dst), src, ok ? 16u : 0u);  // zero fill past the cache's end
+      const uint16_t* src = (values ? a.V : a.K) + ((long long)hk * a.cap + (ok ? pos : 0)) * D + d0;
+      const uint32_t dst = values ? sb + L::V + vmajor_off<D>(row, d0) : sb + L::K + kmajor_off<kTcN>(row, d0);
+      cp_async16(dst, src, ok ? 16u : 0u);
     }
     cp_async_commit();
   };
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_addr(&tmem_slot), L::TMEM_COLS);
   // Launched as a programmatic dependent of the append kernel: a first
   // sub-tile of positions committed before this call (written at least two
   // launches back) is fetched before the dependency wait; the queries and the
   // block's own keys and values after it.
-  const bool early = pos0 + kBN <= a.P;
-  if (early) load_sub(0, 0);
+  const bool early = pos0 + kTcN <= a.P;
+  if (early) {
+    load_kv(0, false);
+    load_kv(0, true);
+  }
   griddep_wait();
   griddep_launch();
-  // queries of this CTA's 32 (row, head) pairs, rotated at P + r and scaled by
-  // 1/sqrt(D) by the append kernel: two binary16 parts hi + lo (about 22
-  // significant bits; zeros past M).
+  // the queries of this CTA's 128 pairs, rotated at P + r and scaled by
+  // 1/sqrt(D) by the append kernel: binary16 hi and lo parts (zeros past M)
   {
-    constexpr int QCH = kMT * 16 * (D / 8);
-    for (int q = tid; q < 2 * QCH; q += kThreads) {
+    constexpr int QCH = kTcM * (D / 8);
+    for (int q = tid; q < 2 * QCH; q += kTcThreads) {
       const int part = q / QCH, cc = q % QCH;
-      const int mm = cc / (D / 8), col = (cc % (D / 8)) * 8, m = m0 + mm;
+      const int mm = cc / (D / 8), d0 = (cc % (D / 8)) * 8, m = m0 + mm;
       const bool ok = m < M;
       const long long row = ok ? (long long)(m / G) * a.Hq + hk * G + m % G : 0;
-      cp_async16(smem_addr((part ? Qlo : Qs) + mm * LD + col), (part ? a.ql : a.qh) + row * D + col, ok ? 16u : 0u);
+      cp_async16(sb + (part ? L::QL : L::QH) + kmajor_off<kTcM>(mm, d0), (part ? a.ql : a.qh) + row * D + d0,
+                 ok ? 16u : 0u);
     }
+    cp_async_commit();
   }
-  if (early) cp_async_commit();  // the queries as a group of their own
-  else load_sub(0, 0);           // the queries travel with the first tile
-
-  const int mt = w >> 1, dh = w & 1;
-  const int mrow = m0 + mt * 16;         // first pair of this warp's tile
-  const bool live = mrow < M;            // uniform per warp
-  int lim[2];                            // last visible position of rows g, g + 8 (-1: none)
-#pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    const int m = mrow + g + 8 * ri;
-    lim[ri] = m < M ? a.P + m / G : -1;
+  if (!early) {
+    load_kv(0, false);
+    load_kv(0, true);
   }
-  float o_acc[NTO][4];
-#pragma unroll
-  for (int nt = 0; nt < NTO; ++nt) o_acc[nt][0] = o_acc[nt][1] = o_acc[nt][2] = o_acc[nt][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  // this warp's D half of the query fragments
-  const uint32_t q_base = smem_addr(Qs + (mt * 16 + (lane & 15)) * LD + dh * (D / 2) + (lane >> 4) * 8);
-  const uint32_t qlo_base = q_base + SM::Q_BYTES;
-  __shared__ float xs[4][kNS * 4][32];  // partial scores of each warp, in fragment order
+  cp_async_wait<0>();
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t t_s = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's lanes of S
+  const uint32_t t_o = t_s + L::O_COL;                        // and of O
+  const int m = m0 + tid;
+  // last position this pair sees in this split (-1: none): its own window, and
+  // no further than the split's end (a split need not be a multiple of 64)
+  const int lim = m < M ? min(a.P + m / G, pos_end - 1) : -1;
+  float m_run = -INFINITY, l_run = 0.f;
+  constexpr uint32_t IDESC_S = umma_idesc_f16(kTcM, kTcN, false);
+  constexpr uint32_t IDESC_O = umma_idesc_f16(kTcM, D, true);
 
   for (int sub = 0; sub < nsub; ++sub) {
-    if (sub + 1 < nsub) {
-      load_sub(sub + 1, (sub + 1) & 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    const uint32_t ph = (uint32_t)(sub & 1);
+    // S = Q_hi K^T + Q_lo K^T
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_f16(tmem, umma_desc(sb + (part ? L::QL : L::QH) + ks * kTcM * 32, 128, 256),
+                   umma_desc(sb + L::K + ks * kTcN * 32, 128, 256), IDESC_S, (part | ks) ? 1u : 0u);
+      umma_commit(bar_s);
     }
+    const bool ok_s = mbar_wait(bar_s, ph, abort, a.err);
+    tc_fence_after();
+    // the key tile is free: fetch the next one while this one's softmax and P V run
+    if (sub + 1 < nsub) load_kv(sub + 1, false);
+    // this pair's row of S; mask, running max and sum
+    float sv[kTcN];
+#pragma unroll
+    for (int c0 = 0; c0 < kTcN; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(t_s + (uint32_t)c0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sv[c0 + j] = __uint_as_float(v[j]);
+    }
+    const int pbase = pos0 + sub * kTcN;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kTcN; ++j) {
+      sv[j] = pbase + j <= lim ? sv[j] : -INFINITY;
+      mx = fmaxf(mx, sv[j]);
+    }
+    const float mn = fmaxf(m_run, mx);
+    const float alpha = mn == -INFINITY ? 1.f : expf(m_run - mn);
+    const float msub = mn == -INFINITY ? 0.f : mn;
+    m_run = mn;
+    float ps = 0.f;
+#pragma unroll
+    for (int j0 = 0; j0 < kTcN; j0 += 8) {
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = expf(sv[j0 + 2 * e] - msub), p1 = expf(sv[j0 + 2 * e + 1] - msub);
+        const __half2 h2 = __floats2half2_rn(p0, p1);
+        hi[e] = pack_half2(h2);
+        lo[e] = pack_half2(__floats2half2_rn(p0 - __low2float(h2), p1 - __high2float(h2)));
+        ps += p0;
+        ps += p1;
+      }
+      const uint32_t off = kmajor_off<kTcM>(tid, j0);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sb + L::PH + off), "r"(hi[0]), "r"(hi[1]),
+                   "r"(hi[2]), "r"(hi[3])
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sb + L::PL + off), "r"(lo[0]), "r"(lo[1]),
+                   "r"(lo[2]), "r"(lo[3])
+                   : "memory");
+    }
+    l_run = fmaf(l_run, alpha, ps);
+    // O *= alpha for this pair (the whole warp when any of its rows changed)
+    if (sub > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(t_o + (uint32_t)c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+        tmem_st32(t_o + (uint32_t)c0, v);
+      }
+      tmem_st_wait();
+    }
+    // this sub-tile's values landed (the next key tile may still be in flight)
+    if (sub + 1 < nsub) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
-    if (live) {
-      const uint16_t* Ks = KVs + ((sub & 1) * 2) * kBN * LD;
-      const uint16_t* Vs = Ks + kBN * LD;
-      // S = Q K^T: 16 pairs x kBN positions.  Each warp of the tile sums over
-      // its D half (hi and lo query parts in separate accumulators), then the
-      // two halves are added through shared memory, half 0 first.
-      float sh[kNS][4], sl[kNS][4];
+    // O += P_hi V + P_lo V
+    if (tid == 0 && ok_s) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part)
 #pragma unroll
-      for (int nt = 0; nt < kNS; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
-      // lanes 0-7 / 8-15: rows of n-tile 2j at columns +0 / +8; lanes 16-31: n-tile 2j+1
-      const uint32_t k_base =
-          smem_addr(Ks + ((lane >> 4) * 8 + (lane & 7)) * LD + dh * (D / 2) + ((lane >> 3) & 1) * 8);
-#pragma unroll
-      for (int kk = 0; kk < D / 32; ++kk) {
-        uint32_t a0, a1, a2, a3, l0, l1, l2, l3, b[2 * kNS];
-        ldsm_x4(q_base + kk * 32, a0, a1, a2, a3);
-        ldsm_x4(qlo_base + kk * 32, l0, l1, l2, l3);
-#pragma unroll
-        for (int j = 0; j < kNS / 2; ++j)
-          ldsm_x4(k_base + j * 16 * LD * 2 + kk * 32, b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
-#pragma unroll
-        for (int nt = 0; nt < kNS; ++nt) mma_f16(sh[nt], a0, a1, a2, a3, b[2 * nt], b[2 * nt + 1]);
-#pragma unroll
-        for (int nt = 0; nt < kNS; ++nt) mma_f16(sl[nt], l0, l1, l2, l3, b[2 * nt], b[2 * nt + 1]);
-      }
-      float sacc[kNS][4];
-#pragma unroll
-      for (int nt = 0; nt < kNS; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float part = sh[nt][e] + sl[nt][e];
-          xs[w][nt * 4 + e][lane] = part;
-          sacc[nt][e] = part;
-        }
-      if (mt == 0) named_bar(1, 64);  // the tile's two warps (constant ids)
-      else named_bar(2, 64);
-#pragma unroll
-      for (int nt = 0; nt < kNS; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float other = xs[w ^ 1][nt * 4 + e][lane];
-          sacc[nt][e] = dh == 0 ? sacc[nt][e] + other : other + sacc[nt][e];
-        }
-      // mask, running max and sum; p rounded to binary16 feeds P V and the sum
-      const int pbase = pos0 + sub * kBN;
-      float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int nt = 0; nt < kNS; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int ri = e >> 1, pos = pbase + nt * 8 + 2 * c + (e & 1);
-          const float v = pos <= lim[ri] ? sacc[nt][e] : -INFINITY;
-          sacc[nt][e] = v;
-          mx[ri] = fmaxf(mx[ri], v);
-        }
-      float alpha[2], msub[2];
-#pragma unroll
-      for (int ri = 0; ri < 2; ++ri) {
-        mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 1));
-        mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 2));
-        const float mn = fmaxf(m_run[ri], mx[ri]);
-        alpha[ri] = mn == -INFINITY ? 1.f : expf(m_run[ri] - mn);
-        msub[ri] = mn == -INFINITY ? 0.f : mn;
-        m_run[ri] = mn;
-      }
-      uint32_t pa[kNS][2], pl[kNS][2];  // p as binary16 pairs hi, lo: [n-tile][row g / g + 8]
-      float ps[2] = {0.f, 0.f};
-#pragma unroll
-      for (int nt = 0; nt < kNS; ++nt)
-#pragma unroll
-        for (int ri = 0; ri < 2; ++ri) {
-          const float p0 = expf(sacc[nt][2 * ri] - msub[ri]), p1 = expf(sacc[nt][2 * ri + 1] - msub[ri]);
-          const __half2 h2 = __floats2half2_rn(p0, p1);
-          pa[nt][ri] = pack_half2(h2);
-          pl[nt][ri] = pack_half2(__floats2half2_rn(p0 - __low2float(h2), p1 - __high2float(h2)));
-          ps[ri] += p0;
-          ps[ri] += p1;
-        }
-#pragma unroll
-      for (int ri = 0; ri < 2; ++ri) {
-        ps[ri] += __shfl_xor_sync(0xffffffffu, ps[ri], 1);
-        ps[ri] += __shfl_xor_sync(0xffffffffu, ps[ri], 2);
-        l_run[ri] = fmaf(l_run[ri], alpha[ri], ps[ri]);
-      }
-#pragma unroll
-      for (int nt = 0; nt < NTO; ++nt) {
-        o_acc[nt][0] *= alpha[0];
-        o_acc[nt][1] *= alpha[0];
-        o_acc[nt][2] *= alpha[1];
-        o_acc[nt][3] *= alpha[1];
-      }
-      // O += P V over this warp's half of the head dim; lanes 0-15 address the
-      // 16 positions of a k-step, lanes 16-31 the same for the next n-tile
-      const uint32_t v_base = smem_addr(Vs + (lane & 15) * LD + dh * (D / 2) + (lane >> 4) * 8);
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        const uint32_t a0 = pa[2 * kk][0], a1 = pa[2 * kk][1], a2 = pa[2 * kk + 1][0], a3 = pa[2 * kk + 1][1];
-        const uint32_t l0 = pl[2 * kk][0], l1 = pl[2 * kk][1], l2 = pl[2 * kk + 1][0], l3 = pl[2 * kk + 1][1];
-#pragma unroll
-        for (int nt = 0; nt < NTO; nt += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(v_base + (kk * 16 * LD + nt * 8) * 2, b0, b1, b2, b3);
-          mma_f16(o_acc[nt], a0, a1, a2, a3, b0, b1);
-          mma_f16(o_acc[nt], l0, l1, l2, l3, b0, b1);
-          mma_f16(o_acc[nt + 1], a0, a1, a2, a3, b2, b3);
-          mma_f16(o_acc[nt + 1], l0, l1, l2, l3, b2, b3);
-        }
-      }
+        for (int ks = 0; ks < kTcN / 16; ++ks)
+          umma_f16(tmem + L::O_COL, umma_desc(sb + (part ? L::PL : L::PH) + ks * kTcM * 32, 128, 256),
+                   umma_desc(sb + L::V + 2 * ks * (D / 8) * 128, (D / 8) * 128, 128), IDESC_O,
+                   (sub | part | ks) ? 1u : 0u);
+      umma_commit(bar_o);
+    } else if (tid == 0) {
+      umma_commit(bar_o);  // nothing issued: the barrier still completes
     }
-    __syncthreads();  // the next load reuses this stage
+    mbar_wait(bar_o, ph, abort, a.err);
+    tc_fence_after();
+    // the value tile is free: fetch the next one
+    if (sub + 1 < nsub) {
+      load_kv(sub + 1, true);
+      cp_async_wait<1>();  // the next key tile (the older group) has landed
+      fence_async_smem();
+      __syncthreads();
+    }
   }
 
-  // partial results of this split
-  if (!live) return;
+  // partial results of this split: the unnormalised O row, then (max, sum)
   const long long base = (long long)(hk * a.nsplit + s) * Mpad;
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(t_o + (uint32_t)c0, v);
+    tmem_ld_wait();
+    if (m < M && nsub > 0) {
+      float4* dst = reinterpret_cast<float4*>(a.part_o + (base + m) * D + c0);
 #pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    const int m = mrow + g + 8 * ri;
-    if (m >= M) continue;
-    if (dh == 0 && c == 0) a.part_ml[base + m] = make_float2(m_run[ri], l_run[ri]);
-    float* dst = a.part_o + (base + m) * D + dh * (D / 2) + 2 * c;
-#pragma unroll
-    for (int nt = 0; nt < NTO; ++nt)
-      *reinterpret_cast<float2*>(dst + nt * 8) = make_float2(o_acc[nt][2 * ri], o_acc[nt][2 * ri + 1]);
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                             __uint_as_float(v[4 * j + 3]));
+    }
   }
+  if (m < M) a.part_ml[base + m] = make_float2(m_run, l_run);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- combine
@@ -433,9 +442,9 @@ cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s, int* launches) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.n_mtiles + kMT - 1) / kMT, a.nsplit, a.Hkv);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = AttnSmem<D>::BYTES;
+  cfg.gridDim = dim3((a.k * (a.Hq / a.Hkv) + kTcM - 1) / kTcM, a.nsplit, a.Hkv);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = TcSmem<D>::BYTES + 128;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -453,10 +462,10 @@ cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s, int* launches) {
 
 cudaError_t attn_setup_kernels() {
   cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       AttnSmem<128>::BYTES);
+                                       TcSmem<128>::BYTES + 128);
   if (e) return e;
   return cudaFuncSetAttribute(attn_partial_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              AttnSmem<256>::BYTES);
+                              TcSmem<256>::BYTES + 128);
 }
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s, int* launches) {

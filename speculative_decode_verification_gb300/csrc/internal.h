@@ -170,6 +170,7 @@ struct AttnArgs {
   float2* part_ml;      // [Hkv][nsplit][16 n_mtiles] (running max, sum)
   void* o;              // [k, Hq * D]
   int dtype;
+  int* err;             // device error word (a pipeline wait that ran out)
 };
 constexpr int kAttnMaxM = 512;   // k * (Hq / Hkv) per call
 cudaError_t attn_setup_kernels();

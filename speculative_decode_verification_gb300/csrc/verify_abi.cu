@@ -687,9 +687,12 @@ static bool attn_params_ok(const verify_attn_params* p) {
 // About 128 key splits per KV head at full length, and at least 128
 // positions per split (a sweep at 4,096 and 65,536 positions, k = 1 and 9).
 int32_t attn_default_split(int64_t capacity) {
+  // about 74 splits per KV head: with two KV heads, one wave of one
+  // partial-kernel CTA per SM on a 148- to 152-SM GPU; a multiple of the
+  // kernel's 64-position sub-tile, at least 128
   if (capacity < 1) return 128;
-  const int64_t per = (capacity + 127) / 128;
-  const int64_t s = (per + 31) / 32 * 32;
+  const int64_t per = (capacity + 73) / 74;
+  const int64_t s = (per + 63) / 64 * 64;
   return (int32_t)(s < 128 ? 128 : (s > (1 << 20) ? (1 << 20) : s));
 }
 
@@ -734,6 +737,7 @@ verify_status attn_verify_k(verify_ctx* ctx, const verify_attn_params* p, verify
   a.Hq = p->n_q_heads; a.Hkv = p->n_kv_heads; a.D = D; a.rope_dim = p->rope_dim;
   for (int j = 0; j < p->rope_dim / 2; ++j) a.inv_freq[j] = pow((double)p->rope_theta, -2.0 * j / p->rope_dim);
   a.P = cache->len; a.k = k; a.split = cache->split; a.nsplit = (int)nsplit;
+  a.err = ctx->err;
   a.n_mtiles = (k * G + 15) / 16;
   char* base = static_cast<char*>(cache->work);
   a.qh = reinterpret_cast<uint16_t*>(base + w.qh);

@@ -80,6 +80,6 @@ def test_attention_cache_bookkeeping_on_host(lib):
     assert B.attn_workspace_bytes(p, 1024, 256, 1) == want
     assert B.attn_workspace_bytes(p, 1024, 250, 1) == 0  # split not a multiple of 32
     assert B.attn_workspace_bytes(B.attn_params(24, 5, 256), 1024, 256, 1) == 0
-    # default split: about capacity / 128, a multiple of 32, at least 128
+    # default split: about 74 splits per KV head, a multiple of 64, at least 128
     assert B.attn_default_split(100) == 128 and B.attn_default_split(4128) == 128
-    assert B.attn_default_split(65568) == 544 and B.attn_default_split(65568) % 32 == 0
+    assert B.attn_default_split(65568) == 896 and -(-65568 // 896) == 74
