@@ -72,17 +72,42 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait that ignores the abort flag: used before a CTA exits, for
+// copies or MMAs it has issued, so that none is in flight when its shared or
+// tensor memory is released.  Records a timeout in the error word.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* err) {
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitTimeoutCycles) {
+      record_error(err, VERIFY_DEV_ETIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }
-// 2-D tiled load of the box at (x = innermost coordinate, y) into shared memory.
+// 2-D tiled load of the box at (x = innermost coordinate, y) into shared
+// memory, completing on an mbarrier (expected bytes).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(m), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// 3-D tiled load of the box at (x = innermost coordinate, y, z) into shared
+// memory, completing on an mbarrier (expected bytes).  Box elements outside
+// the tensor's extent arrive as zeros.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(m), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 
@@ -93,6 +118,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+
+// Bulk copy of `bytes` contiguous bytes (16-byte aligned, multiple of 16)
+// from shared to global memory, tracked by this thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every bulk group this thread committed has read its source
+// (the shared memory may then be reused; the writes complete with the grid).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // An L2 eviction policy for data read once per call (the weight stream): its
 // lines are the first to go, so that it does not push the small data reused
@@ -245,18 +281,29 @@ __device__ __forceinline__ bool wait_count(const int* p, int target, volatile in
 // ------------------------------------------------- tcgen05 (TMEM, UMMA)
 //
 // Fifth-generation tensor core: one thread issues an MMA whose operands are
-// read from shared memory through 64-bit matrix descriptors and whose fp32
-// accumulator lives in tensor memory (TMEM: 128 lanes x 512 32-bit columns
-// per SM).  Operands here use the canonical no-swizzle layouts: "core
-// matrices" of 8 rows x 16 bytes stored contiguously (128 B), with the byte
-// stride between core matrices along K (LBO) and along M/N (SBO) in the
-// descriptor, for K-major and MN-major operands alike.
+// read from shared memory through 64-bit matrix descriptors (or, for A, from
+// tensor memory) and whose fp32 accumulator lives in tensor memory (TMEM: 128
+// lanes x 512 32-bit columns per SM).  Two shared-memory layouts are used:
+//  - no swizzle: "core matrices" of 8 rows x 16 bytes stored contiguously
+//    (128 B), with the byte stride between core matrices along K (LBO) and
+//    along M/N (SBO) in the descriptor, for K-major and MN-major operands;
+//  - 128-byte swizzle: rows of 128 bytes in atoms of 8 rows (1 KB, 1 KB
+//    aligned), the 16-byte chunk c of row r stored at chunk c ^ (r % 8) (the
+//    layout a TMA tile load with 128-byte swizzle writes).  K-major: SBO is the
+//    stride between 8-row groups, and a K step inside the 128-byte row moves
+//    the start address by its byte offset; MN-major: LBO is the stride between
+//    atoms along M/N (64 binary16 each), SBO the stride between 8-row groups
+//    along K.
 
 // Shared-memory matrix descriptor: start address, LBO, SBO (bytes, multiples
 // of 16), descriptor version 1, no swizzle.
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+// The same with the 128-byte swizzle (layout type 2 in bits 61-63).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return umma_desc(saddr, lbo, sbo) | ((uint64_t)2 << 61);
 }
 // Instruction descriptor of kind::f16 with binary16 A and B, fp32 D, shape
 // M x N; b_mn_major: B stored MN-major (else K-major); A is K-major.
@@ -270,6 +317,17 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
       "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D (TMEM) = A B^T (+ D), A read from tensor memory: row i in lane i, two
+// binary16 per 32-bit column (the lower K index in the low half), K = 16 per
+// MMA in 8 columns from a_tmem.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // The mbarrier receives one arrival once every MMA this thread issued before has completed.

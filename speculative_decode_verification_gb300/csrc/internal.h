@@ -152,6 +152,13 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, float eps, int zc, in
 // block's rotated keys and values into the cache, the rotation table), split
 // partials (one CTA per (M group, key split, KV head)), combine.
 struct AttnArgs {
+  // tensor maps of the K and V caches for the split kernel's tile loads (set
+  // by the launcher): {D, P + k, Hkv} binary16, boxes of 64 x 64 x 1,
+  // 128-byte swizzle, zeros past P + k
+  CUtensorMap tm_k, tm_v;
+  // tensor maps of the queries' lo and hi parts for the same kernel:
+  // {D, Hkv * q_rows} binary16, boxes of 64 x 128, 128-byte swizzle
+  CUtensorMap tm_ql, tm_qh;
   const uint16_t* q;    long long ld_q;
   const uint16_t* gate; long long ld_gate;
   const uint16_t* kin;  long long ld_k;
@@ -161,13 +168,16 @@ struct AttnArgs {
   long long cap;
   int Hq, Hkv, D, rope_dim;
   double inv_freq[128];  // theta^(-2j / rope_dim), j < rope_dim / 2, computed on the host in float64
+  double qscale;         // log2(e) / sqrt(D): scores in log2 units
   int P, k, split;
   int nsplit;           // ceil((P + k) / split)
   int n_mtiles;         // ceil(k * Hq / Hkv / 16): 16 (row, head) pairs per tile
-  uint16_t* qh;         // [k][Hq][D] binary16: rotated, scaled queries (hi part)
-  uint16_t* ql;         // the remainders (lo part)
+  int q_rows;           // query rows per KV head: k * Hq / Hkv rounded up to 128
+  uint16_t* qh;         // [Hkv][q_rows][D] binary16: rotated, scaled queries (hi part), row r * G + g
+                        // of KV head h for query head h * G + g of block row r (rows past k * G unused)
+  uint16_t* ql;         // the remainders (lo part), same layout
   float* part_o;        // [Hkv][nsplit][16 n_mtiles][D] unnormalised outputs
-  float2* part_ml;      // [Hkv][nsplit][16 n_mtiles] (running max, sum)
+  float2* part_ml;      // [Hkv][nsplit][16 n_mtiles] (running max in log2 units, sum)
   void* o;              // [k, Hq * D]
   int dtype;
   int* err;             // device error word (a pipeline wait that ran out)

@@ -660,8 +660,9 @@ verify_status verify_lm_head_accept(verify_ctx* ctx, const verify_q4_weight* W, 
 // ------------------------------------------------------------ attention
 
 // Workspace of one attention call: the rotated queries (hi and lo binary16
-// parts), then (max, sum) and the unnormalised outputs of every (KV head,
-// split, pair), each 256-byte aligned.
+// parts, per KV head its pairs in rows padded to a multiple of 128), then
+// (max, sum) and the unnormalised outputs of every (KV head, split, pair),
+// each 256-byte aligned.
 struct AttnWork {
   long long qh, ql, ml, po, total;
 };
@@ -669,10 +670,11 @@ static AttnWork attn_work(const verify_attn_params* p, long long nsplit, int k) 
   auto up = [](long long b) { return (b + 255) / 256 * 256; };
   const long long G = p->n_q_heads / p->n_kv_heads;
   const long long Mpad = (k * G + 15) / 16 * 16;
+  const long long qbytes = p->n_kv_heads * ((k * G + 127) / 128 * 128) * p->head_dim * 2;
   AttnWork w;
   w.qh = 0;
-  w.ql = up((long long)k * p->n_q_heads * p->head_dim * 2);
-  w.ml = w.ql + up((long long)k * p->n_q_heads * p->head_dim * 2);
+  w.ql = up(qbytes);
+  w.ml = w.ql + up(qbytes);
   w.po = w.ml + up(p->n_kv_heads * nsplit * Mpad * 8);
   w.total = w.po + up(p->n_kv_heads * nsplit * Mpad * (long long)p->head_dim * 4);
   return w;
@@ -736,9 +738,11 @@ verify_status attn_verify_k(verify_ctx* ctx, const verify_attn_params* p, verify
   a.K = cache->K; a.V = cache->V; a.cap = cache->capacity;
   a.Hq = p->n_q_heads; a.Hkv = p->n_kv_heads; a.D = D; a.rope_dim = p->rope_dim;
   for (int j = 0; j < p->rope_dim / 2; ++j) a.inv_freq[j] = pow((double)p->rope_theta, -2.0 * j / p->rope_dim);
+  a.qscale = 1.4426950408889634 / sqrt((double)D);
   a.P = cache->len; a.k = k; a.split = cache->split; a.nsplit = (int)nsplit;
   a.err = ctx->err;
   a.n_mtiles = (k * G + 15) / 16;
+  a.q_rows = (k * G + 127) / 128 * 128;
   char* base = static_cast<char*>(cache->work);
   a.qh = reinterpret_cast<uint16_t*>(base + w.qh);
   a.ql = reinterpret_cast<uint16_t*>(base + w.ql);

@@ -75,8 +75,9 @@ def test_attention_cache_bookkeeping_on_host(lib):
     assert lib.attn_commit(C.byref(c), 3) == B.OK
     assert c.len == 13 and c.pending_k == 0
     p = B.attn_params(24, 2, 256)
-    # rotated queries (hi, lo), then (max, sum) and outputs of 2 heads x 4 splits x 16 pairs
-    want = 2 * 24 * 256 * 2 + 2 * 4 * 16 * 8 + 2 * 4 * 16 * 256 * 4
+    # rotated queries (hi, lo: per KV head 12 pairs in 128 rows), then (max,
+    # sum) and outputs of 2 heads x 4 splits x 16 pairs
+    want = 2 * (2 * 128 * 256 * 2) + 2 * 4 * 16 * 8 + 2 * 4 * 16 * 256 * 4
     assert B.attn_workspace_bytes(p, 1024, 256, 1) == want
     assert B.attn_workspace_bytes(p, 1024, 250, 1) == 0  # split not a multiple of 32
     assert B.attn_workspace_bytes(B.attn_params(24, 5, 256), 1024, 256, 1) == 0
