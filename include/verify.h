@@ -493,8 +493,10 @@ typedef struct {
  * split (a multiple of 32, >= 32) fixes how the key positions are cut for
  * the split-KV kernel: [s*split, (s+1)*split).  Results are bit-identical
  * across widths (row r of a width-k call == a width-1 call at len + r) for
- * one split value.  work: caller device memory of attn_workspace_bytes(...)
- * bytes (partial results and the rotation table).  After attn_verify_k(k)
+ * one split value.  K and V must be 16-byte aligned device memory (the
+ * split kernel reads them with TMA tile loads).  work: caller device memory
+ * of attn_workspace_bytes(...) bytes, 256-byte aligned (the rotated queries
+ * and the partial results).  After attn_verify_k(k)
  * the block's keys and values sit at len .. len+k-1 and pending_k == k;
  * attn_commit(a) makes a of them committed (len += a); the others are
  * overwritten by the next verify.
@@ -540,8 +542,8 @@ int64_t attn_workspace_bytes(const verify_attn_params* p, int64_t capacity, int3
  * rope(x, pos) rotates the pair (x_i, x_{i+rope_dim/2}) by the angle
  * pos * theta^(-2i/rope_dim) for i < rope_dim/2; other dims pass through.
  * o: [k, n_q_heads*head_dim], VERIFY_F32 or VERIFY_BF16 (row stride
- * n_q_heads*head_dim).  Three kernel launches (append, split partials,
- * combine).  Limits: 1 <= k <= 32, k * n_q_heads / n_kv_heads <= 512,
+ * n_q_heads*head_dim).  Three kernel launches (append; split partials on
+ * the tcgen05 tensor cores with TMEM accumulators; combine).  Limits: 1 <= k <= 32, k * n_q_heads / n_kv_heads <= 512,
  * len + k <= capacity.  Arithmetic: rotation angles in float64, the
  * rotation in fp32; q.K and p.V on the tensor cores with binary16 operands and
  * fp32 sums, the scaled query and the probabilities each carried as a pair of
