@@ -105,6 +105,66 @@ def test_attn_matches_oracle(vf, case):
     assert cache.c.pending_k == k and cache.c.len == P
 
 
+# The split kernel's pipeline edges: the ten-slot ring of head dim 128
+# wrapping many times, splits that are not a multiple of its 64-position
+# sub-tile, a cache filled exactly to capacity (the tile loads' zero fill
+# starts at P + k) and one KV head holding 16 rows x 12 query heads (two
+# 128-pair tiles).
+PIPE_CASES = [
+    # Hq, Hkv, D, P, k, split, capacity - (P + k)
+    (8, 2, 128, 4000, 9, 2048, 0),
+    (8, 2, 128, 1000, 9, 96, 0),
+    (24, 2, 256, 3000, 4, 1024, 0),
+    (12, 1, 256, 777, 16, 160, 5),
+]
+
+
+@pytest.mark.parametrize("case", PIPE_CASES, ids=[f"H{c[0]}_{c[1]}_D{c[2]}_P{c[3]}_k{c[4]}_s{c[5]}_x{c[6]}" for c in PIPE_CASES])
+def test_pipeline_shapes(vf, case):
+    Hq, Hkv, D, P, k, split, extra = case
+    cache = Cache(27, f"pipe.{D}.{P}.{split}", Hq, Hkv, D, P + k + extra, P, split, max_k=max(16, k))
+    inp = S.attn_inputs(27, f"pipe.in.{D}.{P}.{k}", k, Hq, Hkv, D)
+    o = cache.verify(vf, inp, k)
+    oo, k_app, v_app = cache.oracle(inp, P)
+    assert_close(o, oo.reshape(k, -1), what="o")
+    _check_appended(cache, P, k, k_app, v_app)
+
+
+def test_growing_scores_raise_the_running_max(vf):
+    """Keys scaled up with their position (x (1 + pos/16)), so that nearly
+    every 64-position sub-tile raises each row's running maximum by far more
+    than 2^8: the rescale of the output tile and the sum, against the
+    oracle."""
+    Hq, Hkv, D, P, k = 24, 2, 256, 2000, 9
+    cache = Cache(28, "grow", Hq, Hkv, D, P + k, P, 512)
+    K1 = cache.K0.view(np.float16).astype(np.float32)
+    K1[:, :P] *= (1.0 + np.arange(P, dtype=np.float32) / 16.0)[None, :, None]
+    cache.K0 = K1.astype(np.float16).view(np.uint16)
+    cache.K.copy_(dev(cache.K0))
+    inp = S.attn_inputs(28, "grow.in", k, Hq, Hkv, D)
+    o = cache.verify(vf, inp, k)
+    oo, _, _ = cache.oracle(inp, P)
+    assert_close(o, oo.reshape(k, -1), what="o")
+
+
+def test_stale_workspace_does_not_leak(vf):
+    """The query rows past k * Hq / Hkv of the workspace are never cleared:
+    a workspace filled with NaN bits, then a width-16 call, then a width-3
+    call over the same cache, each against the oracle."""
+    import torch
+
+    Hq, Hkv, D, P = 24, 2, 256, 600
+    cache = Cache(29, "stale", Hq, Hkv, D, P + 16, P, 256)
+    cache.work.fill_(0xFF)
+    for k in (16, 3):
+        inp = S.attn_inputs(29, f"stale.in.{k}", k, Hq, Hkv, D)
+        o = cache.verify(vf, inp, k)
+        oo, _, _ = cache.oracle(inp, P)
+        assert np.all(np.isfinite(o)), f"k={k}"
+        assert_close(o, oo.reshape(k, -1), what=f"o k={k}")
+    torch.cuda.synchronize()
+
+
 def test_bf16_output_is_rne_of_f32(vf):
     Hq, Hkv, D, P, k = 24, 2, 256, 100, 5
     cache = Cache(21, "attn.bf", Hq, Hkv, D, P + k, P)
