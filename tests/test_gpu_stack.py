@@ -157,6 +157,38 @@ def test_stack_rows_equal_single_row_steps(vf, k):
         assert np.array_equal(host(h1)[0].view(np.uint32), hk[r].view(np.uint32)), f"row {r}"
 
 
+@pytest.mark.parametrize("k", [1, 9, 16, 17])
+def test_stack_call_equals_layer_calls(vf, k):
+    """verify_stack_k (layers after the first chained to the one before by
+    dependent launches) equals verify_layer_k layer by layer bit for bit:
+    the residual, every layer's routes and every state snapshot."""
+    import torch
+
+    ds = DeviceStack(vf, SMALL, seed=3, n_slots=k + 1, graphs=False, layers=3)
+    T, L = ds.sh["T"], ds.n_layers
+    h0 = S.f32_normal(3, f"stack.fuse{k}", (k, SMALL["H"]))
+    runs = []
+    for fused in (True, False):
+        for st in ds.states:
+            st.cur, st.pending_k = 0, 0
+        h = torch.from_numpy(h0.copy()).cuda()
+        idx = torch.zeros((L, k, T), dtype=torch.int32, device="cuda")
+        if fused:
+            vf.verify_stack_k(ds.layers, ds.states, h, k, idx)
+        else:
+            for l in range(L):
+                vf.verify_layer_k(ds.layers[l], ds.states[l], h, k, idx[l])
+        torch.cuda.synchronize()
+        runs.append((host(h).view(np.uint32), host(idx),
+                     [(np.stack([host(x).view(np.uint32) for x in s]), np.stack([host(x).view(np.uint16) for x in t]))
+                      for s, t in ds.state_tensors]))
+    (ha, ia, sa), (hb, ib, sb) = runs
+    assert np.array_equal(ha, hb), "residual"
+    assert np.array_equal(ia, ib), "routes"
+    for l in range(L):
+        assert np.array_equal(sa[l][0], sb[l][0]) and np.array_equal(sa[l][1], sb[l][1]), f"snapshots, layer {l}"
+
+
 def test_device_weights_match_host_redraw(vf):
     """The stack's weights drawn on the device (centred recipe) are the host
     generator's bits: the oracle side re-draws exactly what the GPU uses."""
