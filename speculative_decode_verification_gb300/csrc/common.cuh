@@ -375,13 +375,27 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // ------------------------------------------------ programmatic dependent launch
 //
 // A kernel launched with programmatic stream serialization may start while
-// the kernel before it is still running.  Every kernel here follows one rule:
-// before griddep_wait() it reads only data that no kernel of the running
-// sequence writes (weights, parameters) or that was written at least two
-// kernels earlier (the DeltaNet state slot, written by the layer's previous
-// call), and it writes nothing; it triggers its own dependents only after its
-// wait.  So when a kernel starts, the kernel two places before it has
-// finished.  Without the launch attribute both instructions are no-ops.
+// the kernel before it is still running; it completes only after its
+// griddep_wait() has returned, i.e. after the kernel before it completed, so
+// completion follows stream order.  Rules:
+//  - before griddep_wait() a kernel writes nothing and reads only data that
+//    no kernel of the running sequence writes (weights, parameters, state
+//    slots and words written by earlier calls, whose first kernel is
+//    launched without the attribute and starts after all earlier work), or
+//    data written by a kernel that has certainly finished when it starts;
+//  - the norm and the expert combine trigger their dependent (griddep_launch)
+//    at their start: the kernel after them (a dense product, the next
+//    layer's norm) reads only static data before its own wait, and a
+//    product's weight prefetch then overlaps the kernels before it;
+//  - every other kernel triggers after its own wait, so that when its
+//    dependent starts, the kernel two places before it has finished: the
+//    DeltaNet step reads its state slot and the device-held commit word, the
+//    expert kernel its scheduling words (reset by the previous call's
+//    combine) and the combine the residual and the shared gate logit before
+//    their waits on that basis.  (Early triggers in the dense products and
+//    the DeltaNet step measured slower: their dependents' CTAs then share
+//    the SMs with the running kernel.)
+// Without the launch attribute both instructions are no-ops.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

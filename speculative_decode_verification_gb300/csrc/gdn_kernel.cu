@@ -342,8 +342,11 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const floa
     const int c = i * nt + tid;
     wt[i] = c < n ? (zc ? 1.f + w[c] : w[c]) : 0.f;
   }
-  griddep_wait();
+  // the kernel after a norm (a product) reads only its weights before its
+  // own wait: it may start now and fetch them while this kernel's
+  // predecessor finishes
   griddep_launch();
+  griddep_wait();
   const int r = blockIdx.x;
   const float* xr = x + (long long)r * n;
   __shared__ float red[8];

@@ -827,8 +827,10 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeArgs a) {
   const int r = live ? (int)(i / a.H) : 0, n = live ? (int)(i % a.H) : 0;
   const float yo = live && a.dtype == 2 ? reinterpret_cast<const float*>(a.y)[(long long)r * a.H + n] : 0.f;
   const float sg = live && a.has_shared ? __ldcg(a.shared_logit + (long long)r * a.logits_ld) : 0.f;
-  griddep_wait();
+  // the kernel after the combine (the next layer's norm) reads only static
+  // data before its own wait: it may start now
   griddep_launch();
+  griddep_wait();
   if (blockIdx.x == 0) {  // the routed-expert kernel is done: reset its counters and unit counts
     for (int i = threadIdx.x; i < kMoeSchedWords; i += blockDim.x) a.work[i] = 0;
   }
