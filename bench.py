@@ -46,17 +46,17 @@ EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
 
 # DRAM traffic of the routed-expert kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum) of both layers of a 2-layer
-# stack at k = 9: 412.19 MB read and 5.98 MB written over two launches whose
+# stack at k = 9: 412.20 MB read and 6.01 MB written over two launches whose
 # algorithmic bytes sum to 2 x 206226468.  Expert traffic grows with the
 # distinct experts read, like the algorithmic bytes, so a full launch's
 # traffic is this ratio times its bytes.  The figure holds only for the
 # kernel sources it was taken on; any change to them reports null until the
 # kernel is captured again.
-MOE_TRAFFIC_RATIO = 418.17472e6 / (2 * 206226468.0)
+MOE_TRAFFIC_RATIO = 418.21e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
-    "q4_kernels.cu": "7c2684ed52c90a824ba00ea4c146d3ad0c4be127b4851875a351b2b4b438ad35",
-    "common.cuh": "3c7de14039580caf156b44b6e1c560f4cc81b8c0cb9346e712921c24b6aafcfd",
-    "internal.h": "4c192abe46cbaf6257ad563a1d289d447c040ff68ace2f8baa723d2a49c93924",
+    "q4_kernels.cu": "1e35f828636a784d772be335d206b57fea75d88e3aadcf61c2512f2b078eaa65",
+    "common.cuh": "3152f57d8b02c0851d797f946658401567ffcc928311abd7bf76f26a90568479",
+    "internal.h": "9135b5f4291f9afa3784a1209fc6542a6f75be2155304d81e7aec62fc7bbb8d9",
 }
 
 
