@@ -122,7 +122,10 @@ __global__ void attn_append_kernel(const AttnArgs a) {
 //             nothing is rescaled; the result, O / sum, is the same.
 // TMEM: S / P tiles at columns 0 and 64, the query's hi part at 128, O at
 // 256 (the hi part arrives by TMA in ring slots 3 and 4 and is moved to TMEM
-// before those slots take their first tiles).  Shared memory: the query's lo part (K-major) and the ring of key and
+// before those slots take their first tiles).  With fewer than 128 pairs only
+// the pairs' rows, rounded up to 8, are loaded; the other rows of the query
+// tiles hold whatever shared memory held, and their scores are masked and
+// their outputs never stored.  Shared memory: the query's lo part (K-major) and the ring of key and
 // value tiles, all 1 KB-aligned 128-byte-swizzle layouts (keys K-major,
 // values MN-major: their rows are the cache's rows).  At the end each O row
 // goes through shared memory to a bulk copy.  Every wait is a bounded
@@ -153,6 +156,10 @@ struct TcSmem {
   static_assert(SLOTS * TILE_BYTES >= kTcM * (D * 4 + 16), "the O tile is staged in the ring");
   static_assert(SLOTS >= 5 && 2 * TILE_BYTES == Q_BYTES, "the query's hi part is staged in slots 3 and 4");
 };
+
+// Rows of one query tile load: the M pairs of a KV head rounded up to 8, at
+// most 128 (rows past it stay unloaded: pairs past M, never stored).
+__host__ __device__ constexpr int query_box_rows(int M) { return M < kTcM ? (M + 7) / 8 * 8 : kTcM; }
 
 // ring item i -> sub-tile and operand, in the order the MMAs consume them:
 // K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}
@@ -217,15 +224,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_partial_kernel(const __gri
       // positions committed before this call (written at least two launches
       // back) are fetched before the dependency wait, the rest after it.
       // The query (written by the append kernel) follows the dependency wait,
-      // which comes at the latest before the fourth tile: its lo part into
-      // its own region, its hi part into ring slots 3 and 4, from where the
-      // softmax warps move it to TMEM before those slots take tiles.
+      // which comes right after the first key tile (fetching more before it
+      // measured slower: the query then shares the bandwidth with every CTA's
+      // prefetch): its lo part into its own region, its hi part into ring
+      // slots 3 and 4, from where the softmax warps move it to TMEM before
+      // those slots take tiles.
       bool waited = false;
       int issued = 0;
       auto wait_then_query = [&]() {
         griddep_wait();
         waited = true;
-        mbar_arrive_expect_tx(q_lo, (uint32_t)(2 * L::Q_BYTES));
+        mbar_arrive_expect_tx(q_lo, (uint32_t)(2 * (D / 64) * query_box_rows(M) * 128));
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
           tma_load_2d(sb + L::QL + c * L::BLOCK_Q, &a.tm_ql, q_lo, 64 * c, hk * a.q_rows + m0);
@@ -240,7 +249,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_partial_kernel(const __gri
         else if (i & 1) j = (i + 1) / 2, values = false;
         else j = i / 2 - 1, values = true;
         const int p0 = pos0 + j * kTcN;
-        if (!waited && (p0 + kTcN > a.P || i >= 3)) wait_then_query();
+        if (!waited && (p0 + kTcN > a.P || i >= 1)) wait_then_query();
         if (i == 3 && !mbar_wait(q_full, 0, abort, a.err)) break;  // the staged hi part was read
         const int slot = i % NS, use = i / NS;
         if (use > 0 && !mbar_wait(empty(slot), (uint32_t)((use - 1) & 1), abort, a.err)) break;
@@ -572,13 +581,13 @@ cudaError_t encode_cache_map(CUtensorMap* m, uint16_t* base, const AttnArgs& a) 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Host: the tensor map of the queries' lo parts: {D, Hkv * q_rows} binary16,
-// boxes of 64 dims x 128 rows, 128-byte swizzle.
+// Host: the tensor map of the queries' hi or lo parts: {D, Hkv * q_rows}
+// binary16, boxes of 64 dims x query_box_rows(M) rows, 128-byte swizzle.
 cudaError_t encode_query_map(CUtensorMap* m, uint16_t* base, const AttnArgs& a) {
   if (!g_encode) return cudaErrorInitializationError;
   const cuuint64_t dims[2] = {(cuuint64_t)a.D, (cuuint64_t)a.Hkv * a.q_rows};
   const cuuint64_t strides[1] = {(cuuint64_t)a.D * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kTcM}, es[2] = {1, 1};
+  const cuuint32_t box[2] = {64, (cuuint32_t)query_box_rows(a.k * (a.Hq / a.Hkv))}, es[2] = {1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
