@@ -54,9 +54,9 @@ EXPERT_BYTES = lambda H, I: int((2 * I * H + H * I) * 0.5625)  # noqa: E731
 # kernel is captured again.
 MOE_TRAFFIC_RATIO = 418.21e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
-    "q4_kernels.cu": "1e35f828636a784d772be335d206b57fea75d88e3aadcf61c2512f2b078eaa65",
+    "q4_kernels.cu": "a94468e049b2fbd81dd3166390c0df9f1db161b0dbc8452b3257527cd279805e",
     "common.cuh": "3152f57d8b02c0851d797f946658401567ffcc928311abd7bf76f26a90568479",
-    "internal.h": "9135b5f4291f9afa3784a1209fc6542a6f75be2155304d81e7aec62fc7bbb8d9",
+    "internal.h": "9d94fe9e427b0fe0f83ebf42fc42a575100154e9a82eaf976192a200893214a4",
 }
 
 

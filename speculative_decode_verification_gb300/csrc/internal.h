@@ -65,7 +65,7 @@ struct DenseArgs {
   int r0;
 };
 
-// Routed experts.  Both kernels recompute the (cheap, deterministic) routing.
+// Routed experts: the routing kernel, the expert kernel and the combine.
 struct MoeArgs {
   const float* logits;
   long long logits_ld;

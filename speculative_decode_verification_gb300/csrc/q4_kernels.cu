@@ -31,8 +31,8 @@
 //    through distributed shared memory in rank order (no global scratch, no
 //    atomics).
 //  * Routed MoE: a one-CTA kernel routes every row (a warp per row) and
-//    writes the routes.  Then four CTAs per SM, two stages of 8 activation
-//    rows: each CTA reads the routes, builds the list of work units and works
+//    writes the routes.  Then four CTAs per SM, a four-stage ring of 9 KB
+//    blocks: each CTA reads the routes, builds the list of work units and works
 //    through items: first the gate/up items (expert, row chunk, 64 gate + 64
 //    up rows; SwiGLU into the h rows), then the down items (expert, row chunk, 128 output rows;
 //    one partial output per (row, rank)).  A down item starts once every
