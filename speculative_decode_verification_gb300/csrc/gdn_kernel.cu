@@ -49,8 +49,10 @@ template <int D>
 __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const GdnArgs a) {
   using SH = GdnShape<D>;
   constexpr int TPR = SH::TPR, NT = SH::THREADS, NV4 = SH::NV4, P = SH::P;
-  __shared__ __align__(16) float qn[kGdnMaxK][D];
-  __shared__ __align__(16) float kn[kGdnMaxK][D];
+  // rows padded by 16 floats: the two half-warps of the L2 norms read
+  // adjacent rows in different banks
+  __shared__ __align__(16) float qn[kGdnMaxK][D + 16];
+  __shared__ __align__(16) float kn[kGdnMaxK][D + 16];
   __shared__ float vs[kGdnMaxK][kGdnRows];
   __shared__ float ys[kGdnMaxK][kGdnRows];
   __shared__ float gs[kGdnMaxK], bs[kGdnMaxK], kq[kGdnMaxK];
@@ -185,34 +187,37 @@ __global__ void __launch_bounds__(GdnShape<D>::THREADS) gdn_verify_kernel(const 
   }
   __syncthreads();
 
-  // ---- 2. L2 norms of q and k per row (warp w: rows w, w + NT/32, ...), k.q
+  // ---- 2. L2 norms of q and k per row, k.q: half-warp h takes rows h,
+  //      h + NT/16, ... (all of a 16-row block at once for D >= 64)
   {
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int r = warp; r < k; r += NT / 32) {
+    constexpr int HW = NT / 16;
+    const int hw = tid >> 4, hl = tid & 15;
+    const unsigned half = 0xFFFFu << (16 * (hw & 1));
+    for (int r = hw; r < k; r += HW) {
       float sq = 0.f, sk = 0.f;
 #pragma unroll
-      for (int j = lane; j < D; j += 32) {
+      for (int j = hl; j < D; j += 16) {
         sq = fmaf(qn[r][j], qn[r][j], sq);
         sk = fmaf(kn[r][j], kn[r][j], sk);
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        sq += __shfl_xor_sync(0xffffffffu, sq, off);
-        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+      for (int off = 8; off > 0; off >>= 1) {
+        sq += __shfl_xor_sync(half, sq, off);
+        sk += __shfl_xor_sync(half, sk, off);
       }
-      const float nq = sqrtf(sq + a.l2_eps), nk = sqrtf(sk + a.l2_eps);
+      const float iq = a.q_scale / sqrtf(sq + a.l2_eps), ik = 1.f / sqrtf(sk + a.l2_eps);
       float dot = 0.f;
 #pragma unroll
-      for (int j = lane; j < D; j += 32) {
-        const float qv = qn[r][j] / nq * a.q_scale;
-        const float kv = kn[r][j] / nk;
+      for (int j = hl; j < D; j += 16) {
+        const float qv = qn[r][j] * iq;
+        const float kv = kn[r][j] * ik;
         qn[r][j] = qv;
         kn[r][j] = kv;
         dot = fmaf(kv, qv, dot);
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-      if (lane == 0) kq[r] = dot;
+      for (int off = 8; off > 0; off >>= 1) dot += __shfl_xor_sync(half, dot, off);
+      if (hl == 0) kq[r] = dot;
     }
   }
   __syncthreads();
