@@ -56,7 +56,7 @@ MOE_TRAFFIC_RATIO = 418.21e6 / (2 * 206226468.0)
 MOE_TRAFFIC_SOURCES = {
     "q4_kernels.cu": "a94468e049b2fbd81dd3166390c0df9f1db161b0dbc8452b3257527cd279805e",
     "common.cuh": "3152f57d8b02c0851d797f946658401567ffcc928311abd7bf76f26a90568479",
-    "internal.h": "9d94fe9e427b0fe0f83ebf42fc42a575100154e9a82eaf976192a200893214a4",
+    "internal.h": "696848aff2ec6ff05f190ffe0d7e8dcbbeb1b1fc9cfeb8b2064a4bb5a8586494",
 }
 
 

@@ -91,6 +91,16 @@ struct MoeArgs {
   int n_sm;                   // SMs of the GPU
 };
 
+// CTAs per SM of the routed-expert grid: three when an upper bound of the
+// gate/up items fits one wave of four per SM (fewer CTAs per SM stream
+// faster each), else all that fit (more CTAs shorten the waves of large
+// expert sets).  The grid changes no result: an item's arithmetic is the same
+// on any CTA.
+inline int moe_ctas_per_sm_for(int k, int top_k, int E, int has_shared, int I, int num_sms, int max_per_sm) {
+  const int est = ((k * top_k < E ? k * top_k : E) + has_shared) * (I / 64);
+  return est <= 4 * num_sms && max_per_sm > 3 ? 3 : max_per_sm;
+}
+
 // Shape rules of the routed-expert call, shared by q4_gather_experts_k and
 // its no-allocation twin so that both accept the same calls: 0 (fine) or the
 // verify_status to return, with a message.

@@ -135,7 +135,7 @@ extern "C" verify_status q4_gather_experts_k_noalloc(
   a.err = device_error ? device_error : err_word;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.k = k; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
-  a.G = d->moe_ctas_per_sm * d->num_sms;
+  a.G = vk::moe_ctas_per_sm_for(k, top_k, E, a.has_shared, I, d->num_sms, d->moe_ctas_per_sm) * d->num_sms;
   a.n_sm = d->num_sms;
   // The error word and the scheduling words must start at zero: a previous
   // call may have stopped on a device error and left them set.

@@ -372,7 +372,7 @@ verify_status q4_gather_experts_k(verify_ctx* ctx, const verify_q4_experts* gate
   a.idx_out = idx_out; a.w_out = w_out; a.y = y; a.err = ctx->err;
   a.E = E; a.T = top_k; a.H = H; a.I = I; a.dtype = dtype_out;
   a.has_shared = n_shared ? 1 : 0;
-  a.G = ctx->moe_ctas_per_sm * ctx->num_sms;
+  a.G = vk::moe_ctas_per_sm_for(k, top_k, E, a.has_shared, I, ctx->num_sms, ctx->moe_ctas_per_sm) * ctx->num_sms;
   a.n_sm = ctx->num_sms;
   const size_t y_elem = dtype_out == VERIFY_BF16 ? 2 : 4;
   // passes of up to VERIFY_PASS_K rows (each row's routing, experts and
